@@ -1,0 +1,182 @@
+/*
+ * sketch.h -- C ABI of the GB300 (sm_103a) library for randomized low-rank
+ * gradient sketching of linear layers (RGC / LoGRA).
+ *
+ * For a linear layer with weight W (d x k, out x in), input X (T x k) and
+ * output derivative D (T x d), the weight gradient is G = D^T X.  The library
+ * never forms G.  It
+ *   (a) draws a seeded projection P (k x r),
+ *   (b) forms the saved projected input XP = X P,
+ *   (c) accumulates the fp32 sketch C += D^T (XP) over microbatches, and
+ *   (d) rebuilds H = C P^T block by block, fused with the weight update, and
+ *       writes W back to BF16 by stochastic rounding.
+ * Sources (page title, section): "Randomized Gradient Compression" -- "How it
+ * works" and footnote 1; "LoGRA: Scaling LLM Reinforcement Learning with
+ * Low-Rank Gradient Sketches" -- Key Contributions 1 and 2; "LoGRA: Low-Rank
+ * Gradient Sketches" -- "The Core Move", "Why the Sketch Can Be Accumulated
+ * Without a Full Gradient", "Why the Update Is Low-Rank but Not an Exact
+ * Recovery", "Why Refreshing the Projection Enables New Update Directions",
+ * "Minimal Causal Code".  LoGRA's projection A (r x k) is P^T and its sketch
+ * S is C.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named X, D, XP, W, C, P, ws, dev_status, wnorm2_* are DEVICE
+ *   pointers on the current CUDA device.  BF16 tensors are passed as uint16_t
+ *   bit patterns (the upper half of an IEEE fp32).
+ * - Layouts are row-major.  P is k x r fp32 contiguous (row stride r).  C is
+ *   d x r fp32 contiguous (row stride r).  X, D, XP, W have an explicit row
+ *   stride in elements (ld_*), which must be >= the row width and a multiple
+ *   of 8 (16 bytes); every pointer must be 16-byte aligned.
+ * - Sizes: 1 <= r <= 256; k a multiple of 8; T, d, k >= 1 and < 2^31;
+ *   d*k < 2^40.
+ * - Ownership: the caller allocates and owns every buffer, including the
+ *   workspace `ws` (query its size with sketch_workspace_bytes; pass NULL and
+ *   0 when that size is 0).  The library allocates no memory and keeps no
+ *   state between calls; it is safe to call from several host threads.
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream).  Calls that share a workspace must be ordered on one
+ *   stream.
+ * - Errors: argument errors are found on the host, return a nonzero
+ *   sketch_status and launch nothing.  A failed launch returns
+ *   SKETCH_ERR_CUDA.  Data-dependent conditions found on the device (see
+ *   SKETCH_DEV_*) are written to `dev_status`; nothing traps or spins.
+ *   sketch_last_error() describes the last failure on the calling thread.
+ * - Random bits: one Philox4x32-10 stream per (seed, layer, step, purpose);
+ *   key = (seed low word, seed high word), counter = (block, step, layer,
+ *   purpose).  Every output is a pure function of its inputs, so repeated
+ *   calls and replicas produce bit-identical results.
+ */
+#ifndef RGS_SKETCH_H
+#define RGS_SKETCH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SKETCH_API __attribute__((visibility("default")))
+#else
+#define SKETCH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SKETCH_OK = 0,
+    SKETCH_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or stride */
+    SKETCH_ERR_UNSUPPORTED = 2,  /* valid request outside what the kernels handle */
+    SKETCH_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small */
+    SKETCH_ERR_CUDA = 4          /* a CUDA call or kernel launch failed */
+} sketch_status;
+
+typedef enum {
+    /* entries +-1/sqrt(r) from Philox sign bits ("LoGRA: Low-Rank Gradient
+       Sketches", "Why the Sketch Can Be Accumulated Without a Full Gradient") */
+    SKETCH_PROJ_RADEMACHER = 0,
+    /* sqrt(k/r) * Q, Q the orthonormal factor of a k x r Gaussian matrix with
+       the sign correction diag(R) > 0 ("Randomized Gradient Compression",
+       footnote 1) */
+    SKETCH_PROJ_GAUSSIAN_QR = 1
+} sketch_proj_kind;
+
+typedef enum {
+    SKETCH_OP_SAMPLE_PROJECTION = 0,
+    SKETCH_OP_PROJECT_INPUTS = 1,
+    SKETCH_OP_ACCUMULATE = 2,
+    SKETCH_OP_UPDATE_NORMSGD = 3,
+    SKETCH_OP_UPDATE_SGD = 4
+} sketch_op;
+
+/* Bits of the device status word (int32) written by the update calls. */
+#define SKETCH_DEV_H_ZERO 1        /* ||H||_F == 0: W left unchanged */
+#define SKETCH_DEV_H_NONFINITE 2   /* ||H||_F is inf or NaN: W left unchanged */
+#define SKETCH_DEV_W_NONFINITE 4   /* ||W||_F is inf or NaN: W left unchanged */
+#define SKETCH_DEV_QR_BREAKDOWN 8  /* non-positive pivot in the QR Cholesky */
+
+/* Workspace bytes the call `op` needs for these sizes (0 = none).  Arguments
+ * that an op does not use are ignored.  Returns 0 for invalid sizes too; the
+ * call itself reports those. */
+SKETCH_API size_t sketch_workspace_bytes(sketch_op op, int64_t T, int64_t d, int64_t k, int64_t r);
+
+/* (a) Draw the projection P (k x r fp32, row-major, written in full) for
+ * (seed, layer, step).  A fixed projection uses a constant step; a projection
+ * refreshed after every update uses the step counter ("Randomized Gradient
+ * Compression", "How it works": a new random projection after every update;
+ * "LoGRA: Low-Rank Gradient Sketches", "Why Refreshing the Projection
+ * Enables New Update Directions").
+ * SKETCH_PROJ_GAUSSIAN_QR needs 4*r <= k (CholeskyQR2 in fp32 keeps the frame
+ * orthonormal to ~1e-6 only for well-conditioned Gaussian matrices) and a
+ * workspace; it reports a QR breakdown in *dev_status (nullable) as
+ * SKETCH_DEV_QR_BREAKDOWN.  SKETCH_PROJ_RADEMACHER needs no workspace. */
+SKETCH_API sketch_status sketch_sample_projection(sketch_proj_kind kind, uint64_t seed, uint32_t layer,
+                                       uint32_t step, int64_t k, int64_t r, float* P,
+                                       int32_t* dev_status, void* ws, size_t ws_bytes,
+                                       void* stream);
+
+/* (b) XP = X P rounded once to BF16 (round to nearest even) after fp32
+ * accumulation.  X: T x k BF16 (row stride ld_x); P: k x r fp32; XP: T x r BF16
+ * (row stride ld_xp), written in columns [0, r) only.  This is what the layer
+ * saves for backpropagation instead of X ("Randomized Gradient Compression",
+ * "How it works"). */
+SKETCH_API sketch_status sketch_project_inputs(const uint16_t* X, int64_t T, int64_t k, int64_t ld_x,
+                                    const float* P, int64_t r, uint16_t* XP, int64_t ld_xp,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/* (c) C = (overwrite ? 0 : C) + D^T XP in fp32, for one microbatch.  D: T x d
+ * BF16 (row stride ld_d, token-major as produced by the backward pass);
+ * XP: T x r BF16 (row stride ld_xp); C: d x r fp32, read (unless overwrite) and
+ * written.  The dense d x k gradient is never formed ("Randomized
+ * Gradient Compression", "How it works": C += D.T (X P); "LoGRA: Scaling LLM
+ * Reinforcement Learning with Low-Rank Gradient Sketches", Key Contributions 1:
+ * accumulated in fp32).  overwrite=1 on the first microbatch replaces zeroing
+ * C ("LoGRA: Low-Rank Gradient Sketches", "Minimal Causal Code"). */
+SKETCH_API sketch_status sketch_accumulate(const uint16_t* D, int64_t T, int64_t d, int64_t ld_d,
+                                const uint16_t* XP, int64_t ld_xp, int64_t r, float* C,
+                                int overwrite, void* ws, size_t ws_bytes, void* stream);
+
+/* (d) Normalized SGD, W <- W - tau * ||W||_F * H / ||H||_F with H = C P^T
+ * ("Randomized Gradient Compression", "How it works").  H is rebuilt 128 rows
+ * at a time on chip and never stored; ||H||_F^2 = <P^T P, C^T C> comes from
+ * two r x r Gram matrices.  The step scale s = fl32(tau*||W||/||H||) is
+ * computed on the device (no host synchronisation).  Each weight becomes
+ * v = fmaf(-s, H_ij, W_ij) and is written back by stochastic rounding with
+ * 16 Philox bits of element index i*k + j.
+ *   wnorm2_in  (nullable): ||W||_F^2 carried from the previous update of this
+ *              W; when NULL the call reads W once more to compute it.
+ *   wnorm2_out (nullable): receives ||W_new||_F^2 for the next call.
+ *   dev_status (nullable): receives the SKETCH_DEV_* flags (0 = updated).
+ * On a nonzero device status W is left bit-unchanged.  W: d x k BF16 (row
+ * stride ld_w), updated in place; C: d x r fp32; P: k x r fp32. */
+SKETCH_API sketch_status sketch_apply_update_normsgd(uint16_t* W, int64_t d, int64_t k, int64_t ld_w,
+                                          const float* C, const float* P, int64_t r, float tau,
+                                          uint64_t seed, uint32_t layer, uint32_t step,
+                                          const double* wnorm2_in, double* wnorm2_out,
+                                          int32_t* dev_status, void* ws, size_t ws_bytes,
+                                          void* stream);
+
+/* (d') LoGRA's basic SGD, W <- W - alpha_eta * S A with S = C and A = P^T
+ * ("LoGRA: Low-Rank Gradient Sketches", "Why the Update Is Low-Rank but Not an
+ * Exact Recovery"), with the same on-chip rebuild and stochastic rounding.
+ * The receiver of a policy synchronisation applies the received factor
+ * alpha*eta*U with alpha_eta = 1 and the regenerated projection ("LoGRA:
+ * Scaling LLM Reinforcement Learning with Low-Rank Gradient Sketches", Key
+ * Contributions 2).  dev_status (nullable) is set to 0. */
+SKETCH_API sketch_status sketch_apply_update_sgd(uint16_t* W, int64_t d, int64_t k, int64_t ld_w,
+                                      const float* C, const float* P, int64_t r, float alpha_eta,
+                                      uint64_t seed, uint32_t layer, uint32_t step,
+                                      int32_t* dev_status, void* ws, size_t ws_bytes,
+                                      void* stream);
+
+/* Static string for a status code. */
+SKETCH_API const char* sketch_status_string(sketch_status status);
+
+/* Description of the last failing call on the calling thread ("" if none). */
+SKETCH_API const char* sketch_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RGS_SKETCH_H */

@@ -1,0 +1,10 @@
+"""GB300 (sm_103a) library for randomized low-rank gradient sketching of linear
+layers (RGC / LoGRA): seeded projections, projected inputs, fp32 sketch
+accumulation and the fused rebuild + stochastically rounded BF16 update.
+
+The compute path is the C-ABI shared library ``lib/libsketch.so`` (declared in
+``include/sketch.h``); ``binding`` is its thin Python wrapper.
+"""
+from .binding import (PROJ_GAUSSIAN_QR, PROJ_RADEMACHER, SketchError, accumulate,  # noqa: F401
+                      apply_update_normsgd, apply_update_sgd, project_inputs, sample_projection,
+                      workspace_bytes)

@@ -1,0 +1,215 @@
+"""Thin Python binding of libsketch (include/sketch.h).
+
+Argument marshalling only: every step of the method runs in the library's CUDA
+kernels.  PyTorch supplies device memory (including the workspace each call
+needs) and the stream.  There is no CPU fallback: if the compiled library is
+missing, every call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libsketch.so")
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_WORKSPACE = 3
+ERR_CUDA = 4
+
+PROJ_RADEMACHER = 0
+PROJ_GAUSSIAN_QR = 1
+
+OP_SAMPLE_PROJECTION = 0
+OP_PROJECT_INPUTS = 1
+OP_ACCUMULATE = 2
+OP_UPDATE_NORMSGD = 3
+OP_UPDATE_SGD = 4
+
+DEV_H_ZERO = 1
+DEV_H_NONFINITE = 2
+DEV_W_NONFINITE = 4
+DEV_QR_BREAKDOWN = 8
+
+EXPORTS = ("sketch_workspace_bytes", "sketch_sample_projection", "sketch_project_inputs",
+           "sketch_accumulate", "sketch_apply_update_normsgd", "sketch_apply_update_sgd",
+           "sketch_status_string", "sketch_last_error")
+
+
+class SketchError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s (status %d)" % (message, status))
+        self.status = status
+
+
+_lib = None
+_c = ctypes
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_u32 = ctypes.c_uint32
+_u64 = ctypes.c_uint64
+_SIGS = {
+    "sketch_workspace_bytes": (ctypes.c_size_t, [_c.c_int, _i64, _i64, _i64, _i64]),
+    "sketch_sample_projection": (_c.c_int, [_c.c_int, _u64, _u32, _u32, _i64, _i64, _vp, _vp, _vp,
+                                            _c.c_size_t, _vp]),
+    "sketch_project_inputs": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
+                                         _c.c_size_t, _vp]),
+    "sketch_accumulate": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _c.c_int, _vp,
+                                     _c.c_size_t, _vp]),
+    "sketch_apply_update_normsgd": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _c.c_float,
+                                               _u64, _u32, _u32, _vp, _vp, _vp, _vp, _c.c_size_t,
+                                               _vp]),
+    "sketch_apply_update_sgd": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _c.c_float, _u64,
+                                           _u32, _u32, _vp, _vp, _c.c_size_t, _vp]),
+    "sketch_status_string": (_c.c_char_p, [_c.c_int]),
+    "sketch_last_error": (_c.c_char_p, []),
+}
+
+
+def lib():
+    """Load libsketch.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libsketch.so is not built (expected at %s); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(status):
+    if status != OK:
+        l = lib()
+        raise SketchError(status, "%s: %s" % (l.sketch_status_string(status).decode(),
+                                              l.sketch_last_error().decode()))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream), s
+
+
+def _rows(t, dtype, name):
+    """Row-major 2-D CUDA tensor of ``dtype`` with unit column stride; returns ld."""
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError("%s must be 2-D with unit column stride" % name)
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], ((t.shape[1] + 7) // 8) * 8)
+
+
+def _contig(t, dtype, name):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
+
+
+def _workspace(nbytes, device, stream):
+    if nbytes == 0:
+        return None
+    with torch.cuda.stream(stream):
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def workspace_bytes(op, T=0, d=0, k=0, r=1):
+    return int(lib().sketch_workspace_bytes(op, T, d, k, r))
+
+
+def sample_projection(kind, seed, layer, step, P, dev_status=None, stream=None):
+    """Fill P (k x r fp32) with the projection for (seed, layer, step)."""
+    _contig(P, torch.float32, "P")
+    k, r = P.shape
+    h, s = _stream_handle(stream, P.device)
+    nbytes = workspace_bytes(OP_SAMPLE_PROJECTION, 0, 0, k, r) if kind == PROJ_GAUSSIAN_QR else 0
+    ws = _workspace(nbytes, P.device, s)
+    _check(lib().sketch_sample_projection(kind, seed & 0xFFFFFFFFFFFFFFFF, layer, step, k, r,
+                                          _ptr(P), _ptr(dev_status), _ptr(ws), nbytes, h))
+    return P
+
+
+def project_inputs(X, P, XP, stream=None):
+    """XP[:, :r] = bf16(X P)."""
+    ld_x = _rows(X, torch.bfloat16, "X")
+    ld_xp = _rows(XP, torch.bfloat16, "XP")
+    _contig(P, torch.float32, "P")
+    T, k = X.shape
+    r = P.shape[1]
+    if P.shape[0] != k or XP.shape[0] != T or XP.shape[1] < r:
+        raise ValueError("shape mismatch: X %s, P %s, XP %s" % (tuple(X.shape), tuple(P.shape),
+                                                                tuple(XP.shape)))
+    h, s = _stream_handle(stream, X.device)
+    nbytes = workspace_bytes(OP_PROJECT_INPUTS, T, 0, k, r)
+    ws = _workspace(nbytes, X.device, s)
+    _check(lib().sketch_project_inputs(_ptr(X), T, k, ld_x, _ptr(P), r, _ptr(XP), ld_xp, _ptr(ws),
+                                       nbytes, h))
+    return XP
+
+
+def accumulate(D, XP, C, overwrite=False, r=None, stream=None):
+    """C = (0 if overwrite else C) + D^T XP[:, :r]."""
+    ld_d = _rows(D, torch.bfloat16, "D")
+    ld_xp = _rows(XP, torch.bfloat16, "XP")
+    _contig(C, torch.float32, "C")
+    T, d = D.shape
+    r = C.shape[1] if r is None else r
+    if C.shape[0] != d or XP.shape[0] != T or XP.shape[1] < r or C.shape[1] != r:
+        raise ValueError("shape mismatch: D %s, XP %s, C %s" % (tuple(D.shape), tuple(XP.shape),
+                                                                tuple(C.shape)))
+    h, s = _stream_handle(stream, D.device)
+    nbytes = workspace_bytes(OP_ACCUMULATE, T, d, 0, r)
+    ws = _workspace(nbytes, D.device, s)
+    _check(lib().sketch_accumulate(_ptr(D), T, d, ld_d, _ptr(XP), ld_xp, r, _ptr(C),
+                                   1 if overwrite else 0, _ptr(ws), nbytes, h))
+    return C
+
+
+def apply_update_normsgd(W, C, P, tau, seed, layer, step, wnorm2_in=None, wnorm2_out=None,
+                         dev_status=None, stream=None):
+    """W <- SR_bf16(W - tau ||W|| H / ||H||), H = C P^T, in place."""
+    ld_w = _rows(W, torch.bfloat16, "W")
+    _contig(C, torch.float32, "C")
+    _contig(P, torch.float32, "P")
+    d, k = W.shape
+    r = C.shape[1]
+    if C.shape[0] != d or P.shape != (k, r):
+        raise ValueError("shape mismatch: W %s, C %s, P %s" % (tuple(W.shape), tuple(C.shape),
+                                                               tuple(P.shape)))
+    h, s = _stream_handle(stream, W.device)
+    nbytes = workspace_bytes(OP_UPDATE_NORMSGD, 0, d, k, r)
+    ws = _workspace(nbytes, W.device, s)
+    _check(lib().sketch_apply_update_normsgd(_ptr(W), d, k, ld_w, _ptr(C), _ptr(P), r, float(tau),
+                                             seed & 0xFFFFFFFFFFFFFFFF, layer, step,
+                                             _ptr(wnorm2_in), _ptr(wnorm2_out), _ptr(dev_status),
+                                             _ptr(ws), nbytes, h))
+    return W
+
+
+def apply_update_sgd(W, C, P, alpha_eta, seed, layer, step, dev_status=None, stream=None):
+    """W <- SR_bf16(W - alpha_eta C P^T), in place."""
+    ld_w = _rows(W, torch.bfloat16, "W")
+    _contig(C, torch.float32, "C")
+    _contig(P, torch.float32, "P")
+    d, k = W.shape
+    r = C.shape[1]
+    if C.shape[0] != d or P.shape != (k, r):
+        raise ValueError("shape mismatch: W %s, C %s, P %s" % (tuple(W.shape), tuple(C.shape),
+                                                               tuple(P.shape)))
+    h, s = _stream_handle(stream, W.device)
+    nbytes = workspace_bytes(OP_UPDATE_SGD, 0, d, k, r)
+    ws = _workspace(nbytes, W.device, s)
+    _check(lib().sketch_apply_update_sgd(_ptr(W), d, k, ld_w, _ptr(C), _ptr(P), r,
+                                         float(alpha_eta), seed & 0xFFFFFFFFFFFFFFFF, layer, step,
+                                         _ptr(dev_status), _ptr(ws), nbytes, h))
+    return W

@@ -1,0 +1,70 @@
+// Device helpers shared by the library's kernels: Philox4x32-10, BF16 bit
+// handling and stochastic rounding, launch bookkeeping.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sketch.h"
+
+namespace rgs {
+
+// Purpose word (counter word 3) of each Philox stream.
+constexpr uint32_t kTagSR = 0u;
+constexpr uint32_t kTagRademacher = 1u;
+constexpr uint32_t kTagGaussian = 2u;
+
+struct Philox4 {
+  uint32_t w0, w1, w2, w3;
+};
+
+// Philox4x32-10 of Salmon, Moraes, Dror and Shaw ("Parallel random numbers:
+// as easy as 1, 2, 3", SC'11): ten rounds of the two-multiplier S-box with a
+// Weyl key schedule; the key is bumped before every round but the first.
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                 uint32_t c3, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c0;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0);
+    const uint32_t lo1 = 0xCD9E8D57u * c2;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2);
+    const uint32_t n0 = hi1 ^ c1 ^ k0;
+    const uint32_t n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+  }
+  return Philox4{c0, c1, c2, c3};
+}
+
+// Block `block` of the stream (seed, layer, step, tag).
+__device__ __forceinline__ Philox4 stream_block(uint64_t seed, uint32_t layer, uint32_t step,
+                                                uint32_t tag, uint32_t block) {
+  return philox4x32_10(block, step, layer, tag, (uint32_t)(seed & 0xFFFFFFFFull),
+                       (uint32_t)(seed >> 32));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) {
+  return __uint_as_float(h << 16);
+}
+
+// Stochastic rounding of v to BF16 with 16 random bits: add them below the
+// kept mantissa and truncate, so the magnitude rounds up with probability
+// (dropped bits) / 2^16.  NaN becomes the canonical quiet NaN.
+__device__ __forceinline__ uint32_t sr_bf16_bits(float v, uint32_t rand16) {
+  const uint32_t b = __float_as_uint(v);
+  const uint32_t r = (b + rand16) >> 16;
+  return (v != v) ? 0x7FC0u : r;
+}
+
+__host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) {
+  return (a + b - 1) / b;
+}
+
+}  // namespace rgs

@@ -1,0 +1,207 @@
+// (a) Projection P (k x r fp32): Rademacher signs or a Gaussian-QR frame.
+//
+// Rademacher: entries +-1/sqrt(r) ("LoGRA: Low-Rank Gradient Sketches", "Why
+// the Sketch Can Be Accumulated Without a Full Gradient").  Element e = j*r + l
+// takes bit e % 128 of Philox block e / 128 of the sign stream.
+//
+// Gaussian QR: P = sqrt(k/r) Q with Q the orthonormal factor of a Gaussian
+// k x r matrix and diag(R) > 0 ("Randomized Gradient Compression",
+// footnote 1).  The frame is computed by CholeskyQR2 in fp32: twice
+// (Gram A = G^T G, Cholesky A = R^T R, G <- G R^-1).  Cholesky factors have a
+// positive diagonal, so the result is the sign-corrected QR factor without an
+// explicit sign fix.  For 4r <= k the Gaussian matrix is well conditioned and
+// the second pass leaves P^T P = (k/r) I to about 1e-6.
+#include "common.cuh"
+#include "internal.h"
+
+namespace rgs {
+namespace {
+
+// One thread per 32 consecutive elements (one 32-bit word of a Philox block).
+__global__ void __launch_bounds__(256) rademacher_kernel(const ProjBatch batch) {
+  const ProjProblem& pb = batch.p[blockIdx.y];
+  const int64_t n = pb.k * batch.r;
+  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t e0 = w * 32;
+  if (e0 >= n) return;
+  const Philox4 blk = stream_block(batch.seed, pb.layer, batch.step, kTagRademacher, (uint32_t)(w >> 2));
+  const uint32_t word = (w & 3) == 0 ? blk.w0 : (w & 3) == 1 ? blk.w1 : (w & 3) == 2 ? blk.w2 : blk.w3;
+  const float pos = pb.scale, neg = -pb.scale;
+  float4* out = reinterpret_cast<float4*>(pb.P + e0);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    if (e0 + 4 * q >= n) break;  // n is a multiple of 8
+    const uint32_t bits = word >> (4 * q);
+    float4 v;
+    v.x = (bits & 1u) ? neg : pos;
+    v.y = (bits & 2u) ? neg : pos;
+    v.z = (bits & 4u) ? neg : pos;
+    v.w = (bits & 8u) ? neg : pos;
+    out[q] = v;
+  }
+}
+
+// Box-Muller on one Philox block: 4 standard normal draws for elements
+// 4b .. 4b+3; lanes 0,1 use words (0,1) and lanes 2,3 use words (2,3); even
+// lanes take the cosine branch, odd lanes the sine branch.  u = (w + 1/2) 2^-32.
+__device__ __forceinline__ float4 gaussian4(const Philox4& blk) {
+  const float u0 = fmaf((float)blk.w0, 0x1p-32f, 0x1p-33f);
+  const float u1 = fmaf((float)blk.w1, 0x1p-32f, 0x1p-33f);
+  const float u2 = fmaf((float)blk.w2, 0x1p-32f, 0x1p-33f);
+  const float u3 = fmaf((float)blk.w3, 0x1p-32f, 0x1p-33f);
+  const float ra = sqrtf(-2.0f * logf(u0));
+  const float rb = sqrtf(-2.0f * logf(u2));
+  float sa, ca, sb, cb;
+  sincospif(2.0f * u1, &sa, &ca);
+  sincospif(2.0f * u3, &sb, &cb);
+  return make_float4(ra * ca, ra * sa, rb * cb, rb * sb);
+}
+
+__global__ void __launch_bounds__(256) gaussian_kernel(const ProjBatch batch) {
+  const ProjProblem& pb = batch.p[blockIdx.y];
+  const int64_t n = pb.k * batch.r;
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (4 * b >= n) return;
+  const Philox4 blk = stream_block(batch.seed, pb.layer, batch.step, kTagGaussian, (uint32_t)b);
+  reinterpret_cast<float4*>(pb.P)[b] = gaussian4(blk);
+}
+
+__device__ __forceinline__ int packed_upper(int i, int j, int r) {
+  return i * r - (i * (i - 1)) / 2 + (j - i);
+}
+
+// One block per problem.  Cholesky of the r x r Gram matrix (packed upper
+// triangle in shared memory, right-looking), then the upper-triangular inverse
+// R^-1 written in full (zeros below the diagonal) to pb.rinv.
+__global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
+  extern __shared__ float R[];  // r(r+1)/2
+  const ProjProblem& pb = batch.p[blockIdx.x];
+  const int r = batch.r;
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  for (int i = warp; i < r; i += nwarps)
+    for (int j = i + lane; j < r; j += 32) R[packed_upper(i, j, r)] = pb.gram[i * r + j];
+  __syncthreads();
+  bool broken = false;
+  for (int p = 0; p < r; ++p) {
+    const float diag = R[packed_upper(p, p, r)];
+    if (!(diag > 0.0f) || !isfinite(diag)) {  // uniform across the block
+      broken = true;
+      break;
+    }
+    const float rp = sqrtf(diag);
+    const float inv = 1.0f / rp;
+    __syncthreads();  // everyone has read the pivot
+    for (int j = p + tid; j < r; j += nthreads)
+      R[packed_upper(p, j, r)] = (j == p) ? rp : R[packed_upper(p, j, r)] * inv;
+    __syncthreads();
+    for (int i = p + 1 + warp; i < r; i += nwarps) {
+      const float rpi = R[packed_upper(p, i, r)];
+      for (int j = i + lane; j < r; j += 32)
+        R[packed_upper(i, j, r)] = fmaf(-rpi, R[packed_upper(p, j, r)], R[packed_upper(i, j, r)]);
+    }
+    __syncthreads();
+  }
+  float* X = pb.rinv;
+  if (broken) {
+    for (int e = tid; e < r * r; e += nthreads) X[e] = 0.0f;
+    if (tid == 0) atomicOr(batch.status, SKETCH_DEV_QR_BREAKDOWN);
+    return;
+  }
+  // X = R^-1, rows from the bottom: X[i][j] = -(sum_{m=i+1..j} R[i][m] X[m][j]) / R[i][i].
+  for (int i = r - 1; i >= 0; --i) {
+    const float inv_ii = 1.0f / R[packed_upper(i, i, r)];
+    for (int j = tid; j < r; j += nthreads) {
+      float v;
+      if (j < i) {
+        v = 0.0f;
+      } else if (j == i) {
+        v = inv_ii;
+      } else {
+        float s = 0.0f;
+        for (int m = i + 1; m <= j; ++m) s = fmaf(R[packed_upper(i, m, r)], X[m * r + j], s);
+        v = -s * inv_ii;
+      }
+      X[i * r + j] = v;
+    }
+    __syncthreads();
+  }
+}
+
+// P rows [32*blockIdx.x, +32) <- scale * P_rows * Rinv (Rinv upper triangular).
+__global__ void __launch_bounds__(256) tri_apply_kernel(const ProjBatch batch, int final_pass) {
+  extern __shared__ float smem[];
+  const ProjProblem& pb = batch.p[blockIdx.y];
+  const int r = batch.r;
+  const int64_t row0 = (int64_t)blockIdx.x * 32;
+  if (row0 >= pb.k) return;
+  const int rows = (int)((pb.k - row0) < 32 ? (pb.k - row0) : 32);
+  float* S = smem;           // 32 x r
+  float* O = smem + 32 * r;  // 32 x r
+  float* P = pb.P + row0 * r;
+  for (int e = threadIdx.x; e < rows * r; e += blockDim.x) S[e] = P[e];
+  __syncthreads();
+  const float scale = final_pass ? pb.scale : 1.0f;
+  const float* __restrict__ X = pb.rinv;
+  for (int e = threadIdx.x; e < rows * r; e += blockDim.x) {
+    const int row = e / r, c = e % r;
+    float acc = 0.0f;
+    for (int m = 0; m <= c; ++m) acc = fmaf(S[row * r + m], X[m * r + c], acc);
+    O[e] = acc * scale;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < rows * r; e += blockDim.x) P[e] = O[e];
+}
+
+}  // namespace
+
+void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
+  const GramChunks g = gram_chunks(k);
+  float* partials = cur.take<float>((size_t)g.nchunks * r * r);
+  float* gram = cur.take<float>((size_t)r * r);
+  float* rinv = cur.take<float>((size_t)r * r);
+  if (p) {
+    p->partials = partials;
+    p->gram = gram;
+    p->rinv = rinv;
+  }
+}
+
+cudaError_t launch_rademacher(const ProjBatch& batch, int64_t max_k, cudaStream_t stream) {
+  const int64_t words = ceil_div(max_k * batch.r, 32);
+  rademacher_kernel<<<dim3((unsigned)ceil_div(words, 256), batch.n), 256, 0, stream>>>(batch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream_t stream) {
+  const int r = batch.r;
+  const int64_t blocks4 = ceil_div(max_k * r, 4);
+  gaussian_kernel<<<dim3((unsigned)ceil_div(blocks4, 256), batch.n), 256, 0, stream>>>(batch);
+  GramBatch gb;
+  gb.n = batch.n;
+  gb.r = r;
+  for (int i = 0; i < batch.n; ++i) {
+    gb.e[i].A = batch.p[i].P;
+    gb.e[i].rows = batch.p[i].k;
+    gb.e[i].partials = batch.p[i].partials;
+    gb.e[i].out = batch.p[i].gram;
+  }
+  const size_t chol_smem = sizeof(float) * (size_t)r * (r + 1) / 2;
+  const size_t apply_smem = sizeof(float) * 2 * 32 * (size_t)r;
+  cudaError_t err = cudaFuncSetAttribute(chol_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)chol_smem);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(tri_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)apply_smem);
+  if (err != cudaSuccess) return err;
+  for (int pass = 0; pass < 2; ++pass) {
+    err = launch_gram(gb, stream);
+    if (err != cudaSuccess) return err;
+    chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch);
+    tri_apply_kernel<<<dim3((unsigned)ceil_div(max_k, 32), batch.n), 256, apply_smem, stream>>>(
+        batch, pass == 1);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace rgs

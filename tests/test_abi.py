@@ -1,0 +1,114 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, sizes workspaces, and rejects bad arguments on the host
+before launching anything (no call here reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from rank_gradient_sketching_philox_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sketch.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SKETCH_API\s+[\w\s\*]+?\b(sketch_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for required in ("sketch_sample_projection", "sketch_project_inputs", "sketch_accumulate",
+                     "sketch_apply_update_normsgd", "sketch_apply_update_sgd",
+                     "sketch_workspace_bytes", "sketch_status_string", "sketch_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(binding.EXPORTS) | set(declared_functions())
+
+
+def test_status_strings(lib):
+    for st in range(5):
+        assert lib.sketch_status_string(st)
+    assert lib.sketch_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(lib):
+    ws = binding.workspace_bytes
+    assert ws(binding.OP_UPDATE_SGD, 0, 4096, 4096, 64) == 0
+    a = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 64)
+    b = ws(binding.OP_UPDATE_NORMSGD, 0, 8192, 4096, 64)
+    c = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 128)
+    assert 0 < a < b and a < c
+    assert ws(binding.OP_SAMPLE_PROJECTION, 0, 0, 4096, 64) > 64 * 64 * 4
+    assert ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 0) == 0     # invalid r
+    assert ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 257) == 0   # invalid r
+
+
+def _call(fn, *args):
+    return getattr(binding.lib(), fn)(*args)
+
+
+NULL = None
+
+
+@pytest.mark.parametrize("args,status,msg", [
+    # (T, k, ld_x, r, ld_xp)
+    ((0, 64, 64, 8, 8), binding.ERR_INVALID_ARG, "T="),
+    ((16, 60, 64, 8, 8), binding.ERR_INVALID_ARG, "k=60"),
+    ((16, 64, 60, 8, 8), binding.ERR_INVALID_ARG, "ld_x"),
+    ((16, 64, 72, 0, 8), binding.ERR_INVALID_ARG, "r=0"),
+    ((16, 64, 72, 300, 304), binding.ERR_INVALID_ARG, "r=300"),
+    ((16, 64, 64, 8, 4), binding.ERR_INVALID_ARG, "ld_xp"),
+    ((16, 64, 64, 8, 8), binding.ERR_INVALID_ARG, "X is NULL"),
+])
+def test_project_inputs_argument_errors(lib, args, status, msg):
+    T, k, ld_x, r, ld_xp = args
+    st = lib.sketch_project_inputs(NULL, T, k, ld_x, NULL, r, NULL, ld_xp, NULL, 0, NULL)
+    assert st == status
+    assert msg in lib.sketch_last_error().decode()
+
+
+def test_accumulate_argument_errors(lib):
+    assert lib.sketch_accumulate(NULL, 16, 0, 8, NULL, 8, 8, NULL, 1, NULL, 0, NULL) == binding.ERR_INVALID_ARG
+    assert b"d=" in lib.sketch_last_error()
+    assert lib.sketch_accumulate(NULL, 16, 10, 10, NULL, 8, 8, NULL, 1, NULL, 0, NULL) == binding.ERR_INVALID_ARG
+    assert b"ld_d" in lib.sketch_last_error()
+    assert lib.sketch_accumulate(NULL, 16, 10, 16, NULL, 8, 8, NULL, 1, NULL, 0, NULL) == binding.ERR_INVALID_ARG
+    assert b"D is NULL" in lib.sketch_last_error()
+
+
+def test_update_argument_errors(lib):
+    st = lib.sketch_apply_update_normsgd(NULL, 8, 12, 16, NULL, NULL, 4, 1e-3, 0, 0, 0, NULL, NULL,
+                                         NULL, NULL, 0, NULL)
+    assert st == binding.ERR_INVALID_ARG and b"k=12" in lib.sketch_last_error()
+    st = lib.sketch_apply_update_sgd(NULL, 8, 16, 16, NULL, NULL, 4, 1e-3, 0, 0, 0, NULL, NULL, 0, NULL)
+    assert st == binding.ERR_INVALID_ARG and b"W is NULL" in lib.sketch_last_error()
+
+
+def test_sample_projection_argument_errors(lib):
+    st = lib.sketch_sample_projection(5, 0, 0, 0, 64, 8, NULL, NULL, NULL, 0, NULL)
+    assert st == binding.ERR_INVALID_ARG and b"kind" in lib.sketch_last_error()
+    st = lib.sketch_sample_projection(0, 0, 0, 0, 64, 8, NULL, NULL, NULL, 0, NULL)
+    assert st == binding.ERR_INVALID_ARG and b"P is NULL" in lib.sketch_last_error()
+    st = lib.sketch_sample_projection(1, 0, 0, 0, 63, 8, NULL, NULL, NULL, 0, NULL)
+    assert st == binding.ERR_INVALID_ARG and b"k=63" in lib.sketch_last_error()
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    X = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        binding.project_inputs(X, torch.zeros(8, 2), torch.zeros(4, 2, dtype=torch.bfloat16))

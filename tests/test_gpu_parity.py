@@ -1,0 +1,363 @@
+"""GPU path against the CPU oracle, element by element, on seeded inputs.
+
+Each C-ABI call is compared with the oracle on identical inputs:
+  * Philox-driven outputs (Rademacher P) must be bit-exact;
+  * the QR frame within 1e-5 relative Frobenius of the oracle's and
+    orthonormal to 1e-5 (P^T P = (k/r) I);
+  * XP within one BF16 step of the oracle (plus 1e-5 of its RMS for values
+    near zero, the size of the fp32 accumulation error) and bit-identical on
+    >= 99% (that error, about u*sqrt(k) relative, moves a value across a BF16
+    rounding boundary on well under 1% of elements);
+  * C within 2e-3 relative Frobenius, and element-wise within 1e-4 of its RMS
+    (fp32 accumulation over T terms is good to a few 1e-6 relative);
+  * W after an update: >= 99.99% bit-identical and every other element exactly
+    one BF16 step away.
+Small cases cover several tiles plus ragged edges; full-size layer shapes are
+checked on sampled rows that the oracle computes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import rank_gradient_sketching_philox_gb300 as rgs
+from rank_gradient_sketching_philox_gb300 import binding, synth
+
+from gpu_util import bits, from_bits, rel_fro, w_parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+    orc.lib()
+
+
+# --------------------------------------------------------------------------
+# (a) projections
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("k,r,layer,step", [(512, 16, 0, 0), (4096, 64, 3, 0), (2048, 128, 7, 5),
+                                            (8192, 256, 1, 2), (24, 4, 0, 9), (16, 3, 2, 1),
+                                            (8, 1, 0, 0), (1000, 50, 11, 3)])
+def test_rademacher_bit_exact(k, r, layer, step):
+    P = torch.empty(k, r, dtype=torch.float32, device=DEV)
+    rgs.sample_projection(rgs.PROJ_RADEMACHER, 0x5EED, layer, step, P)
+    ref = orc.sample_rademacher(0x5EED, layer, step, k, r)
+    assert np.array_equal(P.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("k,r,layer,step", [(512, 16, 0, 0), (4096, 64, 2, 1), (12288, 64, 5, 3),
+                                            (2048, 256, 1, 0), (1000, 50, 4, 7), (64, 16, 0, 2),
+                                            (8192, 4, 3, 3)])
+def test_qr_projection_matches_oracle(k, r, layer, step):
+    P = torch.empty(k, r, dtype=torch.float32, device=DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 77, layer, step, P, dev_status=status)
+    assert int(status.item()) == 0
+    got = P.cpu().numpy().astype(np.float64)
+    ref = orc.sample_qr(77, layer, step, k, r)
+    assert rel_fro(got, ref) < 1e-5
+    M = got.T @ got
+    assert np.abs(M - (k / r) * np.eye(r)).max() / (k / r) < 1e-5
+
+
+def test_qr_rejects_wide_frames():
+    P = torch.empty(32, 16, dtype=torch.float32, device=DEV)
+    with pytest.raises(binding.SketchError) as ei:
+        rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 0, 0, 0, P)
+    assert ei.value.status == binding.ERR_UNSUPPORTED
+
+
+def test_projection_deterministic():
+    a = torch.empty(4096, 64, dtype=torch.float32, device=DEV)
+    b = torch.empty_like(a)
+    rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 5, 1, 1, a)
+    rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 5, 1, 1, b)
+    assert torch.equal(a, b)
+
+
+# --------------------------------------------------------------------------
+# (b) projected inputs
+# --------------------------------------------------------------------------
+
+def _pad8(n):
+    return (n + 7) // 8 * 8
+
+
+def _padded_bf16(rows, cols, device=DEV, fill=float("nan")):
+    """rows x cols BF16 view into a buffer whose row stride is a multiple of 8."""
+    return torch.full((rows, _pad8(cols)), fill, dtype=torch.bfloat16, device=device)[:, :cols]
+
+
+def _xp_check(got_bits, ref_bits):
+    """One BF16 step of the oracle's value, or the fp32-accumulation slack
+    (1e-5 of the RMS of XP) for values near zero; >= 99% bit-identical."""
+    got = orc.bf16_to_f32(got_bits).astype(np.float64)
+    ref = orc.bf16_to_f32(ref_bits).astype(np.float64)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7)
+    rms = math.sqrt(float(np.mean(ref * ref)))
+    assert np.all(np.abs(got - ref) <= ulp + 1e-5 * rms)
+    assert np.mean(got_bits == ref_bits) >= 0.99
+
+
+@pytest.mark.parametrize("T,k,r,kind", [(128, 512, 16, 1), (300, 1024, 64, 0), (77, 104, 24, 1),
+                                        (64, 256, 1, 0), (130, 2048, 256, 1), (1, 8, 3, 0)])
+def test_project_inputs_matches_oracle(T, k, r, kind):
+    X = synth.normal_bf16((T, k), 1.0, 31 + T)
+    if kind == 0:
+        P = orc.sample_rademacher(3, 0, 0, k, r)
+    else:
+        P = orc.sample_qr(3, 0, 0, k, r) if 4 * r <= k else orc.sample_rademacher(3, 0, 0, k, r)
+    XP = _padded_bf16(T, r)
+    rgs.project_inputs(X.to(DEV), torch.from_numpy(P).to(DEV), XP)
+    _xp_check(bits(XP), orc.project_inputs(bits(X), P))
+
+
+def test_project_inputs_strided_rows_leave_padding():
+    T, k, r, ld_x, ld_xp = 100, 320, 16, 336, 24
+    X_full = synth.normal_bf16((T, ld_x), 1.0, 8).to(DEV)
+    X = X_full[:, :k]
+    P = orc.sample_qr(1, 0, 0, k, r)
+    XP_full = torch.full((T, ld_xp), 7.0, dtype=torch.bfloat16, device=DEV)
+    rgs.project_inputs(X, torch.from_numpy(P).to(DEV), XP_full[:, :r])
+    _xp_check(bits(XP_full[:, :r]), orc.project_inputs(bits(X), P))
+    assert torch.all(XP_full[:, r:] == 7.0)
+
+
+def test_project_inputs_full_size_sampled_tokens():
+    """4096 tokens x k=4096 -> r=64 (the LoGRA worked example's shape), QR P;
+    compared on 64 sampled tokens."""
+    T, k, r = 4096, 4096, 64
+    X = synth.layer_x(T, k, 0, 0, device=DEV)
+    P = torch.empty(k, r, dtype=torch.float32, device=DEV)
+    rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 0, 0, 0, P)
+    XP = torch.empty(T, r, dtype=torch.bfloat16, device=DEV)
+    rgs.project_inputs(X, P, XP)
+    rows = np.random.default_rng(0).choice(T, 64, replace=False)
+    ref = orc.project_inputs(bits(X[rows]), P.cpu().numpy())
+    _xp_check(bits(XP)[rows], ref)
+
+
+# --------------------------------------------------------------------------
+# (c) accumulation
+# --------------------------------------------------------------------------
+
+def _c_check(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert rel_fro(got, ref) < 2e-3
+    rms = math.sqrt(float(np.mean(ref * ref)))
+    assert np.abs(got - ref).max() <= 1e-4 * rms
+
+
+@pytest.mark.parametrize("T,d,r,mbs", [(128, 256, 16, 4), (513, 200, 64, 2), (40, 40, 4, 3),
+                                       (1000, 1032, 256, 1), (17, 9, 1, 2), (64, 130, 20, 2)])
+def test_accumulate_matches_oracle_same_xp(T, d, r, mbs):
+    C = torch.empty(d, r, dtype=torch.float32, device=DEV)
+    C_or = np.zeros((d, r), np.float32)
+    for mb in range(mbs):
+        D = synth.normal_bf16((T, d), 1e-3, 100 + mb)
+        XPb = orc.bf16_from_double(np.random.default_rng(mb).standard_normal((T, r)) * 8)
+        Dd = _padded_bf16(T, d)
+        Dd.copy_(D.to(DEV))
+        XPd = _padded_bf16(T, r)
+        XPd.copy_(from_bits(XPb, DEV))
+        rgs.accumulate(Dd, XPd, C, overwrite=(mb == 0))
+        C_or = orc.accumulate(bits(D), XPb, C_or, overwrite=(mb == 0))
+    _c_check(C.cpu().numpy(), C_or)
+
+
+def test_accumulate_adds_to_existing_sketch():
+    T, d, r = 96, 64, 8
+    D = synth.normal_bf16((T, d), 1e-3, 4)
+    XPb = orc.bf16_from_double(np.random.default_rng(1).standard_normal((T, r)))
+    C0 = np.random.default_rng(2).standard_normal((d, r)).astype(np.float32) * 1e-3
+    C = torch.from_numpy(C0).to(DEV)
+    rgs.accumulate(D.to(DEV), from_bits(XPb, DEV), C, overwrite=False)
+    _c_check(C.cpu().numpy(), orc.accumulate(bits(D), XPb, C0, overwrite=False))
+
+
+def test_chained_sketch_matches_oracle_chain():
+    """Single linear 256 x 512, r=16, 4 microbatches of 128 tokens, both
+    projection kinds: GPU XP and C against the oracle's own chain."""
+    d, k, r, T = 256, 512, 16, 128
+    for kind in (rgs.PROJ_RADEMACHER, rgs.PROJ_GAUSSIAN_QR):
+        P = torch.empty(k, r, dtype=torch.float32, device=DEV)
+        rgs.sample_projection(kind, 0, 0, 0, P)
+        P_or = orc.sample_projection(kind, 0, 0, 0, k, r)
+        C = torch.empty(d, r, dtype=torch.float32, device=DEV)
+        C_or = np.zeros((d, r), np.float32)
+        for mb in range(4):
+            X = synth.layer_x(T, k, 0, mb)
+            D = synth.layer_d(T, d, 0, mb)
+            XP = torch.empty(T, r, dtype=torch.bfloat16, device=DEV)
+            rgs.project_inputs(X.to(DEV), P, XP)
+            rgs.accumulate(D.to(DEV), XP, C, overwrite=(mb == 0))
+            C_or = orc.accumulate(bits(D), orc.project_inputs(bits(X), P_or), C_or, overwrite=(mb == 0))
+        assert rel_fro(C.cpu().numpy(), C_or) < 2e-3
+        H = orc.rebuild(C.cpu().numpy(), P.cpu().numpy())
+        H_or = orc.rebuild(C_or, P_or)
+        assert rel_fro(H, H_or) < 2e-3
+
+
+def test_accumulate_full_size_sampled_rows():
+    """d=12288 rows (the 8B stack's gate/up), 4096 tokens, r=64, heavy-tailed D;
+    64 sampled rows of C computed by the oracle."""
+    T, d, r = 4096, 12288, 64
+    D = synth.layer_d(T, d, 5, 0, device=DEV, heavy_tail=True)
+    XPb = orc.bf16_from_double(np.random.default_rng(3).standard_normal((T, r)) * 8)
+    C = torch.empty(d, r, dtype=torch.float32, device=DEV)
+    rgs.accumulate(D, from_bits(XPb, DEV), C, overwrite=True)
+    rows = np.sort(np.random.default_rng(1).choice(d, 64, replace=False))
+    ref = orc.accumulate(bits(D[:, rows]), XPb, np.zeros((64, r), np.float32), overwrite=True)
+    _c_check(C.cpu().numpy()[rows], ref)
+
+
+# --------------------------------------------------------------------------
+# (d) updates
+# --------------------------------------------------------------------------
+
+def _w_check(got_bits, ref_bits):
+    same, maxd = w_parity(got_bits, ref_bits)
+    assert maxd <= 1, "an element is more than one BF16 step from the oracle"
+    assert same >= 0.9999, "only %.6f of W is bit-identical" % same
+    return same
+
+
+def _rand_c(d, r, seed, scale=1.0):
+    return (np.random.default_rng(seed).standard_normal((d, r)) * scale).astype(np.float32)
+
+
+@pytest.mark.parametrize("d,k,r,kind", [(256, 512, 16, 1), (256, 512, 16, 0), (40, 24, 4, 0),
+                                        (130, 136, 20, 1), (1024, 2048, 128, 1),
+                                        (300, 4096, 256, 1), (7, 8, 1, 0)])
+def test_normsgd_matches_oracle(d, k, r, kind):
+    W0 = synth.layer_weight(d, k, 3)
+    P = (orc.sample_qr(2, 3, 1, k, r) if kind == 1 and 4 * r <= k
+         else orc.sample_rademacher(2, 3, 1, k, r))
+    C = _rand_c(d, r, d + k)
+    W = W0.to(DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    out = torch.zeros(1, dtype=torch.float64, device=DEV)
+    rgs.apply_update_normsgd(W, torch.from_numpy(C).to(DEV), torch.from_numpy(P).to(DEV), 1e-3,
+                             0, 3, 1, wnorm2_out=out, dev_status=status)
+    assert int(status.item()) == 0
+    W_or, st, _ = orc.update_normsgd(bits(W0), C, P, 1e-3, 0, 3, 1, dense_h_norm=(d * k <= 1 << 22))
+    assert st == 0
+    _w_check(bits(W), W_or)
+    assert abs(out.item() - orc.norm_w(W_or) ** 2) <= 1e-6 * orc.norm_w(W_or) ** 2
+
+
+def test_normsgd_strided_w_keeps_padding():
+    d, k, r, ld = 64, 96, 8, 104
+    Wf = synth.normal_bf16((d, ld), 0.02, 5).to(DEV)
+    pad_before = Wf[:, k:].clone()
+    P = orc.sample_rademacher(0, 0, 0, k, r)
+    C = _rand_c(d, r, 9)
+    W0 = bits(Wf[:, :k])
+    rgs.apply_update_normsgd(Wf[:, :k], torch.from_numpy(C).to(DEV), torch.from_numpy(P).to(DEV),
+                             1e-3, 0, 0, 0)
+    W_or, _, _ = orc.update_normsgd(W0, C, P, 1e-3, 0, 0, 0)
+    _w_check(bits(Wf[:, :k]), W_or)
+    assert torch.equal(Wf[:, k:], pad_before)
+
+
+def test_normsgd_carried_norm_chain():
+    """Two refreshed steps; the second reuses the ||W||^2 the first wrote."""
+    d, k, r = 512, 1024, 32
+    W = synth.layer_weight(d, k, 1).to(DEV)
+    W_ref = bits(W)
+    carried = torch.zeros(1, dtype=torch.float64, device=DEV)
+    for step in range(2):
+        P = torch.empty(k, r, dtype=torch.float32, device=DEV)
+        rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 9, 1, step, P)
+        C = _rand_c(d, r, 40 + step)
+        rgs.apply_update_normsgd(W, torch.from_numpy(C).to(DEV), P, 1e-3, 9, 1, step,
+                                 wnorm2_in=carried if step else None, wnorm2_out=carried)
+        W_ref, st, _ = orc.update_normsgd(W_ref, C, P.cpu().numpy(), 1e-3, 9, 1, step)
+        assert st == 0
+        _w_check(bits(W), W_ref)
+
+
+def test_normsgd_degenerate_inputs_leave_w_unchanged():
+    d, k, r = 64, 128, 8
+    W0 = synth.layer_weight(d, k, 0).to(DEV)
+    P = torch.from_numpy(orc.sample_rademacher(0, 0, 0, k, r)).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    W = W0.clone()
+    rgs.apply_update_normsgd(W, torch.zeros(d, r, device=DEV), P, 1e-3, 0, 0, 0, dev_status=status)
+    assert int(status.item()) == binding.DEV_H_ZERO and torch.equal(W, W0)
+    C = torch.ones(d, r, device=DEV)
+    C[3, 2] = float("nan")
+    rgs.apply_update_normsgd(W, C, P, 1e-3, 0, 0, 0, dev_status=status)
+    assert int(status.item()) & binding.DEV_H_NONFINITE and torch.equal(W, W0)
+    rgs.apply_update_normsgd(W, torch.ones(d, r, device=DEV), P, 0.0, 0, 0, 0, dev_status=status)
+    assert int(status.item()) == 0 and torch.equal(W, W0)
+
+
+@pytest.mark.parametrize("d,k,r", [(4096, 4096, 64), (256, 512, 16), (72, 40, 5)])
+def test_sgd_matches_oracle(d, k, r):
+    """The LoGRA worked example shape (d = k = 4096, r = 64, alpha*eta = 1e-4)
+    with a sketch of the size 8 x 4096 tokens produce."""
+    W0 = synth.layer_weight(d, k, 2)
+    P = orc.sample_rademacher(0, 2, 0, k, r)
+    C = _rand_c(d, r, 5, scale=1.45)
+    W = W0.to(DEV)
+    rgs.apply_update_sgd(W, torch.from_numpy(C).to(DEV), torch.from_numpy(P).to(DEV), 1e-4, 0, 2, 0)
+    _w_check(bits(W), orc.update_sgd(bits(W0), C, P, 1e-4, 0, 2, 0))
+
+
+@pytest.mark.parametrize("d,k,r", [(12288, 4096, 64), (2048, 6144, 256), (28672, 8192, 16)])
+def test_normsgd_full_size_sampled_rows(d, k, r):
+    """Full layer shapes of the Qwen3 stacks and the long-response sweep; the
+    oracle computes s from the whole W and the Gram route, then the sampled
+    rows one by one."""
+    W = synth.layer_weight(d, k, 4, device=DEV)
+    W0_bits = bits(W)
+    P = torch.empty(k, r, dtype=torch.float32, device=DEV)
+    rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 1, 4, 0, P)
+    C = torch.from_numpy(_rand_c(d, r, 11)).to(DEV)
+    rgs.apply_update_normsgd(W, C, P, 1e-3, 1, 4, 0)
+    Cn, Pn = C.cpu().numpy(), P.cpu().numpy()
+    s, st = orc.normsgd_scale(orc.norm_w(W0_bits), orc.norm_h_gram(Cn, Pn), 1e-3)
+    assert st == 0
+    rows = np.sort(np.random.default_rng(d).choice(d, 16, replace=False)).astype(np.int32)
+    ref = orc.update_rows(W0_bits[rows], rows, Cn, Pn, s, 1, 4, 0)
+    _w_check(bits(W)[rows], ref)
+
+
+def test_update_repeatable():
+    d, k, r = 512, 512, 32
+    W0 = synth.layer_weight(d, k, 0).to(DEV)
+    P = torch.from_numpy(orc.sample_qr(0, 0, 0, k, r)).to(DEV)
+    C = torch.from_numpy(_rand_c(d, r, 0)).to(DEV)
+    a, b = W0.clone(), W0.clone()
+    rgs.apply_update_normsgd(a, C, P, 1e-3, 0, 0, 0)
+    rgs.apply_update_normsgd(b, C, P, 1e-3, 0, 0, 0)
+    assert torch.equal(a, b) and not torch.equal(a, W0)
+
+
+def test_calls_on_a_side_stream():
+    d, k, r, T = 128, 256, 16, 64
+    s = torch.cuda.Stream()
+    X = synth.normal_bf16((T, k), 1.0, 1).to(DEV)
+    D = synth.normal_bf16((T, d), 1e-3, 2).to(DEV)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        P = torch.empty(k, r, dtype=torch.float32, device=DEV)
+        rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 3, 0, 0, P, stream=s)
+        XP = torch.empty(T, r, dtype=torch.bfloat16, device=DEV)
+        rgs.project_inputs(X, P, XP, stream=s)
+        C = torch.empty(d, r, dtype=torch.float32, device=DEV)
+        rgs.accumulate(D, XP, C, overwrite=True, stream=s)
+    s.synchronize()
+    P_or = orc.sample_qr(3, 0, 0, k, r)
+    C_or = orc.accumulate(bits(D), orc.project_inputs(bits(X), P_or), np.zeros((d, r)), True)
+    assert rel_fro(C.cpu().numpy(), C_or) < 2e-3
