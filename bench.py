@@ -1,0 +1,484 @@
+"""Benchmark of the sketching hot path on GB300.
+
+One step = the whole path over one batch of synthetic input for a stack of
+linear layers: draw every layer's projection, then for each microbatch project
+every layer's input (XP = X P) and accumulate every layer's sketch
+(C += D^T XP), then rebuild-and-update every layer's BF16 weights.
+
+Default workload: the Qwen3-8B-shaped stack (36 blocks x q,k,v,o,gate,up,down =
+252 linears, 6.95e9 weights), rank 64, 32768 tokens per step in 4096-token
+microbatches, refreshed Gaussian-QR projections, normalized SGD with tau=1e-3.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}]
+
+Prints one JSON line (rank 0).  ``value`` is whole-job tokens/s with inputs
+resident in HBM; ``e2e`` repeats the step with every input copied from pinned
+host memory inside the timed region.  ``--impl reference`` times the CPU oracle
+(the plain C statement of the method) on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sketch-accumulate tokens/s and update weights/s on 1 GB300, % of HBM roofline"
+NBUF = 3  # input buffers per distinct shape; consecutive uses of one buffer are > 4x L2 apart
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="qwen3-8b-stack")
+    ap.add_argument("--rank", type=int, default=64)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps in the end-to-end (host buffers) measurement; default = --steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def workload_config(wl, r, n):
+    return {
+        "workload": wl.name,
+        "layers": len(wl.layers),
+        "weights": wl.weights,
+        "rank": r,
+        "tokens_per_step_per_gpu": wl.tokens_per_step,
+        "microbatch_tokens": wl.microbatch,
+        "projection": "gaussian-qr refreshed every step" if "qr" in wl.projection else wl.projection,
+        "update": "%s step_size=%g, ||W||^2 carried between steps" % (wl.update, wl.step_size),
+        "parallelism": "dp%d" % n,
+        "l2": "inputs rotate through %d buffers per shape (reuse distance > 4x L2); W, C, P per layer"
+              % NBUF,
+    }
+
+
+# --------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the workload
+# --------------------------------------------------------------------------
+
+def oracle_sample(wl, r, tokens_sample=16, rows_sample=4):
+    """Time the CPU oracle on one block of the stack and scale to one step.
+
+    Sample: the first transformer block's linears; the QR (or Rademacher)
+    projection of each; projection + accumulation of ``tokens_sample`` tokens;
+    ||W|| and the Gram-route ||H||; the update of ``rows_sample`` rows of each.
+    Per-layer, per-token and per-row costs are measured, then multiplied by the
+    step's counts (blocks, tokens, rows)."""
+    import numpy as np
+    import torch
+
+    import oracle as orc
+    from rank_gradient_sketching_philox_gb300 import synth
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    orc.lib()
+    seen, block = set(), []
+    for name, d, k in wl.layers:
+        tag = name.split(".")[-1]
+        if tag in seen:
+            break
+        seen.add(tag)
+        block.append((name, d, k))
+    nblocks = len(wl.layers) // len(block)
+    T = tokens_sample
+    t_sample = t_tok = t_norm = t_rows = 0.0
+    for li, (_, d, k) in enumerate(block):
+        t0 = time.perf_counter()
+        P = (orc.sample_qr(0, li, 0, k, r) if "qr" in wl.projection
+             else orc.sample_rademacher(0, li, 0, k, r))
+        t1 = time.perf_counter()
+        X = u16(synth.normal_bf16((T, k), 1.0, 5 + li))
+        D = u16(synth.normal_bf16((T, d), 1e-3, 9 + li))
+        t2 = time.perf_counter()
+        XP = orc.project_inputs(X, P)
+        C = orc.accumulate(D, XP, np.zeros((d, r), np.float32), overwrite=True)
+        t3 = time.perf_counter()
+        W = u16(synth.layer_weight(d, k, li))
+        t4 = time.perf_counter()
+        s, _ = orc.normsgd_scale(orc.norm_w(W), orc.norm_h_gram(C, P), wl.step_size)
+        t5 = time.perf_counter()
+        orc.update_rows(W[:rows_sample], np.arange(rows_sample, dtype=np.int32), C, P, s, 0, li, 0)
+        t6 = time.perf_counter()
+        t_sample += t1 - t0
+        t_tok += t3 - t2
+        t_norm += t5 - t4
+        t_rows += (t6 - t5) * (d / rows_sample)
+    per_step = nblocks * (t_sample + t_tok * (wl.tokens_per_step / T) + t_norm + t_rows)
+    return {
+        "step_seconds": per_step,
+        "tokens_per_s": wl.tokens_per_step / per_step,
+        "sample": ("oracle on block 0 of the stack (%d linears, r=%d): projection of each, "
+                   "projection+accumulation of %d tokens, ||W|| and Gram ||H||, update of %d rows "
+                   "each; scaled to %d blocks x %d tokens x all rows" %
+                   (len(block), r, T, rows_sample, nblocks, wl.tokens_per_step)),
+    }
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from rank_gradient_sketching_philox_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    times, rates, res = [], [], None
+    for _ in range(args.warmup):
+        oracle_sample(wl, args.rank, tokens_sample=8, rows_sample=2)
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        res = oracle_sample(wl, args.rank, tokens_sample=8, rows_sample=2)
+        times.append(time.perf_counter() - t0)
+        rates.append(res["tokens_per_s"])
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": wl.tokens_per_step / value * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(wl, args.rank, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": res["sample"], "wall_seconds_per_sample": statistics.median(times)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__ as entry
+    import rank_gradient_sketching_philox_gb300 as rgs
+    from rank_gradient_sketching_philox_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    entry.build()
+
+    wl = synth.WORKLOADS[args.workload]
+    r = args.rank
+    T = wl.microbatch
+    nmb = wl.microbatches
+    layers = wl.layers
+    L = len(layers)
+    kind = rgs.PROJ_GAUSSIAN_QR if "qr" in wl.projection else rgs.PROJ_RADEMACHER
+    seed = 0
+    tau = wl.step_size
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- resident state -------------------------------------------------
+    W = [synth.normal_bf16((d, k), synth.W_STD, synth.seed_w(li), device=dev)
+         for li, (_, d, k) in enumerate(layers)]
+    C = [torch.empty(d, r, dtype=torch.float32, device=dev) for _, d, _ in layers]
+    P = [torch.empty(k, r, dtype=torch.float32, device=dev) for _, _, k in layers]
+    XP = [torch.empty(T, max(8, (r + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :r]
+          for _ in layers]
+    wn2 = torch.zeros(L, dtype=torch.float64, device=dev)
+    status = torch.zeros(L, dtype=torch.int32, device=dev)
+    xpool, dpool = {}, {}
+    for li, (_, d, k) in enumerate(layers):
+        if k not in xpool:
+            xpool[k] = [synth.normal_bf16((T, k), synth.X_STD, 7000 + 10 * k + b, device=dev)
+                        for b in range(NBUF)]
+        if d not in dpool:
+            dpool[d] = [synth.layer_d(T, d, 9000 + d, b, device=dev, heavy_tail=wl.heavy_tail)
+                        for b in range(NBUF)]
+    torch.cuda.synchronize()
+
+    def xbuf(li, m):
+        return xpool[layers[li][2]][(li + m) % NBUF]
+
+    def dbuf(li, m):
+        return dpool[layers[li][1]][(li + 2 * m + 1) % NBUF]
+
+    def sample_phase(s):
+        for li in range(L):
+            rgs.sample_projection(kind, seed, li, s, P[li])
+
+    def project(li, m, X=None):
+        rgs.project_inputs(xbuf(li, m) if X is None else X, P[li], XP[li])
+
+    def accumulate(li, m, D=None):
+        rgs.accumulate(dbuf(li, m) if D is None else D, XP[li], C[li], overwrite=(m == 0))
+
+    def update_phase(s, carried):
+        for li in range(L):
+            rgs.apply_update_normsgd(W[li], C[li], P[li], tau, seed, li, s,
+                                     wnorm2_in=wn2[li:li + 1] if carried else None,
+                                     wnorm2_out=wn2[li:li + 1], dev_status=status[li:li + 1])
+
+    def allreduce_sketch():
+        # data parallel: each rank sketches its own microbatches; the sketches add
+        if world > 1:
+            for c in C:
+                dist.all_reduce(c)
+
+    def step(s, carried=True):
+        sample_phase(s)
+        for m in range(nmb):
+            for li in range(L):
+                project(li, m)
+            for li in reversed(range(L)):
+                accumulate(li, m)
+        allreduce_sketch()
+        update_phase(s, carried)
+
+    # ---- warm-up ---------------------------------------------------------
+    for s in range(args.warmup):
+        step(s, carried=(s > 0))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    # ---- timed region: K steps, inputs resident in HBM --------------------
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ev[0].record(stream)
+        for s in range(args.warmup, args.warmup + args.steps):
+            step(s)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+    elapsed = ev[0].elapsed_time(ev[1]) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+        dist.barrier()
+    ms_per_step = elapsed / args.steps * 1e3
+    value = wl.tokens_per_step * args.steps * world / elapsed
+
+    # ---- per-phase timings (each phase alone, same buffers) ---------------
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3
+
+    s_next = args.warmup + args.steps
+    t_sample = timed(lambda: sample_phase(s_next))
+    t_project = timed(lambda: [project(li, m) for m in range(nmb) for li in range(L)])
+    t_accum = timed(lambda: [accumulate(li, m) for m in range(nmb) for li in range(L)])
+    t_update = timed(lambda: update_phase(s_next, True))
+    nst = int((status != 0).sum().item())
+
+    # algorithmic bytes: the minimum each call must move
+    acc_bytes = sum(nmb * (2 * T * d + 2 * T * r + 8 * d * r) for _, d, _ in layers)
+    proj_bytes = sum(nmb * (2 * T * k + 2 * T * r + 4 * k * r) for _, _, k in layers)
+    upd_bytes = sum(4 * d * k + 8 * d * r + 8 * k * r for _, d, k in layers)
+    peak, peak_kind = measured_peaks()
+
+    def gbs(bytes_, secs):
+        return bytes_ / secs / 1e9
+
+    components = {
+        "sample_projection": {"ms_per_step": t_sample * 1e3, "launches": L},
+        "project_inputs": {"ms_per_step": t_project * 1e3, "tokens_per_s": wl.tokens_per_step / t_project,
+                           "gbs": gbs(proj_bytes, t_project),
+                           "hbm_frac": gbs(proj_bytes, t_project) / peak, "launches": nmb * L},
+        "accumulate": {"ms_per_step": t_accum * 1e3, "tokens_per_s": wl.tokens_per_step / t_accum,
+                       "gbs": gbs(acc_bytes, t_accum), "hbm_frac": gbs(acc_bytes, t_accum) / peak,
+                       "launches": nmb * L},
+        "update_normsgd": {"ms_per_step": t_update * 1e3, "weights_per_s": wl.weights / t_update,
+                           "gbs": gbs(upd_bytes, t_update), "hbm_frac": gbs(upd_bytes, t_update) / peak,
+                           "launches": L,
+                           "bytes_model": "4 B/weight (W read+write, ||W||^2 carried) + 8dr + 8kr"},
+        "nonzero_device_status": nst,
+    }
+    name, secs, bytes_, nl = max(("accumulate", t_accum, acc_bytes, nmb * L),
+                                 ("project_inputs", t_project, proj_bytes, nmb * L),
+                                 ("update_normsgd", t_update, upd_bytes, L), key=lambda x: x[1])
+    roofline = {
+        "kernel": name,
+        "bound": "hbm",
+        "achieved": gbs(bytes_, secs),
+        "peak": peak,
+        "unit": "GB/s",
+        "frac": gbs(bytes_, secs) / peak,
+        "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                        else "fallback 6.8 TB/s"),
+        "bytes_per_launch": bytes_ / nl,
+        "avg_launch_ms": secs / nl * 1e3,
+        "traffic": None,
+    }
+
+    # ---- end to end: inputs copied from pinned host memory every step -----
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else args.steps
+    e2e = None
+    if e2e_steps > 0:
+        hx = {k: [b.cpu().pin_memory() for b in v] for k, v in xpool.items()}
+        hd = {d: [b.cpu().pin_memory() for b in v] for d, v in dpool.items()}
+        stage_x = {k: torch.empty_like(v[0]) for k, v in xpool.items()}
+        stage_d = {d: torch.empty_like(v[0]) for d, v in dpool.items()}
+        h2d = sum(nmb * (stage_x[k].numel() * 2 + stage_d[d].numel() * 2) for _, d, k in layers)
+        d2h = status.numel() * 4 + wn2.numel() * 8
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(s_next + 1, s_next + 1 + e2e_steps):
+            sample_phase(s)
+            for m in range(nmb):
+                for li, (_, d, k) in enumerate(layers):
+                    X = stage_x[k]
+                    X.copy_(hx[k][(li + m) % NBUF], non_blocking=True)
+                    project(li, m, X)
+                for li in reversed(range(L)):
+                    d = layers[li][1]
+                    Dd = stage_d[d]
+                    Dd.copy_(hd[d][(li + 2 * m + 1) % NBUF], non_blocking=True)
+                    accumulate(li, m, Dd)
+            allreduce_sketch()
+            update_phase(s, True)
+            _ = status.cpu(), wn2.cpu()  # the step's result read back to the host
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_elapsed = e0.elapsed_time(e1) / 1e3
+        if world > 1:
+            t = torch.tensor([e2e_elapsed], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_elapsed = float(t.item())
+        e2e = {"value": wl.tokens_per_step * e2e_steps * world / e2e_elapsed, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    # this library's kernel launches per step, from the launch plan of each call
+    qr_launches = 1 + 2 * (2 + 1 + 1)  # gaussian + 2 x (gram partial, gram reduce, cholesky, apply)
+    per_step = (L * (qr_launches if kind == rgs.PROJ_GAUSSIAN_QR else 1) + 2 * nmb * L
+                + L * 4)  # update: gram partial, gram reduce, finalize, rebuild+update
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res = oracle_sample(wl, r)
+        cpu = {"value": res["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": res["sample"]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16+fp32",
+            "data": "synthetic",
+            "config": workload_config(wl, r, world),
+            "components": components,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": per_step * args.steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
