@@ -239,7 +239,7 @@ def main():
 
     import __graft_entry__ as entry
     import rank_gradient_sketching_philox_gb300 as rgs
-    from rank_gradient_sketching_philox_gb300 import synth
+    from rank_gradient_sketching_philox_gb300 import binding, synth
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -286,21 +286,34 @@ def main():
     def dbuf(li, m):
         return dpool[layers[li][1]][(li + 2 * m + 1) % NBUF]
 
+    layer_ids = list(range(L))
+    # workspaces of the batched calls, allocated once
+    ws_sample = torch.empty(rgs.workspace_bytes_batched(
+        binding.OP_SAMPLE_PROJECTION, k=[k for _, _, k in layers], r=r) if kind == rgs.PROJ_GAUSSIAN_QR
+        else 1, dtype=torch.uint8, device=dev)
+    ws_project = torch.empty(max(1, rgs.workspace_bytes_batched(
+        binding.OP_PROJECT_INPUTS, T=[T] * L, k=[k for _, _, k in layers], r=r)), dtype=torch.uint8, device=dev)
+    ws_update = torch.empty(rgs.workspace_bytes_batched(
+        binding.OP_UPDATE_NORMSGD, d=[d for _, d, _ in layers], k=[k for _, _, k in layers], r=r),
+        dtype=torch.uint8, device=dev)
+    wn2_views = [wn2[li:li + 1] for li in range(L)]
+    status_views = [status[li:li + 1] for li in range(L)]
+
     def sample_phase(s):
-        for li in range(L):
-            rgs.sample_projection(kind, seed, li, s, P[li])
+        rgs.sample_projection_batched(kind, seed, s, P, layer_ids, ws=ws_sample)
 
-    def project(li, m, X=None):
-        rgs.project_inputs(xbuf(li, m) if X is None else X, P[li], XP[li])
+    def project_phase(m, Xs=None):
+        rgs.project_inputs_batched(Xs if Xs is not None else [xbuf(li, m) for li in range(L)], P, XP,
+                                   ws=ws_project)
 
-    def accumulate(li, m, D=None):
-        rgs.accumulate(dbuf(li, m) if D is None else D, XP[li], C[li], overwrite=(m == 0))
+    def accumulate_phase(m, Ds=None):
+        rgs.accumulate_batched(Ds if Ds is not None else [dbuf(li, m) for li in range(L)], XP, C,
+                               overwrite=(m == 0))
 
     def update_phase(s, carried):
-        for li in range(L):
-            rgs.apply_update_normsgd(W[li], C[li], P[li], tau, seed, li, s,
-                                     wnorm2_in=wn2[li:li + 1] if carried else None,
-                                     wnorm2_out=wn2[li:li + 1], dev_status=status[li:li + 1])
+        rgs.apply_update_normsgd_batched(W, C, P, tau, seed, layer_ids, s,
+                                         wnorm2_in=wn2_views if carried else None,
+                                         wnorm2_out=wn2_views, dev_status=status_views, ws=ws_update)
 
     def allreduce_sketch():
         # data parallel: each rank sketches its own microbatches; the sketches add
@@ -311,10 +324,8 @@ def main():
     def step(s, carried=True):
         sample_phase(s)
         for m in range(nmb):
-            for li in range(L):
-                project(li, m)
-            for li in reversed(range(L)):
-                accumulate(li, m)
+            project_phase(m)
+            accumulate_phase(m)
         allreduce_sketch()
         update_phase(s, carried)
 
@@ -357,8 +368,8 @@ def main():
 
     s_next = args.warmup + args.steps
     t_sample = timed(lambda: sample_phase(s_next))
-    t_project = timed(lambda: [project(li, m) for m in range(nmb) for li in range(L)])
-    t_accum = timed(lambda: [accumulate(li, m) for m in range(nmb) for li in range(L)])
+    t_project = timed(lambda: [project_phase(m) for m in range(nmb)])
+    t_accum = timed(lambda: [accumulate_phase(m) for m in range(nmb)])
     t_update = timed(lambda: update_phase(s_next, True))
     nst = int((status != 0).sum().item())
 
@@ -371,23 +382,30 @@ def main():
     def gbs(bytes_, secs):
         return bytes_ / secs / 1e9
 
+    # kernel launches of each phase (from the batched launch plan)
+    ceil = lambda a, b: -(-a // b)
+    n_sample = (1 + 2 * 4) * ceil(L, 256) if kind == rgs.PROJ_GAUSSIAN_QR else ceil(L, 256)
+    n_proj = nmb * ceil(L, 96)          # skinny GEMM launches (plus one P split each)
+    n_acc = nmb * ceil(L, 96)
+    n_upd = ceil(L, 60)                 # rebuild+update launches
+    n_upd_aux = 4 * ceil(L, 128)        # Gram partial + reduce, finalize, split
     components = {
-        "sample_projection": {"ms_per_step": t_sample * 1e3, "launches": L},
+        "sample_projection": {"ms_per_step": t_sample * 1e3, "launches": n_sample},
         "project_inputs": {"ms_per_step": t_project * 1e3, "tokens_per_s": wl.tokens_per_step / t_project,
                            "gbs": gbs(proj_bytes, t_project),
-                           "hbm_frac": gbs(proj_bytes, t_project) / peak, "launches": nmb * L},
+                           "hbm_frac": gbs(proj_bytes, t_project) / peak, "launches": 2 * n_proj},
         "accumulate": {"ms_per_step": t_accum * 1e3, "tokens_per_s": wl.tokens_per_step / t_accum,
                        "gbs": gbs(acc_bytes, t_accum), "hbm_frac": gbs(acc_bytes, t_accum) / peak,
-                       "launches": nmb * L},
+                       "launches": n_acc},
         "update_normsgd": {"ms_per_step": t_update * 1e3, "weights_per_s": wl.weights / t_update,
                            "gbs": gbs(upd_bytes, t_update), "hbm_frac": gbs(upd_bytes, t_update) / peak,
-                           "launches": L,
+                           "launches": n_upd + n_upd_aux,
                            "bytes_model": "4 B/weight (W read+write, ||W||^2 carried) + 8dr + 8kr"},
         "nonzero_device_status": nst,
     }
-    name, secs, bytes_, nl = max(("accumulate", t_accum, acc_bytes, nmb * L),
-                                 ("project_inputs", t_project, proj_bytes, nmb * L),
-                                 ("update_normsgd", t_update, upd_bytes, L), key=lambda x: x[1])
+    name, secs, bytes_, nl = max(("accumulate", t_accum, acc_bytes, n_acc),
+                                 ("project_inputs", t_project, proj_bytes, n_proj),
+                                 ("update_normsgd", t_update, upd_bytes, n_upd), key=lambda x: x[1])
     roofline = {
         "kernel": name,
         "bound": "hbm",
@@ -406,11 +424,12 @@ def main():
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else args.steps
     e2e = None
     if e2e_steps > 0:
+        # every layer's X and D of a microbatch come from pinned host memory
         hx = {k: [b.cpu().pin_memory() for b in v] for k, v in xpool.items()}
         hd = {d: [b.cpu().pin_memory() for b in v] for d, v in dpool.items()}
-        stage_x = {k: torch.empty_like(v[0]) for k, v in xpool.items()}
-        stage_d = {d: torch.empty_like(v[0]) for d, v in dpool.items()}
-        h2d = sum(nmb * (stage_x[k].numel() * 2 + stage_d[d].numel() * 2) for _, d, k in layers)
+        stage_x = [torch.empty(T, k, dtype=torch.bfloat16, device=dev) for _, _, k in layers]
+        stage_d = [torch.empty(T, d, dtype=torch.bfloat16, device=dev) for _, d, _ in layers]
+        h2d = nmb * sum(stage_x[li].numel() * 2 + stage_d[li].numel() * 2 for li in range(L))
         d2h = status.numel() * 4 + wn2.numel() * 8
         torch.cuda.synchronize()
         if world > 1:
@@ -421,14 +440,11 @@ def main():
             sample_phase(s)
             for m in range(nmb):
                 for li, (_, d, k) in enumerate(layers):
-                    X = stage_x[k]
-                    X.copy_(hx[k][(li + m) % NBUF], non_blocking=True)
-                    project(li, m, X)
-                for li in reversed(range(L)):
-                    d = layers[li][1]
-                    Dd = stage_d[d]
-                    Dd.copy_(hd[d][(li + 2 * m + 1) % NBUF], non_blocking=True)
-                    accumulate(li, m, Dd)
+                    stage_x[li].copy_(hx[k][(li + m) % NBUF], non_blocking=True)
+                project_phase(m, stage_x)
+                for li, (_, d, k) in enumerate(layers):
+                    stage_d[li].copy_(hd[d][(li + 2 * m + 1) % NBUF], non_blocking=True)
+                accumulate_phase(m, stage_d)
             allreduce_sketch()
             update_phase(s, True)
             _ = status.cpu(), wn2.cpu()  # the step's result read back to the host
@@ -442,10 +458,8 @@ def main():
         e2e = {"value": wl.tokens_per_step * e2e_steps * world / e2e_elapsed, "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
-    # this library's kernel launches per step, from the launch plan of each call
-    qr_launches = 1 + 2 * (2 + 1 + 1)  # gaussian + 2 x (gram partial, gram reduce, cholesky, apply)
-    per_step = (L * (qr_launches if kind == rgs.PROJ_GAUSSIAN_QR else 1) + 2 * nmb * L
-                + L * 4)  # update: gram partial, gram reduce, finalize, rebuild+update
+    # this library's kernel launches per step, from the launch plan of each batched call
+    per_step = n_sample + 2 * n_proj + n_acc + n_upd + n_upd_aux
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res = oracle_sample(wl, r)

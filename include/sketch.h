@@ -169,6 +169,77 @@ SKETCH_API sketch_status sketch_apply_update_sgd(uint16_t* W, int64_t d, int64_t
                                       int32_t* dev_status, void* ws, size_t ws_bytes,
                                       void* stream);
 
+/* ---- Batched forms ----------------------------------------------------------
+ * One call covers many layers, one problem per layer, in a few kernel launches
+ * (every layer's tiles share each launch, so small layers still fill the GPU).
+ * Problems share r and, for the updates, the scale, seed and step; each
+ * problem follows the contract of the single-layer call of the same name
+ * (layouts, alignment, errors: a bad problem fails the whole call before
+ * anything is launched).  `problems` is a HOST array of n >= 1 entries.  The
+ * workspace is the concatenation of the problems' regions: its size is
+ * sketch_workspace_bytes_batched, the sum of the per-problem sizes. */
+typedef struct {
+    float* P;          /* k x r fp32, written */
+    int64_t k;
+    uint32_t layer;
+} sketch_projection_problem;
+
+typedef struct {
+    const uint16_t* X; /* T x k BF16 */
+    int64_t T, k, ld_x;
+    const float* P;    /* k x r fp32 */
+    uint16_t* XP;      /* T x r BF16, written */
+    int64_t ld_xp;
+} sketch_project_problem;
+
+typedef struct {
+    const uint16_t* D; /* T x d BF16 */
+    int64_t T, d, ld_d;
+    const uint16_t* XP;/* T x r BF16 */
+    int64_t ld_xp;
+    float* C;          /* d x r fp32, read (unless overwrite) and written */
+} sketch_accumulate_problem;
+
+typedef struct {
+    uint16_t* W;       /* d x k BF16, updated in place */
+    int64_t d, k, ld_w;
+    const float* C;    /* d x r fp32 */
+    const float* P;    /* k x r fp32 */
+    uint32_t layer;    /* Philox counter word of this layer's rounding stream */
+    const double* wnorm2_in;  /* normalized SGD only, nullable */
+    double* wnorm2_out;       /* normalized SGD only, nullable */
+    int32_t* dev_status;      /* nullable */
+} sketch_update_problem;
+
+/* Workspace bytes of a batched call: the sum over problems i of
+ * sketch_workspace_bytes(op, T[i], d[i], k[i], r).  Arrays an op does not use
+ * may be NULL. */
+SKETCH_API size_t sketch_workspace_bytes_batched(sketch_op op, int n, const int64_t* T, const int64_t* d,
+                                                 const int64_t* k, int64_t r);
+SKETCH_API sketch_status sketch_sample_projection_batched(sketch_proj_kind kind, uint64_t seed, uint32_t step,
+                                                          int n, const sketch_projection_problem* problems,
+                                                          int64_t r, int32_t* dev_status, void* ws,
+                                                          size_t ws_bytes, void* stream);
+SKETCH_API sketch_status sketch_project_inputs_batched(int n, const sketch_project_problem* problems, int64_t r,
+                                                       void* ws, size_t ws_bytes, void* stream);
+SKETCH_API sketch_status sketch_accumulate_batched(int n, const sketch_accumulate_problem* problems, int64_t r,
+                                                   int overwrite, void* ws, size_t ws_bytes, void* stream);
+SKETCH_API sketch_status sketch_apply_update_normsgd_batched(int n, const sketch_update_problem* problems,
+                                                             int64_t r, float tau, uint64_t seed, uint32_t step,
+                                                             void* ws, size_t ws_bytes, void* stream);
+SKETCH_API sketch_status sketch_apply_update_sgd_batched(int n, const sketch_update_problem* problems, int64_t r,
+                                                         float alpha_eta, uint64_t seed, uint32_t step, void* ws,
+                                                         size_t ws_bytes, void* stream);
+
+/* Read and clear the device error word of the current device: bits set by
+ * kernels whose bounded internal waits gave up (a kernel that cannot make
+ * progress records the failure and exits instead of hanging).  0 = none.
+ * Synchronizes `stream`.  The outputs of a call that set a bit are undefined. */
+#define SKETCH_DEVERR_TIMEOUT_LOAD 1   /* a TMA tile never arrived */
+#define SKETCH_DEVERR_TIMEOUT_MMA 2    /* tensor-core work never completed */
+#define SKETCH_DEVERR_TIMEOUT_STAGE 4  /* a pipeline stage was never released */
+SKETCH_API sketch_status sketch_read_device_errors(int32_t* flags, void* stream);
+
 /* Static string for a status code. */
 SKETCH_API const char* sketch_status_string(sketch_status status);
 

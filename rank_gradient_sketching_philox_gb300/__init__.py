@@ -6,5 +6,7 @@ The compute path is the C-ABI shared library ``lib/libsketch.so`` (declared in
 ``include/sketch.h``); ``binding`` is its thin Python wrapper.
 """
 from .binding import (PROJ_GAUSSIAN_QR, PROJ_RADEMACHER, SketchError, accumulate,  # noqa: F401
-                      apply_update_normsgd, apply_update_sgd, project_inputs, sample_projection,
-                      workspace_bytes)
+                      accumulate_batched, apply_update_normsgd, apply_update_normsgd_batched,
+                      apply_update_sgd, apply_update_sgd_batched, project_inputs,
+                      project_inputs_batched, read_device_errors, sample_projection,
+                      sample_projection_batched, workspace_bytes, workspace_bytes_batched)

@@ -35,7 +35,33 @@ DEV_QR_BREAKDOWN = 8
 
 EXPORTS = ("sketch_workspace_bytes", "sketch_sample_projection", "sketch_project_inputs",
            "sketch_accumulate", "sketch_apply_update_normsgd", "sketch_apply_update_sgd",
-           "sketch_status_string", "sketch_last_error")
+           "sketch_workspace_bytes_batched", "sketch_sample_projection_batched",
+           "sketch_project_inputs_batched", "sketch_accumulate_batched",
+           "sketch_apply_update_normsgd_batched", "sketch_apply_update_sgd_batched",
+           "sketch_read_device_errors", "sketch_status_string", "sketch_last_error")
+
+
+class ProjectionProblem(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_void_p), ("k", ctypes.c_int64), ("layer", ctypes.c_uint32)]
+
+
+class ProjectProblem(ctypes.Structure):
+    _fields_ = [("X", ctypes.c_void_p), ("T", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("ld_x", ctypes.c_int64), ("P", ctypes.c_void_p), ("XP", ctypes.c_void_p),
+                ("ld_xp", ctypes.c_int64)]
+
+
+class AccumulateProblem(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_void_p), ("T", ctypes.c_int64), ("d", ctypes.c_int64),
+                ("ld_d", ctypes.c_int64), ("XP", ctypes.c_void_p), ("ld_xp", ctypes.c_int64),
+                ("C", ctypes.c_void_p)]
+
+
+class UpdateProblem(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("d", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("ld_w", ctypes.c_int64), ("C", ctypes.c_void_p), ("P", ctypes.c_void_p),
+                ("layer", ctypes.c_uint32), ("wnorm2_in", ctypes.c_void_p),
+                ("wnorm2_out", ctypes.c_void_p), ("dev_status", ctypes.c_void_p)]
 
 
 class SketchError(RuntimeError):
@@ -63,6 +89,16 @@ _SIGS = {
                                                _vp]),
     "sketch_apply_update_sgd": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _c.c_float, _u64,
                                            _u32, _u32, _vp, _vp, _c.c_size_t, _vp]),
+    "sketch_read_device_errors": (_c.c_int, [_c.POINTER(_c.c_int32), _vp]),
+    "sketch_workspace_bytes_batched": (ctypes.c_size_t, [_c.c_int, _c.c_int, _vp, _vp, _vp, _i64]),
+    "sketch_sample_projection_batched": (_c.c_int, [_c.c_int, _u64, _u32, _c.c_int, _vp, _i64, _vp, _vp,
+                                                    _c.c_size_t, _vp]),
+    "sketch_project_inputs_batched": (_c.c_int, [_c.c_int, _vp, _i64, _vp, _c.c_size_t, _vp]),
+    "sketch_accumulate_batched": (_c.c_int, [_c.c_int, _vp, _i64, _c.c_int, _vp, _c.c_size_t, _vp]),
+    "sketch_apply_update_normsgd_batched": (_c.c_int, [_c.c_int, _vp, _i64, _c.c_float, _u64, _u32, _vp,
+                                                       _c.c_size_t, _vp]),
+    "sketch_apply_update_sgd_batched": (_c.c_int, [_c.c_int, _vp, _i64, _c.c_float, _u64, _u32, _vp,
+                                                   _c.c_size_t, _vp]),
     "sketch_status_string": (_c.c_char_p, [_c.c_int]),
     "sketch_last_error": (_c.c_char_p, []),
 }
@@ -116,11 +152,25 @@ def _contig(t, dtype, name):
         raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
 
 
-def _workspace(nbytes, device, stream):
+def _workspace(nbytes, device, stream, given=None):
+    """The caller's workspace tensor if given (checked), else a fresh one."""
     if nbytes == 0:
         return None
+    if given is not None:
+        if not given.is_cuda or given.numel() * given.element_size() < nbytes:
+            raise ValueError("workspace needs %d bytes" % nbytes)
+        return given
     with torch.cuda.stream(stream):
         return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def read_device_errors(stream=None, device=None):
+    """Read and clear the device error word (bits of timed-out waits); syncs the stream."""
+    dev = device if device is not None else torch.cuda.current_device()
+    h, _ = _stream_handle(stream, dev)
+    flags = ctypes.c_int32(0)
+    _check(lib().sketch_read_device_errors(ctypes.byref(flags), h))
+    return int(flags.value)
 
 
 def workspace_bytes(op, T=0, d=0, k=0, r=1):
@@ -213,3 +263,116 @@ def apply_update_sgd(W, C, P, alpha_eta, seed, layer, step, dev_status=None, str
                                          float(alpha_eta), seed & 0xFFFFFFFFFFFFFFFF, layer, step,
                                          _ptr(dev_status), _ptr(ws), nbytes, h))
     return W
+
+
+# --------------------------------------------------------------------------
+# Batched forms: one call per phase for a whole stack of layers
+# --------------------------------------------------------------------------
+
+def _i64_array(vals):
+    return (ctypes.c_int64 * len(vals))(*vals)
+
+
+def workspace_bytes_batched(op, T=None, d=None, k=None, r=1):
+    n = len(next(x for x in (T, d, k) if x is not None))
+    arr = [None if x is None else _i64_array(x) for x in (T, d, k)]
+    return int(lib().sketch_workspace_bytes_batched(
+        op, n, *[None if a is None else ctypes.cast(a, ctypes.c_void_p) for a in arr], r))
+
+
+def sample_projection_batched(kind, seed, step, Ps, layers, dev_status=None, ws=None, stream=None):
+    """Fill every P (k_i x r fp32) for (seed, layers[i], step)."""
+    n = len(Ps)
+    r = Ps[0].shape[1]
+    probs = (ProjectionProblem * n)()
+    for i, (P, layer) in enumerate(zip(Ps, layers)):
+        _contig(P, torch.float32, "P")
+        if P.shape[1] != r:
+            raise ValueError("all projections of a batch share r")
+        probs[i] = ProjectionProblem(P.data_ptr(), P.shape[0], layer)
+    h, s = _stream_handle(stream, Ps[0].device)
+    nbytes = (workspace_bytes_batched(OP_SAMPLE_PROJECTION, k=[P.shape[0] for P in Ps], r=r)
+              if kind == PROJ_GAUSSIAN_QR else 0)
+    wsb = _workspace(nbytes, Ps[0].device, s, ws)
+    _check(lib().sketch_sample_projection_batched(kind, seed & 0xFFFFFFFFFFFFFFFF, step, n, probs, r,
+                                                  _ptr(dev_status), _ptr(wsb), nbytes, h))
+    return Ps
+
+
+def project_inputs_batched(Xs, Ps, XPs, ws=None, stream=None):
+    n = len(Xs)
+    r = Ps[0].shape[1]
+    probs = (ProjectProblem * n)()
+    for i, (X, P, XP) in enumerate(zip(Xs, Ps, XPs)):
+        ld_x = _rows(X, torch.bfloat16, "X")
+        ld_xp = _rows(XP, torch.bfloat16, "XP")
+        _contig(P, torch.float32, "P")
+        if P.shape != (X.shape[1], r) or XP.shape[0] != X.shape[0] or XP.shape[1] < r:
+            raise ValueError("shape mismatch in problem %d" % i)
+        probs[i] = ProjectProblem(X.data_ptr(), X.shape[0], X.shape[1], ld_x, P.data_ptr(),
+                                  XP.data_ptr(), ld_xp)
+    h, s = _stream_handle(stream, Xs[0].device)
+    nbytes = workspace_bytes_batched(OP_PROJECT_INPUTS, T=[X.shape[0] for X in Xs],
+                                     k=[X.shape[1] for X in Xs], r=r)
+    wsb = _workspace(nbytes, Xs[0].device, s, ws)
+    _check(lib().sketch_project_inputs_batched(n, probs, r, _ptr(wsb), nbytes, h))
+    return XPs
+
+
+def accumulate_batched(Ds, XPs, Cs, overwrite=False, ws=None, stream=None):
+    n = len(Ds)
+    r = Cs[0].shape[1]
+    probs = (AccumulateProblem * n)()
+    for i, (D, XP, C) in enumerate(zip(Ds, XPs, Cs)):
+        ld_d = _rows(D, torch.bfloat16, "D")
+        ld_xp = _rows(XP, torch.bfloat16, "XP")
+        _contig(C, torch.float32, "C")
+        if C.shape != (D.shape[1], r) or XP.shape[0] != D.shape[0] or XP.shape[1] < r:
+            raise ValueError("shape mismatch in problem %d" % i)
+        probs[i] = AccumulateProblem(D.data_ptr(), D.shape[0], D.shape[1], ld_d, XP.data_ptr(), ld_xp,
+                                     C.data_ptr())
+    h, s = _stream_handle(stream, Ds[0].device)
+    nbytes = workspace_bytes_batched(OP_ACCUMULATE, T=[D.shape[0] for D in Ds],
+                                     d=[D.shape[1] for D in Ds], r=r)
+    wsb = _workspace(nbytes, Ds[0].device, s, ws)
+    _check(lib().sketch_accumulate_batched(n, probs, r, 1 if overwrite else 0, _ptr(wsb), nbytes, h))
+    return Cs
+
+
+def _update_batched(normsgd, Ws, Cs, Ps, step_size, seed, layers, step, wnorm2_in, wnorm2_out,
+                    dev_status, ws, stream):
+    n = len(Ws)
+    r = Cs[0].shape[1]
+    probs = (UpdateProblem * n)()
+    for i in range(n):
+        W, C, P = Ws[i], Cs[i], Ps[i]
+        ld_w = _rows(W, torch.bfloat16, "W")
+        _contig(C, torch.float32, "C")
+        _contig(P, torch.float32, "P")
+        if C.shape != (W.shape[0], r) or P.shape != (W.shape[1], r):
+            raise ValueError("shape mismatch in problem %d" % i)
+        pick = (lambda lst: None if lst is None else lst[i])
+        probs[i] = UpdateProblem(W.data_ptr(), W.shape[0], W.shape[1], ld_w, C.data_ptr(), P.data_ptr(),
+                                 layers[i], _ptr(pick(wnorm2_in)), _ptr(pick(wnorm2_out)),
+                                 _ptr(pick(dev_status)))
+    h, s = _stream_handle(stream, Ws[0].device)
+    op = OP_UPDATE_NORMSGD if normsgd else OP_UPDATE_SGD
+    nbytes = workspace_bytes_batched(op, d=[W.shape[0] for W in Ws], k=[W.shape[1] for W in Ws], r=r)
+    wsb = _workspace(nbytes, Ws[0].device, s, ws)
+    fn = lib().sketch_apply_update_normsgd_batched if normsgd else lib().sketch_apply_update_sgd_batched
+    _check(fn(n, probs, r, float(step_size), seed & 0xFFFFFFFFFFFFFFFF, step, _ptr(wsb), nbytes, h))
+    return Ws
+
+
+def apply_update_normsgd_batched(Ws, Cs, Ps, tau, seed, layers, step, wnorm2_in=None, wnorm2_out=None,
+                                 dev_status=None, ws=None, stream=None):
+    """Normalized-SGD update of every W_i (lists of per-layer tensors; the
+    optional lists hold one-element device tensors or None entries)."""
+    return _update_batched(True, Ws, Cs, Ps, tau, seed, layers, step, wnorm2_in, wnorm2_out,
+                           dev_status, ws, stream)
+
+
+def apply_update_sgd_batched(Ws, Cs, Ps, alpha_eta, seed, layers, step, dev_status=None, ws=None,
+                             stream=None):
+    return _update_batched(False, Ws, Cs, Ps, alpha_eta, seed, layers, step, None, None, dev_status,
+                           ws, stream)

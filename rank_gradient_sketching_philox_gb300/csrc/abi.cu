@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -88,19 +89,205 @@ sketch_status launch_result(cudaError_t err, const char* what) {
     if (st_ != SKETCH_OK) return st_; \
   } while (0)
 
-size_t sample_ws_bytes(sketch_proj_kind kind, int64_t k, int64_t r) {
-  if (kind != SKETCH_PROJ_GAUSSIAN_QR) return 0;
+size_t qr_ws_bytes(int64_t k, int64_t r) {
   rgs::WsCursor cur;
   rgs::carve_qr_workspace(cur, k, (int)r, nullptr);
   cur.take<int32_t>(1);  // scratch status word
+  cur.take<char>(0);
   return cur.offset;
 }
 
 size_t update_ws_bytes(bool normsgd, int64_t d, int64_t k, int64_t r) {
-  if (!normsgd) return 0;
   rgs::WsCursor cur;
-  rgs::carve_update_workspace(cur, d, k, (int)r, true, nullptr);
-  return cur.offset;
+  return rgs::carve_update_workspace(cur, d, k, (int)r, normsgd, nullptr);
+}
+
+size_t op_ws_bytes(sketch_op op, int64_t T, int64_t d, int64_t k, int64_t r) {
+  if (r < 1 || r > rgs::kMaxRank) return 0;
+  switch (op) {
+    case SKETCH_OP_SAMPLE_PROJECTION: return (k >= 1) ? qr_ws_bytes(k, r) : 0;
+    case SKETCH_OP_PROJECT_INPUTS: return (T >= 1 && k >= 1) ? rgs::project_workspace_bytes(T, k, r) : 0;
+    case SKETCH_OP_ACCUMULATE: return (T >= 1 && d >= 1) ? rgs::accumulate_workspace_bytes(T, d, r) : 0;
+    case SKETCH_OP_UPDATE_NORMSGD: return (d >= 1 && k >= 1) ? update_ws_bytes(true, d, k, r) : 0;
+    case SKETCH_OP_UPDATE_SGD: return (d >= 1 && k >= 1) ? update_ws_bytes(false, d, k, r) : 0;
+  }
+  return 0;
+}
+
+sketch_status check_n(int n) {
+  if (n < 1 || n > (1 << 20)) return fail(SKETCH_ERR_INVALID_ARG, "n=%d out of [1, 2^20]", n);
+  return SKETCH_OK;
+}
+
+// ---- per-problem checks ------------------------------------------------------
+sketch_status check_projection(const sketch_projection_problem& p) {
+  TRY(check_k(p.k));
+  CHECK_PTR(p.P);
+  return SKETCH_OK;
+}
+
+sketch_status check_project(const sketch_project_problem& p, int64_t r) {
+  TRY(check_dim("T", p.T));
+  TRY(check_k(p.k));
+  TRY(check_ld("ld_x", p.ld_x, p.k));
+  TRY(check_ld("ld_xp", p.ld_xp, r));
+  CHECK_PTR(p.X);
+  CHECK_PTR(p.P);
+  CHECK_PTR(p.XP);
+  return SKETCH_OK;
+}
+
+sketch_status check_accumulate(const sketch_accumulate_problem& p, int64_t r) {
+  TRY(check_dim("T", p.T));
+  TRY(check_dim("d", p.d));
+  TRY(check_ld("ld_d", p.ld_d, p.d));
+  TRY(check_ld("ld_xp", p.ld_xp, r));
+  CHECK_PTR(p.D);
+  CHECK_PTR(p.XP);
+  CHECK_PTR(p.C);
+  return SKETCH_OK;
+}
+
+sketch_status check_update(const sketch_update_problem& p) {
+  TRY(check_dim("d", p.d));
+  TRY(check_k(p.k));
+  TRY(check_ld("ld_w", p.ld_w, p.k));
+  CHECK_PTR(p.W);
+  CHECK_PTR(p.C);
+  CHECK_PTR(p.P);
+  CHECK_OPT_ALIGN(p.wnorm2_in, 8);
+  CHECK_OPT_ALIGN(p.wnorm2_out, 8);
+  CHECK_OPT_ALIGN(p.dev_status, 4);
+  if (p.d * p.k >= (int64_t(1) << 40)) return fail(SKETCH_ERR_INVALID_ARG, "d*k too large");
+  if ((p.d * p.k) / 8 > (int64_t)UINT32_MAX)
+    return fail(SKETCH_ERR_INVALID_ARG, "d*k exceeds the 2^35 weights one rounding stream covers");
+  return SKETCH_OK;
+}
+
+// ---- batched implementations --------------------------------------------------
+sketch_status do_sample(sketch_proj_kind kind, uint64_t seed, uint32_t step, int n,
+                        const sketch_projection_problem* probs, int64_t r, int32_t* dev_status, void* ws,
+                        size_t ws_bytes, cudaStream_t s) {
+  if (kind != SKETCH_PROJ_RADEMACHER && kind != SKETCH_PROJ_GAUSSIAN_QR)
+    return fail(SKETCH_ERR_INVALID_ARG, "unknown projection kind %d", (int)kind);
+  TRY(check_n(n));
+  if (probs == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "problems is NULL");
+  TRY(check_rank(r));
+  CHECK_OPT_ALIGN(dev_status, 4);
+  size_t need = 0;
+  for (int i = 0; i < n; ++i) {
+    TRY(check_projection(probs[i]));
+    if (probs[i].k * r > (int64_t(1) << 34)) return fail(SKETCH_ERR_INVALID_ARG, "k*r too large");
+    if (kind == SKETCH_PROJ_GAUSSIAN_QR) {
+      if (4 * r > probs[i].k)
+        return fail(SKETCH_ERR_UNSUPPORTED, "Gaussian-QR projection needs 4*r <= k (k=%lld, r=%lld)",
+                    (long long)probs[i].k, (long long)r);
+      need += qr_ws_bytes(probs[i].k, r);
+    }
+  }
+  if (kind == SKETCH_PROJ_GAUSSIAN_QR) TRY(check_ws(ws, ws_bytes, need));
+  static thread_local rgs::ProjBatch batch;
+  rgs::WsCursor cur;
+  cur.base = static_cast<char*>(ws);
+  int32_t* first_status = nullptr;
+  cudaError_t err = cudaSuccess;
+  for (int base = 0; base < n && err == cudaSuccess; base += rgs::kMaxBatch) {
+    const int m = (n - base) < rgs::kMaxBatch ? (n - base) : rgs::kMaxBatch;
+    batch.n = m;
+    batch.r = (int)r;
+    batch.seed = seed;
+    batch.step = step;
+    int64_t max_k = 0;
+    for (int i = 0; i < m; ++i) {
+      const sketch_projection_problem& pr = probs[base + i];
+      rgs::ProjProblem& pb = batch.p[i];
+      pb.P = pr.P;
+      pb.k = pr.k;
+      pb.layer = pr.layer;
+      max_k = pr.k > max_k ? pr.k : max_k;
+      if (kind == SKETCH_PROJ_RADEMACHER) {
+        pb.scale = (float)(1.0 / std::sqrt((double)r));
+      } else {
+        rgs::carve_qr_workspace(cur, pr.k, (int)r, &pb);
+        int32_t* scratch = cur.take<int32_t>(1);
+        cur.take<char>(0);
+        if (first_status == nullptr) first_status = scratch;
+        pb.scale = (float)std::sqrt((double)pr.k / (double)r);
+      }
+    }
+    if (kind == SKETCH_PROJ_RADEMACHER) {
+      err = rgs::launch_rademacher(batch, max_k, s);
+    } else {
+      batch.status = dev_status ? dev_status : first_status;
+      if (base == 0) err = cudaMemsetAsync(batch.status, 0, sizeof(int32_t), s);
+      if (err == cudaSuccess) err = rgs::launch_gaussian_qr(batch, max_k, s);
+    }
+  }
+  if (err == cudaSuccess && kind == SKETCH_PROJ_RADEMACHER && dev_status)
+    err = cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s);
+  return launch_result(err, "sample_projection");
+}
+
+sketch_status do_project(int n, const sketch_project_problem* probs, int64_t r, void* ws, size_t ws_bytes,
+                         cudaStream_t s) {
+  TRY(check_n(n));
+  if (probs == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "problems is NULL");
+  TRY(check_rank(r));
+  size_t need = 0;
+  std::vector<rgs::ProjectProblem> v((size_t)n);
+  for (int i = 0; i < n; ++i) {
+    TRY(check_project(probs[i], r));
+    need += rgs::project_workspace_bytes(probs[i].T, probs[i].k, r);
+    v[i] = rgs::ProjectProblem{probs[i].X, probs[i].T, probs[i].k, probs[i].ld_x, probs[i].P, probs[i].XP,
+                               probs[i].ld_xp};
+  }
+  TRY(check_ws(ws, ws_bytes, need));
+  return launch_result(rgs::launch_project_inputs(n, v.data(), (int)r, ws, s), "project_inputs");
+}
+
+sketch_status do_accumulate(int n, const sketch_accumulate_problem* probs, int64_t r, int overwrite, void* ws,
+                            size_t ws_bytes, cudaStream_t s) {
+  TRY(check_n(n));
+  if (probs == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "problems is NULL");
+  TRY(check_rank(r));
+  if (overwrite != 0 && overwrite != 1) return fail(SKETCH_ERR_INVALID_ARG, "overwrite must be 0 or 1");
+  size_t need = 0;
+  std::vector<rgs::AccumulateProblem> v((size_t)n);
+  for (int i = 0; i < n; ++i) {
+    TRY(check_accumulate(probs[i], r));
+    need += rgs::accumulate_workspace_bytes(probs[i].T, probs[i].d, r);
+    v[i] = rgs::AccumulateProblem{probs[i].D, probs[i].T, probs[i].d, probs[i].ld_d, probs[i].XP, probs[i].ld_xp,
+                                  probs[i].C};
+  }
+  TRY(check_ws(ws, ws_bytes, need));
+  return launch_result(rgs::launch_accumulate(n, v.data(), (int)r, overwrite, s), "accumulate");
+}
+
+sketch_status do_update(bool normsgd, int n, const sketch_update_problem* probs, int64_t r, float step_size,
+                        uint64_t seed, uint32_t step, void* ws, size_t ws_bytes, cudaStream_t s) {
+  TRY(check_n(n));
+  if (probs == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "problems is NULL");
+  TRY(check_rank(r));
+  if (!std::isfinite(step_size)) return fail(SKETCH_ERR_INVALID_ARG, "%s is not finite", normsgd ? "tau" : "alpha_eta");
+  size_t need = 0;
+  for (int i = 0; i < n; ++i) {
+    TRY(check_update(probs[i]));
+    need += update_ws_bytes(normsgd, probs[i].d, probs[i].k, r);
+  }
+  TRY(check_ws(ws, ws_bytes, need));
+  std::vector<rgs::UpdateProblem> v((size_t)n);
+  std::vector<rgs::UpdateWorkspace> w((size_t)n);
+  rgs::WsCursor cur;
+  cur.base = static_cast<char*>(ws);
+  for (int i = 0; i < n; ++i) {
+    const sketch_update_problem& p = probs[i];
+    v[i] = rgs::UpdateProblem{p.W, p.d, p.k, p.ld_w, p.C, p.P, p.layer,
+                              normsgd ? p.wnorm2_in : nullptr, normsgd ? p.wnorm2_out : nullptr, p.dev_status};
+    rgs::carve_update_workspace(cur, p.d, p.k, (int)r, normsgd, &w[i]);
+  }
+  cudaError_t err = normsgd ? rgs::launch_update_normsgd(n, v.data(), w.data(), (int)r, step_size, seed, step, s)
+                            : rgs::launch_update_sgd(n, v.data(), w.data(), (int)r, step_size, seed, step, s);
+  return launch_result(err, normsgd ? "apply_update_normsgd" : "apply_update_sgd");
 }
 
 }  // namespace
@@ -121,158 +308,93 @@ const char* sketch_status_string(sketch_status status) {
 const char* sketch_last_error(void) { return g_last_error; }
 
 size_t sketch_workspace_bytes(sketch_op op, int64_t T, int64_t d, int64_t k, int64_t r) {
-  if (r < 1 || r > rgs::kMaxRank) return 0;
-  switch (op) {
-    case SKETCH_OP_SAMPLE_PROJECTION:
-      return (k >= 1) ? sample_ws_bytes(SKETCH_PROJ_GAUSSIAN_QR, k, r) : 0;
-    case SKETCH_OP_PROJECT_INPUTS:
-      return (T >= 1 && k >= 1) ? rgs::project_workspace_bytes(T, k, r) : 0;
-    case SKETCH_OP_ACCUMULATE:
-      return (T >= 1 && d >= 1) ? rgs::accumulate_workspace_bytes(T, d, r) : 0;
-    case SKETCH_OP_UPDATE_NORMSGD:
-      return (d >= 1 && k >= 1) ? update_ws_bytes(true, d, k, r) : 0;
-    case SKETCH_OP_UPDATE_SGD:
-      return 0;
-  }
-  return 0;
+  return op_ws_bytes(op, T, d, k, r);
 }
 
-sketch_status sketch_sample_projection(sketch_proj_kind kind, uint64_t seed, uint32_t layer,
-                                       uint32_t step, int64_t k, int64_t r, float* P,
-                                       int32_t* dev_status, void* ws, size_t ws_bytes,
-                                       void* stream) {
-  if (kind != SKETCH_PROJ_RADEMACHER && kind != SKETCH_PROJ_GAUSSIAN_QR)
-    return fail(SKETCH_ERR_INVALID_ARG, "unknown projection kind %d", (int)kind);
-  TRY(check_k(k));
-  TRY(check_rank(r));
-  CHECK_PTR(P);
-  CHECK_OPT_ALIGN(dev_status, 4);
-  if (k * r > (int64_t(1) << 34)) return fail(SKETCH_ERR_INVALID_ARG, "k*r too large");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rgs::ProjBatch storage;
-  rgs::ProjBatch* batch = &storage;
-  batch->n = 1;
-  batch->r = (int)r;
-  batch->seed = seed;
-  batch->step = step;
-  rgs::ProjProblem& pb = batch->p[0];
-  pb.P = P;
-  pb.k = k;
-  pb.layer = layer;
-  cudaError_t err;
-  if (kind == SKETCH_PROJ_RADEMACHER) {
-    pb.scale = (float)(1.0 / std::sqrt((double)r));
-    if (dev_status) {
-      err = cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s);
-      if (err != cudaSuccess) return launch_result(err, "sample_projection");
-    }
-    err = rgs::launch_rademacher(*batch, k, s);
-    return launch_result(err, "sample_projection (Rademacher)");
-  }
-  if (4 * r > k) {
-    return fail(SKETCH_ERR_UNSUPPORTED, "Gaussian-QR projection needs 4*r <= k (k=%lld, r=%lld)",
-                (long long)k, (long long)r);
-  }
-  const size_t need = sample_ws_bytes(kind, k, r);
-  sketch_status st = check_ws(ws, ws_bytes, need);
-  if (st) return st;
-  rgs::WsCursor cur;
-  cur.base = static_cast<char*>(ws);
-  rgs::carve_qr_workspace(cur, k, (int)r, &pb);
-  int32_t* scratch_status = cur.take<int32_t>(1);
-  pb.scale = (float)std::sqrt((double)k / (double)r);
-  batch->status = dev_status ? dev_status : scratch_status;
-  err = cudaMemsetAsync(batch->status, 0, sizeof(int32_t), s);
-  if (err == cudaSuccess) err = rgs::launch_gaussian_qr(*batch, k, s);
-  return launch_result(err, "sample_projection (Gaussian QR)");
+size_t sketch_workspace_bytes_batched(sketch_op op, int n, const int64_t* T, const int64_t* d, const int64_t* k,
+                                      int64_t r) {
+  size_t total = 0;
+  for (int i = 0; i < n; ++i)
+    total += op_ws_bytes(op, T ? T[i] : 0, d ? d[i] : 0, k ? k[i] : 0, r);
+  return total;
 }
 
-sketch_status sketch_project_inputs(const uint16_t* X, int64_t T, int64_t k, int64_t ld_x,
-                                    const float* P, int64_t r, uint16_t* XP, int64_t ld_xp,
-                                    void* ws, size_t ws_bytes, void* stream) {
-  TRY(check_dim("T", T));
-  TRY(check_k(k));
-  TRY(check_rank(r));
-  TRY(check_ld("ld_x", ld_x, k));
-  TRY(check_ld("ld_xp", ld_xp, r));
-  CHECK_PTR(X);
-  CHECK_PTR(P);
-  CHECK_PTR(XP);
-  TRY(check_ws(ws, ws_bytes, rgs::project_workspace_bytes(T, k, r)));
-  cudaError_t err = rgs::launch_project_inputs(X, T, k, ld_x, P, (int)r, XP, ld_xp, ws,
-                                               static_cast<cudaStream_t>(stream));
-  return launch_result(err, "project_inputs");
+sketch_status sketch_sample_projection(sketch_proj_kind kind, uint64_t seed, uint32_t layer, uint32_t step,
+                                       int64_t k, int64_t r, float* P, int32_t* dev_status, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  const sketch_projection_problem p{P, k, layer};
+  return do_sample(kind, seed, step, 1, &p, r, dev_status, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
-sketch_status sketch_accumulate(const uint16_t* D, int64_t T, int64_t d, int64_t ld_d,
-                                const uint16_t* XP, int64_t ld_xp, int64_t r, float* C,
-                                int overwrite, void* ws, size_t ws_bytes, void* stream) {
-  TRY(check_dim("T", T));
-  TRY(check_dim("d", d));
-  TRY(check_rank(r));
-  TRY(check_ld("ld_d", ld_d, d));
-  TRY(check_ld("ld_xp", ld_xp, r));
-  CHECK_PTR(D);
-  CHECK_PTR(XP);
-  CHECK_PTR(C);
-  if (overwrite != 0 && overwrite != 1) return fail(SKETCH_ERR_INVALID_ARG, "overwrite must be 0 or 1");
-  TRY(check_ws(ws, ws_bytes, rgs::accumulate_workspace_bytes(T, d, r)));
-  cudaError_t err = rgs::launch_accumulate(D, T, d, ld_d, XP, ld_xp, (int)r, C, overwrite, ws,
-                                           static_cast<cudaStream_t>(stream));
-  return launch_result(err, "accumulate");
+sketch_status sketch_sample_projection_batched(sketch_proj_kind kind, uint64_t seed, uint32_t step, int n,
+                                               const sketch_projection_problem* problems, int64_t r,
+                                               int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  return do_sample(kind, seed, step, n, problems, r, dev_status, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
-static sketch_status check_update_args(uint16_t* W, int64_t d, int64_t k, int64_t ld_w,
-                                       const float* C, const float* P, int64_t r) {
-  TRY(check_dim("d", d));
-  TRY(check_k(k));
-  TRY(check_rank(r));
-  TRY(check_ld("ld_w", ld_w, k));
-  CHECK_PTR(W);
-  CHECK_PTR(C);
-  CHECK_PTR(P);
-  if (d * k >= (int64_t(1) << 40)) return fail(SKETCH_ERR_INVALID_ARG, "d*k too large");
-  if ((d * k) / 8 > (int64_t)UINT32_MAX)
-    return fail(SKETCH_ERR_INVALID_ARG, "d*k exceeds the 2^35 weights one rounding stream covers");
-  return SKETCH_OK;
+sketch_status sketch_project_inputs(const uint16_t* X, int64_t T, int64_t k, int64_t ld_x, const float* P,
+                                    int64_t r, uint16_t* XP, int64_t ld_xp, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  const sketch_project_problem p{X, T, k, ld_x, P, XP, ld_xp};
+  return do_project(1, &p, r, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
-sketch_status sketch_apply_update_normsgd(uint16_t* W, int64_t d, int64_t k, int64_t ld_w,
-                                          const float* C, const float* P, int64_t r, float tau,
-                                          uint64_t seed, uint32_t layer, uint32_t step,
-                                          const double* wnorm2_in, double* wnorm2_out,
-                                          int32_t* dev_status, void* ws, size_t ws_bytes,
-                                          void* stream) {
-  TRY(check_update_args(W, d, k, ld_w, C, P, r));
-  CHECK_OPT_ALIGN(wnorm2_in, 8);
-  CHECK_OPT_ALIGN(wnorm2_out, 8);
-  CHECK_OPT_ALIGN(dev_status, 4);
-  if (!std::isfinite(tau)) return fail(SKETCH_ERR_INVALID_ARG, "tau is not finite");
-  const size_t need = update_ws_bytes(true, d, k, r);
-  TRY(check_ws(ws, ws_bytes, need));
-  rgs::WsCursor cur;
-  cur.base = static_cast<char*>(ws);
-  rgs::UpdateWorkspace uw;
-  rgs::carve_update_workspace(cur, d, k, (int)r, true, &uw);
-  cudaError_t err = rgs::launch_update_normsgd(W, d, k, ld_w, C, P, (int)r, tau, seed, layer, step,
-                                               wnorm2_in, wnorm2_out, dev_status, uw,
-                                               static_cast<cudaStream_t>(stream));
-  return launch_result(err, "apply_update_normsgd");
+sketch_status sketch_project_inputs_batched(int n, const sketch_project_problem* problems, int64_t r, void* ws,
+                                            size_t ws_bytes, void* stream) {
+  return do_project(n, problems, r, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
-sketch_status sketch_apply_update_sgd(uint16_t* W, int64_t d, int64_t k, int64_t ld_w,
-                                      const float* C, const float* P, int64_t r, float alpha_eta,
-                                      uint64_t seed, uint32_t layer, uint32_t step,
-                                      int32_t* dev_status, void* ws, size_t ws_bytes,
+sketch_status sketch_accumulate(const uint16_t* D, int64_t T, int64_t d, int64_t ld_d, const uint16_t* XP,
+                                int64_t ld_xp, int64_t r, float* C, int overwrite, void* ws, size_t ws_bytes,
+                                void* stream) {
+  const sketch_accumulate_problem p{D, T, d, ld_d, XP, ld_xp, C};
+  return do_accumulate(1, &p, r, overwrite, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+sketch_status sketch_accumulate_batched(int n, const sketch_accumulate_problem* problems, int64_t r, int overwrite,
+                                        void* ws, size_t ws_bytes, void* stream) {
+  return do_accumulate(n, problems, r, overwrite, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+sketch_status sketch_apply_update_normsgd(uint16_t* W, int64_t d, int64_t k, int64_t ld_w, const float* C,
+                                          const float* P, int64_t r, float tau, uint64_t seed, uint32_t layer,
+                                          uint32_t step, const double* wnorm2_in, double* wnorm2_out,
+                                          int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  const sketch_update_problem p{W, d, k, ld_w, C, P, layer, wnorm2_in, wnorm2_out, dev_status};
+  return do_update(true, 1, &p, r, tau, seed, step, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+sketch_status sketch_apply_update_normsgd_batched(int n, const sketch_update_problem* problems, int64_t r,
+                                                  float tau, uint64_t seed, uint32_t step, void* ws,
+                                                  size_t ws_bytes, void* stream) {
+  return do_update(true, n, problems, r, tau, seed, step, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+sketch_status sketch_apply_update_sgd(uint16_t* W, int64_t d, int64_t k, int64_t ld_w, const float* C,
+                                      const float* P, int64_t r, float alpha_eta, uint64_t seed, uint32_t layer,
+                                      uint32_t step, int32_t* dev_status, void* ws, size_t ws_bytes,
                                       void* stream) {
-  (void)ws;
-  (void)ws_bytes;
-  TRY(check_update_args(W, d, k, ld_w, C, P, r));
-  CHECK_OPT_ALIGN(dev_status, 4);
-  if (!std::isfinite(alpha_eta)) return fail(SKETCH_ERR_INVALID_ARG, "alpha_eta is not finite");
-  cudaError_t err = rgs::launch_update_sgd(W, d, k, ld_w, C, P, (int)r, alpha_eta, seed, layer, step,
-                                           dev_status, static_cast<cudaStream_t>(stream));
-  return launch_result(err, "apply_update_sgd");
+  const sketch_update_problem p{W, d, k, ld_w, C, P, layer, nullptr, nullptr, dev_status};
+  return do_update(false, 1, &p, r, alpha_eta, seed, step, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+sketch_status sketch_apply_update_sgd_batched(int n, const sketch_update_problem* problems, int64_t r,
+                                              float alpha_eta, uint64_t seed, uint32_t step, void* ws,
+                                              size_t ws_bytes, void* stream) {
+  return do_update(false, n, problems, r, alpha_eta, seed, step, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+sketch_status sketch_read_device_errors(int32_t* flags, void* stream) {
+  if (flags == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "flags is NULL");
+  int* word = nullptr;
+  cudaError_t err = rgs::device_error_word(&word);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  if (err == cudaSuccess) err = cudaMemcpyAsync(&host, word, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaMemsetAsync(word, 0, sizeof(int32_t), s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  *flags = host;
+  return launch_result(err, "read_device_errors");
 }
 
 }  // extern "C"

@@ -3,9 +3,10 @@
 // ||C P^T||_F^2 = <P^T P, C^T C>.
 //
 // Two deterministic passes over a batch of matrices: partial Grams over at
-// most 64 fixed row chunks (each output of a chunk is one fp32 dot product over
-// that chunk's rows), then a fixed-order fp32 sum over the chunks.  Neither pass
-// uses atomics, so the result does not depend on scheduling.
+// most 64 fixed row chunks, then a fixed-order sum over the chunks.  Products
+// are summed in fp32 over 32-row tiles and the tiles in double, so an entry is
+// good to about 1e-8 relative.  Neither pass uses atomics, so the result does
+// not depend on scheduling.
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,7 +31,7 @@ __global__ void __launch_bounds__(256) gram_partial_kernel(const GramBatch batch
   int64_t row_end = row_begin + g.chunk_rows;
   if (row_end > en.rows) row_end = en.rows;
   const float* __restrict__ A = en.A;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  double acc[4] = {0.0, 0.0, 0.0, 0.0};
   for (int64_t base = row_begin; base < row_end; base += kTile) {
     for (int i = ty; i < kTile; i += 8) {
       const int64_t row = base + i;
@@ -39,15 +40,18 @@ __global__ void __launch_bounds__(256) gram_partial_kernel(const GramBatch batch
       sb[i][tx] = (ok && b0 + tx < r) ? A[row * r + b0 + tx] : 0.f;
     }
     __syncthreads();
+    float tile[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int i = 0; i < kTile; ++i) {
       const float bv = sb[i][tx];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) acc[m] = fmaf(sa[i][ty + 8 * m], bv, acc[m]);
+      for (int m = 0; m < 4; ++m) tile[m] = fmaf(sa[i][ty + 8 * m], bv, tile[m]);
     }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) acc[m] += (double)tile[m];
     __syncthreads();
   }
-  float* out = en.partials + (size_t)blockIdx.x * r * r;
+  double* out = en.partials + (size_t)blockIdx.x * r * r;
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int a = a0 + ty + 8 * m, b = b0 + tx;
@@ -62,7 +66,7 @@ __global__ void gram_reduce_kernel(const GramBatch batch) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= rr) return;
   const int nchunks = gram_chunks(en.rows).nchunks;
-  float s = 0.f;
+  double s = 0.0;
   for (int c = 0; c < nchunks; ++c) s += en.partials[(size_t)c * rr + e];
   en.out[e] = s;
 }

@@ -2,6 +2,7 @@
 // Arguments have been validated by the caller; these functions only launch.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -23,6 +24,14 @@ struct WsCursor {
   }
 };
 
+// ---- runtime helpers (runtime.cu) -----------------------------------------
+// BF16 2-D tensor map, 128-byte swizzle, zero fill outside the tensor.
+cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+// Device address of the current device's error word (bits from tc.cuh).
+cudaError_t device_error_word(int** out);
+int num_sms();
+
 // Row chunking of a partial Gram matrix over `rows` rows: at most 64 chunks.
 struct GramChunks {
   int nchunks;
@@ -42,8 +51,8 @@ __host__ __device__ inline GramChunks gram_chunks(int64_t rows) {
 struct GramEntry {
   const float* A;   // rows x r, row-major
   int64_t rows;
-  float* partials;  // gram_chunks(rows).nchunks x r x r
-  float* out;       // r x r
+  double* partials; // gram_chunks(rows).nchunks x r x r
+  double* out;      // r x r
 };
 struct GramBatch {
   int n;
@@ -58,8 +67,8 @@ struct ProjProblem {
   int64_t k;
   uint32_t layer;
   float scale;      // QR: sqrt(k / r) rounded to fp32; Rademacher: 1/sqrt(r)
-  float* partials;  // QR: nchunks(k) x r x r
-  float* gram;      // QR: r x r
+  double* partials; // QR: nchunks(k) x r x r
+  double* gram;     // QR: r x r
   float* rinv;      // QR: r x r
 };
 struct ProjBatch {
@@ -77,41 +86,61 @@ cudaError_t launch_rademacher(const ProjBatch& batch, int64_t max_k, cudaStream_
 cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream_t stream);
 
 // ---- (b) projected inputs -------------------------------------------------
+struct ProjectProblem {
+  const uint16_t* X;  // T x k BF16, row stride ld_x
+  int64_t T, k, ld_x;
+  const float* P;     // k x r fp32
+  uint16_t* XP;       // T x r BF16, row stride ld_xp
+  int64_t ld_xp;
+};
 size_t project_workspace_bytes(int64_t T, int64_t k, int64_t r);
-cudaError_t launch_project_inputs(const uint16_t* X, int64_t T, int64_t k, int64_t ld_x,
-                                  const float* P, int r, uint16_t* XP, int64_t ld_xp, void* ws,
-                                  cudaStream_t stream);
+// Workspace: the problems' regions of project_workspace_bytes, back to back.
+cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, void* ws, cudaStream_t stream);
 
 // ---- (c) sketch accumulation ----------------------------------------------
+struct AccumulateProblem {
+  const uint16_t* D;  // T x d BF16, row stride ld_d
+  int64_t T, d, ld_d;
+  const uint16_t* XP; // T x r BF16, row stride ld_xp
+  int64_t ld_xp;
+  float* C;           // d x r fp32
+};
 size_t accumulate_workspace_bytes(int64_t T, int64_t d, int64_t r);
-cudaError_t launch_accumulate(const uint16_t* D, int64_t T, int64_t d, int64_t ld_d,
-                              const uint16_t* XP, int64_t ld_xp, int r, float* C, int overwrite,
-                              void* ws, cudaStream_t stream);
+cudaError_t launch_accumulate(int n, const AccumulateProblem* probs, int r, int overwrite, cudaStream_t stream);
 
 // ---- (d) rebuild + update -------------------------------------------------
+struct UpdateProblem {
+  uint16_t* W;        // d x k BF16, row stride ld_w
+  int64_t d, k, ld_w;
+  const float* C;     // d x r fp32
+  const float* P;     // k x r fp32
+  uint32_t layer;
+  const double* wnorm2_in;
+  double* wnorm2_out;
+  int32_t* dev_status;
+};
 struct UpdateWorkspace {
-  float* gram_partials_p;  // nchunks(k) x r x r
-  float* gram_partials_c;  // nchunks(d) x r x r
-  float* gram_p;           // r x r
-  float* gram_c;           // r x r
+  double* gram_partials_p; // nchunks(k) x r x r
+  double* gram_partials_c; // nchunks(d) x r x r
+  double* gram_p;          // r x r
+  double* gram_c;          // r x r
+  float* c_norm;           // d: Euclidean norm of each row of C
+  float* p_norm;           // k: Euclidean norm of each row of P
   double* wnorm_partials;  // kWnormBlocks
-  double* wnew_partials;   // one per update block
   float* scale;            // the step scale s
   int32_t* status;         // scratch status when the caller passes none
   uint32_t* ticket;        // last-block counter of the update kernel
+  double* wnew_partials;   // one per update block
+  uint16_t* c_split;       // d x 2 r_pad BF16: [high | low] part of C
+  uint16_t* p_split;       // k x 2 r_pad BF16: [high | low] part of P
 };
 constexpr int kWnormBlocks = 1024;
-void carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool normsgd,
-                            UpdateWorkspace* ws);
+// Carves one layer's workspace at the cursor; returns its size (a multiple of 256).
+size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool normsgd, UpdateWorkspace* ws);
 
-cudaError_t launch_update_normsgd(uint16_t* W, int64_t d, int64_t k, int64_t ld_w, const float* C,
-                                  const float* P, int r, float tau, uint64_t seed, uint32_t layer,
-                                  uint32_t step, const double* wnorm2_in, double* wnorm2_out,
-                                  int32_t* dev_status, const UpdateWorkspace& ws,
-                                  cudaStream_t stream);
-cudaError_t launch_update_sgd(uint16_t* W, int64_t d, int64_t k, int64_t ld_w, const float* C,
-                              const float* P, int r, float alpha_eta, uint64_t seed,
-                              uint32_t layer, uint32_t step, int32_t* dev_status,
-                              cudaStream_t stream);
+cudaError_t launch_update_normsgd(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, float tau,
+                                  uint64_t seed, uint32_t step, cudaStream_t stream);
+cudaError_t launch_update_sgd(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, float alpha_eta,
+                              uint64_t seed, uint32_t step, cudaStream_t stream);
 
 }  // namespace rgs

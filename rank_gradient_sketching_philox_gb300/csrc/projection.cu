@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
   for (int i = warp; i < r; i += nwarps)
-    for (int j = i + lane; j < r; j += 32) R[packed_upper(i, j, r)] = pb.gram[i * r + j];
+    for (int j = i + lane; j < r; j += 32) R[packed_upper(i, j, r)] = (float)pb.gram[i * r + j];
   __syncthreads();
   bool broken = false;
   for (int p = 0; p < r; ++p) {
@@ -157,8 +157,8 @@ __global__ void __launch_bounds__(256) tri_apply_kernel(const ProjBatch batch, i
 
 void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
   const GramChunks g = gram_chunks(k);
-  float* partials = cur.take<float>((size_t)g.nchunks * r * r);
-  float* gram = cur.take<float>((size_t)r * r);
+  double* partials = cur.take<double>((size_t)g.nchunks * r * r);
+  double* gram = cur.take<double>((size_t)r * r);
   float* rinv = cur.take<float>((size_t)r * r);
   if (p) {
     p->partials = partials;

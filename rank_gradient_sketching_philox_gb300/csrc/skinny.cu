@@ -1,0 +1,422 @@
+// Skinny GEMMs of the sketch path on the 5th-generation tensor cores:
+//   (b) XP = bf16(X P)        M = tokens, N = r, K = k       (A, B K-major)
+//   (c) C (+)= D^T XP (fp32)  M = d,      N = r, K = tokens  (A, B MN-major)
+// ("Randomized Gradient Compression", "How it works": the layer saves X P and
+// accumulates C += D.T (X P); "LoGRA: Scaling LLM Reinforcement Learning with
+// Low-Rank Gradient Sketches", Key Contributions 1: in fp32.)
+//
+// Both are HBM-bound streams of one BF16 operand (X or D) against a small,
+// L2-resident second operand.  Design per CTA (128 threads):
+//   * 128 output rows; the K range is split across a thread-block cluster of S
+//     CTAs (S in 1..8), so a few M tiles still fill the GPU;
+//   * warp 0 lane 0 streams 64-wide K chunks into a ring of shared-memory stages
+//     with TMA (128-byte swizzle), completion counted on mbarriers;
+//   * warp 1 lane 0 issues tcgen05.mma (M=128, N=r rounded to 16, K=16) into a
+//     TMEM accumulator and releases each stage with tcgen05.commit;
+//   * the four warps move the accumulator TMEM -> shared memory, then each CTA
+//     of the cluster sums a 128/S-row slice of all S partial tiles through
+//     distributed shared memory in a fixed order (deterministic, no atomics and
+//     no global scratch) and writes its rows.
+// XP = X P uses P split into BF16 high and low parts (P = hi + lo to 2^-17),
+// summed by two MMAs into the same accumulator, so XP is fp32-accurate before
+// its final rounding.  Every wait is bounded (tc.cuh) and sets the device error
+// word instead of hanging.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace rgs {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kChunk = 64;  // K elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kMaxStages = 8;
+
+// A launch covers up to kMaxProblems independent problems that share r (and so
+// N): one GEMM per layer.  Their M tiles are laid end to end along grid.y.
+constexpr int kMaxProblems = 96;
+
+struct SkinnyBatch {
+  CUtensorMap tmA[kMaxProblems];   // X (K-major) or D (MN-major) of each problem
+  CUtensorMap tmB[kMaxProblems];   // P^T split [hi rows; lo rows] or XP
+  void* out[kMaxProblems];
+  int64_t ld_out[kMaxProblems];    // row stride of out, in elements
+  int M[kMaxProblems];             // output rows
+  int kchunks[kMaxProblems];       // 64-wide K chunks
+  int tile_begin[kMaxProblems + 1];
+  int n;                           // problems in this launch
+  int N;                           // output columns (r)
+  int n_pad;                       // MMA N: r rounded up to 16
+  int stages;                      // pipeline depth
+  uint32_t a_bytes;                // A tile bytes per stage (16 KB)
+  uint32_t b_bytes;                // bytes of one B tile per stage
+  uint32_t stage_bytes;            // a_bytes + NB * b_bytes
+  int red_stride;                  // floats per row of the fp32 reduction tile
+  uint32_t tmem_cols;              // power of two >= max(32, n_pad)
+  int out_mode;                    // 0: BF16 round-to-nearest store; 1: fp32 store; 2: fp32 add
+  int* err;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <bool A_MN, bool B_MN, int NB>
+__global__ void __launch_bounds__(kThreads, 1) skinny_gemm_kernel(const __grid_constant__ SkinnyBatch a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ volatile int issued, consumed;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t S = gridDim.x;
+  const uint32_t rank = (S > 1) ? tc::cluster_ctarank() : 0u;
+  int p = 0;
+  while (p + 1 < a.n && a.tile_begin[p + 1] <= (int)blockIdx.y) ++p;
+  const CUtensorMap* tmA = &a.tmA[p];
+  const CUtensorMap* tmB = &a.tmB[p];
+  const int M = a.M[p];
+  const int kchunks = a.kchunks[p];
+  const int m0 = ((int)blockIdx.y - a.tile_begin[p]) * 128;
+  const int c_begin = (int)((int64_t)kchunks * rank / S);
+  const int c_end = (int)((int64_t)kchunks * (rank + 1) / S);
+  const int nmine = c_end - c_begin;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    issued = 0;
+    consumed = 0;
+    for (int s = 0; s < a.stages; ++s) {
+      tc::mbar_init(&full_bar[s], 1);
+      tc::mbar_init(&empty_bar[s], 1);
+    }
+    tc::mbar_init(&acc_bar, 1);
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(tmA);
+    tc::prefetch_tmap(tmB);
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, a.tmem_cols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: TMA ring ----
+    for (int i = 0; i < nmine; ++i) {
+      const int s = i % a.stages, u = i / a.stages;
+      if (u > 0 && !tc::mbar_wait(&empty_bar[s], (u - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))
+        break;
+      uint8_t* st = smem + (size_t)s * a.stage_bytes;
+      tc::mbar_arrive_expect_tx(&full_bar[s], a.stage_bytes);
+      const int kc = (c_begin + i) * kChunk;
+      if (A_MN) {  // D: [64 tokens][64 rows of C] per box, two boxes for 128 rows
+        tc::tma_load_2d(st, tmA, &full_bar[s], m0, kc);
+        tc::tma_load_2d(st + 8192, tmA, &full_bar[s], m0 + 64, kc);
+      } else {  // X: [128 tokens][64 k]
+        tc::tma_load_2d(st, tmA, &full_bar[s], kc, m0);
+      }
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        uint8_t* bt = st + a.a_bytes + nb * a.b_bytes;
+        if (B_MN) {  // XP: [64 tokens][64 rank columns] per box
+          for (int j = 0; j * 64 < a.n_pad; ++j) tc::tma_load_2d(bt + j * 8192, tmB, &full_bar[s], j * 64, kc);
+        } else {  // P^T split: [n_pad rank rows][64 k]; high part in rows [0, n_pad), low in [n_pad, 2 n_pad)
+          tc::tma_load_2d(bt, tmB, &full_bar[s], kc, nb * a.n_pad);
+        }
+      }
+      issued = i + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer ----
+    const uint32_t idesc = tc::idesc_bf16(128, a.n_pad, A_MN, B_MN);
+    for (int i = 0; i < nmine; ++i) {
+      const int s = i % a.stages, u = i / a.stages;
+      if (!tc::mbar_wait(&full_bar[s], u & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) break;
+      tc::tc_fence_after();
+      const uint32_t sa = tc::smem_u32(smem + (size_t)s * a.stage_bytes);
+#pragma unroll
+      for (int kk = 0; kk < kChunk / 16; ++kk) {
+        const uint64_t ad = A_MN ? tc::sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                 : tc::sdesc_sw128(sa + kk * 32, 16, 1024);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const uint32_t sb = sa + a.a_bytes + nb * a.b_bytes;
+          const uint64_t bd = B_MN ? tc::sdesc_sw128(sb + kk * 2048, 8192, 1024)
+                                   : tc::sdesc_sw128(sb + kk * 32, 16, 1024);
+          tc::mma_bf16(tmem, ad, bd, idesc, (i > 0 || kk > 0 || nb > 0) ? 1u : 0u);
+        }
+      }
+      tc::mma_commit(&empty_bar[s]);
+      consumed = i + 1;
+    }
+    if (nmine > 0) tc::mma_commit(&acc_bar);
+  }
+  __syncwarp();
+
+  // ---- accumulator -> shared memory (fp32, row stride red_stride) ----
+  float* red = reinterpret_cast<float*>(smem);  // all stages are consumed once acc_bar fires
+  const int q = warp * 32 + lane;               // accumulator row = TMEM lane
+  const int ncols32 = (a.n_pad + 31) / 32;
+  bool have = false;
+  if (nmine > 0) have = tc::mbar_wait(&acc_bar, 0, &abort_flag, a.err, tc::kErrTimeoutMma);
+  tc::tc_fence_after();
+  if (have) {
+    for (int cg = 0; cg < ncols32; ++cg) {
+      uint32_t v[32];
+      tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cg * 32), v);
+      tc::tmem_wait_ld();
+      float4* dst = reinterpret_cast<float4*>(red + (size_t)q * a.red_stride + cg * 32);
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        dst[t] = make_float4(__uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]),
+                             __uint_as_float(v[4 * t + 2]), __uint_as_float(v[4 * t + 3]));
+    }
+  } else {
+    float4* dst = reinterpret_cast<float4*>(red + (size_t)q * a.red_stride);
+    for (int t = 0; t < ncols32 * 8; ++t) dst[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (S > 1) tc::cluster_sync();
+  else __syncthreads();
+
+  // ---- cluster reduction of this CTA's row slice, fixed order over ranks ----
+  const int rows_per = 128 / (int)S;
+  const int r0 = (int)rank * rows_per;
+  const int ncol4 = (a.N + 3) / 4;
+  const uint32_t red_base = tc::smem_u32(red);
+  for (int e = threadIdx.x; e < rows_per * ncol4; e += kThreads) {
+    const int row = r0 + e / ncol4, c = (e % ncol4) * 4;
+    const uint32_t off = (uint32_t)((row * a.red_stride + c) * 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (uint32_t src = 0; src < S; ++src) {
+      const float4 v = (S > 1) ? tc::ld_dsmem_f4(tc::mapa_shared(red_base + off, src))
+                               : *reinterpret_cast<const float4*>(red + row * a.red_stride + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int64_t grow = (int64_t)m0 + row;
+    if (grow >= M || abort_flag) continue;
+    const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (a.out_mode == 0) {
+      uint16_t* o = static_cast<uint16_t*>(a.out[p]) + grow * a.ld_out[p] + c;
+      for (int t = 0; t < 4 && c + t < a.N; ++t) o[t] = __bfloat16_as_ushort(__float2bfloat16_rn(vals[t]));
+    } else {
+      float* o = static_cast<float*>(a.out[p]) + grow * a.ld_out[p] + c;
+      for (int t = 0; t < 4 && c + t < a.N; ++t) o[t] = (a.out_mode == 2) ? o[t] + vals[t] : vals[t];
+    }
+  }
+  if (S > 1) tc::cluster_sync();  // no CTA leaves while its tile may still be read
+
+  // ---- on a timeout, give copies still in flight a bounded chance to land ----
+  if (threadIdx.x == 0 && abort_flag) {
+    volatile int dummy = 0;
+    for (int i = consumed; i < issued; ++i)
+      tc::mbar_wait(&full_bar[i % a.stages], (i / a.stages) & 1, &dummy, nullptr, 0, 100000000ull);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// P (k x r fp32) -> P^T split into BF16 high and low parts: rows [0, n_pad)
+// hold the high part, rows [n_pad, 2 n_pad) the low part, each k wide; rank
+// rows r..n_pad-1 are zero.  32 x 32 tiles transposed through shared memory;
+// grid.z indexes the problem.
+struct SplitT {
+  const float* P[kMaxProblems];
+  uint16_t* out[kMaxProblems];
+  int64_t k[kMaxProblems];
+  int r;
+  int n_pad;
+};
+
+__global__ void __launch_bounds__(256) split_transpose_kernel(const __grid_constant__ SplitT a) {
+  __shared__ float t[32][33];
+  const int pr = blockIdx.z;
+  const int64_t k = a.k[pr];
+  const int64_t j0 = (int64_t)blockIdx.x * 32;
+  if (j0 >= k) return;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int l0 = blockIdx.y * 32;
+  const int r = a.r, n_pad = a.n_pad;
+  const float* P = a.P[pr];
+  for (int dy = ty; dy < 32; dy += 8) {
+    const int64_t j = j0 + dy;
+    const int l = l0 + tx;
+    t[dy][tx] = (j < k && l < r) ? P[j * r + l] : 0.f;
+  }
+  __syncthreads();
+  uint16_t* hi = a.out[pr];
+  uint16_t* lo = hi + (int64_t)n_pad * k;
+  for (int dy = ty; dy < 32; dy += 8) {
+    const int l = l0 + dy;
+    const int64_t j = j0 + tx;
+    if (l < n_pad && j < k) {
+      const float v = t[tx][dy];
+      const __nv_bfloat16 h = __float2bfloat16_rn(v);
+      const __nv_bfloat16 w = __float2bfloat16_rn(v - __bfloat162float(h));
+      hi[(int64_t)l * k + j] = __bfloat16_as_ushort(h);
+      lo[(int64_t)l * k + j] = __bfloat16_as_ushort(w);
+    }
+  }
+}
+
+int round16(int r) { return (r + 15) / 16 * 16; }
+
+uint32_t tmem_cols_for(int n_pad) {
+  uint32_t c = 32;
+  while ((int)c < n_pad) c <<= 1;
+  return c;
+}
+
+// Cluster split: enough CTAs for two per SM, at most 8 per cluster and at
+// least one K chunk per CTA.
+int choose_split(int m_tiles, int kchunks) {
+  const int target = 2 * num_sms();
+  int s = 1;
+  while (s < 8 && m_tiles * s < target && 2 * s <= kchunks) s *= 2;
+  return s;
+}
+
+// Launch geometry of a batch: cluster split, stages, shared memory.
+template <bool A_MN, bool B_MN, int NB>
+cudaError_t launch_skinny(SkinnyBatch& a, cudaStream_t stream) {
+  const int tiles = a.tile_begin[a.n];
+  int min_chunks = a.kchunks[0];
+  for (int i = 1; i < a.n; ++i) min_chunks = a.kchunks[i] < min_chunks ? a.kchunks[i] : min_chunks;
+  const int split = choose_split(tiles, min_chunks);
+  a.stage_bytes = a.a_bytes + NB * a.b_bytes;
+  const uint32_t budget = 96u * 1024u;  // two CTAs per SM when the stages fit
+  int stages = (int)(budget / a.stage_bytes);
+  if (stages < 2) stages = 2;
+  if (stages > kMaxStages) stages = kMaxStages;
+  a.stages = stages;
+  a.red_stride = (a.n_pad + 31) / 32 * 32 + 4;
+  a.tmem_cols = tmem_cols_for(a.n_pad);
+  size_t smem = (size_t)stages * a.stage_bytes;
+  const size_t red_bytes = (size_t)128 * a.red_stride * sizeof(float);
+  if (red_bytes > smem) smem = red_bytes;
+  // at most two CTAs per SM, so their TMEM (<= 2 x 256 columns) always fits
+  if (smem < 80 * 1024) smem = 80 * 1024;
+  smem += 1024;  // alignment slack
+  auto kernel = skinny_gemm_kernel<A_MN, B_MN, NB>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)split, (unsigned)tiles, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+}  // namespace
+
+size_t project_workspace_bytes(int64_t, int64_t k, int64_t r) {
+  WsCursor cur;
+  cur.take<uint16_t>((size_t)2 * round16((int)r) * k);
+  cur.take<char>(0);  // a multiple of 256, so regions of a batch stay aligned
+  return cur.offset;
+}
+
+cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, void* ws, cudaStream_t stream) {
+  const int n_pad = round16(r);
+  int* errw = nullptr;
+  cudaError_t err = device_error_word(&errw);
+  if (err != cudaSuccess) return err;
+  WsCursor cur;
+  cur.base = static_cast<char*>(ws);
+  static thread_local SkinnyBatch a;
+  static thread_local SplitT sp;
+  for (int base = 0; base < n; base += kMaxProblems) {
+    const int m = (n - base) < kMaxProblems ? (n - base) : kMaxProblems;
+    int64_t max_k = 0;
+    a.tile_begin[0] = 0;
+    for (int i = 0; i < m; ++i) {
+      const ProjectProblem& pr = probs[base + i];
+      uint16_t* pt = cur.take<uint16_t>((size_t)2 * n_pad * pr.k);
+      cur.take<char>(0);
+      sp.P[i] = pr.P;
+      sp.out[i] = pt;
+      sp.k[i] = pr.k;
+      max_k = pr.k > max_k ? pr.k : max_k;
+      err = make_tmap_bf16_2d(&a.tmA[i], pr.X, (uint64_t)pr.k, (uint64_t)pr.T, (uint64_t)pr.ld_x * 2, 64, 128);
+      if (err == cudaSuccess)
+        err = make_tmap_bf16_2d(&a.tmB[i], pt, (uint64_t)pr.k, (uint64_t)2 * n_pad, (uint64_t)pr.k * 2, 64,
+                                (uint32_t)n_pad);
+      if (err != cudaSuccess) return err;
+      a.out[i] = pr.XP;
+      a.ld_out[i] = pr.ld_xp;
+      a.M[i] = (int)pr.T;
+      a.kchunks[i] = (int)ceil_div(pr.k, kChunk);
+      a.tile_begin[i + 1] = a.tile_begin[i] + (int)ceil_div(pr.T, 128);
+    }
+    sp.r = r;
+    sp.n_pad = n_pad;
+    split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 32), (unsigned)ceil_div(n_pad, 32), (unsigned)m), 256, 0,
+                             stream>>>(sp);
+    a.n = m;
+    a.N = r;
+    a.n_pad = n_pad;
+    a.a_bytes = 128 * kChunk * 2;
+    a.b_bytes = (uint32_t)n_pad * kChunk * 2;
+    a.out_mode = 0;
+    a.err = errw;
+    err = launch_skinny<false, false, 2>(a, stream);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaGetLastError();
+}
+
+size_t accumulate_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
+
+cudaError_t launch_accumulate(int n, const AccumulateProblem* probs, int r, int overwrite, cudaStream_t stream) {
+  const int n_pad = round16(r);
+  int* errw = nullptr;
+  cudaError_t err = device_error_word(&errw);
+  if (err != cudaSuccess) return err;
+  static thread_local SkinnyBatch a;
+  for (int base = 0; base < n; base += kMaxProblems) {
+    const int m = (n - base) < kMaxProblems ? (n - base) : kMaxProblems;
+    a.tile_begin[0] = 0;
+    for (int i = 0; i < m; ++i) {
+      const AccumulateProblem& pr = probs[base + i];
+      err = make_tmap_bf16_2d(&a.tmA[i], pr.D, (uint64_t)pr.d, (uint64_t)pr.T, (uint64_t)pr.ld_d * 2, 64, 64);
+      if (err == cudaSuccess)
+        err = make_tmap_bf16_2d(&a.tmB[i], pr.XP, (uint64_t)r, (uint64_t)pr.T, (uint64_t)pr.ld_xp * 2, 64, 64);
+      if (err != cudaSuccess) return err;
+      a.out[i] = pr.C;
+      a.ld_out[i] = r;
+      a.M[i] = (int)pr.d;
+      a.kchunks[i] = (int)ceil_div(pr.T, kChunk);
+      a.tile_begin[i + 1] = a.tile_begin[i] + (int)ceil_div(pr.d, 128);
+    }
+    a.n = m;
+    a.N = r;
+    a.n_pad = n_pad;
+    a.a_bytes = 128 * kChunk * 2;
+    a.b_bytes = (uint32_t)((n_pad + 63) / 64) * 64 * kChunk * 2;
+    a.out_mode = overwrite ? 1 : 2;
+    a.err = errw;
+    err = launch_skinny<true, true, 1>(a, stream);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace rgs

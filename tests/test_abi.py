@@ -29,7 +29,8 @@ def test_header_declares_the_path():
     names = declared_functions()
     for required in ("sketch_sample_projection", "sketch_project_inputs", "sketch_accumulate",
                      "sketch_apply_update_normsgd", "sketch_apply_update_sgd",
-                     "sketch_workspace_bytes", "sketch_status_string", "sketch_last_error"):
+                     "sketch_workspace_bytes", "sketch_read_device_errors",
+                     "sketch_status_string", "sketch_last_error"):
         assert required in names
 
 
@@ -47,7 +48,7 @@ def test_status_strings(lib):
 
 def test_workspace_sizes(lib):
     ws = binding.workspace_bytes
-    assert ws(binding.OP_UPDATE_SGD, 0, 4096, 4096, 64) == 0
+    assert ws(binding.OP_UPDATE_SGD, 0, 4096, 4096, 64) == 4 * (4096 + 4096) * 64
     a = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 64)
     b = ws(binding.OP_UPDATE_NORMSGD, 0, 8192, 4096, 64)
     c = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 128)
@@ -105,6 +106,10 @@ def test_sample_projection_argument_errors(lib):
     assert st == binding.ERR_INVALID_ARG and b"P is NULL" in lib.sketch_last_error()
     st = lib.sketch_sample_projection(1, 0, 0, 0, 63, 8, NULL, NULL, NULL, 0, NULL)
     assert st == binding.ERR_INVALID_ARG and b"k=63" in lib.sketch_last_error()
+
+
+def test_read_device_errors_needs_output(lib):
+    assert lib.sketch_read_device_errors(NULL, NULL) == binding.ERR_INVALID_ARG
 
 
 def test_binding_refuses_cpu_tensors(lib):

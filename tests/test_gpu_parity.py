@@ -39,6 +39,13 @@ def _built():
     orc.lib()
 
 
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    binding.read_device_errors()
+    yield
+    assert binding.read_device_errors() == 0, "a kernel's bounded wait timed out"
+
+
 # --------------------------------------------------------------------------
 # (a) projections
 # --------------------------------------------------------------------------
@@ -361,3 +368,78 @@ def test_calls_on_a_side_stream():
     P_or = orc.sample_qr(3, 0, 0, k, r)
     C_or = orc.accumulate(bits(D), orc.project_inputs(bits(X), P_or), np.zeros((d, r)), True)
     assert rel_fro(C.cpu().numpy(), C_or) < 2e-3
+
+
+# --------------------------------------------------------------------------
+# batched calls: one call per phase for a stack of layers
+# --------------------------------------------------------------------------
+
+STACK = [(256, 512), (128, 512), (520, 256), (64, 1024), (200, 136)]  # (d, k), ragged shapes
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_batched_stack_matches_oracle(kind):
+    """Projection, projected inputs, accumulation and both updates for a small
+    stack of differently shaped layers, each compared with the oracle."""
+    r, T, step, seed = 16, 96, 2, 11
+    layers = list(range(len(STACK)))
+    Ps = [torch.empty(k, r, dtype=torch.float32, device=DEV) for _, k in STACK]
+    rgs.sample_projection_batched(kind, seed, step, Ps, layers)
+    for li, (_, k) in enumerate(STACK):
+        ref = orc.sample_projection(kind, seed, li, step, k, r)
+        if kind == 0:
+            assert np.array_equal(Ps[li].cpu().numpy().view(np.uint32), ref.view(np.uint32))
+        else:
+            assert rel_fro(Ps[li].cpu().numpy(), ref) < 1e-5
+    Xs = [synth.normal_bf16((T, k), 1.0, 300 + li) for li, (_, k) in enumerate(STACK)]
+    Ds = [synth.normal_bf16((T, d), 1e-3, 400 + li) for li, (d, _) in enumerate(STACK)]
+    XPs = [_padded_bf16(T, r) for _ in STACK]
+    rgs.project_inputs_batched([X.to(DEV) for X in Xs], Ps, XPs)
+    Cs = [torch.full((d, r), 5.0, dtype=torch.float32, device=DEV) for d, _ in STACK]
+    rgs.accumulate_batched([D.to(DEV) for D in Ds], XPs, Cs, overwrite=True)
+    for li in layers:
+        Pn = Ps[li].cpu().numpy()
+        _xp_check(bits(XPs[li]), orc.project_inputs(bits(Xs[li]), Pn))
+        C_or = orc.accumulate(bits(Ds[li]), bits(XPs[li]), np.zeros((STACK[li][0], r)), True)
+        _c_check(Cs[li].cpu().numpy(), C_or)
+    W0 = [synth.layer_weight(d, k, li) for li, (d, k) in enumerate(STACK)]
+    Ws = [w.to(DEV) for w in W0]
+    out = [torch.zeros(1, dtype=torch.float64, device=DEV) for _ in STACK]
+    st = [torch.full((1,), -1, dtype=torch.int32, device=DEV) for _ in STACK]
+    rgs.apply_update_normsgd_batched(Ws, Cs, Ps, 1e-3, seed, layers, step, wnorm2_out=out, dev_status=st)
+    Ws2 = [w.to(DEV) for w in W0]
+    rgs.apply_update_sgd_batched(Ws2, Cs, Ps, 1e-4, seed, layers, step)
+    for li in layers:
+        Cn, Pn = Cs[li].cpu().numpy(), Ps[li].cpu().numpy()
+        W_or, s_or, _ = orc.update_normsgd(bits(W0[li]), Cn, Pn, 1e-3, seed, li, step)
+        assert s_or == 0 and int(st[li].item()) == 0
+        _w_check(bits(Ws[li]), W_or)
+        assert abs(out[li].item() - orc.norm_w(W_or) ** 2) <= 1e-6 * orc.norm_w(W_or) ** 2
+        _w_check(bits(Ws2[li]), orc.update_sgd(bits(W0[li]), Cn, Pn, 1e-4, seed, li, step))
+
+
+def test_batched_calls_span_several_launches():
+    """More layers than one launch's parameter table holds (96 GEMM problems,
+    60 update problems, 128 norm problems): every layer still matches."""
+    n, d, k, r, T = 140, 72, 64, 8, 40
+    layers = list(range(n))
+    Ps = [torch.empty(k, r, dtype=torch.float32, device=DEV) for _ in range(n)]
+    rgs.sample_projection_batched(rgs.PROJ_RADEMACHER, 3, 0, Ps, layers)
+    X = synth.normal_bf16((T, k), 1.0, 9).to(DEV)
+    D = synth.normal_bf16((T, d), 1e-3, 10).to(DEV)
+    XPs = [_padded_bf16(T, r) for _ in range(n)]
+    rgs.project_inputs_batched([X] * n, Ps, XPs)
+    Cs = [torch.empty(d, r, dtype=torch.float32, device=DEV) for _ in range(n)]
+    rgs.accumulate_batched([D] * n, XPs, Cs, overwrite=True)
+    W0 = synth.layer_weight(d, k, 0)
+    Ws = [W0.to(DEV) for _ in range(n)]
+    rgs.apply_update_normsgd_batched(Ws, Cs, Ps, 1e-3, 3, layers, 0)
+    for li in (0, 59, 60, 95, 96, 127, 128, 139):
+        Pn = Ps[li].cpu().numpy()
+        assert np.array_equal(Pn.view(np.uint32), orc.sample_rademacher(3, li, 0, k, r).view(np.uint32))
+        XP_or = orc.project_inputs(bits(X), Pn)
+        _xp_check(bits(XPs[li]), XP_or)
+        C_or = orc.accumulate(bits(D), bits(XPs[li]), np.zeros((d, r)), True)
+        _c_check(Cs[li].cpu().numpy(), C_or)
+        W_or, st, _ = orc.update_normsgd(bits(W0), Cs[li].cpu().numpy(), Pn, 1e-3, 3, li, 0)
+        _w_check(bits(Ws[li]), W_or)
