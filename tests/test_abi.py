@@ -48,7 +48,8 @@ def test_status_strings(lib):
 
 def test_workspace_sizes(lib):
     ws = binding.workspace_bytes
-    assert ws(binding.OP_UPDATE_SGD, 0, 4096, 4096, 64) == 4 * (4096 + 4096) * 64
+    # BF16 high/low parts of C and P plus their fp32 row norms
+    assert ws(binding.OP_UPDATE_SGD, 0, 4096, 4096, 64) == 4 * (4096 + 4096) * 64 + 4 * (4096 + 4096)
     a = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 64)
     b = ws(binding.OP_UPDATE_NORMSGD, 0, 8192, 4096, 64)
     c = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 128)
