@@ -169,6 +169,30 @@ SKETCH_API sketch_status sketch_apply_update_sgd(uint16_t* W, int64_t d, int64_t
                                       int32_t* dev_status, void* ws, size_t ws_bytes,
                                       void* stream);
 
+/* (d, without allocation) The normalized-SGD update of
+ * sketch_apply_update_normsgd, same arguments and results, for callers that
+ * cannot allocate device memory: a plugin handed only its input and output
+ * buffers, or a process that has given all free device memory to another pool
+ * (cudaMalloc would fail or stall the device there).  The method on the pages
+ * has no counterpart to this entry point; it changes only where the scratch
+ * lives.  The scratch is a fixed array of sketch_noalloc_scratch_bytes() (32
+ * MiB) in device memory, reserved on each device that loads the library's
+ * device code and held until the process exits.  Layers whose workspace,
+ * sketch_workspace_bytes(SKETCH_OP_UPDATE_NORMSGD, 0, d, k, r), is larger are
+ * rejected with SKETCH_ERR_WORKSPACE before anything is launched.  The first
+ * call on a device looks up the array's device address (make that first call
+ * before any stream capture).  All calls share the array: calls whose work
+ * overlaps on the GPU race, so order them on one stream.  Nothing in the array
+ * needs to start at zero. */
+SKETCH_API sketch_status sketch_apply_update_normsgd_noalloc(uint16_t* W, int64_t d, int64_t k, int64_t ld_w,
+                                                             const float* C, const float* P, int64_t r,
+                                                             float tau, uint64_t seed, uint32_t layer,
+                                                             uint32_t step, const double* wnorm2_in,
+                                                             double* wnorm2_out, int32_t* dev_status,
+                                                             void* stream);
+/* Size of the fixed scratch array of sketch_apply_update_normsgd_noalloc. */
+SKETCH_API size_t sketch_noalloc_scratch_bytes(void);
+
 /* ---- Batched forms ----------------------------------------------------------
  * One call covers many layers, one problem per layer, in a few kernel launches
  * (every layer's tiles share each launch, so small layers still fill the GPU).

@@ -38,6 +38,7 @@ EXPORTS = ("sketch_workspace_bytes", "sketch_sample_projection", "sketch_project
            "sketch_workspace_bytes_batched", "sketch_sample_projection_batched",
            "sketch_project_inputs_batched", "sketch_accumulate_batched",
            "sketch_apply_update_normsgd_batched", "sketch_apply_update_sgd_batched",
+           "sketch_apply_update_normsgd_noalloc", "sketch_noalloc_scratch_bytes",
            "sketch_read_device_errors", "sketch_status_string", "sketch_last_error")
 
 
@@ -99,6 +100,9 @@ _SIGS = {
                                                        _c.c_size_t, _vp]),
     "sketch_apply_update_sgd_batched": (_c.c_int, [_c.c_int, _vp, _i64, _c.c_float, _u64, _u32, _vp,
                                                    _c.c_size_t, _vp]),
+    "sketch_apply_update_normsgd_noalloc": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _c.c_float,
+                                                       _u64, _u32, _u32, _vp, _vp, _vp, _vp]),
+    "sketch_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "sketch_status_string": (_c.c_char_p, [_c.c_int]),
     "sketch_last_error": (_c.c_char_p, []),
 }
@@ -243,6 +247,26 @@ def apply_update_normsgd(W, C, P, tau, seed, layer, step, wnorm2_in=None, wnorm2
                                              seed & 0xFFFFFFFFFFFFFFFF, layer, step,
                                              _ptr(wnorm2_in), _ptr(wnorm2_out), _ptr(dev_status),
                                              _ptr(ws), nbytes, h))
+    return W
+
+
+def apply_update_normsgd_noalloc(W, C, P, tau, seed, layer, step, wnorm2_in=None, wnorm2_out=None,
+                                 dev_status=None, stream=None):
+    """apply_update_normsgd without a workspace: the library's fixed device
+    scratch array is used instead (for callers that cannot allocate)."""
+    ld_w = _rows(W, torch.bfloat16, "W")
+    _contig(C, torch.float32, "C")
+    _contig(P, torch.float32, "P")
+    d, k = W.shape
+    r = C.shape[1]
+    if C.shape[0] != d or P.shape != (k, r):
+        raise ValueError("shape mismatch: W %s, C %s, P %s" % (tuple(W.shape), tuple(C.shape),
+                                                               tuple(P.shape)))
+    h, _ = _stream_handle(stream, W.device)
+    _check(lib().sketch_apply_update_normsgd_noalloc(_ptr(W), d, k, ld_w, _ptr(C), _ptr(P), r,
+                                                     float(tau), seed & 0xFFFFFFFFFFFFFFFF, layer,
+                                                     step, _ptr(wnorm2_in), _ptr(wnorm2_out),
+                                                     _ptr(dev_status), h))
     return W
 
 

@@ -292,6 +292,12 @@ sketch_status do_update(bool normsgd, int n, const sketch_update_problem* probs,
 
 }  // namespace
 
+namespace rgs {
+void set_last_error(const char* message) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s", message);
+}
+}  // namespace rgs
+
 extern "C" {
 
 const char* sketch_status_string(sketch_status status) {
