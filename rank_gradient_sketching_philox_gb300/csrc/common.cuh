@@ -29,10 +29,10 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
       k0 += 0x9E3779B9u;
       k1 += 0xBB67AE85u;
     }
-    const uint32_t lo0 = 0xD2511F53u * c0;
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0);
-    const uint32_t lo1 = 0xCD9E8D57u * c2;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2);
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;  // one wide multiply gives both halves
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    const uint32_t lo0 = (uint32_t)p0, hi0 = (uint32_t)(p0 >> 32);
+    const uint32_t lo1 = (uint32_t)p1, hi1 = (uint32_t)(p1 >> 32);
     const uint32_t n0 = hi1 ^ c1 ^ k0;
     const uint32_t n2 = hi0 ^ c3 ^ k1;
     c0 = n0;
@@ -41,6 +41,43 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
     c3 = lo0;
   }
   return Philox4{c0, c1, c2, c3};
+}
+
+// Philox4x32-10 with the round keys taken from a table (rk0[i] = k0 + i*W0,
+// rk1[i] = k1 + i*W1, filled on the host): when the table lives in a kernel's
+// parameters, each round's XOR reads its key straight from the constant bank.
+__device__ __forceinline__ Philox4 philox4x32_10_rk(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                    const uint32_t* rk0, const uint32_t* rk1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ rk0[round];
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ rk1[round];
+    c1 = (uint32_t)p1;
+    c3 = (uint32_t)p0;
+    c0 = n0;
+    c2 = n2;
+  }
+  return Philox4{c0, c1, c2, c3};
+}
+
+// Round-key table of philox4x32_10_rk for a 64-bit seed.
+__host__ __device__ inline void philox_round_keys(uint64_t seed, uint32_t* rk0, uint32_t* rk1) {
+  uint32_t a = (uint32_t)(seed & 0xFFFFFFFFull), b = (uint32_t)(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    rk0[i] = a;
+    rk1[i] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+}
+
+// min of a and b that returns NaN when either is NaN (PTX min.NaN).
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
 // Block `block` of the stream (seed, layer, step, tag).

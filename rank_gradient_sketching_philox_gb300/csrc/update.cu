@@ -20,7 +20,8 @@
 namespace rgs {
 namespace {
 
-constexpr int kMaxUpd = 48;     // layers per rebuild+update launch (kernel parameter table)
+constexpr int kMaxUpd = 40;     // layers per rebuild+update launch (kernel parameter table)
+constexpr int kMaxCtas = 256;   // persistent CTAs per launch (one per SM)
 constexpr int kMaxAux = 128;    // layers per norm / split launch
 
 __device__ __forceinline__ double block_sum_double(double v, double* red) {
@@ -156,7 +157,9 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__
 struct UpdBatch {
   CUtensorMap tm_c[kMaxUpd];   // C split, d x (2 r_pad) BF16: [hi | lo]
   CUtensorMap tm_p[kMaxUpd];   // P split, k x (2 r_pad) BF16: [hi | lo]
-  CUtensorMap tm_w[kMaxUpd];   // W, d x k BF16
+  CUtensorMap tm_w[kMaxUpd];   // W, d x k BF16 (tile loads)
+  uint16_t* W[kMaxUpd];        // W for the results, stored from registers
+  int64_t ld_w[kMaxUpd];
   const float* C[kMaxUpd];     // fp32 C and P for the exact recomputation
   const float* P[kMaxUpd];
   const float* c_norm[kMaxUpd];
@@ -172,11 +175,14 @@ struct UpdBatch {
   double* unit_partials[kMaxUpd];      // ||W_new||^2 of each unit
   uint32_t* ticket[kMaxUpd];
   double* wnorm2_out[kMaxUpd];
+  int cta_unit_begin[kMaxCtas + 1];  // units of CTA b: [cta_unit_begin[b], cta_unit_begin[b + 1])
   int n;
   int unit_tiles;
-  int stages;
+  int p_stages;       // P ring depth
+  int w_stages;       // W ring depth
   float scale_val;
   uint64_t seed;
+  uint32_t rk0[10], rk1[10];  // Philox round keys of the seed
   uint32_t step;
   int r;
   int r_pad;          // r rounded up to 16 (MMA K extent)
@@ -185,19 +191,84 @@ struct UpdBatch {
   uint32_t b_bytes;   // bytes of the P_hi (or P_lo) tile: kchunks x NCOLS x 128
   uint32_t w_bytes;   // bytes of the W tile: NCOLS/64 x 16 KB
   int* err;
+  uint4* care;        // careful-element queue: cap_care entries per CTA, {p, i, j, W bits}
+  int cap_care;
+  int* care_counts;   // entries each CTA queued
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-constexpr int kEpiWarps = 16;                     // warps 4..19
+constexpr int kEpiWarps = 16;                     // warps 4..19: four per TMEM lane quarter
 constexpr int kUpdThreads = (4 + kEpiWarps) * 32;
-constexpr int kMaxStagesUpd = 4;
+constexpr int kMaxStagesUpd = 8;
 
 struct Unit {
   int p, rb, ct0, ct1;
 };
+
+// Error-free transformations (Ogita, Rump and Oishi, "Accurate Sum and Dot
+// Product", 2005): a + b = s + e and a * b = p + e exactly in fp32.  The
+// explicit _rn intrinsics keep the compiler from fusing or reordering them.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// H_ij = c_i . p_j by one thread, compensated (Dot2 of the same paper, two
+// interleaved chains merged by TwoSum): as accurate as a dot product carried in
+// twice fp32 precision and then rounded to fp32, so it is fl32 of the exact H
+// except when H lies within ~2^-40 of its size of an fp32 rounding boundary.
+// All fp32: this GPU's FP64 rate is far too low for the purpose.
+__device__ __noinline__ float exact_dot(const float* __restrict__ crow, const float* __restrict__ prow, int r) {
+  float hi0 = 0.f, lo0 = 0.f, hi1 = 0.f, lo1 = 0.f;
+  auto term = [](float c, float pv, float& hi, float& lo) {
+    const float m = __fmul_rn(c, pv);
+    float sum, err;
+    two_sum(hi, m, sum, err);
+    hi = sum;
+    lo = __fadd_rn(lo, __fadd_rn(err, __fmaf_rn(c, pv, -m)));
+  };
+  int l = 0;
+  // eight terms' loads issued together, then their two chains
+  for (; l + 8 <= r; l += 8) {
+    float cv[8], pv[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      cv[m] = crow[l + m];
+      pv[m] = prow[l + m];
+    }
+#pragma unroll
+    for (int m = 0; m < 8; m += 2) {
+      term(cv[m], pv[m], hi0, lo0);
+      term(cv[m + 1], pv[m + 1], hi1, lo1);
+    }
+  }
+  for (; l < r; ++l) term(crow[l], prow[l], hi0, lo0);
+  float hs, ht;
+  two_sum(hi0, hi1, hs, ht);
+  return __fadd_rn(hs, __fadd_rn(__fadd_rn(lo0, lo1), ht));
+}
+
+// W_new of one careful element (i, j) of problem p from its original BF16
+// bits w16: v = fmaf(-s, fl32(H_ij), w), rounded with the element's own 16
+// Philox bits.  Returns the BF16 bits.  Inlined where it is used outside the
+// main loop, called out of line inside it.
+__device__ __forceinline__ uint32_t careful_element_inl(const UpdBatch& a, int p, int i, int j, uint32_t w16) {
+  const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
+  const float h = exact_dot(a.C[p] + (int64_t)i * a.r, a.P[p] + (int64_t)j * a.r, a.r);
+  const float v = fmaf(-s, h, __uint_as_float(w16 << 16));
+  const uint32_t e = (uint32_t)i * ((uint32_t)a.k[p] >> 3) + ((uint32_t)j >> 3);  // element index / 8
+  const Philox4 rnd = philox4x32_10_rk(e, a.step, a.layer[p], kTagSR, a.rk0, a.rk1);
+  const uint32_t wsel = (j & 7) >> 1;
+  const uint32_t word = wsel == 0 ? rnd.w0 : wsel == 1 ? rnd.w1 : wsel == 2 ? rnd.w2 : rnd.w3;
+  return sr_bf16_bits(v, (j & 1) ? (word >> 16) : (word & 0xFFFFu));
+}
+__device__ __noinline__ uint32_t careful_element(const UpdBatch& a, int p, int i, int j, uint32_t w16) {
+  return careful_element_inl(a, p, i, j, w16);
+}
 
 __device__ __forceinline__ Unit decode_unit(const UpdBatch& a, int u) {
   Unit x;
@@ -216,45 +287,56 @@ __device__ __forceinline__ bool layer_skipped(const UpdBatch& a, int p) {
   return a.status_in[p] != nullptr && *a.status_in[p] != 0;
 }
 
-// Persistent rebuild + update.  Warp 0 (one lane) streams C row blocks and,
-// per column tile, P_hi/P_lo rows and the W tile into a ring of stages with
-// TMA; warp 1 (one lane) issues H = C_hi P_hi^T + C_hi P_lo^T + C_lo P_hi^T
-// (tcgen05.mma, M=128, N=NCOLS) into one of two TMEM buffers; warps 4..19 read
-// H (warp w: TMEM lanes 32(w%4).., column quarter (w-4)/4), form
-// v = fmaf(-s, H, w) and stochastically round it with 16 Philox bits per weight
-// in shared memory, then one thread stores the tile with TMA.
+// Persistent rebuild + update.  Warp 0 (one lane) streams, with TMA, the C row
+// block of each unit, the P_hi/P_lo rows of each column tile into a P ring and
+// the W tile into a deeper W ring; warp 1 (one lane) issues
+// H = C_hi P_hi^T + C_hi P_lo^T + C_lo P_hi^T (tcgen05.mma, M=128, N=NCOLS)
+// into one of two TMEM buffers and frees the P stage with tcgen05.commit;
+// warps 4..11 (two per TMEM lane quarter, one column half each) copy their W
+// values to registers and free the W stage at once, then read H from TMEM,
+// form v = fmaf(-s, H, w), round it stochastically with 16 Philox bits per
+// weight and store the results straight from registers.  Keeping the P and W
+// rings apart lets up to four W tiles per SM be in flight while the epilogue
+// works.
 //
 // Exactness where it matters: |H_tc - H| <= ||c_i|| ||p_j|| 2^-14 (three BF16
 // products leave ~3 * 2^-18 per term; the bound has >4x margin).  When that
-// could move v across more than one BF16 step (|v| < s ||c_i|| ||p_j|| 2^-5),
+// could move v across more than one BF16 step (|v| < s ||c_i|| max_j ||p_j|| 2^-5
+// with the maximum over the thread's columns of the tile),
 // the warp recomputes H_ij in double from fp32 C and P and uses fl32(H_ij),
 // which is the value the definition rounds.
 template <int NCOLS>
 __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const __grid_constant__ UpdBatch a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kMaxStagesUpd], empty_bar[kMaxStagesUpd];
+  __shared__ __align__(8) uint64_t pfull_bar[kMaxStagesUpd], pempty_bar[kMaxStagesUpd];
+  __shared__ __align__(8) uint64_t wfull_bar[kMaxStagesUpd], wempty_bar[kMaxStagesUpd];
   __shared__ __align__(8) uint64_t cfull_bar, cempty_bar, tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
-  __shared__ float warp_sq[kEpiWarps];
+  __shared__ double warp_sq[kEpiWarps];
+  __shared__ int care_count;
 
   uint8_t* smem = align1024(smem_raw);
   uint8_t* s_chi = smem;
   uint8_t* s_clo = s_chi + a.a_bytes;
-  uint8_t* s_stage0 = s_clo + a.a_bytes;
-  const uint32_t stage_bytes = 2 * a.b_bytes + a.w_bytes;
+  uint8_t* s_p0 = s_clo + a.a_bytes;                        // P ring: NSP x (hi, lo)
+  uint8_t* s_w0 = s_p0 + (size_t)a.p_stages * 2 * a.b_bytes;  // W ring: NSW x W tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NS = a.stages;
-  const int units = a.unit_begin[a.n];
-  const int u_begin = (int)((int64_t)units * blockIdx.x / gridDim.x);
-  const int u_end = (int)((int64_t)units * (blockIdx.x + 1) / gridDim.x);
+  const int NSP = a.p_stages, NSW = a.w_stages;
+  const int u_begin = a.cta_unit_begin[blockIdx.x];
+  const int u_end = a.cta_unit_begin[blockIdx.x + 1];
   constexpr uint32_t kTmemCols = 2 * NCOLS;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < NS; ++s) {
-      tc::mbar_init(&full_bar[s], 1);
-      tc::mbar_init(&empty_bar[s], 2);
+    care_count = 0;
+    for (int s = 0; s < NSP; ++s) {
+      tc::mbar_init(&pfull_bar[s], 1);
+      tc::mbar_init(&pempty_bar[s], 1);           // MMA commit
+    }
+    for (int s = 0; s < NSW; ++s) {
+      tc::mbar_init(&wfull_bar[s], 1);
+      tc::mbar_init(&wempty_bar[s], kEpiWarps);   // every epilogue warp
     }
     tc::mbar_init(&cfull_bar, 1);
     tc::mbar_init(&cempty_bar, 1);
@@ -273,7 +355,8 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
   if (warp == 0 && lane == 0) {
     // ---------------- producer ----------------
     int it = 0, cl = 0, prev_p = -1, prev_rb = -1;
-    for (int u = u_begin; u < u_end && !abort_flag; ++u) {
+    bool stop = false;
+    for (int u = u_begin; u < u_end && !stop; ++u) {
       const Unit x = decode_unit(a, u);
       if (layer_skipped(a, x.p)) continue;
       const int i0 = x.rb * 128;
@@ -289,26 +372,37 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         prev_rb = x.rb;
       }
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
-        const int s = it % NS;
-        if (it >= NS && !tc::mbar_wait(&empty_bar[s], ((it / NS) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))
-          break;
-        uint8_t* st = s_stage0 + (size_t)s * stage_bytes;
         const int j0 = ct * NCOLS;
-        tc::mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-        for (int c = 0; c < a.kchunks; ++c) {
-          tc::tma_load_2d(st + c * NCOLS * 128, &a.tm_p[x.p], &full_bar[s], c * 64, j0);
-          tc::tma_load_2d(st + a.b_bytes + c * NCOLS * 128, &a.tm_p[x.p], &full_bar[s], a.r_pad + c * 64, j0);
+        // W tile first: it comes from HBM and is waited on longest
+        const int sw = it % NSW;
+        if (it >= NSW && !tc::mbar_wait(&wempty_bar[sw], ((it / NSW) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+          stop = true;
+          break;
         }
+        uint8_t* wst = s_w0 + (size_t)sw * a.w_bytes;
+        tc::mbar_arrive_expect_tx(&wfull_bar[sw], a.w_bytes);
 #pragma unroll
         for (int bx = 0; bx < NCOLS / 64; ++bx)
-          tc::tma_load_2d(st + 2 * a.b_bytes + bx * 16384, &a.tm_w[x.p], &full_bar[s], j0 + 64 * bx, i0);
+          tc::tma_load_2d(wst + bx * 16384, &a.tm_w[x.p], &wfull_bar[sw], j0 + 64 * bx, i0);
+        const int sp = it % NSP;
+        if (it >= NSP && !tc::mbar_wait(&pempty_bar[sp], ((it / NSP) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+          stop = true;
+          break;
+        }
+        uint8_t* pst = s_p0 + (size_t)sp * 2 * a.b_bytes;
+        tc::mbar_arrive_expect_tx(&pfull_bar[sp], 2 * a.b_bytes);
+        for (int c = 0; c < a.kchunks; ++c) {
+          tc::tma_load_2d(pst + c * NCOLS * 128, &a.tm_p[x.p], &pfull_bar[sp], c * 64, j0);
+          tc::tma_load_2d(pst + a.b_bytes + c * NCOLS * 128, &a.tm_p[x.p], &pfull_bar[sp], a.r_pad + c * 64, j0);
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     const uint32_t idesc = tc::idesc_bf16(128, NCOLS, false, false);
     int it = 0, cl = 0, prev_p = -1, prev_rb = -1;
-    for (int u = u_begin; u < u_end && !abort_flag; ++u) {
+    bool stop = false;
+    for (int u = u_begin; u < u_end && !stop; ++u) {
       const Unit x = decode_unit(a, u);
       if (layer_skipped(a, x.p)) continue;
       if (x.p != prev_p || x.rb != prev_rb) {
@@ -318,12 +412,14 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         prev_rb = x.rb;
       }
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
-        const int s = it % NS, b = it & 1;
-        if (!tc::mbar_wait(&full_bar[s], (it / NS) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) break;
-        if (it >= 2 && !tc::mbar_wait(&tempty_bar[b], ((it >> 1) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))
+        const int sp = it % NSP, b = it & 1;
+        if (!tc::mbar_wait(&pfull_bar[sp], (it / NSP) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad) ||
+            (it >= 2 && !tc::mbar_wait(&tempty_bar[b], ((it >> 1) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))) {
+          stop = true;
           break;
+        }
         tc::tc_fence_after();
-        const uint32_t st = tc::smem_u32(s_stage0 + (size_t)s * stage_bytes);
+        const uint32_t pst = tc::smem_u32(s_p0 + (size_t)sp * 2 * a.b_bytes);
         const uint32_t d_tmem = tmem + (uint32_t)(b * NCOLS);
         uint32_t acc = 0;
         for (int c = 0; c < a.kchunks; ++c) {
@@ -331,15 +427,15 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
             const uint32_t off_a = c * 16384 + kk * 32, off_b = c * NCOLS * 128 + kk * 32;
             const uint64_t ahi = tc::sdesc_sw128(tc::smem_u32(s_chi) + off_a, 16, 1024);
             const uint64_t alo = tc::sdesc_sw128(tc::smem_u32(s_clo) + off_a, 16, 1024);
-            const uint64_t bhi = tc::sdesc_sw128(st + off_b, 16, 1024);
-            const uint64_t blo = tc::sdesc_sw128(st + a.b_bytes + off_b, 16, 1024);
+            const uint64_t bhi = tc::sdesc_sw128(pst + off_b, 16, 1024);
+            const uint64_t blo = tc::sdesc_sw128(pst + a.b_bytes + off_b, 16, 1024);
             tc::mma_bf16(d_tmem, ahi, bhi, idesc, acc);
             tc::mma_bf16(d_tmem, ahi, blo, idesc, 1u);
             tc::mma_bf16(d_tmem, alo, bhi, idesc, 1u);
             acc = 1u;
           }
         }
-        tc::mma_commit(&empty_bar[s]);
+        tc::mma_commit(&pempty_bar[sp]);
         tc::mma_commit(&tfull_bar[b]);
       }
       // release the C row block once its last unit is issued
@@ -348,16 +444,16 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         const Unit y = decode_unit(a, u + 1);
         last_of_c = (y.p != x.p || y.rb != x.rb);
       }
-      if (last_of_c) tc::mma_commit(&cempty_bar);
+      if (last_of_c && !stop) tc::mma_commit(&cempty_bar);
     }
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------
     const int ew = warp - 4;
     const int quarter = warp & 3;
     constexpr int kCols = NCOLS / 4;           // columns per thread per tile
+    constexpr int kPass = 16;                  // columns per pass: two 8-column groups
     const int col_base = (ew >> 2) * kCols;    // column quarter of the tile
     const int q = quarter * 32 + lane;         // tile row = TMEM lane
-    const uint32_t key0 = (uint32_t)(a.seed & 0xFFFFFFFFull), key1 = (uint32_t)(a.seed >> 32);
     const bool storer = (ew == 0 && lane == 0);
     int it = 0;
     // Every epilogue warp runs the same loop and reaches every named barrier;
@@ -366,128 +462,180 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       const Unit x = decode_unit(a, u);
       const int p = x.p;
       if (layer_skipped(a, p)) continue;
-      const int64_t d = a.d[p], k = a.k[p];
-      const int64_t i = (int64_t)x.rb * 128 + q;
+      // d, k < 2^31 and d*k/8 < 2^32 (checked on the host): 32-bit indices
+      const int d = (int)a.d[p], k = (int)a.k[p];
+      const int i = x.rb * 128 + q;
+      const uint32_t k8 = (uint32_t)k >> 3;
       const bool row_ok = i < d;
       const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
       const float thr_row = row_ok ? fabsf(s) * a.c_norm[p][i] * 0x1p-5f : 0.f;
       const uint32_t layer = a.layer[p];
-      const float* __restrict__ Cp = a.C[p];
-      const float* __restrict__ Pp = a.P[p];
       const bool need_norm = a.wnorm2_out[p] != nullptr;
-      float sq = 0.f;
+      uint16_t* wrow = a.W[p] + (int64_t)(row_ok ? i : 0) * a.ld_w[p];
+      float sq = 0.f, sq_comp = 0.f;  // Kahan-compensated sum of squares
+
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
-        const int st_idx = it % NS, b = it & 1;
-        bool live = tc::mbar_wait(&tfull_bar[b], (it >> 1) & 1, &abort_flag, a.err, tc::kErrTimeoutMma) &&
-                    tc::mbar_wait(&full_bar[st_idx], (it / NS) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad);
+        const int sw = it % NSW, b = it & 1;
+        const int j0 = ct * NCOLS;
+        // largest norm of the P rows of this thread's columns (for the exactness
+        // test), loaded before the waits so that its latency hides behind them
+        float pmax = 0.f;
+        {
+          const float* pnorm = a.p_norm[p];
+          const int jc = j0 + col_base + 2 * (lane % (kCols / 2));
+          if (jc + 1 < k) {
+            const float2 pn = *reinterpret_cast<const float2*>(pnorm + jc);
+            pmax = fmaxf(pn.x, pn.y);
+          } else if (jc < k) {
+            pmax = pnorm[jc];
+          }
+        }
+        // W tile and H of this tile
+        bool live = tc::mbar_wait(&wfull_bar[sw], (it / NSW) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad) &&
+                    tc::mbar_wait(&tfull_bar[b], (it >> 1) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
         live = __all_sync(0xFFFFFFFFu, live);
         tc::tc_fence_after();
-        uint32_t h[kCols];
-        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col_base);
-        if (live) {
-          if constexpr (kCols == 32) tc::tmem_ld_32x32b_x32(taddr, h);
-          else tc::tmem_ld_32x32b_x16(taddr, h);
-          tc::tmem_wait_ld();
-        }
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&tempty_bar[b]);
-        uint8_t* s_w = s_stage0 + (size_t)st_idx * stage_bytes + 2 * a.b_bytes;
-        const int64_t j0 = (int64_t)ct * NCOLS;
+        const uint8_t* s_w = s_w0 + (size_t)sw * a.w_bytes;
+        for (int o = 16; o > 0; o >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
+        const float thr = thr_row * pmax;
+#pragma unroll 1
+        for (int half = 0; half < kCols / kPass; ++half) {
+          const int col32 = col_base + half * kPass;
+          uint32_t win[2][4];
 #pragma unroll
-        for (int g = 0; g < kCols / 8; ++g) {
-          const int col = col_base + 8 * g;
-          const int64_t j = j0 + col;
-          const bool ok = live && row_ok && j < k;
-          uint4* wp = reinterpret_cast<uint4*>(s_w + (col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
-          const uint4 raw = *wp;
-          const uint32_t win[4] = {raw.x, raw.y, raw.z, raw.w};
-          float wv[8], v[8];
-          uint32_t out[8], rnd16[8];
-          uint32_t flags = 0;
-          if (ok) {
-            const uint64_t e = (uint64_t)i * (uint64_t)k + (uint64_t)j;  // multiple of 8
-            const Philox4 rnd = philox4x32_10((uint32_t)(e >> 3), a.step, layer, kTagSR, key0, key1);
-            const uint32_t rw[4] = {rnd.w0, rnd.w1, rnd.w2, rnd.w3};
-            const float4 pn0 = *reinterpret_cast<const float4*>(a.p_norm[p] + j);
-            const float4 pn1 = *reinterpret_cast<const float4*>(a.p_norm[p] + j + 4);
-            const float pn[8] = {pn0.x, pn0.y, pn0.z, pn0.w, pn1.x, pn1.y, pn1.z, pn1.w};
+          for (int g = 0; g < 2; ++g) {
+            const int col = col32 + 8 * g;
+            const uint4 raw = *reinterpret_cast<const uint4*>(
+                s_w + (col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
+            win[g][0] = raw.x;
+            win[g][1] = raw.y;
+            win[g][2] = raw.z;
+            win[g][3] = raw.w;
+          }
+          uint32_t h[16];
+          if (live) {
+            tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col32), h);
+            tc::tmem_wait_ld();
+          }
+          // two 8-column groups; their Philox blocks are independent chains
+          uint32_t rw[2][4];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              wv[t] = bf16_bits_to_float((t & 1) ? (win[t >> 1] >> 16) : (win[t >> 1] & 0xFFFFu));
-              rnd16[t] = (t & 1) ? (rw[t >> 1] >> 16) : (rw[t >> 1] & 0xFFFFu);
-              v[t] = fmaf(-s, __uint_as_float(h[8 * g + t]), wv[t]);
-              out[t] = sr_bf16_bits(v[t], rnd16[t]);
-              if (fabsf(v[t]) < thr_row * pn[t]) flags |= 1u << t;
+          for (int g = 0; g < 2; ++g) {
+            // Philox block of element index e = i*k + j (j a multiple of 8): e / 8
+            const uint32_t blk = (uint32_t)i * k8 + ((uint32_t)(j0 + col32 + 8 * g) >> 3);
+            const Philox4 rnd = philox4x32_10_rk(blk, a.step, layer, kTagSR, a.rk0, a.rk1);
+            rw[g][0] = rnd.w0;
+            rw[g][1] = rnd.w1;
+            rw[g][2] = rnd.w2;
+            rw[g][3] = rnd.w3;
+          }
+          // v = fmaf(-s, H, w) and stochastic rounding: add 16 random bits below
+          // the BF16 mantissa and keep the upper halves (one PRMT per pair).  A
+          // group that holds a NaN or a value small enough for the exactness
+          // test is flagged for the careful path below.
+          uint32_t wout[2][4];
+          uint32_t careful = 0;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            float gmin = __int_as_float(0x7F800000);
+#pragma unroll
+            for (int t2 = 0; t2 < 4; ++t2) {
+              const uint32_t wword = win[g][t2], rword = rw[g][t2];
+              const float v0 = fmaf(-s, __uint_as_float(h[8 * g + 2 * t2]), __uint_as_float(wword << 16));
+              const float v1 = fmaf(-s, __uint_as_float(h[8 * g + 2 * t2 + 1]), __uint_as_float(wword & 0xFFFF0000u));
+              const uint32_t s0 = __float_as_uint(v0) + (rword & 0xFFFFu);
+              const uint32_t s1 = __float_as_uint(v1) + (rword >> 16);
+              wout[g][t2] = __byte_perm(s0, s1, 0x7632);
+              gmin = fmin_nan(gmin, fmin_nan(fabsf(v0), fabsf(v1)));  // NaN if any v is NaN
+            }
+            const bool ok = live && row_ok && j0 + col32 + 8 * g < k;
+            if (ok && !(gmin >= thr)) careful |= 1u << g;  // small value or NaN
+          }
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            if (!(live && row_ok && j0 + col32 + 8 * g < k)) continue;
+            *reinterpret_cast<uint4*>(wrow + j0 + col32 + 8 * g) =
+                make_uint4(wout[g][0], wout[g][1], wout[g][2], wout[g][3]);
+            if (need_norm) {
+              float gs = 0.f;
+#pragma unroll
+              for (int t2 = 0; t2 < 4; ++t2) {
+                const float lo = __uint_as_float(wout[g][t2] << 16), hi = __uint_as_float(wout[g][t2] & 0xFFFF0000u);
+                gs = fmaf(lo, lo, gs);
+                gs = fmaf(hi, hi, gs);
+              }
+              const float y = gs - sq_comp;
+              const float tsum = sq + y;
+              sq_comp = (tsum - sq) - y;
+              sq = tsum;
             }
           }
-          // exact recomputation of flagged elements, one warp-wide dot product each
-          uint32_t pending = __ballot_sync(0xFFFFFFFFu, flags != 0);
-          while (pending) {
-            const int src = __ffs(pending) - 1;
-            pending &= pending - 1;
-            uint32_t fl = __shfl_sync(0xFFFFFFFFu, flags, src);
-            const int64_t isrc = (int64_t)x.rb * 128 + quarter * 32 + src;
-            while (fl) {
-              const int t = __ffs(fl) - 1;
-              fl &= fl - 1;
-              const float* crow = Cp + isrc * a.r;
-              const float* prow = Pp + (j + t) * a.r;
-              double dot = 0.0;
-              for (int l = lane; l < a.r; l += 32) dot = fma((double)crow[l], (double)prow[l], dot);
-              for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-              if (lane == src) {
+          // Careful path (rare, warp-uniform): in a flagged group, each element
+          // whose |v| is below the threshold (or NaN) is queued as {p, i, j, W
+          // bits} and redone exactly at the end of the kernel, after everything
+          // stored here; a full queue has the warp do it at once.  The norm sum
+          // above keeps the tensor-core value of such an element (below the
+          // threshold: far too small to matter), except that a NaN makes it NaN.
+          const uint32_t flagged = __ballot_sync(0xFFFFFFFFu, careful != 0);
+          if (flagged) {
+            uint32_t h2[16];
+            if (live) {
+              tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col32), h2);
+              tc::tmem_wait_ld();
+            }
+            uint32_t over = 0;  // elements (bit 8g+t) that did not fit in the queue
+            if (careful) {
 #pragma unroll
-                for (int tt = 0; tt < 8; ++tt) {
-                  if (tt == t) {
-                    v[tt] = fmaf(-s, (float)dot, wv[tt]);
-                    out[tt] = sr_bf16_bits(v[tt], rnd16[tt]);
-                  }
+              for (int g = 0; g < 2; ++g) {
+                if (!((careful >> g) & 1u)) continue;
+                const int col = col32 + 8 * g;
+                const uint4 raw = *reinterpret_cast<const uint4*>(
+                    s_w + (col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
+                const uint32_t wws[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                  const uint32_t w16 = (wws[t >> 1] >> (16 * (t & 1))) & 0xFFFFu;
+                  const float v = fmaf(-s, __uint_as_float(h2[8 * g + t]), __uint_as_float(w16 << 16));
+                  if (fabsf(v) >= thr) continue;
+                  if (v != v && need_norm) sq = __int_as_float(0x7FC00000);
+                  const int slot = atomicAdd(&care_count, 1);
+                  if (slot < a.cap_care)
+                    a.care[(size_t)blockIdx.x * a.cap_care + slot] = make_uint4((uint32_t)p, (uint32_t)i, (uint32_t)(j0 + col + t), w16);
+                  else
+                    over |= 1u << (8 * g + t);
                 }
               }
             }
-          }
-          if (ok) {
-            uint32_t wout[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) wout[t] = out[2 * t] | (out[2 * t + 1] << 16);
-            *wp = make_uint4(wout[0], wout[1], wout[2], wout[3]);
-            if (need_norm) {
-#pragma unroll
-              for (int t = 0; t < 8; ++t) {
-                const float nv = bf16_bits_to_float(out[t]);
-                sq = fmaf(nv, nv, sq);
-              }
+            while (over) {  // queue full: this thread redoes its elements now
+              const int bit = __ffs(over) - 1;
+              over &= over - 1;
+              const int col = col32 + bit;
+              const uint4 raw = *reinterpret_cast<const uint4*>(
+                  s_w + (col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
+              const uint32_t wsel = (bit & 7) >> 1;
+              const uint32_t word = wsel == 0 ? raw.x : wsel == 1 ? raw.y : wsel == 2 ? raw.z : raw.w;
+              const uint32_t w16 = (word >> (16 * (bit & 1))) & 0xFFFFu;
+              wrow[j0 + col] = (uint16_t)careful_element(a, p, i, j0 + col, w16);
             }
           }
-        }
-        tc::fence_proxy_async_smem();
-        tc::named_barrier(1, kEpiWarps * 32);
-        if (storer && live) {
-          const int i0 = x.rb * 128;
-#pragma unroll
-          for (int bx = 0; bx < NCOLS / 64; ++bx)
-            tc::tma_store_2d(&a.tm_w[p], s_w + bx * 16384, (int)j0 + 64 * bx, i0);
-          tc::bulk_commit();
-          if (NS >= 2) {
-            if (it > 0) {
-              tc::bulk_wait_read<1>();
-              tc::mbar_arrive(&empty_bar[(it - 1) % NS]);
-            }
-          } else {
-            tc::bulk_wait_read<0>();
-            tc::mbar_arrive(&empty_bar[st_idx]);
+          if (half == kCols / kPass - 1) {  // this warp is done with the TMEM buffer
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&tempty_bar[b]);
           }
         }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&wempty_bar[sw]);
       }
       if (need_norm) {
         // ||W_new||^2 of this unit, then the layer's last unit sums all units in order
-        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-        if (lane == 0) warp_sq[ew] = sq;
+        double dsq = (double)sq - (double)sq_comp;
+        for (int o = 16; o > 0; o >>= 1) dsq += __shfl_xor_sync(0xFFFFFFFFu, dsq, o);
+        if (lane == 0) warp_sq[ew] = dsq;
         tc::named_barrier(1, kEpiWarps * 32);
         if (storer) {
           double tot = 0.0;
-          for (int w = 0; w < kEpiWarps; ++w) tot += (double)warp_sq[w];
+          for (int w = 0; w < kEpiWarps; ++w) tot += warp_sq[w];
           const int lu = u - a.unit_begin[p];
           a.unit_partials[p][lu] = tot;
           __threadfence();
@@ -503,10 +651,6 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         tc::named_barrier(1, kEpiWarps * 32);  // warp_sq reusable
       }
     }
-    if (storer) {
-      tc::bulk_wait_all();
-      if (NS >= 2 && it > 0) tc::mbar_arrive(&empty_bar[(it - 1) % NS]);
-    }
   }
   // SGD: every layer's status word reads 0 (written by the first CTA)
   if (blockIdx.x == 0) {
@@ -516,6 +660,22 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+  // the number of careful elements this CTA queued, for the fixup kernel
+  if (threadIdx.x == 0) a.care_counts[blockIdx.x] = min(care_count, a.cap_care);
+}
+
+// The careful elements each CTA of the update kernel queued, one per thread;
+// launched right after it on the same stream, so every store of the update
+// is ordered before these.  (Kept out of the update kernel: the code would
+// cost the main loop registers.)
+__global__ void __launch_bounds__(256) care_fixup_kernel(const __grid_constant__ UpdBatch a) {
+  const int nq = a.care_counts[blockIdx.x];
+  const uint4* cq = a.care + (size_t)blockIdx.x * a.cap_care;
+  for (int e = threadIdx.x; e < nq; e += blockDim.x) {
+    const uint4 en = cq[e];
+    const int p = (int)en.x, i = (int)en.y, j = (int)en.z;
+    a.W[p][(int64_t)i * a.ld_w[p] + j] = (uint16_t)careful_element_inl(a, p, i, j, en.w);
+  }
 }
 
 int round16(int r) { return (r + 15) / 16 * 16; }
@@ -534,6 +694,7 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   static thread_local UpdBatch a;
   a.scale_val = scale_val;
   a.seed = seed;
+  philox_round_keys(seed, a.rk0, a.rk1);
   a.step = step;
   a.r = r;
   a.r_pad = r_pad;
@@ -542,14 +703,21 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   a.b_bytes = (uint32_t)a.kchunks * NCOLS * 128u;
   a.w_bytes = (uint32_t)(NCOLS / 64) * 16384u;
   a.err = errw;
-  const size_t max_smem = 227 * 1024;
+  // dynamic shared memory: what the opt-in limit leaves next to the static arrays
+  cudaFuncAttributes fa;
+  err = cudaFuncGetAttributes(&fa, update_persistent_kernel<NCOLS>);
+  if (err != cudaSuccess) return err;
+  const size_t max_smem = 227 * 1024 - fa.sharedSizeBytes;
   const size_t fixed = 2 * (size_t)a.a_bytes + 1024;
-  const size_t stage = 2 * (size_t)a.b_bytes + a.w_bytes;
-  int stages = (int)((max_smem - fixed) / stage);
-  if (stages > kMaxStagesUpd) stages = kMaxStagesUpd;
-  if (stages < 1) return cudaErrorInvalidConfiguration;
-  a.stages = stages;
-  const size_t smem = fixed + (size_t)stages * stage;
+  const size_t p_stage = 2 * (size_t)a.b_bytes;
+  // two P stages when they fit next to at least two W stages, else one
+  int p_stages = (fixed + 2 * p_stage + 2 * a.w_bytes <= max_smem) ? 2 : 1;
+  int w_stages = (int)((max_smem - fixed - p_stages * p_stage) / a.w_bytes);
+  if (w_stages > kMaxStagesUpd) w_stages = kMaxStagesUpd;
+  if (w_stages < 1) return cudaErrorInvalidConfiguration;
+  a.p_stages = p_stages;
+  a.w_stages = w_stages;
+  const size_t smem = fixed + p_stages * p_stage + (size_t)w_stages * a.w_bytes;
   err = cudaFuncSetAttribute(update_persistent_kernel<NCOLS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
   if (err != cudaSuccess) return err;
@@ -560,9 +728,9 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
     int64_t total_tiles = 0;
     for (int i = 0; i < m; ++i)
       total_tiles += ceil_div(probs[base + i].d, 128) * ceil_div(probs[base + i].k, NCOLS);
-    // about four units per CTA for balance, at least four tiles per unit to
-    // amortize the C row block
-    int64_t ut = total_tiles / (4 * (int64_t)nsm);
+    // about twelve units per CTA, at least four tiles per unit so the C row
+    // block is reused; CTAs then get contiguous unit ranges of equal tile count
+    int64_t ut = total_tiles / (12 * (int64_t)nsm);
     if (ut < 4) ut = 4;
     if (ut > 64) ut = 64;
     a.unit_tiles = (int)ut;
@@ -576,6 +744,8 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       if (err == cudaSuccess)
         err = make_tmap_bf16_2d(&a.tm_w[i], pr.W, (uint64_t)pr.k, (uint64_t)pr.d, (uint64_t)pr.ld_w * 2, 64, 128);
       if (err != cudaSuccess) return err;
+      a.W[i] = pr.W;
+      a.ld_w[i] = pr.ld_w;
       a.C[i] = pr.C;
       a.P[i] = pr.P;
       a.c_norm[i] = w.c_norm;
@@ -594,8 +764,42 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       a.wnorm2_out[i] = normsgd ? pr.wnorm2_out : nullptr;
     }
     const int units = a.unit_begin[m];
-    const int grid = units < nsm ? units : nsm;
+    int grid = units < nsm ? units : nsm;
+    if (grid > kMaxCtas) grid = kMaxCtas;
+    {
+      // split the units into `grid` contiguous ranges of about equal tile count
+      int64_t tile_total = 0;
+      for (int i = 0; i < m; ++i) tile_total += (int64_t)a.n_ct[i] * ceil_div(probs[base + i].d, 128);
+      int cta = 0;
+      int64_t acc = 0;
+      a.cta_unit_begin[0] = 0;
+      int u = 0;
+      for (int i = 0; i < m; ++i) {
+        const int nrb = (int)ceil_div(probs[base + i].d, 128);
+        for (int rb = 0; rb < nrb; ++rb) {
+          for (int cu = 0; cu < a.n_cu[i]; ++cu, ++u) {
+            const int t0 = cu * a.unit_tiles;
+            const int t1 = (t0 + a.unit_tiles < a.n_ct[i]) ? t0 + a.unit_tiles : a.n_ct[i];
+            acc += t1 - t0;
+            // close CTA ranges whose share of tiles is reached
+            while (cta + 1 < grid && acc * grid >= tile_total * (cta + 1)) a.cta_unit_begin[++cta] = u + 1;
+          }
+        }
+      }
+      while (cta + 1 <= grid) a.cta_unit_begin[++cta] = units;
+    }
+    {
+      // the chunk's careful-element queues are contiguous; an equal share per CTA
+      int64_t entries = 0;
+      for (int i = 0; i < m; ++i) entries += ws[base + i].care_entries;
+      // the first 64 entries (1 KB) hold the per-CTA counts
+      a.care_counts = reinterpret_cast<int*>(ws[base].care);
+      a.care = ws[base].care + 64;
+      const int64_t per_cta = (entries - 64) / grid;
+      a.cap_care = per_cta > (int64_t)(1 << 30) ? (1 << 30) : (int)per_cta;
+    }
     update_persistent_kernel<NCOLS><<<grid, kUpdThreads, smem, stream>>>(a);
+    care_fixup_kernel<<<grid, 256, 0, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
@@ -638,6 +842,13 @@ cudaError_t launch_update(int n, const UpdateProblem* probs, const UpdateWorkspa
 }
 
 }  // namespace
+
+int64_t care_queue_entries(int64_t d, int64_t k) {
+  // one entry per 1024 weights (a few times what trained-scale weights use),
+  // at least 1024 and whole 256-byte blocks
+  const int64_t e = (d * k + 1023) / 1024;
+  return ((e < 1024 ? 1024 : e) + 15) / 16 * 16;
+}
 
 size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool normsgd, UpdateWorkspace* ws) {
   const size_t start = cur.offset;
