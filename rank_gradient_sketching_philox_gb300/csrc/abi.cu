@@ -99,8 +99,7 @@ size_t qr_ws_bytes(int64_t k, int64_t r) {
 
 size_t update_ws_bytes(bool normsgd, int64_t d, int64_t k, int64_t r) {
   rgs::WsCursor cur;
-  return rgs::carve_update_workspace(cur, d, k, (int)r, normsgd, nullptr) +
-         (size_t)rgs::care_queue_entries(d, k) * sizeof(uint4);
+  return rgs::carve_update_workspace(cur, d, k, (int)r, normsgd, nullptr);
 }
 
 size_t op_ws_bytes(sketch_op op, int64_t T, int64_t d, int64_t k, int64_t r) {
@@ -285,14 +284,6 @@ sketch_status do_update(bool normsgd, int n, const sketch_update_problem* probs,
     v[i] = rgs::UpdateProblem{p.W, p.d, p.k, p.ld_w, p.C, p.P, p.layer,
                               normsgd ? p.wnorm2_in : nullptr, normsgd ? p.wnorm2_out : nullptr, p.dev_status};
     rgs::carve_update_workspace(cur, p.d, p.k, (int)r, normsgd, &w[i]);
-  }
-  int64_t entries = 0;
-  for (int i = 0; i < n; ++i) entries += rgs::care_queue_entries(probs[i].d, probs[i].k);
-  uint4* queue = cur.take<uint4>((size_t)entries);
-  for (int i = 0; i < n; ++i) {
-    w[i].care = queue;
-    w[i].care_entries = rgs::care_queue_entries(probs[i].d, probs[i].k);
-    queue += w[i].care_entries;
   }
   cudaError_t err = normsgd ? rgs::launch_update_normsgd(n, v.data(), w.data(), (int)r, step_size, seed, step, s)
                             : rgs::launch_update_sgd(n, v.data(), w.data(), (int)r, step_size, seed, step, s);

@@ -135,15 +135,13 @@ struct UpdateWorkspace {
   double* wnew_partials;   // one per update block
   uint16_t* c_split;       // d x 2 r_pad BF16: [high | low] part of C
   uint16_t* p_split;       // k x 2 r_pad BF16: [high | low] part of P
-  uint4* care;             // careful-element queue; the queues of a batch are contiguous
-  int64_t care_entries;    // its entries (care_queue_entries(d, k))
+  uint32_t* flags;         // careful-group flag bitmap (flag_words(d, k, r) words)
 };
 constexpr int kWnormBlocks = 1024;
-// Entries of a layer's careful-element queue (16 bytes each; a multiple of 16).
-int64_t care_queue_entries(int64_t d, int64_t k);
-// Carves one layer's workspace at the cursor, without its careful-element
-// queue (the caller carves the batch's queues in one block after all layers);
-// returns its size (a multiple of 256).
+// 32-bit words of a layer's careful-group flag bitmap (one bit per 8 weights of
+// the padded tile grid).
+int64_t flag_words(int64_t d, int64_t k, int r);
+// Carves one layer's workspace at the cursor; returns its size (a multiple of 256).
 size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool normsgd, UpdateWorkspace* ws);
 
 cudaError_t launch_update_normsgd(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, float tau,

@@ -191,9 +191,11 @@ struct UpdBatch {
   uint32_t b_bytes;   // bytes of the P_hi (or P_lo) tile: kchunks x NCOLS x 128
   uint32_t w_bytes;   // bytes of the W tile: NCOLS/64 x 16 KB
   int* err;
-  uint4* care;        // careful-element queue: cap_care entries per CTA, {p, i, j, W bits}
-  int cap_care;
-  int* care_counts;   // entries each CTA queued
+  // careful-group flags, one bit per 8-weight group: per tile (rb, ct), word
+  // ew * (NCOLS/32) + g holds bit `lane` for row rb*128 + (ew&3)*32 + lane,
+  // columns ct*NCOLS + (ew>>2)*(NCOLS/4) + 8g..+7 (ew = epilogue warp)
+  uint32_t* flags[kMaxUpd];
+  int64_t flag_word_begin[kMaxUpd + 1];  // prefix over the batch (fixup kernel)
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -215,59 +217,6 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   s = __fadd_rn(a, b);
   const float bb = __fsub_rn(s, a);
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-
-// H_ij = c_i . p_j by one thread, compensated (Dot2 of the same paper, two
-// interleaved chains merged by TwoSum): as accurate as a dot product carried in
-// twice fp32 precision and then rounded to fp32, so it is fl32 of the exact H
-// except when H lies within ~2^-40 of its size of an fp32 rounding boundary.
-// All fp32: this GPU's FP64 rate is far too low for the purpose.
-__device__ __noinline__ float exact_dot(const float* __restrict__ crow, const float* __restrict__ prow, int r) {
-  float hi0 = 0.f, lo0 = 0.f, hi1 = 0.f, lo1 = 0.f;
-  auto term = [](float c, float pv, float& hi, float& lo) {
-    const float m = __fmul_rn(c, pv);
-    float sum, err;
-    two_sum(hi, m, sum, err);
-    hi = sum;
-    lo = __fadd_rn(lo, __fadd_rn(err, __fmaf_rn(c, pv, -m)));
-  };
-  int l = 0;
-  // eight terms' loads issued together, then their two chains
-  for (; l + 8 <= r; l += 8) {
-    float cv[8], pv[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      cv[m] = crow[l + m];
-      pv[m] = prow[l + m];
-    }
-#pragma unroll
-    for (int m = 0; m < 8; m += 2) {
-      term(cv[m], pv[m], hi0, lo0);
-      term(cv[m + 1], pv[m + 1], hi1, lo1);
-    }
-  }
-  for (; l < r; ++l) term(crow[l], prow[l], hi0, lo0);
-  float hs, ht;
-  two_sum(hi0, hi1, hs, ht);
-  return __fadd_rn(hs, __fadd_rn(__fadd_rn(lo0, lo1), ht));
-}
-
-// W_new of one careful element (i, j) of problem p from its original BF16
-// bits w16: v = fmaf(-s, fl32(H_ij), w), rounded with the element's own 16
-// Philox bits.  Returns the BF16 bits.  Inlined where it is used outside the
-// main loop, called out of line inside it.
-__device__ __forceinline__ uint32_t careful_element_inl(const UpdBatch& a, int p, int i, int j, uint32_t w16) {
-  const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
-  const float h = exact_dot(a.C[p] + (int64_t)i * a.r, a.P[p] + (int64_t)j * a.r, a.r);
-  const float v = fmaf(-s, h, __uint_as_float(w16 << 16));
-  const uint32_t e = (uint32_t)i * ((uint32_t)a.k[p] >> 3) + ((uint32_t)j >> 3);  // element index / 8
-  const Philox4 rnd = philox4x32_10_rk(e, a.step, a.layer[p], kTagSR, a.rk0, a.rk1);
-  const uint32_t wsel = (j & 7) >> 1;
-  const uint32_t word = wsel == 0 ? rnd.w0 : wsel == 1 ? rnd.w1 : wsel == 2 ? rnd.w2 : rnd.w3;
-  return sr_bf16_bits(v, (j & 1) ? (word >> 16) : (word & 0xFFFFu));
-}
-__device__ __noinline__ uint32_t careful_element(const UpdBatch& a, int p, int i, int j, uint32_t w16) {
-  return careful_element_inl(a, p, i, j, w16);
 }
 
 __device__ __forceinline__ Unit decode_unit(const UpdBatch& a, int u) {
@@ -309,12 +258,11 @@ template <int NCOLS>
 __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const __grid_constant__ UpdBatch a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t pfull_bar[kMaxStagesUpd], pempty_bar[kMaxStagesUpd];
-  __shared__ __align__(8) uint64_t wfull_bar[kMaxStagesUpd], wempty_bar[kMaxStagesUpd];
+  __shared__ __align__(8) uint64_t wfull_bar[kMaxStagesUpd], wempty_bar[kMaxStagesUpd], sfull_bar[kMaxStagesUpd];
   __shared__ __align__(8) uint64_t cfull_bar, cempty_bar, tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ double warp_sq[kEpiWarps];
-  __shared__ int care_count;
 
   uint8_t* smem = align1024(smem_raw);
   uint8_t* s_chi = smem;
@@ -329,14 +277,14 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    care_count = 0;
     for (int s = 0; s < NSP; ++s) {
       tc::mbar_init(&pfull_bar[s], 1);
       tc::mbar_init(&pempty_bar[s], 1);           // MMA commit
     }
     for (int s = 0; s < NSW; ++s) {
       tc::mbar_init(&wfull_bar[s], 1);
-      tc::mbar_init(&wempty_bar[s], kEpiWarps);   // every epilogue warp
+      tc::mbar_init(&sfull_bar[s], kEpiWarps);    // every epilogue warp: results in the stage
+      tc::mbar_init(&wempty_bar[s], 1);           // store warp: the stage's TMA store has read it
     }
     tc::mbar_init(&cfull_bar, 1);
     tc::mbar_init(&cempty_bar, 1);
@@ -446,12 +394,41 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       }
       if (last_of_c && !stop) tc::mma_commit(&cempty_bar);
     }
+  } else if (warp == 2 && lane == 0) {
+    // ---------------- store warp ----------------
+    // Writes each finished tile from its W stage to W with TMA, then frees
+    // the stage once the copy has read it.
+    int it = 0;
+    bool stop = false;
+    for (int u = u_begin; u < u_end && !stop; ++u) {
+      const Unit x = decode_unit(a, u);
+      if (layer_skipped(a, x.p)) continue;
+      for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
+        const int sw = it % NSW;
+        if (!tc::mbar_wait(&sfull_bar[sw], (it / NSW) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+          stop = true;
+          break;
+        }
+        uint8_t* wst = s_w0 + (size_t)sw * a.w_bytes;
+        if (!abort_flag) {  // after a timed-out wait the stage may hold anything
+#pragma unroll
+          for (int bx = 0; bx < NCOLS / 64; ++bx)
+            tc::tma_store_2d(&a.tm_w[x.p], wst + bx * 16384, ct * NCOLS + 64 * bx, x.rb * 128);
+          tc::bulk_commit();
+          tc::bulk_wait_read<0>();
+        }
+        tc::mbar_arrive(&wempty_bar[sw]);
+      }
+    }
+    tc::bulk_wait_all();  // the writes are done before the CTA exits
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------
     const int ew = warp - 4;
     const int quarter = warp & 3;
     constexpr int kCols = NCOLS / 4;           // columns per thread per tile
-    constexpr int kPass = 16;                  // columns per pass: two 8-column groups
+    constexpr int kPass = kCols < 32 ? kCols : 32;  // columns per pass
+    constexpr int kGroups = kPass / 8;              // 8-column groups (Philox blocks) per pass
+    constexpr int kGroupsPerWarp = kCols / 8;       // flag words of a warp per tile
     const int col_base = (ew >> 2) * kCols;    // column quarter of the tile
     const int q = quarter * 32 + lane;         // tile row = TMEM lane
     const bool storer = (ew == 0 && lane == 0);
@@ -495,32 +472,21 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
                     tc::mbar_wait(&tfull_bar[b], (it >> 1) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
         live = __all_sync(0xFFFFFFFFu, live);
         tc::tc_fence_after();
-        const uint8_t* s_w = s_w0 + (size_t)sw * a.w_bytes;
+        uint8_t* s_w = s_w0 + (size_t)sw * a.w_bytes;
         for (int o = 16; o > 0; o >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
         const float thr = thr_row * pmax;
 #pragma unroll 1
         for (int half = 0; half < kCols / kPass; ++half) {
           const int col32 = col_base + half * kPass;
-          uint32_t win[2][4];
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            const int col = col32 + 8 * g;
-            const uint4 raw = *reinterpret_cast<const uint4*>(
-                s_w + (col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
-            win[g][0] = raw.x;
-            win[g][1] = raw.y;
-            win[g][2] = raw.z;
-            win[g][3] = raw.w;
-          }
+          // H of the pass from TMEM, 16 columns at a time; the first load
+          // completes while the Philox blocks of the pass (independent chains)
+          // are computed
+          const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col32);
           uint32_t h[16];
-          if (live) {
-            tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col32), h);
-            tc::tmem_wait_ld();
-          }
-          // two 8-column groups; their Philox blocks are independent chains
-          uint32_t rw[2][4];
+          if (live) tc::tmem_ld_32x32b<16>(taddr, h);
+          uint32_t rw[kGroups][4];
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
+          for (int g = 0; g < kGroups; ++g) {
             // Philox block of element index e = i*k + j (j a multiple of 8): e / 8
             const uint32_t blk = (uint32_t)i * k8 + ((uint32_t)(j0 + col32 + 8 * g) >> 3);
             const Philox4 rnd = philox4x32_10_rk(blk, a.step, layer, kTagSR, a.rk0, a.rk1);
@@ -529,38 +495,65 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
             rw[g][2] = rnd.w2;
             rw[g][3] = rnd.w3;
           }
-          // v = fmaf(-s, H, w) and stochastic rounding: add 16 random bits below
-          // the BF16 mantissa and keep the upper halves (one PRMT per pair).  A
-          // group that holds a NaN or a value small enough for the exactness
-          // test is flagged for the careful path below.
-          uint32_t wout[2][4];
-          uint32_t careful = 0;
+          if (live) tc::tmem_wait_ld_regs<16>(h);
+          // Per 8-column group: v = fmaf(-s, H, w) and stochastic rounding (add
+          // 16 random bits below the BF16 mantissa, keep the upper halves: one
+          // PRMT per pair); the results go back into the W stage in place (the
+          // store warp writes the tile out with TMA, clipping rows and columns
+          // outside W).  A group that holds a NaN or a value small enough for
+          // the exactness test is flagged for the careful path.
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
+          for (int g = 0; g < kGroups; ++g) {
+            if (g == 2 && live) {  // next 16 columns of H
+              tc::tmem_ld_32x32b<16>(taddr + 16, h);
+              tc::tmem_wait_ld_regs<16>(h);
+            }
+            const int col = col32 + 8 * g;
+            uint8_t* sp = s_w + (col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4);
+            const uint4 raw = *reinterpret_cast<const uint4*>(sp);
+            const uint32_t win[4] = {raw.x, raw.y, raw.z, raw.w};
+            const uint32_t* rwg = rw[g];
+            uint32_t wout[4];
             float gmin = __int_as_float(0x7F800000);
 #pragma unroll
             for (int t2 = 0; t2 < 4; ++t2) {
-              const uint32_t wword = win[g][t2], rword = rw[g][t2];
-              const float v0 = fmaf(-s, __uint_as_float(h[8 * g + 2 * t2]), __uint_as_float(wword << 16));
-              const float v1 = fmaf(-s, __uint_as_float(h[8 * g + 2 * t2 + 1]), __uint_as_float(wword & 0xFFFF0000u));
+              const uint32_t wword = win[t2], rword = rwg[t2];
+              const float v0 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2]), __uint_as_float(wword << 16));
+              const float v1 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2 + 1]), __uint_as_float(wword & 0xFFFF0000u));
               const uint32_t s0 = __float_as_uint(v0) + (rword & 0xFFFFu);
               const uint32_t s1 = __float_as_uint(v1) + (rword >> 16);
-              wout[g][t2] = __byte_perm(s0, s1, 0x7632);
+              wout[t2] = __byte_perm(s0, s1, 0x7632);
               gmin = fmin_nan(gmin, fmin_nan(fabsf(v0), fabsf(v1)));  // NaN if any v is NaN
             }
-            const bool ok = live && row_ok && j0 + col32 + 8 * g < k;
-            if (ok && !(gmin >= thr)) careful |= 1u << g;  // small value or NaN
-          }
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            if (!(live && row_ok && j0 + col32 + 8 * g < k)) continue;
-            *reinterpret_cast<uint4*>(wrow + j0 + col32 + 8 * g) =
-                make_uint4(wout[g][0], wout[g][1], wout[g][2], wout[g][3]);
-            if (need_norm) {
+            const bool ok = live && row_ok && j0 + col < k;
+            const bool flag = ok && !(gmin >= thr);  // small value or NaN
+            // Careful path (rare, warp-uniform): each element of a flagged group
+            // whose |v| is below the threshold (or NaN) is queued as {p, i, j, W
+            // bits} and redone exactly by the fixup kernel after this kernel's
+            // stores; when the CTA's queue is full the thread does it at once.
+            // The norm sum keeps the tensor-core value of a queued element
+            // (below the threshold: far too small to matter), except that a NaN
+            // makes it NaN.
+            // Careful path: a flagged group keeps its original W here and is
+            // marked in the flag bitmap (the word of the whole warp, written on
+            // every call); the fixup kernel redoes its 8 elements exactly from
+            // the original W after this kernel's stores.  The norm sum keeps the
+            // tensor-core values of the group (they differ from the exact ones
+            // by at most one BF16 step, or are below the threshold), except that
+            // a NaN makes it NaN.
+            const uint32_t fword = __ballot_sync(0xFFFFFFFFu, flag);
+            if (lane == 0)  // every word of the layer is written on every call
+              a.flags[p][((size_t)x.rb * a.n_ct[p] + ct) * (16 * kGroupsPerWarp) + ew * kGroupsPerWarp +
+                         half * kGroups + g] = fword;
+            if (flag) {
+              if (need_norm && gmin != gmin) sq = __int_as_float(0x7FC00000);
+            }
+            if (live) *reinterpret_cast<uint4*>(sp) = flag ? raw : make_uint4(wout[0], wout[1], wout[2], wout[3]);
+            if (need_norm && ok) {
               float gs = 0.f;
 #pragma unroll
               for (int t2 = 0; t2 < 4; ++t2) {
-                const float lo = __uint_as_float(wout[g][t2] << 16), hi = __uint_as_float(wout[g][t2] & 0xFFFF0000u);
+                const float lo = __uint_as_float(wout[t2] << 16), hi = __uint_as_float(wout[t2] & 0xFFFF0000u);
                 gs = fmaf(lo, lo, gs);
                 gs = fmaf(hi, hi, gs);
               }
@@ -570,62 +563,17 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
               sq = tsum;
             }
           }
-          // Careful path (rare, warp-uniform): in a flagged group, each element
-          // whose |v| is below the threshold (or NaN) is queued as {p, i, j, W
-          // bits} and redone exactly at the end of the kernel, after everything
-          // stored here; a full queue has the warp do it at once.  The norm sum
-          // above keeps the tensor-core value of such an element (below the
-          // threshold: far too small to matter), except that a NaN makes it NaN.
-          const uint32_t flagged = __ballot_sync(0xFFFFFFFFu, careful != 0);
-          if (flagged) {
-            uint32_t h2[16];
-            if (live) {
-              tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col32), h2);
-              tc::tmem_wait_ld();
-            }
-            uint32_t over = 0;  // elements (bit 8g+t) that did not fit in the queue
-            if (careful) {
-#pragma unroll
-              for (int g = 0; g < 2; ++g) {
-                if (!((careful >> g) & 1u)) continue;
-                const int col = col32 + 8 * g;
-                const uint4 raw = *reinterpret_cast<const uint4*>(
-                    s_w + (col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
-                const uint32_t wws[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                  const uint32_t w16 = (wws[t >> 1] >> (16 * (t & 1))) & 0xFFFFu;
-                  const float v = fmaf(-s, __uint_as_float(h2[8 * g + t]), __uint_as_float(w16 << 16));
-                  if (fabsf(v) >= thr) continue;
-                  if (v != v && need_norm) sq = __int_as_float(0x7FC00000);
-                  const int slot = atomicAdd(&care_count, 1);
-                  if (slot < a.cap_care)
-                    a.care[(size_t)blockIdx.x * a.cap_care + slot] = make_uint4((uint32_t)p, (uint32_t)i, (uint32_t)(j0 + col + t), w16);
-                  else
-                    over |= 1u << (8 * g + t);
-                }
-              }
-            }
-            while (over) {  // queue full: this thread redoes its elements now
-              const int bit = __ffs(over) - 1;
-              over &= over - 1;
-              const int col = col32 + bit;
-              const uint4 raw = *reinterpret_cast<const uint4*>(
-                  s_w + (col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
-              const uint32_t wsel = (bit & 7) >> 1;
-              const uint32_t word = wsel == 0 ? raw.x : wsel == 1 ? raw.y : wsel == 2 ? raw.z : raw.w;
-              const uint32_t w16 = (word >> (16 * (bit & 1))) & 0xFFFFu;
-              wrow[j0 + col] = (uint16_t)careful_element(a, p, i, j0 + col, w16);
-            }
-          }
           if (half == kCols / kPass - 1) {  // this warp is done with the TMEM buffer
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&tempty_bar[b]);
           }
         }
+        // this warp's results are in the stage: make them visible to the TMA
+        // engine and tell the store warp
+        tc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&wempty_bar[sw]);
+        if (lane == 0) tc::mbar_arrive(&sfull_bar[sw]);
       }
       if (need_norm) {
         // ||W_new||^2 of this unit, then the layer's last unit sums all units in order
@@ -660,21 +608,116 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
-  // the number of careful elements this CTA queued, for the fixup kernel
-  if (threadIdx.x == 0) a.care_counts[blockIdx.x] = min(care_count, a.cap_care);
 }
 
-// The careful elements each CTA of the update kernel queued, one per thread;
-// launched right after it on the same stream, so every store of the update
-// is ordered before these.  (Kept out of the update kernel: the code would
-// cost the main loop registers.)
-__global__ void __launch_bounds__(256) care_fixup_kernel(const __grid_constant__ UpdBatch a) {
-  const int nq = a.care_counts[blockIdx.x];
-  const uint4* cq = a.care + (size_t)blockIdx.x * a.cap_care;
-  for (int e = threadIdx.x; e < nq; e += blockDim.x) {
-    const uint4 en = cq[e];
-    const int p = (int)en.x, i = (int)en.y, j = (int)en.z;
-    a.W[p][(int64_t)i * a.ld_w[p] + j] = (uint16_t)careful_element_inl(a, p, i, j, en.w);
+// One careful group, warp-wide: W_new of the 8 elements (i, j..j+7) of
+// problem p from their original W, with H_i,j+t computed by the compensated
+// dot product (Dot2 of the same paper; lanes 4t..4t+3 take column t, every
+// fourth term each, merged by TwoSum), v = fmaf(-s, fl32(H), w) and the
+// group's Philox block.  The dot product is as accurate as one carried in
+// twice fp32 precision and then rounded, so it is fl32 of the exact H except
+// when H lies within ~2^-40 of its size of an fp32 rounding boundary.  All
+// fp32: this GPU's FP64 rate is far too low for the purpose.
+__device__ __forceinline__ void careful_group_warp(const UpdBatch& a, int p, int i, int j) {
+  const int lane = threadIdx.x & 31, t = lane >> 2, q = lane & 3;
+  const int r = a.r;
+  const float* crow = a.C[p] + (int64_t)i * r;
+  const float* prow = a.P[p] + (int64_t)(j + t) * r;
+  uint16_t* wp = a.W[p] + (int64_t)i * a.ld_w[p] + j + t;
+  const uint32_t w16 = *wp;  // the original: the update kernel left the group alone
+  float hi = 0.f, lo = 0.f;
+  auto term = [&](float c, float pv) {
+    const float m = __fmul_rn(c, pv);
+    float sum, err;
+    two_sum(hi, m, sum, err);
+    hi = sum;
+    lo = __fadd_rn(lo, __fadd_rn(err, __fmaf_rn(c, pv, -m)));
+  };
+  // the terms l = q, q+4, ... of this lane, sixteen loads of C and P at a
+  // time issued together (one round trip per 64 terms of the row)
+  int l = q;
+  for (; l + 60 < r; l += 64) {
+    float cv[16], pv[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      cv[m] = crow[l + 4 * m];
+      pv[m] = prow[l + 4 * m];
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) term(cv[m], pv[m]);
+  }
+  if (l < r) {
+    float cv[16], pv[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const bool in = l + 4 * m < r;
+      cv[m] = in ? crow[l + 4 * m] : 0.f;
+      pv[m] = in ? prow[l + 4 * m] : 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) term(cv[m], pv[m]);  // zero terms change nothing
+  }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, o), olo = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+    float sum, err;
+    two_sum(hi, ohi, sum, err);
+    hi = sum;
+    lo = __fadd_rn(lo, __fadd_rn(olo, err));
+  }
+  const float h = __fadd_rn(hi, lo);
+  const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
+  const uint32_t blk = (uint32_t)i * ((uint32_t)a.k[p] >> 3) + ((uint32_t)j >> 3);  // element index / 8
+  const Philox4 rnd = philox4x32_10_rk(blk, a.step, a.layer[p], kTagSR, a.rk0, a.rk1);
+  const uint32_t word = (t >> 1) == 0 ? rnd.w0 : (t >> 1) == 1 ? rnd.w1 : (t >> 1) == 2 ? rnd.w2 : rnd.w3;
+  const float v = fmaf(-s, h, __uint_as_float(w16 << 16));
+  const uint32_t o = sr_bf16_bits(v, (t & 1) ? (word >> 16) : (word & 0xFFFFu));
+  __syncwarp();
+  if (q == 0) *wp = (uint16_t)o;
+}
+
+// The careful groups the update kernel flagged.  Each warp scans 32 flag words
+// at a time (one per lane) and does every group whose bit is set, warp-wide;
+// launched right after the update kernel on the same stream, so every store
+// of the update is ordered before these.  Kept out of the update kernel: the
+// code would cost the main loop registers.
+template <int NCOLS>
+__global__ void __launch_bounds__(512) care_fixup_kernel(const __grid_constant__ UpdBatch a) {
+  constexpr int kGroupsPerWarp = NCOLS / 32, kWordsPerTile = 16 * kGroupsPerWarp;
+  const int lane = threadIdx.x & 31;
+  const int64_t total = a.flag_word_begin[a.n];
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  int p = 0;  // each lane's problem; its words only move forward
+  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32; base < total;
+       base += warps * 32) {
+    const int64_t w = base + lane;
+    uint32_t bits = 0;
+    if (w < total) {
+      while (p + 1 < a.n && a.flag_word_begin[p + 1] <= w) ++p;
+      if (!layer_skipped(a, p)) bits = a.flags[p][w - a.flag_word_begin[p]];
+    }
+    uint32_t pending = __ballot_sync(0xFFFFFFFFu, bits != 0u);
+    while (pending) {
+      const int src = __ffs(pending) - 1;
+      pending &= pending - 1;
+      const int ps = __shfl_sync(0xFFFFFFFFu, p, src);
+      uint32_t b = __shfl_sync(0xFFFFFFFFu, bits, src);
+      // a layer has fewer than 2^29 flag words (d*k < 2^35): 32-bit from here
+      const uint32_t lw = (uint32_t)(base + src - a.flag_word_begin[ps]);
+      const uint32_t tile = lw / kWordsPerTile, wt = lw % kWordsPerTile;
+      const int ew = (int)(wt / kGroupsPerWarp), gw = (int)(wt % kGroupsPerWarp);
+      const uint32_t nct = (uint32_t)a.n_ct[ps];
+      const int rb = (int)(tile / nct), ct = (int)(tile % nct);
+      const int j = ct * NCOLS + (ew >> 2) * (NCOLS / 4) + 8 * gw;
+      if (j + 8 > a.k[ps]) continue;  // never flagged (a guard against a corrupted bitmap)
+      while (b) {
+        const int row = __ffs(b) - 1;
+        b &= b - 1;
+        const int i = rb * 128 + (ew & 3) * 32 + row;
+        if (i >= a.d[ps]) break;  // never flagged, as above
+        careful_group_warp(a, ps, i, j);
+      }
+    }
   }
 }
 
@@ -734,6 +777,7 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
     if (ut < 4) ut = 4;
     if (ut > 64) ut = 64;
     a.unit_tiles = (int)ut;
+    a.flag_word_begin[0] = 0;
     a.unit_begin[0] = 0;
     for (int i = 0; i < m; ++i) {
       const UpdateProblem& pr = probs[base + i];
@@ -760,6 +804,8 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       a.status_in[i] = normsgd ? (pr.dev_status ? pr.dev_status : w.status) : nullptr;
       a.status_out[i] = normsgd ? nullptr : pr.dev_status;
       a.unit_partials[i] = w.wnew_partials;
+      a.flags[i] = w.flags;
+      a.flag_word_begin[i + 1] = a.flag_word_begin[i] + flag_words(pr.d, pr.k, r);
       a.ticket[i] = w.ticket;
       a.wnorm2_out[i] = normsgd ? pr.wnorm2_out : nullptr;
     }
@@ -788,18 +834,8 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       }
       while (cta + 1 <= grid) a.cta_unit_begin[++cta] = units;
     }
-    {
-      // the chunk's careful-element queues are contiguous; an equal share per CTA
-      int64_t entries = 0;
-      for (int i = 0; i < m; ++i) entries += ws[base + i].care_entries;
-      // the first 64 entries (1 KB) hold the per-CTA counts
-      a.care_counts = reinterpret_cast<int*>(ws[base].care);
-      a.care = ws[base].care + 64;
-      const int64_t per_cta = (entries - 64) / grid;
-      a.cap_care = per_cta > (int64_t)(1 << 30) ? (1 << 30) : (int)per_cta;
-    }
     update_persistent_kernel<NCOLS><<<grid, kUpdThreads, smem, stream>>>(a);
-    care_fixup_kernel<<<grid, 256, 0, stream>>>(a);
+    care_fixup_kernel<NCOLS><<<2 * nsm, 512, 0, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
@@ -843,11 +879,9 @@ cudaError_t launch_update(int n, const UpdateProblem* probs, const UpdateWorkspa
 
 }  // namespace
 
-int64_t care_queue_entries(int64_t d, int64_t k) {
-  // one entry per 1024 weights (a few times what trained-scale weights use),
-  // at least 1024 and whole 256-byte blocks
-  const int64_t e = (d * k + 1023) / 1024;
-  return ((e < 1024 ? 1024 : e) + 15) / 16 * 16;
+int64_t flag_words(int64_t d, int64_t k, int r) {
+  const int ncols = update_ncols(r);
+  return ceil_div(d, 128) * ceil_div(k, ncols) * (16 * ncols / 32);
 }
 
 size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool normsgd, UpdateWorkspace* ws) {
@@ -869,6 +903,7 @@ size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool n
   w.p_norm = cur.take<float>((size_t)k);
   w.c_split = cur.take<uint16_t>((size_t)d * 2 * r_pad);
   w.p_split = cur.take<uint16_t>((size_t)k * 2 * r_pad);
+  w.flags = cur.take<uint32_t>((size_t)flag_words(d, k, r));
   cur.take<char>(0);  // end on a 256-byte boundary
   if (ws) *ws = w;
   return cur.offset - start;

@@ -48,11 +48,10 @@ def test_status_strings(lib):
 
 def test_workspace_sizes(lib):
     ws = binding.workspace_bytes
-    # BF16 high/low parts of C and P, their fp32 row norms, and a queue of
-    # 16-byte careful-element entries, one per 1024 weights
+    # BF16 high/low parts of C and P, their fp32 row norms, and the careful-group
+    # flag bitmap (one bit per 8 weights)
     assert ws(binding.OP_UPDATE_SGD, 0, 4096, 4096, 64) == (4 * (4096 + 4096) * 64 + 4 * (4096 + 4096)
-                                                           + 16 * 4096 * 4096 // 1024)
-    assert ws(binding.OP_UPDATE_SGD, 0, 8, 8, 1) >= 16 * 1024       # the queue's minimum
+                                                           + 4096 * 4096 // 64)
     a = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 64)
     b = ws(binding.OP_UPDATE_NORMSGD, 0, 8192, 4096, 64)
     c = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 128)
