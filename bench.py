@@ -342,10 +342,12 @@ def main():
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
+        launches0 = rgs.kernel_launches()
         ev[0].record(stream)
         for s in range(args.warmup, args.warmup + args.steps):
             step(s)
         ev[1].record(stream)
+        launches = rgs.kernel_launches() - launches0
         torch.cuda.synchronize()
     elapsed = ev[0].elapsed_time(ev[1]) / 1e3
     if world > 1:
@@ -357,20 +359,24 @@ def main():
     value = wl.tokens_per_step * args.steps * world / elapsed
 
     # ---- per-phase timings (each phase alone, same buffers) ---------------
-    def timed(fn):
+    phase_launches = {}
+
+    def timed(fn, name):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        l0 = rgs.kernel_launches()
         a.record(stream)
         fn()
         b.record(stream)
+        phase_launches[name] = rgs.kernel_launches() - l0
         torch.cuda.synchronize()
         return a.elapsed_time(b) / 1e3
 
     s_next = args.warmup + args.steps
-    t_sample = timed(lambda: sample_phase(s_next))
-    t_project = timed(lambda: [project_phase(m) for m in range(nmb)])
-    t_accum = timed(lambda: [accumulate_phase(m) for m in range(nmb)])
-    t_update = timed(lambda: update_phase(s_next, True))
+    t_sample = timed(lambda: sample_phase(s_next), "sample")
+    t_project = timed(lambda: [project_phase(m) for m in range(nmb)], "project")
+    t_accum = timed(lambda: [accumulate_phase(m) for m in range(nmb)], "accumulate")
+    t_update = timed(lambda: update_phase(s_next, True), "update")
     nst = int((status != 0).sum().item())
 
     # algorithmic bytes: the minimum each call must move
@@ -382,13 +388,15 @@ def main():
     def gbs(bytes_, secs):
         return bytes_ / secs / 1e9
 
-    # kernel launches of each phase (from the batched launch plan)
+    # launches of each phase, counted by the library; the dominant kernel of a
+    # phase is its skinny GEMM (projection, accumulation) or the persistent
+    # rebuild+update kernel (one per 40 layers)
     ceil = lambda a, b: -(-a // b)
-    n_sample = (1 + 2 * 4) * ceil(L, 256) if kind == rgs.PROJ_GAUSSIAN_QR else ceil(L, 256)
-    n_proj = nmb * ceil(L, 96)          # skinny GEMM launches (plus one P split each)
-    n_acc = nmb * ceil(L, 96)
-    n_upd = ceil(L, 60)                 # rebuild+update launches
-    n_upd_aux = 4 * ceil(L, 128)        # Gram partial + reduce, finalize, split
+    n_sample = phase_launches["sample"]
+    n_proj = phase_launches["project"] // 2   # skinny GEMM launches (each with one P split)
+    n_acc = phase_launches["accumulate"]
+    n_upd = ceil(L, 40)
+    n_upd_aux = phase_launches["update"] - n_upd
     components = {
         "sample_projection": {"ms_per_step": t_sample * 1e3, "launches": n_sample},
         "project_inputs": {"ms_per_step": t_project * 1e3, "tokens_per_s": wl.tokens_per_step / t_project,
@@ -458,8 +466,6 @@ def main():
         e2e = {"value": wl.tokens_per_step * e2e_steps * world / e2e_elapsed, "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
-    # this library's kernel launches per step, from the launch plan of each batched call
-    per_step = n_sample + 2 * n_proj + n_acc + n_upd + n_upd_aux
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res = oracle_sample(wl, r)
@@ -485,7 +491,7 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": per_step * args.steps,
+            "gpu_launches": launches,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)

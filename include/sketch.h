@@ -264,6 +264,11 @@ SKETCH_API sketch_status sketch_apply_update_sgd_batched(int n, const sketch_upd
 #define SKETCH_DEVERR_TIMEOUT_STAGE 4  /* a pipeline stage was never released */
 SKETCH_API sketch_status sketch_read_device_errors(int32_t* flags, void* stream);
 
+/* Number of kernels this library has launched in this process (every device
+ * and thread), counted on the host as each launch is issued.  Instrumentation
+ * for benchmarks and tests; the pages have no counterpart.  Never fails. */
+SKETCH_API uint64_t sketch_kernel_launches(void);
+
 /* Static string for a status code. */
 SKETCH_API const char* sketch_status_string(sketch_status status);
 

@@ -39,7 +39,8 @@ EXPORTS = ("sketch_workspace_bytes", "sketch_sample_projection", "sketch_project
            "sketch_project_inputs_batched", "sketch_accumulate_batched",
            "sketch_apply_update_normsgd_batched", "sketch_apply_update_sgd_batched",
            "sketch_apply_update_normsgd_noalloc", "sketch_noalloc_scratch_bytes",
-           "sketch_read_device_errors", "sketch_status_string", "sketch_last_error")
+           "sketch_read_device_errors", "sketch_kernel_launches", "sketch_status_string",
+           "sketch_last_error")
 
 
 class ProjectionProblem(ctypes.Structure):
@@ -91,6 +92,7 @@ _SIGS = {
     "sketch_apply_update_sgd": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _c.c_float, _u64,
                                            _u32, _u32, _vp, _vp, _c.c_size_t, _vp]),
     "sketch_read_device_errors": (_c.c_int, [_c.POINTER(_c.c_int32), _vp]),
+    "sketch_kernel_launches": (_c.c_uint64, []),
     "sketch_workspace_bytes_batched": (ctypes.c_size_t, [_c.c_int, _c.c_int, _vp, _vp, _vp, _i64]),
     "sketch_sample_projection_batched": (_c.c_int, [_c.c_int, _u64, _u32, _c.c_int, _vp, _i64, _vp, _vp,
                                                     _c.c_size_t, _vp]),
@@ -175,6 +177,11 @@ def read_device_errors(stream=None, device=None):
     flags = ctypes.c_int32(0)
     _check(lib().sketch_read_device_errors(ctypes.byref(flags), h))
     return int(flags.value)
+
+
+def kernel_launches():
+    """Kernels this library has launched in this process (counted on the host)."""
+    return int(lib().sketch_kernel_launches())
 
 
 def workspace_bytes(op, T=0, d=0, k=0, r=1):

@@ -390,6 +390,8 @@ sketch_status sketch_apply_update_sgd_batched(int n, const sketch_update_problem
   return do_update(false, n, problems, r, alpha_eta, seed, step, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
+uint64_t sketch_kernel_launches(void) { return rgs::launches_issued(); }
+
 sketch_status sketch_read_device_errors(int32_t* flags, void* stream) {
   if (flags == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "flags is NULL");
   int* word = nullptr;

@@ -76,8 +76,10 @@ __global__ void gram_reduce_kernel(const GramBatch batch) {
 cudaError_t launch_gram(const GramBatch& batch, cudaStream_t stream) {
   if (batch.n <= 0) return cudaSuccess;
   const int tiles = (int)ceil_div(batch.r, kTile);
+  count_launch();
   gram_partial_kernel<<<dim3(64, tiles * tiles, batch.n), 256, 0, stream>>>(batch);
   const int rr = batch.r * batch.r;
+  count_launch();
   gram_reduce_kernel<<<dim3((unsigned)ceil_div(rr, 256), batch.n), 256, 0, stream>>>(batch);
   return cudaGetLastError();
 }

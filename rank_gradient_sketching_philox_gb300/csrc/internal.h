@@ -31,6 +31,9 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner
 // Device address of the current device's error word (bits from tc.cuh).
 cudaError_t device_error_word(int** out);
 int num_sms();
+// Counts one kernel launch issued by this library (sketch_kernel_launches).
+void count_launch();
+uint64_t launches_issued();
 // Message returned by sketch_last_error() on this thread.
 void set_last_error(const char* message);
 

@@ -169,6 +169,7 @@ void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
 
 cudaError_t launch_rademacher(const ProjBatch& batch, int64_t max_k, cudaStream_t stream) {
   const int64_t words = ceil_div(max_k * batch.r, 32);
+  count_launch();
   rademacher_kernel<<<dim3((unsigned)ceil_div(words, 256), batch.n), 256, 0, stream>>>(batch);
   return cudaGetLastError();
 }
@@ -176,6 +177,7 @@ cudaError_t launch_rademacher(const ProjBatch& batch, int64_t max_k, cudaStream_
 cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream_t stream) {
   const int r = batch.r;
   const int64_t blocks4 = ceil_div(max_k * r, 4);
+  count_launch();
   gaussian_kernel<<<dim3((unsigned)ceil_div(blocks4, 256), batch.n), 256, 0, stream>>>(batch);
   GramBatch gb;
   gb.n = batch.n;
@@ -197,7 +199,9 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
   for (int pass = 0; pass < 2; ++pass) {
     err = launch_gram(gb, stream);
     if (err != cudaSuccess) return err;
+    count_launch();
     chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch);
+    count_launch();
     tri_apply_kernel<<<dim3((unsigned)ceil_div(max_k, 32), batch.n), 256, apply_smem, stream>>>(
         batch, pass == 1);
   }

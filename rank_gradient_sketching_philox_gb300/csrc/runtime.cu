@@ -4,6 +4,7 @@
 // cached device properties.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -111,6 +112,13 @@ cudaError_t device_error_word(int** out) {
   *out = g_error_ptr[dev];
   return cudaSuccess;
 }
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+uint64_t launches_issued() { return g_launches.load(std::memory_order_relaxed); }
 
 int num_sms() {
   int dev = 0;

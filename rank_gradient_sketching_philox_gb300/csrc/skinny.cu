@@ -322,6 +322,7 @@ cudaError_t launch_skinny(SkinnyBatch& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
@@ -368,6 +369,7 @@ cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, voi
     }
     sp.r = r;
     sp.n_pad = n_pad;
+    count_launch();
     split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 32), (unsigned)ceil_div(n_pad, 32), (unsigned)m), 256, 0,
                              stream>>>(sp);
     a.n = m;

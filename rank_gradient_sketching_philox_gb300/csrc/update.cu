@@ -834,7 +834,9 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       }
       while (cta + 1 <= grid) a.cta_unit_begin[++cta] = units;
     }
+    count_launch();
     update_persistent_kernel<NCOLS><<<grid, kUpdThreads, smem, stream>>>(a);
+    count_launch();
     care_fixup_kernel<NCOLS><<<2 * nsm, 512, 0, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
@@ -863,6 +865,7 @@ cudaError_t launch_split(int n, const UpdateProblem* probs, const UpdateWorkspac
       max_rows = pr.d > max_rows ? pr.d : max_rows;
       max_rows = pr.k > max_rows ? pr.k : max_rows;
     }
+    count_launch();
     split_rows_kernel<<<dim3((unsigned)ceil_div(max_rows, 8), (unsigned)(2 * m)), 256, 0, stream>>>(sb);
   }
   return cudaGetLastError();
@@ -928,7 +931,10 @@ cudaError_t launch_update_normsgd(int n, const UpdateProblem* probs, const Updat
       wb.partials[nw] = ws[base + i].wnorm_partials;
       ++nw;
     }
-    if (nw > 0) wnorm_partial_kernel<<<dim3(kWnormBlocks, nw), 256, 0, stream>>>(wb);
+    if (nw > 0) {
+      count_launch();
+      wnorm_partial_kernel<<<dim3(kWnormBlocks, nw), 256, 0, stream>>>(wb);
+    }
     gb.n = 2 * m;
     gb.r = r;
     for (int i = 0; i < m; ++i) {
@@ -949,6 +955,7 @@ cudaError_t launch_update_normsgd(int n, const UpdateProblem* probs, const Updat
     if (err != cudaSuccess) return err;
     fb.rr = r * r;
     fb.tau = tau;
+    count_launch();
     normsgd_finalize_kernel<<<m, 256, 0, stream>>>(fb);
   }
   return launch_update(n, probs, ws, r, true, 0.f, seed, step, stream);

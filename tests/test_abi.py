@@ -120,3 +120,12 @@ def test_binding_refuses_cpu_tensors(lib):
     X = torch.zeros(4, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         binding.project_inputs(X, torch.zeros(8, 2), torch.zeros(4, 2, dtype=torch.bfloat16))
+
+
+def test_launch_counter_ignores_rejected_calls(lib):
+    """The launch counter moves only when a kernel is launched: a call that
+    fails validation on the host launches nothing."""
+    before = binding.kernel_launches()
+    st = _call("sketch_project_inputs", NULL, 16, 60, 64, NULL, 8, NULL, 8, NULL, 0, NULL)
+    assert st == binding.ERR_INVALID_ARG
+    assert binding.kernel_launches() == before >= 0
