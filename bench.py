@@ -17,6 +17,7 @@ host memory inside the timed region.  ``--impl reference`` times the CPU oracle
 (the plain C statement of the method) on a bounded sample of the same workload.
 """
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -43,6 +44,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="steps in the end-to-end (host buffers) measurement; default = --steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="keep only the first N layers of the workload (a smaller case for profiling)")
     return ap.parse_args()
 
 
@@ -251,6 +254,8 @@ def main():
     entry.build()
 
     wl = synth.WORKLOADS[args.workload]
+    if args.layers:
+        wl = dataclasses.replace(wl, name="%s[:%d]" % (wl.name, args.layers), layers=wl.layers[:args.layers])
     r = args.rank
     T = wl.microbatch
     nmb = wl.microbatches

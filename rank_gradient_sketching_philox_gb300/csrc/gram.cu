@@ -3,72 +3,117 @@
 // ||C P^T||_F^2 = <P^T P, C^T C>.
 //
 // Two deterministic passes over a batch of matrices: partial Grams over at
-// most 64 fixed row chunks, then a fixed-order sum over the chunks.  Products
-// are summed in fp32 over 32-row tiles and the tiles in double, so an entry is
-// good to about 1e-8 relative.  Neither pass uses atomics, so the result does
-// not depend on scheduling.
+// most 64 fixed row chunks, then a fixed-order sum over the chunks.  Within a
+// chunk, products are summed in fp32 over 32-row tiles and the tiles are added
+// with TwoSum into a (hi, lo) pair; the chunk sum carries the pairs the same
+// way.  Only the 32-term tile sums round, so an entry is good to about 1e-7 of
+// the sum of its |terms| however many rows there are, without FP64 arithmetic
+// (far slower than fp32 on this GPU).  Neither pass uses atomics, so the
+// result does not depend on scheduling.
 #include "common.cuh"
 #include "internal.h"
 
 namespace rgs {
 namespace {
 
-constexpr int kTile = 32;
+constexpr int kTile = 64;   // output tile edge
+constexpr int kRows = 32;   // rows staged per step
 
-// grid (64 chunks, tiles*tiles, batch); block 256 = 32 x 8 threads.
-// Thread (tx, ty) owns outputs (a = a0 + ty + 8m, b = b0 + tx), m = 0..3.
+// (hi, lo) += x with TwoSum (Knuth): exact error of the addition kept in lo.
+__device__ __forceinline__ void acc2(float& hi, float& lo, float x) {
+  const float s = __fadd_rn(hi, x);
+  const float bb = __fsub_rn(s, hi);
+  const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(x, bb));
+  hi = s;
+  lo = __fadd_rn(lo, e);
+}
+
+// grid (64 chunks, tile pairs ta <= tb, batch); block 256 = 16 x 16 threads.
+// Thread (tx, ty) owns the 4 x 4 outputs a = a0 + 4ty + i, b = b0 + 4tx + j.
 __global__ void __launch_bounds__(256) gram_partial_kernel(const GramBatch batch) {
-  __shared__ float sa[kTile][kTile + 1];
-  __shared__ float sb[kTile][kTile + 1];
+  __shared__ __align__(16) float sa[kRows][kTile];
+  __shared__ __align__(16) float sb[kRows][kTile];
   const GramEntry& en = batch.e[blockIdx.z];
   const int r = batch.r;
   const GramChunks g = gram_chunks(en.rows);
   if ((int)blockIdx.x >= g.nchunks) return;
   const int tiles = (int)ceil_div(r, kTile);
-  const int a0 = (blockIdx.y / tiles) * kTile, b0 = (blockIdx.y % tiles) * kTile;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  // blockIdx.y enumerates the pairs ta <= tb row by row
+  int ta = 0, rem = (int)blockIdx.y;
+  while (rem >= tiles - ta) {
+    rem -= tiles - ta;
+    ++ta;
+  }
+  const int tb = ta + rem;
+  const int a0 = ta * kTile, b0 = tb * kTile;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int64_t row_begin = (int64_t)blockIdx.x * g.chunk_rows;
   int64_t row_end = row_begin + g.chunk_rows;
   if (row_end > en.rows) row_end = en.rows;
   const float* __restrict__ A = en.A;
-  double acc[4] = {0.0, 0.0, 0.0, 0.0};
-  for (int64_t base = row_begin; base < row_end; base += kTile) {
-    for (int i = ty; i < kTile; i += 8) {
+  float hi[16], lo[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0.f;
+  for (int64_t base = row_begin; base < row_end; base += kRows) {
+    // stage 32 rows of columns a0.. and b0.. (zero outside the matrix)
+    for (int e = threadIdx.x; e < kRows * kTile; e += 256) {
+      const int i = e / kTile, c = e % kTile;
       const int64_t row = base + i;
       const bool ok = row < row_end;
-      sa[i][tx] = (ok && a0 + tx < r) ? A[row * r + a0 + tx] : 0.f;
-      sb[i][tx] = (ok && b0 + tx < r) ? A[row * r + b0 + tx] : 0.f;
+      sa[i][c] = (ok && a0 + c < r) ? A[row * r + a0 + c] : 0.f;
+      sb[i][c] = (ok && b0 + c < r) ? A[row * r + b0 + c] : 0.f;
     }
     __syncthreads();
-    float tile[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int i = 0; i < kTile; ++i) {
-      const float bv = sb[i][tx];
+    float t[16];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) tile[m] = fmaf(sa[i][ty + 8 * m], bv, tile[m]);
+    for (int e = 0; e < 16; ++e) t[e] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < kRows; ++i) {
+      const float4 av = *reinterpret_cast<const float4*>(&sa[i][4 * ty]);
+      const float4 bv = *reinterpret_cast<const float4*>(&sb[i][4 * tx]);
+      const float aa[4] = {av.x, av.y, av.z, av.w}, bb[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) t[4 * p + q] = fmaf(aa[p], bb[q], t[4 * p + q]);
     }
 #pragma unroll
-    for (int m = 0; m < 4; ++m) acc[m] += (double)tile[m];
+    for (int e = 0; e < 16; ++e) acc2(hi[e], lo[e], t[e]);
     __syncthreads();
   }
-  double* out = en.partials + (size_t)blockIdx.x * r * r;
+  float2* out = en.partials + (size_t)blockIdx.x * r * r;
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const int a = a0 + ty + 8 * m, b = b0 + tx;
-    if (a < r && b < r) out[(size_t)a * r + b] = acc[m];
-  }
+  for (int p = 0; p < 4; ++p)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int a = a0 + 4 * ty + p, b = b0 + 4 * tx + q;
+      if (a < r && b < r) out[(size_t)a * r + b] = make_float2(hi[4 * p + q], lo[4 * p + q]);
+    }
 }
 
-// out[e] = sum over chunks c, in order, of partials[c][e].  grid (.., batch).
+// out[a][b] = sum over chunks c, in order, of partials[c][a][b] (TwoSum on the
+// pairs), for the tiles ta <= tb the partial kernel wrote; the other half is
+// the mirror image.  grid (.., batch).
 __global__ void gram_reduce_kernel(const GramBatch batch) {
   const GramEntry& en = batch.e[blockIdx.y];
-  const int rr = batch.r * batch.r;
+  const int r = batch.r, rr = r * r;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= rr) return;
+  int a = e / r, b = e % r;
+  if (a / kTile > b / kTile) {  // below the computed tiles: read the mirror
+    const int t = a;
+    a = b;
+    b = t;
+  }
+  const int src = a * r + b;
   const int nchunks = gram_chunks(en.rows).nchunks;
-  double s = 0.0;
-  for (int c = 0; c < nchunks; ++c) s += en.partials[(size_t)c * rr + e];
-  en.out[e] = s;
+  float hi = 0.f, lo = 0.f;
+  for (int c = 0; c < nchunks; ++c) {
+    const float2 v = en.partials[(size_t)c * rr + src];
+    acc2(hi, lo, v.x);
+    lo = __fadd_rn(lo, v.y);
+  }
+  en.out[e] = (double)hi + (double)lo;
 }
 
 }  // namespace
@@ -77,7 +122,7 @@ cudaError_t launch_gram(const GramBatch& batch, cudaStream_t stream) {
   if (batch.n <= 0) return cudaSuccess;
   const int tiles = (int)ceil_div(batch.r, kTile);
   count_launch();
-  gram_partial_kernel<<<dim3(64, tiles * tiles, batch.n), 256, 0, stream>>>(batch);
+  gram_partial_kernel<<<dim3(64, tiles * (tiles + 1) / 2, batch.n), 256, 0, stream>>>(batch);
   const int rr = batch.r * batch.r;
   count_launch();
   gram_reduce_kernel<<<dim3((unsigned)ceil_div(rr, 256), batch.n), 256, 0, stream>>>(batch);

@@ -56,7 +56,7 @@ __host__ __device__ inline GramChunks gram_chunks(int64_t rows) {
 struct GramEntry {
   const float* A;   // rows x r, row-major
   int64_t rows;
-  double* partials; // gram_chunks(rows).nchunks x r x r
+  float2* partials; // gram_chunks(rows).nchunks x r x r (hi, lo) pairs
   double* out;      // r x r
 };
 struct GramBatch {
@@ -72,7 +72,7 @@ struct ProjProblem {
   int64_t k;
   uint32_t layer;
   float scale;      // QR: sqrt(k / r) rounded to fp32; Rademacher: 1/sqrt(r)
-  double* partials; // QR: nchunks(k) x r x r
+  float2* partials; // QR: nchunks(k) x r x r (hi, lo) pairs
   double* gram;     // QR: r x r
   float* rinv;      // QR: r x r
 };
@@ -125,8 +125,8 @@ struct UpdateProblem {
   int32_t* dev_status;
 };
 struct UpdateWorkspace {
-  double* gram_partials_p; // nchunks(k) x r x r
-  double* gram_partials_c; // nchunks(d) x r x r
+  float2* gram_partials_p; // nchunks(k) x r x r
+  float2* gram_partials_c; // nchunks(d) x r x r
   double* gram_p;          // r x r
   double* gram_c;          // r x r
   float* c_norm;           // d: Euclidean norm of each row of C

@@ -129,35 +129,72 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
 }
 
 // P rows [32*blockIdx.x, +32) <- scale * P_rows * Rinv (Rinv upper triangular).
+// P rows <- (P rows) X, X = R^-1 upper triangular, in place; on the final pass
+// also times the scale sqrt(k/r).  A block takes RB rows and all r columns:
+// thread t owns the 4 x 4 outputs of column quad t % r4 and row quad t / r4
+// (r4 = ceil(r/4) quads, RB = 4 * floor(256 / r4) rows).  The block's rows are
+// staged in shared memory first, so the in-place writes cannot race its reads.
 __global__ void __launch_bounds__(256) tri_apply_kernel(const ProjBatch batch, int final_pass) {
-  extern __shared__ float smem[];
+  extern __shared__ float S[];  // RB x (r + 1)
   const ProjProblem& pb = batch.p[blockIdx.y];
-  const int r = batch.r;
-  const int64_t row0 = (int64_t)blockIdx.x * 32;
+  const int r = batch.r, r4 = (r + 3) / 4, rq_n = 256 / r4, RB = 4 * rq_n, ld = r + 1;
+  const int64_t row0 = (int64_t)blockIdx.x * RB;
   if (row0 >= pb.k) return;
-  const int rows = (int)((pb.k - row0) < 32 ? (pb.k - row0) : 32);
-  float* S = smem;           // 32 x r
-  float* O = smem + 32 * r;  // 32 x r
+  const int rows = (int)((pb.k - row0) < RB ? (pb.k - row0) : RB);
   float* P = pb.P + row0 * r;
-  for (int e = threadIdx.x; e < rows * r; e += blockDim.x) S[e] = P[e];
+  for (int e = threadIdx.x; e < rows * r; e += blockDim.x) S[(e / r) * ld + e % r] = P[e];
   __syncthreads();
-  const float scale = final_pass ? pb.scale : 1.0f;
+  const int cq = threadIdx.x % r4, rq = threadIdx.x / r4;
+  if (rq >= rq_n) return;
+  const int c0 = 4 * cq, q0 = 4 * rq;
   const float* __restrict__ X = pb.rinv;
-  for (int e = threadIdx.x; e < rows * r; e += blockDim.x) {
-    const int row = e / r, c = e % r;
-    float acc = 0.0f;
-    for (int m = 0; m <= c; ++m) acc = fmaf(S[row * r + m], X[m * r + c], acc);
-    O[e] = acc * scale;
+  float acc[4][4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[p][q] = 0.f;
+  const int mend = (c0 + 4 < r) ? c0 + 4 : r;  // X is upper triangular: m <= c
+  const bool vec = (r & 3) == 0;
+  for (int m = 0; m < mend; ++m) {
+    float xv[4];
+    if (vec) {
+      const float4 x4 = *reinterpret_cast<const float4*>(X + (size_t)m * r + c0);
+      xv[0] = x4.x;
+      xv[1] = x4.y;
+      xv[2] = x4.z;
+      xv[3] = x4.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xv[q] = (c0 + q < r) ? X[(size_t)m * r + c0 + q] : 0.f;
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float sv = S[(q0 + p) * ld + m];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(sv, xv[q], acc[p][q]);
+    }
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < rows * r; e += blockDim.x) P[e] = O[e];
+  const float scale = final_pass ? pb.scale : 1.0f;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    if (q0 + p >= rows) break;
+    float* out = P + (size_t)(q0 + p) * r + c0;
+    if (vec) {
+      *reinterpret_cast<float4*>(out) =
+          make_float4(acc[p][0] * scale, acc[p][1] * scale, acc[p][2] * scale, acc[p][3] * scale);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c0 + q < r) out[q] = acc[p][q] * scale;
+    }
+  }
 }
 
 }  // namespace
 
 void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
   const GramChunks g = gram_chunks(k);
-  double* partials = cur.take<double>((size_t)g.nchunks * r * r);
+  float2* partials = cur.take<float2>((size_t)g.nchunks * r * r);
   double* gram = cur.take<double>((size_t)r * r);
   float* rinv = cur.take<float>((size_t)r * r);
   if (p) {
@@ -189,7 +226,8 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
     gb.e[i].out = batch.p[i].gram;
   }
   const size_t chol_smem = sizeof(float) * (size_t)r * (r + 1) / 2;
-  const size_t apply_smem = sizeof(float) * 2 * 32 * (size_t)r;
+  const int r4 = (r + 3) / 4, apply_rows = 4 * (256 / r4);
+  const size_t apply_smem = sizeof(float) * (size_t)apply_rows * (r + 1);
   cudaError_t err = cudaFuncSetAttribute(chol_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)chol_smem);
   if (err != cudaSuccess) return err;
@@ -202,7 +240,7 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
     count_launch();
     chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch);
     count_launch();
-    tri_apply_kernel<<<dim3((unsigned)ceil_div(max_k, 32), batch.n), 256, apply_smem, stream>>>(
+    tri_apply_kernel<<<dim3((unsigned)ceil_div(max_k, apply_rows), batch.n), 256, apply_smem, stream>>>(
         batch, pass == 1);
   }
   return cudaGetLastError();

@@ -892,8 +892,8 @@ size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool n
   UpdateWorkspace w{};
   const int r_pad = round16(r);
   if (normsgd) {
-    w.gram_partials_p = cur.take<double>((size_t)gram_chunks(k).nchunks * r * r);
-    w.gram_partials_c = cur.take<double>((size_t)gram_chunks(d).nchunks * r * r);
+    w.gram_partials_p = cur.take<float2>((size_t)gram_chunks(k).nchunks * r * r);
+    w.gram_partials_c = cur.take<float2>((size_t)gram_chunks(d).nchunks * r * r);
     w.gram_p = cur.take<double>((size_t)r * r);
     w.gram_c = cur.take<double>((size_t)r * r);
     w.wnorm_partials = cur.take<double>(kWnormBlocks);
