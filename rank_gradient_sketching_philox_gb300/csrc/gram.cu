@@ -28,8 +28,33 @@ __device__ __forceinline__ void acc2(float& hi, float& lo, float x) {
   lo = __fadd_rn(lo, e);
 }
 
+// Rows [row, row + 32) x columns [c0, c0 + 64) of A into registers: element
+// (e / 16, 4 (e % 16) .. + 3) for e = threadIdx.x and threadIdx.x + 256; zero
+// outside the matrix.  Vector loads when r is a multiple of 4.
+__device__ __forceinline__ void load_rows(const float* __restrict__ A, int r, int64_t row, int64_t row_end, int c0,
+                                          float4 (&v)[2]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int e = threadIdx.x + 256 * h;
+    const int64_t rw = row + (e >> 4);
+    const int c = c0 + 4 * (e & 15);
+    v[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (rw >= row_end) continue;
+    const float* src = A + rw * r + c;
+    if ((r & 3) == 0 && c + 3 < r) {
+      v[h] = *reinterpret_cast<const float4*>(src);
+    } else {
+      if (c < r) v[h].x = src[0];
+      if (c + 1 < r) v[h].y = src[1];
+      if (c + 2 < r) v[h].z = src[2];
+      if (c + 3 < r) v[h].w = src[3];
+    }
+  }
+}
+
 // grid (64 chunks, tile pairs ta <= tb, batch); block 256 = 16 x 16 threads.
 // Thread (tx, ty) owns the 4 x 4 outputs a = a0 + 4ty + i, b = b0 + 4tx + j.
+// The next 32 rows are loaded into registers while the current ones are used.
 __global__ void __launch_bounds__(256) gram_partial_kernel(const GramBatch batch) {
   __shared__ __align__(16) float sa[kRows][kTile];
   __shared__ __align__(16) float sb[kRows][kTile];
@@ -45,32 +70,39 @@ __global__ void __launch_bounds__(256) gram_partial_kernel(const GramBatch batch
     ++ta;
   }
   const int tb = ta + rem;
+  const bool diag = ta == tb;
   const int a0 = ta * kTile, b0 = tb * kTile;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int64_t row_begin = (int64_t)blockIdx.x * g.chunk_rows;
   int64_t row_end = row_begin + g.chunk_rows;
   if (row_end > en.rows) row_end = en.rows;
   const float* __restrict__ A = en.A;
+  const float(*sbb)[kTile] = diag ? sa : sb;
   float hi[16], lo[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0.f;
+  float4 va[2], vb[2];
+  load_rows(A, r, row_begin, row_end, a0, va);
+  if (!diag) load_rows(A, r, row_begin, row_end, b0, vb);
   for (int64_t base = row_begin; base < row_end; base += kRows) {
-    // stage 32 rows of columns a0.. and b0.. (zero outside the matrix)
-    for (int e = threadIdx.x; e < kRows * kTile; e += 256) {
-      const int i = e / kTile, c = e % kTile;
-      const int64_t row = base + i;
-      const bool ok = row < row_end;
-      sa[i][c] = (ok && a0 + c < r) ? A[row * r + a0 + c] : 0.f;
-      sb[i][c] = (ok && b0 + c < r) ? A[row * r + b0 + c] : 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = threadIdx.x + 256 * h;
+      *reinterpret_cast<float4*>(&sa[e >> 4][4 * (e & 15)]) = va[h];
+      if (!diag) *reinterpret_cast<float4*>(&sb[e >> 4][4 * (e & 15)]) = vb[h];
     }
     __syncthreads();
+    if (base + kRows < row_end) {
+      load_rows(A, r, base + kRows, row_end, a0, va);
+      if (!diag) load_rows(A, r, base + kRows, row_end, b0, vb);
+    }
     float t[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) t[e] = 0.f;
 #pragma unroll 4
     for (int i = 0; i < kRows; ++i) {
       const float4 av = *reinterpret_cast<const float4*>(&sa[i][4 * ty]);
-      const float4 bv = *reinterpret_cast<const float4*>(&sb[i][4 * tx]);
+      const float4 bv = *reinterpret_cast<const float4*>(&sbb[i][4 * tx]);
       const float aa[4] = {av.x, av.y, av.z, av.w}, bb[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
       for (int p = 0; p < 4; ++p)
