@@ -211,10 +211,21 @@ typedef struct {
 typedef struct {
     const uint16_t* X; /* T x k BF16 */
     int64_t T, k, ld_x;
-    const float* P;    /* k x r fp32 */
+    const float* P;    /* k x r fp32; may be NULL when P_split is given */
     uint16_t* XP;      /* T x r BF16, written */
     int64_t ld_xp;
+    /* nullable: the split of P made by sketch_split_projection_batched for
+     * this k and r; the call then reads it instead of splitting P again */
+    const uint16_t* P_split;
 } sketch_project_problem;
+
+/* One projection to split: P (k x r fp32) into P_split, which holds
+ * sketch_projection_split_elems(k, r) uint16_t, caller-owned. */
+typedef struct {
+    const float* P;
+    int64_t k;
+    uint16_t* P_split;
+} sketch_split_problem;
 
 typedef struct {
     const uint16_t* D; /* T x d BF16 */
@@ -246,6 +257,17 @@ SKETCH_API sketch_status sketch_sample_projection_batched(sketch_proj_kind kind,
                                                           size_t ws_bytes, void* stream);
 SKETCH_API sketch_status sketch_project_inputs_batched(int n, const sketch_project_problem* problems, int64_t r,
                                                        void* ws, size_t ws_bytes, void* stream);
+/* The BF16 split of projections as sketch_project_inputs uses them: with
+ * n_pad = r rounded up to 16, rows [0, n_pad) of P_split hold the BF16 of P^T
+ * (round to nearest even) and rows [n_pad, 2 n_pad) the BF16 of the remainder
+ * P^T - hi, each row k values (rows r..n_pad-1 of each half are zero); the
+ * tensor cores form X P as X hi + X lo.  A layer's P is split once per
+ * refresh and the split passed to every sketch_project_inputs_batched call of
+ * that P (the pages split nothing: this only saves work; a call without a
+ * split makes its own in the workspace).  P_split must not overlap P. */
+SKETCH_API size_t sketch_projection_split_elems(int64_t k, int64_t r);
+SKETCH_API sketch_status sketch_split_projection_batched(int n, const sketch_split_problem* problems, int64_t r,
+                                                         void* stream);
 SKETCH_API sketch_status sketch_accumulate_batched(int n, const sketch_accumulate_problem* problems, int64_t r,
                                                    int overwrite, void* ws, size_t ws_bytes, void* stream);
 SKETCH_API sketch_status sketch_apply_update_normsgd_batched(int n, const sketch_update_problem* problems,

@@ -8,5 +8,6 @@ The compute path is the C-ABI shared library ``lib/libsketch.so`` (declared in
 from .binding import (PROJ_GAUSSIAN_QR, PROJ_RADEMACHER, SketchError, accumulate,  # noqa: F401
                       accumulate_batched, apply_update_normsgd, apply_update_normsgd_batched,
                       apply_update_sgd, apply_update_sgd_batched, kernel_launches, project_inputs,
-                      project_inputs_batched, read_device_errors, sample_projection,
+                      project_inputs_batched, projection_split_elems, read_device_errors,
+                      sample_projection, split_projection_batched,
                       sample_projection_batched, workspace_bytes, workspace_bytes_batched)

@@ -39,7 +39,8 @@ EXPORTS = ("sketch_workspace_bytes", "sketch_sample_projection", "sketch_project
            "sketch_project_inputs_batched", "sketch_accumulate_batched",
            "sketch_apply_update_normsgd_batched", "sketch_apply_update_sgd_batched",
            "sketch_apply_update_normsgd_noalloc", "sketch_noalloc_scratch_bytes",
-           "sketch_read_device_errors", "sketch_kernel_launches", "sketch_status_string",
+           "sketch_read_device_errors", "sketch_kernel_launches", "sketch_projection_split_elems",
+           "sketch_split_projection_batched", "sketch_status_string",
            "sketch_last_error")
 
 
@@ -50,7 +51,11 @@ class ProjectionProblem(ctypes.Structure):
 class ProjectProblem(ctypes.Structure):
     _fields_ = [("X", ctypes.c_void_p), ("T", ctypes.c_int64), ("k", ctypes.c_int64),
                 ("ld_x", ctypes.c_int64), ("P", ctypes.c_void_p), ("XP", ctypes.c_void_p),
-                ("ld_xp", ctypes.c_int64)]
+                ("ld_xp", ctypes.c_int64), ("P_split", ctypes.c_void_p)]
+
+
+class SplitProblem(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_void_p), ("k", ctypes.c_int64), ("P_split", ctypes.c_void_p)]
 
 
 class AccumulateProblem(ctypes.Structure):
@@ -93,6 +98,8 @@ _SIGS = {
                                            _u32, _u32, _vp, _vp, _c.c_size_t, _vp]),
     "sketch_read_device_errors": (_c.c_int, [_c.POINTER(_c.c_int32), _vp]),
     "sketch_kernel_launches": (_c.c_uint64, []),
+    "sketch_projection_split_elems": (_c.c_size_t, [_i64, _i64]),
+    "sketch_split_projection_batched": (_c.c_int, [_c.c_int, _vp, _i64, _vp]),
     "sketch_workspace_bytes_batched": (ctypes.c_size_t, [_c.c_int, _c.c_int, _vp, _vp, _vp, _i64]),
     "sketch_sample_projection_batched": (_c.c_int, [_c.c_int, _u64, _u32, _c.c_int, _vp, _i64, _vp, _vp,
                                                     _c.c_size_t, _vp]),
@@ -330,7 +337,32 @@ def sample_projection_batched(kind, seed, step, Ps, layers, dev_status=None, ws=
     return Ps
 
 
-def project_inputs_batched(Xs, Ps, XPs, ws=None, stream=None):
+def projection_split_elems(k, r):
+    return int(lib().sketch_projection_split_elems(k, r))
+
+
+def split_projection_batched(Ps, splits=None, stream=None):
+    """BF16 splits of the projections Ps (k x r fp32) for project_inputs_batched;
+    returns the list of split buffers (uint16, allocated when not given)."""
+    n = len(Ps)
+    r = Ps[0].shape[1]
+    if splits is None:
+        splits = [torch.empty(projection_split_elems(P.shape[0], r), dtype=torch.int16, device=P.device)
+                  for P in Ps]
+    probs = (SplitProblem * n)()
+    for i, (P, S) in enumerate(zip(Ps, splits)):
+        _contig(P, torch.float32, "P")
+        if P.shape[1] != r or S.numel() * S.element_size() < 2 * projection_split_elems(P.shape[0], r):
+            raise ValueError("shape mismatch in problem %d" % i)
+        probs[i] = SplitProblem(P.data_ptr(), P.shape[0], S.data_ptr())
+    h, _ = _stream_handle(stream, Ps[0].device)
+    _check(lib().sketch_split_projection_batched(n, probs, r, h))
+    return splits
+
+
+def project_inputs_batched(Xs, Ps, XPs, ws=None, stream=None, splits=None):
+    """XP = bf16(X P) for each problem; `splits` (from split_projection_batched
+    for these Ps) skips splitting P again."""
     n = len(Xs)
     r = Ps[0].shape[1]
     probs = (ProjectProblem * n)()
@@ -341,7 +373,7 @@ def project_inputs_batched(Xs, Ps, XPs, ws=None, stream=None):
         if P.shape != (X.shape[1], r) or XP.shape[0] != X.shape[0] or XP.shape[1] < r:
             raise ValueError("shape mismatch in problem %d" % i)
         probs[i] = ProjectProblem(X.data_ptr(), X.shape[0], X.shape[1], ld_x, P.data_ptr(),
-                                  XP.data_ptr(), ld_xp)
+                                  XP.data_ptr(), ld_xp, splits[i].data_ptr() if splits is not None else None)
     h, s = _stream_handle(stream, Xs[0].device)
     nbytes = workspace_bytes_batched(OP_PROJECT_INPUTS, T=[X.shape[0] for X in Xs],
                                      k=[X.shape[1] for X in Xs], r=r)

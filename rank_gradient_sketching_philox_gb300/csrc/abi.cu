@@ -132,7 +132,7 @@ sketch_status check_project(const sketch_project_problem& p, int64_t r) {
   TRY(check_ld("ld_x", p.ld_x, p.k));
   TRY(check_ld("ld_xp", p.ld_xp, r));
   CHECK_PTR(p.X);
-  CHECK_PTR(p.P);
+  if (p.P == nullptr && p.P_split == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "P and P_split are both NULL");
   CHECK_PTR(p.XP);
   return SKETCH_OK;
 }
@@ -239,7 +239,7 @@ sketch_status do_project(int n, const sketch_project_problem* probs, int64_t r, 
     TRY(check_project(probs[i], r));
     need += rgs::project_workspace_bytes(probs[i].T, probs[i].k, r);
     v[i] = rgs::ProjectProblem{probs[i].X, probs[i].T, probs[i].k, probs[i].ld_x, probs[i].P, probs[i].XP,
-                               probs[i].ld_xp};
+                               probs[i].ld_xp, probs[i].P_split};
   }
   TRY(check_ws(ws, ws_bytes, need));
   return launch_result(rgs::launch_project_inputs(n, v.data(), (int)r, ws, s), "project_inputs");
@@ -348,6 +348,32 @@ sketch_status sketch_project_inputs(const uint16_t* X, int64_t T, int64_t k, int
 sketch_status sketch_project_inputs_batched(int n, const sketch_project_problem* problems, int64_t r, void* ws,
                                             size_t ws_bytes, void* stream) {
   return do_project(n, problems, r, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t sketch_projection_split_elems(int64_t k, int64_t r) {
+  if (k < 1 || k > kMaxDim || k % 8 != 0 || r < 1 || r > rgs::kMaxRank) return 0;
+  return (size_t)2 * (size_t)((r + 15) / 16 * 16) * (size_t)k;
+}
+
+sketch_status sketch_split_projection_batched(int n, const sketch_split_problem* problems, int64_t r,
+                                              void* stream) {
+  TRY(check_n(n));
+  if (problems == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "problems is NULL");
+  TRY(check_rank(r));
+  std::vector<const float*> P((size_t)n);
+  std::vector<int64_t> k((size_t)n);
+  std::vector<uint16_t*> out((size_t)n);
+  for (int i = 0; i < n; ++i) {
+    TRY(check_k(problems[i].k));
+    CHECK_PTR(problems[i].P);
+    CHECK_PTR(problems[i].P_split);
+    P[i] = problems[i].P;
+    k[i] = problems[i].k;
+    out[i] = problems[i].P_split;
+  }
+  return launch_result(rgs::launch_split_projection(n, P.data(), k.data(), out.data(), (int)r,
+                                                    static_cast<cudaStream_t>(stream)),
+                       "split_projection");
 }
 
 sketch_status sketch_accumulate(const uint16_t* D, int64_t T, int64_t d, int64_t ld_d, const uint16_t* XP,

@@ -97,8 +97,12 @@ struct ProjectProblem {
   const float* P;     // k x r fp32
   uint16_t* XP;       // T x r BF16, row stride ld_xp
   int64_t ld_xp;
+  const uint16_t* P_split;  // nullable: a ready split of P (2 n_pad x k BF16)
 };
 size_t project_workspace_bytes(int64_t T, int64_t k, int64_t r);
+// P (k x r fp32) -> [hi(P^T); lo(P^T)] (2 n_pad x k BF16) for each problem.
+cudaError_t launch_split_projection(int n, const float* const* P, const int64_t* k, uint16_t* const* out, int r,
+                                    cudaStream_t stream);
 // Workspace: the problems' regions of project_workspace_bytes, back to back.
 cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, void* ws, cudaStream_t stream);
 

@@ -133,19 +133,24 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
 // also times the scale sqrt(k/r).  A block takes RB rows and all r columns:
 // thread t owns the 4 x 4 outputs of column quad t % r4 and row quad t / r4
 // (r4 = ceil(r/4) quads, RB = 4 * floor(256 / r4) rows).  The block's rows are
-// staged in shared memory first, so the in-place writes cannot race its reads.
+// staged in shared memory first, so the in-place writes cannot race its reads;
+// X follows through shared memory 32 rows at a time.
+constexpr int kXRows = 32;
 __global__ void __launch_bounds__(256) tri_apply_kernel(const ProjBatch batch, int final_pass) {
-  extern __shared__ float S[];  // RB x (r + 1)
+  extern __shared__ float smem[];
   const ProjProblem& pb = batch.p[blockIdx.y];
   const int r = batch.r, r4 = (r + 3) / 4, rq_n = 256 / r4, RB = 4 * rq_n, ld = r + 1;
+  const int xld = 4 * r4;  // X rows padded to whole quads (16-byte aligned)
+  float* S = smem;                    // RB x (r + 1)
+  float* Xs = smem + RB * ld + 3;     // kXRows x xld, 16-byte aligned below
+  Xs = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(Xs) + 15) & ~uintptr_t(15));
   const int64_t row0 = (int64_t)blockIdx.x * RB;
   if (row0 >= pb.k) return;
   const int rows = (int)((pb.k - row0) < RB ? (pb.k - row0) : RB);
   float* P = pb.P + row0 * r;
   for (int e = threadIdx.x; e < rows * r; e += blockDim.x) S[(e / r) * ld + e % r] = P[e];
-  __syncthreads();
   const int cq = threadIdx.x % r4, rq = threadIdx.x / r4;
-  if (rq >= rq_n) return;
+  const bool active = rq < rq_n;
   const int c0 = 4 * cq, q0 = 4 * rq;
   const float* __restrict__ X = pb.rinv;
   float acc[4][4];
@@ -153,28 +158,33 @@ __global__ void __launch_bounds__(256) tri_apply_kernel(const ProjBatch batch, i
   for (int p = 0; p < 4; ++p)
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[p][q] = 0.f;
-  const int mend = (c0 + 4 < r) ? c0 + 4 : r;  // X is upper triangular: m <= c
-  const bool vec = (r & 3) == 0;
-  for (int m = 0; m < mend; ++m) {
-    float xv[4];
-    if (vec) {
-      const float4 x4 = *reinterpret_cast<const float4*>(X + (size_t)m * r + c0);
-      xv[0] = x4.x;
-      xv[1] = x4.y;
-      xv[2] = x4.z;
-      xv[3] = x4.w;
-    } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) xv[q] = (c0 + q < r) ? X[(size_t)m * r + c0 + q] : 0.f;
+  for (int m0 = 0; m0 < r; m0 += kXRows) {
+    const int mrows = (r - m0) < kXRows ? (r - m0) : kXRows;
+    __syncthreads();  // S staged (first chunk) / the previous X chunk used
+    for (int e = threadIdx.x; e < mrows * xld; e += blockDim.x) {
+      const int mm = e / xld, c = e % xld;
+      Xs[e] = c < r ? X[(size_t)(m0 + mm) * r + c] : 0.f;
     }
+    __syncthreads();
+    if (!active) continue;
+    // X is upper triangular: rows m > c0 + 3 add nothing to these columns
+    int mend = c0 + 4 - m0;
+    if (mend > mrows) mend = mrows;
+#pragma unroll 4
+    for (int mm = 0; mm < mend; ++mm) {
+      const float4 x4 = *reinterpret_cast<const float4*>(Xs + mm * xld + c0);
+      const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const float sv = S[(q0 + p) * ld + m];
+      for (int p = 0; p < 4; ++p) {
+        const float sv = S[(q0 + p) * ld + m0 + mm];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(sv, xv[q], acc[p][q]);
+        for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(sv, xv[q], acc[p][q]);
+      }
     }
   }
+  if (!active) return;
   const float scale = final_pass ? pb.scale : 1.0f;
+  const bool vec = (r & 3) == 0;
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     if (q0 + p >= rows) break;
@@ -227,7 +237,7 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
   }
   const size_t chol_smem = sizeof(float) * (size_t)r * (r + 1) / 2;
   const int r4 = (r + 3) / 4, apply_rows = 4 * (256 / r4);
-  const size_t apply_smem = sizeof(float) * (size_t)apply_rows * (r + 1);
+  const size_t apply_smem = sizeof(float) * ((size_t)apply_rows * (r + 1) + 3 + 4 + (size_t)kXRows * 4 * r4);
   cudaError_t err = cudaFuncSetAttribute(chol_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)chol_smem);
   if (err != cudaSuccess) return err;

@@ -335,6 +335,28 @@ size_t project_workspace_bytes(int64_t, int64_t k, int64_t r) {
   return cur.offset;
 }
 
+cudaError_t launch_split_projection(int n, const float* const* P, const int64_t* k, uint16_t* const* out, int r,
+                                    cudaStream_t stream) {
+  static thread_local SplitT sp;
+  const int n_pad = round16(r);
+  for (int base = 0; base < n; base += kMaxProblems) {
+    const int m = (n - base) < kMaxProblems ? (n - base) : kMaxProblems;
+    int64_t max_k = 0;
+    for (int i = 0; i < m; ++i) {
+      sp.P[i] = P[base + i];
+      sp.out[i] = out[base + i];
+      sp.k[i] = k[base + i];
+      max_k = k[base + i] > max_k ? k[base + i] : max_k;
+    }
+    sp.r = r;
+    sp.n_pad = n_pad;
+    count_launch();
+    split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 32), (unsigned)ceil_div(n_pad, 32), (unsigned)m), 256, 0,
+                             stream>>>(sp);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, void* ws, cudaStream_t stream) {
   const int n_pad = round16(r);
   int* errw = nullptr;
@@ -343,19 +365,26 @@ cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, voi
   WsCursor cur;
   cur.base = static_cast<char*>(ws);
   static thread_local SkinnyBatch a;
-  static thread_local SplitT sp;
   for (int base = 0; base < n; base += kMaxProblems) {
     const int m = (n - base) < kMaxProblems ? (n - base) : kMaxProblems;
-    int64_t max_k = 0;
+    // problems without a ready split get one in their workspace region
+    const float* sp_P[kMaxProblems];
+    int64_t sp_k[kMaxProblems];
+    uint16_t* sp_out[kMaxProblems];
+    int nsplit = 0;
     a.tile_begin[0] = 0;
     for (int i = 0; i < m; ++i) {
       const ProjectProblem& pr = probs[base + i];
-      uint16_t* pt = cur.take<uint16_t>((size_t)2 * n_pad * pr.k);
+      uint16_t* region = cur.take<uint16_t>((size_t)2 * n_pad * pr.k);
       cur.take<char>(0);
-      sp.P[i] = pr.P;
-      sp.out[i] = pt;
-      sp.k[i] = pr.k;
-      max_k = pr.k > max_k ? pr.k : max_k;
+      const uint16_t* pt = pr.P_split;
+      if (pt == nullptr) {
+        sp_P[nsplit] = pr.P;
+        sp_k[nsplit] = pr.k;
+        sp_out[nsplit] = region;
+        ++nsplit;
+        pt = region;
+      }
       err = make_tmap_bf16_2d(&a.tmA[i], pr.X, (uint64_t)pr.k, (uint64_t)pr.T, (uint64_t)pr.ld_x * 2, 64, 128);
       if (err == cudaSuccess)
         err = make_tmap_bf16_2d(&a.tmB[i], pt, (uint64_t)pr.k, (uint64_t)2 * n_pad, (uint64_t)pr.k * 2, 64,
@@ -367,11 +396,10 @@ cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, voi
       a.kchunks[i] = (int)ceil_div(pr.k, kChunk);
       a.tile_begin[i + 1] = a.tile_begin[i] + (int)ceil_div(pr.T, 128);
     }
-    sp.r = r;
-    sp.n_pad = n_pad;
-    count_launch();
-    split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 32), (unsigned)ceil_div(n_pad, 32), (unsigned)m), 256, 0,
-                             stream>>>(sp);
+    if (nsplit > 0) {
+      err = launch_split_projection(nsplit, sp_P, sp_k, sp_out, r, stream);
+      if (err != cudaSuccess) return err;
+    }
     a.n = m;
     a.N = r;
     a.n_pad = n_pad;

@@ -129,3 +129,20 @@ def test_launch_counter_ignores_rejected_calls(lib):
     st = _call("sketch_project_inputs", NULL, 16, 60, 64, NULL, 8, NULL, 8, NULL, 0, NULL)
     assert st == binding.ERR_INVALID_ARG
     assert binding.kernel_launches() == before >= 0
+
+
+def test_projection_split_sizes(lib):
+    assert binding.projection_split_elems(4096, 64) == 2 * 64 * 4096
+    assert binding.projection_split_elems(4096, 20) == 2 * 32 * 4096   # r padded to 16
+    assert binding.projection_split_elems(60, 8) == 0                  # k not a multiple of 8
+    assert binding.projection_split_elems(64, 257) == 0
+
+
+def test_split_and_project_reject_missing_pointers(lib):
+    before = binding.kernel_launches()
+    probs = (binding.SplitProblem * 1)(binding.SplitProblem(None, 64, None))
+    assert _call("sketch_split_projection_batched", 1, probs, 8, NULL) == binding.ERR_INVALID_ARG
+    pp = (binding.ProjectProblem * 1)(binding.ProjectProblem(1 << 20, 16, 64, 64, None, 1 << 21, 8, None))
+    assert _call("sketch_project_inputs_batched", 1, pp, 8, NULL, 0, NULL) == binding.ERR_INVALID_ARG
+    assert "P_split" in binding.lib().sketch_last_error().decode()
+    assert binding.kernel_launches() == before

@@ -32,6 +32,11 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
+def bits_t(t):
+    """BF16 tensor -> int16 view (bit patterns, on the device)."""
+    return t.contiguous().view(torch.int16)
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     import __graft_entry__ as g
@@ -125,6 +130,27 @@ def test_project_inputs_matches_oracle(T, k, r, kind):
     XP = _padded_bf16(T, r)
     rgs.project_inputs(X.to(DEV), torch.from_numpy(P).to(DEV), XP)
     _xp_check(bits(XP), orc.project_inputs(bits(X), P))
+
+
+@pytest.mark.parametrize("r", [64, 20, 256])
+def test_project_inputs_with_reused_split(r):
+    """A split made once by split_projection_batched gives the same XP, bit for
+    bit, as letting each call split P itself, across several microbatches and
+    layers of different k; one split launch replaces one per call."""
+    ks, T = [512, 1024, 136], 200
+    Ps = [torch.from_numpy(orc.sample_rademacher(5, li, 0, k, r)).to(DEV) for li, k in enumerate(ks)]
+    splits = rgs.split_projection_batched(Ps)
+    for mb in range(2):
+        Xs = [synth.normal_bf16((T, k), 1.0, 100 * mb + li).to(DEV) for li, k in enumerate(ks)]
+        ref = [_padded_bf16(T, r) for _ in ks]
+        got = [_padded_bf16(T, r) for _ in ks]
+        rgs.project_inputs_batched(Xs, Ps, ref)
+        before = rgs.kernel_launches()
+        rgs.project_inputs_batched(Xs, Ps, got, splits=splits)
+        assert rgs.kernel_launches() - before == 1  # the skinny GEMM only
+        for li in range(len(ks)):
+            assert torch.equal(bits_t(got[li]), bits_t(ref[li]))
+            _xp_check(bits(got[li]), orc.project_inputs(bits(Xs[li]), Ps[li].cpu().numpy()))
 
 
 def test_project_inputs_strided_rows_leave_padding():
