@@ -242,7 +242,7 @@ def main():
 
     import __graft_entry__ as entry
     import rank_gradient_sketching_philox_gb300 as rgs
-    from rank_gradient_sketching_philox_gb300 import binding, synth
+    from rank_gradient_sketching_philox_gb300 import binding, dataparallel, synth
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -269,7 +269,8 @@ def main():
     # ---- resident state -------------------------------------------------
     W = [synth.normal_bf16((d, k), synth.W_STD, synth.seed_w(li), device=dev)
          for li, (_, d, k) in enumerate(layers)]
-    C = [torch.empty(d, r, dtype=torch.float32, device=dev) for _, d, _ in layers]
+    # every layer's sketch in one buffer: one all-reduce per step across replicas
+    C_flat, C = dataparallel.flat_sketches([(d, r) for _, d, _ in layers], dev)
     P = [torch.empty(k, r, dtype=torch.float32, device=dev) for _, _, k in layers]
     XP = [torch.empty(T, max(8, (r + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :r]
           for _ in layers]
@@ -328,9 +329,7 @@ def main():
 
     def allreduce_sketch():
         # data parallel: each rank sketches its own microbatches; the sketches add
-        if world > 1:
-            for c in C:
-                dist.all_reduce(c)
+        dataparallel.allreduce_sketches(C_flat)
 
     def step(s, carried=True):
         sample_phase(s)

@@ -146,3 +146,11 @@ def test_split_and_project_reject_missing_pointers(lib):
     assert _call("sketch_project_inputs_batched", 1, pp, 8, NULL, 0, NULL) == binding.ERR_INVALID_ARG
     assert "P_split" in binding.lib().sketch_last_error().decode()
     assert binding.kernel_launches() == before
+
+
+def test_policy_sync_payload_is_the_factor_and_seed():
+    import torch
+    from rank_gradient_sketching_philox_gb300 import policy_sync
+    C = torch.arange(12, dtype=torch.float32).view(4, 3)
+    assert torch.equal(policy_sync.payload(C, 0.5), C * 0.5)
+    assert policy_sync.payload_bytes(4096, 64) == 4 * 4096 * 64 + 16       # vs 2*4096*4096 of BF16 W

@@ -23,7 +23,7 @@ import torch
 
 import oracle as orc
 import rank_gradient_sketching_philox_gb300 as rgs
-from rank_gradient_sketching_philox_gb300 import binding, synth
+from rank_gradient_sketching_philox_gb300 import binding, policy_sync, synth
 
 from gpu_util import bits, from_bits, rel_fro, w_parity
 
@@ -378,6 +378,30 @@ def test_sgd_nan_sketch_row_gives_canonical_nan():
     got = bits(W)
     assert np.all(ref[5] == 0x7FC0) and np.array_equal(got[5], ref[5])
     _w_check(np.delete(got, 5, 0), np.delete(ref, 5, 0))
+
+
+@pytest.mark.parametrize("kind", [rgs.PROJ_GAUSSIAN_QR, rgs.PROJ_RADEMACHER])
+def test_policy_sync_receiver_matches_trainer(kind):
+    """A rollout worker that receives U = alpha*eta*C and (seed, layer, step),
+    regenerates P and applies the update ends with the trainer's W, bit for
+    bit; both match the oracle's update."""
+    d, k, r, seed, layer, step = 512, 1024, 32, 7, 2, 5
+    W0 = synth.layer_weight(d, k, 6)
+    C = torch.from_numpy(_rand_c(d, r, 3)).to(DEV)
+    P_t = torch.empty(k, r, dtype=torch.float32, device=DEV)
+    rgs.sample_projection(kind, seed, layer, step, P_t)
+    U = policy_sync.payload(C, 1e-4)
+    W_t = W0.to(DEV)
+    policy_sync.apply(W_t, U, P_t, seed, layer, step)
+    U_rx = torch.from_numpy(U.cpu().numpy().copy()).to(DEV)      # what travels
+    P_r = torch.empty(k, r, dtype=torch.float32, device=DEV)
+    rgs.sample_projection(kind, seed, layer, step, P_r)           # regenerated, not sent
+    W_r = W0.to(DEV)
+    policy_sync.apply(W_r, U_rx, P_r, seed, layer, step)
+    assert torch.equal(P_t, P_r)
+    assert torch.equal(bits_t(W_t), bits_t(W_r))
+    _w_check(bits(W_t), orc.update_sgd(bits(W0), U.cpu().numpy(), P_t.cpu().numpy(), 1.0, seed, layer, step))
+    assert policy_sync.payload_bytes(d, r) == 4 * d * r + 16 < 2 * d * k
 
 
 @pytest.mark.parametrize("d,k,r", [(12288, 4096, 64), (2048, 6144, 256), (28672, 8192, 16)])
