@@ -73,6 +73,26 @@ __host__ __device__ inline void philox_round_keys(uint64_t seed, uint32_t* rk0, 
   }
 }
 
+// min of a, b and c that returns NaN when any is NaN (PTX three-input min.NaN).
+__device__ __forceinline__ float fmin3_nan(float a, float b, float c) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Integer multiply-adds (the multiplier pipe, leaving the ALU pipe to the rest):
+// mad_lo = low 32 bits of a*b + c, mad_hi = high 32 bits of a*b, plus c.
+__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // min of a and b that returns NaN when either is NaN (PTX min.NaN).
 __device__ __forceinline__ float fmin_nan(float a, float b) {
   float r;

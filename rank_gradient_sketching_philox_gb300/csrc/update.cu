@@ -120,33 +120,58 @@ __global__ void __launch_bounds__(256) normsgd_finalize_kernel(const __grid_cons
 // ---- BF16 high/low split of C and P, and their row norms ---------------------
 struct SplitBatch {
   const float* src[2 * kMaxAux];
-  int64_t rows[2 * kMaxAux];
+  int64_t row_begin[2 * kMaxAux + 1];  // prefix of the entries' row counts
   uint16_t* dst[2 * kMaxAux];   // rows x (2 r_pad): [hi | lo]
   float* norm[2 * kMaxAux];     // rows: Euclidean norm of each source row
+  int n;
   int r;
   int r_pad;
 };
 
-// One warp per row: x = hi + lo to 2^-17 relative (columns r..r_pad-1 zero)
-// and ||row||_2.  grid (rows / 8, entries), 256 threads.
+// One warp per row, grid-stride over the rows of all entries: x = hi + lo to
+// 2^-17 relative (columns r..r_pad-1 zero) and ||row||_2.  Lane l takes the
+// columns 4l..4l+3 of each 128-column step (vector loads and stores when r is
+// a multiple of 4).
 __global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__ SplitBatch b) {
-  const int en = blockIdx.y;
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= b.rows[en]) return;
-  const float* src = b.src[en] + row * b.r;
-  uint16_t* dst = b.dst[en] + row * 2 * b.r_pad;
-  float sq = 0.f;
-  for (int col = lane; col < b.r_pad; col += 32) {
-    const float v = (col < b.r) ? src[col] : 0.f;
-    sq = fmaf(v, v, sq);
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    const __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
-    dst[col] = __bfloat16_as_ushort(h);
-    dst[b.r_pad + col] = __bfloat16_as_ushort(l);
+  const int64_t total = b.row_begin[b.n];
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const bool vec = (b.r & 3) == 0;
+  int en = 0;  // rows of a warp only move forward
+  for (int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < total; g += warps) {
+    while (en + 1 < b.n && b.row_begin[en + 1] <= g) ++en;
+    const int64_t row = g - b.row_begin[en];
+    const float* src = b.src[en] + row * b.r;
+    uint16_t* dst = b.dst[en] + row * 2 * b.r_pad;
+    float sq = 0.f;
+    for (int c0 = 4 * lane; c0 < b.r_pad; c0 += 128) {
+      float v[4];
+      if (vec && c0 < b.r) {
+        const float4 f = *reinterpret_cast<const float4*>(src + c0);
+        v[0] = f.x;
+        v[1] = f.y;
+        v[2] = f.z;
+        v[3] = f.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = (c0 + t < b.r) ? src[c0 + t] : 0.f;
+      }
+      uint16_t hi[4], lo[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        sq = fmaf(v[t], v[t], sq);
+        const __nv_bfloat16 h = __float2bfloat16_rn(v[t]);
+        hi[t] = __bfloat16_as_ushort(h);
+        lo[t] = __bfloat16_as_ushort(__float2bfloat16_rn(v[t] - __bfloat162float(h)));
+      }
+      // r_pad is a multiple of 16: the 4 columns are inside the row, 8-byte aligned
+      *reinterpret_cast<uint2*>(dst + c0) = make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+      *reinterpret_cast<uint2*>(dst + b.r_pad + c0) =
+          make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+    }
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+    if (lane == 0) b.norm[en][row] = sqrtf(sq);
   }
-  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-  if (lane == 0) b.norm[en][row] = sqrtf(sq);
 }
 
 // ---- the rebuild + update kernel -------------------------------------------------
@@ -429,6 +454,15 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     constexpr int kPass = kCols < 32 ? kCols : 32;  // columns per pass
     constexpr int kGroups = kPass / 8;              // 8-column groups (Philox blocks) per pass
     constexpr int kGroupsPerWarp = kCols / 8;       // flag words of a warp per tile
+    // byte offset in a W stage (two 64-column, 128-byte-swizzled boxes) of this
+    // thread's 8-column groups: row q, column col_base + 8g
+    uint32_t stage_off[kGroupsPerWarp];
+#pragma unroll
+    for (int g = 0; g < kGroupsPerWarp; ++g) {
+      const int col = (ew >> 2) * kCols + 8 * g;
+      const int qq = (warp & 3) * 32 + lane;
+      stage_off[g] = (uint32_t)((col >> 6) * 16384 + qq * 128 + ((((col & 63) >> 3) ^ (qq & 7)) << 4));
+    }
     const int col_base = (ew >> 2) * kCols;    // column quarter of the tile
     const int q = quarter * 32 + lane;         // tile row = TMEM lane
     const bool storer = (ew == 0 && lane == 0);
@@ -474,7 +508,13 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         tc::tc_fence_after();
         uint8_t* s_w = s_w0 + (size_t)sw * a.w_bytes;
         for (int o = 16; o > 0; o >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
+        // The exactness test compares v^2 with thr^2 (multiplies on the idle FMA
+        // pipe instead of absolute values on the busy ALU pipe).  Where thr^2
+        // would leave the normal range, or thr is NaN, every group of the row
+        // is flagged instead (always safe); thr = 0 flags nothing.
         const float thr = thr_row * pmax;
+        const bool thr_ok = thr == 0.f || (thr >= 0x1p-60f && thr <= 0x1p60f);
+        const float thr2 = thr * thr;
 #pragma unroll 1
         for (int half = 0; half < kCols / kPass; ++half) {
           const int col32 = col_base + half * kPass;
@@ -502,6 +542,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           // store warp writes the tile out with TMA, clipping rows and columns
           // outside W).  A group that holds a NaN or a value small enough for
           // the exactness test is flagged for the careful path.
+          uint32_t fwords[kGroups];
 #pragma unroll
           for (int g = 0; g < kGroups; ++g) {
             if (g == 2 && live) {  // next 16 columns of H
@@ -509,24 +550,36 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
               tc::tmem_wait_ld_regs<16>(h);
             }
             const int col = col32 + 8 * g;
-            uint8_t* sp = s_w + (col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4);
+            uint8_t* sp = s_w + stage_off[half * kGroups + g];
             const uint4 raw = *reinterpret_cast<const uint4*>(sp);
             const uint32_t win[4] = {raw.x, raw.y, raw.z, raw.w};
             const uint32_t* rwg = rw[g];
             uint32_t wout[4];
-            float gmin = __int_as_float(0x7F800000);
+            float av[8];
 #pragma unroll
             for (int t2 = 0; t2 < 4; ++t2) {
+              // BF16 -> fp32 by shifting into the high half; the integer steps use
+              // multiply-adds so that they share the multiplier pipe with Philox
+              // instead of crowding the ALU pipe: r_hi = r >> 16,
+              // r_lo = r - r_hi * 2^16 = r & 0xFFFF
               const uint32_t wword = win[t2], rword = rwg[t2];
-              const float v0 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2]), __uint_as_float(wword << 16));
-              const float v1 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2 + 1]), __uint_as_float(wword & 0xFFFF0000u));
-              const uint32_t s0 = __float_as_uint(v0) + (rword & 0xFFFFu);
-              const uint32_t s1 = __float_as_uint(v1) + (rword >> 16);
+              const float v0 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2]),
+                                    __uint_as_float(mad_lo(wword, 0x10000u, 0u)));
+              const float v1 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2 + 1]),
+                                    __uint_as_float(wword & 0xFFFF0000u));
+              const uint32_t r_hi = mad_hi(rword, 0x10000u, 0u);
+              const uint32_t r_lo = mad_lo(r_hi, 0xFFFF0000u, rword);
+              const uint32_t s0 = mad_lo(r_lo, 1u, __float_as_uint(v0));
+              const uint32_t s1 = mad_hi(rword, 0x10000u, __float_as_uint(v1));
               wout[t2] = __byte_perm(s0, s1, 0x7632);
-              gmin = fmin_nan(gmin, fmin_nan(fabsf(v0), fabsf(v1)));  // NaN if any v is NaN
+              av[2 * t2] = v0 * v0;
+              av[2 * t2 + 1] = v1 * v1;
             }
+            // smallest v^2 of the group; NaN if any v is NaN
+            const float gmin = fmin3_nan(fmin3_nan(av[0], av[1], av[2]), fmin3_nan(av[3], av[4], av[5]),
+                                         fmin_nan(av[6], av[7]));
             const bool ok = live && row_ok && j0 + col < k;
-            const bool flag = ok && !(gmin >= thr);  // small value or NaN
+            const bool flag = ok && (!thr_ok || !(gmin > thr2));  // small value or NaN
             // Careful path (rare, warp-uniform): each element of a flagged group
             // whose |v| is below the threshold (or NaN) is queued as {p, i, j, W
             // bits} and redone exactly by the fixup kernel after this kernel's
@@ -541,14 +594,12 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
             // tensor-core values of the group (they differ from the exact ones
             // by at most one BF16 step, or are below the threshold), except that
             // a NaN makes it NaN.
-            const uint32_t fword = __ballot_sync(0xFFFFFFFFu, flag);
-            if (lane == 0)  // every word of the layer is written on every call
-              a.flags[p][((size_t)x.rb * a.n_ct[p] + ct) * (16 * kGroupsPerWarp) + ew * kGroupsPerWarp +
-                         half * kGroups + g] = fword;
+            fwords[g] = __ballot_sync(0xFFFFFFFFu, flag);
             if (flag) {
               if (need_norm && gmin != gmin) sq = __int_as_float(0x7FC00000);
             }
-            if (live) *reinterpret_cast<uint4*>(sp) = flag ? raw : make_uint4(wout[0], wout[1], wout[2], wout[3]);
+            if (live) *reinterpret_cast<uint4*>(sp) = make_uint4(wout[0], wout[1], wout[2], wout[3]);
+            if (flag) *reinterpret_cast<uint4*>(sp) = raw;  // rare: the fixup kernel needs the original
             if (need_norm && ok) {
               float gs = 0.f;
 #pragma unroll
@@ -562,6 +613,14 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
               sq_comp = (tsum - sq) - y;
               sq = tsum;
             }
+          }
+          if (lane == 0) {  // every word of the layer is written on every call
+            uint32_t* fw = a.flags[p] + ((size_t)x.rb * a.n_ct[p] + ct) * (16 * kGroupsPerWarp) +
+                           ew * kGroupsPerWarp + half * kGroups;
+            if constexpr (kGroups == 4)
+              *reinterpret_cast<uint4*>(fw) = make_uint4(fwords[0], fwords[1], fwords[2], fwords[3]);
+            else
+              *reinterpret_cast<uint2*>(fw) = make_uint2(fwords[0], fwords[1]);
           }
           if (half == kCols / kPass - 1) {  // this warp is done with the TMEM buffer
             tc::tc_fence_before();
@@ -851,22 +910,23 @@ cudaError_t launch_split(int n, const UpdateProblem* probs, const UpdateWorkspac
   sb.r_pad = r_pad;
   for (int base = 0; base < n; base += kMaxAux) {
     const int m = (n - base) < kMaxAux ? (n - base) : kMaxAux;
-    int64_t max_rows = 0;
+    sb.n = 2 * m;
+    sb.row_begin[0] = 0;
     for (int i = 0; i < m; ++i) {
       const UpdateProblem& pr = probs[base + i];
       sb.src[2 * i] = pr.C;
-      sb.rows[2 * i] = pr.d;
       sb.dst[2 * i] = ws[base + i].c_split;
       sb.norm[2 * i] = ws[base + i].c_norm;
+      sb.row_begin[2 * i + 1] = sb.row_begin[2 * i] + pr.d;
       sb.src[2 * i + 1] = pr.P;
-      sb.rows[2 * i + 1] = pr.k;
       sb.dst[2 * i + 1] = ws[base + i].p_split;
       sb.norm[2 * i + 1] = ws[base + i].p_norm;
-      max_rows = pr.d > max_rows ? pr.d : max_rows;
-      max_rows = pr.k > max_rows ? pr.k : max_rows;
+      sb.row_begin[2 * i + 2] = sb.row_begin[2 * i + 1] + pr.k;
     }
+    const int64_t blocks = ceil_div(sb.row_begin[2 * m], 8);
+    const int grid = (int)(blocks < 8 * (int64_t)num_sms() ? blocks : 8 * (int64_t)num_sms());
     count_launch();
-    split_rows_kernel<<<dim3((unsigned)ceil_div(max_rows, 8), (unsigned)(2 * m)), 256, 0, stream>>>(sb);
+    split_rows_kernel<<<grid, 256, 0, stream>>>(sb);
   }
   return cudaGetLastError();
 }
