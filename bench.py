@@ -49,6 +49,14 @@ def parse():
     return ap.parse_args()
 
 
+# DRAM bytes (read + write) per algorithmic byte of each phase's main kernel, from
+# one ncu capture of one Qwen3-8B block (profiles/qwen3_8b_one_block_kernels.md);
+# traffic grows with the units processed, so a full launch's traffic is this
+# ratio times its algorithmic bytes.
+TRAFFIC_PER_ALGORITHMIC_BYTE = {"project_inputs": 244.3 / 315.0, "accumulate": 268.3 / 342.4,
+                                "update_normsgd": 754.1 / 791.4}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -435,7 +443,10 @@ def main():
                         else "fallback 6.8 TB/s"),
         "bytes_per_launch": bytes_ / nl,
         "avg_launch_ms": secs / nl * 1e3,
-        "traffic": None,
+        "traffic": (TRAFFIC_PER_ALGORITHMIC_BYTE[name] * bytes_ / nl
+                    if name in TRAFFIC_PER_ALGORITHMIC_BYTE else None),
+        "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum on one Qwen3-8B block, scaled "
+                          "to a full launch by algorithmic bytes (profiles/qwen3_8b_one_block_kernels.md)",
     }
 
     # ---- end to end: inputs copied from pinned host memory every step -----
