@@ -130,71 +130,96 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
 
 // P rows [32*blockIdx.x, +32) <- scale * P_rows * Rinv (Rinv upper triangular).
 // P rows <- (P rows) X, X = R^-1 upper triangular, in place; on the final pass
-// also times the scale sqrt(k/r).  A block takes RB rows and all r columns:
-// thread t owns the 4 x 4 outputs of column quad t % r4 and row quad t / r4
-// (r4 = ceil(r/4) quads, RB = 4 * floor(256 / r4) rows).  The block's rows are
-// staged in shared memory first, so the in-place writes cannot race its reads;
-// X follows through shared memory 32 rows at a time.
+// also times the scale sqrt(k/r).  With r8 = r rounded up to 8 and co = r8/8
+// column octets, a block of 256 threads takes RB = 8 * floor(256 / co) rows and
+// all columns: thread t < RB/8 * co owns the 8 x 8 outputs of column octet
+// t % co and row octet t / co (the rest only help to stage).  The block's
+// rows are staged (transposed) in shared memory first, so the in-place writes
+// cannot race its reads; X follows 32 rows at a time.  Per row m of X a thread
+// reads 8 staged values and 8 X values (four 16-byte shared loads) for 64 FMAs.
 constexpr int kXRows = 32;
+__host__ __device__ inline int tri_rows(int r) { return 8 * (256 / ((r + 7) / 8)); }
+__host__ __device__ inline size_t tri_smem_floats(int r) {
+  const int r8 = (r + 7) / 8 * 8, rb = tri_rows(r);
+  return (size_t)r * (rb + 4) + 4 + (size_t)kXRows * r8;
+}
 __global__ void __launch_bounds__(256) tri_apply_kernel(const ProjBatch batch, int final_pass) {
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) float smem[];
   const ProjProblem& pb = batch.p[blockIdx.y];
-  const int r = batch.r, r4 = (r + 3) / 4, rq_n = 256 / r4, RB = 4 * rq_n, ld = r + 1;
-  const int xld = 4 * r4;  // X rows padded to whole quads (16-byte aligned)
-  float* S = smem;                    // RB x (r + 1)
-  float* Xs = smem + RB * ld + 3;     // kXRows x xld, 16-byte aligned below
-  Xs = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(Xs) + 15) & ~uintptr_t(15));
+  const int r = batch.r, r8 = (r + 7) / 8 * 8, co_n = r8 / 8, RB = tri_rows(r), ldt = RB + 4;
+  float* St = smem;                                   // r x (RB + 4): St[m][row]
+  float* Xs = smem + (((size_t)r * ldt + 3) & ~size_t(3));  // kXRows x r8
   const int64_t row0 = (int64_t)blockIdx.x * RB;
   if (row0 >= pb.k) return;
   const int rows = (int)((pb.k - row0) < RB ? (pb.k - row0) : RB);
   float* P = pb.P + row0 * r;
-  for (int e = threadIdx.x; e < rows * r; e += blockDim.x) S[(e / r) * ld + e % r] = P[e];
-  const int cq = threadIdx.x % r4, rq = threadIdx.x / r4;
-  const bool active = rq < rq_n;
-  const int c0 = 4 * cq, q0 = 4 * rq;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a warp reads 16 rows at a time, each coalesced; the 16 loads are issued
+  // before any store so that their latencies overlap
+  for (int mc0 = 0; mc0 < r; mc0 += 32) {
+    const int mc = mc0 + lane;
+    for (int row0w = warp; row0w < rows; row0w += 128) {
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int row = row0w + 8 * i;
+        v[i] = (row < rows && mc < r) ? P[(size_t)row * r + mc] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int row = row0w + 8 * i;
+        if (row < rows && mc < r) St[(size_t)mc * ldt + row] = v[i];
+      }
+    }
+  }
+  const int co = threadIdx.x % co_n, ro = threadIdx.x / co_n;
+  const bool active = ro < RB / 8;
+  const int c0 = 8 * co, q0 = 8 * ro;
   const float* __restrict__ X = pb.rinv;
-  float acc[4][4];
+  float acc[8][8];
 #pragma unroll
-  for (int p = 0; p < 4; ++p)
+  for (int p = 0; p < 8; ++p)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[p][q] = 0.f;
+    for (int q = 0; q < 8; ++q) acc[p][q] = 0.f;
   for (int m0 = 0; m0 < r; m0 += kXRows) {
     const int mrows = (r - m0) < kXRows ? (r - m0) : kXRows;
-    __syncthreads();  // S staged (first chunk) / the previous X chunk used
-    for (int e = threadIdx.x; e < mrows * xld; e += blockDim.x) {
-      const int mm = e / xld, c = e % xld;
-      Xs[e] = c < r ? X[(size_t)(m0 + mm) * r + c] : 0.f;
-    }
+    __syncthreads();  // St staged (first chunk) / the previous X chunk used
+    for (int mm = warp; mm < mrows; mm += 8)
+      for (int c = lane; c < r8; c += 32) Xs[mm * r8 + c] = c < r ? X[(size_t)(m0 + mm) * r + c] : 0.f;
     __syncthreads();
     if (!active) continue;
-    // X is upper triangular: rows m > c0 + 3 add nothing to these columns
-    int mend = c0 + 4 - m0;
+    // X is upper triangular: rows m > c0 + 7 add nothing to these columns
+    int mend = c0 + 8 - m0;
     if (mend > mrows) mend = mrows;
-#pragma unroll 4
+#pragma unroll 2
     for (int mm = 0; mm < mend; ++mm) {
-      const float4 x4 = *reinterpret_cast<const float4*>(Xs + mm * xld + c0);
-      const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+      const float4 sa = *reinterpret_cast<const float4*>(St + (size_t)(m0 + mm) * ldt + q0);
+      const float4 sb = *reinterpret_cast<const float4*>(St + (size_t)(m0 + mm) * ldt + q0 + 4);
+      const float4 xa = *reinterpret_cast<const float4*>(Xs + mm * r8 + c0);
+      const float4 xb = *reinterpret_cast<const float4*>(Xs + mm * r8 + c0 + 4);
+      const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const float sv = S[(q0 + p) * ld + m0 + mm];
+      for (int p = 0; p < 8; ++p)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(sv, xv[q], acc[p][q]);
-      }
+        for (int q = 0; q < 8; ++q) acc[p][q] = fmaf(sv[p], xv[q], acc[p][q]);
     }
   }
   if (!active) return;
   const float scale = final_pass ? pb.scale : 1.0f;
   const bool vec = (r & 3) == 0;
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
+  for (int p = 0; p < 8; ++p) {
     if (q0 + p >= rows) break;
     float* out = P + (size_t)(q0 + p) * r + c0;
-    if (vec) {
+    if (vec && c0 + 8 <= r) {
       *reinterpret_cast<float4*>(out) =
           make_float4(acc[p][0] * scale, acc[p][1] * scale, acc[p][2] * scale, acc[p][3] * scale);
+      *reinterpret_cast<float4*>(out + 4) =
+          make_float4(acc[p][4] * scale, acc[p][5] * scale, acc[p][6] * scale, acc[p][7] * scale);
     } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < 8; ++q)
         if (c0 + q < r) out[q] = acc[p][q] * scale;
     }
   }
@@ -236,8 +261,8 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
     gb.e[i].out = batch.p[i].gram;
   }
   const size_t chol_smem = sizeof(float) * (size_t)r * (r + 1) / 2;
-  const int r4 = (r + 3) / 4, apply_rows = 4 * (256 / r4);
-  const size_t apply_smem = sizeof(float) * ((size_t)apply_rows * (r + 1) + 3 + 4 + (size_t)kXRows * 4 * r4);
+  const int apply_rows = tri_rows(r);
+  const size_t apply_smem = sizeof(float) * tri_smem_floats(r);
   cudaError_t err = cudaFuncSetAttribute(chol_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)chol_smem);
   if (err != cudaSuccess) return err;

@@ -23,7 +23,7 @@ import torch
 
 import oracle as orc
 import rank_gradient_sketching_philox_gb300 as rgs
-from rank_gradient_sketching_philox_gb300 import binding, policy_sync, synth
+from rank_gradient_sketching_philox_gb300 import binding, diagnostics, policy_sync, synth
 
 from gpu_util import bits, from_bits, rel_fro, w_parity
 
@@ -526,3 +526,28 @@ def test_batched_calls_span_several_launches():
         _c_check(Cs[li].cpu().numpy(), C_or)
         W_or, st, _ = orc.update_normsgd(bits(W0), Cs[li].cpu().numpy(), Pn, 1e-3, 3, li, 0)
         _w_check(bits(Ws[li]), W_or)
+
+
+# --------------------------------------------------------------------------
+# reconstruction diagnostic over ranks and projection kinds
+# --------------------------------------------------------------------------
+
+def test_reconstruction_cosine_follows_closed_forms():
+    """cos(G, H) of the library's sketch against the dense gradient, for both
+    projection kinds over r in {4, 16, 64, 256}: one step matches the closed
+    form; averaging over 8 refreshed projections matches its closed form and
+    beats a fixed projection."""
+    d, k, T = 256, 1024, 256
+    Ds = [synth.normal_bf16((T, d), 1.0, 70 + m).to(DEV) for m in range(2)]
+    Xs = [synth.normal_bf16((T, k), 1.0, 80 + m).to(DEV) for m in range(2)]
+    rows = diagnostics.sweep(Ds, Xs, ranks=(4, 16, 64, 256), steps=8)
+    assert len(rows) == 16
+    by = {(row["kind"], row["r"], row["refreshed"]): row for row in rows}
+    for (kind, r, refreshed), row in by.items():
+        if not refreshed:  # one fixed projection: the single-step closed form
+            single = diagnostics.expected_cosine(
+                binding.PROJ_RADEMACHER if kind == "rademacher" else binding.PROJ_GAUSSIAN_QR, k, r, 1)
+            assert abs(row["cos"] - single) <= 0.15 * single, row
+        else:
+            assert abs(row["cos"] - row["expected_cos"]) <= 0.15 * row["expected_cos"], row
+            assert row["cos"] > by[(kind, r, False)]["cos"], row
