@@ -257,6 +257,22 @@ SKETCH_API sketch_status sketch_sample_projection_batched(sketch_proj_kind kind,
                                                           size_t ws_bytes, void* stream);
 SKETCH_API sketch_status sketch_project_inputs_batched(int n, const sketch_project_problem* problems, int64_t r,
                                                        void* ws, size_t ws_bytes, void* stream);
+/* fp32-accurate saved XP.  The same calls as sketch_project_inputs_batched and
+ * sketch_accumulate_batched, except that XP is kept to about 2^-17 relative
+ * instead of one BF16 rounding (2^-9): XP holds, per token row, the BF16 of
+ * the fp32 product in columns [0, r) and the BF16 of the remainder in columns
+ * [n_pad, n_pad + r), n_pad = r rounded up to 16; so ld_xp >= 2 * n_pad, 4
+ * bytes per value like fp32.  The accumulate call reads XP as the sum of the
+ * two halves.  This removes the XP rounding term (~1e-3 relative) from C
+ * ("Randomized Gradient Compression", "How it works": the layer saves X P; its
+ * precision is this build's choice).  Columns [r, n_pad) and [n_pad + r,
+ * 2 n_pad) are not written, and their contents do not affect C. */
+SKETCH_API sketch_status sketch_project_inputs_fp32xp_batched(int n, const sketch_project_problem* problems,
+                                                              int64_t r, void* ws, size_t ws_bytes, void* stream);
+SKETCH_API sketch_status sketch_accumulate_fp32xp_batched(int n, const sketch_accumulate_problem* problems,
+                                                          int64_t r, int overwrite, void* ws, size_t ws_bytes,
+                                                          void* stream);
+
 /* The BF16 split of projections as sketch_project_inputs uses them: with
  * n_pad = r rounded up to 16, rows [0, n_pad) of P_split hold the BF16 of P^T
  * (round to nearest even) and rows [n_pad, 2 n_pad) the BF16 of the remainder

@@ -40,7 +40,8 @@ EXPORTS = ("sketch_workspace_bytes", "sketch_sample_projection", "sketch_project
            "sketch_apply_update_normsgd_batched", "sketch_apply_update_sgd_batched",
            "sketch_apply_update_normsgd_noalloc", "sketch_noalloc_scratch_bytes",
            "sketch_read_device_errors", "sketch_kernel_launches", "sketch_projection_split_elems",
-           "sketch_split_projection_batched", "sketch_status_string",
+           "sketch_split_projection_batched", "sketch_project_inputs_fp32xp_batched",
+           "sketch_accumulate_fp32xp_batched", "sketch_status_string",
            "sketch_last_error")
 
 
@@ -100,6 +101,8 @@ _SIGS = {
     "sketch_kernel_launches": (_c.c_uint64, []),
     "sketch_projection_split_elems": (_c.c_size_t, [_i64, _i64]),
     "sketch_split_projection_batched": (_c.c_int, [_c.c_int, _vp, _i64, _vp]),
+    "sketch_project_inputs_fp32xp_batched": (_c.c_int, [_c.c_int, _vp, _i64, _vp, _c.c_size_t, _vp]),
+    "sketch_accumulate_fp32xp_batched": (_c.c_int, [_c.c_int, _vp, _i64, _c.c_int, _vp, _c.c_size_t, _vp]),
     "sketch_workspace_bytes_batched": (ctypes.c_size_t, [_c.c_int, _c.c_int, _vp, _vp, _vp, _i64]),
     "sketch_sample_projection_batched": (_c.c_int, [_c.c_int, _u64, _u32, _c.c_int, _vp, _i64, _vp, _vp,
                                                     _c.c_size_t, _vp]),
@@ -360,9 +363,7 @@ def split_projection_batched(Ps, splits=None, stream=None):
     return splits
 
 
-def project_inputs_batched(Xs, Ps, XPs, ws=None, stream=None, splits=None):
-    """XP = bf16(X P) for each problem; `splits` (from split_projection_batched
-    for these Ps) skips splitting P again."""
+def _project_batched(Xs, Ps, XPs, ws, stream, splits, fn, xp_cols):
     n = len(Xs)
     r = Ps[0].shape[1]
     probs = (ProjectProblem * n)()
@@ -370,7 +371,7 @@ def project_inputs_batched(Xs, Ps, XPs, ws=None, stream=None, splits=None):
         ld_x = _rows(X, torch.bfloat16, "X")
         ld_xp = _rows(XP, torch.bfloat16, "XP")
         _contig(P, torch.float32, "P")
-        if P.shape != (X.shape[1], r) or XP.shape[0] != X.shape[0] or XP.shape[1] < r:
+        if P.shape != (X.shape[1], r) or XP.shape[0] != X.shape[0] or XP.shape[1] < xp_cols:
             raise ValueError("shape mismatch in problem %d" % i)
         probs[i] = ProjectProblem(X.data_ptr(), X.shape[0], X.shape[1], ld_x, P.data_ptr(),
                                   XP.data_ptr(), ld_xp, splits[i].data_ptr() if splits is not None else None)
@@ -378,11 +379,17 @@ def project_inputs_batched(Xs, Ps, XPs, ws=None, stream=None, splits=None):
     nbytes = workspace_bytes_batched(OP_PROJECT_INPUTS, T=[X.shape[0] for X in Xs],
                                      k=[X.shape[1] for X in Xs], r=r)
     wsb = _workspace(nbytes, Xs[0].device, s, ws)
-    _check(lib().sketch_project_inputs_batched(n, probs, r, _ptr(wsb), nbytes, h))
+    _check(getattr(lib(), fn)(n, probs, r, _ptr(wsb), nbytes, h))
     return XPs
 
 
-def accumulate_batched(Ds, XPs, Cs, overwrite=False, ws=None, stream=None):
+def project_inputs_batched(Xs, Ps, XPs, ws=None, stream=None, splits=None):
+    """XP = bf16(X P) for each problem; `splits` (from split_projection_batched
+    for these Ps) skips splitting P again."""
+    return _project_batched(Xs, Ps, XPs, ws, stream, splits, "sketch_project_inputs_batched", Ps[0].shape[1])
+
+
+def _accumulate_batched(Ds, XPs, Cs, overwrite, ws, stream, fn, xp_cols):
     n = len(Ds)
     r = Cs[0].shape[1]
     probs = (AccumulateProblem * n)()
@@ -390,7 +397,7 @@ def accumulate_batched(Ds, XPs, Cs, overwrite=False, ws=None, stream=None):
         ld_d = _rows(D, torch.bfloat16, "D")
         ld_xp = _rows(XP, torch.bfloat16, "XP")
         _contig(C, torch.float32, "C")
-        if C.shape != (D.shape[1], r) or XP.shape[0] != D.shape[0] or XP.shape[1] < r:
+        if C.shape != (D.shape[1], r) or XP.shape[0] != D.shape[0] or XP.shape[1] < xp_cols:
             raise ValueError("shape mismatch in problem %d" % i)
         probs[i] = AccumulateProblem(D.data_ptr(), D.shape[0], D.shape[1], ld_d, XP.data_ptr(), ld_xp,
                                      C.data_ptr())
@@ -398,8 +405,30 @@ def accumulate_batched(Ds, XPs, Cs, overwrite=False, ws=None, stream=None):
     nbytes = workspace_bytes_batched(OP_ACCUMULATE, T=[D.shape[0] for D in Ds],
                                      d=[D.shape[1] for D in Ds], r=r)
     wsb = _workspace(nbytes, Ds[0].device, s, ws)
-    _check(lib().sketch_accumulate_batched(n, probs, r, 1 if overwrite else 0, _ptr(wsb), nbytes, h))
+    _check(getattr(lib(), fn)(n, probs, r, 1 if overwrite else 0, _ptr(wsb), nbytes, h))
     return Cs
+
+
+def accumulate_batched(Ds, XPs, Cs, overwrite=False, ws=None, stream=None):
+    return _accumulate_batched(Ds, XPs, Cs, overwrite, ws, stream, "sketch_accumulate_batched", Cs[0].shape[1])
+
+
+def xp_split_cols(r):
+    """Columns of the fp32-accurate XP form: a BF16 pair, 2 * round16(r)."""
+    return 2 * ((r + 15) // 16 * 16)
+
+
+def project_inputs_fp32xp_batched(Xs, Ps, XPs, ws=None, stream=None, splits=None):
+    """XP kept to ~2^-17 relative as a BF16 pair (hi in columns [0, r), lo at
+    [round16(r), round16(r) + r)); each XP is T x >= xp_split_cols(r) BF16."""
+    return _project_batched(Xs, Ps, XPs, ws, stream, splits, "sketch_project_inputs_fp32xp_batched",
+                            xp_split_cols(Ps[0].shape[1]))
+
+
+def accumulate_fp32xp_batched(Ds, XPs, Cs, overwrite=False, ws=None, stream=None):
+    """C = (0 or C) + D^T (XP_hi + XP_lo) from the fp32-accurate XP form."""
+    return _accumulate_batched(Ds, XPs, Cs, overwrite, ws, stream, "sketch_accumulate_fp32xp_batched",
+                               xp_split_cols(Cs[0].shape[1]))
 
 
 def _update_batched(normsgd, Ws, Cs, Ps, step_size, seed, layers, step, wnorm2_in, wnorm2_out,

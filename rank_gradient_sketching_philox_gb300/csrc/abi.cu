@@ -228,8 +228,11 @@ sketch_status do_sample(sketch_proj_kind kind, uint64_t seed, uint32_t step, int
   return launch_result(err, "sample_projection");
 }
 
+// XP width: r columns, or the BF16 pair of the fp32-accurate form (2 * round16(r)).
+int64_t xp_width(int64_t r, bool xp_split) { return xp_split ? 2 * ((r + 15) / 16 * 16) : r; }
+
 sketch_status do_project(int n, const sketch_project_problem* probs, int64_t r, void* ws, size_t ws_bytes,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool xp_split = false) {
   TRY(check_n(n));
   if (probs == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "problems is NULL");
   TRY(check_rank(r));
@@ -237,16 +240,17 @@ sketch_status do_project(int n, const sketch_project_problem* probs, int64_t r, 
   std::vector<rgs::ProjectProblem> v((size_t)n);
   for (int i = 0; i < n; ++i) {
     TRY(check_project(probs[i], r));
+    TRY(check_ld("ld_xp", probs[i].ld_xp, xp_width(r, xp_split)));
     need += rgs::project_workspace_bytes(probs[i].T, probs[i].k, r);
     v[i] = rgs::ProjectProblem{probs[i].X, probs[i].T, probs[i].k, probs[i].ld_x, probs[i].P, probs[i].XP,
                                probs[i].ld_xp, probs[i].P_split};
   }
   TRY(check_ws(ws, ws_bytes, need));
-  return launch_result(rgs::launch_project_inputs(n, v.data(), (int)r, ws, s), "project_inputs");
+  return launch_result(rgs::launch_project_inputs(n, v.data(), (int)r, ws, s, xp_split), "project_inputs");
 }
 
 sketch_status do_accumulate(int n, const sketch_accumulate_problem* probs, int64_t r, int overwrite, void* ws,
-                            size_t ws_bytes, cudaStream_t s) {
+                            size_t ws_bytes, cudaStream_t s, bool xp_split = false) {
   TRY(check_n(n));
   if (probs == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "problems is NULL");
   TRY(check_rank(r));
@@ -255,12 +259,13 @@ sketch_status do_accumulate(int n, const sketch_accumulate_problem* probs, int64
   std::vector<rgs::AccumulateProblem> v((size_t)n);
   for (int i = 0; i < n; ++i) {
     TRY(check_accumulate(probs[i], r));
+    TRY(check_ld("ld_xp", probs[i].ld_xp, xp_width(r, xp_split)));
     need += rgs::accumulate_workspace_bytes(probs[i].T, probs[i].d, r);
     v[i] = rgs::AccumulateProblem{probs[i].D, probs[i].T, probs[i].d, probs[i].ld_d, probs[i].XP, probs[i].ld_xp,
                                   probs[i].C};
   }
   TRY(check_ws(ws, ws_bytes, need));
-  return launch_result(rgs::launch_accumulate(n, v.data(), (int)r, overwrite, s), "accumulate");
+  return launch_result(rgs::launch_accumulate(n, v.data(), (int)r, overwrite, s, xp_split), "accumulate");
 }
 
 sketch_status do_update(bool normsgd, int n, const sketch_update_problem* probs, int64_t r, float step_size,
@@ -348,6 +353,16 @@ sketch_status sketch_project_inputs(const uint16_t* X, int64_t T, int64_t k, int
 sketch_status sketch_project_inputs_batched(int n, const sketch_project_problem* problems, int64_t r, void* ws,
                                             size_t ws_bytes, void* stream) {
   return do_project(n, problems, r, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+sketch_status sketch_project_inputs_fp32xp_batched(int n, const sketch_project_problem* problems, int64_t r,
+                                                   void* ws, size_t ws_bytes, void* stream) {
+  return do_project(n, problems, r, ws, ws_bytes, static_cast<cudaStream_t>(stream), true);
+}
+
+sketch_status sketch_accumulate_fp32xp_batched(int n, const sketch_accumulate_problem* problems, int64_t r,
+                                               int overwrite, void* ws, size_t ws_bytes, void* stream) {
+  return do_accumulate(n, problems, r, overwrite, ws, ws_bytes, static_cast<cudaStream_t>(stream), true);
 }
 
 size_t sketch_projection_split_elems(int64_t k, int64_t r) {

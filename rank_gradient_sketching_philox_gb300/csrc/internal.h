@@ -104,7 +104,10 @@ size_t project_workspace_bytes(int64_t T, int64_t k, int64_t r);
 cudaError_t launch_split_projection(int n, const float* const* P, const int64_t* k, uint16_t* const* out, int r,
                                     cudaStream_t stream);
 // Workspace: the problems' regions of project_workspace_bytes, back to back.
-cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, void* ws, cudaStream_t stream);
+// xp_split: write XP as a BF16 pair (hi in columns [0, r), lo = bf16(XP - hi) at
+// [n_pad, n_pad + r), n_pad = r rounded up to 16) instead of one BF16 rounding.
+cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, void* ws, cudaStream_t stream,
+                                  bool xp_split = false);
 
 // ---- (c) sketch accumulation ----------------------------------------------
 struct AccumulateProblem {
@@ -115,7 +118,9 @@ struct AccumulateProblem {
   float* C;           // d x r fp32
 };
 size_t accumulate_workspace_bytes(int64_t T, int64_t d, int64_t r);
-cudaError_t launch_accumulate(int n, const AccumulateProblem* probs, int r, int overwrite, cudaStream_t stream);
+// xp_split: XP is the BF16 pair launch_project_inputs writes with xp_split.
+cudaError_t launch_accumulate(int n, const AccumulateProblem* probs, int r, int overwrite, cudaStream_t stream,
+                              bool xp_split = false);
 
 // ---- (d) rebuild + update -------------------------------------------------
 struct UpdateProblem {

@@ -55,7 +55,9 @@ struct SkinnyBatch {
   uint32_t stage_bytes;            // a_bytes + NB * b_bytes
   int red_stride;                  // floats per row of the fp32 reduction tile
   uint32_t tmem_cols;              // power of two >= max(32, n_pad)
-  int out_mode;                    // 0: BF16 round-to-nearest store; 1: fp32 store; 2: fp32 add
+  int out_mode;                    // 0: BF16 round-to-nearest store; 1: fp32 store; 2: fp32 add;
+                                   // 3: BF16 split store, hi in columns [0, N), lo at [n_pad, n_pad + N)
+  int b_col_off;                   // MN-major B: column offset of B operand nb is nb * b_col_off
   int* err;
 };
 
@@ -126,7 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_gemm_kernel(const __grid_c
       for (int nb = 0; nb < NB; ++nb) {
         uint8_t* bt = st + a.a_bytes + nb * a.b_bytes;
         if (B_MN) {  // XP: [64 tokens][64 rank columns] per box
-          for (int j = 0; j * 64 < a.n_pad; ++j) tc::tma_load_2d(bt + j * 8192, tmB, &full_bar[s], j * 64, kc);
+          for (int j = 0; j * 64 < a.n_pad; ++j)
+            tc::tma_load_2d(bt + j * 8192, tmB, &full_bar[s], nb * a.b_col_off + j * 64, kc);
         } else {  // P^T split: [n_pad rank rows][64 k]; high part in rows [0, n_pad), low in [n_pad, 2 n_pad)
           tc::tma_load_2d(bt, tmB, &full_bar[s], kc, nb * a.n_pad);
         }
@@ -208,6 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_gemm_kernel(const __grid_c
     if (a.out_mode == 0) {
       uint16_t* o = static_cast<uint16_t*>(a.out[p]) + grow * a.ld_out[p] + c;
       for (int t = 0; t < 4 && c + t < a.N; ++t) o[t] = __bfloat16_as_ushort(__float2bfloat16_rn(vals[t]));
+    } else if (a.out_mode == 3) {
+      uint16_t* o = static_cast<uint16_t*>(a.out[p]) + grow * a.ld_out[p] + c;
+      for (int t = 0; t < 4 && c + t < a.N; ++t) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(vals[t]);
+        o[t] = __bfloat16_as_ushort(h);
+        o[a.n_pad + t] = __bfloat16_as_ushort(__float2bfloat16_rn(vals[t] - __bfloat162float(h)));
+      }
     } else {
       float* o = static_cast<float*>(a.out[p]) + grow * a.ld_out[p] + c;
       for (int t = 0; t < 4 && c + t < a.N; ++t) o[t] = (a.out_mode == 2) ? o[t] + vals[t] : vals[t];
@@ -357,7 +367,8 @@ cudaError_t launch_split_projection(int n, const float* const* P, const int64_t*
   return cudaGetLastError();
 }
 
-cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, void* ws, cudaStream_t stream) {
+cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, void* ws, cudaStream_t stream,
+                                  bool xp_split) {
   const int n_pad = round16(r);
   int* errw = nullptr;
   cudaError_t err = device_error_word(&errw);
@@ -405,7 +416,8 @@ cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, voi
     a.n_pad = n_pad;
     a.a_bytes = 128 * kChunk * 2;
     a.b_bytes = (uint32_t)n_pad * kChunk * 2;
-    a.out_mode = 0;
+    a.out_mode = xp_split ? 3 : 0;
+    a.b_col_off = 0;
     a.err = errw;
     err = launch_skinny<false, false, 2>(a, stream);
     if (err != cudaSuccess) return err;
@@ -415,7 +427,8 @@ cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, voi
 
 size_t accumulate_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 
-cudaError_t launch_accumulate(int n, const AccumulateProblem* probs, int r, int overwrite, cudaStream_t stream) {
+cudaError_t launch_accumulate(int n, const AccumulateProblem* probs, int r, int overwrite, cudaStream_t stream,
+                              bool xp_split) {
   const int n_pad = round16(r);
   int* errw = nullptr;
   cudaError_t err = device_error_word(&errw);
@@ -428,7 +441,8 @@ cudaError_t launch_accumulate(int n, const AccumulateProblem* probs, int r, int 
       const AccumulateProblem& pr = probs[base + i];
       err = make_tmap_bf16_2d(&a.tmA[i], pr.D, (uint64_t)pr.d, (uint64_t)pr.T, (uint64_t)pr.ld_d * 2, 64, 64);
       if (err == cudaSuccess)
-        err = make_tmap_bf16_2d(&a.tmB[i], pr.XP, (uint64_t)r, (uint64_t)pr.T, (uint64_t)pr.ld_xp * 2, 64, 64);
+        err = make_tmap_bf16_2d(&a.tmB[i], pr.XP, (uint64_t)(xp_split ? 2 * n_pad : r), (uint64_t)pr.T,
+                                (uint64_t)pr.ld_xp * 2, 64, 64);
       if (err != cudaSuccess) return err;
       a.out[i] = pr.C;
       a.ld_out[i] = r;
@@ -443,7 +457,13 @@ cudaError_t launch_accumulate(int n, const AccumulateProblem* probs, int r, int 
     a.b_bytes = (uint32_t)((n_pad + 63) / 64) * 64 * kChunk * 2;
     a.out_mode = overwrite ? 1 : 2;
     a.err = errw;
-    err = launch_skinny<true, true, 1>(a, stream);
+    if (xp_split) {  // D^T XP_hi + D^T XP_lo, both into the same accumulator
+      a.b_col_off = n_pad;
+      err = launch_skinny<true, true, 2>(a, stream);
+    } else {
+      a.b_col_off = 0;
+      err = launch_skinny<true, true, 1>(a, stream);
+    }
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;

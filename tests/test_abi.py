@@ -154,3 +154,15 @@ def test_policy_sync_payload_is_the_factor_and_seed():
     C = torch.arange(12, dtype=torch.float32).view(4, 3)
     assert torch.equal(policy_sync.payload(C, 0.5), C * 0.5)
     assert policy_sync.payload_bytes(4096, 64) == 4 * 4096 * 64 + 16       # vs 2*4096*4096 of BF16 W
+
+
+def test_fp32_xp_needs_room_for_the_pair(lib):
+    """The fp32-accurate XP form needs ld_xp >= 2 * round16(r)."""
+    before = binding.kernel_launches()
+    pp = (binding.ProjectProblem * 1)(binding.ProjectProblem(1 << 20, 16, 64, 64, 1 << 21, 1 << 22, 24, None))
+    assert _call("sketch_project_inputs_fp32xp_batched", 1, pp, 8, NULL, 0, NULL) == binding.ERR_INVALID_ARG
+    assert "ld_xp" in binding.lib().sketch_last_error().decode()
+    ap = (binding.AccumulateProblem * 1)(binding.AccumulateProblem(1 << 20, 16, 64, 64, 1 << 21, 24, 1 << 22))
+    assert _call("sketch_accumulate_fp32xp_batched", 1, ap, 8, 1, NULL, 0, NULL) == binding.ERR_INVALID_ARG
+    assert binding.kernel_launches() == before
+    assert binding.xp_split_cols(64) == 128 and binding.xp_split_cols(20) == 64

@@ -253,6 +253,35 @@ def test_accumulate_full_size_sampled_rows():
     _c_check(C.cpu().numpy()[rows], ref)
 
 
+@pytest.mark.parametrize("T,d,k,r", [(300, 136, 512, 16), (256, 256, 1024, 64), (130, 72, 256, 20),
+                                     (64, 128, 1024, 256)])
+def test_fp32_xp_removes_the_xp_rounding_from_c(T, d, k, r):
+    """The fp32-accurate XP (a BF16 pair) is within 2^-16 of the exact X P, and
+    the sketch built from it is within 5e-5 of the exact D^T (X P): the BF16
+    rounding of XP (about 1e-3 in C) is gone."""
+    X = synth.normal_bf16((T, k), 1.0, 90 + T)
+    D = synth.normal_bf16((T, d), 1e-3, 91 + T)
+    P = orc.sample_qr(6, 1, 0, k, r) if 4 * r <= k else orc.sample_rademacher(6, 1, 0, k, r)
+    n_pad = (r + 15) // 16 * 16
+    XP2 = _padded_bf16(T, rgs.xp_split_cols(r))
+    rgs.project_inputs_fp32xp_batched([X.to(DEV)], [torch.from_numpy(P).to(DEV)], [XP2])
+    got = (XP2[:, :r].float() + XP2[:, n_pad:n_pad + r].float()).cpu().numpy().astype(np.float64)
+    exact = orc.project_inputs_exact(bits(X), P)
+    rms = math.sqrt(float(np.mean(exact * exact)))
+    assert np.all(np.abs(got - exact) <= 2.0 ** -16 * np.abs(exact) + 1e-5 * rms)
+    C = torch.full((d, r), float("nan"), dtype=torch.float32, device=DEV)
+    rgs.accumulate_fp32xp_batched([D.to(DEV)], [XP2], [C], overwrite=True)
+    C_exact = orc.accumulate_exact(bits(D), exact, np.zeros((d, r)))
+    err32 = rel_fro(C.cpu().numpy(), C_exact)
+    assert err32 <= 5e-5
+    # the BF16-XP path on the same inputs, for scale
+    XP1 = _padded_bf16(T, r)
+    rgs.project_inputs(X.to(DEV), torch.from_numpy(P).to(DEV), XP1)
+    C1 = torch.empty(d, r, dtype=torch.float32, device=DEV)
+    rgs.accumulate(D.to(DEV), XP1, C1, overwrite=True)
+    assert err32 * 10 <= rel_fro(C1.cpu().numpy(), C_exact)
+
+
 # --------------------------------------------------------------------------
 # (d) updates
 # --------------------------------------------------------------------------
