@@ -220,7 +220,6 @@ struct UpdBatch {
   // ew * (NCOLS/32) + g holds bit `lane` for row rb*128 + (ew&3)*32 + lane,
   // columns ct*NCOLS + (ew>>2)*(NCOLS/4) + 8g..+7 (ew = epilogue warp)
   uint32_t* flags[kMaxUpd];
-  int64_t flag_word_begin[kMaxUpd + 1];  // prefix over the batch (fixup kernel)
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -259,6 +258,72 @@ __device__ __forceinline__ Unit decode_unit(const UpdBatch& a, int u) {
 
 __device__ __forceinline__ bool layer_skipped(const UpdBatch& a, int p) {
   return a.status_in[p] != nullptr && *a.status_in[p] != 0;
+}
+
+// One careful group, warp-wide: W_new of the 8 elements (i, j..j+7) of
+// problem p from their original W, with H_i,j+t computed by the compensated
+// dot product (Dot2 of the same paper; lanes 4t..4t+3 take column t, every
+// fourth term each, merged by TwoSum), v = fmaf(-s, fl32(H), w) and the
+// group's Philox block.  The dot product is as accurate as one carried in
+// twice fp32 precision and then rounded, so it is fl32 of the exact H except
+// when H lies within ~2^-40 of its size of an fp32 rounding boundary.  All
+// fp32: this GPU's FP64 rate is far too low for the purpose.
+__device__ __forceinline__ void careful_group_warp(const UpdBatch& a, int p, int i, int j) {
+  const int lane = threadIdx.x & 31, t = lane >> 2, q = lane & 3;
+  const int r = a.r;
+  const float* crow = a.C[p] + (int64_t)i * r;
+  const float* prow = a.P[p] + (int64_t)(j + t) * r;
+  uint16_t* wp = a.W[p] + (int64_t)i * a.ld_w[p] + j + t;
+  const uint32_t w16 = *wp;  // the original: the update kernel left the group alone
+  float hi = 0.f, lo = 0.f;
+  auto term = [&](float c, float pv) {
+    const float m = __fmul_rn(c, pv);
+    float sum, err;
+    two_sum(hi, m, sum, err);
+    hi = sum;
+    lo = __fadd_rn(lo, __fadd_rn(err, __fmaf_rn(c, pv, -m)));
+  };
+  // the terms l = q, q+4, ... of this lane, sixteen loads of C and P at a
+  // time issued together (one round trip per 64 terms of the row)
+  int l = q;
+  for (; l + 60 < r; l += 64) {
+    float cv[16], pv[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      cv[m] = crow[l + 4 * m];
+      pv[m] = prow[l + 4 * m];
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) term(cv[m], pv[m]);
+  }
+  if (l < r) {
+    float cv[16], pv[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const bool in = l + 4 * m < r;
+      cv[m] = in ? crow[l + 4 * m] : 0.f;
+      pv[m] = in ? prow[l + 4 * m] : 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) term(cv[m], pv[m]);  // zero terms change nothing
+  }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, o), olo = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+    float sum, err;
+    two_sum(hi, ohi, sum, err);
+    hi = sum;
+    lo = __fadd_rn(lo, __fadd_rn(olo, err));
+  }
+  const float h = __fadd_rn(hi, lo);
+  const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
+  const uint32_t blk = (uint32_t)i * ((uint32_t)a.k[p] >> 3) + ((uint32_t)j >> 3);  // element index / 8
+  const Philox4 rnd = philox4x32_10_rk(blk, a.step, a.layer[p], kTagSR, a.rk0, a.rk1);
+  const uint32_t word = (t >> 1) == 0 ? rnd.w0 : (t >> 1) == 1 ? rnd.w1 : (t >> 1) == 2 ? rnd.w2 : rnd.w3;
+  const float v = fmaf(-s, h, __uint_as_float(w16 << 16));
+  const uint32_t o = sr_bf16_bits(v, (t & 1) ? (word >> 16) : (word & 0xFFFFu));
+  __syncwarp();
+  if (q == 0) *wp = (uint16_t)o;
 }
 
 // Persistent rebuild + update.  Warp 0 (one lane) streams, with TMA, the C row
@@ -446,6 +511,8 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       }
     }
     tc::bulk_wait_all();  // the writes are done before the CTA exits
+    // ... and visible to the generic loads of the careful-group pass below
+    asm volatile("fence.proxy.async.global;" ::: "memory");
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------
     const int ew = warp - 4;
@@ -580,26 +647,19 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
                                          fmin_nan(av[6], av[7]));
             const bool ok = live && row_ok && j0 + col < k;
             const bool flag = ok && (!thr_ok || !(gmin > thr2));  // small value or NaN
-            // Careful path (rare, warp-uniform): each element of a flagged group
-            // whose |v| is below the threshold (or NaN) is queued as {p, i, j, W
-            // bits} and redone exactly by the fixup kernel after this kernel's
-            // stores; when the CTA's queue is full the thread does it at once.
-            // The norm sum keeps the tensor-core value of a queued element
-            // (below the threshold: far too small to matter), except that a NaN
-            // makes it NaN.
             // Careful path: a flagged group keeps its original W here and is
             // marked in the flag bitmap (the word of the whole warp, written on
-            // every call); the fixup kernel redoes its 8 elements exactly from
-            // the original W after this kernel's stores.  The norm sum keeps the
-            // tensor-core values of the group (they differ from the exact ones
-            // by at most one BF16 step, or are below the threshold), except that
-            // a NaN makes it NaN.
+            // every call); the careful-group pass at the end of this kernel
+            // redoes its 8 elements exactly from the original W, once the
+            // tiles are stored.  The norm sum keeps the tensor-core values of
+            // the group (they differ from the exact ones by at most one BF16
+            // step, or are below the threshold), except that a NaN makes it NaN.
             fwords[g] = __ballot_sync(0xFFFFFFFFu, flag);
             if (flag) {
               if (need_norm && gmin != gmin) sq = __int_as_float(0x7FC00000);
             }
             if (live) *reinterpret_cast<uint4*>(sp) = make_uint4(wout[0], wout[1], wout[2], wout[3]);
-            if (flag) *reinterpret_cast<uint4*>(sp) = raw;  // rare: the fixup kernel needs the original
+            if (flag) *reinterpret_cast<uint4*>(sp) = raw;  // rare: the careful pass needs the original
             if (need_norm && ok) {
               float gs = 0.f;
 #pragma unroll
@@ -667,114 +727,36 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
-}
+  if (abort_flag) return;
 
-// One careful group, warp-wide: W_new of the 8 elements (i, j..j+7) of
-// problem p from their original W, with H_i,j+t computed by the compensated
-// dot product (Dot2 of the same paper; lanes 4t..4t+3 take column t, every
-// fourth term each, merged by TwoSum), v = fmaf(-s, fl32(H), w) and the
-// group's Philox block.  The dot product is as accurate as one carried in
-// twice fp32 precision and then rounded, so it is fl32 of the exact H except
-// when H lies within ~2^-40 of its size of an fp32 rounding boundary.  All
-// fp32: this GPU's FP64 rate is far too low for the purpose.
-__device__ __forceinline__ void careful_group_warp(const UpdBatch& a, int p, int i, int j) {
-  const int lane = threadIdx.x & 31, t = lane >> 2, q = lane & 3;
-  const int r = a.r;
-  const float* crow = a.C[p] + (int64_t)i * r;
-  const float* prow = a.P[p] + (int64_t)(j + t) * r;
-  uint16_t* wp = a.W[p] + (int64_t)i * a.ld_w[p] + j + t;
-  const uint32_t w16 = *wp;  // the original: the update kernel left the group alone
-  float hi = 0.f, lo = 0.f;
-  auto term = [&](float c, float pv) {
-    const float m = __fmul_rn(c, pv);
-    float sum, err;
-    two_sum(hi, m, sum, err);
-    hi = sum;
-    lo = __fadd_rn(lo, __fadd_rn(err, __fmaf_rn(c, pv, -m)));
-  };
-  // the terms l = q, q+4, ... of this lane, sixteen loads of C and P at a
-  // time issued together (one round trip per 64 terms of the row)
-  int l = q;
-  for (; l + 60 < r; l += 64) {
-    float cv[16], pv[16];
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      cv[m] = crow[l + 4 * m];
-      pv[m] = prow[l + 4 * m];
-    }
-#pragma unroll
-    for (int m = 0; m < 16; ++m) term(cv[m], pv[m]);
-  }
-  if (l < r) {
-    float cv[16], pv[16];
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const bool in = l + 4 * m < r;
-      cv[m] = in ? crow[l + 4 * m] : 0.f;
-      pv[m] = in ? prow[l + 4 * m] : 0.f;
-    }
-#pragma unroll
-    for (int m = 0; m < 16; ++m) term(cv[m], pv[m]);  // zero terms change nothing
-  }
-#pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, o), olo = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
-    float sum, err;
-    two_sum(hi, ohi, sum, err);
-    hi = sum;
-    lo = __fadd_rn(lo, __fadd_rn(olo, err));
-  }
-  const float h = __fadd_rn(hi, lo);
-  const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
-  const uint32_t blk = (uint32_t)i * ((uint32_t)a.k[p] >> 3) + ((uint32_t)j >> 3);  // element index / 8
-  const Philox4 rnd = philox4x32_10_rk(blk, a.step, a.layer[p], kTagSR, a.rk0, a.rk1);
-  const uint32_t word = (t >> 1) == 0 ? rnd.w0 : (t >> 1) == 1 ? rnd.w1 : (t >> 1) == 2 ? rnd.w2 : rnd.w3;
-  const float v = fmaf(-s, h, __uint_as_float(w16 << 16));
-  const uint32_t o = sr_bf16_bits(v, (t & 1) ? (word >> 16) : (word & 0xFFFFu));
-  __syncwarp();
-  if (q == 0) *wp = (uint16_t)o;
-}
-
-// The careful groups the update kernel flagged.  Each warp scans 32 flag words
-// at a time (one per lane) and does every group whose bit is set, warp-wide;
-// launched right after the update kernel on the same stream, so every store
-// of the update is ordered before these.  Kept out of the update kernel: the
-// code would cost the main loop registers.
-template <int NCOLS>
-__global__ void __launch_bounds__(512) care_fixup_kernel(const __grid_constant__ UpdBatch a) {
-  constexpr int kGroupsPerWarp = NCOLS / 32, kWordsPerTile = 16 * kGroupsPerWarp;
-  const int lane = threadIdx.x & 31;
-  const int64_t total = a.flag_word_begin[a.n];
-  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  int p = 0;  // each lane's problem; its words only move forward
-  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32; base < total;
-       base += warps * 32) {
-    const int64_t w = base + lane;
-    uint32_t bits = 0;
-    if (w < total) {
-      while (p + 1 < a.n && a.flag_word_begin[p + 1] <= w) ++p;
-      if (!layer_skipped(a, p)) bits = a.flags[p][w - a.flag_word_begin[p]];
-    }
-    uint32_t pending = __ballot_sync(0xFFFFFFFFu, bits != 0u);
-    while (pending) {
-      const int src = __ffs(pending) - 1;
-      pending &= pending - 1;
-      const int ps = __shfl_sync(0xFFFFFFFFu, p, src);
-      uint32_t b = __shfl_sync(0xFFFFFFFFu, bits, src);
-      // a layer has fewer than 2^29 flag words (d*k < 2^35): 32-bit from here
-      const uint32_t lw = (uint32_t)(base + src - a.flag_word_begin[ps]);
-      const uint32_t tile = lw / kWordsPerTile, wt = lw % kWordsPerTile;
-      const int ew = (int)(wt / kGroupsPerWarp), gw = (int)(wt % kGroupsPerWarp);
-      const uint32_t nct = (uint32_t)a.n_ct[ps];
-      const int rb = (int)(tile / nct), ct = (int)(tile % nct);
-      const int j = ct * NCOLS + (ew >> 2) * (NCOLS / 4) + 8 * gw;
-      if (j + 8 > a.k[ps]) continue;  // never flagged (a guard against a corrupted bitmap)
-      while (b) {
-        const int row = __ffs(b) - 1;
-        b &= b - 1;
-        const int i = rb * 128 + (ew & 3) * 32 + row;
-        if (i >= a.d[ps]) break;  // never flagged, as above
-        careful_group_warp(a, ps, i, j);
+  // Careful groups of this CTA's tiles: each flagged group still holds its
+  // original W (the stage kept it and the TMA stores above have completed), so
+  // it is redone exactly here, warp-wide, the CTA's warps taking tiles in turn.
+  constexpr int kWarps = kUpdThreads / 32;
+  constexpr int kGroupsPerWarpT = NCOLS / 32, kWordsPerTile = 16 * kGroupsPerWarpT;
+  int tile_seq = 0;
+  for (int u = u_begin; u < u_end; ++u) {
+    const Unit x = decode_unit(a, u);
+    if (layer_skipped(a, x.p)) continue;
+    for (int ct = x.ct0; ct < x.ct1; ++ct, ++tile_seq) {
+      if (tile_seq % kWarps != warp) continue;
+      const uint32_t* fw = a.flags[x.p] + ((size_t)x.rb * a.n_ct[x.p] + ct) * kWordsPerTile;
+      for (int w0 = 0; w0 < kWordsPerTile; w0 += 32) {
+        const uint32_t bits = (w0 + lane < kWordsPerTile) ? fw[w0 + lane] : 0u;
+        uint32_t pending = __ballot_sync(0xFFFFFFFFu, bits != 0u);
+        while (pending) {
+          const int src = __ffs(pending) - 1;
+          pending &= pending - 1;
+          uint32_t b = __shfl_sync(0xFFFFFFFFu, bits, src);
+          const int wt = w0 + src, ew = wt / kGroupsPerWarpT, gw = wt % kGroupsPerWarpT;
+          const int j = ct * NCOLS + (ew >> 2) * (NCOLS / 4) + 8 * gw;
+          while (b) {
+            const int row = __ffs(b) - 1;
+            b &= b - 1;
+            const int i = x.rb * 128 + (ew & 3) * 32 + row;
+            careful_group_warp(a, x.p, i, j);
+          }
+        }
       }
     }
   }
@@ -836,7 +818,6 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
     if (ut < 4) ut = 4;
     if (ut > 64) ut = 64;
     a.unit_tiles = (int)ut;
-    a.flag_word_begin[0] = 0;
     a.unit_begin[0] = 0;
     for (int i = 0; i < m; ++i) {
       const UpdateProblem& pr = probs[base + i];
@@ -864,7 +845,6 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       a.status_out[i] = normsgd ? nullptr : pr.dev_status;
       a.unit_partials[i] = w.wnew_partials;
       a.flags[i] = w.flags;
-      a.flag_word_begin[i + 1] = a.flag_word_begin[i] + flag_words(pr.d, pr.k, r);
       a.ticket[i] = w.ticket;
       a.wnorm2_out[i] = normsgd ? pr.wnorm2_out : nullptr;
     }
@@ -895,8 +875,6 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
     }
     count_launch();
     update_persistent_kernel<NCOLS><<<grid, kUpdThreads, smem, stream>>>(a);
-    count_launch();
-    care_fixup_kernel<NCOLS><<<2 * nsm, 512, 0, stream>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
