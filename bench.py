@@ -408,12 +408,12 @@ def main():
 
     # launches of each phase, counted by the library; the dominant kernel of a
     # phase is its skinny GEMM (projection, accumulation) or the persistent
-    # rebuild+update kernel (one per 40 layers)
+    # rebuild+update kernel (one per 56 layers)
     ceil = lambda a, b: -(-a // b)
     n_sample = phase_launches["sample"]
     n_proj = phase_launches["project"]        # skinny GEMM launches (P split once per step)
     n_acc = phase_launches["accumulate"]
-    n_upd = ceil(L, 40)
+    n_upd = ceil(L, 56)  # layers per rebuild+update launch
     n_upd_aux = phase_launches["update"] - n_upd
     components = {
         "sample_projection": {"ms_per_step": t_sample * 1e3, "launches": n_sample},

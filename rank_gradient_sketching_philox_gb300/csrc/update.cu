@@ -20,7 +20,7 @@
 namespace rgs {
 namespace {
 
-constexpr int kMaxUpd = 40;     // layers per rebuild+update launch (kernel parameter table)
+constexpr int kMaxUpd = 56;     // layers per rebuild+update launch (kernel parameter table, < 32 KB)
 constexpr int kMaxCtas = 256;   // persistent CTAs per launch (one per SM)
 constexpr int kMaxAux = 128;    // layers per norm / split launch
 
@@ -221,6 +221,9 @@ struct UpdBatch {
   // columns ct*NCOLS + (ew>>2)*(NCOLS/4) + 8g..+7 (ew = epilogue warp)
   uint32_t* flags[kMaxUpd];
 };
+
+// kernel parameters are limited to 32764 bytes
+static_assert(sizeof(UpdBatch) <= 32764, "UpdBatch exceeds the kernel parameter limit");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));

@@ -164,14 +164,15 @@ def test_project_inputs_strided_rows_leave_padding():
     assert torch.all(XP_full[:, r:] == 7.0)
 
 
-def test_project_inputs_full_size_sampled_tokens():
-    """4096 tokens x k=4096 -> r=64 (the LoGRA worked example's shape), QR P;
-    compared on 64 sampled tokens."""
-    T, k, r = 4096, 4096, 64
+@pytest.mark.parametrize("T,k,r,kind", [(4096, 4096, 64, 1), (16384, 8192, 256, 1), (16384, 8192, 4, 0)])
+def test_project_inputs_full_size_sampled_tokens(T, k, r, kind):
+    """4096 tokens x k=4096 -> r=64 (the LoGRA worked example's shape, QR P)
+    and one 16384-token response of the long-response sweep (k=8192, r=256
+    with QR P, r=4 with Rademacher P); compared on 64 sampled tokens."""
     X = synth.layer_x(T, k, 0, 0, device=DEV)
     P = torch.empty(k, r, dtype=torch.float32, device=DEV)
-    rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 0, 0, 0, P)
-    XP = torch.empty(T, r, dtype=torch.bfloat16, device=DEV)
+    rgs.sample_projection(kind, 0, 0, 0, P)
+    XP = _padded_bf16(T, r)
     rgs.project_inputs(X, P, XP)
     rows = np.random.default_rng(0).choice(T, 64, replace=False)
     ref = orc.project_inputs(bits(X[rows]), P.cpu().numpy())
@@ -240,14 +241,17 @@ def test_chained_sketch_matches_oracle_chain():
         assert rel_fro(H, H_or) < 2e-3
 
 
-def test_accumulate_full_size_sampled_rows():
-    """d=12288 rows (the 8B stack's gate/up), 4096 tokens, r=64, heavy-tailed D;
-    64 sampled rows of C computed by the oracle."""
-    T, d, r = 4096, 12288, 64
+@pytest.mark.parametrize("T,d,r", [(4096, 12288, 64), (16384, 28672, 256), (16384, 8192, 4)])
+def test_accumulate_full_size_sampled_rows(T, d, r):
+    """d=12288 rows (the 8B stack's gate/up), 4096 tokens, r=64, and one
+    16384-token response of the long-response sweep (d=28672 at r=256, d=8192
+    at r=4), heavy-tailed D; 64 sampled rows of C computed by the oracle."""
     D = synth.layer_d(T, d, 5, 0, device=DEV, heavy_tail=True)
     XPb = orc.bf16_from_double(np.random.default_rng(3).standard_normal((T, r)) * 8)
+    XP = _padded_bf16(T, r)
+    XP.copy_(from_bits(XPb, DEV))
     C = torch.empty(d, r, dtype=torch.float32, device=DEV)
-    rgs.accumulate(D, from_bits(XPb, DEV), C, overwrite=True)
+    rgs.accumulate(D, XP, C, overwrite=True)
     rows = np.sort(np.random.default_rng(1).choice(d, 64, replace=False))
     ref = orc.accumulate(bits(D[:, rows]), XPb, np.zeros((64, r), np.float32), overwrite=True)
     _c_check(C.cpu().numpy()[rows], ref)
