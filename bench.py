@@ -383,6 +383,9 @@ def main():
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         l0 = rgs.kernel_launches()
+        # the GPU first spins ~10 ms, so that the host's launch work for the phase
+        # is queued before the start event and the phase is timed on the device
+        torch.cuda._sleep(20_000_000)
         a.record(stream)
         fn()
         b.record(stream)

@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
                     tc::mbar_wait(&tfull_bar[b], (it >> 1) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
         live = __all_sync(0xFFFFFFFFu, live);
         tc::tc_fence_after();
-        uint8_t* s_w = s_w0 + (size_t)sw * a.w_bytes;
+        const uint32_t s_w32 = tc::smem_u32(s_w0) + (uint32_t)sw * a.w_bytes;
         for (int o = 16; o > 0; o >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
         // The exactness test compares v^2 with thr^2 (multiplies on the idle FMA
         // pipe instead of absolute values on the busy ALU pipe).  Where thr^2
@@ -620,8 +620,8 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
               tc::tmem_wait_ld_regs<16>(h);
             }
             const int col = col32 + 8 * g;
-            uint8_t* sp = s_w + stage_off[half * kGroups + g];
-            const uint4 raw = *reinterpret_cast<const uint4*>(sp);
+            const uint32_t sp = s_w32 + stage_off[half * kGroups + g];
+            const uint4 raw = tc::lds128(sp);
             const uint32_t win[4] = {raw.x, raw.y, raw.z, raw.w};
             const uint32_t* rwg = rw[g];
             uint32_t wout[4];
@@ -661,8 +661,8 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
             if (flag) {
               if (need_norm && gmin != gmin) sq = __int_as_float(0x7FC00000);
             }
-            if (live) *reinterpret_cast<uint4*>(sp) = make_uint4(wout[0], wout[1], wout[2], wout[3]);
-            if (flag) *reinterpret_cast<uint4*>(sp) = raw;  // rare: the careful pass needs the original
+            if (live) tc::sts128(sp, make_uint4(wout[0], wout[1], wout[2], wout[3]));
+            if (flag) tc::sts128(sp, raw);  // rare: the careful pass needs the original
             if (need_norm && ok) {
               float gs = 0.f;
 #pragma unroll
