@@ -62,6 +62,48 @@ __device__ __forceinline__ Philox4 philox4x32_10_rk(uint32_t c0, uint32_t c1, ui
   return Philox4{c0, c1, c2, c3};
 }
 
+// philox4x32_10_rk for NB counters (blk[b], c1, c2, c3) that differ only in
+// the first word, computed round by round across the blocks so that their
+// independent chains interleave.  The first round's product of c2 is the same
+// for every block and is formed once.
+template <int NB>
+__device__ __forceinline__ void philox4x32_10_rk_multi(const uint32_t (&blk)[NB], uint32_t c1, uint32_t c2,
+                                                       uint32_t c3, const uint32_t* rk0, const uint32_t* rk1,
+                                                       uint32_t (&out)[NB][4]) {
+  const uint64_t q = (uint64_t)0xCD9E8D57u * c2;
+  const uint32_t n0 = (uint32_t)(q >> 32) ^ c1 ^ rk0[0];
+  uint32_t x0[NB], x1[NB], x2[NB], x3[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * blk[b];
+    x0[b] = n0;
+    x1[b] = (uint32_t)q;
+    x2[b] = (uint32_t)(p0 >> 32) ^ c3 ^ rk1[0];
+    x3[b] = (uint32_t)p0;
+  }
+#pragma unroll
+  for (int round = 1; round < 10; ++round) {
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const uint64_t p0 = (uint64_t)0xD2511F53u * x0[b];
+      const uint64_t p1 = (uint64_t)0xCD9E8D57u * x2[b];
+      const uint32_t m0 = (uint32_t)(p1 >> 32) ^ x1[b] ^ rk0[round];
+      const uint32_t m2 = (uint32_t)(p0 >> 32) ^ x3[b] ^ rk1[round];
+      x1[b] = (uint32_t)p1;
+      x3[b] = (uint32_t)p0;
+      x0[b] = m0;
+      x2[b] = m2;
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    out[b][0] = x0[b];
+    out[b][1] = x1[b];
+    out[b][2] = x2[b];
+    out[b][3] = x3[b];
+  }
+}
+
 // Round-key table of philox4x32_10_rk for a 64-bit seed.
 __host__ __device__ inline void philox_round_keys(uint64_t seed, uint32_t* rk0, uint32_t* rk1) {
   uint32_t a = (uint32_t)(seed & 0xFFFFFFFFull), b = (uint32_t)(seed >> 32);

@@ -594,17 +594,12 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col32);
           uint32_t h[16];
           if (live) tc::tmem_ld_32x32b<16>(taddr, h);
-          uint32_t rw[kGroups][4];
+          // Philox block of element index e = i*k + j (j a multiple of 8): e / 8
+          uint32_t blks[kGroups];
 #pragma unroll
-          for (int g = 0; g < kGroups; ++g) {
-            // Philox block of element index e = i*k + j (j a multiple of 8): e / 8
-            const uint32_t blk = (uint32_t)i * k8 + ((uint32_t)(j0 + col32 + 8 * g) >> 3);
-            const Philox4 rnd = philox4x32_10_rk(blk, a.step, layer, kTagSR, a.rk0, a.rk1);
-            rw[g][0] = rnd.w0;
-            rw[g][1] = rnd.w1;
-            rw[g][2] = rnd.w2;
-            rw[g][3] = rnd.w3;
-          }
+          for (int g = 0; g < kGroups; ++g) blks[g] = (uint32_t)i * k8 + ((uint32_t)(j0 + col32 + 8 * g) >> 3);
+          uint32_t rw[kGroups][4];
+          philox4x32_10_rk_multi<kGroups>(blks, a.step, layer, kTagSR, a.rk0, a.rk1, rw);
           if (live) tc::tmem_wait_ld_regs<16>(h);
           // Per 8-column group: v = fmaf(-s, H, w) and stochastic rounding (add
           // 16 random bits below the BF16 mantissa, keep the upper halves: one
