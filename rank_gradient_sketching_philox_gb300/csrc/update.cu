@@ -578,13 +578,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         tc::tc_fence_after();
         const uint32_t s_w32 = tc::smem_u32(s_w0) + (uint32_t)sw * a.w_bytes;
         for (int o = 16; o > 0; o >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
-        // The exactness test compares v^2 with thr^2 (multiplies on the idle FMA
-        // pipe instead of absolute values on the busy ALU pipe).  Where thr^2
-        // would leave the normal range, or thr is NaN, every group of the row
-        // is flagged instead (always safe); thr = 0 flags nothing.
         const float thr = thr_row * pmax;
-        const bool thr_ok = thr == 0.f || (thr >= 0x1p-60f && thr <= 0x1p60f);
-        const float thr2 = thr * thr;
 #pragma unroll 1
         for (int half = 0; half < kCols / kPass; ++half) {
           const int col32 = col_base + half * kPass;
@@ -637,14 +631,14 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
               const uint32_t s0 = mad_lo(r_lo, 1u, __float_as_uint(v0));
               const uint32_t s1 = mad_hi(rword, 0x10000u, __float_as_uint(v1));
               wout[t2] = __byte_perm(s0, s1, 0x7632);
-              av[2 * t2] = v0 * v0;
-              av[2 * t2 + 1] = v1 * v1;
+              av[2 * t2] = fabsf(v0);  // folded into the min as an operand modifier
+              av[2 * t2 + 1] = fabsf(v1);
             }
-            // smallest v^2 of the group; NaN if any v is NaN
+            // smallest |v| of the group; NaN if any v is NaN
             const float gmin = fmin3_nan(fmin3_nan(av[0], av[1], av[2]), fmin3_nan(av[3], av[4], av[5]),
                                          fmin_nan(av[6], av[7]));
             const bool ok = live && row_ok && j0 + col < k;
-            const bool flag = ok && (!thr_ok || !(gmin > thr2));  // small value or NaN
+            const bool flag = ok && !(gmin >= thr);  // small value or NaN
             // Careful path: a flagged group keeps its original W here and is
             // marked in the flag bitmap (the word of the whole warp, written on
             // every call); the careful-group pass at the end of this kernel
