@@ -115,6 +115,18 @@ __host__ __device__ inline void philox_round_keys(uint64_t seed, uint32_t* rk0, 
   }
 }
 
+// acc + lo*lo + hi*hi for the two BF16 halves of w (low half first), each step
+// one fused multiply-add with BF16 multiplicands (exact products, one rounding),
+// so no unpacking to fp32 first.
+__device__ __forceinline__ float sq_acc_bf16x2(uint32_t w, float acc) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "fma.rn.f32.bf16 %0, lo, lo, %0;\n\t"
+      "fma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w));
+  return acc;
+}
+
 // min of a, b and c that returns NaN when any is NaN (PTX three-input min.NaN).
 __device__ __forceinline__ float fmin3_nan(float a, float b, float c) {
   float r;

@@ -602,6 +602,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           // outside W).  A group that holds a NaN or a value small enough for
           // the exactness test is flagged for the careful path.
           uint32_t fwords[kGroups];
+          float gs = 0.f;  // sum of squares of this pass's results (normalized SGD)
 #pragma unroll
           for (int g = 0; g < kGroups; ++g) {
             if (g == 2 && live) {  // next 16 columns of H
@@ -653,18 +654,15 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
             if (live) tc::sts128(sp, make_uint4(wout[0], wout[1], wout[2], wout[3]));
             if (flag) tc::sts128(sp, raw);  // rare: the careful pass needs the original
             if (need_norm && ok) {
-              float gs = 0.f;
 #pragma unroll
-              for (int t2 = 0; t2 < 4; ++t2) {
-                const float lo = __uint_as_float(wout[t2] << 16), hi = __uint_as_float(wout[t2] & 0xFFFF0000u);
-                gs = fmaf(lo, lo, gs);
-                gs = fmaf(hi, hi, gs);
-              }
-              const float y = gs - sq_comp;
-              const float tsum = sq + y;
-              sq_comp = (tsum - sq) - y;
-              sq = tsum;
+              for (int t2 = 0; t2 < 4; ++t2) gs = sq_acc_bf16x2(wout[t2], gs);
             }
+          }
+          if (need_norm) {  // the pass's squares into the compensated sum
+            const float y = gs - sq_comp;
+            const float tsum = sq + y;
+            sq_comp = (tsum - sq) - y;
+            sq = tsum;
           }
           if (lane == 0) {  // every word of the layer is written on every call
             uint32_t* fw = a.flags[p] + ((size_t)x.rb * a.n_ct[p] + ct) * (16 * kGroupsPerWarp) +
