@@ -215,6 +215,7 @@ struct UpdBatch {
   uint32_t a_bytes;   // bytes of the C_hi (or C_lo) tile: kchunks x 16 KB
   uint32_t b_bytes;   // bytes of the P_hi (or P_lo) tile: kchunks x NCOLS x 128
   uint32_t w_bytes;   // bytes of the W tile: NCOLS/64 x 16 KB
+  int list_cap;       // entries of the careful-word list that fit the dynamic shared memory
   int* err;
   // careful-group flags, one bit per 8-weight group: per tile (rb, ct), word
   // ew * (NCOLS/32) + g holds bit `lane` for row rb*128 + (ew&3)*32 + lane,
@@ -257,10 +258,6 @@ __device__ __forceinline__ Unit decode_unit(const UpdBatch& a, int u) {
   x.ct0 = cu * a.unit_tiles;
   x.ct1 = min(a.n_ct[p], x.ct0 + a.unit_tiles);
   return x;
-}
-
-__device__ __forceinline__ bool layer_skipped(const UpdBatch& a, int p) {
-  return a.status_in[p] != nullptr && *a.status_in[p] != 0;
 }
 
 // One careful group, warp-wide: W_new of the 8 elements (i, j..j+7) of
@@ -329,24 +326,28 @@ __device__ __forceinline__ void careful_group_warp(const UpdBatch& a, int p, int
   if (q == 0) *wp = (uint16_t)o;
 }
 
-// Persistent rebuild + update.  Warp 0 (one lane) streams, with TMA, the C row
-// block of each unit, the P_hi/P_lo rows of each column tile into a P ring and
-// the W tile into a deeper W ring; warp 1 (one lane) issues
+// Persistent rebuild + update, one CTA per SM, each CTA a contiguous range of
+// units (a unit: one 128-row block of one layer and up to unit_tiles column
+// tiles of NCOLS).  Warp 0 (one lane) streams with TMA the split C row block of
+// each unit (C_hi, C_lo), the P_hi/P_lo rows of each column tile into a P ring
+// and the W tile into a deeper W ring.  Warp 1 (one lane) issues
 // H = C_hi P_hi^T + C_hi P_lo^T + C_lo P_hi^T (tcgen05.mma, M=128, N=NCOLS)
-// into one of two TMEM buffers and frees the P stage with tcgen05.commit;
-// warps 4..11 (two per TMEM lane quarter, one column half each) copy their W
-// values to registers and free the W stage at once, then read H from TMEM,
-// form v = fmaf(-s, H, w), round it stochastically with 16 Philox bits per
-// weight and store the results straight from registers.  Keeping the P and W
-// rings apart lets up to four W tiles per SM be in flight while the epilogue
-// works.
+// into one of two TMEM buffers and frees the P stage with tcgen05.commit.
+// The 16 epilogue warps (warps 4..19, four per TMEM lane quarter, one column
+// quarter each) read H from TMEM, form v = fmaf(-s, H, w) with w from the W
+// stage, round it stochastically with 16 Philox bits per weight and write the
+// BF16 results back into the stage; warp 2 (one lane) writes each finished
+// tile to W with a TMA tensor store and frees the stage.  After the main loop
+// all 20 warps redo the flagged groups (the careful groups, below).
 //
-// Exactness where it matters: |H_tc - H| <= ||c_i|| ||p_j|| 2^-14 (three BF16
-// products leave ~3 * 2^-18 per term; the bound has >4x margin).  When that
-// could move v across more than one BF16 step (|v| < s ||c_i|| max_j ||p_j|| 2^-5
-// with the maximum over the thread's columns of the tile),
-// the warp recomputes H_ij in double from fp32 C and P and uses fl32(H_ij),
-// which is the value the definition rounds.
+// Exactness where it matters: |H_tc - H| <= ~2^-14.2 ||c_i|| ||p_j|| (the
+// dropped lo*lo and residual terms, ~3 * 2^-16 of sum |c_l p_l|, plus the fp32
+// accumulation), which moves v across at most one BF16 step unless
+// |v| < s ||c_i|| ||p_j|| 2^-6.  A group of 8 weights holding a |v| below
+// s ||c_i|| max_j ||p_j|| 2^-5 (the maximum over the warp's 32 columns of the
+// tile: twice that margin) or a NaN keeps its original W in the stage and is
+// flagged; the careful pass recomputes its elements with fl32(H_ij) from a
+// compensated dot product, which is the value the definition rounds.
 template <int NCOLS>
 __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const __grid_constant__ UpdBatch a) {
   extern __shared__ uint8_t smem_raw[];
@@ -355,6 +356,8 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
   __shared__ __align__(8) uint64_t cfull_bar, cempty_bar, tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
+  __shared__ int clist_n;  // entries of the careful-word list
+  __shared__ uint32_t skip_mask[(kMaxUpd + 31) / 32];  // layers whose status_in is nonzero
   __shared__ double warp_sq[kEpiWarps];
 
   uint8_t* smem = align1024(smem_raw);
@@ -388,10 +391,21 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     tc::fence_mbar_init();
   }
   if (warp == 1) tc::tmem_alloc(&tmem_slot, kTmemCols);
+  if (warp == 3) {
+    // the skipped layers, read once here instead of at every unit
+#pragma unroll
+    for (int h = 0; h < (kMaxUpd + 31) / 32; ++h) {
+      const int pp = 32 * h + lane;
+      const bool sk = pp < a.n && a.status_in[pp] != nullptr && *a.status_in[pp] != 0;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, sk);
+      if (lane == 0) skip_mask[h] = m;
+    }
+  }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  auto layer_skipped = [&](int pp) { return (skip_mask[pp >> 5] >> (pp & 31)) & 1u; };
 
   if (warp == 0 && lane == 0) {
     // ---------------- producer ----------------
@@ -399,7 +413,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     bool stop = false;
     for (int u = u_begin; u < u_end && !stop; ++u) {
       const Unit x = decode_unit(a, u);
-      if (layer_skipped(a, x.p)) continue;
+      if (layer_skipped(x.p)) continue;
       const int i0 = x.rb * 128;
       if (x.p != prev_p || x.rb != prev_rb) {
         if (cl > 0 && !tc::mbar_wait(&cempty_bar, (cl - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) break;
@@ -445,7 +459,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     bool stop = false;
     for (int u = u_begin; u < u_end && !stop; ++u) {
       const Unit x = decode_unit(a, u);
-      if (layer_skipped(a, x.p)) continue;
+      if (layer_skipped(x.p)) continue;
       if (x.p != prev_p || x.rb != prev_rb) {
         if (!tc::mbar_wait(&cfull_bar, cl & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) break;
         ++cl;
@@ -495,7 +509,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     bool stop = false;
     for (int u = u_begin; u < u_end && !stop; ++u) {
       const Unit x = decode_unit(a, u);
-      if (layer_skipped(a, x.p)) continue;
+      if (layer_skipped(x.p)) continue;
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
         const int sw = it % NSW;
         if (!tc::mbar_wait(&sfull_bar[sw], (it / NSW) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
@@ -542,7 +556,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     for (int u = u_begin; u < u_end; ++u) {
       const Unit x = decode_unit(a, u);
       const int p = x.p;
-      if (layer_skipped(a, p)) continue;
+      if (layer_skipped(p)) continue;
       // d, k < 2^31 and d*k/8 < 2^32 (checked on the host): 32-bit indices
       const int d = (int)a.d[p], k = (int)a.k[p];
       const int i = x.rb * 128 + q;
@@ -579,105 +593,108 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         const uint32_t s_w32 = tc::smem_u32(s_w0) + (uint32_t)sw * a.w_bytes;
         for (int o = 16; o > 0; o >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
         const float thr = thr_row * pmax;
+        // live is the same in the whole warp: one branch per tile
+        if (live) {
 #pragma unroll 1
-        for (int half = 0; half < kCols / kPass; ++half) {
-          const int col32 = col_base + half * kPass;
-          // H of the pass from TMEM, 16 columns at a time; the first load
-          // completes while the Philox blocks of the pass (independent chains)
-          // are computed
-          const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col32);
-          uint32_t h[16];
-          if (live) tc::tmem_ld_32x32b<16>(taddr, h);
-          // Philox block of element index e = i*k + j (j a multiple of 8): e / 8
-          uint32_t blks[kGroups];
+          for (int half = 0; half < kCols / kPass; ++half) {
+            const int col32 = col_base + half * kPass;
+            // H of the pass from TMEM, 16 columns at a time; the first load
+            // completes while the Philox blocks of the pass (independent chains)
+            // are computed
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col32);
+            uint32_t h[16];
+            tc::tmem_ld_32x32b<16>(taddr, h);
+            // Philox block of element index e = i*k + j (j a multiple of 8): e / 8
+            uint32_t blks[kGroups];
 #pragma unroll
-          for (int g = 0; g < kGroups; ++g) blks[g] = (uint32_t)i * k8 + ((uint32_t)(j0 + col32 + 8 * g) >> 3);
-          uint32_t rw[kGroups][4];
-          philox4x32_10_rk_multi<kGroups>(blks, a.step, layer, kTagSR, a.rk0, a.rk1, rw);
-          if (live) tc::tmem_wait_ld_regs<16>(h);
-          // Per 8-column group: v = fmaf(-s, H, w) and stochastic rounding (add
-          // 16 random bits below the BF16 mantissa, keep the upper halves: one
-          // PRMT per pair); the results go back into the W stage in place (the
-          // store warp writes the tile out with TMA, clipping rows and columns
-          // outside W).  A group that holds a NaN or a value small enough for
-          // the exactness test is flagged for the careful path.
-          uint32_t fwords[kGroups];
-          float gs = 0.f;  // sum of squares of this pass's results (normalized SGD)
+            for (int g = 0; g < kGroups; ++g) blks[g] = (uint32_t)i * k8 + ((uint32_t)(j0 + col32 + 8 * g) >> 3);
+            uint32_t rw[kGroups][4];
+            philox4x32_10_rk_multi<kGroups>(blks, a.step, layer, kTagSR, a.rk0, a.rk1, rw);
+            tc::tmem_wait_ld_regs<16>(h);
+            // Per 8-column group: v = fmaf(-s, H, w) and stochastic rounding (add
+            // 16 random bits below the BF16 mantissa, keep the upper halves: one
+            // PRMT per pair); the results go back into the W stage in place (the
+            // store warp writes the tile out with TMA, clipping rows and columns
+            // outside W).  A group that holds a NaN or a value small enough for
+            // the exactness test is flagged for the careful path.
+            uint32_t fwords[kGroups];
+            float gs = 0.f;  // sum of squares of this pass's results (normalized SGD)
 #pragma unroll
-          for (int g = 0; g < kGroups; ++g) {
-            if (g == 2 && live) {  // next 16 columns of H
-              tc::tmem_ld_32x32b<16>(taddr + 16, h);
-              tc::tmem_wait_ld_regs<16>(h);
-            }
-            const int col = col32 + 8 * g;
-            const uint32_t sp = s_w32 + stage_off[half * kGroups + g];
-            const uint4 raw = tc::lds128(sp);
-            const uint32_t win[4] = {raw.x, raw.y, raw.z, raw.w};
-            const uint32_t* rwg = rw[g];
-            uint32_t wout[4];
-            float av[8];
+            for (int g = 0; g < kGroups; ++g) {
+              if (g == 2) {  // next 16 columns of H
+                tc::tmem_ld_32x32b<16>(taddr + 16, h);
+                tc::tmem_wait_ld_regs<16>(h);
+              }
+              const int col = col32 + 8 * g;
+              const uint32_t sp = s_w32 + stage_off[half * kGroups + g];
+              const uint4 raw = tc::lds128(sp);
+              const uint32_t win[4] = {raw.x, raw.y, raw.z, raw.w};
+              const uint32_t* rwg = rw[g];
+              uint32_t wout[4];
+              float av[8];
 #pragma unroll
-            for (int t2 = 0; t2 < 4; ++t2) {
-              // BF16 -> fp32 by shifting into the high half; the integer steps use
-              // multiply-adds so that they share the multiplier pipe with Philox
-              // instead of crowding the ALU pipe: r_hi = r >> 16,
-              // r_lo = r - r_hi * 2^16 = r & 0xFFFF
-              const uint32_t wword = win[t2], rword = rwg[t2];
-              const float v0 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2]),
-                                    __uint_as_float(mad_lo(wword, 0x10000u, 0u)));
-              const float v1 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2 + 1]),
-                                    __uint_as_float(wword & 0xFFFF0000u));
-              const uint32_t r_hi = mad_hi(rword, 0x10000u, 0u);
-              const uint32_t r_lo = mad_lo(r_hi, 0xFFFF0000u, rword);
-              const uint32_t s0 = mad_lo(r_lo, 1u, __float_as_uint(v0));
-              const uint32_t s1 = mad_hi(rword, 0x10000u, __float_as_uint(v1));
-              wout[t2] = __byte_perm(s0, s1, 0x7632);
-              av[2 * t2] = fabsf(v0);  // folded into the min as an operand modifier
-              av[2 * t2 + 1] = fabsf(v1);
-            }
-            // smallest |v| of the group; NaN if any v is NaN
-            const float gmin = fmin3_nan(fmin3_nan(av[0], av[1], av[2]), fmin3_nan(av[3], av[4], av[5]),
-                                         fmin_nan(av[6], av[7]));
-            const bool ok = live && row_ok && j0 + col < k;
-            const bool flag = ok && !(gmin >= thr);  // small value or NaN
-            // Careful path: a flagged group keeps its original W here and is
-            // marked in the flag bitmap (the word of the whole warp, written on
-            // every call); the careful-group pass at the end of this kernel
-            // redoes its 8 elements exactly from the original W, once the
-            // tiles are stored.  The norm sum keeps the tensor-core values of
-            // the group (they differ from the exact ones by at most one BF16
-            // step, or are below the threshold), except that a NaN makes it NaN.
-            fwords[g] = __ballot_sync(0xFFFFFFFFu, flag);
-            if (flag) {
-              if (need_norm && gmin != gmin) sq = __int_as_float(0x7FC00000);
-            }
-            if (live) tc::sts128(sp, make_uint4(wout[0], wout[1], wout[2], wout[3]));
-            if (flag) tc::sts128(sp, raw);  // rare: the careful pass needs the original
-            if (need_norm && ok) {
+              for (int t2 = 0; t2 < 4; ++t2) {
+                // BF16 -> fp32 by shifting into the high half; the integer steps
+                // use multiply-adds so that they share the multiplier pipe with
+                // Philox instead of crowding the ALU pipe: r_hi = r >> 16,
+                // r_lo = r - r_hi * 2^16 = r & 0xFFFF
+                const uint32_t wword = win[t2], rword = rwg[t2];
+                const float v0 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2]),
+                                      __uint_as_float(mad_lo(wword, 0x10000u, 0u)));
+                const float v1 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2 + 1]),
+                                      __uint_as_float(wword & 0xFFFF0000u));
+                const uint32_t r_hi = mad_hi(rword, 0x10000u, 0u);
+                const uint32_t r_lo = mad_lo(r_hi, 0xFFFF0000u, rword);
+                const uint32_t s0 = mad_lo(r_lo, 1u, __float_as_uint(v0));
+                const uint32_t s1 = mad_hi(rword, 0x10000u, __float_as_uint(v1));
+                wout[t2] = __byte_perm(s0, s1, 0x7632);
+                av[2 * t2] = fabsf(v0);  // folded into the min as an operand modifier
+                av[2 * t2 + 1] = fabsf(v1);
+              }
+              // smallest |v| of the group; NaN if any v is NaN
+              const float gmin = fmin3_nan(fmin3_nan(av[0], av[1], av[2]), fmin3_nan(av[3], av[4], av[5]),
+                                           fmin_nan(av[6], av[7]));
+              const bool ok = row_ok && j0 + col < k;
+              const bool flag = ok && !(gmin >= thr);  // small value or NaN
+              // Careful path: a flagged group keeps its original W here and is
+              // marked in the flag bitmap (the word of the whole warp, written on
+              // every call); the careful-group pass at the end of this kernel
+              // redoes its 8 elements exactly from the original W, once the
+              // tiles are stored.  The norm sum keeps the tensor-core values of
+              // the group (they differ from the exact ones by at most one BF16
+              // step, or are below the threshold), except that a NaN makes it
+              // NaN.  The rare writes are predicated, not branched around.
+              fwords[g] = __ballot_sync(0xFFFFFFFFu, flag);
+              tc::sts128(sp, make_uint4(wout[0], wout[1], wout[2], wout[3]));
+              tc::sts128_if(sp, raw, flag);  // rare: the careful pass needs the original
+              if (need_norm) {
+                float t = gs;
 #pragma unroll
-              for (int t2 = 0; t2 < 4; ++t2) gs = sq_acc_bf16x2(wout[t2], gs);
+                for (int t2 = 0; t2 < 4; ++t2) t = sq_acc_bf16x2(wout[t2], t);
+                gs = ok ? t : gs;
+                sq = (ok && gmin != gmin) ? __int_as_float(0x7FC00000) : sq;
+              }
             }
-          }
-          if (need_norm) {  // the pass's squares into the compensated sum
-            const float y = gs - sq_comp;
-            const float tsum = sq + y;
-            sq_comp = (tsum - sq) - y;
-            sq = tsum;
-          }
-          if (lane == 0) {  // every word of the layer is written on every call
-            uint32_t* fw = a.flags[p] + ((size_t)x.rb * a.n_ct[p] + ct) * (16 * kGroupsPerWarp) +
-                           ew * kGroupsPerWarp + half * kGroups;
-            if constexpr (kGroups == 4)
-              *reinterpret_cast<uint4*>(fw) = make_uint4(fwords[0], fwords[1], fwords[2], fwords[3]);
-            else
-              *reinterpret_cast<uint2*>(fw) = make_uint2(fwords[0], fwords[1]);
-          }
-          if (half == kCols / kPass - 1) {  // this warp is done with the TMEM buffer
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&tempty_bar[b]);
+            if (need_norm) {  // the pass's squares into the compensated sum
+              const float y = gs - sq_comp;
+              const float tsum = sq + y;
+              sq_comp = (tsum - sq) - y;
+              sq = tsum;
+            }
+            if (lane == 0) {  // every word of the layer is written on every call
+              uint32_t* fw = a.flags[p] + ((size_t)x.rb * a.n_ct[p] + ct) * (16 * kGroupsPerWarp) +
+                             ew * kGroupsPerWarp + half * kGroups;
+              if constexpr (kGroups == 4)
+                *reinterpret_cast<uint4*>(fw) = make_uint4(fwords[0], fwords[1], fwords[2], fwords[3]);
+              else
+                *reinterpret_cast<uint2*>(fw) = make_uint2(fwords[0], fwords[1]);
+            }
           }
         }
+        // this warp is done with the TMEM buffer
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&tempty_bar[b]);
         // this warp's results are in the stage: make them visible to the TMA
         // engine and tell the store warp
         tc::fence_proxy_async_smem();
@@ -719,36 +736,100 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
   if (abort_flag) return;
 
-  // Careful groups of this CTA's tiles: each flagged group still holds its
+  // Careful groups of this CTA's tiles.  Each flagged group still holds its
   // original W (the stage kept it and the TMA stores above have completed), so
-  // it is redone exactly here, warp-wide, the CTA's warps taking tiles in turn.
+  // it is redone exactly here.  Pass 1: the warps read the flag words of the
+  // CTA's units (units in turn) and append the nonzero ones to a list in the
+  // now idle dynamic shared memory.
+  // Pass 2: the warps take the list's words in turn, so each warp redoes about
+  // the same number of groups; the operands of a warp's next word are
+  // prefetched into L2 while it works on the current one.  A word that finds
+  // the list full is redone at once by the warp that read it.
   constexpr int kWarps = kUpdThreads / 32;
   constexpr int kGroupsPerWarpT = NCOLS / 32, kWordsPerTile = 16 * kGroupsPerWarpT;
-  int tile_seq = 0;
-  for (int u = u_begin; u < u_end; ++u) {
+  constexpr int kBatch = 8;  // flag words per lane per load batch
+  uint4* clist = reinterpret_cast<uint4*>(smem);
+  if (threadIdx.x == 0) clist_n = 0;
+  __syncthreads();
+  // the careful groups of word `bits` at word index widx of layer p
+  auto redo_word = [&](int p, uint32_t widx, uint32_t bits) {
+    const uint32_t tile = widx / kWordsPerTile, wt = widx % kWordsPerTile;
+    const int n_ct = a.n_ct[p];
+    const int rb = (int)(tile / (uint32_t)n_ct), ct = (int)(tile % (uint32_t)n_ct);
+    const int ew = (int)wt / kGroupsPerWarpT, gw = (int)wt % kGroupsPerWarpT;
+    const int j = ct * NCOLS + (ew >> 2) * (NCOLS / 4) + 8 * gw;
+    while (bits) {
+      const int row = __ffs(bits) - 1;
+      bits &= bits - 1;
+      careful_group_warp(a, p, rb * 128 + (ew & 3) * 32 + row, j);
+    }
+  };
+  // pass 1: warp w reads the flag words of units w, w + kWarps, ... (a unit's
+  // words are contiguous), kBatch words per lane at a time
+  for (int u = u_begin + warp; u < u_end; u += kWarps) {
     const Unit x = decode_unit(a, u);
-    if (layer_skipped(a, x.p)) continue;
-    for (int ct = x.ct0; ct < x.ct1; ++ct, ++tile_seq) {
-      if (tile_seq % kWarps != warp) continue;
-      const uint32_t* fw = a.flags[x.p] + ((size_t)x.rb * a.n_ct[x.p] + ct) * kWordsPerTile;
-      for (int w0 = 0; w0 < kWordsPerTile; w0 += 32) {
-        const uint32_t bits = (w0 + lane < kWordsPerTile) ? fw[w0 + lane] : 0u;
-        uint32_t pending = __ballot_sync(0xFFFFFFFFu, bits != 0u);
-        while (pending) {
-          const int src = __ffs(pending) - 1;
-          pending &= pending - 1;
-          uint32_t b = __shfl_sync(0xFFFFFFFFu, bits, src);
-          const int wt = w0 + src, ew = wt / kGroupsPerWarpT, gw = wt % kGroupsPerWarpT;
-          const int j = ct * NCOLS + (ew >> 2) * (NCOLS / 4) + 8 * gw;
-          while (b) {
-            const int row = __ffs(b) - 1;
-            b &= b - 1;
-            const int i = x.rb * 128 + (ew & 3) * 32 + row;
-            careful_group_warp(a, x.p, i, j);
-          }
+    if (layer_skipped(x.p)) continue;
+    const uint32_t wbeg = (uint32_t)(x.rb * a.n_ct[x.p] + x.ct0) * (uint32_t)kWordsPerTile;
+    const uint32_t nwords = (uint32_t)(x.ct1 - x.ct0) * (uint32_t)kWordsPerTile;
+    const uint32_t* fw = a.flags[x.p] + wbeg;
+    for (uint32_t w0 = 0; w0 < nwords; w0 += 32 * kBatch) {
+      uint32_t v[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const uint32_t idx = w0 + 32 * b + lane;
+        v[b] = idx < nwords ? fw[idx] : 0u;
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const uint32_t nz = __ballot_sync(0xFFFFFFFFu, v[b] != 0u);
+        if (nz == 0u) continue;
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&clist_n, __popc(nz));
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+        const int slot = base + __popc(nz & ((1u << lane) - 1u));
+        const uint32_t widx = wbeg + w0 + 32 * b + lane;
+        const bool mine = v[b] != 0u;
+        if (mine && slot < a.list_cap) clist[slot] = make_uint4((uint32_t)x.p, widx, v[b], 0u);
+        uint32_t over = __ballot_sync(0xFFFFFFFFu, mine && slot >= a.list_cap);
+        while (over) {  // the list is full: redo these words here
+          const int src = __ffs(over) - 1;
+          over &= over - 1;
+          redo_word(x.p, __shfl_sync(0xFFFFFFFFu, widx, src), __shfl_sync(0xFFFFFFFFu, v[b], src));
         }
       }
     }
+  }
+  __syncthreads();
+  const int n_list = clist_n < a.list_cap ? clist_n : a.list_cap;
+  // pass 2: entries warp, warp + kWarps, ...; the operands of the warp's next
+  // entry are prefetched into L2 while it works on the current one
+  for (int e = warp; e < n_list; e += kWarps) {
+    const uint4 en = clist[e];
+    if (e + kWarps < n_list) {
+      const uint4 nx = clist[e + kWarps];
+      const int p2 = (int)nx.x;
+      const uint32_t tile = nx.y / kWordsPerTile, wt = nx.y % kWordsPerTile;
+      const int n_ct = a.n_ct[p2];
+      const int rb = (int)(tile / (uint32_t)n_ct), ct = (int)(tile % (uint32_t)n_ct);
+      const int ew = (int)wt / kGroupsPerWarpT, gw = (int)wt % kGroupsPerWarpT;
+      const int j = ct * NCOLS + (ew >> 2) * (NCOLS / 4) + 8 * gw;
+      const int i = rb * 128 + (ew & 3) * 32 + __ffs(nx.z) - 1;
+      const int r = a.r, kk = (int)a.k[p2];
+      const int jn = (kk - j) < 8 ? (kk - j) : 8;
+      // P rows j..j+jn-1 (contiguous), the C row and the W group: one address
+      // per 128-byte line, every address inside its buffer
+      const char* pbase = reinterpret_cast<const char*>(a.P[p2] + (int64_t)j * r);
+      const int pbytes = jn * r * 4, plines = pbytes / 128 + 2;
+      const char* cbase = reinterpret_cast<const char*>(a.C[p2] + (int64_t)i * r);
+      const int cbytes = r * 4, clines = cbytes / 128 + 2;
+      for (int l = lane; l < plines + clines + 1; l += 32) {
+        const char* ad = l < plines ? pbase + min(128 * l, pbytes - 1)
+                         : l < plines + clines ? cbase + min(128 * (l - plines), cbytes - 1)
+                                               : reinterpret_cast<const char*>(a.W[p2] + (int64_t)i * a.ld_w[p2] + j);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(ad));
+      }
+    }
+    redo_word((int)en.x, en.y, en.z);
   }
 }
 
@@ -792,6 +873,7 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   a.p_stages = p_stages;
   a.w_stages = w_stages;
   const size_t smem = fixed + p_stages * p_stage + (size_t)w_stages * a.w_bytes;
+  a.list_cap = (int)((smem - 1024) / 16);  // after the 1024-byte alignment
   err = cudaFuncSetAttribute(update_persistent_kernel<NCOLS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
   if (err != cudaSuccess) return err;

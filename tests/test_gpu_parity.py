@@ -413,6 +413,29 @@ def test_sgd_nan_sketch_row_gives_canonical_nan():
     _w_check(np.delete(got, 5, 0), np.delete(ref, 5, 0))
 
 
+def test_sgd_nonfinite_weights_follow_the_definition():
+    """NaN weights of any payload (quiet, with a small payload, negative) give
+    the canonical BF16 NaN; +-Inf weights stay +-Inf (v = Inf - s H); every
+    other element is unaffected, with whole 8-column groups of NaN and Inf
+    neighbours among them."""
+    d, k, r = 128, 256, 16
+    W0 = synth.layer_weight(d, k, 4)
+    specials = {(3, 5): 0x7FC0, (3, 6): 0x7F81, (17, 200): 0xFFC0, (64, 0): 0x7F80,
+                (65, 255): 0xFF80, (100, 8): 0x7FFF, (127, 129): 0xFF81}
+    for (i, j), b in specials.items():
+        W0[i, j] = torch.tensor([b], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)[0]
+    P = orc.sample_rademacher(1, 0, 0, k, r)
+    C = _rand_c(d, r, 8)
+    W = W0.to(DEV)
+    rgs.apply_update_sgd(W, torch.from_numpy(C).to(DEV), torch.from_numpy(P).to(DEV), 1e-3, 1, 0, 0)
+    ref = orc.update_sgd(bits(W0), C, P, 1e-3, 1, 0, 0)
+    got = bits(W)
+    for (i, j), b in specials.items():
+        expect = 0x7F80 if b == 0x7F80 else 0xFF80 if b == 0xFF80 else 0x7FC0
+        assert ref[i, j] == expect and got[i, j] == expect, ((i, j), hex(got[i, j]), hex(ref[i, j]))
+    _w_check(got, ref)
+
+
 @pytest.mark.parametrize("kind", [rgs.PROJ_GAUSSIAN_QR, rgs.PROJ_RADEMACHER])
 def test_policy_sync_receiver_matches_trainer(kind):
     """A rollout worker that receives U = alpha*eta*C and (seed, layer, step),
