@@ -154,21 +154,38 @@ __global__ void __launch_bounds__(256) tri_apply_kernel(const ProjBatch batch, i
   const int rows = (int)((pb.k - row0) < RB ? (pb.k - row0) : RB);
   float* P = pb.P + row0 * r;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // a warp reads 16 rows at a time, each coalesced; the 16 loads are issued
-  // before any store so that their latencies overlap
-  for (int mc0 = 0; mc0 < r; mc0 += 32) {
-    const int mc = mc0 + lane;
-    for (int row0w = warp; row0w < rows; row0w += 128) {
-      float v[16];
+  // Staging: thread t takes rows t, t + 256, ... and reads each in pieces of up
+  // to 64 values, all loads of a piece issued before its transposed stores
+  // (consecutive threads write consecutive rows: no bank conflicts).
+  if ((r & 3) == 0) {
+    const int nv = r >> 2;  // float4 per row
+    for (int row = threadIdx.x; row < rows; row += 256) {
+      const float4* src = reinterpret_cast<const float4*>(P + (size_t)row * r);
+      for (int c0 = 0; c0 < nv; c0 += 16) {
+        float4 v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int row = row0w + 8 * i;
-        v[i] = (row < rows && mc < r) ? P[(size_t)row * r + mc] : 0.f;
+        for (int m = 0; m < 16; ++m) v[m] = (c0 + m < nv) ? src[c0 + m] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          if (c0 + m >= nv) break;
+          float* dst = St + (size_t)(4 * (c0 + m)) * ldt + row;
+          dst[0] = v[m].x;
+          dst[ldt] = v[m].y;
+          dst[2 * ldt] = v[m].z;
+          dst[3 * ldt] = v[m].w;
+        }
       }
+    }
+  } else {
+    for (int row = threadIdx.x; row < rows; row += 256) {
+      const float* src = P + (size_t)row * r;
+      for (int c0 = 0; c0 < r; c0 += 16) {
+        float v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int row = row0w + 8 * i;
-        if (row < rows && mc < r) St[(size_t)mc * ldt + row] = v[i];
+        for (int m = 0; m < 16; ++m) v[m] = (c0 + m < r) ? src[c0 + m] : 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          if (c0 + m < r) St[(size_t)(c0 + m) * ldt + row] = v[m];
       }
     }
   }
