@@ -242,6 +242,221 @@ __global__ void __launch_bounds__(256) tri_apply_kernel(const ProjBatch batch, i
   }
 }
 
+// The same product for r <= 64 (at most eight column octets), arranged so that
+// every lane of a warp has the same triangular extent: warp w takes column
+// octet co = w % co_n of the 256-row group w / co_n, lane l the row octet l of
+// that group (8 x 8 outputs each).  A block covers RB = 256 * (8 / co_n) rows,
+// staged (transposed) with all of X before any output is written.  Warps of
+// low octets finish early and leave the SM to other blocks; no lane idles
+// inside a warp.
+__host__ __device__ inline int tri_rows_small(int r) { return 256 * (8 / ((r + 7) / 8)); }
+__host__ __device__ inline size_t tri_small_smem_floats(int r) {
+  const int r8 = (r + 7) / 8 * 8;
+  return (((size_t)r * (tri_rows_small(r) + 4) + 3) & ~size_t(3)) + (size_t)r * r8;
+}
+__global__ void __launch_bounds__(256, 2) tri_apply_small_kernel(const ProjBatch batch, int final_pass) {
+  extern __shared__ __align__(16) float smem[];
+  const ProjProblem& pb = batch.p[blockIdx.y];
+  const int r = batch.r, r8 = (r + 7) / 8 * 8, co_n = r8 / 8, ng = 8 / co_n, RB = 256 * ng, ldt = RB + 4;
+  float* St = smem;                                          // r x (RB + 4): St[m][row]
+  float* Xs = smem + (((size_t)r * ldt + 3) & ~size_t(3));  // r x r8
+  const int64_t row0 = (int64_t)blockIdx.x * RB;
+  if (row0 >= pb.k) return;
+  const int rows = (int)((pb.k - row0) < RB ? (pb.k - row0) : RB);
+  float* P = pb.P + row0 * r;
+  if ((r & 3) == 0) {
+    const int nv = r >> 2;
+    for (int row = threadIdx.x; row < rows; row += 256) {
+      const float4* src = reinterpret_cast<const float4*>(P + (size_t)row * r);
+      float4 v[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) v[m] = (m < nv) ? src[m] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        if (m >= nv) break;
+        float* dst = St + (size_t)(4 * m) * ldt + row;
+        dst[0] = v[m].x;
+        dst[ldt] = v[m].y;
+        dst[2 * ldt] = v[m].z;
+        dst[3 * ldt] = v[m].w;
+      }
+    }
+  } else {
+    for (int row = threadIdx.x; row < rows; row += 256) {
+      const float* src = P + (size_t)row * r;
+      for (int c0 = 0; c0 < r; c0 += 16) {
+        float v[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) v[m] = (c0 + m < r) ? src[c0 + m] : 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          if (c0 + m < r) St[(size_t)(c0 + m) * ldt + row] = v[m];
+      }
+    }
+  }
+  const float* __restrict__ X = pb.rinv;
+  for (int e = threadIdx.x; e < r * r8; e += 256) {
+    const int m = e / r8, c = e % r8;
+    Xs[e] = c < r ? X[(size_t)m * r + c] : 0.f;
+  }
+  __syncthreads();  // no block-wide barrier after this point
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int co = warp % co_n, grp = warp / co_n;
+  if (grp >= ng) return;
+  const int c0 = 8 * co, q0 = grp * 256 + 8 * lane;
+  if (q0 >= rows) return;
+  float acc[8][8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[p][q] = 0.f;
+  // X is upper triangular: rows m > c0 + 7 add nothing to these columns
+  const int mend = (c0 + 8) < r ? (c0 + 8) : r;
+#pragma unroll 2
+  for (int m = 0; m < mend; ++m) {
+    const float4 sa = *reinterpret_cast<const float4*>(St + (size_t)m * ldt + q0);
+    const float4 sb = *reinterpret_cast<const float4*>(St + (size_t)m * ldt + q0 + 4);
+    const float4 xa = *reinterpret_cast<const float4*>(Xs + m * r8 + c0);
+    const float4 xb = *reinterpret_cast<const float4*>(Xs + m * r8 + c0 + 4);
+    const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+    const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+    for (int p = 0; p < 8; ++p)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[p][q] = fmaf(sv[p], xv[q], acc[p][q]);
+  }
+  const float scale = final_pass ? pb.scale : 1.0f;
+  const bool vec = (r & 3) == 0;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    if (q0 + p >= rows) break;
+    float* out = P + (size_t)(q0 + p) * r + c0;
+    if (vec && c0 + 8 <= r) {
+      *reinterpret_cast<float4*>(out) =
+          make_float4(acc[p][0] * scale, acc[p][1] * scale, acc[p][2] * scale, acc[p][3] * scale);
+      *reinterpret_cast<float4*>(out + 4) =
+          make_float4(acc[p][4] * scale, acc[p][5] * scale, acc[p][6] * scale, acc[p][7] * scale);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (c0 + q < r) out[q] = acc[p][q] * scale;
+    }
+  }
+}
+
+// The same product for 32 <= r <= 64 with r a multiple of 4, pipelined: a block
+// takes up to kTriBlocks consecutive 256-row groups of one problem (the grid
+// lists exactly the groups that exist) and copies the next group into shared
+// memory (asynchronous 16-byte copies, row-major with the 16-byte chunks of
+// row R XOR-swizzled by (R / 8) % 8) while it computes the current one.  Its 16
+// warps each take one column quad co4 (8 x 4 outputs per lane, lane l the row
+// octet l); the quads are dealt so that every scheduler's four warps carry the
+// same triangular work (1 + 8 + 9 + 16 = 2 + 7 + 10 + 15 = ... rows of X).  Per
+// four rows m of X a thread reads its 8 x 4 staged values and 4 x 4 X values
+// (twelve 16-byte shared loads, conflict-free) for 128 FMAs.
+constexpr int kTriBlocks = 4;
+constexpr int kTriThreads = 512;
+__host__ __device__ inline int tri_pipe_chunks(int r) { return r > 32 ? 16 : 8; }  // 16-byte chunks per staged row
+__host__ __device__ inline bool tri_pipe_ok(int r) { return r >= 32 && r <= 64 && (r & 3) == 0; }
+__host__ __device__ inline size_t tri_pipe_smem_bytes(int r) {
+  return 2 * (size_t)256 * tri_pipe_chunks(r) * 16 + (size_t)r * ((r + 7) / 8 * 8) * 4;
+}
+struct TriGrid {
+  int blk_begin[kMaxBatch + 1];  // blocks of problem i: [blk_begin[i], blk_begin[i + 1])
+};
+__global__ void __launch_bounds__(kTriThreads, 1) tri_apply_pipe_kernel(const __grid_constant__ ProjBatch batch,
+                                                                        const __grid_constant__ TriGrid grid,
+                                                                        int final_pass) {
+  extern __shared__ __align__(16) float smem[];
+  int y = 0;  // this block's problem
+  {
+    int lo = 0, hi = batch.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (grid.blk_begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    }
+    y = lo;
+  }
+  const ProjProblem& pb = batch.p[y];
+  const int r = batch.r, r8 = (r + 7) / 8 * 8, ldc = tri_pipe_chunks(r), nc = r >> 2;
+  float* Sbuf = smem;                    // 2 x 256 rows x ldc chunks
+  float* Xs = smem + 2 * 256 * ldc * 4;  // r x r8
+  const int64_t first = (int64_t)((int)blockIdx.x - grid.blk_begin[y]) * kTriBlocks * 256;
+  const int64_t left = (pb.k - first + 255) / 256;
+  const int nblk = left < kTriBlocks ? (int)left : kTriBlocks;
+  float* P = pb.P;
+  auto stage = [&](int blk, int buf) {  // rows [row0, row0 + 256) into buffer buf, zero past k
+    const int64_t row0 = first + (int64_t)blk * 256;
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(Sbuf + (size_t)buf * 256 * ldc * 4);
+    for (int e = threadIdx.x; e < 256 * nc; e += kTriThreads) {
+      const int R = e / nc, c = e % nc;
+      const bool in = row0 + R < pb.k;
+      const float* src = in ? P + (row0 + R) * r + 4 * c : P;
+      const uint32_t dst = base + (uint32_t)(R * ldc + (c ^ ((R >> 3) & 7))) * 16u;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(in ? 16 : 0)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  stage(0, 0);
+  const float* __restrict__ X = pb.rinv;
+  for (int e = threadIdx.x; e < r * r8; e += kTriThreads) {
+    const int m = e / r8, c = e % r8;
+    Xs[e] = c < r ? X[(size_t)m * r + c] : 0.f;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // scheduler warp % 4 holds the quads {s, 7 - s, 8 + s, 15 - s}
+  const int sch = warp & 3, slot = warp >> 2;
+  const int co4 = slot == 0 ? sch : slot == 1 ? 7 - sch : slot == 2 ? 8 + sch : 15 - sch;
+  const int c0 = 4 * co4, q0 = 8 * lane;
+  const bool busy = c0 < r;
+  const int mend = (c0 + 4) < r ? (c0 + 4) : r;  // X is upper triangular; a multiple of 4
+  const float scale = final_pass ? pb.scale : 1.0f;
+  for (int blk = 0; blk < nblk; ++blk) {
+    if (blk + 1 < nblk) {
+      stage(blk + 1, (blk + 1) & 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();  // this group's rows (and X) are in shared memory
+    const int64_t row0 = first + (int64_t)blk * 256;
+    if (busy && row0 + q0 < pb.k) {
+      const float4* S4 = reinterpret_cast<const float4*>(Sbuf + (size_t)(blk & 1) * 256 * ldc * 4);
+      float acc[8][4];
+#pragma unroll
+      for (int p = 0; p < 8; ++p)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[p][q] = 0.f;
+      for (int m0 = 0; m0 < mend; m0 += 4) {
+        const int ch = (m0 >> 2) ^ (lane & 7);
+        float4 sv[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) sv[p] = S4[(q0 + p) * ldc + ch];
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+          const float4 xa = *reinterpret_cast<const float4*>(Xs + (m0 + mm) * r8 + c0);
+          const float xv[4] = {xa.x, xa.y, xa.z, xa.w};
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const float sp = mm == 0 ? sv[p].x : mm == 1 ? sv[p].y : mm == 2 ? sv[p].z : sv[p].w;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(sp, xv[q], acc[p][q]);
+          }
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        if (row0 + q0 + p >= pb.k) break;
+        float* out = P + (row0 + q0 + p) * r + c0;
+        *reinterpret_cast<float4*>(out) =
+            make_float4(acc[p][0] * scale, acc[p][1] * scale, acc[p][2] * scale, acc[p][3] * scale);
+      }
+    }
+    __syncthreads();  // the buffer is refilled two groups on
+  }
+}
+
 }  // namespace
 
 void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
@@ -286,14 +501,42 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
   err = cudaFuncSetAttribute(tri_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)apply_smem);
   if (err != cudaSuccess) return err;
+  const bool pipe = tri_pipe_ok(r);
+  const size_t pipe_smem = pipe ? tri_pipe_smem_bytes(r) : 0;
+  if (pipe) {
+    err = cudaFuncSetAttribute(tri_apply_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)pipe_smem);
+    if (err != cudaSuccess) return err;
+  }
+  static thread_local TriGrid tg;
+  if (pipe) {
+    tg.blk_begin[0] = 0;
+    for (int i = 0; i < batch.n; ++i)
+      tg.blk_begin[i + 1] = tg.blk_begin[i] + (int)ceil_div(batch.p[i].k, (int64_t)256 * kTriBlocks);
+  }
+  const bool small = !pipe && r <= 64;
+  const int small_rows = small ? tri_rows_small(r) : 0;
+  const size_t small_smem = small ? sizeof(float) * tri_small_smem_floats(r) : 0;
+  if (small) {
+    err = cudaFuncSetAttribute(tri_apply_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)small_smem);
+    if (err != cudaSuccess) return err;
+  }
   for (int pass = 0; pass < 2; ++pass) {
     err = launch_gram(gb, stream);
     if (err != cudaSuccess) return err;
     count_launch();
     chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch);
     count_launch();
-    tri_apply_kernel<<<dim3((unsigned)ceil_div(max_k, apply_rows), batch.n), 256, apply_smem, stream>>>(
-        batch, pass == 1);
+    if (pipe)
+      tri_apply_pipe_kernel<<<(unsigned)tg.blk_begin[batch.n], kTriThreads, pipe_smem, stream>>>(batch, tg,
+                                                                                                  pass == 1);
+    else if (small)
+      tri_apply_small_kernel<<<dim3((unsigned)ceil_div(max_k, small_rows), batch.n), 256, small_smem, stream>>>(
+          batch, pass == 1);
+    else
+      tri_apply_kernel<<<dim3((unsigned)ceil_div(max_k, apply_rows), batch.n), 256, apply_smem, stream>>>(
+          batch, pass == 1);
   }
   return cudaGetLastError();
 }
