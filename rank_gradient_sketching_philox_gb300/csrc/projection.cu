@@ -44,17 +44,23 @@ __global__ void __launch_bounds__(256) rademacher_kernel(const ProjBatch batch) 
 // Box-Muller on one Philox block: 4 standard normal draws for elements
 // 4b .. 4b+3; lanes 0,1 use words (0,1) and lanes 2,3 use words (2,3); even
 // lanes take the cosine branch, odd lanes the sine branch.  u = (w + 1/2) 2^-32.
+// The hardware approximations serve: the draws only seed the QR frame, which is
+// checked against the exact frame to 1e-5, and their errors (a few 2^-22
+// absolute) are far below that.  cos and sin of 2 pi u are taken as -cos and
+// -sin of 2 pi (u - 1/2), an argument in [-pi, pi) where the approximations hold
+// their bound.
 __device__ __forceinline__ float4 gaussian4(const Philox4& blk) {
   const float u0 = fmaf((float)blk.w0, 0x1p-32f, 0x1p-33f);
   const float u1 = fmaf((float)blk.w1, 0x1p-32f, 0x1p-33f);
   const float u2 = fmaf((float)blk.w2, 0x1p-32f, 0x1p-33f);
   const float u3 = fmaf((float)blk.w3, 0x1p-32f, 0x1p-33f);
-  const float ra = sqrtf(-2.0f * logf(u0));
-  const float rb = sqrtf(-2.0f * logf(u2));
+  constexpr float kTwoPi = 6.28318530717958647692f;
+  const float ra = sqrtf(-2.0f * __logf(u0));
+  const float rb = sqrtf(-2.0f * __logf(u2));
   float sa, ca, sb, cb;
-  sincospif(2.0f * u1, &sa, &ca);
-  sincospif(2.0f * u3, &sb, &cb);
-  return make_float4(ra * ca, ra * sa, rb * cb, rb * sb);
+  __sincosf(kTwoPi * (u1 - 0.5f), &sa, &ca);
+  __sincosf(kTwoPi * (u3 - 0.5f), &sb, &cb);
+  return make_float4(-ra * ca, -ra * sa, -rb * cb, -rb * sb);
 }
 
 __global__ void __launch_bounds__(256) gaussian_kernel(const ProjBatch batch) {
@@ -72,9 +78,15 @@ __device__ __forceinline__ int packed_upper(int i, int j, int r) {
 
 // One block per problem.  Cholesky of the r x r Gram matrix (packed upper
 // triangle in shared memory, right-looking), then the upper-triangular inverse
-// R^-1 written in full (zeros below the diagonal) to pb.rinv.
+// R^-1 written in full (zeros below the diagonal) to pb.rinv.  For r <= 128 the
+// inverse is built in shared memory and copied out at the end (each of its r
+// row steps reads the rows below it); larger ones build it in place.
+__host__ __device__ inline bool chol_x_in_smem(int r) { return r <= 128; }
+__host__ __device__ inline size_t chol_smem_floats(int r) {
+  return (((size_t)r * (r + 1) / 2 + 3) & ~size_t(3)) + (chol_x_in_smem(r) ? (size_t)r * r : 0);
+}
 __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
-  extern __shared__ float R[];  // r(r+1)/2
+  extern __shared__ float R[];  // r(r+1)/2, then (r <= 128) r x r for X
   const ProjProblem& pb = batch.p[blockIdx.x];
   const int r = batch.r;
   const int tid = threadIdx.x, nthreads = blockDim.x;
@@ -102,12 +114,13 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
     }
     __syncthreads();
   }
-  float* X = pb.rinv;
   if (broken) {
-    for (int e = tid; e < r * r; e += nthreads) X[e] = 0.0f;
+    for (int e = tid; e < r * r; e += nthreads) pb.rinv[e] = 0.0f;
     if (tid == 0) atomicOr(batch.status, SKETCH_DEV_QR_BREAKDOWN);
     return;
   }
+  const bool xs = chol_x_in_smem(r);
+  float* X = xs ? R + (((size_t)r * (r + 1) / 2 + 3) & ~size_t(3)) : pb.rinv;
   // X = R^-1, rows from the bottom: X[i][j] = -(sum_{m=i+1..j} R[i][m] X[m][j]) / R[i][i].
   for (int i = r - 1; i >= 0; --i) {
     const float inv_ii = 1.0f / R[packed_upper(i, i, r)];
@@ -118,14 +131,27 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
       } else if (j == i) {
         v = inv_ii;
       } else {
-        float s = 0.0f;
-        for (int m = i + 1; m <= j; ++m) s = fmaf(R[packed_upper(i, m, r)], X[m * r + j], s);
+        // four partial sums (terms m = i+1.. in turn) so that the loads and
+        // multiply-adds of one row step overlap instead of forming one chain
+        const float* Ri = R + packed_upper(i, 0, r);  // Ri[m] = R[i][m] for m >= i
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        int m = i + 1;
+        for (; m + 3 <= j; m += 4) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) s4[t] = fmaf(Ri[m + t], X[(m + t) * r + j], s4[t]);
+        }
+        if (m <= j) s4[0] = fmaf(Ri[m], X[m * r + j], s4[0]);
+        if (m + 1 <= j) s4[1] = fmaf(Ri[m + 1], X[(m + 1) * r + j], s4[1]);
+        if (m + 2 <= j) s4[2] = fmaf(Ri[m + 2], X[(m + 2) * r + j], s4[2]);
+        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         v = -s * inv_ii;
       }
       X[i * r + j] = v;
     }
     __syncthreads();
   }
+  if (xs)
+    for (int e = tid; e < r * r; e += nthreads) pb.rinv[e] = X[e];
 }
 
 // P rows [32*blockIdx.x, +32) <- scale * P_rows * Rinv (Rinv upper triangular).
@@ -492,7 +518,7 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
     gb.e[i].partials = batch.p[i].partials;
     gb.e[i].out = batch.p[i].gram;
   }
-  const size_t chol_smem = sizeof(float) * (size_t)r * (r + 1) / 2;
+  const size_t chol_smem = sizeof(float) * chol_smem_floats(r);
   const int apply_rows = tri_rows(r);
   const size_t apply_smem = sizeof(float) * tri_smem_floats(r);
   cudaError_t err = cudaFuncSetAttribute(chol_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
