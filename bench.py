@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="steps in the end-to-end (host buffers) measurement; default = --steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-shared-x", action="store_true",
+                    help="give q/k/v and gate/up inputs of their own instead of one shared X each")
     ap.add_argument("--layers", type=int, default=None,
                     help="keep only the first N layers of the workload (a smaller case for profiling)")
     return ap.parse_args()
@@ -67,8 +69,8 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def workload_config(wl, r, n):
-    return {
+def workload_config(wl, r, n, shared_x=None):
+    cfg = {
         "workload": wl.name,
         "layers": len(wl.layers),
         "weights": wl.weights,
@@ -81,6 +83,9 @@ def workload_config(wl, r, n):
         "l2": "inputs rotate through %d buffers per shape (reuse distance > 4x L2); W, C, P per layer"
               % NBUF,
     }
+    if shared_x is not None:
+        cfg["inputs"] = shared_x
+    return cfg
 
 
 # --------------------------------------------------------------------------
@@ -280,8 +285,19 @@ def main():
     # every layer's sketch in one buffer: one all-reduce per step across replicas
     C_flat, C = dataparallel.flat_sketches([(d, r) for _, d, _ in layers], dev)
     P = [torch.empty(k, r, dtype=torch.float32, device=dev) for _, _, k in layers]
-    XP = [torch.empty(T, max(8, (r + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :r]
-          for _ in layers]
+    # layers that read one X (q/k/v, gate/up) are projected together: one call
+    # with the split of their concatenated P reads X once; each layer's XP is a
+    # column block of its group's result
+    groups = ([[li] for li in range(L)] if args.no_shared_x or r % 8 != 0
+              else synth.input_groups(layers))
+    XPg = [torch.empty(T, max(8, (len(g) * r + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :len(g) * r]
+           for g in groups]
+    XP = [None] * L
+    for gi, g in enumerate(groups):
+        for q, li in enumerate(g):
+            XP[li] = XPg[gi][:, q * r:(q + 1) * r]
+    sizes = sorted({len(g) for g in groups})
+    by_size = {m: [gi for gi, g in enumerate(groups) if len(g) == m] for m in sizes}
     wn2 = torch.zeros(L, dtype=torch.float64, device=dev)
     status = torch.zeros(L, dtype=torch.int32, device=dev)
     xpool, dpool = {}, {}
@@ -305,26 +321,31 @@ def main():
     ws_sample = torch.empty(rgs.workspace_bytes_batched(
         binding.OP_SAMPLE_PROJECTION, k=[k for _, _, k in layers], r=r) if kind == rgs.PROJ_GAUSSIAN_QR
         else 1, dtype=torch.uint8, device=dev)
-    ws_project = torch.empty(max(1, rgs.workspace_bytes_batched(
-        binding.OP_PROJECT_INPUTS, T=[T] * L, k=[k for _, _, k in layers], r=r)), dtype=torch.uint8, device=dev)
+    ws_project = {m: torch.empty(max(1, rgs.workspace_bytes_batched(
+        binding.OP_PROJECT_INPUTS, T=[T] * len(by_size[m]), k=[layers[groups[gi][0]][2] for gi in by_size[m]],
+        r=m * r)), dtype=torch.uint8, device=dev) for m in sizes}
     ws_update = torch.empty(rgs.workspace_bytes_batched(
         binding.OP_UPDATE_NORMSGD, d=[d for _, d, _ in layers], k=[k for _, _, k in layers], r=r),
         dtype=torch.uint8, device=dev)
     wn2_views = [wn2[li:li + 1] for li in range(L)]
     status_views = [status[li:li + 1] for li in range(L)]
 
-    # the BF16 split of each layer's P, made once per refresh and read by every
-    # microbatch's projection
-    P_split = [torch.empty(rgs.projection_split_elems(k, r), dtype=torch.int16, device=dev)
-               for _, _, k in layers]
+    # the BF16 split of each group's concatenated P, made once per refresh and
+    # read by every microbatch's projection
+    P_split = [torch.empty(rgs.projection_split_elems(layers[g[0]][2], len(g) * r), dtype=torch.int16, device=dev)
+               for g in groups]
 
     def sample_phase(s):
         rgs.sample_projection_batched(kind, seed, s, P, layer_ids, ws=ws_sample)
-        rgs.split_projection_batched(P, splits=P_split)
+        rgs.split_projection_grouped([[P[li] for li in g] for g in groups], splits=P_split)
 
     def project_phase(m, Xs=None):
-        rgs.project_inputs_batched(Xs if Xs is not None else [xbuf(li, m) for li in range(L)], P, XP,
-                                   ws=ws_project, splits=P_split)
+        # Xs: one input per group (default: the group's first layer's buffer)
+        for size in sizes:
+            gis = by_size[size]
+            rgs.project_inputs_grouped_batched(
+                [Xs[gi] if Xs is not None else xbuf(groups[gi][0], m) for gi in gis],
+                [P_split[gi] for gi in gis], size * r, [XPg[gi] for gi in gis], ws=ws_project[size])
 
     def accumulate_phase(m, Ds=None):
         rgs.accumulate_batched(Ds if Ds is not None else [dbuf(li, m) for li in range(L)], XP, C,
@@ -402,7 +423,8 @@ def main():
 
     # algorithmic bytes: the minimum each call must move
     acc_bytes = sum(nmb * (2 * T * d + 2 * T * r + 8 * d * r) for _, d, _ in layers)
-    proj_bytes = sum(nmb * (2 * T * k + 2 * T * r + 4 * k * r) for _, _, k in layers)
+    proj_bytes = sum(nmb * (2 * T * layers[g[0]][2] + (2 * T + 4 * layers[g[0]][2]) * len(g) * r)
+                     for g in groups)
     upd_bytes = sum(4 * d * k + 8 * d * r + 8 * k * r for _, d, k in layers)
     peak, peak_kind = measured_peaks()
 
@@ -459,9 +481,9 @@ def main():
         # every layer's X and D of a microbatch come from pinned host memory
         hx = {k: [b.cpu().pin_memory() for b in v] for k, v in xpool.items()}
         hd = {d: [b.cpu().pin_memory() for b in v] for d, v in dpool.items()}
-        stage_x = [torch.empty(T, k, dtype=torch.bfloat16, device=dev) for _, _, k in layers]
+        stage_x = [torch.empty(T, layers[g[0]][2], dtype=torch.bfloat16, device=dev) for g in groups]
         stage_d = [torch.empty(T, d, dtype=torch.bfloat16, device=dev) for _, d, _ in layers]
-        h2d = nmb * sum(stage_x[li].numel() * 2 + stage_d[li].numel() * 2 for li in range(L))
+        h2d = nmb * (sum(x.numel() * 2 for x in stage_x) + sum(d_.numel() * 2 for d_ in stage_d))
         d2h = status.numel() * 4 + wn2.numel() * 8
         torch.cuda.synchronize()
         if world > 1:
@@ -471,8 +493,8 @@ def main():
         for s in range(s_next + 1, s_next + 1 + e2e_steps):
             sample_phase(s)
             for m in range(nmb):
-                for li, (_, d, k) in enumerate(layers):
-                    stage_x[li].copy_(hx[k][(li + m) % NBUF], non_blocking=True)
+                for gi, g in enumerate(groups):
+                    stage_x[gi].copy_(hx[layers[g[0]][2]][(g[0] + m) % NBUF], non_blocking=True)
                 project_phase(m, stage_x)
                 for li, (_, d, k) in enumerate(layers):
                     stage_d[li].copy_(hd[d][(li + 2 * m + 1) % NBUF], non_blocking=True)
@@ -510,7 +532,9 @@ def main():
             "vs_baseline": None,
             "dtype": "bf16+fp32",
             "data": "synthetic",
-            "config": workload_config(wl, r, world),
+            "config": workload_config(wl, r, world, shared_x=(
+                "q/k/v and gate/up read one X each, projected together (grouped splits)"
+                if any(len(g) > 1 for g in groups) else "every layer reads its own X")),
             "components": components,
             "roofline": roofline,
             "cpu_baseline": cpu,

@@ -284,6 +284,30 @@ SKETCH_API sketch_status sketch_accumulate_fp32xp_batched(int n, const sketch_ac
 SKETCH_API size_t sketch_projection_split_elems(int64_t k, int64_t r);
 SKETCH_API sketch_status sketch_split_projection_batched(int n, const sketch_split_problem* problems, int64_t r,
                                                          void* stream);
+
+/* Layers that read the same input X (q, k and v of an attention block; gate
+ * and up of an MLP) are projected together: their projections P_0 .. P_{m-1}
+ * (each k x r fp32) form the k x (m r) concatenation [P_0 | ... | P_{m-1}],
+ * whose split this call writes to P_split (sketch_projection_split_elems(k,
+ * m r) uint16_t, caller-owned, not overlapping any P).  One
+ * sketch_project_inputs_batched call with rank m r and that split then reads X
+ * once and writes, per token row, XP_0 | ... | XP_{m-1}: member q's XP is
+ * columns [q r, (q + 1) r) of the T x (m r) result, which sketch_accumulate
+ * takes as XP = result + q r with ld_xp = the result's row stride ("LoGRA:
+ * Scaling LLM Reinforcement Learning with Low-Rank Gradient Sketches", Key
+ * Contributions: selected attention and MLP projections are sketched; sharing
+ * their input is this build's way to read it once).  Each member column is
+ * the same dot product as in a separate call.  1 <= m <= 16, m r <= 256;
+ * every P 16-byte aligned; r a multiple of 8 when m > 1 (so that each
+ * member's XP starts on a 16-byte boundary). */
+typedef struct {
+    const float* const* P; /* m pointers */
+    int m;
+    int64_t k;
+    uint16_t* P_split;
+} sketch_split_group;
+SKETCH_API sketch_status sketch_split_projection_grouped(int n, const sketch_split_group* groups, int64_t r,
+                                                         void* stream);
 SKETCH_API sketch_status sketch_accumulate_batched(int n, const sketch_accumulate_problem* problems, int64_t r,
                                                    int overwrite, void* ws, size_t ws_bytes, void* stream);
 SKETCH_API sketch_status sketch_apply_update_normsgd_batched(int n, const sketch_update_problem* problems,

@@ -6,8 +6,10 @@ The compute path is the C-ABI shared library ``lib/libsketch.so`` (declared in
 ``include/sketch.h``); ``binding`` is its thin Python wrapper.
 """
 from .binding import (PROJ_GAUSSIAN_QR, PROJ_RADEMACHER, SketchError, accumulate,  # noqa: F401
-                      accumulate_batched, accumulate_fp32xp_batched, project_inputs_fp32xp_batched, xp_split_cols, apply_update_normsgd, apply_update_normsgd_batched,
-                      apply_update_sgd, apply_update_sgd_batched, kernel_launches, project_inputs,
-                      project_inputs_batched, projection_split_elems, read_device_errors,
-                      sample_projection, split_projection_batched,
-                      sample_projection_batched, workspace_bytes, workspace_bytes_batched)
+                      accumulate_batched, accumulate_fp32xp_batched, apply_update_normsgd,
+                      apply_update_normsgd_batched, apply_update_sgd, apply_update_sgd_batched,
+                      kernel_launches, project_inputs, project_inputs_batched,
+                      project_inputs_fp32xp_batched, project_inputs_grouped_batched,
+                      projection_split_elems, read_device_errors, sample_projection,
+                      sample_projection_batched, split_projection_batched, split_projection_grouped,
+                      workspace_bytes, workspace_bytes_batched, xp_split_cols)

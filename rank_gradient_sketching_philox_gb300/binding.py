@@ -41,7 +41,7 @@ EXPORTS = ("sketch_workspace_bytes", "sketch_sample_projection", "sketch_project
            "sketch_apply_update_normsgd_noalloc", "sketch_noalloc_scratch_bytes",
            "sketch_read_device_errors", "sketch_kernel_launches", "sketch_projection_split_elems",
            "sketch_split_projection_batched", "sketch_project_inputs_fp32xp_batched",
-           "sketch_accumulate_fp32xp_batched", "sketch_status_string",
+           "sketch_accumulate_fp32xp_batched", "sketch_split_projection_grouped", "sketch_status_string",
            "sketch_last_error")
 
 
@@ -101,6 +101,7 @@ _SIGS = {
     "sketch_kernel_launches": (_c.c_uint64, []),
     "sketch_projection_split_elems": (_c.c_size_t, [_i64, _i64]),
     "sketch_split_projection_batched": (_c.c_int, [_c.c_int, _vp, _i64, _vp]),
+    "sketch_split_projection_grouped": (_c.c_int, [_c.c_int, _vp, _i64, _vp]),
     "sketch_project_inputs_fp32xp_batched": (_c.c_int, [_c.c_int, _vp, _i64, _vp, _c.c_size_t, _vp]),
     "sketch_accumulate_fp32xp_batched": (_c.c_int, [_c.c_int, _vp, _i64, _c.c_int, _vp, _c.c_size_t, _vp]),
     "sketch_workspace_bytes_batched": (ctypes.c_size_t, [_c.c_int, _c.c_int, _vp, _vp, _vp, _i64]),
@@ -361,6 +362,61 @@ def split_projection_batched(Ps, splits=None, stream=None):
     h, _ = _stream_handle(stream, Ps[0].device)
     _check(lib().sketch_split_projection_batched(n, probs, r, h))
     return splits
+
+
+class SplitGroup(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_void_p), ("m", ctypes.c_int), ("k", ctypes.c_int64), ("P_split", ctypes.c_void_p)]
+
+
+def split_projection_grouped(groups, splits=None, stream=None):
+    """Splits of concatenated projections: groups is a list of lists of P
+    (k x r fp32, one k per group); group g's split is that of [P_0 | ... |
+    P_{m-1}] (k x m r), for project_inputs_grouped_batched.  Returns the split
+    buffers (uint16, allocated when not given)."""
+    n = len(groups)
+    r = groups[0][0].shape[1]
+    if splits is None:
+        splits = [torch.empty(projection_split_elems(g[0].shape[0], len(g) * r), dtype=torch.int16,
+                              device=g[0].device) for g in groups]
+    probs = (SplitGroup * n)()
+    keep = []
+    for i, (g, S) in enumerate(zip(groups, splits)):
+        k = g[0].shape[0]
+        for P in g:
+            _contig(P, torch.float32, "P")
+            if P.shape != (k, r):
+                raise ValueError("shape mismatch in group %d" % i)
+        if S.numel() * S.element_size() < 2 * projection_split_elems(k, len(g) * r):
+            raise ValueError("split buffer of group %d too small" % i)
+        ptrs = (ctypes.c_void_p * len(g))(*[P.data_ptr() for P in g])
+        keep.append(ptrs)
+        probs[i] = SplitGroup(ctypes.cast(ptrs, ctypes.c_void_p), len(g), k, S.data_ptr())
+    h, _ = _stream_handle(stream, groups[0][0].device)
+    _check(lib().sketch_split_projection_grouped(n, probs, r, h))
+    return splits
+
+
+def project_inputs_grouped_batched(Xs, splits, r_total, XPs, ws=None, stream=None):
+    """XP = bf16(X [P_0 | ... | P_{m-1}]) (T x r_total, r_total = m r) for each
+    problem, from the splits of split_projection_grouped; member q's XP is
+    XP[:, q r:(q + 1) r]."""
+    n = len(Xs)
+    probs = (ProjectProblem * n)()
+    for i, (X, S, XP) in enumerate(zip(Xs, splits, XPs)):
+        ld_x = _rows(X, torch.bfloat16, "X")
+        ld_xp = _rows(XP, torch.bfloat16, "XP")
+        if XP.shape[0] != X.shape[0] or XP.shape[1] < r_total:
+            raise ValueError("shape mismatch in problem %d" % i)
+        if S.numel() * S.element_size() < 2 * projection_split_elems(X.shape[1], r_total):
+            raise ValueError("split buffer of problem %d too small" % i)
+        probs[i] = ProjectProblem(X.data_ptr(), X.shape[0], X.shape[1], ld_x, None, XP.data_ptr(), ld_xp,
+                                  S.data_ptr())
+    h, s = _stream_handle(stream, Xs[0].device)
+    nbytes = workspace_bytes_batched(OP_PROJECT_INPUTS, T=[X.shape[0] for X in Xs],
+                                     k=[X.shape[1] for X in Xs], r=r_total)
+    wsb = _workspace(nbytes, Xs[0].device, s, ws)
+    _check(lib().sketch_project_inputs_batched(n, probs, r_total, _ptr(wsb), nbytes, h))
+    return XPs
 
 
 def _project_batched(Xs, Ps, XPs, ws, stream, splits, fn, xp_cols):

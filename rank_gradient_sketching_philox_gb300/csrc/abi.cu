@@ -391,6 +391,34 @@ sketch_status sketch_split_projection_batched(int n, const sketch_split_problem*
                        "split_projection");
 }
 
+sketch_status sketch_split_projection_grouped(int n, const sketch_split_group* groups, int64_t r, void* stream) {
+  TRY(check_n(n));
+  if (groups == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "groups is NULL");
+  TRY(check_rank(r));
+  std::vector<rgs::SplitGroup> g((size_t)n);
+  for (int i = 0; i < n; ++i) {
+    const sketch_split_group& gr = groups[i];
+    if (gr.m < 1 || gr.m > rgs::kMaxGroup)
+      return fail(SKETCH_ERR_INVALID_ARG, "group %d: m=%d out of [1, %d]", i, gr.m, rgs::kMaxGroup);
+    if ((int64_t)gr.m * r > rgs::kMaxRank)
+      return fail(SKETCH_ERR_INVALID_ARG, "group %d: m*r=%lld exceeds %d", i, (long long)gr.m * r, rgs::kMaxRank);
+    if (gr.m > 1 && r % 8 != 0)
+      return fail(SKETCH_ERR_INVALID_ARG, "group %d: r=%lld must be a multiple of 8 when m > 1", i, (long long)r);
+    if (gr.P == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "group %d: P is NULL", i);
+    TRY(check_k(gr.k));
+    CHECK_PTR(gr.P_split);
+    g[i].m = gr.m;
+    g[i].k = gr.k;
+    g[i].out = gr.P_split;
+    for (int q = 0; q < gr.m; ++q) {
+      CHECK_PTR(gr.P[q]);
+      g[i].P[q] = gr.P[q];
+    }
+  }
+  return launch_result(rgs::launch_split_projection_grouped(n, g.data(), (int)r, static_cast<cudaStream_t>(stream)),
+                       "split_projection_grouped");
+}
+
 sketch_status sketch_accumulate(const uint16_t* D, int64_t T, int64_t d, int64_t ld_d, const uint16_t* XP,
                                 int64_t ld_xp, int64_t r, float* C, int overwrite, void* ws, size_t ws_bytes,
                                 void* stream) {

@@ -105,6 +105,17 @@ size_t project_workspace_bytes(int64_t T, int64_t k, int64_t r);
 // P (k x r fp32) -> [hi(P^T); lo(P^T)] (2 n_pad x k BF16) for each problem.
 cudaError_t launch_split_projection(int n, const float* const* P, const int64_t* k, uint16_t* const* out, int r,
                                     cudaStream_t stream);
+// A group of projections of one k that share their inputs X: their split is
+// that of the k x (m r) concatenation [P_0 | ... | P_{m-1}], so one projection
+// call with rank m r reads X once for all of them.
+constexpr int kMaxGroup = 16;
+struct SplitGroup {
+  const float* P[kMaxGroup];
+  int m;
+  int64_t k;
+  uint16_t* out;
+};
+cudaError_t launch_split_projection_grouped(int n, const SplitGroup* groups, int r, cudaStream_t stream);
 // Workspace: the problems' regions of project_workspace_bytes, back to back.
 // xp_split: write XP as a BF16 pair (hi in columns [0, r), lo = bf16(XP - hi) at
 // [n_pad, n_pad + r), n_pad = r rounded up to 16) instead of one BF16 rounding.

@@ -239,13 +239,19 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_gemm_kernel(const __grid_c
 // P (k x r fp32) -> P^T split into BF16 high and low parts: rows [0, n_pad)
 // hold the high part, rows [n_pad, 2 n_pad) the low part, each k wide; rank
 // rows r..n_pad-1 are zero.  32 x 32 tiles transposed through shared memory;
-// grid.z indexes the problem.
+// grid.z indexes the problem.  Problem i writes rows [row_off, row_off + rows)
+// of the high half and the same rows of the low half (which starts n_pad_out
+// rows down); rows past r are zero.  A plain split has row_off 0 and rows =
+// n_pad = n_pad_out; the members of a group write their r rows one after
+// another and the last one also the padding.
 struct SplitT {
   const float* P[kMaxProblems];
   uint16_t* out[kMaxProblems];
   int64_t k[kMaxProblems];
+  int row_off[kMaxProblems];
+  int rows[kMaxProblems];
+  int n_pad_out[kMaxProblems];
   int r;
-  int n_pad;
 };
 
 __global__ void __launch_bounds__(256) split_transpose_kernel(const __grid_constant__ SplitT a) {
@@ -256,7 +262,8 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const __grid_const
   if (j0 >= k) return;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int l0 = blockIdx.y * 32;
-  const int r = a.r, n_pad = a.n_pad;
+  const int r = a.r, rows = a.rows[pr];
+  if (l0 >= rows) return;
   const float* P = a.P[pr];
   for (int dy = ty; dy < 32; dy += 8) {
     const int64_t j = j0 + dy;
@@ -264,12 +271,12 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const __grid_const
     t[dy][tx] = (j < k && l < r) ? P[j * r + l] : 0.f;
   }
   __syncthreads();
-  uint16_t* hi = a.out[pr];
-  uint16_t* lo = hi + (int64_t)n_pad * k;
+  uint16_t* hi = a.out[pr] + (int64_t)a.row_off[pr] * k;
+  uint16_t* lo = hi + (int64_t)a.n_pad_out[pr] * k;
   for (int dy = ty; dy < 32; dy += 8) {
     const int l = l0 + dy;
     const int64_t j = j0 + tx;
-    if (l < n_pad && j < k) {
+    if (l < rows && j < k) {
       const float v = t[tx][dy];
       const __nv_bfloat16 h = __float2bfloat16_rn(v);
       const __nv_bfloat16 w = __float2bfloat16_rn(v - __bfloat162float(h));
@@ -304,7 +311,11 @@ cudaError_t launch_skinny(SkinnyBatch& a, cudaStream_t stream) {
   for (int i = 1; i < a.n; ++i) min_chunks = a.kchunks[i] < min_chunks ? a.kchunks[i] : min_chunks;
   const int split = choose_split(tiles, min_chunks);
   a.stage_bytes = a.a_bytes + NB * a.b_bytes;
-  const uint32_t budget = 96u * 1024u;  // two CTAs per SM when the stages fit
+  // two CTAs per SM when the stages fit in half of shared memory; stages wider
+  // than 48 KB (a B of 192+ rank columns, as grouped projections have) get
+  // the whole SM, since two of them per CTA would leave too few K chunks in
+  // flight to cover the loads
+  const uint32_t budget = a.stage_bytes > 48u * 1024u ? 208u * 1024u : 96u * 1024u;
   int stages = (int)(budget / a.stage_bytes);
   if (stages < 2) stages = 2;
   if (stages > kMaxStages) stages = kMaxStages;
@@ -356,15 +367,54 @@ cudaError_t launch_split_projection(int n, const float* const* P, const int64_t*
       sp.P[i] = P[base + i];
       sp.out[i] = out[base + i];
       sp.k[i] = k[base + i];
+      sp.row_off[i] = 0;
+      sp.rows[i] = n_pad;
+      sp.n_pad_out[i] = n_pad;
       max_k = k[base + i] > max_k ? k[base + i] : max_k;
     }
     sp.r = r;
-    sp.n_pad = n_pad;
     count_launch();
     split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 32), (unsigned)ceil_div(n_pad, 32), (unsigned)m), 256, 0,
                              stream>>>(sp);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_split_projection_grouped(int n, const SplitGroup* groups, int r, cudaStream_t stream) {
+  static thread_local SplitT sp;
+  int i = 0, max_rows = 0;
+  int64_t max_k = 0;
+  auto flush = [&]() -> cudaError_t {
+    if (i == 0) return cudaSuccess;
+    sp.r = r;
+    count_launch();
+    split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 32), (unsigned)ceil_div(max_rows, 32), (unsigned)i), 256,
+                             0, stream>>>(sp);
+    i = 0;
+    max_rows = 0;
+    max_k = 0;
+    return cudaGetLastError();
+  };
+  for (int g = 0; g < n; ++g) {
+    const SplitGroup& gr = groups[g];
+    const int n_pad_out = round16(gr.m * r);
+    for (int q = 0; q < gr.m; ++q) {
+      if (i == kMaxProblems) {
+        const cudaError_t err = flush();
+        if (err != cudaSuccess) return err;
+      }
+      sp.P[i] = gr.P[q];
+      sp.out[i] = gr.out;
+      sp.k[i] = gr.k;
+      sp.row_off[i] = q * r;
+      sp.rows[i] = (q + 1 == gr.m) ? n_pad_out - q * r : r;
+      sp.n_pad_out[i] = n_pad_out;
+      max_rows = sp.rows[i] > max_rows ? sp.rows[i] : max_rows;
+      max_k = gr.k > max_k ? gr.k : max_k;
+      ++i;
+    }
+  }
+  return flush();
 }
 
 cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, void* ws, cudaStream_t stream,

@@ -94,6 +94,24 @@ def _block(prefix, hidden, kv, inter):
             (prefix + "up", inter, hidden), (prefix + "down", hidden, inter)]
 
 
+def input_groups(layers):
+    """Indices of the layers that read the same input X, in order: q, k and v
+    of a block read the attention input, gate and up the MLP input; every
+    other layer reads its own."""
+    groups, open_ = [], {}
+    for li, (name, _, _) in enumerate(layers):
+        prefix, _, kind = name.rpartition(".")
+        key = (prefix, "attn") if kind in ("q", "k", "v") else (prefix, "mlp") if kind in ("gate", "up") else None
+        if key is None:
+            groups.append([li])
+        elif key in open_:
+            groups[open_[key]].append(li)
+        else:
+            open_[key] = len(groups)
+            groups.append([li])
+    return groups
+
+
 def qwen3_stack(blocks, hidden, kv, inter):
     layers = []
     for b in range(blocks):

@@ -166,3 +166,25 @@ def test_fp32_xp_needs_room_for_the_pair(lib):
     assert _call("sketch_accumulate_fp32xp_batched", 1, ap, 8, 1, NULL, 0, NULL) == binding.ERR_INVALID_ARG
     assert binding.kernel_launches() == before
     assert binding.xp_split_cols(64) == 128 and binding.xp_split_cols(20) == 64
+
+
+def test_grouped_split_rejects_bad_groups(lib):
+    """Grouped splits: 1 <= m <= 16, m r <= 256, r a multiple of 8 when m > 1,
+    every pointer present; rejected on the host with no launch."""
+    before = binding.kernel_launches()
+    ptrs = (ctypes.c_void_p * 3)(1 << 20, 1 << 21, 1 << 22)
+    P = ctypes.cast(ptrs, ctypes.c_void_p)
+
+    def grouped(m, k, r, split=1 << 23, p=P):
+        g = (binding.SplitGroup * 1)(binding.SplitGroup(p, m, k, split))
+        return _call("sketch_split_projection_grouped", 1, g, r, NULL)
+
+    assert grouped(0, 64, 64) == binding.ERR_INVALID_ARG
+    assert grouped(17, 64, 8) == binding.ERR_INVALID_ARG
+    assert grouped(3, 64, 96) == binding.ERR_INVALID_ARG        # 3 * 96 > 256
+    assert "256" in binding.lib().sketch_last_error().decode()
+    assert grouped(3, 64, 20) == binding.ERR_INVALID_ARG        # members would start off 16-byte boundaries
+    assert grouped(3, 60, 64) == binding.ERR_INVALID_ARG        # k not a multiple of 8
+    assert grouped(3, 64, 64, split=None) == binding.ERR_INVALID_ARG
+    assert grouped(3, 64, 64, p=None) == binding.ERR_INVALID_ARG
+    assert binding.kernel_launches() == before

@@ -183,6 +183,30 @@ def test_project_inputs_full_size_sampled_tokens(T, k, r, kind):
 # (c) accumulation
 # --------------------------------------------------------------------------
 
+@pytest.mark.parametrize("T,k,r,m", [(300, 512, 64, 3), (129, 1024, 64, 2), (64, 256, 16, 4), (1, 8, 8, 1),
+                                     (200, 4096, 32, 8)])
+def test_grouped_projection_reads_x_once(T, k, r, m):
+    """Members sharing X, projected in one call from the split of their
+    concatenation: each member's columns equal its own projection call, bit for
+    bit, and match the oracle; the accumulate reads each member's columns
+    through the shared result's row stride."""
+    Ps = [torch.from_numpy(orc.sample_rademacher(11, q, 2, k, r)).to(DEV) for q in range(m)]
+    X = synth.normal_bf16((T, k), 1.0, 41).to(DEV)
+    split = rgs.split_projection_grouped([Ps])[0]
+    XPg = _padded_bf16(T, m * r)
+    rgs.project_inputs_grouped_batched([X], [split], m * r, [XPg])
+    D = synth.normal_bf16((T, 96), 1e-2, 42).to(DEV)
+    for q in range(m):
+        own = _padded_bf16(T, r)
+        rgs.project_inputs(X, Ps[q], own)
+        member = XPg[:, q * r:(q + 1) * r]
+        assert torch.equal(bits_t(member), bits_t(own)), q
+        _xp_check(bits(member), orc.project_inputs(bits(X), Ps[q].cpu().numpy()))
+        C = torch.empty(96, r, dtype=torch.float32, device=DEV)
+        rgs.accumulate(D, member, C, overwrite=True)
+        _c_check(C.cpu().numpy(), orc.accumulate(bits(D), bits(own), np.zeros((96, r)), True))
+
+
 def _c_check(got, ref):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
