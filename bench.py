@@ -55,7 +55,7 @@ def parse():
 # one ncu capture of one Qwen3-8B block (profiles/qwen3_8b_one_block_kernels.md);
 # traffic grows with the units processed, so a full launch's traffic is this
 # ratio times its algorithmic bytes.
-TRAFFIC_PER_ALGORITHMIC_BYTE = {"project_inputs": 244.3 / 315.0, "accumulate": 268.3 / 342.4,
+TRAFFIC_PER_ALGORITHMIC_BYTE = {"project_inputs": 214.3 / 214.4, "accumulate": 268.8 / 342.4,
                                 "update_normsgd": 786.3 / 791.4}
 
 
