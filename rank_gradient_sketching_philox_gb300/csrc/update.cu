@@ -128,49 +128,84 @@ struct SplitBatch {
   int r_pad;
 };
 
-// One warp per row, grid-stride over the rows of all entries: x = hi + lo to
-// 2^-17 relative (columns r..r_pad-1 zero) and ||row||_2.  Lane l takes the
-// columns 4l..4l+3 of each 128-column step (vector loads and stores when r is
-// a multiple of 4).
+// Rows of all entries, grid-stride: x = hi + lo to 2^-17 relative (columns
+// r..r_pad-1 zero) and ||row||_2.  A row takes lpr lanes (r_pad / 4 rounded up
+// to a power of two, at most 32), lane c its columns 4c..4c+3 of each 4 lpr
+// step; a warp holds 32 / lpr rows at a time and four such steps, their loads
+// issued before any is used, so one round trip serves up to 4 * 32 / lpr rows.
 __global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__ SplitBatch b) {
+  constexpr int kU = 4;
   const int lane = threadIdx.x & 31;
   const int64_t total = b.row_begin[b.n];
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const bool vec = (b.r & 3) == 0;
-  int en = 0;  // rows of a warp only move forward
-  for (int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < total; g += warps) {
-    while (en + 1 < b.n && b.row_begin[en + 1] <= g) ++en;
-    const int64_t row = g - b.row_begin[en];
-    const float* src = b.src[en] + row * b.r;
-    uint16_t* dst = b.dst[en] + row * 2 * b.r_pad;
-    float sq = 0.f;
-    for (int c0 = 4 * lane; c0 < b.r_pad; c0 += 128) {
-      float v[4];
-      if (vec && c0 < b.r) {
+  int lpr = 1;
+  while (lpr < 32 && 4 * lpr < b.r_pad) lpr <<= 1;
+  const int rps = 32 / lpr, sub = lane / lpr, cl = lane % lpr;
+  int en[kU];  // entry of each step's row (rows of a lane only move forward)
+#pragma unroll
+  for (int u = 0; u < kU; ++u) en[u] = 0;
+  for (int64_t g0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kU * rps; g0 < total;
+       g0 += warps * kU * rps) {
+    float v[kU][4];
+    int64_t row[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t gr = g0 + (int64_t)u * rps + sub;
+      row[u] = -1;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) v[u][t] = 0.f;
+      if (gr >= total) continue;
+      while (en[u] + 1 < b.n && b.row_begin[en[u] + 1] <= gr) ++en[u];
+      row[u] = gr - b.row_begin[en[u]];
+      const float* src = b.src[en[u]] + row[u] * b.r;
+      const int c0 = 4 * cl;
+      if (c0 >= b.r) continue;
+      if (vec) {
         const float4 f = *reinterpret_cast<const float4*>(src + c0);
-        v[0] = f.x;
-        v[1] = f.y;
-        v[2] = f.z;
-        v[3] = f.w;
+        v[u][0] = f.x;
+        v[u][1] = f.y;
+        v[u][2] = f.z;
+        v[u][3] = f.w;
       } else {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) v[t] = (c0 + t < b.r) ? src[c0 + t] : 0.f;
+        for (int t = 0; t < 4; ++t) v[u][t] = (c0 + t < b.r) ? src[c0 + t] : 0.f;
       }
-      uint16_t hi[4], lo[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        sq = fmaf(v[t], v[t], sq);
-        const __nv_bfloat16 h = __float2bfloat16_rn(v[t]);
-        hi[t] = __bfloat16_as_ushort(h);
-        lo[t] = __bfloat16_as_ushort(__float2bfloat16_rn(v[t] - __bfloat162float(h)));
-      }
-      // r_pad is a multiple of 16: the 4 columns are inside the row, 8-byte aligned
-      *reinterpret_cast<uint2*>(dst + c0) = make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
-      *reinterpret_cast<uint2*>(dst + b.r_pad + c0) =
-          make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
     }
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-    if (lane == 0) b.norm[en][row] = sqrtf(sq);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      float sq = 0.f;
+      if (row[u] >= 0) {
+        uint16_t* dst = b.dst[en[u]] + row[u] * 2 * b.r_pad;
+        for (int c0 = 4 * cl; c0 < b.r_pad; c0 += 4 * lpr) {
+          float w[4];
+          if (c0 == 4 * cl) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) w[t] = v[u][t];
+          } else {  // rows wider than 4 lpr columns (r_pad > 128): the rest here
+            const float* src = b.src[en[u]] + row[u] * b.r;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) w[t] = (c0 + t < b.r) ? src[c0 + t] : 0.f;
+          }
+          uint16_t hi[4], lo[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            sq = fmaf(w[t], w[t], sq);
+            const __nv_bfloat16 h = __float2bfloat16_rn(w[t]);
+            hi[t] = __bfloat16_as_ushort(h);
+            lo[t] = __bfloat16_as_ushort(__float2bfloat16_rn(w[t] - __bfloat162float(h)));
+          }
+          // r_pad is a multiple of 16: the 4 columns are inside the row, 8-byte aligned
+          *reinterpret_cast<uint2*>(dst + c0) =
+              make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+          *reinterpret_cast<uint2*>(dst + b.r_pad + c0) =
+              make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+        }
+      }
+      // the row's lanes sum their squares (groups of lpr lanes)
+      for (int o = lpr >> 1; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+      if (row[u] >= 0 && cl == 0) b.norm[en[u]][row[u]] = sqrtf(sq);
+    }
   }
 }
 
