@@ -601,7 +601,6 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       const float thr_row = row_ok ? fabsf(s) * a.c_norm[p][i] * 0x1p-5f : 0.f;
       const uint32_t layer = a.layer[p];
       const bool need_norm = a.wnorm2_out[p] != nullptr;
-      uint16_t* wrow = a.W[p] + (int64_t)(row_ok ? i : 0) * a.ld_w[p];
       float sq = 0.f, sq_comp = 0.f;  // Kahan-compensated sum of squares
 
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
