@@ -69,6 +69,19 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def input_note(groups):
+    return ("q/k/v and gate/up read one X each, projected together (grouped splits)"
+            if any(len(g) > 1 for g in groups) else "every layer reads its own X")
+
+
+def workload_groups(wl, r, no_shared_x):
+    """Layers that read one X (q/k/v, gate/up), or one group per layer."""
+    from rank_gradient_sketching_philox_gb300 import synth
+    if no_shared_x or r % 8 != 0:
+        return [[li] for li in range(len(wl.layers))]
+    return synth.input_groups(wl.layers)
+
+
 def workload_config(wl, r, n, shared_x=None):
     cfg = {
         "workload": wl.name,
@@ -181,7 +194,8 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": workload_config(wl, args.rank, args.gpus),
+        "config": workload_config(wl, args.rank, args.gpus,
+                                  shared_x=input_note(workload_groups(wl, args.rank, args.no_shared_x))),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": res["sample"], "wall_seconds_per_sample": statistics.median(times)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -288,8 +302,7 @@ def main():
     # layers that read one X (q/k/v, gate/up) are projected together: one call
     # with the split of their concatenated P reads X once; each layer's XP is a
     # column block of its group's result
-    groups = ([[li] for li in range(L)] if args.no_shared_x or r % 8 != 0
-              else synth.input_groups(layers))
+    groups = workload_groups(wl, r, args.no_shared_x)
     XPg = [torch.empty(T, max(8, (len(g) * r + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :len(g) * r]
            for g in groups]
     XP = [None] * L
@@ -532,9 +545,7 @@ def main():
             "vs_baseline": None,
             "dtype": "bf16+fp32",
             "data": "synthetic",
-            "config": workload_config(wl, r, world, shared_x=(
-                "q/k/v and gate/up read one X each, projected together (grouped splits)"
-                if any(len(g) > 1 for g in groups) else "every layer reads its own X")),
+            "config": workload_config(wl, r, world, shared_x=input_note(groups)),
             "components": components,
             "roofline": roofline,
             "cpu_baseline": cpu,
