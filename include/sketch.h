@@ -265,7 +265,7 @@ SKETCH_API sketch_status sketch_project_inputs_batched(int n, const sketch_proje
  * bytes per value like fp32.  The accumulate call reads XP as the sum of the
  * two halves.  This removes the XP rounding term (~1e-3 relative) from C
  * ("Randomized Gradient Compression", "How it works": the layer saves X P; its
- * precision is this build's choice).  Columns [r, n_pad) and [n_pad + r,
+ * precision is this library's choice).  Columns [r, n_pad) and [n_pad + r,
  * 2 n_pad) are not written, and their contents do not affect C. */
 SKETCH_API sketch_status sketch_project_inputs_fp32xp_batched(int n, const sketch_project_problem* problems,
                                                               int64_t r, void* ws, size_t ws_bytes, void* stream);
@@ -296,7 +296,7 @@ SKETCH_API sketch_status sketch_split_projection_batched(int n, const sketch_spl
  * takes as XP = result + q r with ld_xp = the result's row stride ("LoGRA:
  * Scaling LLM Reinforcement Learning with Low-Rank Gradient Sketches", Key
  * Contributions: selected attention and MLP projections are sketched; sharing
- * their input is this build's way to read it once).  Each member column is
+ * their input is this library's way to read it once).  Each member column is
  * the same dot product as in a separate call.  1 <= m <= 16, m r <= 256;
  * every P 16-byte aligned; r a multiple of 8 when m > 1 (so that each
  * member's XP starts on a 16-byte boundary). */
