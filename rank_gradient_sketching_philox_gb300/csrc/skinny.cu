@@ -33,6 +33,7 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kChunk = 64;  // K elements per pipeline stage (one 128-byte swizzle row)
 constexpr int kMaxStages = 8;
+constexpr int kAccStripTiles = 1;  // 128-row tiles of C per persistent accumulation item
 
 // A launch covers up to kMaxProblems independent problems that share r (and so
 // N): one GEMM per layer.  Their M tiles are laid end to end along grid.y.
@@ -236,6 +237,197 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_gemm_kernel(const __grid_c
   if (warp == 0) tc::tmem_dealloc(tmem, a.tmem_cols);
 }
 
+// ---- persistent sketch accumulation ------------------------------------------
+// C (+)= D^T XP for many layers with one CTA per SM.  A work item is one layer's
+// strip of MT 128-row tiles of C over all tokens; the CTAs take the items
+// round robin (every item of a launch has the same token count, so the split
+// is even).  Warp 0 (one lane) streams the strip's D columns and the XP rows
+// of each 64-token chunk into a ring of stages with TMA; warp 1 (one lane)
+// issues the MMAs of each chunk into the item's accumulators, which alternate
+// between two TMEM buffers; warps 2..5 read a finished item's accumulators
+// (one row of C per thread) and add them to C while the next item streams.
+// Each row of C is written by one thread after a fixed-order accumulation over
+// the tokens, so results do not depend on timing.
+constexpr int kAccThreads = 192;
+
+template <int MT, int NB>
+__global__ void __launch_bounds__(kAccThreads, 1) acc_persistent_kernel(const __grid_constant__ SkinnyBatch a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ volatile int issued, consumed;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = a.tile_begin[a.n];
+  const uint32_t acc_cols = (uint32_t)(MT * a.n_pad);  // one buffer: MT accumulators
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    issued = 0;
+    consumed = 0;
+    for (int s = 0; s < a.stages; ++s) {
+      tc::mbar_init(&full_bar[s], 1);
+      tc::mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull_bar[b], 1);
+      tc::mbar_init(&tempty_bar[b], 4);  // the four epilogue warps
+    }
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, a.tmem_cols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  auto decode = [&](int item, int& p, int& m0) {
+    p = 0;
+    while (p + 1 < a.n && a.tile_begin[p + 1] <= item) ++p;
+    m0 = (item - a.tile_begin[p]) * 128 * MT;
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: TMA ring over the items' chunks ----
+    int it = 0;
+    bool stop = false;
+    for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
+      int p, m0;
+      decode(item, p, m0);
+      const CUtensorMap* tmA = &a.tmA[p];
+      const CUtensorMap* tmB = &a.tmB[p];
+      for (int c = 0; c < a.kchunks[p]; ++c, ++it) {
+        const int s = it % a.stages, u = it / a.stages;
+        if (u > 0 && !tc::mbar_wait(&empty_bar[s], (u - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+          stop = true;
+          break;
+        }
+        uint8_t* st = smem + (size_t)s * a.stage_bytes;
+        tc::mbar_arrive_expect_tx(&full_bar[s], a.stage_bytes);
+        const int kc = c * kChunk;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {  // D: [64 tokens][64 rows of C] per box, two per tile
+          tc::tma_load_2d(st + mt * 16384, tmA, &full_bar[s], m0 + 128 * mt, kc);
+          tc::tma_load_2d(st + mt * 16384 + 8192, tmA, &full_bar[s], m0 + 128 * mt + 64, kc);
+        }
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {  // XP: [64 tokens][64 rank columns] per box
+          uint8_t* bt = st + MT * 16384 + nb * a.b_bytes;
+          for (int j = 0; j * 64 < a.n_pad; ++j)
+            tc::tma_load_2d(bt + j * 8192, tmB, &full_bar[s], nb * a.b_col_off + j * 64, kc);
+        }
+        issued = it + 1;
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer ----
+    const uint32_t idesc = tc::idesc_bf16(128, a.n_pad, true, true);
+    int it = 0, j = 0;
+    bool stop = false;
+    for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x, ++j) {
+      int p, m0;
+      decode(item, p, m0);
+      const int b = j & 1;
+      if (j >= 2 && !tc::mbar_wait(&tempty_bar[b], ((j >> 1) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))
+        break;
+      tc::tc_fence_after();
+      const uint32_t acc0 = tmem + (uint32_t)b * acc_cols;
+      for (int c = 0; c < a.kchunks[p]; ++c, ++it) {
+        const int s = it % a.stages, u = it / a.stages;
+        if (!tc::mbar_wait(&full_bar[s], u & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) {
+          stop = true;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t sa = tc::smem_u32(smem + (size_t)s * a.stage_bytes);
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk) {
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint64_t ad = tc::sdesc_sw128(sa + mt * 16384 + kk * 2048, 8192, 1024);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const uint64_t bd = tc::sdesc_sw128(sa + MT * 16384 + nb * a.b_bytes + kk * 2048, 8192, 1024);
+              tc::mma_bf16(acc0 + (uint32_t)(mt * a.n_pad), ad, bd, idesc, (c > 0 || kk > 0 || nb > 0) ? 1u : 0u);
+            }
+          }
+        }
+        tc::mma_commit(&empty_bar[s]);
+        consumed = it + 1;
+      }
+      if (!stop) tc::mma_commit(&tfull_bar[b]);
+    }
+  } else if (warp >= 2) {
+    // ---- epilogue: accumulators -> C, one row per thread ----
+    const int quarter = warp & 3;  // TMEM lanes 32 (warp % 4) .. +31
+    const int q = quarter * 32 + lane;
+    const int ncols32 = (a.n_pad + 31) / 32;
+    const bool vec = (a.N & 3) == 0;
+    int j = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
+      int p, m0;
+      decode(item, p, m0);
+      const int b = j & 1;
+      const bool live = tc::mbar_wait(&tfull_bar[b], (j >> 1) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
+      if (!__all_sync(0xFFFFFFFFu, live)) break;
+      tc::tc_fence_after();
+      const int M = a.M[p];
+      float* Cp = static_cast<float*>(a.out[p]);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int64_t grow = (int64_t)m0 + 128 * mt + q;
+        for (int cg = 0; cg < ncols32; ++cg) {
+          uint32_t v[32];
+          tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)b * acc_cols +
+                                     (uint32_t)(mt * a.n_pad + cg * 32), v);
+          tc::tmem_wait_ld();
+          if (grow >= M) continue;
+          float* row = Cp + grow * a.ld_out[p] + cg * 32;
+          const int ncol = a.N - cg * 32 < 32 ? a.N - cg * 32 : 32;
+          if (vec) {
+            float4* r4 = reinterpret_cast<float4*>(row);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              if (4 * t >= ncol) break;
+              float4 o = make_float4(__uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]),
+                                     __uint_as_float(v[4 * t + 2]), __uint_as_float(v[4 * t + 3]));
+              if (a.out_mode == 2) {
+                const float4 c0 = r4[t];
+                o.x += c0.x;
+                o.y += c0.y;
+                o.z += c0.z;
+                o.w += c0.w;
+              }
+              r4[t] = o;
+            }
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+              if (t < ncol) row[t] = (a.out_mode == 2) ? row[t] + __uint_as_float(v[t]) : __uint_as_float(v[t]);
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty_bar[b]);
+    }
+  }
+  __syncwarp();
+  // ---- on a timeout, give copies still in flight a bounded chance to land ----
+  tc::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && abort_flag) {
+    volatile int dummy = 0;
+    for (int i = consumed; i < issued; ++i)
+      tc::mbar_wait(&full_bar[i % a.stages], (i / a.stages) & 1, &dummy, nullptr, 0, 100000000ull);
+  }
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, a.tmem_cols);
+}
+
 // P (k x r fp32) -> P^T split into BF16 high and low parts: rows [0, n_pad)
 // hold the high part, rows [n_pad, 2 n_pad) the low part, each k wide; rank
 // rows r..n_pad-1 are zero.  32 x 32 tiles transposed through shared memory;
@@ -345,6 +537,32 @@ cudaError_t launch_skinny(SkinnyBatch& a, cudaStream_t stream) {
   cfg.numAttrs = 1;
   count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// Tiles of C per persistent work item: wider strips read longer runs of each
+// token row of D, up to what two TMEM buffers of accumulators hold.
+int acc_strip_tiles(int n_pad) {
+  const int mt = kAccStripTiles;
+  return (2 * mt * n_pad <= 512) ? mt : 1;
+}
+
+template <int MT, int NB>
+cudaError_t launch_acc_persistent(SkinnyBatch& a, cudaStream_t stream) {
+  a.stage_bytes = MT * 16384u + NB * a.b_bytes;
+  int stages = (int)((200u * 1024u) / a.stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  a.stages = stages;
+  a.tmem_cols = tmem_cols_for(2 * MT * a.n_pad);
+  const size_t smem = (size_t)stages * a.stage_bytes + 1024;
+  auto kernel = acc_persistent_kernel<MT, NB>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int items = a.tile_begin[a.n];
+  const int grid = items < num_sms() ? items : num_sms();
+  count_launch();
+  kernel<<<grid, kAccThreads, smem, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -507,11 +725,22 @@ cudaError_t launch_accumulate(int n, const AccumulateProblem* probs, int r, int 
     a.b_bytes = (uint32_t)((n_pad + 63) / 64) * 64 * kChunk * 2;
     a.out_mode = overwrite ? 1 : 2;
     a.err = errw;
-    if (xp_split) {  // D^T XP_hi + D^T XP_lo, both into the same accumulator
-      a.b_col_off = n_pad;
+    a.b_col_off = xp_split ? n_pad : 0;  // D^T XP_hi + D^T XP_lo, both into the same accumulator
+    if (a.tile_begin[m] >= 2 * num_sms()) {
+      // enough tiles to keep every SM busy: persistent CTAs over strips of
+      // C, each over all tokens (no split over tokens)
+      const int mt = acc_strip_tiles(n_pad);
+      a.tile_begin[0] = 0;
+      for (int i = 0; i < m; ++i) a.tile_begin[i + 1] = a.tile_begin[i] + (int)ceil_div(a.M[i], 128 * mt);
+      if (mt == 1)
+        err = xp_split ? launch_acc_persistent<1, 2>(a, stream) : launch_acc_persistent<1, 1>(a, stream);
+      else if (mt == 2)
+        err = xp_split ? launch_acc_persistent<2, 2>(a, stream) : launch_acc_persistent<2, 1>(a, stream);
+      else
+        err = xp_split ? launch_acc_persistent<4, 2>(a, stream) : launch_acc_persistent<4, 1>(a, stream);
+    } else if (xp_split) {
       err = launch_skinny<true, true, 2>(a, stream);
     } else {
-      a.b_col_off = 0;
       err = launch_skinny<true, true, 1>(a, stream);
     }
     if (err != cudaSuccess) return err;
