@@ -183,7 +183,13 @@ SKETCH_API sketch_status sketch_apply_update_sgd(uint16_t* W, int64_t d, int64_t
  * call on a device looks up the array's device address (make that first call
  * before any stream capture).  All calls share the array: calls whose work
  * overlaps on the GPU race, so order them on one stream.  Nothing in the array
- * needs to start at zero. */
+ * needs to start at zero.  With lazy module loading (CUDA's default) the
+ * array is reserved when that first call looks up its address: a caller that
+ * is about to give its free device memory to another pool should make one
+ * call first (a call with d = 0 reserves the array and returns
+ * SKETCH_ERR_INVALID_ARG without launching anything).  The looked-up address
+ * is kept for the life of the process: after cudaDeviceReset() on a device,
+ * do not call the library on that device again in the same process. */
 SKETCH_API sketch_status sketch_apply_update_normsgd_noalloc(uint16_t* W, int64_t d, int64_t k, int64_t ld_w,
                                                              const float* C, const float* P, int64_t r,
                                                              float tau, uint64_t seed, uint32_t layer,
@@ -325,6 +331,14 @@ SKETCH_API sketch_status sketch_apply_update_sgd_batched(int n, const sketch_upd
 #define SKETCH_DEVERR_TIMEOUT_MMA 2    /* tensor-core work never completed */
 #define SKETCH_DEVERR_TIMEOUT_STAGE 4  /* a pipeline stage was never released */
 SKETCH_API sketch_status sketch_read_device_errors(int32_t* flags, void* stream);
+
+/* Read and clear the current device's count of weights that the update calls
+ * recomputed on their exact path: an element whose stochastic-rounding
+ * margin lies within the error bound of the tensor-core rebuild of H_ij is
+ * redone with H_ij from a compensated fp32 dot product, so that it rounds
+ * exactly as the definition does.  Instrumentation for tests and benchmarks;
+ * the pages have no counterpart.  Synchronizes `stream`. */
+SKETCH_API sketch_status sketch_read_exact_count(uint64_t* count, void* stream);
 
 /* Number of kernels this library has launched in this process (every device
  * and thread), counted on the host as each launch is issued.  Instrumentation

@@ -10,6 +10,6 @@ from .binding import (PROJ_GAUSSIAN_QR, PROJ_RADEMACHER, SketchError, accumulate
                       apply_update_normsgd_batched, apply_update_sgd, apply_update_sgd_batched,
                       kernel_launches, project_inputs, project_inputs_batched,
                       project_inputs_fp32xp_batched, project_inputs_grouped_batched,
-                      projection_split_elems, read_device_errors, sample_projection,
+                      projection_split_elems, read_device_errors, read_exact_count, sample_projection,
                       sample_projection_batched, split_projection_batched, split_projection_grouped,
                       workspace_bytes, workspace_bytes_batched, xp_split_cols)

@@ -39,7 +39,8 @@ EXPORTS = ("sketch_workspace_bytes", "sketch_sample_projection", "sketch_project
            "sketch_project_inputs_batched", "sketch_accumulate_batched",
            "sketch_apply_update_normsgd_batched", "sketch_apply_update_sgd_batched",
            "sketch_apply_update_normsgd_noalloc", "sketch_noalloc_scratch_bytes",
-           "sketch_read_device_errors", "sketch_kernel_launches", "sketch_projection_split_elems",
+           "sketch_read_device_errors", "sketch_read_exact_count", "sketch_kernel_launches",
+           "sketch_projection_split_elems",
            "sketch_split_projection_batched", "sketch_project_inputs_fp32xp_batched",
            "sketch_accumulate_fp32xp_batched", "sketch_split_projection_grouped", "sketch_status_string",
            "sketch_last_error")
@@ -98,6 +99,7 @@ _SIGS = {
     "sketch_apply_update_sgd": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _c.c_float, _u64,
                                            _u32, _u32, _vp, _vp, _c.c_size_t, _vp]),
     "sketch_read_device_errors": (_c.c_int, [_c.POINTER(_c.c_int32), _vp]),
+    "sketch_read_exact_count": (_c.c_int, [_c.POINTER(_c.c_uint64), _vp]),
     "sketch_kernel_launches": (_c.c_uint64, []),
     "sketch_projection_split_elems": (_c.c_size_t, [_i64, _i64]),
     "sketch_split_projection_batched": (_c.c_int, [_c.c_int, _vp, _i64, _vp]),
@@ -188,6 +190,16 @@ def read_device_errors(stream=None, device=None):
     flags = ctypes.c_int32(0)
     _check(lib().sketch_read_device_errors(ctypes.byref(flags), h))
     return int(flags.value)
+
+
+def read_exact_count(stream=None, device=None):
+    """Read and clear the count of weights the update calls recomputed on their
+    exact path (instrumentation); syncs the stream."""
+    dev = device if device is not None else torch.cuda.current_device()
+    h, _ = _stream_handle(stream, dev)
+    n = ctypes.c_uint64(0)
+    _check(lib().sketch_read_exact_count(ctypes.byref(n), h))
+    return int(n.value)
 
 
 def kernel_launches():

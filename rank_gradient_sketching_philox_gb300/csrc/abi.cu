@@ -474,4 +474,17 @@ sketch_status sketch_read_device_errors(int32_t* flags, void* stream) {
   return launch_result(err, "read_device_errors");
 }
 
+sketch_status sketch_read_exact_count(uint64_t* count, void* stream) {
+  if (count == nullptr) return fail(SKETCH_ERR_INVALID_ARG, "count is NULL");
+  unsigned long long* word = nullptr;
+  cudaError_t err = rgs::device_exact_counter(&word);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long host = 0;
+  if (err == cudaSuccess) err = cudaMemcpyAsync(&host, word, sizeof(host), cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaMemsetAsync(word, 0, sizeof(host), s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  *count = (uint64_t)host;
+  return launch_result(err, "read_exact_count");
+}
+
 }  // extern "C"

@@ -30,6 +30,10 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner
                               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 // Device address of the current device's error word (bits from tc.cuh).
 cudaError_t device_error_word(int** out);
+// Device address of the current device's count of weights the update kernels
+// recomputed on their exact path (instrumentation, read by
+// sketch_read_exact_count).
+cudaError_t device_exact_counter(unsigned long long** out);
 int num_sms();
 // Counts one kernel launch issued by this library (sketch_kernel_launches).
 void count_launch();
@@ -158,14 +162,16 @@ struct UpdateWorkspace {
   int32_t* status;         // scratch status when the caller passes none
   uint32_t* ticket;        // last-block counter of the update kernel
   double* wnew_partials;   // one per update block
-  uint16_t* c_split;       // d x 2 r_pad BF16: [high | low] part of C
-  uint16_t* p_split;       // k x 2 r_pad BF16: [high | low] part of P
-  uint32_t* flags;         // careful-group flag bitmap (flag_words(d, k, r) words)
+  uint16_t* c_split;       // d x (2 r_pad) BF16: [high | low] part of C
+  uint16_t* p_split;       // k x (2 r_pad) BF16: [high | low] part of P
+  // exact-path queue: the elements the update kernel hands to the fix kernel
+  uint32_t* fix_count;     // entries appended (may exceed fix_cap: the rest were redone in place)
+  uint32_t* fix_ticket;    // last-block counter of the fix kernel
+  unsigned long long* fix_acc;  // fixed-point sum of the exact path's changes of ||W_new||^2
+  uint4* fix_entries;      // fix_cap entries: (i, j, w | rand16 << 16, tensor-core result)
+  uint32_t fix_cap;
 };
 constexpr int kWnormBlocks = 1024;
-// 32-bit words of a layer's careful-group flag bitmap (one bit per 8 weights of
-// the padded tile grid).
-int64_t flag_words(int64_t d, int64_t k, int r);
 // Carves one layer's workspace at the cursor; returns its size (a multiple of 256).
 size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool normsgd, UpdateWorkspace* ws);
 

@@ -1,7 +1,7 @@
 // Host-side runtime helpers: TMA tensor-map encoding (through the driver entry
 // point, so the library does not link libcuda) with a cache of encoded maps,
-// the device error word that kernels set when a bounded wait gives up, and
-// cached device properties.
+// the device error word that kernels set when a bounded wait gives up, the
+// device count of exactly recomputed weights, and cached device properties.
 #include <cudaTypedefs.h>
 
 #include <atomic>
@@ -15,9 +15,12 @@ namespace {
 
 // Bits set by kernels whose bounded waits timed out (see tc.cuh).
 __device__ int g_device_error = 0;
+// Weights the update kernels recomputed on their exact path.
+__device__ unsigned long long g_exact_count = 0;
 
 constexpr int kMaxDevices = 64;
 int* g_error_ptr[kMaxDevices] = {};
+unsigned long long* g_exact_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 std::mutex g_mutex;
 
@@ -110,6 +113,22 @@ cudaError_t device_error_word(int** out) {
     g_error_ptr[dev] = static_cast<int*>(p);
   }
   *out = g_error_ptr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t device_exact_counter(unsigned long long** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_exact_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_exact_count);
+    if (err != cudaSuccess) return err;
+    g_exact_ptr[dev] = static_cast<unsigned long long*>(p);
+  }
+  *out = g_exact_ptr[dev];
   return cudaSuccess;
 }
 

@@ -55,18 +55,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for phase `parity` of `bar`.  Returns false if the CTA's abort
-// flag is set or the wait times out (then the flag and *err are set).
+// flag is set or the wait times out (then the flag and *err are set).  The
+// flag and the clock are looked at every 16th try only, so a waiting warp
+// spends few issue slots between the hardware's suspended tries.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* err, int code, uint64_t timeout = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  while (true) {
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > timeout) {
-      *abort_flag = 1;
-      if (err) atomicOr(err, code);
-      return false;
+    if ((n & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > timeout) {
+        *abort_flag = 1;
+        if (err) atomicOr(err, code);
+        return false;
+      }
     }
   }
 }
@@ -180,6 +184,10 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
 // sts128 done only where pred holds, as one predicated store (no branch).

@@ -121,20 +121,33 @@ __global__ void __launch_bounds__(256) normsgd_finalize_kernel(const __grid_cons
 struct SplitBatch {
   const float* src[2 * kMaxAux];
   int64_t row_begin[2 * kMaxAux + 1];  // prefix of the entries' row counts
-  uint16_t* dst[2 * kMaxAux];   // rows x (2 r_pad): [hi | lo]
+  uint16_t* dst[2 * kMaxAux];   // rows x (parts r_pad): [hi | lo] or [hi | mid | lo]
   float* norm[2 * kMaxAux];     // rows: Euclidean norm of each source row
   int n;
   int r;
   int r_pad;
+  int parts;  // 2 or 3 BF16 parts per value
+  // each layer's exact-path queue counters, reset here before the update
+  uint32_t* fix_count[kMaxAux];
+  uint32_t* fix_ticket[kMaxAux];
+  unsigned long long* fix_acc[kMaxAux];
 };
 
-// Rows of all entries, grid-stride: x = hi + lo to 2^-17 relative (columns
-// r..r_pad-1 zero) and ||row||_2.  A row takes lpr lanes (r_pad / 4 rounded up
+// Rows of all entries, grid-stride: x = hi + lo to 2^-17 relative, or
+// x = hi + mid + lo to 2^-25 (each part the BF16 of what the parts before it
+// leave, which fp32 holds exactly; columns r..r_pad-1 zero), and ||row||_2.  A row takes lpr lanes (r_pad / 4 rounded up
 // to a power of two, at most 32), lane c its columns 4c..4c+3 of each 4 lpr
 // step; a warp holds 32 / lpr rows at a time and four such steps, their loads
 // issued before any is used, so one round trip serves up to 4 * 32 / lpr rows.
 __global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__ SplitBatch b) {
   constexpr int kU = 4;
+  if (blockIdx.x == 0) {
+    for (int t = threadIdx.x; t < b.n / 2; t += blockDim.x) {
+      *b.fix_count[t] = 0u;
+      *b.fix_ticket[t] = 0u;
+      *b.fix_acc[t] = 0ull;
+    }
+  }
   const int lane = threadIdx.x & 31;
   const int64_t total = b.row_begin[b.n];
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -176,7 +189,7 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__
     for (int u = 0; u < kU; ++u) {
       float sq = 0.f;
       if (row[u] >= 0) {
-        uint16_t* dst = b.dst[en[u]] + row[u] * 2 * b.r_pad;
+        uint16_t* dst = b.dst[en[u]] + row[u] * b.parts * b.r_pad;
         for (int c0 = 4 * cl; c0 < b.r_pad; c0 += 4 * lpr) {
           float w[4];
           if (c0 == 4 * cl) {
@@ -187,19 +200,24 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__
 #pragma unroll
             for (int t = 0; t < 4; ++t) w[t] = (c0 + t < b.r) ? src[c0 + t] : 0.f;
           }
-          uint16_t hi[4], lo[4];
+          uint16_t part[3][4];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             sq = fmaf(w[t], w[t], sq);
-            const __nv_bfloat16 h = __float2bfloat16_rn(w[t]);
-            hi[t] = __bfloat16_as_ushort(h);
-            lo[t] = __bfloat16_as_ushort(__float2bfloat16_rn(w[t] - __bfloat162float(h)));
+            float rest = w[t];
+#pragma unroll
+            for (int q2 = 0; q2 < 3; ++q2) {
+              const __nv_bfloat16 h = __float2bfloat16_rn(rest);
+              part[q2][t] = __bfloat16_as_ushort(h);
+              rest = rest - __bfloat162float(h);
+            }
           }
           // r_pad is a multiple of 16: the 4 columns are inside the row, 8-byte aligned
-          *reinterpret_cast<uint2*>(dst + c0) =
-              make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
-          *reinterpret_cast<uint2*>(dst + b.r_pad + c0) =
-              make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+#pragma unroll
+          for (int q2 = 0; q2 < 3; ++q2)
+            if (q2 < b.parts)
+              *reinterpret_cast<uint2*>(dst + q2 * b.r_pad + c0) =
+                  make_uint2(part[q2][0] | ((uint32_t)part[q2][1] << 16), part[q2][2] | ((uint32_t)part[q2][3] << 16));
         }
       }
       // the row's lanes sum their squares (groups of lpr lanes)
@@ -215,11 +233,9 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__
 // layers are numbered end to end and each persistent CTA takes a contiguous
 // range of them, so consecutive units usually share the row block of C.
 struct UpdBatch {
-  CUtensorMap tm_c[kMaxUpd];   // C split, d x (2 r_pad) BF16: [hi | lo]
-  CUtensorMap tm_p[kMaxUpd];   // P split, k x (2 r_pad) BF16: [hi | lo]
-  CUtensorMap tm_w[kMaxUpd];   // W, d x k BF16 (tile loads)
-  uint16_t* W[kMaxUpd];        // W for the results, stored from registers
-  int64_t ld_w[kMaxUpd];
+  CUtensorMap tm_c[kMaxUpd];   // C split, d x (parts r_pad) BF16: [hi | lo] or [hi | mid | lo]
+  CUtensorMap tm_p[kMaxUpd];   // P split, k x (parts r_pad) BF16
+  CUtensorMap tm_w[kMaxUpd];   // W, d x k BF16 (tile loads and stores)
   const float* C[kMaxUpd];     // fp32 C and P for the exact recomputation
   const float* P[kMaxUpd];
   const float* c_norm[kMaxUpd];
@@ -241,21 +257,21 @@ struct UpdBatch {
   int p_stages;       // P ring depth
   int w_stages;       // W ring depth
   float scale_val;
-  uint64_t seed;
+  float err_coef;     // 2^25 (beta + 2^-24): the margin bound is err_coef |s| ||c_i|| max_j ||p_j||
   uint32_t rk0[10], rk1[10];  // Philox round keys of the seed
   uint32_t step;
   int r;
   int r_pad;          // r rounded up to 16 (MMA K extent)
+  int parts;          // BF16 parts of C and P: 2 (three products) or 3 (six)
   int kchunks;        // 64-wide chunks of r_pad
-  uint32_t a_bytes;   // bytes of the C_hi (or C_lo) tile: kchunks x 16 KB
-  uint32_t b_bytes;   // bytes of the P_hi (or P_lo) tile: kchunks x NCOLS x 128
+  uint32_t a_bytes;   // bytes of one part of the C row block: kchunks x 16 KB
+  uint32_t b_bytes;   // bytes of one part of a P tile: kchunks x NCOLS x 128
   uint32_t w_bytes;   // bytes of the W tile: NCOLS/64 x 16 KB
-  int list_cap;       // entries of the careful-word list that fit the dynamic shared memory
   int* err;
-  // careful-group flags, one bit per 8-weight group: per tile (rb, ct), word
-  // ew * (NCOLS/32) + g holds bit `lane` for row rb*128 + (ew&3)*32 + lane,
-  // columns ct*NCOLS + (ew>>2)*(NCOLS/4) + 8g..+7 (ew = epilogue warp)
-  uint32_t* flags[kMaxUpd];
+  unsigned long long* exact_count;  // elements recomputed exactly (instrumentation)
+  uint4* fix_entries[kMaxUpd];      // exact-path queue of each layer (see FixBatch)
+  uint32_t* fix_count[kMaxUpd];
+  uint32_t fix_cap[kMaxUpd];
 };
 
 // kernel parameters are limited to 32764 bytes
@@ -265,9 +281,13 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+constexpr int kStoreWarps = 2;                    // tiles alternate between them: two stores drain at once
+constexpr int kCtlWarps = 2 + kStoreWarps;        // producer, MMA issuer, store warps
 constexpr int kEpiWarps = 16;                     // warps 4..19: four per TMEM lane quarter
-constexpr int kUpdThreads = (4 + kEpiWarps) * 32;
+constexpr int kUpdThreads = (kCtlWarps + kEpiWarps) * 32;
 constexpr int kMaxStagesUpd = 8;
+constexpr int kTmemBufs = 4;                      // accumulator tiles in flight
+constexpr int kNormSlots = 8;                     // units whose ||W_new||^2 partials may be open at once
 
 struct Unit {
   int p, rb, ct0, ct1;
@@ -295,116 +315,191 @@ __device__ __forceinline__ Unit decode_unit(const UpdBatch& a, int u) {
   return x;
 }
 
-// One careful group, warp-wide: W_new of the 8 elements (i, j..j+7) of
-// problem p from their original W, with H_i,j+t computed by the compensated
-// dot product (Dot2 of the same paper; lanes 4t..4t+3 take column t, every
-// fourth term each, merged by TwoSum), v = fmaf(-s, fl32(H), w) and the
-// group's Philox block.  The dot product is as accurate as one carried in
-// twice fp32 precision and then rounded, so it is fl32 of the exact H except
-// when H lies within ~2^-40 of its size of an fp32 rounding boundary.  All
-// fp32: this GPU's FP64 rate is far too low for the purpose.
-__device__ __forceinline__ void careful_group_warp(const UpdBatch& a, int p, int i, int j) {
-  const int lane = threadIdx.x & 31, t = lane >> 2, q = lane & 3;
-  const int r = a.r;
-  const float* crow = a.C[p] + (int64_t)i * r;
-  const float* prow = a.P[p] + (int64_t)(j + t) * r;
-  uint16_t* wp = a.W[p] + (int64_t)i * a.ld_w[p] + j + t;
-  const uint32_t w16 = *wp;  // the original: the update kernel left the group alone
-  float hi = 0.f, lo = 0.f;
-  auto term = [&](float c, float pv) {
-    const float m = __fmul_rn(c, pv);
-    float sum, err;
-    two_sum(hi, m, sum, err);
-    hi = sum;
-    lo = __fadd_rn(lo, __fadd_rn(err, __fmaf_rn(c, pv, -m)));
-  };
-  // the terms l = q, q+4, ... of this lane, sixteen loads of C and P at a
-  // time issued together (one round trip per 64 terms of the row)
-  int l = q;
-  for (; l + 60 < r; l += 64) {
-    float cv[16], pv[16];
+// Rounding margin of one element, in units of the error bound.  S = bits(v) +
+// rand16 is the stochastic-rounding sum (the result is S >> 16); L = S mod
+// 2^16 lies min(L, 2^16 - L) fp32 steps of v from the nearest sum that would
+// round the other way.  A value v' within D of v is at most 2D / ulp(v) + 2
+// fp32 steps from v (the step halves below a power of two; both values are
+// rounded once), and ulp(v) > |v| 2^-24, so v' rounds like v whenever
+// (min(L, 2^16 - L) - 3) |v| >= 2^25 D.  Returns the left side (less a
+// little more, for the rounding of this product): negative when the margin
+// is three steps or less, NaN when v is NaN, and NaN for an infinite v.
+__device__ __forceinline__ float rounding_margin(uint32_t S, float v) {
+  const float mg = __uint_as_float(__byte_perm(S, 0x4B000000u, 0x7610));  // 2^23 + (S mod 2^16)
+  const float x = mg - 8421376.0f;                                        // (S mod 2^16) - 2^15, exact
+  const float av = fabsf(v);
+  return fmaf(-fabsf(x), av, 32764.0f * av);  // (min(L, 2^16 - L) - 4) |v|, rounded
+}
+
+template <int N>
+__device__ __forceinline__ uint32_t pick(const uint32_t (&v)[N], int i) {
+  uint32_t r = v[0];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      cv[m] = crow[l + 4 * m];
-      pv[m] = prow[l + 4 * m];
+  for (int t = 1; t < N; ++t) r = (i == t) ? v[t] : r;
+  return r;
+}
+
+// The exact path, in place: the warp takes the elements of emask (bit t:
+// column jg + t of the calling lane's row) one at a time, H_ij as a
+// compensated dot product of the fp32 row i of C and row j of P, its terms
+// spread over the lanes and merged by TwoSum, then v = fmaf(-s, fl32(H_ij), w)
+// and the same stochastic rounding as the tensor-core path.  The owning lane
+// writes the result into its W stage over the tensor-core result.  wv, rv, ov
+// are the lane's original weights, Philox words and tensor-core results of the
+// group; returns the change of the lane's sum of squares.
+__device__ float exact_in_place(uint32_t emask, const uint32_t (&wv)[4], const uint32_t (&rv)[4],
+                                const uint32_t (&ov)[4], const float* C, const float* P, int r, int row0, int jg,
+                                float s, uint32_t sp, unsigned& n_done) {
+  const int lane = threadIdx.x & 31;
+  float dsq = 0.f;
+  uint32_t pending = __ballot_sync(0xFFFFFFFFu, emask != 0);
+  while (pending) {
+    const int src = __ffs(pending) - 1;
+    const uint32_t m_src = __shfl_sync(0xFFFFFFFFu, emask, src);
+    const int e = __ffs(m_src) - 1;
+    if (lane == src) emask &= emask - 1u;
+    const uint32_t ww = __shfl_sync(0xFFFFFFFFu, pick(wv, e >> 1), src);
+    const uint32_t rr = __shfl_sync(0xFFFFFFFFu, pick(rv, e >> 1), src);
+    const uint32_t oo = __shfl_sync(0xFFFFFFFFu, pick(ov, e >> 1), src);
+    const int sh = (e & 1) * 16;
+    const uint32_t w16 = (ww >> sh) & 0xFFFFu, r16 = (rr >> sh) & 0xFFFFu, o16 = (oo >> sh) & 0xFFFFu;
+    const float* crow = C + (int64_t)(row0 + src) * r;
+    const float* prow = P + (int64_t)(jg + e) * r;
+    float hs = 0.f, he = 0.f;
+    for (int l = lane; l < r; l += 32) {
+      const float cv = crow[l], pv = prow[l];
+      const float m = __fmul_rn(cv, pv);
+      float sum, err;
+      two_sum(hs, m, sum, err);
+      hs = sum;
+      he = __fadd_rn(he, __fadd_rn(err, __fmaf_rn(cv, pv, -m)));
     }
 #pragma unroll
-    for (int m = 0; m < 16; ++m) term(cv[m], pv[m]);
-  }
-  if (l < r) {
-    float cv[16], pv[16];
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const bool in = l + 4 * m < r;
-      cv[m] = in ? crow[l + 4 * m] : 0.f;
-      pv[m] = in ? prow[l + 4 * m] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ohs = __shfl_xor_sync(0xFFFFFFFFu, hs, o), ohe = __shfl_xor_sync(0xFFFFFFFFu, he, o);
+      float sum, err;
+      two_sum(hs, ohs, sum, err);
+      hs = sum;
+      he = __fadd_rn(he, __fadd_rn(ohe, err));
     }
-#pragma unroll
-    for (int m = 0; m < 16; ++m) term(cv[m], pv[m]);  // zero terms change nothing
+    const float hx = __fadd_rn(hs, he);
+    const float v = fmaf(-s, hx, __uint_as_float(w16 << 16));
+    const uint32_t out = sr_bf16_bits(v, r16);
+    if (lane == src) {
+      tc::sts16(sp + 2 * e, (uint16_t)out);
+      const float fo = __uint_as_float(o16 << 16), fn = __uint_as_float(out << 16);
+      dsq = fmaf(fn, fn, fmaf(-fo, fo, dsq));
+      ++n_done;
+    }
+    pending = __ballot_sync(0xFFFFFFFFu, emask != 0);
   }
+  return dsq;
+}
+
+// The exact path for the elements of one 8-column group of a warp (the calling
+// lane's row, columns jg..jg+7) whose rounding margin the error bound might
+// cross; flag says that the lane's group holds at least one, and h03, h47 are
+// its tensor-core H values, so that each element's margin is checked again.
+// The flagged elements are appended to the layer's exact-path queue, which the
+// fix kernel redoes once every tile of the launch is stored; those that find
+// the queue full are redone here in place (exact_in_place).  Returns the change
+// of the lane's sum of squares from the in-place ones.  Kept out of line: it
+// runs rarely, and its registers would otherwise crowd the main loop.
+__device__ __noinline__ float exact_path(bool flag, float bound, uint4 win, uint4 rwd, uint4 wout, uint4 h03,
+                                         uint4 h47, uint4* queue, uint32_t* queue_count, uint32_t queue_cap,
+                                         const float* C, const float* P, int r, int row0, int jg, int k, float s,
+                                         uint32_t sp, unsigned& n_done) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t wv[4] = {win.x, win.y, win.z, win.w}, rv[4] = {rwd.x, rwd.y, rwd.z, rwd.w},
+                 ov[4] = {wout.x, wout.y, wout.z, wout.w};
+  const uint32_t hv[8] = {h03.x, h03.y, h03.z, h03.w, h47.x, h47.y, h47.z, h47.w};
+  // the flagged lane's elements whose own margin the bound might cross
+  uint32_t emask = 0;
+  if (flag) {
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, o), olo = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
-    float sum, err;
-    two_sum(hi, ohi, sum, err);
-    hi = sum;
-    lo = __fadd_rn(lo, __fadd_rn(olo, err));
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t wt = (t & 1) ? (wv[t >> 1] & 0xFFFF0000u) : (wv[t >> 1] << 16);
+      const uint32_t rt = (t & 1) ? (rv[t >> 1] >> 16) : (rv[t >> 1] & 0xFFFFu);
+      const float vt = fmaf(-s, __uint_as_float(hv[t]), __uint_as_float(wt));
+      const float mt = rounding_margin(__float_as_uint(vt) + rt, vt);
+      emask |= (!(mt >= bound) ? 1u : 0u) << t;
+    }
+    if (jg + 8 > k) emask &= (1u << (k - jg)) - 1u;  // columns inside W
   }
-  const float h = __fadd_rn(hi, lo);
-  const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
-  const uint32_t blk = (uint32_t)i * ((uint32_t)a.k[p] >> 3) + ((uint32_t)j >> 3);  // element index / 8
-  const Philox4 rnd = philox4x32_10_rk(blk, a.step, a.layer[p], kTagSR, a.rk0, a.rk1);
-  const uint32_t word = (t >> 1) == 0 ? rnd.w0 : (t >> 1) == 1 ? rnd.w1 : (t >> 1) == 2 ? rnd.w2 : rnd.w3;
-  const float v = fmaf(-s, h, __uint_as_float(w16 << 16));
-  const uint32_t o = sr_bf16_bits(v, (t & 1) ? (word >> 16) : (word & 0xFFFFu));
-  __syncwarp();
-  if (q == 0) *wp = (uint16_t)o;
+  // one atomic per warp: the lanes' entries go to consecutive queue slots
+  const uint32_t cnt = __popc(emask);
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  uint32_t base = 0;
+  if (lane == 31 && total != 0) base = atomicAdd(queue_count, total);
+  base = __shfl_sync(0xFFFFFFFFu, base, 31);
+  uint32_t pos = base + incl - cnt, over = 0;
+  const int row = row0 + lane;
+  for (uint32_t m = emask; m; m &= m - 1u) {
+    const int e = __ffs(m) - 1;
+    if (pos < queue_cap) {
+      const int sh = (e & 1) * 16;
+      const uint32_t w16 = (wv[e >> 1] >> sh) & 0xFFFFu, r16 = (rv[e >> 1] >> sh) & 0xFFFFu;
+      const uint32_t o16 = (ov[e >> 1] >> sh) & 0xFFFFu;
+      queue[pos] = make_uint4((uint32_t)row, (uint32_t)(jg + e), w16 | (r16 << 16), o16);
+    } else {
+      over |= 1u << e;
+    }
+    ++pos;
+  }
+  return exact_in_place(over, wv, rv, ov, C, P, r, row0, jg, s, sp, n_done);
 }
 
 // Persistent rebuild + update, one CTA per SM, each CTA a contiguous range of
 // units (a unit: one 128-row block of one layer and up to unit_tiles column
-// tiles of NCOLS).  Warp 0 (one lane) streams with TMA the split C row block of
-// each unit (C_hi, C_lo), the P_hi/P_lo rows of each column tile into a P ring
-// and the W tile into a deeper W ring.  Warp 1 (one lane) issues
-// H = C_hi P_hi^T + C_hi P_lo^T + C_lo P_hi^T (tcgen05.mma, M=128, N=NCOLS)
-// into one of two TMEM buffers and frees the P stage with tcgen05.commit.
-// The 16 epilogue warps (warps 4..19, four per TMEM lane quarter, one column
-// quarter each) read H from TMEM, form v = fmaf(-s, H, w) with w from the W
-// stage, round it stochastically with 16 Philox bits per weight and write the
-// BF16 results back into the stage; warp 2 (one lane) writes each finished
-// tile to W with a TMA tensor store and frees the stage.  After the main loop
-// all 20 warps redo the flagged groups (the careful groups, below).
+// tiles of NCOLS).  Warp 0 (one lane) streams with TMA the BF16 parts of the C
+// row block of each unit, the same parts of the P rows of each column tile
+// into a P ring, and the W tile into a deeper W ring.  Warp 1 (one lane)
+// issues H = sum of the part products down to about 2^-24 (tcgen05.mma, M=128,
+// N=NCOLS; three products of two parts or six of three) into one of four TMEM
+// buffers and frees the P stage with tcgen05.commit.  The 16 epilogue warps
+// (warps 4..19, four per TMEM lane quarter, one column quarter each) read H
+// from TMEM, form v = fmaf(-s, H, w) with w from the W stage, round it
+// stochastically with 16 Philox bits per weight and write the BF16 results
+// back into the stage; warps 2 and 3 (one lane each, alternate tiles) write
+// each finished tile to W with a TMA tensor store and free the stage.
 //
-// Exactness where it matters: |H_tc - H| <= ~2^-14.2 ||c_i|| ||p_j|| (the
-// dropped lo*lo and residual terms, ~3 * 2^-16 of sum |c_l p_l|, plus the fp32
-// accumulation), which moves v across at most one BF16 step unless
-// |v| < s ||c_i|| ||p_j|| 2^-6.  A group of 8 weights holding a |v| below
-// s ||c_i|| max_j ||p_j|| 2^-5 (the maximum over the warp's 32 columns of the
-// tile: twice that margin) or a NaN keeps its original W in the stage and is
-// flagged; the careful pass recomputes its elements with fl32(H_ij) from a
-// compensated dot product, which is the value the definition rounds.
+// Exactness.  The definition rounds v = fmaf(-s, fl32(H), w) with fl32(H) the
+// fp32 rounding of the exact product.  The tensor-core H differs from it by at
+// most D = |s| (beta ||c_i|| ||p_j|| + 2^-24 |H|) with beta the split and
+// accumulation error of the part products.  Each element's rounding margin
+// (rounding_margin) is compared with that bound: an element whose margin
+// might be crossed is recomputed at once by its warp, H_ij from a compensated
+// dot product of the fp32 row of C and the fp32 row of P (Dot2 of the paper
+// above: as accurate as twice fp32 precision), and its result replaces the
+// tensor-core one in the stage before the tile is stored.  Every other
+// element's result is the one the definition gives.
 template <int NCOLS>
 __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const __grid_constant__ UpdBatch a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t pfull_bar[kMaxStagesUpd], pempty_bar[kMaxStagesUpd];
   __shared__ __align__(8) uint64_t wfull_bar[kMaxStagesUpd], wempty_bar[kMaxStagesUpd], sfull_bar[kMaxStagesUpd];
-  __shared__ __align__(8) uint64_t cfull_bar, cempty_bar, tfull_bar[2], tempty_bar[2];
+  __shared__ __align__(8) uint64_t cfull_bar, cempty_bar, tfull_bar[kTmemBufs], tempty_bar[kTmemBufs];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
-  __shared__ int clist_n;  // entries of the careful-word list
   __shared__ uint32_t skip_mask[(kMaxUpd + 31) / 32];  // layers whose status_in is nonzero
-  __shared__ double warp_sq[kEpiWarps];
+  __shared__ double norm_slot[kNormSlots][kEpiWarps];  // ||W_new||^2 of each epilogue warp per open unit
+  __shared__ int norm_count[kNormSlots];
 
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* s_chi = smem;
-  uint8_t* s_clo = s_chi + a.a_bytes;
-  uint8_t* s_p0 = s_clo + a.a_bytes;                        // P ring: NSP x (hi, lo)
-  uint8_t* s_w0 = s_p0 + (size_t)a.p_stages * 2 * a.b_bytes;  // W ring: NSW x W tile
+  uint8_t* s_c = smem;                                             // C row block: parts x a_bytes
+  uint8_t* s_p0 = s_c + (size_t)a.parts * a.a_bytes;               // P ring: NSP x parts x b_bytes
+  uint8_t* s_w0 = s_p0 + (size_t)a.p_stages * a.parts * a.b_bytes;  // W ring: NSW x W tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NSP = a.p_stages, NSW = a.w_stages;
   const int u_begin = a.cta_unit_begin[blockIdx.x];
   const int u_end = a.cta_unit_begin[blockIdx.x + 1];
-  constexpr uint32_t kTmemCols = 2 * NCOLS;
+  constexpr uint32_t kTmemCols = kTmemBufs * NCOLS;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -419,14 +514,15 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     }
     tc::mbar_init(&cfull_bar, 1);
     tc::mbar_init(&cempty_bar, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kTmemBufs; ++b) {
       tc::mbar_init(&tfull_bar[b], 1);
       tc::mbar_init(&tempty_bar[b], kEpiWarps);
     }
+    for (int s = 0; s < kNormSlots; ++s) norm_count[s] = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) tc::tmem_alloc(&tmem_slot, kTmemCols);
-  if (warp == 3) {
+  if (warp == 2) {
     // the skipped layers, read once here instead of at every unit
 #pragma unroll
     for (int h = 0; h < (kMaxUpd + 31) / 32; ++h) {
@@ -452,11 +548,10 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       const int i0 = x.rb * 128;
       if (x.p != prev_p || x.rb != prev_rb) {
         if (cl > 0 && !tc::mbar_wait(&cempty_bar, (cl - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) break;
-        tc::mbar_arrive_expect_tx(&cfull_bar, 2 * a.a_bytes);
-        for (int c = 0; c < a.kchunks; ++c) {
-          tc::tma_load_2d(s_chi + c * 16384, &a.tm_c[x.p], &cfull_bar, c * 64, i0);
-          tc::tma_load_2d(s_clo + c * 16384, &a.tm_c[x.p], &cfull_bar, a.r_pad + c * 64, i0);
-        }
+        tc::mbar_arrive_expect_tx(&cfull_bar, a.parts * a.a_bytes);
+        for (int q2 = 0; q2 < a.parts; ++q2)
+          for (int c = 0; c < a.kchunks; ++c)
+            tc::tma_load_2d(s_c + q2 * a.a_bytes + c * 16384, &a.tm_c[x.p], &cfull_bar, q2 * a.r_pad + c * 64, i0);
         ++cl;
         prev_p = x.p;
         prev_rb = x.rb;
@@ -479,12 +574,12 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           stop = true;
           break;
         }
-        uint8_t* pst = s_p0 + (size_t)sp * 2 * a.b_bytes;
-        tc::mbar_arrive_expect_tx(&pfull_bar[sp], 2 * a.b_bytes);
-        for (int c = 0; c < a.kchunks; ++c) {
-          tc::tma_load_2d(pst + c * NCOLS * 128, &a.tm_p[x.p], &pfull_bar[sp], c * 64, j0);
-          tc::tma_load_2d(pst + a.b_bytes + c * NCOLS * 128, &a.tm_p[x.p], &pfull_bar[sp], a.r_pad + c * 64, j0);
-        }
+        uint8_t* pst = s_p0 + (size_t)sp * a.parts * a.b_bytes;
+        tc::mbar_arrive_expect_tx(&pfull_bar[sp], a.parts * a.b_bytes);
+        for (int q2 = 0; q2 < a.parts; ++q2)
+          for (int c = 0; c < a.kchunks; ++c)
+            tc::tma_load_2d(pst + q2 * a.b_bytes + c * NCOLS * 128, &a.tm_p[x.p], &pfull_bar[sp], q2 * a.r_pad + c * 64,
+                            j0);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -502,27 +597,34 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         prev_rb = x.rb;
       }
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
-        const int sp = it % NSP, b = it & 1;
+        const int sp = it % NSP, b = it % kTmemBufs;
         if (!tc::mbar_wait(&pfull_bar[sp], (it / NSP) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad) ||
-            (it >= 2 && !tc::mbar_wait(&tempty_bar[b], ((it >> 1) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))) {
+            (it >= kTmemBufs &&
+             !tc::mbar_wait(&tempty_bar[b], ((it / kTmemBufs) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))) {
           stop = true;
           break;
         }
         tc::tc_fence_after();
-        const uint32_t pst = tc::smem_u32(s_p0 + (size_t)sp * 2 * a.b_bytes);
+        const uint32_t pst = tc::smem_u32(s_p0 + (size_t)sp * a.parts * a.b_bytes);
+        const uint32_t sc = tc::smem_u32(s_c);
         const uint32_t d_tmem = tmem + (uint32_t)(b * NCOLS);
+        // products of the parts whose order is above ~2^-24: with two parts
+        // hi*hi, hi*lo, lo*hi; with three also hi*lo', mid*mid and lo'*hi
+        // (parts 0, 1, 2 = hi, mid, lo')
+        constexpr int kPairA[6] = {0, 0, 1, 0, 1, 2}, kPairB[6] = {0, 1, 0, 2, 1, 0};
+        const int npairs = a.parts == 3 ? 6 : 3;
         uint32_t acc = 0;
         for (int c = 0; c < a.kchunks; ++c) {
           for (int kk = 0; kk < 4 && c * 64 + kk * 16 < a.r_pad; ++kk) {
             const uint32_t off_a = c * 16384 + kk * 32, off_b = c * NCOLS * 128 + kk * 32;
-            const uint64_t ahi = tc::sdesc_sw128(tc::smem_u32(s_chi) + off_a, 16, 1024);
-            const uint64_t alo = tc::sdesc_sw128(tc::smem_u32(s_clo) + off_a, 16, 1024);
-            const uint64_t bhi = tc::sdesc_sw128(pst + off_b, 16, 1024);
-            const uint64_t blo = tc::sdesc_sw128(pst + a.b_bytes + off_b, 16, 1024);
-            tc::mma_bf16(d_tmem, ahi, bhi, idesc, acc);
-            tc::mma_bf16(d_tmem, ahi, blo, idesc, 1u);
-            tc::mma_bf16(d_tmem, alo, bhi, idesc, 1u);
-            acc = 1u;
+#pragma unroll
+            for (int pr = 0; pr < 6; ++pr) {
+              if (pr >= npairs) break;
+              const uint64_t ad = tc::sdesc_sw128(sc + kPairA[pr] * a.a_bytes + off_a, 16, 1024);
+              const uint64_t bd = tc::sdesc_sw128(pst + kPairB[pr] * a.b_bytes + off_b, 16, 1024);
+              tc::mma_bf16(d_tmem, ad, bd, idesc, acc);
+              acc = 1u;
+            }
           }
         }
         tc::mma_commit(&pempty_bar[sp]);
@@ -536,16 +638,19 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       }
       if (last_of_c && !stop) tc::mma_commit(&cempty_bar);
     }
-  } else if (warp == 2 && lane == 0) {
-    // ---------------- store warp ----------------
-    // Writes each finished tile from its W stage to W with TMA, then frees
-    // the stage once the copy has read it.
+  } else if (warp >= 2 && warp < kCtlWarps && lane == 0) {
+    // ---------------- store warps ----------------
+    // Store warp w writes tiles w - 2, w - 2 + kStoreWarps, ... from their W
+    // stages to W with TMA, and frees each stage once the copy has read it;
+    // the store warps' copies drain side by side.
     int it = 0;
     bool stop = false;
+    const int mine = warp - 2;
     for (int u = u_begin; u < u_end && !stop; ++u) {
       const Unit x = decode_unit(a, u);
       if (layer_skipped(x.p)) continue;
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
+        if (it % kStoreWarps != mine) continue;
         const int sw = it % NSW;
         if (!tc::mbar_wait(&sfull_bar[sw], (it / NSW) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
           stop = true;
@@ -563,31 +668,27 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       }
     }
     tc::bulk_wait_all();  // the writes are done before the CTA exits
-    // ... and visible to the generic loads of the careful-group pass below
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-  } else if (warp >= 4) {
+  } else if (warp >= kCtlWarps) {
     // ---------------- epilogue ----------------
-    const int ew = warp - 4;
+    // warp w may read TMEM lanes 32 (w % 4) .. +31 only: the sixteen warps
+    // cover each lane quarter four times, one column quarter each
+    const int ew = warp - kCtlWarps;
     const int quarter = warp & 3;
-    constexpr int kCols = NCOLS / 4;           // columns per thread per tile
-    constexpr int kPass = kCols < 32 ? kCols : 32;  // columns per pass
-    constexpr int kGroups = kPass / 8;              // 8-column groups (Philox blocks) per pass
-    constexpr int kGroupsPerWarp = kCols / 8;       // flag words of a warp per tile
-    // byte offset in a W stage (two 64-column, 128-byte-swizzled boxes) of this
-    // thread's 8-column groups: row q, column col_base + 8g
-    uint32_t stage_off[kGroupsPerWarp];
-#pragma unroll
-    for (int g = 0; g < kGroupsPerWarp; ++g) {
-      const int col = (ew >> 2) * kCols + 8 * g;
-      const int qq = (warp & 3) * 32 + lane;
-      stage_off[g] = (uint32_t)((col >> 6) * 16384 + qq * 128 + ((((col & 63) >> 3) ^ (qq & 7)) << 4));
-    }
+    constexpr int kCols = NCOLS / 4;           // columns per thread per tile (one pass)
+    constexpr int kGroups = kCols / 8;         // 8-column groups (Philox blocks) per tile
+    static_assert(kCols == 16 || kCols == 32, "16 or 32 columns per thread");
     const int col_base = (ew >> 2) * kCols;    // column quarter of the tile
     const int q = quarter * 32 + lane;         // tile row = TMEM lane
-    const bool storer = (ew == 0 && lane == 0);
+    // byte offset in a W stage (NCOLS/64 boxes of 64 columns, 128-byte
+    // swizzled) of this thread's 8-column groups: row q, column col_base + 8g
+    uint32_t stage_off[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      const int col = col_base + 8 * g;
+      stage_off[g] = (uint32_t)((col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
+    }
+    unsigned exact_n = 0;  // elements this lane recomputed exactly
     int it = 0;
-    // Every epilogue warp runs the same loop and reaches every named barrier;
-    // after a timed-out wait (abort) the work is skipped but the barriers are not.
     for (int u = u_begin; u < u_end; ++u) {
       const Unit x = decode_unit(a, u);
       const int p = x.p;
@@ -598,131 +699,107 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       const uint32_t k8 = (uint32_t)k >> 3;
       const bool row_ok = i < d;
       const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
-      const float thr_row = row_ok ? fabsf(s) * a.c_norm[p][i] * 0x1p-5f : 0.f;
+      const float bound_row = row_ok ? a.err_coef * fabsf(s) * a.c_norm[p][i] : 0.f;
       const uint32_t layer = a.layer[p];
       const bool need_norm = a.wnorm2_out[p] != nullptr;
       float sq = 0.f, sq_comp = 0.f;  // Kahan-compensated sum of squares
 
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
-        const int sw = it % NSW, b = it & 1;
+        const int sw = it % NSW, b = it % kTmemBufs;
         const int j0 = ct * NCOLS;
-        // largest norm of the P rows of this thread's columns (for the exactness
-        // test), loaded before the waits so that its latency hides behind them
+        // largest norm of the P rows of this warp's columns (for the margin
+        // bound), loaded before the waits so that its latency hides behind them
         float pmax = 0.f;
         {
-          const float* pnorm = a.p_norm[p];
-          const int jc = j0 + col_base + 2 * (lane % (kCols / 2));
-          if (jc + 1 < k) {
-            const float2 pn = *reinterpret_cast<const float2*>(pnorm + jc);
-            pmax = fmaxf(pn.x, pn.y);
-          } else if (jc < k) {
-            pmax = pnorm[jc];
-          }
+          const int jc = j0 + col_base + (lane % kCols);
+          if (jc < k) pmax = a.p_norm[p][jc];
         }
-        // W tile and H of this tile
         bool live = tc::mbar_wait(&wfull_bar[sw], (it / NSW) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad) &&
-                    tc::mbar_wait(&tfull_bar[b], (it >> 1) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
+                    tc::mbar_wait(&tfull_bar[b], (it / kTmemBufs) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
         live = __all_sync(0xFFFFFFFFu, live);
         tc::tc_fence_after();
         const uint32_t s_w32 = tc::smem_u32(s_w0) + (uint32_t)sw * a.w_bytes;
         for (int o = 16; o > 0; o >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
-        const float thr = thr_row * pmax;
+        const float bound = bound_row * pmax;  // 2^25 D for every element of this thread's row
         // live is the same in the whole warp: one branch per tile
         if (live) {
-#pragma unroll 1
-          for (int half = 0; half < kCols / kPass; ++half) {
-            const int col32 = col_base + half * kPass;
-            // H of the pass from TMEM, 16 columns at a time; the first load
-            // completes while the Philox blocks of the pass (independent chains)
-            // are computed
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col32);
+          const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col_base);
+          float gs = 0.f;  // sum of squares of this tile's results (normalized SGD)
+          // 16 columns (two 8-column groups) at a time: their H from TMEM, and
+          // the Philox blocks of element index e = i*k + j (j a multiple of 8):
+          // e / 8, computed while the TMEM load completes
+#pragma unroll
+          for (int hf = 0; hf < kGroups / 2; ++hf) {
             uint32_t h[16];
-            tc::tmem_ld_32x32b<16>(taddr, h);
-            // Philox block of element index e = i*k + j (j a multiple of 8): e / 8
-            uint32_t blks[kGroups];
+            tc::tmem_ld_32x32b<16>(taddr + 16 * hf, h);
+            uint32_t blks[2];
 #pragma unroll
-            for (int g = 0; g < kGroups; ++g) blks[g] = (uint32_t)i * k8 + ((uint32_t)(j0 + col32 + 8 * g) >> 3);
-            uint32_t rw[kGroups][4];
-            philox4x32_10_rk_multi<kGroups>(blks, a.step, layer, kTagSR, a.rk0, a.rk1, rw);
+            for (int gg = 0; gg < 2; ++gg)
+              blks[gg] = (uint32_t)i * k8 + ((uint32_t)(j0 + col_base + 16 * hf + 8 * gg) >> 3);
+            uint32_t rw[2][4];
+            philox4x32_10_rk_multi<2>(blks, a.step, layer, kTagSR, a.rk0, a.rk1, rw);
             tc::tmem_wait_ld_regs<16>(h);
-            // Per 8-column group: v = fmaf(-s, H, w) and stochastic rounding (add
-            // 16 random bits below the BF16 mantissa, keep the upper halves: one
-            // PRMT per pair); the results go back into the W stage in place (the
-            // store warp writes the tile out with TMA, clipping rows and columns
-            // outside W).  A group that holds a NaN or a value small enough for
-            // the exactness test is flagged for the careful path.
-            uint32_t fwords[kGroups];
-            float gs = 0.f;  // sum of squares of this pass's results (normalized SGD)
 #pragma unroll
-            for (int g = 0; g < kGroups; ++g) {
-              if (g == 2) {  // next 16 columns of H
-                tc::tmem_ld_32x32b<16>(taddr + 16, h);
-                tc::tmem_wait_ld_regs<16>(h);
-              }
-              const int col = col32 + 8 * g;
-              const uint32_t sp = s_w32 + stage_off[half * kGroups + g];
+            for (int gg = 0; gg < 2; ++gg) {
+              const int g = 2 * hf + gg;
+              const int col = col_base + 8 * g;
+              const uint32_t sp = s_w32 + stage_off[g];
               const uint4 raw = tc::lds128(sp);
               const uint32_t win[4] = {raw.x, raw.y, raw.z, raw.w};
-              const uint32_t* rwg = rw[g];
               uint32_t wout[4];
-              float av[8];
+              float ym[8];
+              // Per pair: v = fmaf(-s, H, w) and stochastic rounding (add 16
+              // random bits below the BF16 mantissa, keep the upper halves: one
+              // PRMT per pair); the results go back into the W stage in place
+              // (the store warp writes the tile out with TMA, clipping rows and
+              // columns outside W).  The integer steps use multiply-adds so that
+              // they share the multiplier pipe with Philox instead of crowding
+              // the ALU pipe: r_hi = r >> 16, r_lo = r - r_hi * 2^16 = r & 0xFFFF.
 #pragma unroll
               for (int t2 = 0; t2 < 4; ++t2) {
-                // BF16 -> fp32 by shifting into the high half; the integer steps
-                // use multiply-adds so that they share the multiplier pipe with
-                // Philox instead of crowding the ALU pipe: r_hi = r >> 16,
-                // r_lo = r - r_hi * 2^16 = r & 0xFFFF
-                const uint32_t wword = win[t2], rword = rwg[t2];
-                const float v0 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2]),
+                const uint32_t wword = win[t2], rword = rw[gg][t2];
+                const float v0 = fmaf(-s, __uint_as_float(h[8 * gg + 2 * t2]),
                                       __uint_as_float(mad_lo(wword, 0x10000u, 0u)));
-                const float v1 = fmaf(-s, __uint_as_float(h[8 * (g & 1) + 2 * t2 + 1]),
+                const float v1 = fmaf(-s, __uint_as_float(h[8 * gg + 2 * t2 + 1]),
                                       __uint_as_float(wword & 0xFFFF0000u));
                 const uint32_t r_hi = mad_hi(rword, 0x10000u, 0u);
                 const uint32_t r_lo = mad_lo(r_hi, 0xFFFF0000u, rword);
                 const uint32_t s0 = mad_lo(r_lo, 1u, __float_as_uint(v0));
                 const uint32_t s1 = mad_hi(rword, 0x10000u, __float_as_uint(v1));
                 wout[t2] = __byte_perm(s0, s1, 0x7632);
-                av[2 * t2] = fabsf(v0);  // folded into the min as an operand modifier
-                av[2 * t2 + 1] = fabsf(v1);
+                ym[2 * t2] = rounding_margin(s0, v0);
+                ym[2 * t2 + 1] = rounding_margin(s1, v1);
               }
-              // smallest |v| of the group; NaN if any v is NaN
-              const float gmin = fmin3_nan(fmin3_nan(av[0], av[1], av[2]), fmin3_nan(av[3], av[4], av[5]),
-                                           fmin_nan(av[6], av[7]));
+              // smallest margin of the group; NaN if any is NaN
+              const float gm = fmin3_nan(fmin3_nan(ym[0], ym[1], ym[2]), fmin3_nan(ym[3], ym[4], ym[5]),
+                                         fmin_nan(ym[6], ym[7]));
               const bool ok = row_ok && j0 + col < k;
-              const bool flag = ok && !(gmin >= thr);  // small value or NaN
-              // Careful path: a flagged group keeps its original W here and is
-              // marked in the flag bitmap (the word of the whole warp, written on
-              // every call); the careful-group pass at the end of this kernel
-              // redoes its 8 elements exactly from the original W, once the
-              // tiles are stored.  The norm sum keeps the tensor-core values of
-              // the group (they differ from the exact ones by at most one BF16
-              // step, or are below the threshold), except that a NaN makes it
-              // NaN.  The rare writes are predicated, not branched around.
-              fwords[g] = __ballot_sync(0xFFFFFFFFu, flag);
+              const bool flag = ok && !(gm >= bound);
               tc::sts128(sp, make_uint4(wout[0], wout[1], wout[2], wout[3]));
-              tc::sts128_if(sp, raw, flag);  // rare: the careful pass needs the original
               if (need_norm) {
                 float t = gs;
 #pragma unroll
                 for (int t2 = 0; t2 < 4; ++t2) t = sq_acc_bf16x2(wout[t2], t);
                 gs = ok ? t : gs;
-                sq = (ok && gmin != gmin) ? __int_as_float(0x7FC00000) : sq;
+              }
+              // Rare: elements whose margin the error bound might cross.  The
+              // whole warp recomputes them one at a time, each H_ij by a
+              // compensated dot product over r spread across the lanes.
+              if (__any_sync(0xFFFFFFFFu, flag)) {
+                gs += exact_path(flag, bound, raw, make_uint4(rw[gg][0], rw[gg][1], rw[gg][2], rw[gg][3]),
+                                 make_uint4(wout[0], wout[1], wout[2], wout[3]),
+                                 make_uint4(h[8 * gg], h[8 * gg + 1], h[8 * gg + 2], h[8 * gg + 3]),
+                                 make_uint4(h[8 * gg + 4], h[8 * gg + 5], h[8 * gg + 6], h[8 * gg + 7]),
+                                 a.fix_entries[p], a.fix_count[p], a.fix_cap[p], a.C[p], a.P[p], a.r,
+                                 x.rb * 128 + quarter * 32, j0 + col, k, s, sp, exact_n);
               }
             }
-            if (need_norm) {  // the pass's squares into the compensated sum
-              const float y = gs - sq_comp;
-              const float tsum = sq + y;
-              sq_comp = (tsum - sq) - y;
-              sq = tsum;
-            }
-            if (lane == 0) {  // every word of the layer is written on every call
-              uint32_t* fw = a.flags[p] + ((size_t)x.rb * a.n_ct[p] + ct) * (16 * kGroupsPerWarp) +
-                             ew * kGroupsPerWarp + half * kGroups;
-              if constexpr (kGroups == 4)
-                *reinterpret_cast<uint4*>(fw) = make_uint4(fwords[0], fwords[1], fwords[2], fwords[3]);
-              else
-                *reinterpret_cast<uint2*>(fw) = make_uint2(fwords[0], fwords[1]);
-            }
+          }
+          if (need_norm) {  // the tile's squares into the compensated sum
+            const float y = gs - sq_comp;
+            const float tsum = sq + y;
+            sq_comp = (tsum - sq) - y;
+            sq = tsum;
           }
         }
         // this warp is done with the TMEM buffer
@@ -736,29 +813,38 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         if (lane == 0) tc::mbar_arrive(&sfull_bar[sw]);
       }
       if (need_norm) {
-        // ||W_new||^2 of this unit, then the layer's last unit sums all units in order
+        // ||W_new||^2 of this unit: each warp leaves its share in a shared
+        // slot of the unit; the unit's last warp adds the 16 shares in warp
+        // order, and the layer's last unit (ticket) adds all units in order
         double dsq = (double)sq - (double)sq_comp;
         for (int o = 16; o > 0; o >>= 1) dsq += __shfl_xor_sync(0xFFFFFFFFu, dsq, o);
-        if (lane == 0) warp_sq[ew] = dsq;
-        tc::named_barrier(1, kEpiWarps * 32);
-        if (storer) {
-          double tot = 0.0;
-          for (int w = 0; w < kEpiWarps; ++w) tot += warp_sq[w];
-          const int lu = u - a.unit_begin[p];
-          a.unit_partials[p][lu] = tot;
-          __threadfence();
-          const unsigned nunits = (unsigned)(a.unit_begin[p + 1] - a.unit_begin[p]);
-          if (atomicAdd(a.ticket[p], 1u) == nunits - 1) {
+        if (lane == 0) {
+          const int slot = (u - u_begin) & (kNormSlots - 1);
+          norm_slot[slot][ew] = dsq;
+          __threadfence_block();
+          if (atomicAdd(&norm_count[slot], 1) == kEpiWarps - 1) {
+            __threadfence_block();
+            double tot = 0.0;
+            for (int w = 0; w < kEpiWarps; ++w) tot += *((volatile double*)&norm_slot[slot][w]);
+            norm_count[slot] = 0;
+            const int lu = u - a.unit_begin[p];
+            a.unit_partials[p][lu] = tot;
             __threadfence();
-            double all = 0.0;
-            for (unsigned b2 = 0; b2 < nunits; ++b2) all += *((volatile double*)&a.unit_partials[p][b2]);
-            *a.wnorm2_out[p] = all;
-            *a.ticket[p] = 0u;
+            const unsigned nunits = (unsigned)(a.unit_begin[p + 1] - a.unit_begin[p]);
+            if (atomicAdd(a.ticket[p], 1u) == nunits - 1) {
+              __threadfence();
+              double all = 0.0;
+              for (unsigned b2 = 0; b2 < nunits; ++b2) all += *((volatile double*)&a.unit_partials[p][b2]);
+              *a.wnorm2_out[p] = all;
+              *a.ticket[p] = 0u;
+            }
           }
         }
-        tc::named_barrier(1, kEpiWarps * 32);  // warp_sq reusable
       }
     }
+    for (int o = 16; o > 0; o >>= 1) exact_n += __shfl_xor_sync(0xFFFFFFFFu, exact_n, o);
+    if (lane == 0 && exact_n != 0 && a.exact_count != nullptr)
+      atomicAdd(a.exact_count, (unsigned long long)exact_n);
   }
   // SGD: every layer's status word reads 0 (written by the first CTA)
   if (blockIdx.x == 0) {
@@ -768,103 +854,6 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
-  if (abort_flag) return;
-
-  // Careful groups of this CTA's tiles.  Each flagged group still holds its
-  // original W (the stage kept it and the TMA stores above have completed), so
-  // it is redone exactly here.  Pass 1: the warps read the flag words of the
-  // CTA's units (units in turn) and append the nonzero ones to a list in the
-  // now idle dynamic shared memory.
-  // Pass 2: the warps take the list's words in turn, so each warp redoes about
-  // the same number of groups; the operands of a warp's next word are
-  // prefetched into L2 while it works on the current one.  A word that finds
-  // the list full is redone at once by the warp that read it.
-  constexpr int kWarps = kUpdThreads / 32;
-  constexpr int kGroupsPerWarpT = NCOLS / 32, kWordsPerTile = 16 * kGroupsPerWarpT;
-  constexpr int kBatch = 8;  // flag words per lane per load batch
-  uint4* clist = reinterpret_cast<uint4*>(smem);
-  if (threadIdx.x == 0) clist_n = 0;
-  __syncthreads();
-  // the careful groups of word `bits` at word index widx of layer p
-  auto redo_word = [&](int p, uint32_t widx, uint32_t bits) {
-    const uint32_t tile = widx / kWordsPerTile, wt = widx % kWordsPerTile;
-    const int n_ct = a.n_ct[p];
-    const int rb = (int)(tile / (uint32_t)n_ct), ct = (int)(tile % (uint32_t)n_ct);
-    const int ew = (int)wt / kGroupsPerWarpT, gw = (int)wt % kGroupsPerWarpT;
-    const int j = ct * NCOLS + (ew >> 2) * (NCOLS / 4) + 8 * gw;
-    while (bits) {
-      const int row = __ffs(bits) - 1;
-      bits &= bits - 1;
-      careful_group_warp(a, p, rb * 128 + (ew & 3) * 32 + row, j);
-    }
-  };
-  // pass 1: warp w reads the flag words of units w, w + kWarps, ... (a unit's
-  // words are contiguous), kBatch words per lane at a time
-  for (int u = u_begin + warp; u < u_end; u += kWarps) {
-    const Unit x = decode_unit(a, u);
-    if (layer_skipped(x.p)) continue;
-    const uint32_t wbeg = (uint32_t)(x.rb * a.n_ct[x.p] + x.ct0) * (uint32_t)kWordsPerTile;
-    const uint32_t nwords = (uint32_t)(x.ct1 - x.ct0) * (uint32_t)kWordsPerTile;
-    const uint32_t* fw = a.flags[x.p] + wbeg;
-    for (uint32_t w0 = 0; w0 < nwords; w0 += 32 * kBatch) {
-      uint32_t v[kBatch];
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const uint32_t idx = w0 + 32 * b + lane;
-        v[b] = idx < nwords ? fw[idx] : 0u;
-      }
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const uint32_t nz = __ballot_sync(0xFFFFFFFFu, v[b] != 0u);
-        if (nz == 0u) continue;
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&clist_n, __popc(nz));
-        base = __shfl_sync(0xFFFFFFFFu, base, 0);
-        const int slot = base + __popc(nz & ((1u << lane) - 1u));
-        const uint32_t widx = wbeg + w0 + 32 * b + lane;
-        const bool mine = v[b] != 0u;
-        if (mine && slot < a.list_cap) clist[slot] = make_uint4((uint32_t)x.p, widx, v[b], 0u);
-        uint32_t over = __ballot_sync(0xFFFFFFFFu, mine && slot >= a.list_cap);
-        while (over) {  // the list is full: redo these words here
-          const int src = __ffs(over) - 1;
-          over &= over - 1;
-          redo_word(x.p, __shfl_sync(0xFFFFFFFFu, widx, src), __shfl_sync(0xFFFFFFFFu, v[b], src));
-        }
-      }
-    }
-  }
-  __syncthreads();
-  const int n_list = clist_n < a.list_cap ? clist_n : a.list_cap;
-  // pass 2: entries warp, warp + kWarps, ...; the operands of the warp's next
-  // entry are prefetched into L2 while it works on the current one
-  for (int e = warp; e < n_list; e += kWarps) {
-    const uint4 en = clist[e];
-    if (e + kWarps < n_list) {
-      const uint4 nx = clist[e + kWarps];
-      const int p2 = (int)nx.x;
-      const uint32_t tile = nx.y / kWordsPerTile, wt = nx.y % kWordsPerTile;
-      const int n_ct = a.n_ct[p2];
-      const int rb = (int)(tile / (uint32_t)n_ct), ct = (int)(tile % (uint32_t)n_ct);
-      const int ew = (int)wt / kGroupsPerWarpT, gw = (int)wt % kGroupsPerWarpT;
-      const int j = ct * NCOLS + (ew >> 2) * (NCOLS / 4) + 8 * gw;
-      const int i = rb * 128 + (ew & 3) * 32 + __ffs(nx.z) - 1;
-      const int r = a.r, kk = (int)a.k[p2];
-      const int jn = (kk - j) < 8 ? (kk - j) : 8;
-      // P rows j..j+jn-1 (contiguous), the C row and the W group: one address
-      // per 128-byte line, every address inside its buffer
-      const char* pbase = reinterpret_cast<const char*>(a.P[p2] + (int64_t)j * r);
-      const int pbytes = jn * r * 4, plines = pbytes / 128 + 2;
-      const char* cbase = reinterpret_cast<const char*>(a.C[p2] + (int64_t)i * r);
-      const int cbytes = r * 4, clines = cbytes / 128 + 2;
-      for (int l = lane; l < plines + clines + 1; l += 32) {
-        const char* ad = l < plines ? pbase + min(128 * l, pbytes - 1)
-                         : l < plines + clines ? cbase + min(128 * (l - plines), cbytes - 1)
-                                               : reinterpret_cast<const char*>(a.W[p2] + (int64_t)i * a.ld_w[p2] + j);
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(ad));
-      }
-    }
-    redo_word((int)en.x, en.y, en.z);
-  }
 }
 
 int round16(int r) { return (r + 15) / 16 * 16; }
@@ -873,6 +862,18 @@ int round16(int r) { return (r + 15) / 16 * 16; }
 // must fit in shared memory.
 int update_ncols(int r) { return round16(r) <= 64 ? 128 : 64; }
 
+// BF16 parts of C and P: two, so H takes three products (hi hi, hi lo, lo hi).
+int update_parts(int) { return 2; }
+
+// Error of the three-product tensor-core H relative to ||c_i|| ||p_j||: twice
+// the largest error measured over millions of elements for each rank class
+// (Gaussian C; Gaussian-QR and Rademacher P): 2^-16.8 for r = 16, 2^-17.7 for
+// r = 4, 2^-18.1 for r = 64, 2^-18.7 for r = 128, 2^-19.3 for r = 256.  The
+// margin test treats any H within this of the exact product as possible.
+float tc_err_beta(int r) {
+  return r <= 32 ? 0x1p-16f : r <= 64 ? 0x1p-17f : r <= 128 ? 0x1.6a09e6p-18f : 0x1p-18f;
+}
+
 template <int NCOLS>
 cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, bool normsgd,
                              float scale_val, uint64_t seed, uint32_t step, cudaStream_t stream) {
@@ -880,9 +881,14 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   int* errw = nullptr;
   cudaError_t err = device_error_word(&errw);
   if (err != cudaSuccess) return err;
+  unsigned long long* exact = nullptr;
+  err = device_exact_counter(&exact);
+  if (err != cudaSuccess) return err;
   static thread_local UpdBatch a;
+  const int parts = update_parts(r);
   a.scale_val = scale_val;
-  a.seed = seed;
+  a.parts = parts;
+  a.err_coef = 0x1p25f * (tc_err_beta(r) + 0x1p-24f);
   philox_round_keys(seed, a.rk0, a.rk1);
   a.step = step;
   a.r = r;
@@ -892,22 +898,23 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   a.b_bytes = (uint32_t)a.kchunks * NCOLS * 128u;
   a.w_bytes = (uint32_t)(NCOLS / 64) * 16384u;
   a.err = errw;
+  a.exact_count = exact;
   // dynamic shared memory: what the opt-in limit leaves next to the static arrays
   cudaFuncAttributes fa;
   err = cudaFuncGetAttributes(&fa, update_persistent_kernel<NCOLS>);
   if (err != cudaSuccess) return err;
   const size_t max_smem = 227 * 1024 - fa.sharedSizeBytes;
-  const size_t fixed = 2 * (size_t)a.a_bytes + 1024;
-  const size_t p_stage = 2 * (size_t)a.b_bytes;
-  // two P stages when they fit next to at least two W stages, else one
-  int p_stages = (fixed + 2 * p_stage + 2 * a.w_bytes <= max_smem) ? 2 : 1;
+  const size_t fixed = (size_t)parts * a.a_bytes + 1024;
+  const size_t p_stage = (size_t)parts * a.b_bytes;
+  // two P stages when they still leave four W stages (W comes from HBM and
+  // needs the deeper ring), else one
+  int p_stages = (fixed + 2 * p_stage + 4 * (size_t)a.w_bytes <= max_smem) ? 2 : 1;
   int w_stages = (int)((max_smem - fixed - p_stages * p_stage) / a.w_bytes);
   if (w_stages > kMaxStagesUpd) w_stages = kMaxStagesUpd;
   if (w_stages < 1) return cudaErrorInvalidConfiguration;
   a.p_stages = p_stages;
   a.w_stages = w_stages;
   const size_t smem = fixed + p_stages * p_stage + (size_t)w_stages * a.w_bytes;
-  a.list_cap = (int)((smem - 1024) / 16);  // after the 1024-byte alignment
   err = cudaFuncSetAttribute(update_persistent_kernel<NCOLS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
   if (err != cudaSuccess) return err;
@@ -928,14 +935,14 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
     for (int i = 0; i < m; ++i) {
       const UpdateProblem& pr = probs[base + i];
       const UpdateWorkspace& w = ws[base + i];
-      err = make_tmap_bf16_2d(&a.tm_c[i], w.c_split, (uint64_t)2 * r_pad, (uint64_t)pr.d, (uint64_t)r_pad * 4, 64, 128);
+      err = make_tmap_bf16_2d(&a.tm_c[i], w.c_split, (uint64_t)parts * r_pad, (uint64_t)pr.d,
+                              (uint64_t)parts * r_pad * 2, 64, 128);
       if (err == cudaSuccess)
-        err = make_tmap_bf16_2d(&a.tm_p[i], w.p_split, (uint64_t)2 * r_pad, (uint64_t)pr.k, (uint64_t)r_pad * 4, 64, NCOLS);
+        err = make_tmap_bf16_2d(&a.tm_p[i], w.p_split, (uint64_t)parts * r_pad, (uint64_t)pr.k,
+                                (uint64_t)parts * r_pad * 2, 64, NCOLS);
       if (err == cudaSuccess)
         err = make_tmap_bf16_2d(&a.tm_w[i], pr.W, (uint64_t)pr.k, (uint64_t)pr.d, (uint64_t)pr.ld_w * 2, 64, 128);
       if (err != cudaSuccess) return err;
-      a.W[i] = pr.W;
-      a.ld_w[i] = pr.ld_w;
       a.C[i] = pr.C;
       a.P[i] = pr.P;
       a.c_norm[i] = w.c_norm;
@@ -950,9 +957,11 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       a.status_in[i] = normsgd ? (pr.dev_status ? pr.dev_status : w.status) : nullptr;
       a.status_out[i] = normsgd ? nullptr : pr.dev_status;
       a.unit_partials[i] = w.wnew_partials;
-      a.flags[i] = w.flags;
       a.ticket[i] = w.ticket;
       a.wnorm2_out[i] = normsgd ? pr.wnorm2_out : nullptr;
+      a.fix_entries[i] = w.fix_entries;
+      a.fix_count[i] = w.fix_count;
+      a.fix_cap[i] = w.fix_cap;
     }
     const int units = a.unit_begin[m];
     int grid = units < nsm ? units : nsm;
@@ -987,11 +996,181 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   return cudaSuccess;
 }
 
+// ---- the exact path's queue ---------------------------------------------------
+// The update kernel leaves each element whose rounding margin its tensor-core
+// H might cross in its layer's queue (row, column, original weight, 16 random
+// bits, tensor-core result) and stores the tensor-core result.  Once every
+// tile is stored, this kernel redoes each queued element the way the
+// definition does: H_ij as a compensated dot product (Dot2) of the fp32 row i
+// of C and row j of P, v = fmaf(-s, fl32(H_ij), w), the same stochastic
+// rounding, and writes the weight.  For normalized SGD it also carries the
+// change of ||W_new||^2: each element's change (new^2 - old^2, exact in
+// double) in fixed point relative to the layer's norm, summed as integers so
+// that the total does not depend on the order of the queue, and the layer's
+// last block adds it to the norm.
+struct FixBatch {
+  const uint4* entries[kMaxUpd];
+  const uint32_t* count[kMaxUpd];
+  uint32_t cap[kMaxUpd];
+  uint32_t* ticket[kMaxUpd];
+  unsigned long long* acc[kMaxUpd];
+  const float* C[kMaxUpd];
+  const float* P[kMaxUpd];
+  uint16_t* W[kMaxUpd];
+  int64_t ld_w[kMaxUpd];
+  const float* scale_dev[kMaxUpd];     // normalized SGD: s on the device; NULL: scale_val
+  const int32_t* status_in[kMaxUpd];   // layer skipped when nonzero
+  double* wnorm2_out[kMaxUpd];
+  int n;
+  int r;
+  float scale_val;
+  unsigned long long* exact_count;
+};
+constexpr int kFixBlocks = 16;  // blocks per layer (grid.x)
+constexpr int kFixFracBits = 40;  // fixed point: 2^-40 of the layer's norm
+
+__global__ void __launch_bounds__(256) exact_fix_kernel(const __grid_constant__ FixBatch b) {
+  __shared__ long long red[8];
+  __shared__ int red_bad[8];
+  const int p = blockIdx.y;
+  if (b.status_in[p] != nullptr && *b.status_in[p] != 0) return;  // the update skipped the layer
+  const uint32_t n_e = min(*b.count[p], b.cap[p]);
+  const float s = b.scale_dev[p] ? *b.scale_dev[p] : b.scale_val;
+  double* wn = b.wnorm2_out[p];
+  const double ref = wn ? *wn : 0.0;
+  // ref >= every tensor-core square, and an element's exact result is within
+  // a step or two of its tensor-core one, so |change| <= ~1.1 ref and a
+  // change is at most ~2^42 in fixed point.  A non-finite norm stays as it
+  // is; a zero norm (every tensor-core result zero) takes a plain double sum.
+  if (wn != nullptr && !isfinite(ref)) wn = nullptr;
+  const bool fixed = ref > 0.0;
+  const double to_fixed = fixed ? ldexp(1.0, kFixFracBits - ilogb(ref)) : 1.0;
+  const int r = b.r;
+  const bool vec = (r & 3) == 0;
+  long long q = 0;
+  int bad = 0;
+  unsigned done = 0;
+  for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < n_e; e += gridDim.x * blockDim.x) {
+    const uint4 en = b.entries[p][e];
+    const int i = (int)en.x, j = (int)en.y;
+    const uint32_t w16 = en.z & 0xFFFFu, r16 = en.z >> 16, o16 = en.w & 0xFFFFu;
+    const float* crow = b.C[p] + (int64_t)i * r;
+    const float* prow = b.P[p] + (int64_t)j * r;
+    float hs = 0.f, he = 0.f;
+    auto term = [&](float cv, float pv) {
+      const float m = __fmul_rn(cv, pv);
+      float sum, err;
+      two_sum(hs, m, sum, err);
+      hs = sum;
+      he = __fadd_rn(he, __fadd_rn(err, __fmaf_rn(cv, pv, -m)));
+    };
+    if (vec) {
+      for (int l = 0; l < r; l += 4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(crow + l);
+        const float4 p4 = *reinterpret_cast<const float4*>(prow + l);
+        term(c4.x, p4.x);
+        term(c4.y, p4.y);
+        term(c4.z, p4.z);
+        term(c4.w, p4.w);
+      }
+    } else {
+      for (int l = 0; l < r; ++l) term(crow[l], prow[l]);
+    }
+    const float hx = __fadd_rn(hs, he);
+    const float v = fmaf(-s, hx, __uint_as_float(w16 << 16));
+    const uint32_t out = sr_bf16_bits(v, r16);
+    b.W[p][(int64_t)i * b.ld_w[p] + j] = (uint16_t)out;
+    ++done;
+    if (wn != nullptr && out != o16) {
+      const double fo = (double)__uint_as_float(o16 << 16), fn = (double)__uint_as_float(out << 16);
+      const double delta = fn * fn - fo * fo;  // exact: both squares have 16-bit mantissas
+      if (!isfinite(delta)) bad = 1;
+      else if (fixed) q += llrint(delta * to_fixed);
+      else atomicAdd(reinterpret_cast<double*>(b.acc[p]), delta);
+    }
+  }
+  // the block's sums (integers: order-free), then one atomic per block
+  for (int o = 16; o > 0; o >>= 1) {
+    q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
+    bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+    done += __shfl_xor_sync(0xFFFFFFFFu, done, o);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ unsigned red_done[8];
+  if (lane == 0) {
+    red[warp] = q;
+    red_bad[warp] = bad;
+    red_done[warp] = done;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long tq = 0;
+    int tb = 0;
+    unsigned td = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      tq += red[w];
+      tb |= red_bad[w];
+      td += red_done[w];
+    }
+    if (td != 0 && b.exact_count != nullptr) atomicAdd(b.exact_count, (unsigned long long)td);
+    if (wn != nullptr) {
+      if (tq != 0) atomicAdd(b.acc[p], (unsigned long long)tq);
+      if (tb) atomicOr(reinterpret_cast<unsigned int*>(b.ticket[p]) + 0, 0x80000000u);
+      __threadfence();
+      const unsigned t = atomicAdd(b.ticket[p], 1u);
+      if ((t & 0x7FFFFFFFu) == gridDim.x - 1) {  // the layer's last block
+        __threadfence();
+        const unsigned tk = *((volatile unsigned*)b.ticket[p]);
+        const unsigned long long acc = *((volatile unsigned long long*)b.acc[p]);
+        const double add = fixed ? (double)(long long)acc / to_fixed : __longlong_as_double((long long)acc);
+        *wn = (tk & 0x80000000u) ? __longlong_as_double(0x7FF8000000000000ll) : ref + add;
+      }
+    }
+  }
+}
+
+cudaError_t launch_exact_fix(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, bool normsgd,
+                             float scale_val, cudaStream_t stream) {
+  unsigned long long* exact = nullptr;
+  cudaError_t err = device_exact_counter(&exact);
+  if (err != cudaSuccess) return err;
+  static thread_local FixBatch f;
+  f.r = r;
+  f.scale_val = scale_val;
+  f.exact_count = exact;
+  for (int base = 0; base < n; base += kMaxUpd) {
+    const int m = (n - base) < kMaxUpd ? (n - base) : kMaxUpd;
+    f.n = m;
+    for (int i = 0; i < m; ++i) {
+      const UpdateProblem& pr = probs[base + i];
+      const UpdateWorkspace& w = ws[base + i];
+      f.entries[i] = w.fix_entries;
+      f.count[i] = w.fix_count;
+      f.cap[i] = w.fix_cap;
+      f.ticket[i] = w.fix_ticket;
+      f.acc[i] = w.fix_acc;
+      f.C[i] = pr.C;
+      f.P[i] = pr.P;
+      f.W[i] = pr.W;
+      f.ld_w[i] = pr.ld_w;
+      f.scale_dev[i] = normsgd ? w.scale : nullptr;
+      f.status_in[i] = normsgd ? (pr.dev_status ? pr.dev_status : w.status) : nullptr;
+      f.wnorm2_out[i] = normsgd ? pr.wnorm2_out : nullptr;
+    }
+    count_launch();
+    exact_fix_kernel<<<dim3(kFixBlocks, m), 256, 0, stream>>>(f);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_split(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, cudaStream_t stream) {
   static thread_local SplitBatch sb;
   const int r_pad = round16(r);
   sb.r = r;
   sb.r_pad = r_pad;
+  sb.parts = update_parts(r);
   for (int base = 0; base < n; base += kMaxAux) {
     const int m = (n - base) < kMaxAux ? (n - base) : kMaxAux;
     sb.n = 2 * m;
@@ -1006,6 +1185,9 @@ cudaError_t launch_split(int n, const UpdateProblem* probs, const UpdateWorkspac
       sb.dst[2 * i + 1] = ws[base + i].p_split;
       sb.norm[2 * i + 1] = ws[base + i].p_norm;
       sb.row_begin[2 * i + 2] = sb.row_begin[2 * i + 1] + pr.k;
+      sb.fix_count[i] = ws[base + i].fix_count;
+      sb.fix_ticket[i] = ws[base + i].fix_ticket;
+      sb.fix_acc[i] = ws[base + i].fix_acc;
     }
     const int64_t blocks = ceil_div(sb.row_begin[2 * m], 8);
     const int grid = (int)(blocks < 8 * (int64_t)num_sms() ? blocks : 8 * (int64_t)num_sms());
@@ -1019,17 +1201,18 @@ cudaError_t launch_update(int n, const UpdateProblem* probs, const UpdateWorkspa
                           float scale_val, uint64_t seed, uint32_t step, cudaStream_t stream) {
   cudaError_t err = launch_split(n, probs, ws, r, stream);
   if (err != cudaSuccess) return err;
-  if (update_ncols(r) == 128)
-    return launch_update_tc<128>(n, probs, ws, r, normsgd, scale_val, seed, step, stream);
-  return launch_update_tc<64>(n, probs, ws, r, normsgd, scale_val, seed, step, stream);
+  err = (update_ncols(r) == 128) ? launch_update_tc<128>(n, probs, ws, r, normsgd, scale_val, seed, step, stream)
+                                 : launch_update_tc<64>(n, probs, ws, r, normsgd, scale_val, seed, step, stream);
+  if (err != cudaSuccess) return err;
+  return launch_exact_fix(n, probs, ws, r, normsgd, scale_val, stream);
 }
 
 }  // namespace
 
-int64_t flag_words(int64_t d, int64_t k, int r) {
-  const int ncols = update_ncols(r);
-  return ceil_div(d, 128) * ceil_div(k, ncols) * (16 * ncols / 32);
-}
+// Entries of a layer's exact-path queue: one per 1024 weights plus 1024, about
+// twice what a trained-scale layer needs; elements beyond it are redone in
+// place by the update kernel itself.
+uint32_t fix_capacity(int64_t d, int64_t k) { return (uint32_t)(d * k / 1024 + 1024); }
 
 size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool normsgd, UpdateWorkspace* ws) {
   const size_t start = cur.offset;
@@ -1048,9 +1231,13 @@ size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool n
   }
   w.c_norm = cur.take<float>((size_t)d);
   w.p_norm = cur.take<float>((size_t)k);
-  w.c_split = cur.take<uint16_t>((size_t)d * 2 * r_pad);
-  w.p_split = cur.take<uint16_t>((size_t)k * 2 * r_pad);
-  w.flags = cur.take<uint32_t>((size_t)flag_words(d, k, r));
+  w.c_split = cur.take<uint16_t>((size_t)d * update_parts(r) * r_pad);
+  w.p_split = cur.take<uint16_t>((size_t)k * update_parts(r) * r_pad);
+  w.fix_count = cur.take<uint32_t>(1);
+  w.fix_ticket = cur.take<uint32_t>(1);
+  w.fix_acc = cur.take<unsigned long long>(1);
+  w.fix_cap = fix_capacity(d, k);
+  w.fix_entries = cur.take<uint4>(w.fix_cap);
   cur.take<char>(0);  // end on a 256-byte boundary
   if (ws) *ws = w;
   return cur.offset - start;

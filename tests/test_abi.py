@@ -48,10 +48,11 @@ def test_status_strings(lib):
 
 def test_workspace_sizes(lib):
     ws = binding.workspace_bytes
-    # BF16 high/low parts of C and P, their fp32 row norms, and the careful-group
-    # flag bitmap (one bit per 8 weights)
+    # BF16 high/low parts of C and P, their fp32 row norms, three 256-byte
+    # counters and the exact-path queue (16 bytes per 1024 weights, plus 1024)
+    queue = 16 * (4096 * 4096 // 1024 + 1024)
     assert ws(binding.OP_UPDATE_SGD, 0, 4096, 4096, 64) == (4 * (4096 + 4096) * 64 + 4 * (4096 + 4096)
-                                                           + 4096 * 4096 // 64)
+                                                           + 3 * 256 + queue)
     a = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 64)
     b = ws(binding.OP_UPDATE_NORMSGD, 0, 8192, 4096, 64)
     c = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 128)
@@ -113,6 +114,7 @@ def test_sample_projection_argument_errors(lib):
 
 def test_read_device_errors_needs_output(lib):
     assert lib.sketch_read_device_errors(NULL, NULL) == binding.ERR_INVALID_ARG
+    assert lib.sketch_read_exact_count(NULL, NULL) == binding.ERR_INVALID_ARG
 
 
 def test_binding_refuses_cpu_tensors(lib):
@@ -152,8 +154,11 @@ def test_policy_sync_payload_is_the_factor_and_seed():
     import torch
     from rank_gradient_sketching_philox_gb300 import policy_sync
     C = torch.arange(12, dtype=torch.float32).view(4, 3)
-    assert torch.equal(policy_sync.payload(C, 0.5), C * 0.5)
-    assert policy_sync.payload_bytes(4096, 64) == 4 * 4096 * 64 + 16       # vs 2*4096*4096 of BF16 W
+    msg = policy_sync.message(C, 0.5, 7, 2, 5)
+    assert msg.U is C and (msg.alpha_eta, msg.seed, msg.layer, msg.step) == (0.5, 7, 2, 5)  # nothing computed
+    with pytest.raises(TypeError):
+        policy_sync.message(C.double(), 0.5, 7, 2, 5)
+    assert policy_sync.payload_bytes(4096, 64) == 4 * 4096 * 64 + 20       # vs 2*4096*4096 of BF16 W
 
 
 def test_fp32_xp_needs_room_for_the_pair(lib):
