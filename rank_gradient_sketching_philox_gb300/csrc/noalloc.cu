@@ -9,13 +9,16 @@
 // workspace taken from a fixed array in device memory that this file owns.
 //
 // The array is kNoAllocScratchBytes long.  It is reserved on a device when the
-// library's device code is loaded there (at the latest on the first call) and
-// stays reserved until the process exits.  Every call shares it: two calls
-// whose kernels overlap on the GPU (different streams, or different host
-// threads) race on it and corrupt each other's results; order such calls on one
-// stream.  No word of it needs to start at zero: each call writes every scratch
-// value it reads before reading it, so the contents left by an earlier call do
-// not matter.
+// library's device code is loaded there (under lazy module loading: when the
+// first call looks up its address) and stays reserved until the process exits.
+// The address found on a device is cached for the life of the process; a
+// cudaDeviceReset() on that device invalidates it (and every other address the
+// library keeps), so the library must not be called on a device after it has
+// been reset.  Every call shares the array: two calls whose kernels overlap on
+// the GPU (different streams, or different host threads) race on it and
+// corrupt each other's results; order such calls on one stream.  No word of it
+// needs to start at zero: each call writes every scratch value it reads before
+// reading it, so the contents left by an earlier call do not matter.
 #include <cstdio>
 #include <mutex>
 

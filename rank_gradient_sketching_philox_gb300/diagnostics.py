@@ -3,7 +3,8 @@ the dense gradient G = D^T X, over ranks and projection kinds.
 
 The sketch C = D^T (X P) and the projection come from the library (the same
 kernels as training); the dense G is formed only here, as the thing H is
-compared with.  ("LoGRA: Scaling LLM Reinforcement Learning with Low-Rank
+compared with.  Both G and H = C P^T are formed in float64 from the library's
+C and P, so the measured cosine carries no rounding of this module's own.  ("LoGRA: Scaling LLM Reinforcement Learning with Low-Rank
 Gradient Sketches", Experimental Findings: reconstruction cosine over ranks;
 "LoGRA: Low-Rank Gradient Sketches", "Why Refreshing the Projection Enables New
 Update Directions": averaging over refreshed projections recovers more of G.)
@@ -34,8 +35,8 @@ def reconstruction(Ds, Xs, r, kind, steps=1, refreshed=True, seed=0, layer=0):
     (P refreshed each step, or the step-0 projection every time)."""
     dev = Xs[0].device
     d, k = Ds[0].shape[1], Xs[0].shape[1]
-    G = sum(D.float().t() @ X.float() for D, X in zip(Ds, Xs))
-    H = torch.zeros(d, k, dtype=torch.float32, device=dev)
+    G = sum(D.double().t() @ X.double() for D, X in zip(Ds, Xs))
+    H = torch.zeros(d, k, dtype=torch.float64, device=dev)
     P = torch.empty(k, r, dtype=torch.float32, device=dev)
     C = torch.empty(d, r, dtype=torch.float32, device=dev)
     for s in range(steps):
@@ -45,7 +46,7 @@ def reconstruction(Ds, Xs, r, kind, steps=1, refreshed=True, seed=0, layer=0):
             XP = torch.empty(X.shape[0], (r + 7) // 8 * 8, dtype=torch.bfloat16, device=dev)[:, :r]
             binding.project_inputs(X, P, XP)
             binding.accumulate(D, XP, C, overwrite=(m == 0))
-        H += C @ P.t()
+        H += C.double() @ P.double().t()
     H /= steps
     gn = torch.linalg.norm(G)
     cos = float((G * H).sum() / (gn * torch.linalg.norm(H)))
