@@ -661,7 +661,7 @@ def main():
     if e2e_steps > 0:
         # Every microbatch's X (per input group) and D (per layer) come from
         # pinned host memory (two host buffers per shape).  The copies run on
-        # their own stream into two device sets used alternately, so the
+        # their own streams into two device sets used alternately, so the
         # copies of microbatch m+1 overlap the kernels of microbatch m.
         hx, hd = {}, {}
         for gi, k in enumerate(gk):
@@ -672,8 +672,9 @@ def main():
                 hd[d] = [dsets[i][li].cpu().pin_memory() for i in range(2)]
         h2d = nmb * (x_bytes + d_bytes)
         d2h = status.numel() * 4 + wn2.numel() * 8
-        copy_stream = torch.cuda.Stream(dev)
-        copied = [torch.cuda.Event() for _ in range(2)]
+        # several copy streams, so that more than one copy engine moves data
+        copy_streams = [torch.cuda.Stream(dev) for _ in range(4)]
+        copied = [[torch.cuda.Event() for _ in copy_streams] for _ in range(2)]
         consumed = [torch.cuda.Event() for _ in range(2)]
         for b in range(2):
             consumed[b].record(stream)
@@ -687,14 +688,16 @@ def main():
                 sample_phase(s)
             for m in range(nmb):
                 b = m % 2
-                copy_stream.wait_event(consumed[b])  # the kernels that read set b are done
-                with torch.cuda.stream(copy_stream):
-                    for gi, k in enumerate(gk):
-                        xsets[b][gi].copy_(hx[k][(gi + m) % 2], non_blocking=True)
-                    for li, (_, d, _) in enumerate(layers):
-                        dsets[b][li].copy_(hd[d][(li + m) % 2], non_blocking=True)
-                copied[b].record(copy_stream)
-                stream.wait_event(copied[b])
+                jobs = ([(xsets[b][gi], hx[k][(gi + m) % 2]) for gi, k in enumerate(gk)] +
+                        [(dsets[b][li], hd[d][(li + m) % 2]) for li, (_, d, _) in enumerate(layers)])
+                for ci, cs in enumerate(copy_streams):
+                    cs.wait_event(consumed[b])  # the kernels that read set b are done
+                    with torch.cuda.stream(cs):
+                        for dst, src in jobs[ci::len(copy_streams)]:
+                            dst.copy_(src, non_blocking=True)
+                    copied[b][ci].record(cs)
+                for ev in copied[b]:
+                    stream.wait_event(ev)
                 project_phase(xsets[b])
                 accumulate_phase(m, dsets[b])
                 consumed[b].record(stream)
@@ -711,8 +714,8 @@ def main():
         e2e = {"value": run.tokens_per_step * e2e_steps * world / e2e_elapsed, "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "h2d_gbs": h2d * e2e_steps / e2e_elapsed / 1e9,
-               "copies": "own stream, two device sets alternating: microbatch m+1's copies overlap "
-                         "microbatch m's kernels"}
+               "copies": "four copy streams, two device sets alternating: microbatch m+1's copies "
+                         "overlap microbatch m's kernels"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

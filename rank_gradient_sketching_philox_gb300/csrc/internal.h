@@ -164,12 +164,13 @@ struct UpdateWorkspace {
   double* wnew_partials;   // one per update block
   uint16_t* c_split;       // d x (2 r_pad) BF16: [high | low] part of C
   uint16_t* p_split;       // k x (2 r_pad) BF16: [high | low] part of P
-  // exact-path queue: the elements the update kernel hands to the fix kernel
-  uint32_t* fix_count;     // entries appended (may exceed fix_cap: the rest were redone in place)
-  uint32_t* fix_ticket;    // last-block counter of the fix kernel
+  // exact-path queue: the elements the update kernel hands to the fix kernel,
+  // a few fixed slots per (tile, epilogue warp)
+  uint8_t* fix_counts;     // slots used per (tile, warp)
+  uint16_t* fix_tags;      // per slot: flagged elements, lane and group of the entry
+  uint4* fix_entries;      // per slot: the group's original weights
+  uint32_t* fix_ticket;    // bit 31: a non-finite change; the fix kernel's block counter
   unsigned long long* fix_acc;  // fixed-point sum of the exact path's changes of ||W_new||^2
-  uint4* fix_entries;      // fix_cap entries: (i, j, w | rand16 << 16, tensor-core result)
-  uint32_t fix_cap;
 };
 constexpr int kWnormBlocks = 1024;
 // Carves one layer's workspace at the cursor; returns its size (a multiple of 256).

@@ -127,8 +127,7 @@ struct SplitBatch {
   int r;
   int r_pad;
   int parts;  // 2 or 3 BF16 parts per value
-  // each layer's exact-path queue counters, reset here before the update
-  uint32_t* fix_count[kMaxAux];
+  // each layer's exact-path counters, reset here before the update
   uint32_t* fix_ticket[kMaxAux];
   unsigned long long* fix_acc[kMaxAux];
 };
@@ -143,7 +142,6 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__
   constexpr int kU = 4;
   if (blockIdx.x == 0) {
     for (int t = threadIdx.x; t < b.n / 2; t += blockDim.x) {
-      *b.fix_count[t] = 0u;
       *b.fix_ticket[t] = 0u;
       *b.fix_acc[t] = 0ull;
     }
@@ -257,7 +255,7 @@ struct UpdBatch {
   int p_stages;       // P ring depth
   int w_stages;       // W ring depth
   float scale_val;
-  float err_coef;     // 2^25 (beta + 2^-24): the margin bound is err_coef |s| ||c_i|| max_j ||p_j||
+  float err_coef;     // 2^41 (beta + 2^-24): the margin bound is err_coef |s| ||c_i|| max_j ||p_j||
   uint32_t rk0[10], rk1[10];  // Philox round keys of the seed
   uint32_t step;
   int r;
@@ -269,9 +267,9 @@ struct UpdBatch {
   uint32_t w_bytes;   // bytes of the W tile: NCOLS/64 x 16 KB
   int* err;
   unsigned long long* exact_count;  // elements recomputed exactly (instrumentation)
-  uint4* fix_entries[kMaxUpd];      // exact-path queue of each layer (see FixBatch)
-  uint32_t* fix_count[kMaxUpd];
-  uint32_t fix_cap[kMaxUpd];
+  uint4* fix_entries[kMaxUpd];      // exact-path queue of each layer: kFixSlots per (tile, warp)
+  uint16_t* fix_tags[kMaxUpd];
+  uint8_t* fix_counts[kMaxUpd];
 };
 
 // kernel parameters are limited to 32764 bytes
@@ -315,20 +313,58 @@ __device__ __forceinline__ Unit decode_unit(const UpdBatch& a, int u) {
   return x;
 }
 
-// Rounding margin of one element, in units of the error bound.  S = bits(v) +
-// rand16 is the stochastic-rounding sum (the result is S >> 16); L = S mod
-// 2^16 lies min(L, 2^16 - L) fp32 steps of v from the nearest sum that would
-// round the other way.  A value v' within D of v is at most 2D / ulp(v) + 2
-// fp32 steps from v (the step halves below a power of two; both values are
-// rounded once), and ulp(v) > |v| 2^-24, so v' rounds like v whenever
-// (min(L, 2^16 - L) - 3) |v| >= 2^25 D.  Returns the left side (less a
-// little more, for the rounding of this product): negative when the margin
-// is three steps or less, NaN when v is NaN, and NaN for an infinite v.
-__device__ __forceinline__ float rounding_margin(uint32_t S, float v) {
-  const float mg = __uint_as_float(__byte_perm(S, 0x4B000000u, 0x7610));  // 2^23 + (S mod 2^16)
-  const float x = mg - 8421376.0f;                                        // (S mod 2^16) - 2^15, exact
-  const float av = fabsf(v);
-  return fmaf(-fabsf(x), av, 32764.0f * av);  // (min(L, 2^16 - L) - 4) |v|, rounded
+// Packed pairs of fp32 operations (one instruction for two lanes of work;
+// each half rounds exactly like the scalar operation).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// Rounding margins of a pair of elements.  S = bits(v) + rand16 is the
+// stochastic-rounding sum (the result is S >> 16); L = S mod 2^16 lies
+// min(L, 2^16 - L) fp32 steps of v from the nearest sum that would round the
+// other way.  A value v' within D of v is at most 2D / ulp(v) + 2 fp32 steps
+// from v (the step halves below a power of two; both values are rounded once),
+// and ulp(v) > |v| 2^-24, so v' rounds like v whenever
+// (min(L, 2^16 - L) - 3) |v| >= 2^25 D.  With x = L - 2^15 and
+// K = 2^30 - 2^18, K - x^2 = (2^15 - |x|)(2^15 + |x|) - 2^18 is at most
+// 2^16 (2^15 - 4 - |x|), so v' rounds like v when x^2 <= K and
+// (K - x^2) |v| >= 2^41 D (the spare step covers the two roundings here).
+// Sets zn = x^2 - K (positive when the margin is four steps or less) and
+// y = zn v, whose magnitude is the left side when zn <= 0; y is NaN when v is.
+// Two packed operations and one of each of these per element.
+__device__ __forceinline__ void rounding_margins(uint32_t s0, uint32_t s1, float2 v, float2& zn, float2& y) {
+  const float2 mg = make_float2(__uint_as_float(__byte_perm(s0, 0x4B000000u, 0x7610)),   // 2^23 + L
+                                __uint_as_float(__byte_perm(s1, 0x4B000000u, 0x7610)));
+  const float2 x = fadd2(mg, make_float2(-8421376.0f, -8421376.0f));  // L - 2^15, exact
+  zn = ffma2(x, x, make_float2(-1073479680.0f, -1073479680.0f));      // x^2 - (2^30 - 2^18)
+  y = fmul2(zn, v);
+}
+
+// Flag of one element from its rounding_margins outputs and the scaled bound
+// 2^41 D (true: the tensor-core result might differ from the definition's).
+__device__ __forceinline__ bool margin_flag(float zn, float y, float bound) {
+  return !(fabsf(y) >= bound) || zn > 0.f;
 }
 
 template <int N>
@@ -339,6 +375,43 @@ __device__ __forceinline__ uint32_t pick(const uint32_t (&v)[N], int i) {
   return r;
 }
 
+// Exact-path queue layout: each (tile, epilogue warp) owns kFixSlots entries
+// of its layer's queue and a one-byte count.  An entry is one lane's 8-column
+// group that holds at least one element whose margin the bound might cross: the
+// group's original weights (16 bytes, fix_entries) and a 16-bit tag (fix_meta:
+// the flagged elements as bits 0..7, the lane at bits 8..12, the group at bits
+// 13..14).  A trained-scale tile has about one such group per warp; a group
+// that finds the slots full is redone in place after the warp's last group of
+// the tile.  Fixed slots make the split between queued and in-place groups the
+// same on every call.
+constexpr uint32_t kFixSlots = 4;
+
+// H_ij as a compensated dot product of c (row i of C) and p (row j of P), r
+// terms, by the whole warp: lane l takes terms l, l + 32, ... into a running
+// TwoSum pair, and the lanes' pairs are merged by TwoSum over a butterfly.
+// Every lane returns the same value, fl32 of the exact sum except within about
+// 2^-40 of a rounding boundary (Dot2: as accurate as twice fp32 precision).
+__device__ __forceinline__ float warp_dot2(const float* c, const float* p, int r, int lane) {
+  float hs = 0.f, he = 0.f;
+  for (int l = lane; l < r; l += 32) {
+    const float cv = c[l], pv = p[l];
+    const float m = __fmul_rn(cv, pv);
+    float sum, err;
+    two_sum(hs, m, sum, err);
+    hs = sum;
+    he = __fadd_rn(he, __fadd_rn(err, __fmaf_rn(cv, pv, -m)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ohs = __shfl_xor_sync(0xFFFFFFFFu, hs, o), ohe = __shfl_xor_sync(0xFFFFFFFFu, he, o);
+    float sum, err;
+    two_sum(hs, ohs, sum, err);
+    hs = sum;
+    he = __fadd_rn(he, __fadd_rn(ohe, err));
+  }
+  return __fadd_rn(hs, he);
+}
+
 // The exact path, in place: the warp takes the elements of emask (bit t:
 // column jg + t of the calling lane's row) one at a time, H_ij as a
 // compensated dot product of the fp32 row i of C and row j of P, its terms
@@ -347,10 +420,11 @@ __device__ __forceinline__ uint32_t pick(const uint32_t (&v)[N], int i) {
 // writes the result into its W stage over the tensor-core result.  wv, rv, ov
 // are the lane's original weights, Philox words and tensor-core results of the
 // group; returns the change of the lane's sum of squares.
-__device__ float exact_in_place(uint32_t emask, const uint32_t (&wv)[4], const uint32_t (&rv)[4],
-                                const uint32_t (&ov)[4], const float* C, const float* P, int r, int row0, int jg,
-                                float s, uint32_t sp, unsigned& n_done) {
+__device__ __forceinline__ float exact_in_place(uint32_t emask, uint4 w4, uint4 r4, uint4 o4, const float* C,
+                                             const float* P, int r, int row0, int jg, float s, uint32_t sp,
+                                             unsigned& n_done) {
   const int lane = threadIdx.x & 31;
+  const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w}, ov[4] = {o4.x, o4.y, o4.z, o4.w};
   float dsq = 0.f;
   uint32_t pending = __ballot_sync(0xFFFFFFFFu, emask != 0);
   while (pending) {
@@ -363,26 +437,7 @@ __device__ float exact_in_place(uint32_t emask, const uint32_t (&wv)[4], const u
     const uint32_t oo = __shfl_sync(0xFFFFFFFFu, pick(ov, e >> 1), src);
     const int sh = (e & 1) * 16;
     const uint32_t w16 = (ww >> sh) & 0xFFFFu, r16 = (rr >> sh) & 0xFFFFu, o16 = (oo >> sh) & 0xFFFFu;
-    const float* crow = C + (int64_t)(row0 + src) * r;
-    const float* prow = P + (int64_t)(jg + e) * r;
-    float hs = 0.f, he = 0.f;
-    for (int l = lane; l < r; l += 32) {
-      const float cv = crow[l], pv = prow[l];
-      const float m = __fmul_rn(cv, pv);
-      float sum, err;
-      two_sum(hs, m, sum, err);
-      hs = sum;
-      he = __fadd_rn(he, __fadd_rn(err, __fmaf_rn(cv, pv, -m)));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ohs = __shfl_xor_sync(0xFFFFFFFFu, hs, o), ohe = __shfl_xor_sync(0xFFFFFFFFu, he, o);
-      float sum, err;
-      two_sum(hs, ohs, sum, err);
-      hs = sum;
-      he = __fadd_rn(he, __fadd_rn(ohe, err));
-    }
-    const float hx = __fadd_rn(hs, he);
+    const float hx = warp_dot2(C + (int64_t)(row0 + src) * r, P + (int64_t)(jg + e) * r, r, lane);
     const float v = fmaf(-s, hx, __uint_as_float(w16 << 16));
     const uint32_t out = sr_bf16_bits(v, r16);
     if (lane == src) {
@@ -396,63 +451,65 @@ __device__ float exact_in_place(uint32_t emask, const uint32_t (&wv)[4], const u
   return dsq;
 }
 
-// The exact path for the elements of one 8-column group of a warp (the calling
-// lane's row, columns jg..jg+7) whose rounding margin the error bound might
-// cross; flag says that the lane's group holds at least one, and h03, h47 are
-// its tensor-core H values, so that each element's margin is checked again.
-// The flagged elements are appended to the layer's exact-path queue, which the
-// fix kernel redoes once every tile of the launch is stored; those that find
-// the queue full are redone here in place (exact_in_place).  Returns the change
-// of the lane's sum of squares from the in-place ones.  Kept out of line: it
-// runs rarely, and its registers would otherwise crowd the main loop.
-__device__ __noinline__ float exact_path(bool flag, float bound, uint4 win, uint4 rwd, uint4 wout, uint4 h03,
-                                         uint4 h47, uint4* queue, uint32_t* queue_count, uint32_t queue_cap,
-                                         const float* C, const float* P, int r, int row0, int jg, int k, float s,
-                                         uint32_t sp, unsigned& n_done) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t wv[4] = {win.x, win.y, win.z, win.w}, rv[4] = {rwd.x, rwd.y, rwd.z, rwd.w},
-                 ov[4] = {wout.x, wout.y, wout.z, wout.w};
-  const uint32_t hv[8] = {h03.x, h03.y, h03.z, h03.w, h47.x, h47.y, h47.z, h47.w};
-  // the flagged lane's elements whose own margin the bound might cross
-  uint32_t emask = 0;
-  if (flag) {
+// Byte offset in a W stage (NCOLS/64 boxes of 64 columns, 128-byte swizzled)
+// of the 8-column group of tile row q that starts at column col.
+__device__ __forceinline__ uint32_t w_stage_offset(int col, int q) {
+  return (uint32_t)((col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
+}
+
+// Groups that found their warp's queue slots full, redone in place once the
+// warp has finished the tile (the TMEM buffer is still its own): bit g of redo
+// is this lane's 8-column group g, whose original weights are back in the
+// stage.  For each such group the tensor-core results are formed again from H
+// in TMEM, exactly as in the main loop, written to the stage, and the elements
+// the margin test flags go through exact_in_place.  Returns the lane's sum of
+// squares of the redone groups.
+__device__ __forceinline__ float redo_in_place(const UpdBatch& a, uint32_t redo, int ngroups, uint32_t taddr,
+                                            uint32_t s_w32, int col_base, int q, int i, int j0, int k, uint32_t k8,
+                                            uint32_t layer, const float* C, const float* P, float s, float bound,
+                                            int row0, bool need_norm, unsigned& n_done) {
+  float sq = 0.f;
+  for (int g = 0; g < ngroups; ++g) {
+    const bool mine = (redo >> g) & 1u;
+    if (!__any_sync(0xFFFFFFFFu, mine)) continue;
+    const int col = col_base + 8 * g;
+    const uint32_t sp = s_w32 + w_stage_offset(col, q);
+    uint32_t h[8];
+    tc::tmem_ld_32x32b_x8(taddr + 8 * g, h);
+    tc::tmem_wait_ld_regs<8>(h);
+    uint32_t emask = 0;
+    uint4 w4 = make_uint4(0, 0, 0, 0), r4 = w4, o4 = w4;
+    if (mine) {
+      w4 = tc::lds128(sp);
+      const uint32_t blk[1] = {(uint32_t)i * k8 + ((uint32_t)(j0 + col) >> 3)};
+      uint32_t rw[1][4];
+      philox4x32_10_rk_multi<1>(blk, a.step, layer, kTagSR, a.rk0, a.rk1, rw);
+      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+      uint32_t out[4];
+      float t = 0.f;
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const uint32_t wt = (t & 1) ? (wv[t >> 1] & 0xFFFF0000u) : (wv[t >> 1] << 16);
-      const uint32_t rt = (t & 1) ? (rv[t >> 1] >> 16) : (rv[t >> 1] & 0xFFFFu);
-      const float vt = fmaf(-s, __uint_as_float(hv[t]), __uint_as_float(wt));
-      const float mt = rounding_margin(__float_as_uint(vt) + rt, vt);
-      emask |= (!(mt >= bound) ? 1u : 0u) << t;
+      for (int t2 = 0; t2 < 4; ++t2) {
+        const float2 v = ffma2(make_float2(-s, -s), make_float2(__uint_as_float(h[2 * t2]), __uint_as_float(h[2 * t2 + 1])),
+                               make_float2(__uint_as_float(wv[t2] << 16), __uint_as_float(wv[t2] & 0xFFFF0000u)));
+        const uint32_t s0 = __float_as_uint(v.x) + (rw[0][t2] & 0xFFFFu);
+        const uint32_t s1 = __float_as_uint(v.y) + (rw[0][t2] >> 16);
+        out[t2] = __byte_perm(s0, s1, 0x7632);
+        float2 zn, y;
+        rounding_margins(s0, s1, v, zn, y);
+        if (margin_flag(zn.x, y.x, bound)) emask |= 1u << (2 * t2);
+        if (margin_flag(zn.y, y.y, bound)) emask |= 2u << (2 * t2);
+        if (need_norm) t = sq_acc_bf16x2(out[t2], t);
+      }
+      if (j0 + col + 8 > k) emask &= (1u << (k - j0 - col)) - 1u;
+      tc::sts128(sp, make_uint4(out[0], out[1], out[2], out[3]));
+      r4 = make_uint4(rw[0][0], rw[0][1], rw[0][2], rw[0][3]);
+      o4 = make_uint4(out[0], out[1], out[2], out[3]);
+      sq += t;
     }
-    if (jg + 8 > k) emask &= (1u << (k - jg)) - 1u;  // columns inside W
+    const float dsq = exact_in_place(emask, w4, r4, o4, C, P, a.r, row0, j0 + col, s, sp, n_done);
+    if (need_norm) sq += dsq;
   }
-  // one atomic per warp: the lanes' entries go to consecutive queue slots
-  const uint32_t cnt = __popc(emask);
-  uint32_t incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-  uint32_t base = 0;
-  if (lane == 31 && total != 0) base = atomicAdd(queue_count, total);
-  base = __shfl_sync(0xFFFFFFFFu, base, 31);
-  uint32_t pos = base + incl - cnt, over = 0;
-  const int row = row0 + lane;
-  for (uint32_t m = emask; m; m &= m - 1u) {
-    const int e = __ffs(m) - 1;
-    if (pos < queue_cap) {
-      const int sh = (e & 1) * 16;
-      const uint32_t w16 = (wv[e >> 1] >> sh) & 0xFFFFu, r16 = (rv[e >> 1] >> sh) & 0xFFFFu;
-      const uint32_t o16 = (ov[e >> 1] >> sh) & 0xFFFFu;
-      queue[pos] = make_uint4((uint32_t)row, (uint32_t)(jg + e), w16 | (r16 << 16), o16);
-    } else {
-      over |= 1u << e;
-    }
-    ++pos;
-  }
-  return exact_in_place(over, wv, rv, ov, C, P, r, row0, jg, s, sp, n_done);
+  return sq;
 }
 
 // Persistent rebuild + update, one CTA per SM, each CTA a contiguous range of
@@ -473,12 +530,15 @@ __device__ __noinline__ float exact_path(bool flag, float bound, uint4 win, uint
 // fp32 rounding of the exact product.  The tensor-core H differs from it by at
 // most D = |s| (beta ||c_i|| ||p_j|| + 2^-24 |H|) with beta the split and
 // accumulation error of the part products.  Each element's rounding margin
-// (rounding_margin) is compared with that bound: an element whose margin
-// might be crossed is recomputed at once by its warp, H_ij from a compensated
-// dot product of the fp32 row of C and the fp32 row of P (Dot2 of the paper
-// above: as accurate as twice fp32 precision), and its result replaces the
-// tensor-core one in the stage before the tile is stored.  Every other
-// element's result is the one the definition gives.
+// (rounding_margins) is compared with that bound.  A lane's 8-column group
+// with an element whose margin might be crossed is queued, with its original
+// weights, in the warp's slots of the tile; exact_fix_kernel then recomputes
+// those elements, H_ij from a compensated dot product of the fp32 row of C and
+// the fp32 row of P (Dot2 of the paper above: as accurate as twice fp32
+// precision), and writes their results over the tensor-core ones.  A group
+// that finds the slots full is redone in place before the tile is stored
+// (redo_in_place).  Every other element's result is the one the definition
+// gives.
 template <int NCOLS>
 __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const __grid_constant__ UpdBatch a) {
   extern __shared__ uint8_t smem_raw[];
@@ -684,8 +744,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     uint32_t stage_off[kGroups];
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
-      const int col = col_base + 8 * g;
-      stage_off[g] = (uint32_t)((col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
+      stage_off[g] = w_stage_offset(col_base + 8 * g, q);
     }
     unsigned exact_n = 0;  // elements this lane recomputed exactly
     int it = 0;
@@ -700,6 +759,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       const bool row_ok = i < d;
       const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
       const float bound_row = row_ok ? a.err_coef * fabsf(s) * a.c_norm[p][i] : 0.f;
+      const float2 ns2 = make_float2(-s, -s);
       const uint32_t layer = a.layer[p];
       const bool need_norm = a.wnorm2_out[p] != nullptr;
       float sq = 0.f, sq_comp = 0.f;  // Kahan-compensated sum of squares
@@ -720,8 +780,15 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         tc::tc_fence_after();
         const uint32_t s_w32 = tc::smem_u32(s_w0) + (uint32_t)sw * a.w_bytes;
         for (int o = 16; o > 0; o >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
-        const float bound = bound_row * pmax;  // 2^25 D for every element of this thread's row
+        const float bound = bound_row * pmax;  // 2^41 D for every element of this thread's row
         // live is the same in the whole warp: one branch per tile
+        // this warp's slice of the layer's exact-path queue for this tile
+        const uint32_t tile = (uint32_t)x.rb * (uint32_t)a.n_ct[p] + (uint32_t)ct;
+        const size_t slot0 = ((size_t)tile * kEpiWarps + ew) * kFixSlots;
+        uint4* const slots = a.fix_entries[p] + slot0;
+        uint16_t* const tags = a.fix_tags[p] + slot0;
+        uint32_t used = 0;       // groups queued in the warp's slots (warp-uniform)
+        uint32_t redo_mask = 0;  // this lane's groups to redo in place
         if (live) {
           const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col_base);
           float gs = 0.f;  // sum of squares of this tile's results (normalized SGD)
@@ -747,54 +814,83 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
               const uint4 raw = tc::lds128(sp);
               const uint32_t win[4] = {raw.x, raw.y, raw.z, raw.w};
               uint32_t wout[4];
-              float ym[8];
-              // Per pair: v = fmaf(-s, H, w) and stochastic rounding (add 16
-              // random bits below the BF16 mantissa, keep the upper halves: one
-              // PRMT per pair); the results go back into the W stage in place
-              // (the store warp writes the tile out with TMA, clipping rows and
-              // columns outside W).  The integer steps use multiply-adds so that
-              // they share the multiplier pipe with Philox instead of crowding
-              // the ALU pipe: r_hi = r >> 16, r_lo = r - r_hi * 2^16 = r & 0xFFFF.
+              float ya[8], za[8];
+              // Per pair: v = fmaf(-s, H, w) (one packed FMA) and stochastic
+              // rounding (add 16 random bits below the BF16 mantissa, keep the
+              // upper halves: one PRMT per pair); the results go back into the
+              // W stage in place (the store warp writes the tile out with TMA,
+              // clipping rows and columns outside W).  The integer steps use
+              // multiply-adds so that they share the multiplier pipe with
+              // Philox instead of crowding the ALU pipe: r_hi = r >> 16,
+              // r_lo = r - r_hi * 2^16 = r & 0xFFFF.
 #pragma unroll
               for (int t2 = 0; t2 < 4; ++t2) {
                 const uint32_t wword = win[t2], rword = rw[gg][t2];
-                const float v0 = fmaf(-s, __uint_as_float(h[8 * gg + 2 * t2]),
-                                      __uint_as_float(mad_lo(wword, 0x10000u, 0u)));
-                const float v1 = fmaf(-s, __uint_as_float(h[8 * gg + 2 * t2 + 1]),
-                                      __uint_as_float(wword & 0xFFFF0000u));
+                const float2 v = ffma2(ns2,
+                                       make_float2(__uint_as_float(h[8 * gg + 2 * t2]),
+                                                   __uint_as_float(h[8 * gg + 2 * t2 + 1])),
+                                       make_float2(__uint_as_float(mad_lo(wword, 0x10000u, 0u)),
+                                                   __uint_as_float(wword & 0xFFFF0000u)));
                 const uint32_t r_hi = mad_hi(rword, 0x10000u, 0u);
                 const uint32_t r_lo = mad_lo(r_hi, 0xFFFF0000u, rword);
-                const uint32_t s0 = mad_lo(r_lo, 1u, __float_as_uint(v0));
-                const uint32_t s1 = mad_hi(rword, 0x10000u, __float_as_uint(v1));
+                const uint32_t s0 = mad_lo(r_lo, 1u, __float_as_uint(v.x));
+                const uint32_t s1 = mad_hi(rword, 0x10000u, __float_as_uint(v.y));
                 wout[t2] = __byte_perm(s0, s1, 0x7632);
-                ym[2 * t2] = rounding_margin(s0, v0);
-                ym[2 * t2 + 1] = rounding_margin(s1, v1);
+                float2 zn, y;
+                rounding_margins(s0, s1, v, zn, y);
+                ya[2 * t2] = y.x;
+                ya[2 * t2 + 1] = y.y;
+                za[2 * t2] = zn.x;
+                za[2 * t2 + 1] = zn.y;
               }
-              // smallest margin of the group; NaN if any is NaN
-              const float gm = fmin3_nan(fmin3_nan(ym[0], ym[1], ym[2]), fmin3_nan(ym[3], ym[4], ym[5]),
-                                         fmin_nan(ym[6], ym[7]));
+              // smallest margin of the group (NaN if any is NaN) and whether
+              // any element lies four steps or less from a rounding boundary
+              const float gm = fmin3_nan(fmin3_nan(fabsf(ya[0]), fabsf(ya[1]), fabsf(ya[2])),
+                                         fmin3_nan(fabsf(ya[3]), fabsf(ya[4]), fabsf(ya[5])),
+                                         fmin_nan(fabsf(ya[6]), fabsf(ya[7])));
+              const float zmax = fmax3(fmax3(za[0], za[1], za[2]), fmax3(za[3], za[4], za[5]), fmaxf(za[6], za[7]));
               const bool ok = row_ok && j0 + col < k;
-              const bool flag = ok && !(gm >= bound);
+              const bool flag = ok && (!(gm >= bound) || zmax > 0.f);
               tc::sts128(sp, make_uint4(wout[0], wout[1], wout[2], wout[3]));
+              float t = gs;
               if (need_norm) {
-                float t = gs;
 #pragma unroll
                 for (int t2 = 0; t2 < 4; ++t2) t = sq_acc_bf16x2(wout[t2], t);
-                gs = ok ? t : gs;
               }
-              // Rare: elements whose margin the error bound might cross.  The
-              // whole warp recomputes them one at a time, each H_ij by a
-              // compensated dot product over r spread across the lanes.
+              // Rare: a group with an element whose margin the bound might
+              // cross.  Its lane queues the group (original weights and the
+              // flagged elements) in this warp's slots for the fix kernel, or,
+              // with the slots full, puts the original weights back into the
+              // stage and redoes the group after the tile's last group.
+              bool redo = false;
               if (__any_sync(0xFFFFFFFFu, flag)) {
-                gs += exact_path(flag, bound, raw, make_uint4(rw[gg][0], rw[gg][1], rw[gg][2], rw[gg][3]),
-                                 make_uint4(wout[0], wout[1], wout[2], wout[3]),
-                                 make_uint4(h[8 * gg], h[8 * gg + 1], h[8 * gg + 2], h[8 * gg + 3]),
-                                 make_uint4(h[8 * gg + 4], h[8 * gg + 5], h[8 * gg + 6], h[8 * gg + 7]),
-                                 a.fix_entries[p], a.fix_count[p], a.fix_cap[p], a.C[p], a.P[p], a.r,
-                                 x.rb * 128 + quarter * 32, j0 + col, k, s, sp, exact_n);
+                uint32_t emask = 0;
+                if (flag) {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) emask |= margin_flag(za[e], ya[e], bound) ? (1u << e) : 0u;
+                  if (j0 + col + 8 > k) emask &= (1u << (k - j0 - col)) - 1u;  // columns inside W
+                }
+                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, emask != 0);
+                const uint32_t pos = used + __popc(bal & ((1u << lane) - 1u));
+                if (emask != 0) {
+                  if (pos < kFixSlots) {
+                    slots[pos] = raw;
+                    tags[pos] = (uint16_t)(emask | ((uint32_t)lane << 8) | ((uint32_t)g << 13));
+                  } else {
+                    tc::sts128(sp, raw);
+                    redo_mask |= 1u << g;
+                    redo = true;
+                  }
+                }
+                used += __popc(bal);
               }
+              if (ok && !redo) gs = t;
             }
           }
+          // groups that found the slots full
+          if (__any_sync(0xFFFFFFFFu, redo_mask != 0))
+            gs += redo_in_place(a, redo_mask, kGroups, taddr, s_w32, col_base, q, i, j0, k, k8, layer, a.C[p],
+                                a.P[p], s, bound, x.rb * 128 + quarter * 32, need_norm, exact_n);
           if (need_norm) {  // the tile's squares into the compensated sum
             const float y = gs - sq_comp;
             const float tsum = sq + y;
@@ -802,6 +898,8 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
             sq = tsum;
           }
         }
+        // the slots this warp filled (every count is written on every call)
+        if (lane == 0) a.fix_counts[p][(size_t)tile * kEpiWarps + ew] = (uint8_t)(used < kFixSlots ? used : kFixSlots);
         // this warp is done with the TMEM buffer
         tc::tc_fence_before();
         __syncwarp();
@@ -888,7 +986,7 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   const int parts = update_parts(r);
   a.scale_val = scale_val;
   a.parts = parts;
-  a.err_coef = 0x1p25f * (tc_err_beta(r) + 0x1p-24f);
+  a.err_coef = 0x1p41f * (tc_err_beta(r) + 0x1p-24f);
   philox_round_keys(seed, a.rk0, a.rk1);
   a.step = step;
   a.r = r;
@@ -960,8 +1058,8 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       a.ticket[i] = w.ticket;
       a.wnorm2_out[i] = normsgd ? pr.wnorm2_out : nullptr;
       a.fix_entries[i] = w.fix_entries;
-      a.fix_count[i] = w.fix_count;
-      a.fix_cap[i] = w.fix_cap;
+      a.fix_tags[i] = w.fix_tags;
+      a.fix_counts[i] = w.fix_counts;
     }
     const int units = a.unit_begin[m];
     int grid = units < nsm ? units : nsm;
@@ -997,146 +1095,192 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
 }
 
 // ---- the exact path's queue ---------------------------------------------------
-// The update kernel leaves each element whose rounding margin its tensor-core
-// H might cross in its layer's queue (row, column, original weight, 16 random
-// bits, tensor-core result) and stores the tensor-core result.  Once every
-// tile is stored, this kernel redoes each queued element the way the
-// definition does: H_ij as a compensated dot product (Dot2) of the fp32 row i
-// of C and row j of P, v = fmaf(-s, fl32(H_ij), w), the same stochastic
+// The update kernel queues each 8-column group holding an element whose
+// rounding margin its tensor-core H might cross (the group's original weights,
+// the flagged elements and their position) and stores the tensor-core results.
+// Once every tile is stored, exact_fix_kernel redoes each flagged element the
+// way the definition does: H_ij as a compensated dot product (Dot2) of the fp32
+// row i of C and row j of P, v = fmaf(-s, fl32(H_ij), w), the same stochastic
 // rounding, and writes the weight.  For normalized SGD it also carries the
 // change of ||W_new||^2: each element's change (new^2 - old^2, exact in
-// double) in fixed point relative to the layer's norm, summed as integers so
-// that the total does not depend on the order of the queue, and the layer's
-// last block adds it to the norm.
+// double) in fixed point relative to its layer's norm, summed as integers so
+// that the total does not depend on the order of the queue;
+// exact_fix_finalize_kernel adds each layer's total to its norm.
 struct FixBatch {
   const uint4* entries[kMaxUpd];
-  const uint32_t* count[kMaxUpd];
-  uint32_t cap[kMaxUpd];
-  uint32_t* ticket[kMaxUpd];
+  const uint16_t* tags[kMaxUpd];
+  const uint8_t* counts[kMaxUpd];
+  uint32_t* ticket[kMaxUpd];           // bit 31: a non-finite change
   unsigned long long* acc[kMaxUpd];
   const float* C[kMaxUpd];
   const float* P[kMaxUpd];
   uint16_t* W[kMaxUpd];
   int64_t ld_w[kMaxUpd];
+  int64_t d[kMaxUpd], k[kMaxUpd];
+  int n_ct[kMaxUpd];                   // column tiles of the layer
+  int tiles[kMaxUpd];
   const float* scale_dev[kMaxUpd];     // normalized SGD: s on the device; NULL: scale_val
   const int32_t* status_in[kMaxUpd];   // layer skipped when nonzero
   double* wnorm2_out[kMaxUpd];
+  uint32_t layer[kMaxUpd];
   int n;
   int r;
+  int ncols;                           // NCOLS of the update launch
   float scale_val;
+  uint32_t rk0[10], rk1[10];           // Philox round keys of the seed
+  uint32_t step;
   unsigned long long* exact_count;
 };
-constexpr int kFixBlocks = 16;  // blocks per layer (grid.x)
 constexpr int kFixFracBits = 40;  // fixed point: 2^-40 of the layer's norm
+constexpr int kFixThreads = 256;
 
-__global__ void __launch_bounds__(256) exact_fix_kernel(const __grid_constant__ FixBatch b) {
-  __shared__ long long red[8];
-  __shared__ int red_bad[8];
+// Fixed-point scale of a layer's changes: ref (the tensor-core ||W_new||^2)
+// is at least every tensor-core square and an exact result is within a step
+// or two of its tensor-core one, so a change is at most ~1.1 ref, ~2^42 in
+// fixed point.  A zero norm (every tensor-core result zero) takes a plain
+// double sum instead.
+__device__ __forceinline__ double fix_to_fixed(double ref) {
+  return ref > 0.0 ? ldexp(1.0, kFixFracBits - ilogb(ref)) : 1.0;
+}
+
+// H_ij as a compensated dot product of c and p (r terms) by one thread: the
+// operands come in 32-term chunks, every load of a chunk issued before its
+// terms are summed (a TwoSum running pair), so an element waits on memory
+// r / 32 times rather than once per term.  fl32 of the exact sum except
+// within about 2^-40 of a rounding boundary.
+__device__ __forceinline__ float thread_dot2(const float* c, const float* p, int r) {
+  float hs = 0.f, he = 0.f;
+  auto term = [&](float cv, float pv) {
+    const float m = __fmul_rn(cv, pv);
+    float sum, err;
+    two_sum(hs, m, sum, err);
+    hs = sum;
+    he = __fadd_rn(he, __fadd_rn(err, __fmaf_rn(cv, pv, -m)));
+  };
+  if ((r & 3) == 0) {
+    for (int l0 = 0; l0 < r; l0 += 32) {
+      float4 cv[8], pv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const bool in = l0 + 4 * q < r;
+        cv[q] = in ? __ldg(reinterpret_cast<const float4*>(c + l0) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        pv[q] = in ? __ldg(reinterpret_cast<const float4*>(p + l0) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (l0 + 4 * q >= r) break;
+        term(cv[q].x, pv[q].x);
+        term(cv[q].y, pv[q].y);
+        term(cv[q].z, pv[q].z);
+        term(cv[q].w, pv[q].w);
+      }
+    }
+  } else {
+    for (int l = 0; l < r; ++l) term(__ldg(c + l), __ldg(p + l));
+  }
+  return __fadd_rn(hs, he);
+}
+
+// One thread per (tile, epilogue warp) slot set of a layer (blockIdx.y), the
+// whole queue in one wave of independent threads (most sets are empty): for
+// each entry, the group's Philox block again and, for each flagged element,
+// H_ij by thread_dot2, then the same v and stochastic rounding as the
+// tensor-core path, written over the tensor-core result in W.  The change of
+// ||W_new||^2 goes, in fixed point relative to the layer's norm, into an
+// integer sum whose total does not depend on the order of the queue;
+// exact_fix_finalize_kernel adds it to the norm.
+__global__ void __launch_bounds__(kFixThreads) exact_fix_kernel(const __grid_constant__ FixBatch b) {
+  __shared__ unsigned block_done;
   const int p = blockIdx.y;
-  if (b.status_in[p] != nullptr && *b.status_in[p] != 0) return;  // the update skipped the layer
-  const uint32_t n_e = min(*b.count[p], b.cap[p]);
-  const float s = b.scale_dev[p] ? *b.scale_dev[p] : b.scale_val;
-  double* wn = b.wnorm2_out[p];
-  const double ref = wn ? *wn : 0.0;
-  // ref >= every tensor-core square, and an element's exact result is within
-  // a step or two of its tensor-core one, so |change| <= ~1.1 ref and a
-  // change is at most ~2^42 in fixed point.  A non-finite norm stays as it
-  // is; a zero norm (every tensor-core result zero) takes a plain double sum.
-  if (wn != nullptr && !isfinite(ref)) wn = nullptr;
-  const bool fixed = ref > 0.0;
-  const double to_fixed = fixed ? ldexp(1.0, kFixFracBits - ilogb(ref)) : 1.0;
-  const int r = b.r;
-  const bool vec = (r & 3) == 0;
-  long long q = 0;
-  int bad = 0;
-  unsigned done = 0;
-  for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < n_e; e += gridDim.x * blockDim.x) {
-    const uint4 en = b.entries[p][e];
-    const int i = (int)en.x, j = (int)en.y;
-    const uint32_t w16 = en.z & 0xFFFFu, r16 = en.z >> 16, o16 = en.w & 0xFFFFu;
-    const float* crow = b.C[p] + (int64_t)i * r;
-    const float* prow = b.P[p] + (int64_t)j * r;
-    float hs = 0.f, he = 0.f;
-    auto term = [&](float cv, float pv) {
-      const float m = __fmul_rn(cv, pv);
-      float sum, err;
-      two_sum(hs, m, sum, err);
-      hs = sum;
-      he = __fadd_rn(he, __fadd_rn(err, __fmaf_rn(cv, pv, -m)));
-    };
-    if (vec) {
-      for (int l = 0; l < r; l += 4) {
-        const float4 c4 = *reinterpret_cast<const float4*>(crow + l);
-        const float4 p4 = *reinterpret_cast<const float4*>(prow + l);
-        term(c4.x, p4.x);
-        term(c4.y, p4.y);
-        term(c4.z, p4.z);
-        term(c4.w, p4.w);
-      }
-    } else {
-      for (int l = 0; l < r; ++l) term(crow[l], prow[l]);
-    }
-    const float hx = __fadd_rn(hs, he);
-    const float v = fmaf(-s, hx, __uint_as_float(w16 << 16));
-    const uint32_t out = sr_bf16_bits(v, r16);
-    b.W[p][(int64_t)i * b.ld_w[p] + j] = (uint16_t)out;
-    ++done;
-    if (wn != nullptr && out != o16) {
-      const double fo = (double)__uint_as_float(o16 << 16), fn = (double)__uint_as_float(out << 16);
-      const double delta = fn * fn - fo * fo;  // exact: both squares have 16-bit mantissas
-      if (!isfinite(delta)) bad = 1;
-      else if (fixed) q += llrint(delta * to_fixed);
-      else atomicAdd(reinterpret_cast<double*>(b.acc[p]), delta);
-    }
-  }
-  // the block's sums (integers: order-free), then one atomic per block
-  for (int o = 16; o > 0; o >>= 1) {
-    q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
-    bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, o);
-    done += __shfl_xor_sync(0xFFFFFFFFu, done, o);
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __shared__ unsigned red_done[8];
-  if (lane == 0) {
-    red[warp] = q;
-    red_bad[warp] = bad;
-    red_done[warp] = done;
-  }
+  if (threadIdx.x == 0) block_done = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    long long tq = 0;
-    int tb = 0;
-    unsigned td = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-      tq += red[w];
-      tb |= red_bad[w];
-      td += red_done[w];
-    }
-    if (td != 0 && b.exact_count != nullptr) atomicAdd(b.exact_count, (unsigned long long)td);
-    if (wn != nullptr) {
-      if (tq != 0) atomicAdd(b.acc[p], (unsigned long long)tq);
-      if (tb) atomicOr(reinterpret_cast<unsigned int*>(b.ticket[p]) + 0, 0x80000000u);
-      __threadfence();
-      const unsigned t = atomicAdd(b.ticket[p], 1u);
-      if ((t & 0x7FFFFFFFu) == gridDim.x - 1) {  // the layer's last block
-        __threadfence();
-        const unsigned tk = *((volatile unsigned*)b.ticket[p]);
-        const unsigned long long acc = *((volatile unsigned long long*)b.acc[p]);
-        const double add = fixed ? (double)(long long)acc / to_fixed : __longlong_as_double((long long)acc);
-        *wn = (tk & 0x80000000u) ? __longlong_as_double(0x7FF8000000000000ll) : ref + add;
+  const bool skipped = b.status_in[p] != nullptr && *b.status_in[p] != 0;
+  const int64_t sets = (int64_t)b.tiles[p] * kEpiWarps;
+  const int64_t set = (int64_t)blockIdx.x * kFixThreads + threadIdx.x;
+  const uint32_t cnt = (!skipped && set < sets) ? b.counts[p][set] : 0u;
+  unsigned done = 0;
+  if (cnt != 0) {
+    const int kcols = b.ncols / 4;
+    const float s = b.scale_dev[p] ? *b.scale_dev[p] : b.scale_val;
+    const int r = b.r;
+    const uint32_t k8 = (uint32_t)b.k[p] >> 3;
+    double* wn = b.wnorm2_out[p];
+    const int t = (int)(set / kEpiWarps), ew = (int)(set % kEpiWarps);
+    const int rb = t / b.n_ct[p], ct = t % b.n_ct[p];
+    for (uint32_t e_slot = 0; e_slot < cnt; ++e_slot) {
+      const size_t slot = (size_t)set * kFixSlots + e_slot;
+      const uint4 w4 = b.entries[p][slot];
+      const uint32_t tag = b.tags[p][slot];
+      const int i = rb * 128 + (ew & 3) * 32 + (int)((tag >> 8) & 31u);
+      const int jg = ct * b.ncols + (ew >> 2) * kcols + 8 * (int)(tag >> 13);
+      if (i >= b.d[p] || jg >= b.k[p]) break;  // only after a timed-out update
+      const uint32_t blk[1] = {(uint32_t)i * k8 + ((uint32_t)jg >> 3)};
+      uint32_t rw[1][4];
+      philox4x32_10_rk_multi<1>(blk, b.step, b.layer[p], kTagSR, b.rk0, b.rk1, rw);
+      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+      const float* crow = b.C[p] + (int64_t)i * r;
+      uint16_t* wrow = b.W[p] + (int64_t)i * b.ld_w[p];
+      for (uint32_t m = tag & 0xFFu; m; m &= m - 1u) {
+        const int e = __ffs(m) - 1;
+        const int j = jg + e;
+        const int sh = (e & 1) * 16;
+        const uint32_t w16 = (pick(wv, e >> 1) >> sh) & 0xFFFFu, r16 = (pick(rw[0], e >> 1) >> sh) & 0xFFFFu;
+        const float hx = thread_dot2(crow, b.P[p] + (int64_t)j * r, r);
+        const float v = fmaf(-s, hx, __uint_as_float(w16 << 16));
+        const uint32_t out = sr_bf16_bits(v, r16);
+        ++done;
+        if (wn == nullptr) {
+          wrow[j] = (uint16_t)out;
+          continue;
+        }
+        const uint32_t o16 = wrow[j];  // the tensor-core result
+        if (out == o16) continue;
+        wrow[j] = (uint16_t)out;
+        const double ref = *wn;
+        if (isfinite(ref)) {
+          const double fo = (double)__uint_as_float(o16 << 16), fn = (double)__uint_as_float(out << 16);
+          const double delta = fn * fn - fo * fo;  // exact: both squares have 16-bit mantissas
+          if (!isfinite(delta)) atomicOr(b.ticket[p], 0x80000000u);
+          else if (ref > 0.0) atomicAdd(b.acc[p], (unsigned long long)llrint(delta * fix_to_fixed(ref)));
+          else atomicAdd(reinterpret_cast<double*>(b.acc[p]), delta);
+        }
       }
     }
+  }
+  if (done != 0 && b.exact_count != nullptr) atomicAdd(&block_done, done);
+  __syncthreads();
+  if (threadIdx.x == 0 && block_done != 0 && b.exact_count != nullptr)
+    atomicAdd(b.exact_count, (unsigned long long)block_done);
+}
+
+// After exact_fix_kernel: each layer's fixed-point total of changes added to
+// its ||W_new||^2 (NaN when a change was not finite).
+__global__ void __launch_bounds__(256) exact_fix_finalize_kernel(const __grid_constant__ FixBatch b) {
+  for (int p = threadIdx.x; p < b.n; p += blockDim.x) {
+    double* wn = b.wnorm2_out[p];
+    if (wn == nullptr) continue;
+    if (b.status_in[p] != nullptr && *b.status_in[p] != 0) continue;  // the update skipped the layer
+    const double ref = *wn;
+    if (!isfinite(ref)) continue;
+    const unsigned long long acc = *b.acc[p];
+    const double add = ref > 0.0 ? (double)(long long)acc / fix_to_fixed(ref) : __longlong_as_double((long long)acc);
+    *wn = (*b.ticket[p] & 0x80000000u) ? __longlong_as_double(0x7FF8000000000000ll) : ref + add;
   }
 }
 
+// The fix kernel of the update launches of these problems (the same layers per
+// launch as launch_update_tc).
 cudaError_t launch_exact_fix(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, bool normsgd,
-                             float scale_val, cudaStream_t stream) {
+                             float scale_val, int ncols, uint64_t seed, uint32_t step, cudaStream_t stream) {
   unsigned long long* exact = nullptr;
   cudaError_t err = device_exact_counter(&exact);
   if (err != cudaSuccess) return err;
   static thread_local FixBatch f;
   f.r = r;
+  f.ncols = ncols;
   f.scale_val = scale_val;
+  philox_round_keys(seed, f.rk0, f.rk1);
+  f.step = step;
   f.exact_count = exact;
   for (int base = 0; base < n; base += kMaxUpd) {
     const int m = (n - base) < kMaxUpd ? (n - base) : kMaxUpd;
@@ -1145,22 +1289,35 @@ cudaError_t launch_exact_fix(int n, const UpdateProblem* probs, const UpdateWork
       const UpdateProblem& pr = probs[base + i];
       const UpdateWorkspace& w = ws[base + i];
       f.entries[i] = w.fix_entries;
-      f.count[i] = w.fix_count;
-      f.cap[i] = w.fix_cap;
+      f.tags[i] = w.fix_tags;
+      f.counts[i] = w.fix_counts;
+      f.layer[i] = pr.layer;
       f.ticket[i] = w.fix_ticket;
       f.acc[i] = w.fix_acc;
       f.C[i] = pr.C;
       f.P[i] = pr.P;
       f.W[i] = pr.W;
       f.ld_w[i] = pr.ld_w;
+      f.d[i] = pr.d;
+      f.k[i] = pr.k;
+      f.n_ct[i] = (int)ceil_div(pr.k, ncols);
+      f.tiles[i] = f.n_ct[i] * (int)ceil_div(pr.d, 128);
       f.scale_dev[i] = normsgd ? w.scale : nullptr;
       f.status_in[i] = normsgd ? (pr.dev_status ? pr.dev_status : w.status) : nullptr;
       f.wnorm2_out[i] = normsgd ? pr.wnorm2_out : nullptr;
     }
+    int64_t sets = 0;
+    for (int i = 0; i < m; ++i) sets = std::max(sets, (int64_t)f.tiles[i] * kEpiWarps);
     count_launch();
-    exact_fix_kernel<<<dim3(kFixBlocks, m), 256, 0, stream>>>(f);
+    exact_fix_kernel<<<dim3((unsigned)ceil_div(sets, kFixThreads), m), kFixThreads, 0, stream>>>(f);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    if (normsgd) {
+      count_launch();
+      exact_fix_finalize_kernel<<<1, 256, 0, stream>>>(f);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return err;
+    }
   }
   return cudaSuccess;
 }
@@ -1185,7 +1342,6 @@ cudaError_t launch_split(int n, const UpdateProblem* probs, const UpdateWorkspac
       sb.dst[2 * i + 1] = ws[base + i].p_split;
       sb.norm[2 * i + 1] = ws[base + i].p_norm;
       sb.row_begin[2 * i + 2] = sb.row_begin[2 * i + 1] + pr.k;
-      sb.fix_count[i] = ws[base + i].fix_count;
       sb.fix_ticket[i] = ws[base + i].fix_ticket;
       sb.fix_acc[i] = ws[base + i].fix_acc;
     }
@@ -1201,18 +1357,14 @@ cudaError_t launch_update(int n, const UpdateProblem* probs, const UpdateWorkspa
                           float scale_val, uint64_t seed, uint32_t step, cudaStream_t stream) {
   cudaError_t err = launch_split(n, probs, ws, r, stream);
   if (err != cudaSuccess) return err;
-  err = (update_ncols(r) == 128) ? launch_update_tc<128>(n, probs, ws, r, normsgd, scale_val, seed, step, stream)
-                                 : launch_update_tc<64>(n, probs, ws, r, normsgd, scale_val, seed, step, stream);
+  const int ncols = update_ncols(r);
+  err = (ncols == 128) ? launch_update_tc<128>(n, probs, ws, r, normsgd, scale_val, seed, step, stream)
+                       : launch_update_tc<64>(n, probs, ws, r, normsgd, scale_val, seed, step, stream);
   if (err != cudaSuccess) return err;
-  return launch_exact_fix(n, probs, ws, r, normsgd, scale_val, stream);
+  return launch_exact_fix(n, probs, ws, r, normsgd, scale_val, ncols, seed, step, stream);
 }
 
 }  // namespace
-
-// Entries of a layer's exact-path queue: one per 1024 weights plus 1024, about
-// twice what a trained-scale layer needs; elements beyond it are redone in
-// place by the update kernel itself.
-uint32_t fix_capacity(int64_t d, int64_t k) { return (uint32_t)(d * k / 1024 + 1024); }
 
 size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool normsgd, UpdateWorkspace* ws) {
   const size_t start = cur.offset;
@@ -1233,11 +1385,13 @@ size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool n
   w.p_norm = cur.take<float>((size_t)k);
   w.c_split = cur.take<uint16_t>((size_t)d * update_parts(r) * r_pad);
   w.p_split = cur.take<uint16_t>((size_t)k * update_parts(r) * r_pad);
-  w.fix_count = cur.take<uint32_t>(1);
+  // exact-path queue: kFixSlots entries and a count per (tile, epilogue warp)
+  const int64_t tiles = ceil_div(d, 128) * ceil_div(k, update_ncols(r));
   w.fix_ticket = cur.take<uint32_t>(1);
   w.fix_acc = cur.take<unsigned long long>(1);
-  w.fix_cap = fix_capacity(d, k);
-  w.fix_entries = cur.take<uint4>(w.fix_cap);
+  w.fix_counts = cur.take<uint8_t>((size_t)tiles * kEpiWarps);
+  w.fix_tags = cur.take<uint16_t>((size_t)tiles * kEpiWarps * kFixSlots);
+  w.fix_entries = cur.take<uint4>((size_t)tiles * kEpiWarps * kFixSlots);
   cur.take<char>(0);  // end on a 256-byte boundary
   if (ws) *ws = w;
   return cur.offset - start;
