@@ -203,6 +203,7 @@ __global__ void gram_reduce_kernel(const GramBatch batch) {
   const int src = a * r + b;
   const int nchunks = gram_chunks(en.rows).nchunks;
   float hi = 0.f, lo = 0.f;
+#pragma unroll 8
   for (int c = 0; c < nchunks; ++c) {
     const float2 v = en.partials[(size_t)c * rr + src];
     acc2(hi, lo, v.x);

@@ -46,10 +46,11 @@ struct GramChunks {
   int nchunks;
   int chunk_rows;
 };
-// Row chunks of a Gram: about 512 rows each (16 steps of 32 rows, enough to
-// amortise a block's start and its r x r partial), at most 64.
+// Row chunks of a Gram: about 128 rows each (four steps of 32 rows; a layer's
+// few thousand rows then occupy several blocks per SM, which the partial
+// kernel, latency-bound at one block per SM, needs), at most 64.
 __host__ __device__ inline GramChunks gram_chunks(int64_t rows) {
-  int64_t n = (rows + 511) / 512;
+  int64_t n = (rows + 127) / 128;
   if (n > 64) n = 64;
   if (n < 1) n = 1;
   GramChunks g;

@@ -1181,61 +1181,75 @@ __device__ __forceinline__ float thread_dot2(const float* c, const float* p, int
   return __fadd_rn(hs, he);
 }
 
-// One thread per (tile, epilogue warp) slot set of a layer (blockIdx.y), the
-// whole queue in one wave of independent threads (most sets are empty): for
-// each entry, the group's Philox block again and, for each flagged element,
-// H_ij by thread_dot2, then the same v and stochastic rounding as the
-// tensor-core path, written over the tensor-core result in W.  The change of
-// ||W_new||^2 goes, in fixed point relative to the layer's norm, into an
-// integer sum whose total does not depend on the order of the queue;
-// exact_fix_finalize_kernel adds it to the norm.
+// Each thread reads the count of one (tile, epilogue warp) slot set of a layer
+// (blockIdx.y); the warp lists the used slots of its 32 sets in shared memory
+// and deals them out one per lane, so that no lane works through a full set
+// while the others wait.  For each entry: the group's Philox block again and,
+// for each flagged element, H_ij by thread_dot2, then the same v and
+// stochastic rounding as the tensor-core path, written over the tensor-core
+// result in W.  The change of ||W_new||^2 goes, in fixed point relative to the
+// layer's norm, into an integer sum whose total does not depend on the order
+// of the queue; exact_fix_finalize_kernel adds it to the norm.
 __global__ void __launch_bounds__(kFixThreads) exact_fix_kernel(const __grid_constant__ FixBatch b) {
+  __shared__ uint32_t slots[kFixThreads / 32][32 * kFixSlots];
   __shared__ unsigned block_done;
   const int p = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) block_done = 0;
   __syncthreads();
   const bool skipped = b.status_in[p] != nullptr && *b.status_in[p] != 0;
   const int64_t sets = (int64_t)b.tiles[p] * kEpiWarps;
   const int64_t set = (int64_t)blockIdx.x * kFixThreads + threadIdx.x;
   const uint32_t cnt = (!skipped && set < sets) ? b.counts[p][set] : 0u;
+  // the warp's used slots, in lane order (slot index within the layer)
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  for (uint32_t q = 0; q < cnt; ++q) slots[warp][incl - cnt + q] = (uint32_t)set * kFixSlots + q;
+  __syncwarp();
   unsigned done = 0;
-  if (cnt != 0) {
+  if (total != 0) {
     const int kcols = b.ncols / 4;
     const float s = b.scale_dev[p] ? *b.scale_dev[p] : b.scale_val;
     const int r = b.r;
     const uint32_t k8 = (uint32_t)b.k[p] >> 3;
     double* wn = b.wnorm2_out[p];
-    const int t = (int)(set / kEpiWarps), ew = (int)(set % kEpiWarps);
-    const int rb = t / b.n_ct[p], ct = t % b.n_ct[p];
-    for (uint32_t e_slot = 0; e_slot < cnt; ++e_slot) {
-      const size_t slot = (size_t)set * kFixSlots + e_slot;
+    for (uint32_t idx = lane; idx < total; idx += 32) {
+      const uint32_t slot = slots[warp][idx];
       const uint4 w4 = b.entries[p][slot];
       const uint32_t tag = b.tags[p][slot];
+      const uint32_t sset = slot / kFixSlots;
+      const int t = (int)(sset / kEpiWarps), ew = (int)(sset % kEpiWarps);
+      const int rb = t / b.n_ct[p], ct = t % b.n_ct[p];
       const int i = rb * 128 + (ew & 3) * 32 + (int)((tag >> 8) & 31u);
       const int jg = ct * b.ncols + (ew >> 2) * kcols + 8 * (int)(tag >> 13);
-      if (i >= b.d[p] || jg >= b.k[p]) break;  // only after a timed-out update
+      if (i >= b.d[p] || jg >= b.k[p]) continue;  // only after a timed-out update
+      uint16_t* wrow = b.W[p] + (int64_t)i * b.ld_w[p];
+      // the group's tensor-core results, read before the dot products so that
+      // the load overlaps them (ld_w and jg are multiples of 8)
+      const uint4 o4 = *reinterpret_cast<const uint4*>(wrow + jg);
       const uint32_t blk[1] = {(uint32_t)i * k8 + ((uint32_t)jg >> 3)};
       uint32_t rw[1][4];
       philox4x32_10_rk_multi<1>(blk, b.step, b.layer[p], kTagSR, b.rk0, b.rk1, rw);
-      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w}, ov[4] = {o4.x, o4.y, o4.z, o4.w};
       const float* crow = b.C[p] + (int64_t)i * r;
-      uint16_t* wrow = b.W[p] + (int64_t)i * b.ld_w[p];
       for (uint32_t m = tag & 0xFFu; m; m &= m - 1u) {
         const int e = __ffs(m) - 1;
         const int j = jg + e;
         const int sh = (e & 1) * 16;
         const uint32_t w16 = (pick(wv, e >> 1) >> sh) & 0xFFFFu, r16 = (pick(rw[0], e >> 1) >> sh) & 0xFFFFu;
+        const uint32_t o16 = (pick(ov, e >> 1) >> sh) & 0xFFFFu;
         const float hx = thread_dot2(crow, b.P[p] + (int64_t)j * r, r);
         const float v = fmaf(-s, hx, __uint_as_float(w16 << 16));
         const uint32_t out = sr_bf16_bits(v, r16);
         ++done;
-        if (wn == nullptr) {
-          wrow[j] = (uint16_t)out;
-          continue;
-        }
-        const uint32_t o16 = wrow[j];  // the tensor-core result
         if (out == o16) continue;
         wrow[j] = (uint16_t)out;
+        if (wn == nullptr) continue;
         const double ref = *wn;
         if (isfinite(ref)) {
           const double fo = (double)__uint_as_float(o16 << 16), fn = (double)__uint_as_float(out << 16);
