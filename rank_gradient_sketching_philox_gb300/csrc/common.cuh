@@ -147,13 +147,6 @@ __device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
-// max of a, b and c (PTX three-input max).
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
 // min of a and b that returns NaN when either is NaN (PTX min.NaN).
 __device__ __forceinline__ float fmin_nan(float a, float b) {
   float r;

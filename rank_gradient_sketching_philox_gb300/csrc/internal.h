@@ -158,13 +158,15 @@ struct UpdateWorkspace {
   double* gram_c;          // r x r
   float* c_norm;           // d: Euclidean norm of each row of C
   float* p_norm;           // k: Euclidean norm of each row of P
+  float* c_unscale;        // d: 2^-e of each row's FP16 split of C (NaN: no usable scale)
+  float* p_unscale;        // ceil(k / 128): 2^-f of each 128-row block's FP16 split of P
   double* wnorm_partials;  // kWnormBlocks
   float* scale;            // the step scale s
   int32_t* status;         // scratch status when the caller passes none
   uint32_t* ticket;        // last-block counter of the update kernel
   double* wnew_partials;   // one per update block
-  uint16_t* c_split;       // d x (2 r_pad) BF16: [high | low] part of C
-  uint16_t* p_split;       // k x (2 r_pad) BF16: [high | low] part of P
+  uint16_t* c_split;       // d x (2 r_pad) FP16: [high | low] part of C, each row scaled by 2^e
+  uint16_t* p_split;       // k x (2 r_pad) FP16: [high | low] part of P, 2^f per 128 rows
   // exact-path queue: the elements the update kernel hands to the fix kernel,
   // a few fixed slots per (tile, epilogue warp)
   uint8_t* fix_counts;     // slots used per (tile, warp)

@@ -117,110 +117,182 @@ __global__ void __launch_bounds__(256) normsgd_finalize_kernel(const __grid_cons
   }
 }
 
-// ---- BF16 high/low split of C and P, and their row norms ---------------------
+// ---- FP16 high/low split of C and P, and their row norms --------------------
+// The tensor cores take C and P as two FP16 parts each, scaled by powers of two
+// so that every part is a normal FP16 number: each row of C by its own 2^e
+// (largest |c| in [2^14, 2^15)), P by one 2^f per block of 128 rows (the
+// columns of W one update tile covers).  Then x = hi + lo to about 2^-22
+// relative and the products the MMAs drop (lo lo) are below 2^-22 of the terms.
+// The epilogue undoes the scale exactly: H = acc 2^-e 2^-f.
+constexpr int kSplitRows = 128;  // rows per split block (P: one scale per block)
+
 struct SplitBatch {
-  const float* src[2 * kMaxAux];
-  int64_t row_begin[2 * kMaxAux + 1];  // prefix of the entries' row counts
-  uint16_t* dst[2 * kMaxAux];   // rows x (parts r_pad): [hi | lo] or [hi | mid | lo]
-  float* norm[2 * kMaxAux];     // rows: Euclidean norm of each source row
+  const float* src[2 * kMaxAux];          // entry 2i: C of layer i; 2i + 1: its P
+  int64_t rows[2 * kMaxAux];
+  int64_t block_begin[2 * kMaxAux + 1];   // prefix of the entries' 128-row block counts
+  uint16_t* dst[2 * kMaxAux];     // rows x 2 r_pad FP16 bits: [hi | lo] of the scaled row
+  float* norm[2 * kMaxAux];       // rows: Euclidean norm of each source row
+  float* unscale[2 * kMaxAux];    // C: 2^-e per row; P: 2^-f per 128-row block; NaN: no usable scale
   int n;
   int r;
   int r_pad;
-  int parts;  // 2 or 3 BF16 parts per value
   // each layer's exact-path counters, reset here before the update
   uint32_t* fix_ticket[kMaxAux];
   unsigned long long* fix_acc[kMaxAux];
 };
 
-// Rows of all entries, grid-stride: x = hi + lo to 2^-17 relative, or
-// x = hi + mid + lo to 2^-25 (each part the BF16 of what the parts before it
-// leave, which fp32 holds exactly; columns r..r_pad-1 zero), and ||row||_2.  A row takes lpr lanes (r_pad / 4 rounded up
-// to a power of two, at most 32), lane c its columns 4c..4c+3 of each 4 lpr
-// step; a warp holds 32 / lpr rows at a time and four such steps, their loads
-// issued before any is used, so one round trip serves up to 4 * 32 / lpr rows.
-__global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__ SplitBatch b) {
-  constexpr int kU = 4;
+// Exponent e that brings a largest magnitude m into [2^14, 2^15) (0 for m = 0);
+// false when m is not finite or e falls outside [-100, 100], where the scaled
+// parts or the unscaled products could leave the normal fp32 range.
+__device__ __forceinline__ bool split_exponent(float m, int& e) {
+  if (m == 0.f) {
+    e = 0;
+    return true;
+  }
+  if (!(m <= 3.4028234e38f)) {  // inf or NaN
+    e = 0;
+    return false;
+  }
+  int E;
+  frexpf(m, &E);  // m = f 2^E, f in [0.5, 1)
+  e = 15 - E;
+  if (e < -100 || e > 100) {
+    e = e < -100 ? -100 : 100;
+    return false;
+  }
+  return true;
+}
+
+// One block of 256 threads per 128 rows of an entry (grid over all entries'
+// blocks).  A row takes lpr lanes (r_pad / 4 rounded up to a power of two, at
+// most 32), lane c its columns 4c..4c+3 of each 4 lpr-column step; warp w takes
+// rows 16w..16w+15.  For P the block's largest |p| is found first (the rows are
+// read twice; the second read comes from L2).
+__global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__ SplitBatch b) {
+  __shared__ float wmax[8];
+  __shared__ int blk_e;
+  __shared__ bool blk_ok;
   if (blockIdx.x == 0) {
     for (int t = threadIdx.x; t < b.n / 2; t += blockDim.x) {
       *b.fix_ticket[t] = 0u;
       *b.fix_acc[t] = 0ull;
     }
   }
-  const int lane = threadIdx.x & 31;
-  const int64_t total = b.row_begin[b.n];
-  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const bool vec = (b.r & 3) == 0;
+  // the entry of this block, by bisection of the block prefix
+  int en = 0;
+  {
+    int hi = b.n - 1;
+    while (en < hi) {
+      const int mid = (en + hi + 1) >> 1;
+      if (b.block_begin[mid] <= (int64_t)blockIdx.x) en = mid;
+      else hi = mid - 1;
+    }
+  }
+  const bool is_p = en & 1;
+  const int64_t rows = b.rows[en];
+  const int64_t row0 = ((int64_t)blockIdx.x - b.block_begin[en]) * kSplitRows;
+  const float* __restrict__ src = b.src[en];
+  const int r = b.r, r_pad = b.r_pad;
+  const bool vec = (r & 3) == 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int lpr = 1;
-  while (lpr < 32 && 4 * lpr < b.r_pad) lpr <<= 1;
+  while (lpr < 32 && 4 * lpr < r_pad) lpr <<= 1;
   const int rps = 32 / lpr, sub = lane / lpr, cl = lane % lpr;
-  int en[kU];  // entry of each step's row (rows of a lane only move forward)
+  const int nq = r_pad / (4 * lpr);  // 1, or 2 for r_pad = 256
+  auto load4 = [&](int64_t row, int c0, float (&v)[4]) {
+    const float* s4 = src + row * r + c0;
+    if (vec && c0 < r) {
+      const float4 f = *reinterpret_cast<const float4*>(s4);
+      v[0] = f.x;
+      v[1] = f.y;
+      v[2] = f.z;
+      v[3] = f.w;
+    } else {
 #pragma unroll
-  for (int u = 0; u < kU; ++u) en[u] = 0;
-  for (int64_t g0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kU * rps; g0 < total;
-       g0 += warps * kU * rps) {
-    float v[kU][4];
-    int64_t row[kU];
+      for (int t = 0; t < 4; ++t) v[t] = (c0 + t < r) ? s4[t] : 0.f;
+    }
+  };
+  if (is_p) {
+    float m = 0.f;
+    for (int st = 0; st < 16 / rps; ++st) {
+      const int64_t row = row0 + warp * 16 + st * rps + sub;
+      if (row >= rows) continue;
+      for (int q = 0; q < nq; ++q) {
+        float v[4];
+        load4(row, 4 * cl + 4 * lpr * q, v);
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int64_t gr = g0 + (int64_t)u * rps + sub;
-      row[u] = -1;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) v[u][t] = 0.f;
-      if (gr >= total) continue;
-      while (en[u] + 1 < b.n && b.row_begin[en[u] + 1] <= gr) ++en[u];
-      row[u] = gr - b.row_begin[en[u]];
-      const float* src = b.src[en[u]] + row[u] * b.r;
-      const int c0 = 4 * cl;
-      if (c0 >= b.r) continue;
-      if (vec) {
-        const float4 f = *reinterpret_cast<const float4*>(src + c0);
-        v[u][0] = f.x;
-        v[u][1] = f.y;
-        v[u][2] = f.z;
-        v[u][3] = f.w;
-      } else {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) v[u][t] = (c0 + t < b.r) ? src[c0 + t] : 0.f;
+        for (int t = 0; t < 4; ++t) m = fmaxf(m, fabsf(v[t]) + 0.f * v[t]);  // NaN stays NaN
       }
     }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+      m = (m != m || om != om) ? __int_as_float(0x7FC00000) : fmaxf(m, om);
+    }
+    if (lane == 0) wmax[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float bm = 0.f;
+      for (int w = 0; w < 8; ++w) bm = (bm != bm || wmax[w] != wmax[w]) ? __int_as_float(0x7FC00000) : fmaxf(bm, wmax[w]);
+      int e;
+      blk_ok = split_exponent(bm, e);
+      blk_e = e;
+      b.unscale[en][row0 / kSplitRows] = blk_ok ? ldexpf(1.f, -e) : __int_as_float(0x7FC00000);
+    }
+    __syncthreads();
+  }
+  for (int st = 0; st < 16 / rps; ++st) {
+    const int64_t row = row0 + warp * 16 + st * rps + sub;
+    const bool in = row < rows;
+    float v[2][4];
+    float sq = 0.f, m = 0.f;
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      float sq = 0.f;
-      if (row[u] >= 0) {
-        uint16_t* dst = b.dst[en[u]] + row[u] * b.parts * b.r_pad;
-        for (int c0 = 4 * cl; c0 < b.r_pad; c0 += 4 * lpr) {
-          float w[4];
-          if (c0 == 4 * cl) {
+    for (int q = 0; q < 2; ++q) {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) w[t] = v[u][t];
-          } else {  // rows wider than 4 lpr columns (r_pad > 128): the rest here
-            const float* src = b.src[en[u]] + row[u] * b.r;
+      for (int t = 0; t < 4; ++t) v[q][t] = 0.f;
+      if (in && q < nq) load4(row, 4 * cl + 4 * lpr * q, v[q]);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) w[t] = (c0 + t < b.r) ? src[c0 + t] : 0.f;
-          }
-          uint16_t part[3][4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            sq = fmaf(w[t], w[t], sq);
-            float rest = w[t];
-#pragma unroll
-            for (int q2 = 0; q2 < 3; ++q2) {
-              const __nv_bfloat16 h = __float2bfloat16_rn(rest);
-              part[q2][t] = __bfloat16_as_ushort(h);
-              rest = rest - __bfloat162float(h);
-            }
-          }
-          // r_pad is a multiple of 16: the 4 columns are inside the row, 8-byte aligned
-#pragma unroll
-          for (int q2 = 0; q2 < 3; ++q2)
-            if (q2 < b.parts)
-              *reinterpret_cast<uint2*>(dst + q2 * b.r_pad + c0) =
-                  make_uint2(part[q2][0] | ((uint32_t)part[q2][1] << 16), part[q2][2] | ((uint32_t)part[q2][3] << 16));
-        }
+      for (int t = 0; t < 4; ++t) {
+        sq = fmaf(v[q][t], v[q][t], sq);
+        m = fmaxf(m, fabsf(v[q][t]) + 0.f * v[q][t]);
       }
-      // the row's lanes sum their squares (groups of lpr lanes)
-      for (int o = lpr >> 1; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-      if (row[u] >= 0 && cl == 0) b.norm[en[u]][row[u]] = sqrtf(sq);
+    }
+    // the row's lanes combine their squares and maxima (groups of lpr lanes)
+    for (int o = lpr >> 1; o > 0; o >>= 1) {
+      sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+      const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+      m = (m != m || om != om) ? __int_as_float(0x7FC00000) : fmaxf(m, om);
+    }
+    int e;
+    bool ok;
+    if (is_p) {
+      e = blk_e;
+      ok = blk_ok;
+    } else {
+      ok = split_exponent(m, e);
+    }
+    if (!in) continue;
+    if (cl == 0) {
+      b.norm[en][row] = sqrtf(sq);
+      if (!is_p) b.unscale[en][row] = ok ? ldexpf(1.f, -e) : __int_as_float(0x7FC00000);
+    }
+    const float sc = ldexpf(1.f, e);
+    uint16_t* dst = b.dst[en] + row * 2 * r_pad;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      if (q >= nq) break;
+      const int c0 = 4 * cl + 4 * lpr * q;
+      uint32_t hi2[2], lo2[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const float y0 = v[q][2 * t] * sc, y1 = v[q][2 * t + 1] * sc;
+        const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
+        const __half l0 = __float2half_rn(y0 - __half2float(h0)), l1 = __float2half_rn(y1 - __half2float(h1));
+        hi2[t] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+        lo2[t] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+      }
+      // r_pad is a multiple of 16: the 4 columns are inside the row, 8-byte aligned
+      *reinterpret_cast<uint2*>(dst + c0) = make_uint2(hi2[0], hi2[1]);
+      *reinterpret_cast<uint2*>(dst + r_pad + c0) = make_uint2(lo2[0], lo2[1]);
     }
   }
 }
@@ -231,13 +303,15 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const __grid_constant__
 // layers are numbered end to end and each persistent CTA takes a contiguous
 // range of them, so consecutive units usually share the row block of C.
 struct UpdBatch {
-  CUtensorMap tm_c[kMaxUpd];   // C split, d x (parts r_pad) BF16: [hi | lo] or [hi | mid | lo]
-  CUtensorMap tm_p[kMaxUpd];   // P split, k x (parts r_pad) BF16
+  CUtensorMap tm_c[kMaxUpd];   // C split, d x (2 r_pad) FP16: [hi | lo] of each row scaled by 2^e
+  CUtensorMap tm_p[kMaxUpd];   // P split, k x (2 r_pad) FP16, 2^f per 128 rows
   CUtensorMap tm_w[kMaxUpd];   // W, d x k BF16 (tile loads and stores)
   const float* C[kMaxUpd];     // fp32 C and P for the exact recomputation
   const float* P[kMaxUpd];
   const float* c_norm[kMaxUpd];
   const float* p_norm[kMaxUpd];
+  const float* c_unscale[kMaxUpd];   // 2^-e of each row of the C split
+  const float* p_unscale[kMaxUpd];   // 2^-f of each 128-row block of the P split
   int64_t d[kMaxUpd], k[kMaxUpd];
   int n_ct[kMaxUpd];           // column tiles of the layer
   int n_cu[kMaxUpd];           // units per row block
@@ -255,12 +329,12 @@ struct UpdBatch {
   int p_stages;       // P ring depth
   int w_stages;       // W ring depth
   float scale_val;
-  float err_coef;     // 2^41 (beta + 2^-24): the margin bound is err_coef |s| ||c_i|| max_j ||p_j||
+  float err_coef;     // 2^25 (beta + 2^-24): the margin bound is err_coef |s| ||c_i|| max_j ||p_j||
   uint32_t rk0[10], rk1[10];  // Philox round keys of the seed
   uint32_t step;
   int r;
   int r_pad;          // r rounded up to 16 (MMA K extent)
-  int parts;          // BF16 parts of C and P: 2 (three products) or 3 (six)
+  int parts;          // FP16 parts of C and P: 2 (three products)
   int kchunks;        // 64-wide chunks of r_pad
   uint32_t a_bytes;   // bytes of one part of the C row block: kchunks x 16 KB
   uint32_t b_bytes;   // bytes of one part of a P tile: kchunks x NCOLS x 128
@@ -313,8 +387,8 @@ __device__ __forceinline__ Unit decode_unit(const UpdBatch& a, int u) {
   return x;
 }
 
-// Packed pairs of fp32 operations (one instruction for two lanes of work;
-// each half rounds exactly like the scalar operation).
+// Packed pair of fp32 fused multiply-adds (one instruction for two lanes of
+// work; each half rounds exactly like fmaf).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 d;
   asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
@@ -323,48 +397,21 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
   return d;
 }
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
 
-// Rounding margins of a pair of elements.  S = bits(v) + rand16 is the
-// stochastic-rounding sum (the result is S >> 16); L = S mod 2^16 lies
-// min(L, 2^16 - L) fp32 steps of v from the nearest sum that would round the
-// other way.  A value v' within D of v is at most 2D / ulp(v) + 2 fp32 steps
-// from v (the step halves below a power of two; both values are rounded once),
-// and ulp(v) > |v| 2^-24, so v' rounds like v whenever
-// (min(L, 2^16 - L) - 3) |v| >= 2^25 D.  With x = L - 2^15 and
-// K = 2^30 - 2^18, K - x^2 = (2^15 - |x|)(2^15 + |x|) - 2^18 is at most
-// 2^16 (2^15 - 4 - |x|), so v' rounds like v when x^2 <= K and
-// (K - x^2) |v| >= 2^41 D (the spare step covers the two roundings here).
-// Sets zn = x^2 - K (positive when the margin is four steps or less) and
-// y = zn v, whose magnitude is the left side when zn <= 0; y is NaN when v is.
-// Two packed operations and one of each of these per element.
-__device__ __forceinline__ void rounding_margins(uint32_t s0, uint32_t s1, float2 v, float2& zn, float2& y) {
-  const float2 mg = make_float2(__uint_as_float(__byte_perm(s0, 0x4B000000u, 0x7610)),   // 2^23 + L
-                                __uint_as_float(__byte_perm(s1, 0x4B000000u, 0x7610)));
-  const float2 x = fadd2(mg, make_float2(-8421376.0f, -8421376.0f));  // L - 2^15, exact
-  zn = ffma2(x, x, make_float2(-1073479680.0f, -1073479680.0f));      // x^2 - (2^30 - 2^18)
-  y = fmul2(zn, v);
-}
-
-// Flag of one element from its rounding_margins outputs and the scaled bound
-// 2^41 D (true: the tensor-core result might differ from the definition's).
-__device__ __forceinline__ bool margin_flag(float zn, float y, float bound) {
-  return !(fabsf(y) >= bound) || zn > 0.f;
+// Rounding margin of one element, in units of the error bound.  S = bits(v) +
+// rand16 is the stochastic-rounding sum (the result is S >> 16); L = S mod
+// 2^16 lies min(L, 2^16 - L) fp32 steps of v from the nearest sum that would
+// round the other way.  A value v' within D of v is at most 2D / ulp(v) + 2
+// fp32 steps from v (the step halves below a power of two; both values are
+// rounded once), and ulp(v) > |v| 2^-24, so v' rounds like v whenever
+// (min(L, 2^16 - L) - 3) |v| >= 2^25 D.  Returns the left side (less a
+// little more, for the rounding of this product): negative when the margin
+// is three steps or less, NaN when v is NaN or infinite.
+__device__ __forceinline__ float rounding_margin(uint32_t S, float v) {
+  const float mg = __uint_as_float(__byte_perm(S, 0x4B000000u, 0x7610));  // 2^23 + (S mod 2^16)
+  const float x = mg - 8421376.0f;                                        // (S mod 2^16) - 2^15, exact
+  const float av = fabsf(v);
+  return fmaf(-fabsf(x), av, 32764.0f * av);  // (min(L, 2^16 - L) - 4) |v|, rounded
 }
 
 template <int N>
@@ -466,8 +513,8 @@ __device__ __forceinline__ uint32_t w_stage_offset(int col, int q) {
 // squares of the redone groups.
 __device__ __forceinline__ float redo_in_place(const UpdBatch& a, uint32_t redo, int ngroups, uint32_t taddr,
                                             uint32_t s_w32, int col_base, int q, int i, int j0, int k, uint32_t k8,
-                                            uint32_t layer, const float* C, const float* P, float s, float bound,
-                                            int row0, bool need_norm, unsigned& n_done) {
+                                            uint32_t layer, const float* C, const float* P, float s, float s_t,
+                                            float bound, int row0, bool need_norm, unsigned& n_done) {
   float sq = 0.f;
   for (int g = 0; g < ngroups; ++g) {
     const bool mine = (redo >> g) & 1u;
@@ -489,15 +536,13 @@ __device__ __forceinline__ float redo_in_place(const UpdBatch& a, uint32_t redo,
       float t = 0.f;
 #pragma unroll
       for (int t2 = 0; t2 < 4; ++t2) {
-        const float2 v = ffma2(make_float2(-s, -s), make_float2(__uint_as_float(h[2 * t2]), __uint_as_float(h[2 * t2 + 1])),
+        const float2 v = ffma2(make_float2(-s_t, -s_t), make_float2(__uint_as_float(h[2 * t2]), __uint_as_float(h[2 * t2 + 1])),
                                make_float2(__uint_as_float(wv[t2] << 16), __uint_as_float(wv[t2] & 0xFFFF0000u)));
         const uint32_t s0 = __float_as_uint(v.x) + (rw[0][t2] & 0xFFFFu);
         const uint32_t s1 = __float_as_uint(v.y) + (rw[0][t2] >> 16);
         out[t2] = __byte_perm(s0, s1, 0x7632);
-        float2 zn, y;
-        rounding_margins(s0, s1, v, zn, y);
-        if (margin_flag(zn.x, y.x, bound)) emask |= 1u << (2 * t2);
-        if (margin_flag(zn.y, y.y, bound)) emask |= 2u << (2 * t2);
+        if (!(rounding_margin(s0, v.x) >= bound)) emask |= 1u << (2 * t2);
+        if (!(rounding_margin(s1, v.y) >= bound)) emask |= 2u << (2 * t2);
         if (need_norm) t = sq_acc_bf16x2(out[t2], t);
       }
       if (j0 + col + 8 > k) emask &= (1u << (k - j0 - col)) - 1u;
@@ -514,14 +559,15 @@ __device__ __forceinline__ float redo_in_place(const UpdBatch& a, uint32_t redo,
 
 // Persistent rebuild + update, one CTA per SM, each CTA a contiguous range of
 // units (a unit: one 128-row block of one layer and up to unit_tiles column
-// tiles of NCOLS).  Warp 0 (one lane) streams with TMA the BF16 parts of the C
+// tiles of NCOLS).  Warp 0 (one lane) streams with TMA the FP16 parts of the C
 // row block of each unit, the same parts of the P rows of each column tile
 // into a P ring, and the W tile into a deeper W ring.  Warp 1 (one lane)
-// issues H = sum of the part products down to about 2^-24 (tcgen05.mma, M=128,
-// N=NCOLS; three products of two parts or six of three) into one of four TMEM
-// buffers and frees the P stage with tcgen05.commit.  The 16 epilogue warps
+// issues the scaled H = sum of the part products hi hi + hi lo + lo hi
+// (tcgen05.mma kind::f16, M=128, N=NCOLS) into one of four TMEM buffers and
+// frees the P stage with tcgen05.commit.  The 16 epilogue warps
 // (warps 4..19, four per TMEM lane quarter, one column quarter each) read H
-// from TMEM, form v = fmaf(-s, H, w) with w from the W stage, round it
+// from TMEM, form v = fmaf(-s, H, w) with w from the W stage (the split's
+// scales folded into s), round it
 // stochastically with 16 Philox bits per weight and write the BF16 results
 // back into the stage; warps 2 and 3 (one lane each, alternate tiles) write
 // each finished tile to W with a TMA tensor store and free the stage.
@@ -530,7 +576,7 @@ __device__ __forceinline__ float redo_in_place(const UpdBatch& a, uint32_t redo,
 // fp32 rounding of the exact product.  The tensor-core H differs from it by at
 // most D = |s| (beta ||c_i|| ||p_j|| + 2^-24 |H|) with beta the split and
 // accumulation error of the part products.  Each element's rounding margin
-// (rounding_margins) is compared with that bound.  A lane's 8-column group
+// (rounding_margin) is compared with that bound.  A lane's 8-column group
 // with an element whose margin might be crossed is queued, with its original
 // weights, in the warp's slots of the tile; exact_fix_kernel then recomputes
 // those elements, H_ij from a compensated dot product of the fp32 row of C and
@@ -644,7 +690,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = tc::idesc_bf16(128, NCOLS, false, false);
+    const uint32_t idesc = tc::idesc_f16(128, NCOLS, false, false);
     int it = 0, cl = 0, prev_p = -1, prev_rb = -1;
     bool stop = false;
     for (int u = u_begin; u < u_end && !stop; ++u) {
@@ -668,11 +714,10 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         const uint32_t pst = tc::smem_u32(s_p0 + (size_t)sp * a.parts * a.b_bytes);
         const uint32_t sc = tc::smem_u32(s_c);
         const uint32_t d_tmem = tmem + (uint32_t)(b * NCOLS);
-        // products of the parts whose order is above ~2^-24: with two parts
-        // hi*hi, hi*lo, lo*hi; with three also hi*lo', mid*mid and lo'*hi
-        // (parts 0, 1, 2 = hi, mid, lo')
-        constexpr int kPairA[6] = {0, 0, 1, 0, 1, 2}, kPairB[6] = {0, 1, 0, 2, 1, 0};
-        const int npairs = a.parts == 3 ? 6 : 3;
+        // the products of the parts above ~2^-22 of the terms: hi*hi, hi*lo,
+        // lo*hi (lo*lo is dropped)
+        constexpr int kPairA[3] = {0, 0, 1}, kPairB[3] = {0, 1, 0};
+        const int npairs = 3;
         uint32_t acc = 0;
         for (int c = 0; c < a.kchunks; ++c) {
           for (int kk = 0; kk < 4 && c * 64 + kk * 16 < a.r_pad; ++kk) {
@@ -759,7 +804,8 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       const bool row_ok = i < d;
       const float s = a.scale_dev[p] ? *a.scale_dev[p] : a.scale_val;
       const float bound_row = row_ok ? a.err_coef * fabsf(s) * a.c_norm[p][i] : 0.f;
-      const float2 ns2 = make_float2(-s, -s);
+      // the tensor cores return H scaled by this row's 2^e and the tile's 2^f
+      const float s_row = row_ok ? s * a.c_unscale[p][i] : 0.f;
       const uint32_t layer = a.layer[p];
       const bool need_norm = a.wnorm2_out[p] != nullptr;
       float sq = 0.f, sq_comp = 0.f;  // Kahan-compensated sum of squares
@@ -774,13 +820,21 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           const int jc = j0 + col_base + (lane % kCols);
           if (jc < k) pmax = a.p_norm[p][jc];
         }
+        const float p_un = a.p_unscale[p][j0 / kSplitRows];
         bool live = tc::mbar_wait(&wfull_bar[sw], (it / NSW) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad) &&
                     tc::mbar_wait(&tfull_bar[b], (it / kTmemBufs) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
         live = __all_sync(0xFFFFFFFFu, live);
         tc::tc_fence_after();
         const uint32_t s_w32 = tc::smem_u32(s_w0) + (uint32_t)sw * a.w_bytes;
         for (int o = 16; o > 0; o >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
-        const float bound = bound_row * pmax;  // 2^41 D for every element of this thread's row
+        // v = fmaf(-s, H, w) as fmaf(-s_t, acc, w) with s_t = s 2^-e 2^-f, the
+        // same number when s_t is a normal float (s = 0 gives v = w either
+        // way); otherwise, or when a scale is missing (NaN), the bound is NaN
+        // and every element of the tile takes the exact path
+        const float s_t = s_row * p_un;
+        const bool scaled_ok = s == 0.f || (fabsf(s_t) >= 0x1p-126f && fabsf(s_t) <= 3.4028234e38f);
+        const float bound = scaled_ok ? bound_row * pmax : __int_as_float(0x7FC00000);  // 2^25 D
+        const float2 ns2 = make_float2(-s_t, -s_t);
         // live is the same in the whole warp: one branch per tile
         // this warp's slice of the layer's exact-path queue for this tile
         const uint32_t tile = (uint32_t)x.rb * (uint32_t)a.n_ct[p] + (uint32_t)ct;
@@ -814,7 +868,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
               const uint4 raw = tc::lds128(sp);
               const uint32_t win[4] = {raw.x, raw.y, raw.z, raw.w};
               uint32_t wout[4];
-              float ya[8], za[8];
+              float ym[8];
               // Per pair: v = fmaf(-s, H, w) (one packed FMA) and stochastic
               // rounding (add 16 random bits below the BF16 mantissa, keep the
               // upper halves: one PRMT per pair); the results go back into the
@@ -836,21 +890,14 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
                 const uint32_t s0 = mad_lo(r_lo, 1u, __float_as_uint(v.x));
                 const uint32_t s1 = mad_hi(rword, 0x10000u, __float_as_uint(v.y));
                 wout[t2] = __byte_perm(s0, s1, 0x7632);
-                float2 zn, y;
-                rounding_margins(s0, s1, v, zn, y);
-                ya[2 * t2] = y.x;
-                ya[2 * t2 + 1] = y.y;
-                za[2 * t2] = zn.x;
-                za[2 * t2 + 1] = zn.y;
+                ym[2 * t2] = rounding_margin(s0, v.x);
+                ym[2 * t2 + 1] = rounding_margin(s1, v.y);
               }
-              // smallest margin of the group (NaN if any is NaN) and whether
-              // any element lies four steps or less from a rounding boundary
-              const float gm = fmin3_nan(fmin3_nan(fabsf(ya[0]), fabsf(ya[1]), fabsf(ya[2])),
-                                         fmin3_nan(fabsf(ya[3]), fabsf(ya[4]), fabsf(ya[5])),
-                                         fmin_nan(fabsf(ya[6]), fabsf(ya[7])));
-              const float zmax = fmax3(fmax3(za[0], za[1], za[2]), fmax3(za[3], za[4], za[5]), fmaxf(za[6], za[7]));
+              // smallest margin of the group; NaN if any is NaN
+              const float gm = fmin3_nan(fmin3_nan(ym[0], ym[1], ym[2]), fmin3_nan(ym[3], ym[4], ym[5]),
+                                         fmin_nan(ym[6], ym[7]));
               const bool ok = row_ok && j0 + col < k;
-              const bool flag = ok && (!(gm >= bound) || zmax > 0.f);
+              const bool flag = ok && !(gm >= bound);
               tc::sts128(sp, make_uint4(wout[0], wout[1], wout[2], wout[3]));
               float t = gs;
               if (need_norm) {
@@ -867,7 +914,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
                 uint32_t emask = 0;
                 if (flag) {
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) emask |= margin_flag(za[e], ya[e], bound) ? (1u << e) : 0u;
+                  for (int e = 0; e < 8; ++e) emask |= (ym[e] >= bound) ? 0u : (1u << e);
                   if (j0 + col + 8 > k) emask &= (1u << (k - j0 - col)) - 1u;  // columns inside W
                 }
                 const uint32_t bal = __ballot_sync(0xFFFFFFFFu, emask != 0);
@@ -890,7 +937,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           // groups that found the slots full
           if (__any_sync(0xFFFFFFFFu, redo_mask != 0))
             gs += redo_in_place(a, redo_mask, kGroups, taddr, s_w32, col_base, q, i, j0, k, k8, layer, a.C[p],
-                                a.P[p], s, bound, x.rb * 128 + quarter * 32, need_norm, exact_n);
+                                a.P[p], s, s_t, bound, x.rb * 128 + quarter * 32, need_norm, exact_n);
           if (need_norm) {  // the tile's squares into the compensated sum
             const float y = gs - sq_comp;
             const float tsum = sq + y;
@@ -960,17 +1007,16 @@ int round16(int r) { return (r + 15) / 16 * 16; }
 // must fit in shared memory.
 int update_ncols(int r) { return round16(r) <= 64 ? 128 : 64; }
 
-// BF16 parts of C and P: two, so H takes three products (hi hi, hi lo, lo hi).
+// FP16 parts of C and P: two, so H takes three products (hi hi, hi lo, lo hi).
 int update_parts(int) { return 2; }
 
 // Error of the three-product tensor-core H relative to ||c_i|| ||p_j||: twice
 // the largest error measured over millions of elements for each rank class
-// (Gaussian C; Gaussian-QR and Rademacher P): 2^-16.8 for r = 16, 2^-17.7 for
-// r = 4, 2^-18.1 for r = 64, 2^-18.7 for r = 128, 2^-19.3 for r = 256.  The
-// margin test treats any H within this of the exact product as possible.
-float tc_err_beta(int r) {
-  return r <= 32 ? 0x1p-16f : r <= 64 ? 0x1p-17f : r <= 128 ? 0x1.6a09e6p-18f : 0x1p-18f;
-}
+// (Gaussian C at two scales; Gaussian-QR and Rademacher P), whose largest were
+// 2^-22.9 for r = 4, 2^-21.3 for r = 16, 2^-21.3 for r = 64, 2^-21.6 for
+// r = 128 and 2^-21.1 for r = 256.  The margin test treats any H within this
+// of the exact product as possible.
+float tc_err_beta(int) { return 0x1p-20f; }
 
 template <int NCOLS>
 cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, bool normsgd,
@@ -986,7 +1032,7 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   const int parts = update_parts(r);
   a.scale_val = scale_val;
   a.parts = parts;
-  a.err_coef = 0x1p41f * (tc_err_beta(r) + 0x1p-24f);
+  a.err_coef = 0x1p25f * (tc_err_beta(r) + 0x1p-24f);
   philox_round_keys(seed, a.rk0, a.rk1);
   a.step = step;
   a.r = r;
@@ -1045,6 +1091,8 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       a.P[i] = pr.P;
       a.c_norm[i] = w.c_norm;
       a.p_norm[i] = w.p_norm;
+      a.c_unscale[i] = w.c_unscale;
+      a.p_unscale[i] = w.p_unscale;
       a.d[i] = pr.d;
       a.k[i] = pr.k;
       a.n_ct[i] = (int)ceil_div(pr.k, NCOLS);
@@ -1338,31 +1386,32 @@ cudaError_t launch_exact_fix(int n, const UpdateProblem* probs, const UpdateWork
 
 cudaError_t launch_split(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, cudaStream_t stream) {
   static thread_local SplitBatch sb;
-  const int r_pad = round16(r);
   sb.r = r;
-  sb.r_pad = r_pad;
-  sb.parts = update_parts(r);
+  sb.r_pad = round16(r);
   for (int base = 0; base < n; base += kMaxAux) {
     const int m = (n - base) < kMaxAux ? (n - base) : kMaxAux;
     sb.n = 2 * m;
-    sb.row_begin[0] = 0;
+    sb.block_begin[0] = 0;
     for (int i = 0; i < m; ++i) {
       const UpdateProblem& pr = probs[base + i];
+      const UpdateWorkspace& w = ws[base + i];
       sb.src[2 * i] = pr.C;
-      sb.dst[2 * i] = ws[base + i].c_split;
-      sb.norm[2 * i] = ws[base + i].c_norm;
-      sb.row_begin[2 * i + 1] = sb.row_begin[2 * i] + pr.d;
+      sb.rows[2 * i] = pr.d;
+      sb.dst[2 * i] = w.c_split;
+      sb.norm[2 * i] = w.c_norm;
+      sb.unscale[2 * i] = w.c_unscale;
+      sb.block_begin[2 * i + 1] = sb.block_begin[2 * i] + ceil_div(pr.d, kSplitRows);
       sb.src[2 * i + 1] = pr.P;
-      sb.dst[2 * i + 1] = ws[base + i].p_split;
-      sb.norm[2 * i + 1] = ws[base + i].p_norm;
-      sb.row_begin[2 * i + 2] = sb.row_begin[2 * i + 1] + pr.k;
-      sb.fix_ticket[i] = ws[base + i].fix_ticket;
-      sb.fix_acc[i] = ws[base + i].fix_acc;
+      sb.rows[2 * i + 1] = pr.k;
+      sb.dst[2 * i + 1] = w.p_split;
+      sb.norm[2 * i + 1] = w.p_norm;
+      sb.unscale[2 * i + 1] = w.p_unscale;
+      sb.block_begin[2 * i + 2] = sb.block_begin[2 * i + 1] + ceil_div(pr.k, kSplitRows);
+      sb.fix_ticket[i] = w.fix_ticket;
+      sb.fix_acc[i] = w.fix_acc;
     }
-    const int64_t blocks = ceil_div(sb.row_begin[2 * m], 8);
-    const int grid = (int)(blocks < 8 * (int64_t)num_sms() ? blocks : 8 * (int64_t)num_sms());
     count_launch();
-    split_rows_kernel<<<grid, 256, 0, stream>>>(sb);
+    split_fp16_kernel<<<(unsigned)sb.block_begin[2 * m], 256, 0, stream>>>(sb);
   }
   return cudaGetLastError();
 }
@@ -1397,8 +1446,10 @@ size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool n
   }
   w.c_norm = cur.take<float>((size_t)d);
   w.p_norm = cur.take<float>((size_t)k);
-  w.c_split = cur.take<uint16_t>((size_t)d * update_parts(r) * r_pad);
-  w.p_split = cur.take<uint16_t>((size_t)k * update_parts(r) * r_pad);
+  w.c_unscale = cur.take<float>((size_t)d);
+  w.p_unscale = cur.take<float>((size_t)ceil_div(k, kSplitRows));
+  w.c_split = cur.take<uint16_t>((size_t)d * 2 * r_pad);
+  w.p_split = cur.take<uint16_t>((size_t)k * 2 * r_pad);
   // exact-path queue: kFixSlots entries and a count per (tile, epilogue warp)
   const int64_t tiles = ceil_div(d, 128) * ceil_div(k, update_ncols(r));
   w.fix_ticket = cur.take<uint32_t>(1);

@@ -469,6 +469,33 @@ def test_update_tiny_weights_match_oracle(update):
     _w_check(bits(W), ref)
 
 
+@pytest.mark.parametrize("update", ["normsgd", "sgd"])
+def test_update_rows_of_any_scale_match_oracle(update):
+    """The tensor cores see C and P scaled by powers of two (each row of C,
+    each 128 rows of P); rows of C from 1e-30 to 1e6, a zero row, and a P
+    far from unit scale still match the definition, and a row too small for
+    any usable scale goes through the exact path whole."""
+    d, k, r = 384, 640, 32
+    rng = np.random.default_rng(41)
+    W0 = synth.layer_weight(d, k, 12)
+    P = (orc.sample_qr(7, 1, 2, k, r) * 3e-4).astype(np.float32)
+    C = _rand_c(d, r, 43)
+    C *= (10.0 ** rng.uniform(-30, 6, size=(d, 1))).astype(np.float32)
+    C[5] = 0.0
+    C[6] *= 1e-12  # about 1e-40 at most: below the normal fp32 range
+    W = W0.to(DEV)
+    Cd, Pd = torch.from_numpy(C).to(DEV), torch.from_numpy(P).to(DEV)
+    if update == "normsgd":
+        rgs.apply_update_normsgd(W, Cd, Pd, 1e-3, 8, 3, 4)
+        ref, st, _ = orc.update_normsgd(bits(W0), C, P, 1e-3, 8, 3, 4)
+        assert st == 0
+    else:
+        rgs.apply_update_sgd(W, Cd, Pd, 1e-4, 8, 3, 4)
+        ref = orc.update_sgd(bits(W0), C, P, 1e-4, 8, 3, 4)
+    _w_check(bits(W), ref)
+    assert rgs.read_device_errors() == 0
+
+
 def test_exact_path_is_rare_at_trained_scale():
     """At the trained scale W ~ N(0, 0.02) with tau = 1e-3 only the few
     elements with a tiny weight or a rounding sum within a few steps of a carry
