@@ -1181,6 +1181,7 @@ struct FixBatch {
 };
 constexpr int kFixFracBits = 40;  // fixed point: 2^-40 of the layer's norm
 constexpr int kFixThreads = 256;
+constexpr int kFixSetsPerLane = 4;  // slot sets whose counts each lane of the fix kernel reads
 
 // Fixed-point scale of a layer's changes: ref (the tensor-core ||W_new||^2)
 // is at least every tensor-core square and an exact result is within a step
@@ -1229,17 +1230,17 @@ __device__ __forceinline__ float thread_dot2(const float* c, const float* p, int
   return __fadd_rn(hs, he);
 }
 
-// Each thread reads the count of one (tile, epilogue warp) slot set of a layer
-// (blockIdx.y); the warp lists the used slots of its 32 sets in shared memory
-// and deals them out one per lane, so that no lane works through a full set
-// while the others wait.  For each entry: the group's Philox block again and,
+// Each thread reads the counts of kFixSetsPerLane (tile, epilogue warp) slot
+// sets of a layer (blockIdx.y); the warp lists the used slots of its sets in
+// shared memory and deals them out one per lane, so that no lane works through
+// a full set while the others wait, and one wave of blocks covers the queue.  For each entry: the group's Philox block again and,
 // for each flagged element, H_ij by thread_dot2, then the same v and
 // stochastic rounding as the tensor-core path, written over the tensor-core
 // result in W.  The change of ||W_new||^2 goes, in fixed point relative to the
 // layer's norm, into an integer sum whose total does not depend on the order
 // of the queue; exact_fix_finalize_kernel adds it to the norm.
 __global__ void __launch_bounds__(kFixThreads) exact_fix_kernel(const __grid_constant__ FixBatch b) {
-  __shared__ uint32_t slots[kFixThreads / 32][32 * kFixSlots];
+  __shared__ uint32_t slots[kFixThreads / 32][32 * kFixSetsPerLane * kFixSlots];
   __shared__ unsigned block_done;
   const int p = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1247,17 +1248,28 @@ __global__ void __launch_bounds__(kFixThreads) exact_fix_kernel(const __grid_con
   __syncthreads();
   const bool skipped = b.status_in[p] != nullptr && *b.status_in[p] != 0;
   const int64_t sets = (int64_t)b.tiles[p] * kEpiWarps;
-  const int64_t set = (int64_t)blockIdx.x * kFixThreads + threadIdx.x;
-  const uint32_t cnt = (!skipped && set < sets) ? b.counts[p][set] : 0u;
+  // this warp's sets: base + 32 q + lane for q < kFixSetsPerLane (each load a
+  // coalesced run of 32 counts, all issued before any is used)
+  const int64_t base = ((int64_t)blockIdx.x * (kFixThreads / 32) + warp) * 32 * kFixSetsPerLane;
+  uint32_t cnt[kFixSetsPerLane], mine = 0;
+#pragma unroll
+  for (int q = 0; q < kFixSetsPerLane; ++q) {
+    const int64_t set = base + 32 * q + lane;
+    cnt[q] = (!skipped && set < sets) ? b.counts[p][set] : 0u;
+    mine += cnt[q];
+  }
   // the warp's used slots, in lane order (slot index within the layer)
-  uint32_t incl = cnt;
+  uint32_t incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= o) incl += v;
   }
   const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-  for (uint32_t q = 0; q < cnt; ++q) slots[warp][incl - cnt + q] = (uint32_t)set * kFixSlots + q;
+  uint32_t at = incl - mine;
+#pragma unroll
+  for (int q = 0; q < kFixSetsPerLane; ++q)
+    for (uint32_t e = 0; e < cnt[q]; ++e) slots[warp][at++] = (uint32_t)(base + 32 * q + lane) * kFixSlots + e;
   __syncwarp();
   unsigned done = 0;
   if (total != 0) {
@@ -1371,7 +1383,8 @@ cudaError_t launch_exact_fix(int n, const UpdateProblem* probs, const UpdateWork
     int64_t sets = 0;
     for (int i = 0; i < m; ++i) sets = std::max(sets, (int64_t)f.tiles[i] * kEpiWarps);
     count_launch();
-    exact_fix_kernel<<<dim3((unsigned)ceil_div(sets, kFixThreads), m), kFixThreads, 0, stream>>>(f);
+    exact_fix_kernel<<<dim3((unsigned)ceil_div(sets, (int64_t)kFixThreads * kFixSetsPerLane), m), kFixThreads, 0,
+                       stream>>>(f);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (normsgd) {
