@@ -59,6 +59,8 @@ struct SkinnyBatch {
   int out_mode;                    // 0: BF16 round-to-nearest store; 1: fp32 store; 2: fp32 add;
                                    // 3: BF16 split store, hi in columns [0, N), lo at [n_pad, n_pad + N)
   int b_col_off;                   // MN-major B: column offset of B operand nb is nb * b_col_off
+  int k_parts;                     // persistent projection: partial accumulators per tile (K ranges)
+  int acc_bufs;                    // persistent projection: TMEM buffers (tiles in flight)
   int* err;
 };
 
@@ -428,6 +430,207 @@ __global__ void __launch_bounds__(kAccThreads, 1) acc_persistent_kernel(const __
   if (warp == 0) tc::tmem_dealloc(tmem, a.tmem_cols);
 }
 
+// ---- persistent input projection ---------------------------------------------
+// XP = bf16(X (P_hi + P_lo)) for many layers with one CTA per SM.  A work item
+// is one problem's tile of 128 token rows over all of K; the CTAs take the
+// items round robin.  Warp 0 (one lane) streams each 64-wide K chunk of the
+// tile's X rows and of both parts of P^T into a ring of stages with TMA; warp 1
+// (one lane) issues the chunk's MMAs (both parts into the same accumulator)
+// into one of two TMEM buffers; warps 2..5 round a finished item's
+// accumulators to BF16 and store them (one token row per thread) while the
+// next item streams.  The tensor cores' fp32 accumulation loses a little with
+// every addition, so a tile's K chunks go to k_parts accumulators of
+// contiguous K ranges (as many as TMEM holds: up to 4), added in a fixed order
+// by the epilogue; a long single chain (192 chunks for k = 12288) would leave
+// XP measurably less accurate than the split over a cluster does.
+template <int NB>
+__global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const __grid_constant__ SkinnyBatch a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ volatile int issued, consumed;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = a.tile_begin[a.n];
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    issued = 0;
+    consumed = 0;
+    for (int s = 0; s < a.stages; ++s) {
+      tc::mbar_init(&full_bar[s], 1);
+      tc::mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull_bar[b], 1);
+      tc::mbar_init(&tempty_bar[b], 4);  // the four epilogue warps
+    }
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, a.tmem_cols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  auto decode = [&](int item, int& p, int& m0) {
+    p = 0;
+    while (p + 1 < a.n && a.tile_begin[p + 1] <= item) ++p;
+    m0 = (item - a.tile_begin[p]) * 128;
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: TMA ring over the items' chunks ----
+    int it = 0;
+    bool stop = false;
+    for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
+      int p, m0;
+      decode(item, p, m0);
+      const CUtensorMap* tmA = &a.tmA[p];
+      const CUtensorMap* tmB = &a.tmB[p];
+      for (int c = 0; c < a.kchunks[p]; ++c, ++it) {
+        const int s = it % a.stages, u = it / a.stages;
+        if (u > 0 && !tc::mbar_wait(&empty_bar[s], (u - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+          stop = true;
+          break;
+        }
+        uint8_t* st = smem + (size_t)s * a.stage_bytes;
+        tc::mbar_arrive_expect_tx(&full_bar[s], a.stage_bytes);
+        const int kc = c * kChunk;
+        tc::tma_load_2d(st, tmA, &full_bar[s], kc, m0);  // X: [128 tokens][64 k] (past M: zeros)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)  // P^T split: [n_pad rank rows][64 k] of part nb
+          tc::tma_load_2d(st + a.a_bytes + nb * a.b_bytes, tmB, &full_bar[s], kc, nb * a.n_pad);
+        issued = it + 1;
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer ----
+    const uint32_t idesc = tc::idesc_bf16(128, a.n_pad, false, false);
+    const int nbuf = a.acc_bufs, kp = a.k_parts;
+    int it = 0, j = 0;
+    bool stop = false;
+    for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x, ++j) {
+      int p, m0;
+      decode(item, p, m0);
+      const int b = j % nbuf, use = j / nbuf;
+      if (use >= 1 && !tc::mbar_wait(&tempty_bar[b], (use - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))
+        break;
+      tc::tc_fence_after();
+      const int kc = a.kchunks[p];
+      for (int c = 0; c < kc; ++c, ++it) {
+        const int s = it % a.stages, u = it / a.stages;
+        if (!tc::mbar_wait(&full_bar[s], u & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) {
+          stop = true;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t sa = tc::smem_u32(smem + (size_t)s * a.stage_bytes);
+        // partial accumulator of this chunk: contiguous K ranges over the
+        // min(k_parts, chunks) partials, each receiving at least one chunk
+        const int kpe = kc < kp ? kc : kp;
+        const int part = (int)((int64_t)c * kpe / kc);
+        const bool first = c == (int)(((int64_t)part * kc + kpe - 1) / kpe);
+        const uint32_t acc0 = tmem + (uint32_t)((b * kp + part) * a.n_pad);
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk) {
+          const uint64_t ad = tc::sdesc_sw128(sa + kk * 32, 16, 1024);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const uint64_t bd = tc::sdesc_sw128(sa + a.a_bytes + nb * a.b_bytes + kk * 32, 16, 1024);
+            tc::mma_bf16(acc0, ad, bd, idesc, (!first || kk > 0 || nb > 0) ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(&empty_bar[s]);
+        consumed = it + 1;
+      }
+      if (!stop) tc::mma_commit(&tfull_bar[b]);
+    }
+  } else if (warp >= 2) {
+    // ---- epilogue: accumulators -> XP, one token row per thread ----
+    const int quarter = warp & 3;  // TMEM lanes 32 (warp % 4) .. +31
+    const int q = quarter * 32 + lane;
+    const int ncols32 = (a.n_pad + 31) / 32;
+    const int nbuf = a.acc_bufs, kp = a.k_parts;
+    int j = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
+      int p, m0;
+      decode(item, p, m0);
+      const int b = j % nbuf;
+      const bool live = tc::mbar_wait(&tfull_bar[b], (j / nbuf) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
+      if (!__all_sync(0xFFFFFFFFu, live)) break;
+      tc::tc_fence_after();
+      const int64_t grow = (int64_t)m0 + q;
+      uint16_t* row = static_cast<uint16_t*>(a.out[p]) + grow * a.ld_out[p];
+      const int nparts = a.kchunks[p] < kp ? a.kchunks[p] : kp;  // partials that received chunks
+      for (int cg = 0; cg < ncols32; ++cg) {
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(cg * 32);
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)(b * kp * a.n_pad), v);
+        tc::tmem_wait_ld();
+        for (int pt = 1; pt < nparts; ++pt) {  // the partials in K order
+          uint32_t w[32];
+          tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)((b * kp + pt) * a.n_pad), w);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(w[t]));
+        }
+        if (grow >= a.M[p]) continue;
+        const int c0 = cg * 32;
+        const int ncol = a.N - c0 < 32 ? a.N - c0 : 32;
+        if (ncol <= 0) continue;
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float f0 = __uint_as_float(v[2 * t]), f1 = __uint_as_float(v[2 * t + 1]);
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(f0), h1 = __float2bfloat16_rn(f1);
+          hi[t] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+          if (a.out_mode == 3)
+            lo[t] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f0 - __bfloat162float(h0))) |
+                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f1 - __bfloat162float(h1))) << 16);
+        }
+        // the row stride is a multiple of 8 elements: 16-byte stores for
+        // whole 8-column groups, single elements for a ragged end
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          const int cc = c0 + 8 * g8;
+          if (cc + 8 <= a.N) {
+            *reinterpret_cast<uint4*>(row + cc) = make_uint4(hi[4 * g8], hi[4 * g8 + 1], hi[4 * g8 + 2], hi[4 * g8 + 3]);
+            if (a.out_mode == 3)
+              *reinterpret_cast<uint4*>(row + a.n_pad + cc) =
+                  make_uint4(lo[4 * g8], lo[4 * g8 + 1], lo[4 * g8 + 2], lo[4 * g8 + 3]);
+          } else if (cc < a.N) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              if (cc + t < a.N) {
+                row[cc + t] = (uint16_t)(hi[4 * g8 + (t >> 1)] >> (16 * (t & 1)));
+                if (a.out_mode == 3) row[a.n_pad + cc + t] = (uint16_t)(lo[4 * g8 + (t >> 1)] >> (16 * (t & 1)));
+              }
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty_bar[b]);
+    }
+  }
+  __syncwarp();
+  // ---- on a timeout, give copies still in flight a bounded chance to land ----
+  tc::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && abort_flag) {
+    volatile int dummy = 0;
+    for (int i = consumed; i < issued; ++i)
+      tc::mbar_wait(&full_bar[i % a.stages], (i / a.stages) & 1, &dummy, nullptr, 0, 100000000ull);
+  }
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, a.tmem_cols);
+}
+
 // P (k x r fp32) -> P^T split into BF16 high and low parts: rows [0, n_pad)
 // hold the high part, rows [n_pad, 2 n_pad) the low part, each k wide; rank
 // rows r..n_pad-1 are zero.  32 x 32 tiles transposed through shared memory;
@@ -565,6 +768,33 @@ cudaError_t launch_acc_persistent(SkinnyBatch& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_proj_persistent(SkinnyBatch& a, cudaStream_t stream) {
+  a.stage_bytes = a.a_bytes + 2 * a.b_bytes;
+  int stages = (int)((200u * 1024u) / a.stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  a.stages = stages;
+  // partial accumulators: up to 4 per tile, two tiles in flight where TMEM
+  // holds them, else one
+  a.acc_bufs = 2;
+  a.k_parts = 4;
+  while (a.k_parts > 1 && a.acc_bufs * a.k_parts * a.n_pad > 512) a.k_parts >>= 1;
+  if (a.k_parts == 1 && 2 * a.n_pad <= 512) {
+    a.acc_bufs = 1;
+    a.k_parts = 2;
+  }
+  a.tmem_cols = tmem_cols_for(a.acc_bufs * a.k_parts * a.n_pad);
+  const size_t smem = (size_t)stages * a.stage_bytes + 1024;
+  auto kernel = proj_persistent_kernel<2>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int items = a.tile_begin[a.n];
+  const int grid = items < num_sms() ? items : num_sms();
+  count_launch();
+  kernel<<<grid, kAccThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t project_workspace_bytes(int64_t, int64_t k, int64_t r) {
@@ -687,7 +917,14 @@ cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, voi
     a.out_mode = xp_split ? 3 : 0;
     a.b_col_off = 0;
     a.err = errw;
-    err = launch_skinny<false, false, 2>(a, stream);
+    // wide ranks (a stage of more than 48 KB, one CTA per SM) with enough
+    // token tiles to keep every SM busy: persistent CTAs, each tile over all
+    // of K, the next tile's loads overlapping this one's epilogue (measured:
+    // 20% faster at rank 192); narrower ranks run two split-K CTAs per SM,
+    // which streamed X faster than one persistent CTA did (0.88 against 0.54
+    // of HBM at rank 64)
+    err = (n_pad > 128 && a.tile_begin[m] >= 2 * num_sms()) ? launch_proj_persistent(a, stream)
+                                                             : launch_skinny<false, false, 2>(a, stream);
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();

@@ -116,7 +116,8 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, BF16 operands, fp32 accumulator.
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit operands (kind::f16: BF16 or FP16
+// as the instruction descriptor says), fp32 accumulator.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(

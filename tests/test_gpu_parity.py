@@ -179,6 +179,42 @@ def test_project_inputs_full_size_sampled_tokens(T, k, r, kind):
     _xp_check(bits(XP)[rows], ref)
 
 
+@pytest.mark.parametrize("r,m", [(64, 1), (20, 1), (64, 3), (136, 1), (72, 3)])
+def test_project_inputs_persistent_batch_matches_oracle(r, m):
+    """Large batches (3 layers x 16384 tokens): ranks above 128 run persistent
+    CTAs (each tile over all of K), the others split-K CTAs; single layers of
+    rank 64, 20 and 136 (ragged last column groups) and groups of three members
+    at rank 192 and 216; sampled tokens against the oracle, and the BF16 pair
+    form against the exact product."""
+    T, k, n = 16384, 1024, 3
+    Xs = [synth.layer_x(T, k, i, 0, device=DEV) for i in range(n)]
+    Ps = [[torch.from_numpy(orc.sample_qr(5, 3 * i + q, 0, k, r)).to(DEV) for q in range(m)] for i in range(n)]
+    XPs = [_padded_bf16(T, m * r) for _ in range(n)]
+    if m == 1:
+        rgs.project_inputs_batched(Xs, [P[0] for P in Ps], XPs)
+    else:
+        splits = rgs.split_projection_grouped(Ps)
+        rgs.project_inputs_grouped_batched(Xs, splits, m * r, XPs)
+    rows = np.random.default_rng(5).choice(T, 48, replace=False)
+    for i in range(n):
+        for q in range(m):
+            ref = orc.project_inputs(bits(Xs[i][rows]), Ps[i][q].cpu().numpy())
+            _xp_check(bits(XPs[i][:, q * r:(q + 1) * r])[rows], ref)
+    if m == 1:
+        n_pad = (r + 15) // 16 * 16
+        XP2 = [_padded_bf16(T, rgs.xp_split_cols(r)) for _ in range(n)]
+        rgs.project_inputs_fp32xp_batched(Xs, [P[0] for P in Ps], XP2)
+        for i in range(n):
+            got = (XP2[i][rows, :r].float() + XP2[i][rows, n_pad:n_pad + r].float()).cpu().numpy().astype(np.float64)
+            exact = orc.project_inputs_exact(bits(Xs[i][rows]), Ps[i][0].cpu().numpy())
+            # P = hi + lo to 2^-17 of each entry, and fp32 sums of k terms:
+            # within 2^-16 of the sum of the terms' magnitudes
+            x64 = Xs[i][rows].float().cpu().numpy().astype(np.float64)
+            mag = np.abs(x64) @ np.abs(Ps[i][0].cpu().numpy().astype(np.float64))
+            assert np.all(np.abs(got - exact) <= 2.0 ** -16 * mag)
+    assert rgs.read_device_errors() == 0
+
+
 # --------------------------------------------------------------------------
 # (c) accumulation
 # --------------------------------------------------------------------------
