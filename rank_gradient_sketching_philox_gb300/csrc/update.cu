@@ -337,7 +337,7 @@ struct UpdBatch {
   int parts;          // FP16 parts of C and P: 2 (three products)
   int kchunks;        // 64-wide chunks of r_pad
   uint32_t a_bytes;   // bytes of one part of the C row block: kchunks x 16 KB
-  uint32_t b_bytes;   // bytes of one part of a P tile: kchunks x NCOLS x 128
+  uint32_t b_bytes;   // bytes of one part of one 64-wide chunk of a P tile: NCOLS x 128
   uint32_t w_bytes;   // bytes of the W tile: NCOLS/64 x 16 KB
   int* err;
   unsigned long long* exact_count;  // elements recomputed exactly (instrumentation)
@@ -675,17 +675,20 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
 #pragma unroll
         for (int bx = 0; bx < NCOLS / 64; ++bx)
           tc::tma_load_2d(wst + bx * 16384, &a.tm_w[x.p], &wfull_bar[sw], j0 + 64 * bx, i0);
-        const int sp = it % NSP;
-        if (it >= NSP && !tc::mbar_wait(&pempty_bar[sp], ((it / NSP) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
-          stop = true;
-          break;
+        // P: one stage per 64-wide chunk of r (both parts), so that wide
+        // ranks keep two or more chunks in flight
+        for (int c = 0; c < a.kchunks && !stop; ++c) {
+          const int ip = it * a.kchunks + c, sp = ip % NSP;
+          if (ip >= NSP && !tc::mbar_wait(&pempty_bar[sp], ((ip / NSP) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+            stop = true;
+            break;
+          }
+          uint8_t* pst = s_p0 + (size_t)sp * a.parts * a.b_bytes;
+          tc::mbar_arrive_expect_tx(&pfull_bar[sp], a.parts * a.b_bytes);
+          for (int q2 = 0; q2 < a.parts; ++q2)
+            tc::tma_load_2d(pst + q2 * a.b_bytes, &a.tm_p[x.p], &pfull_bar[sp], q2 * a.r_pad + c * 64, j0);
         }
-        uint8_t* pst = s_p0 + (size_t)sp * a.parts * a.b_bytes;
-        tc::mbar_arrive_expect_tx(&pfull_bar[sp], a.parts * a.b_bytes);
-        for (int q2 = 0; q2 < a.parts; ++q2)
-          for (int c = 0; c < a.kchunks; ++c)
-            tc::tma_load_2d(pst + q2 * a.b_bytes + c * NCOLS * 128, &a.tm_p[x.p], &pfull_bar[sp], q2 * a.r_pad + c * 64,
-                            j0);
+        if (stop) break;
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -703,36 +706,39 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         prev_rb = x.rb;
       }
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
-        const int sp = it % NSP, b = it % kTmemBufs;
-        if (!tc::mbar_wait(&pfull_bar[sp], (it / NSP) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad) ||
-            (it >= kTmemBufs &&
-             !tc::mbar_wait(&tempty_bar[b], ((it / kTmemBufs) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))) {
+        const int b = it % kTmemBufs;
+        if (it >= kTmemBufs &&
+            !tc::mbar_wait(&tempty_bar[b], ((it / kTmemBufs) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
           stop = true;
           break;
         }
-        tc::tc_fence_after();
-        const uint32_t pst = tc::smem_u32(s_p0 + (size_t)sp * a.parts * a.b_bytes);
         const uint32_t sc = tc::smem_u32(s_c);
         const uint32_t d_tmem = tmem + (uint32_t)(b * NCOLS);
         // the products of the parts above ~2^-22 of the terms: hi*hi, hi*lo,
         // lo*hi (lo*lo is dropped)
         constexpr int kPairA[3] = {0, 0, 1}, kPairB[3] = {0, 1, 0};
-        const int npairs = 3;
         uint32_t acc = 0;
         for (int c = 0; c < a.kchunks; ++c) {
+          const int ip = it * a.kchunks + c, sp = ip % NSP;
+          if (!tc::mbar_wait(&pfull_bar[sp], (ip / NSP) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) {
+            stop = true;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t pst = tc::smem_u32(s_p0 + (size_t)sp * a.parts * a.b_bytes);
           for (int kk = 0; kk < 4 && c * 64 + kk * 16 < a.r_pad; ++kk) {
-            const uint32_t off_a = c * 16384 + kk * 32, off_b = c * NCOLS * 128 + kk * 32;
+            const uint32_t off_a = c * 16384 + kk * 32, off_b = kk * 32;
 #pragma unroll
-            for (int pr = 0; pr < 6; ++pr) {
-              if (pr >= npairs) break;
+            for (int pr = 0; pr < 3; ++pr) {
               const uint64_t ad = tc::sdesc_sw128(sc + kPairA[pr] * a.a_bytes + off_a, 16, 1024);
               const uint64_t bd = tc::sdesc_sw128(pst + kPairB[pr] * a.b_bytes + off_b, 16, 1024);
               tc::mma_bf16(d_tmem, ad, bd, idesc, acc);
               acc = 1u;
             }
           }
+          tc::mma_commit(&pempty_bar[sp]);
         }
-        tc::mma_commit(&pempty_bar[sp]);
+        if (stop) break;
         tc::mma_commit(&tfull_bar[b]);
       }
       // release the C row block once its last unit is issued
@@ -1003,9 +1009,9 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
 
 int round16(int r) { return (r + 15) / 16 * 16; }
 
-// Columns per tile: the C row block plus two or more stages of (P tile, W tile)
-// must fit in shared memory.
-int update_ncols(int r) { return round16(r) <= 64 ? 128 : 64; }
+// Columns per tile: the C row block (both parts, all of r) plus two P chunk
+// stages and three or more W stages must fit in shared memory.
+int update_ncols(int r) { return round16(r) <= 128 ? 128 : 64; }
 
 // FP16 parts of C and P: two, so H takes three products (hi hi, hi lo, lo hi).
 int update_parts(int) { return 2; }
@@ -1039,7 +1045,7 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   a.r_pad = r_pad;
   a.kchunks = (r_pad + 63) / 64;
   a.a_bytes = (uint32_t)a.kchunks * 16384u;
-  a.b_bytes = (uint32_t)a.kchunks * NCOLS * 128u;
+  a.b_bytes = (uint32_t)NCOLS * 128u;
   a.w_bytes = (uint32_t)(NCOLS / 64) * 16384u;
   a.err = errw;
   a.exact_count = exact;
@@ -1050,9 +1056,9 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   const size_t max_smem = 227 * 1024 - fa.sharedSizeBytes;
   const size_t fixed = (size_t)parts * a.a_bytes + 1024;
   const size_t p_stage = (size_t)parts * a.b_bytes;
-  // two P stages when they still leave four W stages (W comes from HBM and
-  // needs the deeper ring), else one
-  int p_stages = (fixed + 2 * p_stage + 4 * (size_t)a.w_bytes <= max_smem) ? 2 : 1;
+  // two P stages (each one 64-wide chunk of r) when they still leave three W
+  // stages (W comes from HBM and needs the deeper ring), else one
+  int p_stages = (fixed + 2 * p_stage + 3 * (size_t)a.w_bytes <= max_smem) ? 2 : 1;
   int w_stages = (int)((max_smem - fixed - p_stages * p_stage) / a.w_bytes);
   if (w_stages > kMaxStagesUpd) w_stages = kMaxStagesUpd;
   if (w_stages < 1) return cudaErrorInvalidConfiguration;
