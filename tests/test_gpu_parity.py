@@ -389,7 +389,7 @@ def _rand_c(d, r, seed, scale=1.0):
 
 
 @pytest.mark.parametrize("d,k,r,kind", [(256, 512, 16, 1), (256, 512, 16, 0), (40, 24, 4, 0),
-                                        (130, 136, 20, 1), (1024, 2048, 128, 1),
+                                        (130, 136, 20, 1), (1024, 2048, 128, 1), (200, 520, 96, 1),
                                         (300, 4096, 256, 1), (7, 8, 1, 0)])
 def test_normsgd_matches_oracle(d, k, r, kind):
     W0 = synth.layer_weight(d, k, 3)
