@@ -159,10 +159,11 @@ SKETCH_API sketch_status sketch_apply_update_normsgd(uint16_t* W, int64_t d, int
 /* (d') LoGRA's basic SGD, W <- W - alpha_eta * S A with S = C and A = P^T
  * ("LoGRA: Low-Rank Gradient Sketches", "Why the Update Is Low-Rank but Not an
  * Exact Recovery"), with the same on-chip rebuild and stochastic rounding.
- * The receiver of a policy synchronisation applies the received factor
- * alpha*eta*U with alpha_eta = 1 and the regenerated projection ("LoGRA:
- * Scaling LLM Reinforcement Learning with Low-Rank Gradient Sketches", Key
- * Contributions 2).  dev_status (nullable) is set to 0. */
+ * The receiver of a policy synchronisation applies the received factor U
+ * with the received alpha_eta and the projection regenerated from the seed,
+ * which gives the trainer's W bit for bit ("LoGRA: Scaling LLM Reinforcement
+ * Learning with Low-Rank Gradient Sketches", Key Contributions 2).
+ * dev_status (nullable) is set to 0. */
 SKETCH_API sketch_status sketch_apply_update_sgd(uint16_t* W, int64_t d, int64_t k, int64_t ld_w,
                                       const float* C, const float* P, int64_t r, float alpha_eta,
                                       uint64_t seed, uint32_t layer, uint32_t step,
