@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__
   int lpr = 1;
   while (lpr < 32 && 4 * lpr < r_pad) lpr <<= 1;
   const int rps = 32 / lpr, sub = lane / lpr, cl = lane % lpr;
-  const int nq = r_pad / (4 * lpr);  // 1, or 2 for r_pad = 256
+  const int nq = (r_pad + 4 * lpr - 1) / (4 * lpr);  // column steps: 1, or 2 when r_pad > 128
   auto load4 = [&](int64_t row, int c0, float (&v)[4]) {
     const float* s4 = src + row * r + c0;
     if (vec && c0 < r) {
@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__
     for (int q = 0; q < 2; ++q) {
       if (q >= nq) break;
       const int c0 = 4 * cl + 4 * lpr * q;
+      if (c0 >= r_pad) continue;  // lanes past the padded row (r_pad not a multiple of 4 lpr)
       uint32_t hi2[2], lo2[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {

@@ -179,16 +179,19 @@ def test_project_inputs_full_size_sampled_tokens(T, k, r, kind):
     _xp_check(bits(XP)[rows], ref)
 
 
-@pytest.mark.parametrize("r,m", [(64, 1), (20, 1), (64, 3), (136, 1), (72, 3)])
-def test_project_inputs_persistent_batch_matches_oracle(r, m):
+@pytest.mark.parametrize("r,m,k", [(64, 1, 1024), (20, 1, 1024), (64, 3, 1024), (136, 1, 1024), (72, 3, 1024),
+                                   (48, 3, 128)])
+def test_project_inputs_persistent_batch_matches_oracle(r, m, k):
     """Large batches (3 layers x 16384 tokens): ranks above 128 run persistent
     CTAs (each tile over all of K), the others split-K CTAs; single layers of
     rank 64, 20 and 136 (ragged last column groups) and groups of three members
     at rank 192 and 216; sampled tokens against the oracle, and the BF16 pair
-    form against the exact product."""
-    T, k, n = 16384, 1024, 3
+    form against the exact product; k = 128 gives two K chunks, fewer than
+    the four partial accumulators a tile may use."""
+    T, n = 16384, 3
     Xs = [synth.layer_x(T, k, i, 0, device=DEV) for i in range(n)]
-    Ps = [[torch.from_numpy(orc.sample_qr(5, 3 * i + q, 0, k, r)).to(DEV) for q in range(m)] for i in range(n)]
+    sample = orc.sample_qr if 4 * r <= k else orc.sample_rademacher
+    Ps = [[torch.from_numpy(sample(5, 3 * i + q, 0, k, r)).to(DEV) for q in range(m)] for i in range(n)]
     XPs = [_padded_bf16(T, m * r) for _ in range(n)]
     if m == 1:
         rgs.project_inputs_batched(Xs, [P[0] for P in Ps], XPs)
@@ -390,6 +393,7 @@ def _rand_c(d, r, seed, scale=1.0):
 
 @pytest.mark.parametrize("d,k,r,kind", [(256, 512, 16, 1), (256, 512, 16, 0), (40, 24, 4, 0),
                                         (130, 136, 20, 1), (1024, 2048, 128, 1), (200, 520, 96, 1),
+                                        (100, 600, 136, 1), (96, 256, 48, 0),
                                         (300, 4096, 256, 1), (7, 8, 1, 0)])
 def test_normsgd_matches_oracle(d, k, r, kind):
     W0 = synth.layer_weight(d, k, 3)
