@@ -167,11 +167,9 @@ struct UpdateWorkspace {
   double* wnew_partials;   // one per update block
   uint16_t* c_split;       // d x (2 r_pad) FP16: [high | low] part of C, each row scaled by 2^e
   uint16_t* p_split;       // k x (2 r_pad) FP16: [high | low] part of P, 2^f per 128 rows
-  // exact-path queue: the elements the update kernel hands to the fix kernel,
-  // a few fixed slots per (tile, epilogue warp)
-  uint8_t* fix_counts;     // slots used per (tile, warp)
-  uint16_t* fix_tags;      // per slot: flagged elements, lane and group of the entry
-  uint4* fix_entries;      // per slot: the group's original weights
+  // exact-path tags: the groups whose flagged elements the fix kernel recomputes
+  uint8_t* fix_counts;     // per (tile, epilogue warp): tags written
+  uint16_t* fix_tags;      // per (tile, warp): up to 128 tags (flagged elements, lane, group)
   uint32_t* fix_ticket;    // bit 31: a non-finite change; the fix kernel's block counter
   unsigned long long* fix_acc;  // fixed-point sum of the exact path's changes of ||W_new||^2
 };

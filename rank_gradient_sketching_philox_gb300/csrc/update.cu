@@ -342,9 +342,8 @@ struct UpdBatch {
   uint32_t w_bytes;   // bytes of the W tile: NCOLS/64 x 16 KB
   int* err;
   unsigned long long* exact_count;  // elements recomputed exactly (instrumentation)
-  uint4* fix_entries[kMaxUpd];      // exact-path queue of each layer: kFixSlots per (tile, warp)
-  uint16_t* fix_tags[kMaxUpd];
-  uint8_t* fix_counts[kMaxUpd];
+  uint16_t* fix_tags[kMaxUpd];      // exact-path tags of each layer: kFixCap per (tile, warp)
+  uint8_t* fix_counts[kMaxUpd];     // tags written per (tile, warp)
 };
 
 // kernel parameters are limited to 32764 bytes
@@ -423,139 +422,18 @@ __device__ __forceinline__ uint32_t pick(const uint32_t (&v)[N], int i) {
   return r;
 }
 
-// Exact-path queue layout: each (tile, epilogue warp) owns kFixSlots entries
-// of its layer's queue and a one-byte count.  An entry is one lane's 8-column
-// group that holds at least one element whose margin the bound might cross: the
-// group's original weights (16 bytes, fix_entries) and a 16-bit tag (fix_meta:
-// the flagged elements as bits 0..7, the lane at bits 8..12, the group at bits
-// 13..14).  A trained-scale tile has about one such group per warp; a group
-// that finds the slots full is redone in place after the warp's last group of
-// the tile.  Fixed slots make the split between queued and in-place groups the
-// same on every call.
-constexpr uint32_t kFixSlots = 4;
-
-// H_ij as a compensated dot product of c (row i of C) and p (row j of P), r
-// terms, by the whole warp: lane l takes terms l, l + 32, ... into a running
-// TwoSum pair, and the lanes' pairs are merged by TwoSum over a butterfly.
-// Every lane returns the same value, fl32 of the exact sum except within about
-// 2^-40 of a rounding boundary (Dot2: as accurate as twice fp32 precision).
-__device__ __forceinline__ float warp_dot2(const float* c, const float* p, int r, int lane) {
-  float hs = 0.f, he = 0.f;
-  for (int l = lane; l < r; l += 32) {
-    const float cv = c[l], pv = p[l];
-    const float m = __fmul_rn(cv, pv);
-    float sum, err;
-    two_sum(hs, m, sum, err);
-    hs = sum;
-    he = __fadd_rn(he, __fadd_rn(err, __fmaf_rn(cv, pv, -m)));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ohs = __shfl_xor_sync(0xFFFFFFFFu, hs, o), ohe = __shfl_xor_sync(0xFFFFFFFFu, he, o);
-    float sum, err;
-    two_sum(hs, ohs, sum, err);
-    hs = sum;
-    he = __fadd_rn(he, __fadd_rn(ohe, err));
-  }
-  return __fadd_rn(hs, he);
-}
-
-// The exact path, in place: the warp takes the elements of emask (bit t:
-// column jg + t of the calling lane's row) one at a time, H_ij as a
-// compensated dot product of the fp32 row i of C and row j of P, its terms
-// spread over the lanes and merged by TwoSum, then v = fmaf(-s, fl32(H_ij), w)
-// and the same stochastic rounding as the tensor-core path.  The owning lane
-// writes the result into its W stage over the tensor-core result.  wv, rv, ov
-// are the lane's original weights, Philox words and tensor-core results of the
-// group; returns the change of the lane's sum of squares.
-__device__ __forceinline__ float exact_in_place(uint32_t emask, uint4 w4, uint4 r4, uint4 o4, const float* C,
-                                             const float* P, int r, int row0, int jg, float s, uint32_t sp,
-                                             unsigned& n_done) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w}, ov[4] = {o4.x, o4.y, o4.z, o4.w};
-  float dsq = 0.f;
-  uint32_t pending = __ballot_sync(0xFFFFFFFFu, emask != 0);
-  while (pending) {
-    const int src = __ffs(pending) - 1;
-    const uint32_t m_src = __shfl_sync(0xFFFFFFFFu, emask, src);
-    const int e = __ffs(m_src) - 1;
-    if (lane == src) emask &= emask - 1u;
-    const uint32_t ww = __shfl_sync(0xFFFFFFFFu, pick(wv, e >> 1), src);
-    const uint32_t rr = __shfl_sync(0xFFFFFFFFu, pick(rv, e >> 1), src);
-    const uint32_t oo = __shfl_sync(0xFFFFFFFFu, pick(ov, e >> 1), src);
-    const int sh = (e & 1) * 16;
-    const uint32_t w16 = (ww >> sh) & 0xFFFFu, r16 = (rr >> sh) & 0xFFFFu, o16 = (oo >> sh) & 0xFFFFu;
-    const float hx = warp_dot2(C + (int64_t)(row0 + src) * r, P + (int64_t)(jg + e) * r, r, lane);
-    const float v = fmaf(-s, hx, __uint_as_float(w16 << 16));
-    const uint32_t out = sr_bf16_bits(v, r16);
-    if (lane == src) {
-      tc::sts16(sp + 2 * e, (uint16_t)out);
-      const float fo = __uint_as_float(o16 << 16), fn = __uint_as_float(out << 16);
-      dsq = fmaf(fn, fn, fmaf(-fo, fo, dsq));
-      ++n_done;
-    }
-    pending = __ballot_sync(0xFFFFFFFFu, emask != 0);
-  }
-  return dsq;
-}
+// Exact-path tags: an element whose rounding margin the error bound might
+// cross keeps its original weight in W, and its lane's 8-column group gets a
+// 16-bit tag: the flagged elements as bits 0..7 (bit t: column 8g + t of the
+// warp's columns), the lane at bits 8..12, the group g at bits 13..15.  Each
+// (tile, epilogue warp) owns room for a tag per group of the tile and a count
+// byte; every other element of W holds the tensor-core result.
+constexpr int kFixCap = 128;  // 32 lanes x up to 4 groups
 
 // Byte offset in a W stage (NCOLS/64 boxes of 64 columns, 128-byte swizzled)
 // of the 8-column group of tile row q that starts at column col.
 __device__ __forceinline__ uint32_t w_stage_offset(int col, int q) {
   return (uint32_t)((col >> 6) * 16384 + q * 128 + ((((col & 63) >> 3) ^ (q & 7)) << 4));
-}
-
-// Groups that found their warp's queue slots full, redone in place once the
-// warp has finished the tile (the TMEM buffer is still its own): bit g of redo
-// is this lane's 8-column group g, whose original weights are back in the
-// stage.  For each such group the tensor-core results are formed again from H
-// in TMEM, exactly as in the main loop, written to the stage, and the elements
-// the margin test flags go through exact_in_place.  Returns the lane's sum of
-// squares of the redone groups.
-__device__ __forceinline__ float redo_in_place(const UpdBatch& a, uint32_t redo, int ngroups, uint32_t taddr,
-                                            uint32_t s_w32, int col_base, int q, int i, int j0, int k, uint32_t k8,
-                                            uint32_t layer, const float* C, const float* P, float s, float s_t,
-                                            float bound, int row0, bool need_norm, unsigned& n_done) {
-  float sq = 0.f;
-  for (int g = 0; g < ngroups; ++g) {
-    const bool mine = (redo >> g) & 1u;
-    if (!__any_sync(0xFFFFFFFFu, mine)) continue;
-    const int col = col_base + 8 * g;
-    const uint32_t sp = s_w32 + w_stage_offset(col, q);
-    uint32_t h[8];
-    tc::tmem_ld_32x32b_x8(taddr + 8 * g, h);
-    tc::tmem_wait_ld_regs<8>(h);
-    uint32_t emask = 0;
-    uint4 w4 = make_uint4(0, 0, 0, 0), r4 = w4, o4 = w4;
-    if (mine) {
-      w4 = tc::lds128(sp);
-      const uint32_t blk[1] = {(uint32_t)i * k8 + ((uint32_t)(j0 + col) >> 3)};
-      uint32_t rw[1][4];
-      philox4x32_10_rk_multi<1>(blk, a.step, layer, kTagSR, a.rk0, a.rk1, rw);
-      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-      uint32_t out[4];
-      float t = 0.f;
-#pragma unroll
-      for (int t2 = 0; t2 < 4; ++t2) {
-        const float2 v = ffma2(make_float2(-s_t, -s_t), make_float2(__uint_as_float(h[2 * t2]), __uint_as_float(h[2 * t2 + 1])),
-                               make_float2(__uint_as_float(wv[t2] << 16), __uint_as_float(wv[t2] & 0xFFFF0000u)));
-        const uint32_t s0 = __float_as_uint(v.x) + (rw[0][t2] & 0xFFFFu);
-        const uint32_t s1 = __float_as_uint(v.y) + (rw[0][t2] >> 16);
-        out[t2] = __byte_perm(s0, s1, 0x7632);
-        if (!(rounding_margin(s0, v.x) >= bound)) emask |= 1u << (2 * t2);
-        if (!(rounding_margin(s1, v.y) >= bound)) emask |= 2u << (2 * t2);
-        if (need_norm) t = sq_acc_bf16x2(out[t2], t);
-      }
-      if (j0 + col + 8 > k) emask &= (1u << (k - j0 - col)) - 1u;
-      tc::sts128(sp, make_uint4(out[0], out[1], out[2], out[3]));
-      r4 = make_uint4(rw[0][0], rw[0][1], rw[0][2], rw[0][3]);
-      o4 = make_uint4(out[0], out[1], out[2], out[3]);
-      sq += t;
-    }
-    const float dsq = exact_in_place(emask, w4, r4, o4, C, P, a.r, row0, j0 + col, s, sp, n_done);
-    if (need_norm) sq += dsq;
-  }
-  return sq;
 }
 
 // Persistent rebuild + update, one CTA per SM, each CTA a contiguous range of
@@ -577,15 +455,14 @@ __device__ __forceinline__ float redo_in_place(const UpdBatch& a, uint32_t redo,
 // fp32 rounding of the exact product.  The tensor-core H differs from it by at
 // most D = |s| (beta ||c_i|| ||p_j|| + 2^-24 |H|) with beta the split and
 // accumulation error of the part products.  Each element's rounding margin
-// (rounding_margin) is compared with that bound.  A lane's 8-column group
-// with an element whose margin might be crossed is queued, with its original
-// weights, in the warp's slots of the tile; exact_fix_kernel then recomputes
-// those elements, H_ij from a compensated dot product of the fp32 row of C and
-// the fp32 row of P (Dot2 of the paper above: as accurate as twice fp32
-// precision), and writes their results over the tensor-core ones.  A group
-// that finds the slots full is redone in place before the tile is stored
-// (redo_in_place).  Every other element's result is the one the definition
-// gives.
+// (rounding_margin) is compared with that bound.  An element whose margin
+// might be crossed keeps its original weight in W and its group is tagged
+// for the fix kernel; exact_fix_kernel then recomputes those elements, H_ij from a
+// compensated dot product of the fp32 row of C and the fp32 row of P (Dot2 of
+// the paper above: as accurate as twice fp32 precision), and writes their
+// results.  Every other element's result is the one the definition gives.
+// The kernel itself holds no exact-path arithmetic, which keeps its register
+// allocation to the streaming loop.
 template <int NCOLS>
 __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const __grid_constant__ UpdBatch a) {
   extern __shared__ uint8_t smem_raw[];
@@ -798,8 +675,9 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
     for (int g = 0; g < kGroups; ++g) {
       stage_off[g] = w_stage_offset(col_base + 8 * g, q);
     }
-    unsigned exact_n = 0;  // elements this lane recomputed exactly
     int it = 0;
+    int sw = 0;        // W stage of tile it: it % NSW, kept without a division
+    uint32_t wph = 0;  // its phase, (it / NSW) & 1
     for (int u = u_begin; u < u_end; ++u) {
       const Unit x = decode_unit(a, u);
       const int p = x.p;
@@ -818,7 +696,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       float sq = 0.f, sq_comp = 0.f;  // Kahan-compensated sum of squares
 
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
-        const int sw = it % NSW, b = it % kTmemBufs;
+        const int b = it % kTmemBufs;
         const int j0 = ct * NCOLS;
         // largest norm of the P rows of this warp's columns (for the margin
         // bound), loaded before the waits so that its latency hides behind them
@@ -828,7 +706,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           if (jc < k) pmax = a.p_norm[p][jc];
         }
         const float p_un = a.p_unscale[p][j0 / kSplitRows];
-        bool live = tc::mbar_wait(&wfull_bar[sw], (it / NSW) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad) &&
+        bool live = tc::mbar_wait(&wfull_bar[sw], wph, &abort_flag, a.err, tc::kErrTimeoutLoad) &&
                     tc::mbar_wait(&tfull_bar[b], (it / kTmemBufs) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
         live = __all_sync(0xFFFFFFFFu, live);
         tc::tc_fence_after();
@@ -843,13 +721,10 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         const float bound = scaled_ok ? bound_row * pmax : __int_as_float(0x7FC00000);  // 2^25 D
         const float2 ns2 = make_float2(-s_t, -s_t);
         // live is the same in the whole warp: one branch per tile
-        // this warp's slice of the layer's exact-path queue for this tile
-        const uint32_t tile = (uint32_t)x.rb * (uint32_t)a.n_ct[p] + (uint32_t)ct;
-        const size_t slot0 = ((size_t)tile * kEpiWarps + ew) * kFixSlots;
-        uint4* const slots = a.fix_entries[p] + slot0;
-        uint16_t* const tags = a.fix_tags[p] + slot0;
-        uint32_t used = 0;       // groups queued in the warp's slots (warp-uniform)
-        uint32_t redo_mask = 0;  // this lane's groups to redo in place
+        // this warp's entry of the layer's exact-path map for this tile
+        const size_t set = ((size_t)x.rb * (size_t)a.n_ct[p] + (size_t)ct) * kEpiWarps + ew;
+        uint32_t fmap = 0;   // this lane's flagged elements, a byte per group
+        uint32_t nflag = 0;  // the warp's flagged groups (warp-uniform)
         if (live) {
           const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col_base);
           float gs = 0.f;  // sum of squares of this tile's results (normalized SGD)
@@ -903,8 +778,9 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
               // smallest margin of the group; NaN if any is NaN
               const float gm = fmin3_nan(fmin3_nan(ym[0], ym[1], ym[2]), fmin3_nan(ym[3], ym[4], ym[5]),
                                          fmin_nan(ym[6], ym[7]));
-              const bool ok = row_ok && j0 + col < k;
-              const bool flag = ok && !(gm >= bound);
+              // rows past d hold v = 0 against a bound of 0 and pass; columns
+              // past k (the last tile of a row) may flag, and are masked below
+              const bool flag = !(gm >= bound);
               tc::sts128(sp, make_uint4(wout[0], wout[1], wout[2], wout[3]));
               float t = gs;
               if (need_norm) {
@@ -912,48 +788,54 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
                 for (int t2 = 0; t2 < 4; ++t2) t = sq_acc_bf16x2(wout[t2], t);
               }
               // Rare: a group with an element whose margin the bound might
-              // cross.  Its lane queues the group (original weights and the
-              // flagged elements) in this warp's slots for the fix kernel, or,
-              // with the slots full, puts the original weights back into the
-              // stage and redoes the group after the tile's last group.
-              bool redo = false;
+              // cross.  The flagged elements inside W keep their original
+              // weights in the stage (the fix kernel recomputes them from W)
+              // and go into the lane's map word.
               if (__any_sync(0xFFFFFFFFu, flag)) {
                 uint32_t emask = 0;
-                if (flag) {
+                if (flag && row_ok && j0 + col < k) {
 #pragma unroll
                   for (int e = 0; e < 8; ++e) emask |= (ym[e] >= bound) ? 0u : (1u << e);
                   if (j0 + col + 8 > k) emask &= (1u << (k - j0 - col)) - 1u;  // columns inside W
                 }
-                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, emask != 0);
-                const uint32_t pos = used + __popc(bal & ((1u << lane) - 1u));
                 if (emask != 0) {
-                  if (pos < kFixSlots) {
-                    slots[pos] = raw;
-                    tags[pos] = (uint16_t)(emask | ((uint32_t)lane << 8) | ((uint32_t)g << 13));
-                  } else {
-                    tc::sts128(sp, raw);
-                    redo_mask |= 1u << g;
-                    redo = true;
+                  uint32_t sel[4];
+                  t = gs;
+#pragma unroll
+                  for (int t2 = 0; t2 < 4; ++t2) {
+                    const uint32_t m = (((emask >> (2 * t2)) & 1u) ? 0x0000FFFFu : 0u) |
+                                       (((emask >> (2 * t2 + 1)) & 1u) ? 0xFFFF0000u : 0u);
+                    sel[t2] = (wout[t2] & ~m) | (win[t2] & m);
+                    if (need_norm) t = sq_acc_bf16x2(sel[t2], t);
                   }
+                  tc::sts128(sp, make_uint4(sel[0], sel[1], sel[2], sel[3]));
+                  fmap |= emask << (8 * g);
                 }
-                used += __popc(bal);
               }
-              if (ok && !redo) gs = t;
+              if (j0 + col < k) gs = t;
             }
           }
-          // groups that found the slots full
-          if (__any_sync(0xFFFFFFFFu, redo_mask != 0))
-            gs += redo_in_place(a, redo_mask, kGroups, taddr, s_w32, col_base, q, i, j0, k, k8, layer, a.C[p],
-                                a.P[p], s, s_t, bound, x.rb * 128 + quarter * 32, need_norm, exact_n);
-          if (need_norm) {  // the tile's squares into the compensated sum
+          // the tile's flagged groups into the warp's tag list, groups in order
+          // and lanes in order within a group
+          if (__any_sync(0xFFFFFFFFu, fmap != 0)) {
+            uint16_t* const tags = a.fix_tags[p] + set * kFixCap;
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g) {
+              const uint32_t em = (fmap >> (8 * g)) & 0xFFu;
+              const uint32_t bal = __ballot_sync(0xFFFFFFFFu, em != 0);
+              if (em != 0) tags[nflag + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)(em | ((uint32_t)lane << 8) | ((uint32_t)g << 13));
+              nflag += __popc(bal);
+            }
+          }
+          if (need_norm && row_ok) {  // the tile's squares into the compensated sum
             const float y = gs - sq_comp;
             const float tsum = sq + y;
             sq_comp = (tsum - sq) - y;
             sq = tsum;
           }
         }
-        // the slots this warp filled (every count is written on every call)
-        if (lane == 0) a.fix_counts[p][(size_t)tile * kEpiWarps + ew] = (uint8_t)(used < kFixSlots ? used : kFixSlots);
+        // the number of tags (written on every call)
+        if (lane == 0) a.fix_counts[p][set] = (uint8_t)nflag;
         // this warp is done with the TMEM buffer
         tc::tc_fence_before();
         __syncwarp();
@@ -963,6 +845,10 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sfull_bar[sw]);
+        if (++sw == NSW) {
+          sw = 0;
+          wph ^= 1u;
+        }
       }
       if (need_norm) {
         // ||W_new||^2 of this unit: each warp leaves its share in a shared
@@ -994,9 +880,6 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         }
       }
     }
-    for (int o = 16; o > 0; o >>= 1) exact_n += __shfl_xor_sync(0xFFFFFFFFu, exact_n, o);
-    if (lane == 0 && exact_n != 0 && a.exact_count != nullptr)
-      atomicAdd(a.exact_count, (unsigned long long)exact_n);
   }
   // SGD: every layer's status word reads 0 (written by the first CTA)
   if (blockIdx.x == 0) {
@@ -1112,7 +995,6 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
       a.unit_partials[i] = w.wnew_partials;
       a.ticket[i] = w.ticket;
       a.wnorm2_out[i] = normsgd ? pr.wnorm2_out : nullptr;
-      a.fix_entries[i] = w.fix_entries;
       a.fix_tags[i] = w.fix_tags;
       a.fix_counts[i] = w.fix_counts;
     }
@@ -1159,10 +1041,9 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
 // rounding, and writes the weight.  For normalized SGD it also carries the
 // change of ||W_new||^2: each element's change (new^2 - old^2, exact in
 // double) in fixed point relative to its layer's norm, summed as integers so
-// that the total does not depend on the order of the queue;
+// that the total does not depend on the order in which elements are fixed;
 // exact_fix_finalize_kernel adds each layer's total to its norm.
 struct FixBatch {
-  const uint4* entries[kMaxUpd];
   const uint16_t* tags[kMaxUpd];
   const uint8_t* counts[kMaxUpd];
   uint32_t* ticket[kMaxUpd];           // bit 31: a non-finite change
@@ -1188,7 +1069,7 @@ struct FixBatch {
 };
 constexpr int kFixFracBits = 40;  // fixed point: 2^-40 of the layer's norm
 constexpr int kFixThreads = 256;
-constexpr int kFixSetsPerLane = 4;  // slot sets whose counts each lane of the fix kernel reads
+constexpr int kFixSetsPerLane = 4;  // (tile, warp) flag bytes each lane of the fix kernel reads
 
 // Fixed-point scale of a layer's changes: ref (the tensor-core ||W_new||^2)
 // is at least every tensor-core square and an exact result is within a step
@@ -1237,17 +1118,39 @@ __device__ __forceinline__ float thread_dot2(const float* c, const float* p, int
   return __fadd_rn(hs, he);
 }
 
-// Each thread reads the counts of kFixSetsPerLane (tile, epilogue warp) slot
-// sets of a layer (blockIdx.y); the warp lists the used slots of its sets in
-// shared memory and deals them out one per lane, so that no lane works through
-// a full set while the others wait, and one wave of blocks covers the queue.  For each entry: the group's Philox block again and,
-// for each flagged element, H_ij by thread_dot2, then the same v and
-// stochastic rounding as the tensor-core path, written over the tensor-core
-// result in W.  The change of ||W_new||^2 goes, in fixed point relative to the
-// layer's norm, into an integer sum whose total does not depend on the order
-// of the queue; exact_fix_finalize_kernel adds it to the norm.
+// One flagged element: H_ij by thread_dot2, then the same v and stochastic
+// rounding as the tensor-core path from the original weight w16 (still in W),
+// the result written over it.  Returns whether the weight changed; the change
+// of ||W_new||^2 goes, in fixed point relative to the layer's norm, into an
+// integer sum whose total does not depend on the order of the elements.
+__device__ __forceinline__ void fix_element(const FixBatch& b, int p, uint16_t* wrow, const float* crow, int j,
+                                            uint32_t w16, uint32_t r16, float s, double* wn) {
+  const int r = b.r;
+  const float hx = thread_dot2(crow, b.P[p] + (int64_t)j * r, r);
+  const float v = fmaf(-s, hx, __uint_as_float(w16 << 16));
+  const uint32_t out = sr_bf16_bits(v, r16);
+  if (out == w16) return;
+  wrow[j] = (uint16_t)out;
+  if (wn == nullptr) return;
+  const double ref = *wn;
+  if (!isfinite(ref)) return;
+  const double fo = (double)__uint_as_float(w16 << 16), fn = (double)__uint_as_float(out << 16);
+  const double delta = fn * fn - fo * fo;  // exact: both squares have 16-bit mantissas
+  if (!isfinite(delta)) atomicOr(b.ticket[p], 0x80000000u);
+  else if (ref > 0.0) atomicAdd(b.acc[p], (unsigned long long)llrint(delta * fix_to_fixed(ref)));
+  else atomicAdd(reinterpret_cast<double*>(b.acc[p]), delta);
+}
+
+// Each thread reads the tag counts of kFixSetsPerLane (tile, epilogue warp)
+// sets of a layer (blockIdx.y); the warp keeps the running total of its sets'
+// counts in shared memory and deals the tags out one per lane (a lane finds
+// the set of its tag by binary search), so that no lane works through a full
+// set while the others wait.  For a tag: the group's Philox block and weights
+// (original ones where flagged) from W, then fix_element for each flagged
+// element.
 __global__ void __launch_bounds__(kFixThreads) exact_fix_kernel(const __grid_constant__ FixBatch b) {
-  __shared__ uint32_t slots[kFixThreads / 32][32 * kFixSetsPerLane * kFixSlots];
+  constexpr int kSets = 32 * kFixSetsPerLane;
+  __shared__ uint32_t pre[kFixThreads / 32][kSets];  // tags of the warp's sets before each set
   __shared__ unsigned block_done;
   const int p = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1257,74 +1160,60 @@ __global__ void __launch_bounds__(kFixThreads) exact_fix_kernel(const __grid_con
   const int64_t sets = (int64_t)b.tiles[p] * kEpiWarps;
   // this warp's sets: base + 32 q + lane for q < kFixSetsPerLane (each load a
   // coalesced run of 32 counts, all issued before any is used)
-  const int64_t base = ((int64_t)blockIdx.x * (kFixThreads / 32) + warp) * 32 * kFixSetsPerLane;
-  uint32_t cnt[kFixSetsPerLane], mine = 0;
+  const int64_t base = ((int64_t)blockIdx.x * (kFixThreads / 32) + warp) * kSets;
+  uint32_t cnt[kFixSetsPerLane];
 #pragma unroll
   for (int q = 0; q < kFixSetsPerLane; ++q) {
     const int64_t set = base + 32 * q + lane;
     cnt[q] = (!skipped && set < sets) ? b.counts[p][set] : 0u;
-    mine += cnt[q];
   }
-  // the warp's used slots, in lane order (slot index within the layer)
-  uint32_t incl = mine;
+  uint32_t total = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += v;
+  for (int q = 0; q < kFixSetsPerLane; ++q) {
+    uint32_t incl = cnt[q];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    pre[warp][32 * q + lane] = total + incl - cnt[q];
+    total += __shfl_sync(0xFFFFFFFFu, incl, 31);
   }
-  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-  uint32_t at = incl - mine;
-#pragma unroll
-  for (int q = 0; q < kFixSetsPerLane; ++q)
-    for (uint32_t e = 0; e < cnt[q]; ++e) slots[warp][at++] = (uint32_t)(base + 32 * q + lane) * kFixSlots + e;
   __syncwarp();
   unsigned done = 0;
   if (total != 0) {
     const int kcols = b.ncols / 4;
     const float s = b.scale_dev[p] ? *b.scale_dev[p] : b.scale_val;
-    const int r = b.r;
     const uint32_t k8 = (uint32_t)b.k[p] >> 3;
     double* wn = b.wnorm2_out[p];
     for (uint32_t idx = lane; idx < total; idx += 32) {
-      const uint32_t slot = slots[warp][idx];
-      const uint4 w4 = b.entries[p][slot];
-      const uint32_t tag = b.tags[p][slot];
-      const uint32_t sset = slot / kFixSlots;
+      // the last set whose tags start at or before idx (it holds tag idx)
+      int lo = 0;
+#pragma unroll
+      for (int step = kSets / 2; step > 0; step >>= 1)
+        if (pre[warp][lo + step] <= idx) lo += step;
+      const int64_t sset = base + lo;
+      const uint32_t tag = b.tags[p][sset * kFixCap + (idx - pre[warp][lo])];
       const int t = (int)(sset / kEpiWarps), ew = (int)(sset % kEpiWarps);
       const int rb = t / b.n_ct[p], ct = t % b.n_ct[p];
       const int i = rb * 128 + (ew & 3) * 32 + (int)((tag >> 8) & 31u);
       const int jg = ct * b.ncols + (ew >> 2) * kcols + 8 * (int)(tag >> 13);
       if (i >= b.d[p] || jg >= b.k[p]) continue;  // only after a timed-out update
       uint16_t* wrow = b.W[p] + (int64_t)i * b.ld_w[p];
-      // the group's tensor-core results, read before the dot products so that
-      // the load overlaps them (ld_w and jg are multiples of 8)
-      const uint4 o4 = *reinterpret_cast<const uint4*>(wrow + jg);
+      // the group's weights (ld_w and jg are multiples of 8), read before the
+      // dot products so that the load overlaps them
+      const uint4 w4 = *reinterpret_cast<const uint4*>(wrow + jg);
       const uint32_t blk[1] = {(uint32_t)i * k8 + ((uint32_t)jg >> 3)};
       uint32_t rw[1][4];
       philox4x32_10_rk_multi<1>(blk, b.step, b.layer[p], kTagSR, b.rk0, b.rk1, rw);
-      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w}, ov[4] = {o4.x, o4.y, o4.z, o4.w};
-      const float* crow = b.C[p] + (int64_t)i * r;
+      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+      const float* crow = b.C[p] + (int64_t)i * b.r;
       for (uint32_t m = tag & 0xFFu; m; m &= m - 1u) {
         const int e = __ffs(m) - 1;
-        const int j = jg + e;
         const int sh = (e & 1) * 16;
         const uint32_t w16 = (pick(wv, e >> 1) >> sh) & 0xFFFFu, r16 = (pick(rw[0], e >> 1) >> sh) & 0xFFFFu;
-        const uint32_t o16 = (pick(ov, e >> 1) >> sh) & 0xFFFFu;
-        const float hx = thread_dot2(crow, b.P[p] + (int64_t)j * r, r);
-        const float v = fmaf(-s, hx, __uint_as_float(w16 << 16));
-        const uint32_t out = sr_bf16_bits(v, r16);
+        fix_element(b, p, wrow, crow, jg + e, w16, r16, s, wn);
         ++done;
-        if (out == o16) continue;
-        wrow[j] = (uint16_t)out;
-        if (wn == nullptr) continue;
-        const double ref = *wn;
-        if (isfinite(ref)) {
-          const double fo = (double)__uint_as_float(o16 << 16), fn = (double)__uint_as_float(out << 16);
-          const double delta = fn * fn - fo * fo;  // exact: both squares have 16-bit mantissas
-          if (!isfinite(delta)) atomicOr(b.ticket[p], 0x80000000u);
-          else if (ref > 0.0) atomicAdd(b.acc[p], (unsigned long long)llrint(delta * fix_to_fixed(ref)));
-          else atomicAdd(reinterpret_cast<double*>(b.acc[p]), delta);
-        }
       }
     }
   }
@@ -1369,7 +1258,6 @@ cudaError_t launch_exact_fix(int n, const UpdateProblem* probs, const UpdateWork
     for (int i = 0; i < m; ++i) {
       const UpdateProblem& pr = probs[base + i];
       const UpdateWorkspace& w = ws[base + i];
-      f.entries[i] = w.fix_entries;
       f.tags[i] = w.fix_tags;
       f.counts[i] = w.fix_counts;
       f.layer[i] = pr.layer;
@@ -1470,13 +1358,12 @@ size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool n
   w.p_unscale = cur.take<float>((size_t)ceil_div(k, kSplitRows));
   w.c_split = cur.take<uint16_t>((size_t)d * 2 * r_pad);
   w.p_split = cur.take<uint16_t>((size_t)k * 2 * r_pad);
-  // exact-path queue: kFixSlots entries and a count per (tile, epilogue warp)
+  // exact-path tags: a count and kFixCap tags per (tile, epilogue warp)
   const int64_t tiles = ceil_div(d, 128) * ceil_div(k, update_ncols(r));
   w.fix_ticket = cur.take<uint32_t>(1);
   w.fix_acc = cur.take<unsigned long long>(1);
   w.fix_counts = cur.take<uint8_t>((size_t)tiles * kEpiWarps);
-  w.fix_tags = cur.take<uint16_t>((size_t)tiles * kEpiWarps * kFixSlots);
-  w.fix_entries = cur.take<uint4>((size_t)tiles * kEpiWarps * kFixSlots);
+  w.fix_tags = cur.take<uint16_t>((size_t)tiles * kEpiWarps * kFixCap);
   cur.take<char>(0);  // end on a 256-byte boundary
   if (ws) *ws = w;
   return cur.offset - start;

@@ -50,11 +50,10 @@ def test_workspace_sizes(lib):
     ws = binding.workspace_bytes
     # FP16 high/low parts of C and P, their fp32 row norms, the split's scales
     # (one per row of C, one per 128 rows of P: 32 floats in a 256-byte
-    # block), two 256-byte counters and the exact-path queue: per 128 x 128
-    # tile and epilogue warp a one-byte count and four slots of a 2-byte tag
-    # and 16 bytes of weights
+    # block), two 256-byte counters and the exact-path tags: per 128 x 128
+    # tile and epilogue warp a count byte and room for 128 2-byte tags
     tiles = 32 * 32
-    queue = tiles * 16 * (1 + 4 * (2 + 16))
+    queue = tiles * 16 * (1 + 128 * 2)
     assert ws(binding.OP_UPDATE_SGD, 0, 4096, 4096, 64) == (4 * (4096 + 4096) * 64 + 4 * (4096 + 4096)
                                                            + 4 * 4096 + 256 + 2 * 256 + queue)
     a = ws(binding.OP_UPDATE_NORMSGD, 0, 4096, 4096, 64)
