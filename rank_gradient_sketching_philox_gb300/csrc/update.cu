@@ -706,6 +706,16 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           if (jc < k) pmax = a.p_norm[p][jc];
         }
         const float p_un = a.p_unscale[p][j0 / kSplitRows];
+        // the Philox words of this warp's groups: element index e = i*k + j
+        // (j a multiple of 8) gives block e / 8.  They need no tile data, so
+        // they are formed before the waits, the groups' chains interleaved.
+        uint32_t rw[kGroups][4];
+        {
+          uint32_t blks[kGroups];
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) blks[g] = (uint32_t)i * k8 + ((uint32_t)(j0 + col_base + 8 * g) >> 3);
+          philox4x32_10_rk_multi<kGroups>(blks, a.step, layer, kTagSR, a.rk0, a.rk1, rw);
+        }
         bool live = tc::mbar_wait(&wfull_bar[sw], wph, &abort_flag, a.err, tc::kErrTimeoutLoad) &&
                     tc::mbar_wait(&tfull_bar[b], (it / kTmemBufs) & 1, &abort_flag, a.err, tc::kErrTimeoutMma);
         live = __all_sync(0xFFFFFFFFu, live);
@@ -728,19 +738,11 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         if (live) {
           const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NCOLS + col_base);
           float gs = 0.f;  // sum of squares of this tile's results (normalized SGD)
-          // 16 columns (two 8-column groups) at a time: their H from TMEM, and
-          // the Philox blocks of element index e = i*k + j (j a multiple of 8):
-          // e / 8, computed while the TMEM load completes
+          // 16 columns (two 8-column groups) at a time: their H from TMEM
 #pragma unroll
           for (int hf = 0; hf < kGroups / 2; ++hf) {
             uint32_t h[16];
             tc::tmem_ld_32x32b<16>(taddr + 16 * hf, h);
-            uint32_t blks[2];
-#pragma unroll
-            for (int gg = 0; gg < 2; ++gg)
-              blks[gg] = (uint32_t)i * k8 + ((uint32_t)(j0 + col_base + 16 * hf + 8 * gg) >> 3);
-            uint32_t rw[2][4];
-            philox4x32_10_rk_multi<2>(blks, a.step, layer, kTagSR, a.rk0, a.rk1, rw);
             tc::tmem_wait_ld_regs<16>(h);
 #pragma unroll
             for (int gg = 0; gg < 2; ++gg) {
@@ -761,7 +763,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
               // r_lo = r - r_hi * 2^16 = r & 0xFFFF.
 #pragma unroll
               for (int t2 = 0; t2 < 4; ++t2) {
-                const uint32_t wword = win[t2], rword = rw[gg][t2];
+                const uint32_t wword = win[t2], rword = rw[g][t2];
                 const float2 v = ffma2(ns2,
                                        make_float2(__uint_as_float(h[8 * gg + 2 * t2]),
                                                    __uint_as_float(h[8 * gg + 2 * t2 + 1])),
