@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kAccThreads, 1) acc_persistent_kernel(const __
 // contiguous K ranges (as many as TMEM holds: up to 4), added in a fixed order
 // by the epilogue; a long single chain (192 chunks for k = 12288) would leave
 // XP measurably less accurate than the split over a cluster does.
-template <int NB>
+template <int NB, int CB>
 __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const __grid_constant__ SkinnyBatch a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -485,33 +485,49 @@ __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const _
   if (warp == 0 && lane == 0) {
     // ---- producer: TMA ring over the items' chunks ----
     int it = 0;
+    int s = 0;        // stage of chunk it: it % stages, kept without a division
+    uint32_t ph = 0;  // (it / stages) & 1
     bool stop = false;
     for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
       int p, m0;
       decode(item, p, m0);
       const CUtensorMap* tmA = &a.tmA[p];
       const CUtensorMap* tmB = &a.tmB[p];
-      for (int c = 0; c < a.kchunks[p]; ++c, ++it) {
-        const int s = it % a.stages, u = it / a.stages;
-        if (u > 0 && !tc::mbar_wait(&empty_bar[s], (u - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+      const int nst = (a.kchunks[p] + CB - 1) / CB;  // stages of CB chunks
+      for (int c = 0; c < nst; ++c, ++it) {
+        if (it >= a.stages && !tc::mbar_wait(&empty_bar[s], ph ^ 1u, &abort_flag, a.err, tc::kErrTimeoutStage)) {
           stop = true;
           break;
         }
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         tc::mbar_arrive_expect_tx(&full_bar[s], a.stage_bytes);
-        const int kc = c * kChunk;
-        tc::tma_load_2d(st, tmA, &full_bar[s], kc, m0);  // X: [128 tokens][64 k] (past M: zeros)
+        // X: CB boxes of [128 tokens][64 k] (past M or K: zeros), then for
+        // each part nb of the P^T split its CB boxes of [n_pad rank rows][64 k]
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb)  // P^T split: [n_pad rank rows][64 k] of part nb
-          tc::tma_load_2d(st + a.a_bytes + nb * a.b_bytes, tmB, &full_bar[s], kc, nb * a.n_pad);
+        for (int bx = 0; bx < CB; ++bx) {
+          const int kc = (c * CB + bx) * kChunk;
+          tc::tma_load_2d(st + bx * a.a_bytes, tmA, &full_bar[s], kc, m0);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+            tc::tma_load_2d(st + CB * a.a_bytes + (nb * CB + bx) * a.b_bytes, tmB, &full_bar[s], kc, nb * a.n_pad);
+        }
         issued = it + 1;
+        if (++s == a.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
+    // This one thread paces the kernel: per chunk it only waits, forms two
+    // descriptors and issues the MMAs (no divisions; the partial accumulator
+    // of each chunk follows from running boundaries)
     const uint32_t idesc = tc::idesc_bf16(128, a.n_pad, false, false);
     const int nbuf = a.acc_bufs, kp = a.k_parts;
     int it = 0, j = 0;
+    int s = 0;        // stage of chunk it and its phase, as in the producer
+    uint32_t ph = 0;
     bool stop = false;
     for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x, ++j) {
       int p, m0;
@@ -520,32 +536,50 @@ __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const _
       if (use >= 1 && !tc::mbar_wait(&tempty_bar[b], (use - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))
         break;
       tc::tc_fence_after();
-      const int kc = a.kchunks[p];
+      const int kc = (a.kchunks[p] + CB - 1) / CB;  // stages of the item
+      // partial accumulators: contiguous K ranges over min(k_parts, stages)
+      // partials, part q starting at stage ceil(q kc / kpe)
+      const int kpe = kc < kp ? kc : kp;
+      int part = 0, next = (kc + kpe - 1) / kpe;
+      bool first = true;
       for (int c = 0; c < kc; ++c, ++it) {
-        const int s = it % a.stages, u = it / a.stages;
-        if (!tc::mbar_wait(&full_bar[s], u & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) {
+        if (c == next) {
+          ++part;
+          next = ((part + 1) * kc + kpe - 1) / kpe;
+          first = true;
+        }
+        if (!tc::mbar_wait(&full_bar[s], ph, &abort_flag, a.err, tc::kErrTimeoutLoad)) {
           stop = true;
           break;
         }
         tc::tc_fence_after();
         const uint32_t sa = tc::smem_u32(smem + (size_t)s * a.stage_bytes);
-        // partial accumulator of this chunk: contiguous K ranges over the
-        // min(k_parts, chunks) partials, each receiving at least one chunk
-        const int kpe = kc < kp ? kc : kp;
-        const int part = (int)((int64_t)c * kpe / kc);
-        const bool first = c == (int)(((int64_t)part * kc + kpe - 1) / kpe);
         const uint32_t acc0 = tmem + (uint32_t)((b * kp + part) * a.n_pad);
+        // descriptors of the stage's operands; each 16-wide K step adds 32
+        // bytes (2 in the descriptor's address field), each box its size
+        const uint64_t ad0 = tc::sdesc_sw128(sa, 16, 1024);
+        uint64_t bd0[NB];
 #pragma unroll
-        for (int kk = 0; kk < kChunk / 16; ++kk) {
-          const uint64_t ad = tc::sdesc_sw128(sa + kk * 32, 16, 1024);
+        for (int nb = 0; nb < NB; ++nb)
+          bd0[nb] = tc::sdesc_sw128(sa + CB * a.a_bytes + nb * CB * a.b_bytes, 16, 1024);
+        const uint32_t a_step = a.a_bytes >> 4, b_step = a.b_bytes >> 4;
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            const uint64_t bd = tc::sdesc_sw128(sa + a.a_bytes + nb * a.b_bytes + kk * 32, 16, 1024);
-            tc::mma_bf16(acc0, ad, bd, idesc, (!first || kk > 0 || nb > 0) ? 1u : 0u);
+        for (int bx = 0; bx < CB; ++bx) {
+#pragma unroll
+          for (int kk = 0; kk < kChunk / 16; ++kk) {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+              tc::mma_bf16(acc0, ad0 + bx * a_step + 2u * kk, bd0[nb] + bx * b_step + 2u * kk, idesc,
+                           (!first || bx > 0 || kk > 0 || nb > 0) ? 1u : 0u);
           }
         }
         tc::mma_commit(&empty_bar[s]);
         consumed = it + 1;
+        first = false;
+        if (++s == a.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (!stop) tc::mma_commit(&tfull_bar[b]);
     }
@@ -565,7 +599,8 @@ __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const _
       tc::tc_fence_after();
       const int64_t grow = (int64_t)m0 + q;
       uint16_t* row = static_cast<uint16_t*>(a.out[p]) + grow * a.ld_out[p];
-      const int nparts = a.kchunks[p] < kp ? a.kchunks[p] : kp;  // partials that received chunks
+      const int nst = (a.kchunks[p] + CB - 1) / CB;
+      const int nparts = nst < kp ? nst : kp;  // partials that received stages
       for (int cg = 0; cg < ncols32; ++cg) {
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(cg * 32);
         uint32_t v[32];
@@ -769,7 +804,11 @@ cudaError_t launch_acc_persistent(SkinnyBatch& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_proj_persistent(SkinnyBatch& a, cudaStream_t stream) {
-  a.stage_bytes = a.a_bytes + 2 * a.b_bytes;
+  // two 64-wide K chunks per stage (longer runs of each token row of X, half
+  // the per-stage work of the issuing threads) where three such stages fit
+  const uint32_t one = a.a_bytes + 2 * a.b_bytes;
+  const int cb = (3 * 2 * one <= 200u * 1024u) ? 2 : 1;
+  a.stage_bytes = cb * one;
   int stages = (int)((200u * 1024u) / a.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return cudaErrorInvalidConfiguration;
@@ -785,7 +824,7 @@ cudaError_t launch_proj_persistent(SkinnyBatch& a, cudaStream_t stream) {
   }
   a.tmem_cols = tmem_cols_for(a.acc_bufs * a.k_parts * a.n_pad);
   const size_t smem = (size_t)stages * a.stage_bytes + 1024;
-  auto kernel = proj_persistent_kernel<2>;
+  auto kernel = cb == 2 ? proj_persistent_kernel<2, 2> : proj_persistent_kernel<2, 1>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int items = a.tile_begin[a.n];
@@ -917,14 +956,13 @@ cudaError_t launch_project_inputs(int n, const ProjectProblem* probs, int r, voi
     a.out_mode = xp_split ? 3 : 0;
     a.b_col_off = 0;
     a.err = errw;
-    // wide ranks (a stage of more than 48 KB, one CTA per SM) with enough
-    // token tiles to keep every SM busy: persistent CTAs, each tile over all
-    // of K, the next tile's loads overlapping this one's epilogue (measured:
-    // 20% faster at rank 192); narrower ranks run two split-K CTAs per SM,
-    // which streamed X faster than one persistent CTA did (0.88 against 0.54
-    // of HBM at rank 64)
-    err = (n_pad > 128 && a.tile_begin[m] >= 2 * num_sms()) ? launch_proj_persistent(a, stream)
-                                                             : launch_skinny<false, false, 2>(a, stream);
+    // enough token tiles to keep every SM busy: persistent CTAs, each tile
+    // over all of K, the next tile's loads overlapping this one's epilogue
+    // (measured against two split-K CTAs per SM on 36 layers of 4096 tokens:
+    // 0.79 against 0.72 of HBM at rank 64, k = 4096; 0.66 against 0.57 at
+    // rank 128); fewer tiles: split-K CTAs over a cluster
+    err = (a.tile_begin[m] >= 2 * num_sms()) ? launch_proj_persistent(a, stream)
+                                              : launch_skinny<false, false, 2>(a, stream);
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();

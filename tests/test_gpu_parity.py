@@ -180,14 +180,16 @@ def test_project_inputs_full_size_sampled_tokens(T, k, r, kind):
 
 
 @pytest.mark.parametrize("r,m,k", [(64, 1, 1024), (20, 1, 1024), (64, 3, 1024), (136, 1, 1024), (72, 3, 1024),
-                                   (48, 3, 128)])
+                                   (48, 3, 128), (64, 1, 1088), (64, 1, 1000), (32, 1, 64), (40, 2, 200)])
 def test_project_inputs_persistent_batch_matches_oracle(r, m, k):
-    """Large batches (3 layers x 16384 tokens): ranks above 128 run persistent
-    CTAs (each tile over all of K), the others split-K CTAs; single layers of
-    rank 64, 20 and 136 (ragged last column groups) and groups of three members
-    at rank 192 and 216; sampled tokens against the oracle, and the BF16 pair
-    form against the exact product; k = 128 gives two K chunks, fewer than
-    the four partial accumulators a tile may use."""
+    """Large batches (3 layers x 16384 tokens) run persistent CTAs, each tile
+    over all of K: single layers of rank 64, 20 and 136 (ragged last column
+    groups) and groups of two or three members; sampled tokens against the
+    oracle, and the BF16 pair form against the exact product.  Ranks up to 64
+    stage two 64-wide K chunks at a time: k = 1088 and 64 leave the last
+    stage's second chunk wholly past K, k = 1000 and 200 end inside a chunk;
+    k = 128 gives two K chunks, fewer than the four partial accumulators a
+    tile may use."""
     T, n = 16384, 3
     Xs = [synth.layer_x(T, k, i, 0, device=DEV) for i in range(n)]
     sample = orc.sample_qr if 4 * r <= k else orc.sample_rademacher
