@@ -114,9 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_gemm_kernel(const __grid_c
 
   if (warp == 0 && lane == 0) {
     // ---- producer: TMA ring ----
+    int s = 0;        // stage of chunk i: i % stages, kept without a division
+    uint32_t ph = 0;  // (i / stages) & 1
     for (int i = 0; i < nmine; ++i) {
-      const int s = i % a.stages, u = i / a.stages;
-      if (u > 0 && !tc::mbar_wait(&empty_bar[s], (u - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage))
+      if (i >= a.stages && !tc::mbar_wait(&empty_bar[s], ph ^ 1u, &abort_flag, a.err, tc::kErrTimeoutStage))
         break;
       uint8_t* st = smem + (size_t)s * a.stage_bytes;
       tc::mbar_arrive_expect_tx(&full_bar[s], a.stage_bytes);
@@ -138,13 +139,18 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_gemm_kernel(const __grid_c
         }
       }
       issued = i + 1;
+      if (++s == a.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     const uint32_t idesc = tc::idesc_bf16(128, a.n_pad, A_MN, B_MN);
+    int s = 0;        // as in the producer
+    uint32_t ph = 0;
     for (int i = 0; i < nmine; ++i) {
-      const int s = i % a.stages, u = i / a.stages;
-      if (!tc::mbar_wait(&full_bar[s], u & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) break;
+      if (!tc::mbar_wait(&full_bar[s], ph, &abort_flag, a.err, tc::kErrTimeoutLoad)) break;
       tc::tc_fence_after();
       const uint32_t sa = tc::smem_u32(smem + (size_t)s * a.stage_bytes);
 #pragma unroll
@@ -161,6 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_gemm_kernel(const __grid_c
       }
       tc::mma_commit(&empty_bar[s]);
       consumed = i + 1;
+      if (++s == a.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     if (nmine > 0) tc::mma_commit(&acc_bar);
   }
@@ -295,6 +305,8 @@ __global__ void __launch_bounds__(kAccThreads, 1) acc_persistent_kernel(const __
   if (warp == 0 && lane == 0) {
     // ---- producer: TMA ring over the items' chunks ----
     int it = 0;
+    int s = 0;        // stage of chunk it: it % stages, kept without a division
+    uint32_t ph = 0;  // (it / stages) & 1
     bool stop = false;
     for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
       int p, m0;
@@ -302,8 +314,7 @@ __global__ void __launch_bounds__(kAccThreads, 1) acc_persistent_kernel(const __
       const CUtensorMap* tmA = &a.tmA[p];
       const CUtensorMap* tmB = &a.tmB[p];
       for (int c = 0; c < a.kchunks[p]; ++c, ++it) {
-        const int s = it % a.stages, u = it / a.stages;
-        if (u > 0 && !tc::mbar_wait(&empty_bar[s], (u - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+        if (it >= a.stages && !tc::mbar_wait(&empty_bar[s], ph ^ 1u, &abort_flag, a.err, tc::kErrTimeoutStage)) {
           stop = true;
           break;
         }
@@ -322,12 +333,18 @@ __global__ void __launch_bounds__(kAccThreads, 1) acc_persistent_kernel(const __
             tc::tma_load_2d(bt + j * 8192, tmB, &full_bar[s], nb * a.b_col_off + j * 64, kc);
         }
         issued = it + 1;
+        if (++s == a.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
     const uint32_t idesc = tc::idesc_bf16(128, a.n_pad, true, true);
     int it = 0, j = 0;
+    int s = 0;        // stage of chunk it and its phase, as in the producer
+    uint32_t ph = 0;
     bool stop = false;
     for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x, ++j) {
       int p, m0;
@@ -338,8 +355,7 @@ __global__ void __launch_bounds__(kAccThreads, 1) acc_persistent_kernel(const __
       tc::tc_fence_after();
       const uint32_t acc0 = tmem + (uint32_t)b * acc_cols;
       for (int c = 0; c < a.kchunks[p]; ++c, ++it) {
-        const int s = it % a.stages, u = it / a.stages;
-        if (!tc::mbar_wait(&full_bar[s], u & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) {
+        if (!tc::mbar_wait(&full_bar[s], ph, &abort_flag, a.err, tc::kErrTimeoutLoad)) {
           stop = true;
           break;
         }
@@ -359,6 +375,10 @@ __global__ void __launch_bounds__(kAccThreads, 1) acc_persistent_kernel(const __
         }
         tc::mma_commit(&empty_bar[s]);
         consumed = it + 1;
+        if (++s == a.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (!stop) tc::mma_commit(&tfull_bar[b]);
     }
