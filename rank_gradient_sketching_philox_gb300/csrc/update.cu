@@ -525,6 +525,8 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
   if (warp == 0 && lane == 0) {
     // ---------------- producer ----------------
     int it = 0, cl = 0, prev_p = -1, prev_rb = -1;
+    int sw = 0, sp = 0, ip = 0;     // W stage of tile it, P stage of chunk ip (kept without divisions)
+    uint32_t wph = 0, pph = 0;      // their phases
     bool stop = false;
     for (int u = u_begin; u < u_end && !stop; ++u) {
       const Unit x = decode_unit(a, u);
@@ -543,8 +545,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
       for (int ct = x.ct0; ct < x.ct1; ++ct, ++it) {
         const int j0 = ct * NCOLS;
         // W tile first: it comes from HBM and is waited on longest
-        const int sw = it % NSW;
-        if (it >= NSW && !tc::mbar_wait(&wempty_bar[sw], ((it / NSW) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+        if (it >= NSW && !tc::mbar_wait(&wempty_bar[sw], wph ^ 1u, &abort_flag, a.err, tc::kErrTimeoutStage)) {
           stop = true;
           break;
         }
@@ -555,9 +556,8 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           tc::tma_load_2d(wst + bx * 16384, &a.tm_w[x.p], &wfull_bar[sw], j0 + 64 * bx, i0);
         // P: one stage per 64-wide chunk of r (both parts), so that wide
         // ranks keep two or more chunks in flight
-        for (int c = 0; c < a.kchunks && !stop; ++c) {
-          const int ip = it * a.kchunks + c, sp = ip % NSP;
-          if (ip >= NSP && !tc::mbar_wait(&pempty_bar[sp], ((ip / NSP) - 1) & 1, &abort_flag, a.err, tc::kErrTimeoutStage)) {
+        for (int c = 0; c < a.kchunks && !stop; ++c, ++ip) {
+          if (ip >= NSP && !tc::mbar_wait(&pempty_bar[sp], pph ^ 1u, &abort_flag, a.err, tc::kErrTimeoutStage)) {
             stop = true;
             break;
           }
@@ -565,14 +565,24 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
           tc::mbar_arrive_expect_tx(&pfull_bar[sp], a.parts * a.b_bytes);
           for (int q2 = 0; q2 < a.parts; ++q2)
             tc::tma_load_2d(pst + q2 * a.b_bytes, &a.tm_p[x.p], &pfull_bar[sp], q2 * a.r_pad + c * 64, j0);
+          if (++sp == NSP) {
+            sp = 0;
+            pph ^= 1u;
+          }
         }
         if (stop) break;
+        if (++sw == NSW) {
+          sw = 0;
+          wph ^= 1u;
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     const uint32_t idesc = tc::idesc_f16(128, NCOLS, false, false);
     int it = 0, cl = 0, prev_p = -1, prev_rb = -1;
+    int sp = 0;        // P stage of the next chunk and its phase, as in the producer
+    uint32_t pph = 0;
     bool stop = false;
     for (int u = u_begin; u < u_end && !stop; ++u) {
       const Unit x = decode_unit(a, u);
@@ -597,8 +607,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
         constexpr int kPairA[3] = {0, 0, 1}, kPairB[3] = {0, 1, 0};
         uint32_t acc = 0;
         for (int c = 0; c < a.kchunks; ++c) {
-          const int ip = it * a.kchunks + c, sp = ip % NSP;
-          if (!tc::mbar_wait(&pfull_bar[sp], (ip / NSP) & 1, &abort_flag, a.err, tc::kErrTimeoutLoad)) {
+          if (!tc::mbar_wait(&pfull_bar[sp], pph, &abort_flag, a.err, tc::kErrTimeoutLoad)) {
             stop = true;
             break;
           }
@@ -615,6 +624,10 @@ __global__ void __launch_bounds__(kUpdThreads, 1) update_persistent_kernel(const
             }
           }
           tc::mma_commit(&pempty_bar[sp]);
+          if (++sp == NSP) {
+            sp = 0;
+            pph ^= 1u;
+          }
         }
         if (stop) break;
         tc::mma_commit(&tfull_bar[b]);
