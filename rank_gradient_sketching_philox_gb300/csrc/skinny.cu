@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kAccThreads, 1) acc_persistent_kernel(const __
 // contiguous K ranges (as many as TMEM holds: up to 4), added in a fixed order
 // by the epilogue; a long single chain (192 chunks for k = 12288) would leave
 // XP measurably less accurate than the split over a cluster does.
-template <int NB, int CB>
+template <int NB, int CB, bool STACK>
 __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const __grid_constant__ SkinnyBatch a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -521,15 +521,16 @@ __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const _
         }
         uint8_t* st = smem + (size_t)s * a.stage_bytes;
         tc::mbar_arrive_expect_tx(&full_bar[s], a.stage_bytes);
-        // X: CB boxes of [128 tokens][64 k] (past M or K: zeros), then for
-        // each part nb of the P^T split its CB boxes of [n_pad rank rows][64 k]
+        // X: CB boxes of [128 tokens][64 k] (past M or K: zeros), then per
+        // box the parts of the P^T split, [n_pad rank rows][64 k] each, side by
+        // side (so that STACK reads both parts as one operand of 2 n_pad rows)
 #pragma unroll
         for (int bx = 0; bx < CB; ++bx) {
           const int kc = (c * CB + bx) * kChunk;
           tc::tma_load_2d(st + bx * a.a_bytes, tmA, &full_bar[s], kc, m0);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
-            tc::tma_load_2d(st + CB * a.a_bytes + (nb * CB + bx) * a.b_bytes, tmB, &full_bar[s], kc, nb * a.n_pad);
+            tc::tma_load_2d(st + CB * a.a_bytes + (bx * NB + nb) * a.b_bytes, tmB, &full_bar[s], kc, nb * a.n_pad);
         }
         issued = it + 1;
         if (++s == a.stages) {
@@ -543,7 +544,11 @@ __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const _
     // This one thread paces the kernel: per chunk it only waits, forms two
     // descriptors and issues the MMAs (no divisions; the partial accumulator
     // of each chunk follows from running boundaries)
-    const uint32_t idesc = tc::idesc_bf16(128, a.n_pad, false, false);
+    // STACK: one MMA per K step against both parts at once (N = 2 n_pad),
+    // the parts' products in adjacent accumulator columns; else one MMA per
+    // part into the same accumulator
+    const int acc_n = STACK ? NB * a.n_pad : a.n_pad;
+    const uint32_t idesc = tc::idesc_bf16(128, acc_n, false, false);
     const int nbuf = a.acc_bufs, kp = a.k_parts;
     int it = 0, j = 0;
     int s = 0;        // stage of chunk it and its phase, as in the producer
@@ -574,23 +579,27 @@ __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const _
         }
         tc::tc_fence_after();
         const uint32_t sa = tc::smem_u32(smem + (size_t)s * a.stage_bytes);
-        const uint32_t acc0 = tmem + (uint32_t)((b * kp + part) * a.n_pad);
+        const uint32_t acc0 = tmem + (uint32_t)((b * kp + part) * acc_n);
         // descriptors of the stage's operands; each 16-wide K step adds 32
         // bytes (2 in the descriptor's address field), each box its size
         const uint64_t ad0 = tc::sdesc_sw128(sa, 16, 1024);
         uint64_t bd0[NB];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-          bd0[nb] = tc::sdesc_sw128(sa + CB * a.a_bytes + nb * CB * a.b_bytes, 16, 1024);
-        const uint32_t a_step = a.a_bytes >> 4, b_step = a.b_bytes >> 4;
+        for (int nb = 0; nb < NB; ++nb) bd0[nb] = tc::sdesc_sw128(sa + CB * a.a_bytes + nb * a.b_bytes, 16, 1024);
+        const uint32_t a_step = a.a_bytes >> 4, b_step = (NB * a.b_bytes) >> 4;
 #pragma unroll
         for (int bx = 0; bx < CB; ++bx) {
 #pragma unroll
           for (int kk = 0; kk < kChunk / 16; ++kk) {
+            if (STACK) {
+              tc::mma_bf16(acc0, ad0 + bx * a_step + 2u * kk, bd0[0] + bx * b_step + 2u * kk, idesc,
+                           (!first || bx > 0 || kk > 0) ? 1u : 0u);
+            } else {
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-              tc::mma_bf16(acc0, ad0 + bx * a_step + 2u * kk, bd0[nb] + bx * b_step + 2u * kk, idesc,
-                           (!first || bx > 0 || kk > 0 || nb > 0) ? 1u : 0u);
+              for (int nb = 0; nb < NB; ++nb)
+                tc::mma_bf16(acc0, ad0 + bx * a_step + 2u * kk, bd0[nb] + bx * b_step + 2u * kk, idesc,
+                             (!first || bx > 0 || kk > 0 || nb > 0) ? 1u : 0u);
+            }
           }
         }
         tc::mma_commit(&empty_bar[s]);
@@ -621,17 +630,22 @@ __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const _
       uint16_t* row = static_cast<uint16_t*>(a.out[p]) + grow * a.ld_out[p];
       const int nst = (a.kchunks[p] + CB - 1) / CB;
       const int nparts = nst < kp ? nst : kp;  // partials that received stages
+      const int acc_n = STACK ? NB * a.n_pad : a.n_pad;
       for (int cg = 0; cg < ncols32; ++cg) {
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(cg * 32);
         uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)(b * kp * a.n_pad), v);
+        tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)(b * kp * acc_n), v);
         tc::tmem_wait_ld();
-        for (int pt = 1; pt < nparts; ++pt) {  // the partials in K order
-          uint32_t w[32];
-          tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)((b * kp + pt) * a.n_pad), w);
-          tc::tmem_wait_ld();
+        // the partials in K order; with STACK each partial's part products
+        // (columns c and n_pad + c) in part order
+        for (int pt = 0; pt < nparts; ++pt) {
+          for (int nb = (pt == 0 ? 1 : 0); nb < (STACK ? NB : 1); ++nb) {
+            uint32_t w[32];
+            tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)((b * kp + pt) * acc_n + nb * a.n_pad), w);
+            tc::tmem_wait_ld();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(w[t]));
+            for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(w[t]));
+          }
         }
         if (grow >= a.M[p]) continue;
         const int c0 = cg * 32;
@@ -828,23 +842,30 @@ cudaError_t launch_proj_persistent(SkinnyBatch& a, cudaStream_t stream) {
   // the per-stage work of the issuing threads) where three such stages fit
   const uint32_t one = a.a_bytes + 2 * a.b_bytes;
   const int cb = (3 * 2 * one <= 200u * 1024u) ? 2 : 1;
+  // both parts of the split in one MMA (N = 2 n_pad): half the MMA
+  // instructions.  Up to rank 64 this keeps two tiles of accumulators in
+  // TMEM; above, the wider accumulators would leave room for one tile only,
+  // which measured slower than twice the MMAs (rank 128: 0.66 against 0.67 of HBM)
+  const bool stack = a.n_pad <= 64;
+  const int acc_n = stack ? 2 * a.n_pad : a.n_pad;
   a.stage_bytes = cb * one;
   int stages = (int)((200u * 1024u) / a.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return cudaErrorInvalidConfiguration;
   a.stages = stages;
   // partial accumulators: up to 4 per tile, two tiles in flight where TMEM
-  // holds them, else one
+  // holds them, else one tile of two
   a.acc_bufs = 2;
   a.k_parts = 4;
-  while (a.k_parts > 1 && a.acc_bufs * a.k_parts * a.n_pad > 512) a.k_parts >>= 1;
-  if (a.k_parts == 1 && 2 * a.n_pad <= 512) {
+  while (a.k_parts > 1 && a.acc_bufs * a.k_parts * acc_n > 512) a.k_parts >>= 1;
+  if (a.k_parts == 1) {
     a.acc_bufs = 1;
     a.k_parts = 2;
   }
-  a.tmem_cols = tmem_cols_for(a.acc_bufs * a.k_parts * a.n_pad);
+  a.tmem_cols = tmem_cols_for(a.acc_bufs * a.k_parts * acc_n);
   const size_t smem = (size_t)stages * a.stage_bytes + 1024;
-  auto kernel = cb == 2 ? proj_persistent_kernel<2, 2> : proj_persistent_kernel<2, 1>;
+  auto kernel = stack ? (cb == 2 ? proj_persistent_kernel<2, 2, true> : proj_persistent_kernel<2, 1, true>)
+                      : (cb == 2 ? proj_persistent_kernel<2, 2, false> : proj_persistent_kernel<2, 1, false>);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int items = a.tile_begin[a.n];
