@@ -106,13 +106,14 @@ def resolve(args):
 
 
 # DRAM bytes (read + write) per algorithmic byte of each phase's main kernel, from
-# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
-# over one Qwen3-8B block (7 linears, one 4096-token microbatch, every layer's
-# inputs its own): the persistent accumulation 340.3 MB against 342.4 MB, the
-# three grouped projection launches 214.2 MB against 214.4 MB.  Traffic grows
-# with the units processed, so a full launch's traffic is this ratio times its
-# algorithmic bytes.
-TRAFFIC_PER_ALGORITHMIC_BYTE = {"accumulate": 340.27 / 342.36, "project_inputs": 214.19 / 214.4}
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of ten Qwen3-8B
+# blocks (70 linears, one 4096-token microbatch, every layer's inputs its own:
+# launches as large as the full stack's, so the same kernels run): the persistent
+# accumulation 3329.1 MB against 3423.6 MB (XP and part of C still in L2 from the
+# projection), the three persistent projection launches 2176.9 MB against
+# 2144.3 MB.  Traffic grows with the units processed, so a full launch's traffic
+# is this ratio times its algorithmic bytes.
+TRAFFIC_PER_ALGORITHMIC_BYTE = {"accumulate": 3329.14 / 3423.60, "project_inputs": 2176.94 / 2144.34}
 
 
 def measured_peaks():
@@ -650,8 +651,8 @@ def main():
         "bytes_per_launch": bytes_ / nl,
         "avg_launch_ms": secs / nl * 1e3,
         "traffic": ratio * bytes_ / nl if ratio is not None else None,
-        "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the kernel on one "
-                           "Qwen3-8B block (7 linears, inputs of their own), scaled to a full launch by "
+        "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the kernel on ten "
+                           "Qwen3-8B blocks (70 linears, inputs of their own), scaled to a full launch by "
                            "algorithmic bytes" if ratio is not None else None),
     }
 
