@@ -76,82 +76,167 @@ __device__ __forceinline__ int packed_upper(int i, int j, int r) {
   return i * r - (i * (i - 1)) / 2 + (j - i);
 }
 
-// One block per problem.  Cholesky of the r x r Gram matrix (packed upper
-// triangle in shared memory, right-looking), then the upper-triangular inverse
-// R^-1 written in full (zeros below the diagonal) to pb.rinv.  For r <= 128 the
-// inverse is built in shared memory and copied out at the end (each of its r
-// row steps reads the rows below it); larger ones build it in place.
-__host__ __device__ inline bool chol_x_in_smem(int r) { return r <= 128; }
+// One block per problem: R with Gram = R^T R (Cholesky, upper triangular) and
+// its inverse X = R^-1, written in full (zeros below the diagonal) to pb.rinv.
+// Blocked in 32 x 32 tiles so that the block synchronises a few times per tile
+// row rather than a few times per matrix row: the upper tiles live in shared
+// memory (row stride 33, so that columns of a tile fall in distinct banks), the
+// matrix padded to a multiple of 32 with the identity.
+//   Cholesky, right-looking, per tile column k: one warp factors the diagonal
+//   tile; each thread solves one column of the tile row (R_kj = R_kk^-T A_kj);
+//   every warp updates four rows of the trailing tiles (A_ij -= R_ki^T R_kj).
+//   Inverse: each warp inverts one diagonal tile (X_kk = R_kk^-1, one column per
+//   lane); then tile rows from the bottom: X_ij = -X_ii (sum over i < m <= j of
+//   R_im X_mj), the sums first (into scratch), then the products, which replace
+//   row i of R, no longer needed.
+constexpr int kCT = 32, kCTs = 33;  // tile size and row stride (floats)
+__host__ __device__ inline int chol_tiles(int r) { return (r + kCT - 1) / kCT; }
 __host__ __device__ inline size_t chol_smem_floats(int r) {
-  return (((size_t)r * (r + 1) / 2 + 3) & ~size_t(3)) + (chol_x_in_smem(r) ? (size_t)r * r : 0);
+  const int nb = chol_tiles(r);
+  return ((size_t)nb * (nb + 1) / 2 + nb) * kCT * kCTs;  // upper tiles, then a tile row of scratch
+}
+__device__ __forceinline__ float* chol_tile(float* S, int nb, int bi, int bj) {
+  return S + (size_t)(bi * nb - bi * (bi - 1) / 2 + (bj - bi)) * (kCT * kCTs);
 }
 __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
-  extern __shared__ float R[];  // r(r+1)/2, then (r <= 128) r x r for X
+  extern __shared__ float S[];
+  __shared__ int broken;
   const ProjProblem& pb = batch.p[blockIdx.x];
-  const int r = batch.r;
-  const int tid = threadIdx.x, nthreads = blockDim.x;
-  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
-  for (int i = warp; i < r; i += nwarps)
-    for (int j = i + lane; j < r; j += 32) R[packed_upper(i, j, r)] = (float)pb.gram[i * r + j];
-  __syncthreads();
-  bool broken = false;
-  for (int p = 0; p < r; ++p) {
-    const float diag = R[packed_upper(p, p, r)];
-    if (!(diag > 0.0f) || !isfinite(diag)) {  // uniform across the block
-      broken = true;
-      break;
+  const int r = batch.r, nb = chol_tiles(r);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = 8;
+  float* T = S + (size_t)nb * (nb + 1) / 2 * (kCT * kCTs);  // scratch: nb tiles
+  if (tid == 0) broken = 0;
+  for (int bi = 0; bi < nb; ++bi)
+    for (int bj = bi; bj < nb; ++bj) {
+      float* B = chol_tile(S, nb, bi, bj);
+      for (int e = tid; e < kCT * kCT; e += 256) {
+        const int a = e >> 5, c = e & 31, i = bi * kCT + a, j = bj * kCT + c;
+        B[a * kCTs + c] = (i < r && j < r) ? (float)pb.gram[(size_t)i * r + j] : (i == j ? 1.0f : 0.0f);
+      }
     }
-    const float rp = sqrtf(diag);
-    const float inv = 1.0f / rp;
-    __syncthreads();  // everyone has read the pivot
-    for (int j = p + tid; j < r; j += nthreads)
-      R[packed_upper(p, j, r)] = (j == p) ? rp : R[packed_upper(p, j, r)] * inv;
+  __syncthreads();
+
+  // ---- Cholesky ----
+  for (int k = 0; k < nb; ++k) {
+    float* D = chol_tile(S, nb, k, k);
+    if (warp == 0) {  // the diagonal tile, in place
+      for (int p = 0; p < kCT; ++p) {
+        const float d = D[p * kCTs + p];
+        if (!(d > 0.0f) || !isfinite(d)) {  // the same in every lane
+          if (lane == 0) broken = 1;
+          break;
+        }
+        const float rp = sqrtf(d), inv = 1.0f / rp;
+        __syncwarp();
+        const float rpl = lane > p ? D[p * kCTs + lane] * inv : 0.0f;
+        if (lane > p) D[p * kCTs + lane] = rpl;
+        if (lane == p) D[p * kCTs + p] = rp;
+        __syncwarp();
+        if (lane > p)
+          for (int i = p + 1; i <= lane; ++i) D[i * kCTs + lane] = fmaf(-D[p * kCTs + i], rpl, D[i * kCTs + lane]);
+        __syncwarp();
+      }
+    }
     __syncthreads();
-    for (int i = p + 1 + warp; i < r; i += nwarps) {
-      const float rpi = R[packed_upper(p, i, r)];
-      for (int j = i + lane; j < r; j += 32)
-        R[packed_upper(i, j, r)] = fmaf(-rpi, R[packed_upper(p, j, r)], R[packed_upper(i, j, r)]);
+    if (broken) break;
+    // tile row k: R_kj = R_kk^-T A_kj, one column per thread (forward substitution)
+    for (int cidx = tid; cidx < (nb - 1 - k) * kCT; cidx += 256) {
+      float* B = chol_tile(S, nb, k, k + 1 + (cidx >> 5));
+      const int c = cidx & 31;
+      for (int p = 0; p < kCT; ++p) {
+        float v = B[p * kCTs + c];
+        for (int m = 0; m < p; ++m) v = fmaf(-D[m * kCTs + p], B[m * kCTs + c], v);
+        B[p * kCTs + c] = v / D[p * kCTs + p];
+      }
+    }
+    __syncthreads();
+    // trailing tiles k < bi <= bj: A_ij -= R_ki^T R_kj, four rows per warp step
+    const int nt = nb - 1 - k, npairs = nt * (nt + 1) / 2;
+    for (int u = warp; u < npairs * 8; u += kWarps) {
+      int pr = u >> 3, bi = k + 1;
+      for (int len = nt; pr >= len; pr -= len, --len) ++bi;
+      const int bj = bi + pr, a0 = (u & 7) * 4;
+      const float* Ri = chol_tile(S, nb, k, bi);
+      const float* Rj = chol_tile(S, nb, k, bj);
+      float* A = chol_tile(S, nb, bi, bj);
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int p = 0; p < kCT; ++p) {
+        const float rj = Rj[p * kCTs + lane];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[t] = fmaf(Ri[p * kCTs + a0 + t], rj, acc[t]);
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) A[(a0 + t) * kCTs + lane] -= acc[t];
     }
     __syncthreads();
   }
   if (broken) {
-    for (int e = tid; e < r * r; e += nthreads) pb.rinv[e] = 0.0f;
+    for (int e = tid; e < r * r; e += 256) pb.rinv[e] = 0.0f;
     if (tid == 0) atomicOr(batch.status, SKETCH_DEV_QR_BREAKDOWN);
     return;
   }
-  const bool xs = chol_x_in_smem(r);
-  float* X = xs ? R + (((size_t)r * (r + 1) / 2 + 3) & ~size_t(3)) : pb.rinv;
-  // X = R^-1, rows from the bottom: X[i][j] = -(sum_{m=i+1..j} R[i][m] X[m][j]) / R[i][i].
-  for (int i = r - 1; i >= 0; --i) {
-    const float inv_ii = 1.0f / R[packed_upper(i, i, r)];
-    for (int j = tid; j < r; j += nthreads) {
-      float v;
-      if (j < i) {
-        v = 0.0f;
-      } else if (j == i) {
-        v = inv_ii;
-      } else {
-        // four partial sums (terms m = i+1.. in turn) so that the loads and
-        // multiply-adds of one row step overlap instead of forming one chain
-        const float* Ri = R + packed_upper(i, 0, r);  // Ri[m] = R[i][m] for m >= i
-        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        int m = i + 1;
-        for (; m + 3 <= j; m += 4) {
+
+  // ---- inverse: diagonal tiles, one warp each, one column per lane ----
+  for (int k = warp; k < nb; k += kWarps) {
+    const float* D = chol_tile(S, nb, k, k);
+    float* X = T + (size_t)k * (kCT * kCTs);
+    const int j = lane;
+    X[j * kCTs + j] = 1.0f / D[j * kCTs + j];
+    for (int i = j - 1; i >= 0; --i) {
+      float s = 0.0f;
+      for (int m = i + 1; m <= j; ++m) s = fmaf(D[i * kCTs + m], X[m * kCTs + j], s);
+      X[i * kCTs + j] = -s / D[i * kCTs + i];
+    }
+    for (int i = j + 1; i < kCT; ++i) X[i * kCTs + j] = 0.0f;
+    __syncwarp();
+    float* Dw = chol_tile(S, nb, k, k);
+    for (int i = 0; i < kCT; ++i) Dw[i * kCTs + lane] = X[i * kCTs + lane];
+  }
+  __syncthreads();
+  // ---- inverse: off-diagonal tiles, tile rows from the bottom ----
+  for (int bi = nb - 2; bi >= 0; --bi) {
+    const int nt = nb - 1 - bi;
+    // sums: T_j = sum_{bi < m <= bj} R_{bi,m} X_{m,bj}, into scratch tile j - bi - 1
+    for (int u = warp; u < nt * 8; u += kWarps) {
+      const int bj = bi + 1 + (u >> 3), a0 = (u & 7) * 4;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int m = bi + 1; m <= bj; ++m) {
+        const float* Rm = chol_tile(S, nb, bi, m);
+        const float* Xm = chol_tile(S, nb, m, bj);
+        for (int p = 0; p < kCT; ++p) {
+          const float x = Xm[p * kCTs + lane];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) s4[t] = fmaf(Ri[m + t], X[(m + t) * r + j], s4[t]);
+          for (int t = 0; t < 4; ++t) acc[t] = fmaf(Rm[(a0 + t) * kCTs + p], x, acc[t]);
         }
-        if (m <= j) s4[0] = fmaf(Ri[m], X[m * r + j], s4[0]);
-        if (m + 1 <= j) s4[1] = fmaf(Ri[m + 1], X[(m + 1) * r + j], s4[1]);
-        if (m + 2 <= j) s4[2] = fmaf(Ri[m + 2], X[(m + 2) * r + j], s4[2]);
-        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-        v = -s * inv_ii;
       }
-      X[i * r + j] = v;
+      float* Tj = T + (size_t)(bj - bi - 1) * (kCT * kCTs);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) Tj[(a0 + t) * kCTs + lane] = acc[t];
+    }
+    __syncthreads();
+    // products: X_{bi,bj} = -X_{bi,bi} T_j, over row bi of R (no longer needed)
+    const float* Xd = chol_tile(S, nb, bi, bi);
+    for (int u = warp; u < nt * 8; u += kWarps) {
+      const int bj = bi + 1 + (u >> 3), a0 = (u & 7) * 4;
+      const float* Tj = T + (size_t)(bj - bi - 1) * (kCT * kCTs);
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int p = 0; p < kCT; ++p) {
+        const float tv = Tj[p * kCTs + lane];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[t] = fmaf(Xd[(a0 + t) * kCTs + p], tv, acc[t]);
+      }
+      float* O = chol_tile(S, nb, bi, bj);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) O[(a0 + t) * kCTs + lane] = -acc[t];
     }
     __syncthreads();
   }
-  if (xs)
-    for (int e = tid; e < r * r; e += nthreads) pb.rinv[e] = X[e];
+  // ---- out: X in full, zeros below the diagonal ----
+  for (int e = tid; e < r * r; e += 256) {
+    const int i = e / r, j = e % r;
+    pb.rinv[e] = (j < i) ? 0.0f : chol_tile(S, nb, i >> 5, j >> 5)[(i & 31) * kCTs + (j & 31)];
+  }
 }
 
 // P rows [32*blockIdx.x, +32) <- scale * P_rows * Rinv (Rinv upper triangular).
