@@ -10,8 +10,11 @@
 // the sum of its |terms| however many rows there are, without FP64 arithmetic
 // (far slower than fp32 on this GPU).  Neither pass uses atomics, so the
 // result does not depend on scheduling.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace rgs {
 namespace {
@@ -186,6 +189,175 @@ __global__ void __launch_bounds__(256, 4) gram_partial_kernel(const GramBatch ba
   }
 }
 
+// ---- tensor-core partial Gram ------------------------------------------------
+// Chunks of about 1024 rows (gram_chunks_tc), one block per (chunk, matrix),
+// the products on the tensor cores: the chunk's largest magnitude gives a power
+// of two 2^e that brings it into [2^14, 2^15); each element x 2^e is split into
+// FP16 high and low parts (hi + lo within ~2^-22 of it) written, 64 rows at a
+// time, into shared-memory tiles laid out as the MMA's K-major operand (column m
+// of A is row m of the tile, 128-byte swizzle), two sets of tiles so that one
+// step's conversion overlaps the previous step's MMAs; tcgen05.mma (kind::f16,
+// M = 128, N = r rounded to 16, K = 16) accumulates hi hi + hi lo + lo hi of
+// A^T A into TMEM (two M halves when r > 128); warps 0..3, one per TMEM lane
+// quarter, scale the sums by 2^-2e into the chunk's partial (written with a
+// zero low word), which gram_reduce_kernel adds up as for the SIMT kernel.
+constexpr int kGtcThreads = 256;
+constexpr int kGtcStep = 64;  // rows per step: one 128-byte swizzled row of FP16 per column of A
+__host__ __device__ inline int gtc_mpad(int r) { return r <= 128 ? 128 : 256; }
+__host__ __device__ inline int gtc_npad(int r) { return (r + 15) / 16 * 16; }
+__host__ __device__ inline uint32_t gtc_tmem_cols(int r) {
+  const int cols = gtc_npad(r) * (gtc_mpad(r) / 128);
+  uint32_t c = 32;
+  while ((int)c < cols) c <<= 1;
+  return c;
+}
+__device__ __forceinline__ uint8_t* gtc_align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+__device__ __forceinline__ uint32_t gtc_pack(float y0, float y1, uint32_t& lo) {
+  const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
+  const __half l0 = __float2half_rn(y0 - __half2float(h0)), l1 = __float2half_rn(y1 - __half2float(h1));
+  lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+  return (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+}
+__global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch batch) {
+  extern __shared__ uint8_t gtc_raw[];
+  __shared__ __align__(8) uint64_t mma_bar[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ float wmax[kGtcThreads / 32];
+  __shared__ volatile int abort_flag;
+  const GramEntry& en = batch.e[blockIdx.y];
+  const int r = batch.r;
+  const GramChunks g = gram_chunks_tc(en.rows);
+  if ((int)blockIdx.x >= g.nchunks) return;  // the same for the whole block
+  const int mpad = gtc_mpad(r), npad = gtc_npad(r), nmh = mpad / 128;
+  const uint32_t cols = gtc_tmem_cols(r);
+  const uint32_t tile_bytes = (uint32_t)mpad * 128;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // buffer b: hi tile at base + 2 b tile_bytes, lo tile right after it
+  const uint32_t base = tc::smem_u32(gtc_align1024(gtc_raw));
+  const int64_t row_begin = (int64_t)blockIdx.x * g.chunk_rows;
+  const int64_t row_end = row_begin + g.chunk_rows < en.rows ? row_begin + g.chunk_rows : en.rows;
+  const float* __restrict__ A = en.A;
+  if (tid == 0) {
+    abort_flag = 0;
+    tc::mbar_init(&mma_bar[0], 1);
+    tc::mbar_init(&mma_bar[1], 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, cols);
+  // every tile zero: rows m >= r (padding to the MMA's M and N) stay so
+  for (uint32_t e = tid; e < 4 * tile_bytes / 16; e += kGtcThreads) tc::sts128(base + 16u * e, make_uint4(0, 0, 0, 0));
+  // the chunk's largest magnitude (NaN if any element is NaN)
+  float m = 0.f;
+  for (int64_t e = row_begin * r + tid; e < row_end * r; e += kGtcThreads) {
+    const float x = A[e];
+    m = (m != m || x != x) ? __int_as_float(0x7FC00000) : fmaxf(m, fabsf(x));
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+    m = (m != m || om != om) ? __int_as_float(0x7FC00000) : fmaxf(m, om);
+  }
+  if (lane == 0) wmax[warp] = m;
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  float bm = 0.f;
+  for (int w = 0; w < kGtcThreads / 32; ++w)
+    bm = (bm != bm || wmax[w] != wmax[w]) ? __int_as_float(0x7FC00000) : fmaxf(bm, wmax[w]);
+  // 2^e brings the largest magnitude into [2^14, 2^15); a non-finite one keeps
+  // e = 0, so that the products carry it into the Gram
+  int e = 0;
+  if (bm > 0.f && bm <= 3.4028234e38f) {
+    int E;
+    frexpf(bm, &E);
+    e = 15 - E;
+    e = e < -100 ? -100 : (e > 100 ? 100 : e);
+  }
+  const float scale = ldexpf(1.f, e), unscale = ldexpf(1.f, -e);
+  const uint32_t idesc = tc::idesc_f16(128, npad, false, false);
+  const int nsteps = (int)((row_end - row_begin + kGtcStep - 1) / kGtcStep);
+  bool live = true;
+  for (int st = 0; st < nsteps; ++st) {
+    const int b = st & 1;
+    const uint32_t hi_s = base + 2u * b * tile_bytes, lo_s = hi_s + tile_bytes;
+    if (st >= 2) {  // the MMAs of step st - 2 have read this buffer
+      live = tc::mbar_wait(&mma_bar[b], (uint32_t)((st >> 1) - 1) & 1u, &abort_flag, nullptr, 0);
+      live = __syncthreads_and(live);
+      if (!live) break;
+    }
+    // rows [row0, row0 + 64) into buffer b: item (column m of A, 8-row group
+    // k8) is one 16-byte chunk of tile row m; consecutive threads take
+    // consecutive columns, so that each row's loads are coalesced
+    const int64_t row0 = row_begin + (int64_t)st * kGtcStep;
+    for (int it = tid; it < r * 8; it += kGtcThreads) {
+      const int mc = it % r, k8 = it / r;
+      uint32_t hv[4], lv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int64_t ra = row0 + 8 * k8 + 2 * t, rb = ra + 1;
+        const float x0 = ra < row_end ? A[ra * r + mc] : 0.f;
+        const float x1 = rb < row_end ? A[rb * r + mc] : 0.f;
+        hv[t] = gtc_pack(x0 * scale, x1 * scale, lv[t]);
+      }
+      const uint32_t off = (uint32_t)((mc >> 3) * 1024 + (mc & 7) * 128 + ((k8 ^ (mc & 7)) << 4));
+      tc::sts128(hi_s + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
+      tc::sts128(lo_s + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
+    }
+    tc::fence_proxy_async_smem();
+    live = __syncthreads_and(live);
+    if (!live) break;
+    if (tid == 0) {
+      tc::tc_fence_after();
+      for (int mh = 0; mh < nmh; ++mh) {
+        const uint32_t d = tmem + (uint32_t)(mh * npad);
+        const uint32_t arow = (uint32_t)mh * 128 * 128;
+#pragma unroll
+        for (int kk = 0; kk < kGtcStep / 16; ++kk) {
+          const uint64_t ah = tc::sdesc_sw128(hi_s + arow + kk * 32, 16, 1024);
+          const uint64_t al = tc::sdesc_sw128(lo_s + arow + kk * 32, 16, 1024);
+          const uint64_t bh = tc::sdesc_sw128(hi_s + kk * 32, 16, 1024);
+          const uint64_t bl = tc::sdesc_sw128(lo_s + kk * 32, 16, 1024);
+          tc::mma_bf16(d, ah, bh, idesc, (st > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_bf16(d, ah, bl, idesc, 1u);
+          tc::mma_bf16(d, al, bh, idesc, 1u);
+        }
+      }
+      tc::mma_commit(&mma_bar[b]);  // also covers every earlier MMA of this thread
+    }
+  }
+  if (live)
+    live = tc::mbar_wait(&mma_bar[(nsteps - 1) & 1], (uint32_t)((nsteps - 1) >> 1) & 1u, &abort_flag, nullptr, 0);
+  live = __syncthreads_and(live);
+  tc::tc_fence_after();
+  // warps 0..3: the sums of TMEM lane m (row m of A^T A) scaled back by
+  // 2^-2e; a wait that gave up leaves the partial NaN
+  if (warp < 4) {
+    float2* out = en.partials + (size_t)blockIdx.x * r * r;
+    for (int mh = 0; mh < nmh; ++mh) {
+      const int mrow = mh * 128 + warp * 32 + lane;
+      for (int cg = 0; cg * 32 < npad; ++cg) {
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(mh * npad + cg * 32), v);
+        tc::tmem_wait_ld();
+        if (mrow < r) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            const int n = cg * 32 + t;
+            if (n < r)
+              out[(size_t)mrow * r + n] =
+                  make_float2(live ? __uint_as_float(v[t]) * unscale * unscale : __int_as_float(0x7FC00000), 0.f);
+          }
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, cols);
+}
+
 // out[a][b] = sum over chunks c, in order, of partials[c][a][b] (TwoSum on the
 // pairs), for the 4 x 4 blocks the partial kernel wrote (block row <= block
 // column); the other entries are the mirror image.  grid (.., batch).
@@ -201,7 +373,7 @@ __global__ void gram_reduce_kernel(const GramBatch batch) {
     b = t;
   }
   const int src = a * r + b;
-  const int nchunks = gram_chunks(en.rows).nchunks;
+  const int nchunks = batch.tc ? gram_chunks_tc(en.rows).nchunks : gram_chunks(en.rows).nchunks;
   float hi = 0.f, lo = 0.f;
 #pragma unroll 8
   for (int c = 0; c < nchunks; ++c) {
@@ -214,14 +386,32 @@ __global__ void gram_reduce_kernel(const GramBatch batch) {
 
 }  // namespace
 
-cudaError_t launch_gram(const GramBatch& batch, cudaStream_t stream) {
-  if (batch.n <= 0) return cudaSuccess;
-  const int tiles = (int)ceil_div(batch.r, kTile);
-  const size_t smem = gram_smem_bytes(tiles > 1);
-  cudaError_t err = cudaFuncSetAttribute(gram_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
-  count_launch();
-  gram_partial_kernel<<<dim3(64, tiles * (tiles + 1) / 2, batch.n), 256, smem, stream>>>(batch);
+cudaError_t launch_gram(const GramBatch& batch_in, cudaStream_t stream, bool tensor_cores) {
+  if (batch_in.n <= 0) return cudaSuccess;
+  static thread_local GramBatch batch;
+  batch = batch_in;
+  batch.tc = tensor_cores ? 1 : 0;
+  cudaError_t err = cudaSuccess;
+  if (tensor_cores) {
+    // shared memory: two buffers of two tiles, or more, so that the blocks
+    // resident on an SM never ask for more than its 512 TMEM columns
+    const int r = batch.r;
+    const size_t tiles = (size_t)4 * gtc_mpad(r) * 128 + 1024;
+    const int max_blocks = 512 / (int)gtc_tmem_cols(r);
+    const size_t tmem_bound = (size_t)233472 / (size_t)(max_blocks + 1) - 1024 + 16;
+    const size_t smem = tiles > tmem_bound ? tiles : tmem_bound;
+    err = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    count_launch();
+    gram_tc_kernel<<<dim3(64, batch.n), kGtcThreads, smem, stream>>>(batch);
+  } else {
+    const int tiles = (int)ceil_div(batch.r, kTile);
+    const size_t smem = gram_smem_bytes(tiles > 1);
+    err = cudaFuncSetAttribute(gram_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    count_launch();
+    gram_partial_kernel<<<dim3(64, tiles * (tiles + 1) / 2, batch.n), 256, smem, stream>>>(batch);
+  }
   const int rr = batch.r * batch.r;
   count_launch();
   gram_reduce_kernel<<<dim3((unsigned)ceil_div(rr, 256), batch.n), 256, 0, stream>>>(batch);

@@ -66,12 +66,26 @@ struct GramEntry {
   float2* partials; // gram_chunks(rows).nchunks x r x r (hi, lo) pairs
   double* out;      // r x r
 };
+// The tensor-core kernel's chunks: about 1024 rows each (its fixed cost per
+// chunk is higher), at most 64, so the partials fit the same workspace.
+__host__ __device__ inline GramChunks gram_chunks_tc(int64_t rows) {
+  int64_t n = (rows + 1023) / 1024;
+  if (n > 64) n = 64;
+  if (n < 1) n = 1;
+  GramChunks g;
+  g.nchunks = (int)n;
+  g.chunk_rows = (int)((rows + n - 1) / n);
+  return g;
+}
 struct GramBatch {
   int n;
   int r;
+  int tc;  // set by launch_gram: 1 when the tensor-core kernel wrote the partials
   GramEntry e[kMaxBatch];
 };
-cudaError_t launch_gram(const GramBatch& batch, cudaStream_t stream);
+// tensor_cores: partial Grams on the tensor cores (FP16 split of each chunk,
+// good to ~1e-6 of an entry's scale), else the compensated fp32 kernel (~1e-7).
+cudaError_t launch_gram(const GramBatch& batch, cudaStream_t stream, bool tensor_cores);
 
 // ---- (a) projection -------------------------------------------------------
 struct ProjProblem {

@@ -634,7 +634,7 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
     if (err != cudaSuccess) return err;
   }
   for (int pass = 0; pass < 2; ++pass) {
-    err = launch_gram(gb, stream);
+    err = launch_gram(gb, stream, true);
     if (err != cudaSuccess) return err;
     count_launch();
     chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch);
