@@ -190,23 +190,28 @@ __global__ void __launch_bounds__(256, 4) gram_partial_kernel(const GramBatch ba
 }
 
 // ---- tensor-core partial Gram ------------------------------------------------
-// Chunks of about 1024 rows (gram_chunks_tc), one block per (chunk, matrix),
-// the products on the tensor cores: the chunk's largest magnitude gives a power
+// Chunks of gram_chunks_tc rows, one block per (chunk, matrix), the products
+// on the tensor cores: the chunk's largest magnitude gives a power
 // of two 2^e that brings it into [2^14, 2^15); each element x 2^e is split into
 // FP16 high and low parts (hi + lo within ~2^-22 of it) written, 64 rows at a
 // time, into shared-memory tiles laid out as the MMA's K-major operand (column m
 // of A is row m of the tile, 128-byte swizzle), two sets of tiles so that one
 // step's conversion overlaps the previous step's MMAs; tcgen05.mma (kind::f16,
 // M = 128, N = r rounded to 16, K = 16) accumulates hi hi + hi lo + lo hi of
-// A^T A into TMEM (two M halves when r > 128); warps 0..3, one per TMEM lane
-// quarter, scale the sums by 2^-2e into the chunk's partial (written with a
+// A^T A into TMEM (two M halves when r > 128), the steps going to the
+// gram_tc_accs accumulators in turn; warps 0..3, one per TMEM lane quarter, add
+// the accumulators and scale the sums by 2^-2e into the chunk's partial (written with a
 // zero low word), which gram_reduce_kernel adds up as for the SIMT kernel.
 constexpr int kGtcThreads = 256;
 constexpr int kGtcStep = 64;  // rows per step: one 128-byte swizzled row of FP16 per column of A
 __host__ __device__ inline int gtc_mpad(int r) { return r <= 128 ? 128 : 256; }
 __host__ __device__ inline int gtc_npad(int r) { return (r + 15) / 16 * 16; }
+// TMEM columns: the accumulators (nacc x M halves x npad), and at least the
+// span the epilogue's 32-column reads cover
 __host__ __device__ inline uint32_t gtc_tmem_cols(int r) {
-  const int cols = gtc_npad(r) * (gtc_mpad(r) / 128);
+  const int npad = gtc_npad(r), nmh = gtc_mpad(r) / 128, nacc = gram_tc_accs(r);
+  const int reads = (nacc * nmh - 1) * npad + (npad + 31) / 32 * 32;
+  const int cols = nacc * nmh * npad > reads ? nacc * nmh * npad : reads;
   uint32_t c = 32;
   while ((int)c < cols) c <<= 1;
   return c;
@@ -228,9 +233,9 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
   __shared__ volatile int abort_flag;
   const GramEntry& en = batch.e[blockIdx.y];
   const int r = batch.r;
-  const GramChunks g = gram_chunks_tc(en.rows);
+  const GramChunks g = gram_chunks_tc(en.rows, r);
   if ((int)blockIdx.x >= g.nchunks) return;  // the same for the whole block
-  const int mpad = gtc_mpad(r), npad = gtc_npad(r), nmh = mpad / 128;
+  const int mpad = gtc_mpad(r), npad = gtc_npad(r), nmh = mpad / 128, nacc = gram_tc_accs(r);
   const uint32_t cols = gtc_tmem_cols(r);
   const uint32_t tile_bytes = (uint32_t)mpad * 128;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -310,8 +315,9 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
     if (!live) break;
     if (tid == 0) {
       tc::tc_fence_after();
+      const int acc = st % nacc;  // this step's accumulator
       for (int mh = 0; mh < nmh; ++mh) {
-        const uint32_t d = tmem + (uint32_t)(mh * npad);
+        const uint32_t d = tmem + (uint32_t)((acc * nmh + mh) * npad);
         const uint32_t arow = (uint32_t)mh * 128 * 128;
 #pragma unroll
         for (int kk = 0; kk < kGtcStep / 16; ++kk) {
@@ -319,7 +325,7 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
           const uint64_t al = tc::sdesc_sw128(lo_s + arow + kk * 32, 16, 1024);
           const uint64_t bh = tc::sdesc_sw128(hi_s + kk * 32, 16, 1024);
           const uint64_t bl = tc::sdesc_sw128(lo_s + kk * 32, 16, 1024);
-          tc::mma_bf16(d, ah, bh, idesc, (st > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_bf16(d, ah, bh, idesc, (st >= nacc || kk > 0) ? 1u : 0u);
           tc::mma_bf16(d, ah, bl, idesc, 1u);
           tc::mma_bf16(d, al, bh, idesc, 1u);
         }
@@ -339,8 +345,17 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
       const int mrow = mh * 128 + warp * 32 + lane;
       for (int cg = 0; cg * 32 < npad; ++cg) {
         uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(mh * npad + cg * 32), v);
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cg * 32);
+        tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)(mh * npad), v);
         tc::tmem_wait_ld();
+        // the accumulators that received steps, added in order
+        for (int a = 1; a < nacc && a < nsteps; ++a) {
+          uint32_t w[32];
+          tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)((a * nmh + mh) * npad), w);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(w[t]));
+        }
         if (mrow < r) {
 #pragma unroll
           for (int t = 0; t < 32; ++t) {
@@ -373,7 +388,7 @@ __global__ void gram_reduce_kernel(const GramBatch batch) {
     b = t;
   }
   const int src = a * r + b;
-  const int nchunks = batch.tc ? gram_chunks_tc(en.rows).nchunks : gram_chunks(en.rows).nchunks;
+  const int nchunks = batch.tc ? gram_chunks_tc(en.rows, r).nchunks : gram_chunks(en.rows).nchunks;
   float hi = 0.f, lo = 0.f;
 #pragma unroll 8
   for (int c = 0; c < nchunks; ++c) {

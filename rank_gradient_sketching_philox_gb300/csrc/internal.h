@@ -66,10 +66,22 @@ struct GramEntry {
   float2* partials; // gram_chunks(rows).nchunks x r x r (hi, lo) pairs
   double* out;      // r x r
 };
-// The tensor-core kernel's chunks: about 1024 rows each (its fixed cost per
-// chunk is higher), at most 64, so the partials fit the same workspace.
-__host__ __device__ inline GramChunks gram_chunks_tc(int64_t rows) {
-  int64_t n = (rows + 1023) / 1024;
+// The tensor-core kernel: each chunk's products go, 64 rows at a time, to
+// gram_tc_accs(r) TMEM accumulators in turn (as many as 512 columns hold, up
+// to 4), and each accumulator takes about 256 rows per chunk: the tensor
+// cores' fp32 accumulation drifts in proportion to the length of a chain, so
+// longer chains lose measurably (QR orthogonality 7.5e-6 with 1024 rows per
+// accumulator against 1.9e-6 with 256).  At most 64 chunks, so the partials fit
+// the same workspace as the SIMT kernel's.
+__host__ __device__ inline int gram_tc_accs(int r) {
+  const int npad = (r + 15) / 16 * 16, nmh = r <= 128 ? 1 : 2;
+  int a = 512 / (npad * nmh);
+  if (a > 4) a = 4;
+  return a >= 4 ? 4 : (a >= 2 ? 2 : 1);
+}
+__host__ __device__ inline GramChunks gram_chunks_tc(int64_t rows, int r) {
+  const int64_t target = 256 * (int64_t)gram_tc_accs(r);
+  int64_t n = (rows + target - 1) / target;
   if (n > 64) n = 64;
   if (n < 1) n = 1;
   GramChunks g;
