@@ -497,11 +497,32 @@ def main():
         rgs.sample_projection_batched(kind, seed, s, P, layer_ids, ws=ws_sample)
         rgs.split_projection_grouped([[P[li] for li in g] for g in groups], splits=P_split)
 
+    # The projection's independent launches (one per input-group size) go to
+    # side streams that fork from and join back to the main stream, so that one
+    # persistent launch's last CTAs overlap the next launch's first instead of
+    # leaving SMs idle.
+    side = [torch.cuda.Stream(dev) for _ in range(3)]
+
+    def fork_join(fns):
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        done = []
+        for fn, ss in zip(fns, side):
+            ss.wait_event(ev)
+            fn(ss)
+            e = torch.cuda.Event()
+            e.record(ss)
+            done.append(e)
+        for e in done:
+            stream.wait_event(e)
+
     def project_phase(Xs):
-        for size in sizes:
+        def launch(size):
             gis = by_size[size]
-            rgs.project_inputs_grouped_batched([Xs[gi] for gi in gis], [P_split[gi] for gi in gis], size * r,
-                                               [XPg[gi] for gi in gis], ws=ws_project[size])
+            return lambda ss: rgs.project_inputs_grouped_batched(
+                [Xs[gi] for gi in gis], [P_split[gi] for gi in gis], size * r, [XPg[gi] for gi in gis],
+                ws=ws_project[size], stream=ss)
+        fork_join([launch(size) for size in sizes])
 
     def accumulate_phase(m, Ds):
         rgs.accumulate_batched(Ds, XP, C, overwrite=(m == 0))
