@@ -11,8 +11,11 @@
 // positive diagonal, so the result is the sign-corrected QR factor without an
 // explicit sign fix.  For 4r <= k the Gaussian matrix is well conditioned and
 // the second pass leaves P^T P = (k/r) I to about 1e-6.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace rgs {
 namespace {
@@ -568,6 +571,223 @@ __global__ void __launch_bounds__(kTriThreads, 1) tri_apply_pipe_kernel(const __
   }
 }
 
+// P rows <- (P rows) X on the tensor cores, for r <= 128: a block takes up to
+// kTtcRows consecutive rows of one problem (the grid lists the row groups that
+// exist), 128 at a time.  X (scaled by a power of two 2^g from its largest
+// magnitude) is split once per block into FP16 high and low parts and written
+// transposed into swizzled K-major tiles (row n of the tile is column n of X);
+// each 128-row tile of P likewise, each row m scaled by its own 2^e_m (row m of
+// P is row m of the tile, K = r in 64-wide chunks; a row's scale factors out
+// of its products).  tcgen05.mma (kind::f16,
+// M = 128, N = r rounded to 16) accumulates hi hi + hi lo + lo hi into TMEM,
+// and warps 0..3 (one per TMEM lane quarter) write each row's products times
+// 2^-(e_m+g) (and the final pass's scale) over the row, which only this block
+// reads.  Zero padding past r in both operands keeps the padded sums exact.
+constexpr int kTtcRows = 1024;
+constexpr int kTtcThreads = 256;
+__host__ __device__ inline int ttc_npad(int r) { return (r + 15) / 16 * 16; }
+__host__ __device__ inline int ttc_kc(int r) { return (ttc_npad(r) + 63) / 64; }
+__host__ __device__ inline bool ttc_ok(int r) { return r <= 128; }
+__host__ __device__ inline size_t ttc_smem_bytes(int r) {
+  return (size_t)ttc_kc(r) * 2 * 16384 + (size_t)ttc_kc(r) * 2 * ttc_npad(r) * 128 + 1024;
+}
+__host__ __device__ inline uint32_t ttc_tmem_cols(int r) {
+  uint32_t c = 32;
+  while ((int)c < ttc_npad(r)) c <<= 1;
+  return c;
+}
+__device__ __forceinline__ uint32_t ttc_split2(float y0, float y1, uint32_t& lo) {
+  const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
+  const __half l0 = __float2half_rn(y0 - __half2float(h0)), l1 = __float2half_rn(y1 - __half2float(h1));
+  lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+  return (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+}
+// 2^e that brings a largest magnitude m into [2^14, 2^15) (0 for m = 0 or not finite)
+__device__ __forceinline__ int ttc_exponent(float m) {
+  if (!(m > 0.f) || !(m <= 3.4028234e38f)) return 0;
+  int E;
+  frexpf(m, &E);
+  const int e = 15 - E;
+  return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+// largest magnitude over the block (NaN if any is NaN)
+__device__ __forceinline__ float ttc_block_max(float m, float* wmax) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+    m = (m != m || om != om) ? __int_as_float(0x7FC00000) : fmaxf(m, om);
+  }
+  __syncthreads();  // wmax is free
+  if (lane == 0) wmax[warp] = m;
+  __syncthreads();
+  float bm = 0.f;
+  for (int w = 0; w < kTtcThreads / 32; ++w)
+    bm = (bm != bm || wmax[w] != wmax[w]) ? __int_as_float(0x7FC00000) : fmaxf(bm, wmax[w]);
+  return bm;
+}
+__global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_constant__ ProjBatch batch,
+                                                                   const __grid_constant__ TriGrid grid,
+                                                                   int final_pass) {
+  extern __shared__ uint8_t ttc_raw[];
+  __shared__ __align__(8) uint64_t mma_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ float wmax[kTtcThreads / 32];
+  __shared__ int row_e[128];  // each row's scale exponent
+  __shared__ volatile int abort_flag;
+  int y = 0;  // this block's problem
+  {
+    int lo = 0, hi = batch.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (grid.blk_begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    }
+    y = lo;
+  }
+  const ProjProblem& pb = batch.p[y];
+  const int r = batch.r, npad = ttc_npad(r), kc = ttc_kc(r);
+  const uint32_t cols = ttc_tmem_cols(r);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t first = (int64_t)((int)blockIdx.x - grid.blk_begin[y]) * kTtcRows;
+  const int64_t last = first + kTtcRows < pb.k ? first + kTtcRows : pb.k;
+  float* __restrict__ P = pb.P;
+  const float* __restrict__ X = pb.rinv;
+  const uint32_t base = tc::smem_u32(reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(ttc_raw) + 1023) & ~uintptr_t(1023)));
+  // A chunk c: hi at a_s + 2c 16384, lo 16384 further; B chunk c likewise with npad 128-byte rows
+  const uint32_t a_s = base, b_s = base + (uint32_t)kc * 2 * 16384, b_part = (uint32_t)npad * 128;
+  if (tid == 0) {
+    abort_flag = 0;
+    tc::mbar_init(&mma_bar, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, cols);
+  for (uint32_t e = tid; e < (uint32_t)((kc * 2 * 16384 + kc * 2 * npad * 128) / 16); e += kTtcThreads)
+    tc::sts128(base + 16u * e, make_uint4(0, 0, 0, 0));
+  float m = 0.f;
+  for (int e = tid; e < r * r; e += kTtcThreads) {
+    const float x = X[e];
+    m = (m != m || x != x) ? __int_as_float(0x7FC00000) : fmaxf(m, fabsf(x));
+  }
+  tc::tc_fence_before();
+  const int g = ttc_exponent(ttc_block_max(m, wmax));  // (its barriers also publish the zeroed tiles)
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  // B = X^T split: item (column n of X, chunk c, 8-row group k8) is one
+  // 16-byte chunk of tile row n; consecutive threads take consecutive n
+  {
+    const float sx = ldexpf(1.f, g);
+    for (int it = tid; it < r * kc * 8; it += kTtcThreads) {
+      const int n = it % r, rest = it / r, k8 = rest & 7, c = rest >> 3;
+      uint32_t hv[4], lv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int k0 = c * 64 + k8 * 8 + 2 * t;
+        const float x0 = k0 < r ? X[k0 * r + n] : 0.f, x1 = k0 + 1 < r ? X[(k0 + 1) * r + n] : 0.f;
+        hv[t] = ttc_split2(x0 * sx, x1 * sx, lv[t]);
+      }
+      const uint32_t off = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((k8 ^ (n & 7)) << 4));
+      const uint32_t bc = b_s + (uint32_t)c * 2 * b_part;
+      tc::sts128(bc + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
+      tc::sts128(bc + b_part + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
+    }
+  }
+  const uint32_t idesc = tc::idesc_f16(128, npad, false, false);
+  const float out_scale = final_pass ? pb.scale : 1.0f;
+  const bool vec = (r & 3) == 0;
+  const int per_row = 8 * kc;  // conversion items of one row: consecutive threads (8 or 16)
+  uint32_t phase = 0;
+  bool live = true;
+  for (int64_t row0 = first; row0 < last && live; row0 += 128) {
+    const int rows = (int)(last - row0 < 128 ? last - row0 : 128);
+    // A = this tile of P, each row scaled by its own power of two 2^e_m: item
+    // (row m, chunk c, 8-column group k8), the items of a row on consecutive
+    // threads, which find the row's largest magnitude together
+    for (int it = tid; it < 128 * per_row; it += kTtcThreads) {
+      const int k8 = it & 7, c = (it >> 3) % kc, mr = it / per_row;
+      const int k0 = c * 64 + k8 * 8;
+      const float* src = P + (row0 + mr) * r + k0;
+      float x[8];
+      if (vec && mr < rows && k0 + 8 <= r) {  // two 16-byte loads (rows start on 16 bytes when 4 | r)
+        const float4 u0 = reinterpret_cast<const float4*>(src)[0], u1 = reinterpret_cast<const float4*>(src)[1];
+        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) x[t] = (mr < rows && k0 + t < r) ? src[t] : 0.f;
+      }
+      float mx = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx = (mx != mx || x[t] != x[t]) ? __int_as_float(0x7FC00000) : fmaxf(mx, fabsf(x[t]));
+      for (int o = 1; o < per_row; o <<= 1) {
+        const float om = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
+        mx = (mx != mx || om != om) ? __int_as_float(0x7FC00000) : fmaxf(mx, om);
+      }
+      const int em = ttc_exponent(mx);
+      if ((it & (per_row - 1)) == 0) row_e[mr] = em;
+      const float sp = ldexpf(1.f, em);
+      uint32_t hv[4], lv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) hv[t] = ttc_split2(x[2 * t] * sp, x[2 * t + 1] * sp, lv[t]);
+      const uint32_t off = (uint32_t)((mr >> 3) * 1024 + (mr & 7) * 128 + ((k8 ^ (mr & 7)) << 4));
+      const uint32_t ac = a_s + (uint32_t)c * 2 * 16384;
+      tc::sts128(ac + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
+      tc::sts128(ac + 16384 + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
+    }
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc::tc_fence_after();
+      for (int c = 0; c < kc; ++c) {
+        const uint32_t ac = a_s + (uint32_t)c * 2 * 16384, bc = b_s + (uint32_t)c * 2 * b_part;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ah = tc::sdesc_sw128(ac + kk * 32, 16, 1024), al = tc::sdesc_sw128(ac + 16384 + kk * 32, 16, 1024);
+          const uint64_t bh = tc::sdesc_sw128(bc + kk * 32, 16, 1024), bl = tc::sdesc_sw128(bc + b_part + kk * 32, 16, 1024);
+          tc::mma_bf16(tmem, ah, bh, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_bf16(tmem, ah, bl, idesc, 1u);
+          tc::mma_bf16(tmem, al, bh, idesc, 1u);
+        }
+      }
+      tc::mma_commit(&mma_bar);
+    }
+    live = tc::mbar_wait(&mma_bar, phase, &abort_flag, nullptr, 0);
+    phase ^= 1u;
+    live = __syncthreads_and(live);
+    tc::tc_fence_after();
+    if (!live) break;
+    // warps 0..3: row m = TMEM lane 32 w + lane, scaled back and written over P
+    if (warp < 4) {
+      const int mr = warp * 32 + lane;
+      const float us = ldexpf(1.f, -(row_e[mr] + g)) * out_scale;
+      for (int cg = 0; cg * 32 < npad; ++cg) {
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cg * 32), v);
+        tc::tmem_wait_ld();
+        if (mr < rows) {
+          float* dst = P + (row0 + mr) * r + cg * 32;
+          if (vec && cg * 32 + 32 <= r) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              reinterpret_cast<float4*>(dst)[t] =
+                  make_float4(__uint_as_float(v[4 * t]) * us, __uint_as_float(v[4 * t + 1]) * us,
+                              __uint_as_float(v[4 * t + 2]) * us, __uint_as_float(v[4 * t + 3]) * us);
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+              if (cg * 32 + t < r) dst[t] = __uint_as_float(v[t]) * us;
+          }
+        }
+      }
+    }
+    tc::tc_fence_before();
+    __syncthreads();  // the TMEM reads and row_e are done before the next tile
+    tc::tc_fence_after();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, cols);
+}
+
 }  // namespace
 
 void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
@@ -612,7 +832,14 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
   err = cudaFuncSetAttribute(tri_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)apply_smem);
   if (err != cudaSuccess) return err;
-  const bool pipe = tri_pipe_ok(r);
+  // the triangular products: on the tensor cores up to rank 128, else SIMT
+  const bool tcore = ttc_ok(r);
+  const size_t tc_smem = tcore ? ttc_smem_bytes(r) : 0;
+  if (tcore) {
+    err = cudaFuncSetAttribute(tri_apply_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem);
+    if (err != cudaSuccess) return err;
+  }
+  const bool pipe = !tcore && tri_pipe_ok(r);
   const size_t pipe_smem = pipe ? tri_pipe_smem_bytes(r) : 0;
   if (pipe) {
     err = cudaFuncSetAttribute(tri_apply_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -620,12 +847,12 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
     if (err != cudaSuccess) return err;
   }
   static thread_local TriGrid tg;
-  if (pipe) {
+  if (tcore || pipe) {
+    const int64_t rows = tcore ? kTtcRows : (int64_t)256 * kTriBlocks;
     tg.blk_begin[0] = 0;
-    for (int i = 0; i < batch.n; ++i)
-      tg.blk_begin[i + 1] = tg.blk_begin[i] + (int)ceil_div(batch.p[i].k, (int64_t)256 * kTriBlocks);
+    for (int i = 0; i < batch.n; ++i) tg.blk_begin[i + 1] = tg.blk_begin[i] + (int)ceil_div(batch.p[i].k, rows);
   }
-  const bool small = !pipe && r <= 64;
+  const bool small = !tcore && !pipe && r <= 64;
   const int small_rows = small ? tri_rows_small(r) : 0;
   const size_t small_smem = small ? sizeof(float) * tri_small_smem_floats(r) : 0;
   if (small) {
@@ -639,7 +866,9 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
     count_launch();
     chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch);
     count_launch();
-    if (pipe)
+    if (tcore)
+      tri_apply_tc_kernel<<<(unsigned)tg.blk_begin[batch.n], kTtcThreads, tc_smem, stream>>>(batch, tg, pass == 1);
+    else if (pipe)
       tri_apply_pipe_kernel<<<(unsigned)tg.blk_begin[batch.n], kTriThreads, pipe_smem, stream>>>(batch, tg,
                                                                                                   pass == 1);
     else if (small)
