@@ -75,9 +75,6 @@ __global__ void __launch_bounds__(256) gaussian_kernel(const ProjBatch batch) {
   reinterpret_cast<float4*>(pb.P)[b] = gaussian4(blk);
 }
 
-__device__ __forceinline__ int packed_upper(int i, int j, int r) {
-  return i * r - (i * (i - 1)) / 2 + (j - i);
-}
 
 // One block per problem: R with Gram = R^T R (Cholesky, upper triangular) and
 // its inverse X = R^-1, written in full (zeros below the diagonal) to pb.rinv.
@@ -242,340 +239,17 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
   }
 }
 
-// P rows [32*blockIdx.x, +32) <- scale * P_rows * Rinv (Rinv upper triangular).
-// P rows <- (P rows) X, X = R^-1 upper triangular, in place; on the final pass
-// also times the scale sqrt(k/r).  With r8 = r rounded up to 8 and co = r8/8
-// column octets, a block of 256 threads takes RB = 8 * floor(256 / co) rows and
-// all columns: thread t < RB/8 * co owns the 8 x 8 outputs of column octet
-// t % co and row octet t / co (the rest only help to stage).  The block's
-// rows are staged (transposed) in shared memory first, so the in-place writes
-// cannot race its reads; X follows 32 rows at a time.  Per row m of X a thread
-// reads 8 staged values and 8 X values (four 16-byte shared loads) for 64 FMAs.
-constexpr int kXRows = 32;
-__host__ __device__ inline int tri_rows(int r) { return 8 * (256 / ((r + 7) / 8)); }
-__host__ __device__ inline size_t tri_smem_floats(int r) {
-  const int r8 = (r + 7) / 8 * 8, rb = tri_rows(r);
-  return (size_t)r * (rb + 4) + 4 + (size_t)kXRows * r8;
-}
-__global__ void __launch_bounds__(256) tri_apply_kernel(const ProjBatch batch, int final_pass) {
-  extern __shared__ __align__(16) float smem[];
-  const ProjProblem& pb = batch.p[blockIdx.y];
-  const int r = batch.r, r8 = (r + 7) / 8 * 8, co_n = r8 / 8, RB = tri_rows(r), ldt = RB + 4;
-  float* St = smem;                                   // r x (RB + 4): St[m][row]
-  float* Xs = smem + (((size_t)r * ldt + 3) & ~size_t(3));  // kXRows x r8
-  const int64_t row0 = (int64_t)blockIdx.x * RB;
-  if (row0 >= pb.k) return;
-  const int rows = (int)((pb.k - row0) < RB ? (pb.k - row0) : RB);
-  float* P = pb.P + row0 * r;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Staging: thread t takes rows t, t + 256, ... and reads each in pieces of up
-  // to 64 values, all loads of a piece issued before its transposed stores
-  // (consecutive threads write consecutive rows: no bank conflicts).
-  if ((r & 3) == 0) {
-    const int nv = r >> 2;  // float4 per row
-    for (int row = threadIdx.x; row < rows; row += 256) {
-      const float4* src = reinterpret_cast<const float4*>(P + (size_t)row * r);
-      for (int c0 = 0; c0 < nv; c0 += 16) {
-        float4 v[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) v[m] = (c0 + m < nv) ? src[c0 + m] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          if (c0 + m >= nv) break;
-          float* dst = St + (size_t)(4 * (c0 + m)) * ldt + row;
-          dst[0] = v[m].x;
-          dst[ldt] = v[m].y;
-          dst[2 * ldt] = v[m].z;
-          dst[3 * ldt] = v[m].w;
-        }
-      }
-    }
-  } else {
-    for (int row = threadIdx.x; row < rows; row += 256) {
-      const float* src = P + (size_t)row * r;
-      for (int c0 = 0; c0 < r; c0 += 16) {
-        float v[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) v[m] = (c0 + m < r) ? src[c0 + m] : 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m)
-          if (c0 + m < r) St[(size_t)(c0 + m) * ldt + row] = v[m];
-      }
-    }
-  }
-  const int co = threadIdx.x % co_n, ro = threadIdx.x / co_n;
-  const bool active = ro < RB / 8;
-  const int c0 = 8 * co, q0 = 8 * ro;
-  const float* __restrict__ X = pb.rinv;
-  float acc[8][8];
-#pragma unroll
-  for (int p = 0; p < 8; ++p)
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[p][q] = 0.f;
-  for (int m0 = 0; m0 < r; m0 += kXRows) {
-    const int mrows = (r - m0) < kXRows ? (r - m0) : kXRows;
-    __syncthreads();  // St staged (first chunk) / the previous X chunk used
-    for (int mm = warp; mm < mrows; mm += 8)
-      for (int c = lane; c < r8; c += 32) Xs[mm * r8 + c] = c < r ? X[(size_t)(m0 + mm) * r + c] : 0.f;
-    __syncthreads();
-    if (!active) continue;
-    // X is upper triangular: rows m > c0 + 7 add nothing to these columns
-    int mend = c0 + 8 - m0;
-    if (mend > mrows) mend = mrows;
-#pragma unroll 2
-    for (int mm = 0; mm < mend; ++mm) {
-      const float4 sa = *reinterpret_cast<const float4*>(St + (size_t)(m0 + mm) * ldt + q0);
-      const float4 sb = *reinterpret_cast<const float4*>(St + (size_t)(m0 + mm) * ldt + q0 + 4);
-      const float4 xa = *reinterpret_cast<const float4*>(Xs + mm * r8 + c0);
-      const float4 xb = *reinterpret_cast<const float4*>(Xs + mm * r8 + c0 + 4);
-      const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-      for (int p = 0; p < 8; ++p)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[p][q] = fmaf(sv[p], xv[q], acc[p][q]);
-    }
-  }
-  if (!active) return;
-  const float scale = final_pass ? pb.scale : 1.0f;
-  const bool vec = (r & 3) == 0;
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    if (q0 + p >= rows) break;
-    float* out = P + (size_t)(q0 + p) * r + c0;
-    if (vec && c0 + 8 <= r) {
-      *reinterpret_cast<float4*>(out) =
-          make_float4(acc[p][0] * scale, acc[p][1] * scale, acc[p][2] * scale, acc[p][3] * scale);
-      *reinterpret_cast<float4*>(out + 4) =
-          make_float4(acc[p][4] * scale, acc[p][5] * scale, acc[p][6] * scale, acc[p][7] * scale);
-    } else {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (c0 + q < r) out[q] = acc[p][q] * scale;
-    }
-  }
-}
-
-// The same product for r <= 64 (at most eight column octets), arranged so that
-// every lane of a warp has the same triangular extent: warp w takes column
-// octet co = w % co_n of the 256-row group w / co_n, lane l the row octet l of
-// that group (8 x 8 outputs each).  A block covers RB = 256 * (8 / co_n) rows,
-// staged (transposed) with all of X before any output is written.  Warps of
-// low octets finish early and leave the SM to other blocks; no lane idles
-// inside a warp.
-__host__ __device__ inline int tri_rows_small(int r) { return 256 * (8 / ((r + 7) / 8)); }
-__host__ __device__ inline size_t tri_small_smem_floats(int r) {
-  const int r8 = (r + 7) / 8 * 8;
-  return (((size_t)r * (tri_rows_small(r) + 4) + 3) & ~size_t(3)) + (size_t)r * r8;
-}
-__global__ void __launch_bounds__(256, 2) tri_apply_small_kernel(const ProjBatch batch, int final_pass) {
-  extern __shared__ __align__(16) float smem[];
-  const ProjProblem& pb = batch.p[blockIdx.y];
-  const int r = batch.r, r8 = (r + 7) / 8 * 8, co_n = r8 / 8, ng = 8 / co_n, RB = 256 * ng, ldt = RB + 4;
-  float* St = smem;                                          // r x (RB + 4): St[m][row]
-  float* Xs = smem + (((size_t)r * ldt + 3) & ~size_t(3));  // r x r8
-  const int64_t row0 = (int64_t)blockIdx.x * RB;
-  if (row0 >= pb.k) return;
-  const int rows = (int)((pb.k - row0) < RB ? (pb.k - row0) : RB);
-  float* P = pb.P + row0 * r;
-  if ((r & 3) == 0) {
-    const int nv = r >> 2;
-    for (int row = threadIdx.x; row < rows; row += 256) {
-      const float4* src = reinterpret_cast<const float4*>(P + (size_t)row * r);
-      float4 v[16];
-#pragma unroll
-      for (int m = 0; m < 16; ++m) v[m] = (m < nv) ? src[m] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        if (m >= nv) break;
-        float* dst = St + (size_t)(4 * m) * ldt + row;
-        dst[0] = v[m].x;
-        dst[ldt] = v[m].y;
-        dst[2 * ldt] = v[m].z;
-        dst[3 * ldt] = v[m].w;
-      }
-    }
-  } else {
-    for (int row = threadIdx.x; row < rows; row += 256) {
-      const float* src = P + (size_t)row * r;
-      for (int c0 = 0; c0 < r; c0 += 16) {
-        float v[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) v[m] = (c0 + m < r) ? src[c0 + m] : 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m)
-          if (c0 + m < r) St[(size_t)(c0 + m) * ldt + row] = v[m];
-      }
-    }
-  }
-  const float* __restrict__ X = pb.rinv;
-  for (int e = threadIdx.x; e < r * r8; e += 256) {
-    const int m = e / r8, c = e % r8;
-    Xs[e] = c < r ? X[(size_t)m * r + c] : 0.f;
-  }
-  __syncthreads();  // no block-wide barrier after this point
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int co = warp % co_n, grp = warp / co_n;
-  if (grp >= ng) return;
-  const int c0 = 8 * co, q0 = grp * 256 + 8 * lane;
-  if (q0 >= rows) return;
-  float acc[8][8];
-#pragma unroll
-  for (int p = 0; p < 8; ++p)
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[p][q] = 0.f;
-  // X is upper triangular: rows m > c0 + 7 add nothing to these columns
-  const int mend = (c0 + 8) < r ? (c0 + 8) : r;
-#pragma unroll 2
-  for (int m = 0; m < mend; ++m) {
-    const float4 sa = *reinterpret_cast<const float4*>(St + (size_t)m * ldt + q0);
-    const float4 sb = *reinterpret_cast<const float4*>(St + (size_t)m * ldt + q0 + 4);
-    const float4 xa = *reinterpret_cast<const float4*>(Xs + m * r8 + c0);
-    const float4 xb = *reinterpret_cast<const float4*>(Xs + m * r8 + c0 + 4);
-    const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-    const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-    for (int p = 0; p < 8; ++p)
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[p][q] = fmaf(sv[p], xv[q], acc[p][q]);
-  }
-  const float scale = final_pass ? pb.scale : 1.0f;
-  const bool vec = (r & 3) == 0;
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    if (q0 + p >= rows) break;
-    float* out = P + (size_t)(q0 + p) * r + c0;
-    if (vec && c0 + 8 <= r) {
-      *reinterpret_cast<float4*>(out) =
-          make_float4(acc[p][0] * scale, acc[p][1] * scale, acc[p][2] * scale, acc[p][3] * scale);
-      *reinterpret_cast<float4*>(out + 4) =
-          make_float4(acc[p][4] * scale, acc[p][5] * scale, acc[p][6] * scale, acc[p][7] * scale);
-    } else {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (c0 + q < r) out[q] = acc[p][q] * scale;
-    }
-  }
-}
-
-// The same product for 32 <= r <= 64 with r a multiple of 4, pipelined: a block
-// takes up to kTriBlocks consecutive 256-row groups of one problem (the grid
-// lists exactly the groups that exist) and copies the next group into shared
-// memory (asynchronous 16-byte copies, row-major with the 16-byte chunks of
-// row R XOR-swizzled by (R / 8) % 8) while it computes the current one.  Its 16
-// warps each take one column quad co4 (8 x 4 outputs per lane, lane l the row
-// octet l); the quads are dealt so that every scheduler's four warps carry the
-// same triangular work (1 + 8 + 9 + 16 = 2 + 7 + 10 + 15 = ... rows of X).  Per
-// four rows m of X a thread reads its 8 x 4 staged values and 4 x 4 X values
-// (twelve 16-byte shared loads, conflict-free) for 128 FMAs.
-constexpr int kTriBlocks = 4;
-constexpr int kTriThreads = 512;
-__host__ __device__ inline int tri_pipe_chunks(int r) { return r > 32 ? 16 : 8; }  // 16-byte chunks per staged row
-__host__ __device__ inline bool tri_pipe_ok(int r) { return r >= 32 && r <= 64 && (r & 3) == 0; }
-__host__ __device__ inline size_t tri_pipe_smem_bytes(int r) {
-  return 2 * (size_t)256 * tri_pipe_chunks(r) * 16 + (size_t)r * ((r + 7) / 8 * 8) * 4;
-}
+// Rows of a problem per block of the triangular product, listed per problem.
 struct TriGrid {
   int blk_begin[kMaxBatch + 1];  // blocks of problem i: [blk_begin[i], blk_begin[i + 1])
 };
-__global__ void __launch_bounds__(kTriThreads, 1) tri_apply_pipe_kernel(const __grid_constant__ ProjBatch batch,
-                                                                        const __grid_constant__ TriGrid grid,
-                                                                        int final_pass) {
-  extern __shared__ __align__(16) float smem[];
-  int y = 0;  // this block's problem
-  {
-    int lo = 0, hi = batch.n - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (grid.blk_begin[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
-    }
-    y = lo;
-  }
-  const ProjProblem& pb = batch.p[y];
-  const int r = batch.r, r8 = (r + 7) / 8 * 8, ldc = tri_pipe_chunks(r), nc = r >> 2;
-  float* Sbuf = smem;                    // 2 x 256 rows x ldc chunks
-  float* Xs = smem + 2 * 256 * ldc * 4;  // r x r8
-  const int64_t first = (int64_t)((int)blockIdx.x - grid.blk_begin[y]) * kTriBlocks * 256;
-  const int64_t left = (pb.k - first + 255) / 256;
-  const int nblk = left < kTriBlocks ? (int)left : kTriBlocks;
-  float* P = pb.P;
-  auto stage = [&](int blk, int buf) {  // rows [row0, row0 + 256) into buffer buf, zero past k
-    const int64_t row0 = first + (int64_t)blk * 256;
-    const uint32_t base = (uint32_t)__cvta_generic_to_shared(Sbuf + (size_t)buf * 256 * ldc * 4);
-    for (int e = threadIdx.x; e < 256 * nc; e += kTriThreads) {
-      const int R = e / nc, c = e % nc;
-      const bool in = row0 + R < pb.k;
-      const float* src = in ? P + (row0 + R) * r + 4 * c : P;
-      const uint32_t dst = base + (uint32_t)(R * ldc + (c ^ ((R >> 3) & 7))) * 16u;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(in ? 16 : 0)
-                   : "memory");
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
-  stage(0, 0);
-  const float* __restrict__ X = pb.rinv;
-  for (int e = threadIdx.x; e < r * r8; e += kTriThreads) {
-    const int m = e / r8, c = e % r8;
-    Xs[e] = c < r ? X[(size_t)m * r + c] : 0.f;
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // scheduler warp % 4 holds the quads {s, 7 - s, 8 + s, 15 - s}
-  const int sch = warp & 3, slot = warp >> 2;
-  const int co4 = slot == 0 ? sch : slot == 1 ? 7 - sch : slot == 2 ? 8 + sch : 15 - sch;
-  const int c0 = 4 * co4, q0 = 8 * lane;
-  const bool busy = c0 < r;
-  const int mend = (c0 + 4) < r ? (c0 + 4) : r;  // X is upper triangular; a multiple of 4
-  const float scale = final_pass ? pb.scale : 1.0f;
-  for (int blk = 0; blk < nblk; ++blk) {
-    if (blk + 1 < nblk) {
-      stage(blk + 1, (blk + 1) & 1);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
-    __syncthreads();  // this group's rows (and X) are in shared memory
-    const int64_t row0 = first + (int64_t)blk * 256;
-    if (busy && row0 + q0 < pb.k) {
-      const float4* S4 = reinterpret_cast<const float4*>(Sbuf + (size_t)(blk & 1) * 256 * ldc * 4);
-      float acc[8][4];
-#pragma unroll
-      for (int p = 0; p < 8; ++p)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[p][q] = 0.f;
-      for (int m0 = 0; m0 < mend; m0 += 4) {
-        const int ch = (m0 >> 2) ^ (lane & 7);
-        float4 sv[8];
-#pragma unroll
-        for (int p = 0; p < 8; ++p) sv[p] = S4[(q0 + p) * ldc + ch];
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-          const float4 xa = *reinterpret_cast<const float4*>(Xs + (m0 + mm) * r8 + c0);
-          const float xv[4] = {xa.x, xa.y, xa.z, xa.w};
-#pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            const float sp = mm == 0 ? sv[p].x : mm == 1 ? sv[p].y : mm == 2 ? sv[p].z : sv[p].w;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(sp, xv[q], acc[p][q]);
-          }
-        }
-      }
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        if (row0 + q0 + p >= pb.k) break;
-        float* out = P + (row0 + q0 + p) * r + c0;
-        *reinterpret_cast<float4*>(out) =
-            make_float4(acc[p][0] * scale, acc[p][1] * scale, acc[p][2] * scale, acc[p][3] * scale);
-      }
-    }
-    __syncthreads();  // the buffer is refilled two groups on
-  }
-}
 
-// P rows <- (P rows) X on the tensor cores, for r <= 128: a block takes up to
+// P rows <- (P rows) X on the tensor cores: a block takes up to
 // kTtcRows consecutive rows of one problem (the grid lists the row groups that
 // exist), 128 at a time.  X (scaled by a power of two 2^g from its largest
-// magnitude) is split once per block into FP16 high and low parts and written
-// transposed into swizzled K-major tiles (row n of the tile is column n of X);
+// magnitude) is split into FP16 high and low parts and written transposed into
+// swizzled K-major tiles (row n of the tile is column n of X): all of it once
+// per block up to rank 128, above one 64-row chunk of X at a time per tile;
 // each 128-row tile of P likewise, each row m scaled by its own 2^e_m (row m of
 // P is row m of the tile, K = r in 64-wide chunks; a row's scale factors out
 // of its products).  tcgen05.mma (kind::f16,
@@ -587,9 +261,10 @@ constexpr int kTtcRows = 1024;
 constexpr int kTtcThreads = 256;
 __host__ __device__ inline int ttc_npad(int r) { return (r + 15) / 16 * 16; }
 __host__ __device__ inline int ttc_kc(int r) { return (ttc_npad(r) + 63) / 64; }
-__host__ __device__ inline bool ttc_ok(int r) { return r <= 128; }
+// chunks of X^T held at once: all of them up to rank 128, else one at a time
+__host__ __device__ inline int ttc_bchunks(int r) { return ttc_kc(r) <= 2 ? ttc_kc(r) : 1; }
 __host__ __device__ inline size_t ttc_smem_bytes(int r) {
-  return (size_t)ttc_kc(r) * 2 * 16384 + (size_t)ttc_kc(r) * 2 * ttc_npad(r) * 128 + 1024;
+  return (size_t)ttc_kc(r) * 2 * 16384 + (size_t)ttc_bchunks(r) * 2 * ttc_npad(r) * 128 + 1024;
 }
 __host__ __device__ inline uint32_t ttc_tmem_cols(int r) {
   uint32_t c = 32;
@@ -644,7 +319,7 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
     y = lo;
   }
   const ProjProblem& pb = batch.p[y];
-  const int r = batch.r, npad = ttc_npad(r), kc = ttc_kc(r);
+  const int r = batch.r, npad = ttc_npad(r), kc = ttc_kc(r), nbc = ttc_bchunks(r);
   const uint32_t cols = ttc_tmem_cols(r);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t first = (int64_t)((int)blockIdx.x - grid.blk_begin[y]) * kTtcRows;
@@ -661,7 +336,7 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
     tc::fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, cols);
-  for (uint32_t e = tid; e < (uint32_t)((kc * 2 * 16384 + kc * 2 * npad * 128) / 16); e += kTtcThreads)
+  for (uint32_t e = tid; e < (uint32_t)((kc * 2 * 16384 + nbc * 2 * npad * 128) / 16); e += kTtcThreads)
     tc::sts128(base + 16u * e, make_uint4(0, 0, 0, 0));
   float m = 0.f;
   for (int e = tid; e < r * r; e += kTtcThreads) {
@@ -672,12 +347,13 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
   const int g = ttc_exponent(ttc_block_max(m, wmax));  // (its barriers also publish the zeroed tiles)
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  // B = X^T split: item (column n of X, chunk c, 8-row group k8) is one
-  // 16-byte chunk of tile row n; consecutive threads take consecutive n
-  {
-    const float sx = ldexpf(1.f, g);
-    for (int it = tid; it < r * kc * 8; it += kTtcThreads) {
-      const int n = it % r, rest = it / r, k8 = rest & 7, c = rest >> 3;
+  // B = X^T split, chunk c into the buffer at bc: item (column n of X,
+  // 8-row group k8) is one 16-byte chunk of tile row n; consecutive threads
+  // take consecutive n, so that each row of X is read coalesced
+  const float sx = ldexpf(1.f, g);
+  auto convert_b = [&](int c, uint32_t bc) {
+    for (int it = tid; it < r * 8; it += kTtcThreads) {
+      const int n = it % r, k8 = it / r;
       uint32_t hv[4], lv[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -686,15 +362,19 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
         hv[t] = ttc_split2(x0 * sx, x1 * sx, lv[t]);
       }
       const uint32_t off = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((k8 ^ (n & 7)) << 4));
-      const uint32_t bc = b_s + (uint32_t)c * 2 * b_part;
       tc::sts128(bc + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
       tc::sts128(bc + b_part + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
     }
-  }
+  };
+  if (nbc == kc)  // all of X^T, once per block
+    for (int c = 0; c < kc; ++c) convert_b(c, b_s + (uint32_t)c * 2 * b_part);
   const uint32_t idesc = tc::idesc_f16(128, npad, false, false);
   const float out_scale = final_pass ? pb.scale : 1.0f;
   const bool vec = (r & 3) == 0;
-  const int per_row = 8 * kc;  // conversion items of one row: consecutive threads (8 or 16)
+  // conversion items of one row: 8 per 64-wide chunk, padded to a power of two
+  // (8, 16 or 32 consecutive threads, which reduce the row's maximum by shuffles)
+  const int kcp = kc == 3 ? 4 : kc;
+  const int per_row = 8 * kcp;
   uint32_t phase = 0;
   bool live = true;
   for (int64_t row0 = first; row0 < last && live; row0 += 128) {
@@ -703,17 +383,17 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
     // (row m, chunk c, 8-column group k8), the items of a row on consecutive
     // threads, which find the row's largest magnitude together
     for (int it = tid; it < 128 * per_row; it += kTtcThreads) {
-      const int k8 = it & 7, c = (it >> 3) % kc, mr = it / per_row;
-      const int k0 = c * 64 + k8 * 8;
+      const int k8 = it & 7, c = (it >> 3) & (kcp - 1), mr = it / per_row;
+      const int k0 = c * 64 + k8 * 8;  // c >= kc: padding items (zeros, not stored)
       const float* src = P + (row0 + mr) * r + k0;
       float x[8];
-      if (vec && mr < rows && k0 + 8 <= r) {  // two 16-byte loads (rows start on 16 bytes when 4 | r)
+      if (vec && mr < rows && c < kc && k0 + 8 <= r) {  // two 16-byte loads (rows start on 16 bytes when 4 | r)
         const float4 u0 = reinterpret_cast<const float4*>(src)[0], u1 = reinterpret_cast<const float4*>(src)[1];
         x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
         x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
       } else {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = (mr < rows && k0 + t < r) ? src[t] : 0.f;
+        for (int t = 0; t < 8; ++t) x[t] = (mr < rows && c < kc && k0 + t < r) ? src[t] : 0.f;
       }
       float mx = 0.f;
 #pragma unroll
@@ -728,29 +408,46 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
       uint32_t hv[4], lv[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) hv[t] = ttc_split2(x[2 * t] * sp, x[2 * t + 1] * sp, lv[t]);
-      const uint32_t off = (uint32_t)((mr >> 3) * 1024 + (mr & 7) * 128 + ((k8 ^ (mr & 7)) << 4));
-      const uint32_t ac = a_s + (uint32_t)c * 2 * 16384;
-      tc::sts128(ac + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
-      tc::sts128(ac + 16384 + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
-    }
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc::tc_fence_after();
-      for (int c = 0; c < kc; ++c) {
-        const uint32_t ac = a_s + (uint32_t)c * 2 * 16384, bc = b_s + (uint32_t)c * 2 * b_part;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ah = tc::sdesc_sw128(ac + kk * 32, 16, 1024), al = tc::sdesc_sw128(ac + 16384 + kk * 32, 16, 1024);
-          const uint64_t bh = tc::sdesc_sw128(bc + kk * 32, 16, 1024), bl = tc::sdesc_sw128(bc + b_part + kk * 32, 16, 1024);
-          tc::mma_bf16(tmem, ah, bh, idesc, (c > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_bf16(tmem, ah, bl, idesc, 1u);
-          tc::mma_bf16(tmem, al, bh, idesc, 1u);
-        }
+      if (c < kc) {
+        const uint32_t off = (uint32_t)((mr >> 3) * 1024 + (mr & 7) * 128 + ((k8 ^ (mr & 7)) << 4));
+        const uint32_t ac = a_s + (uint32_t)c * 2 * 16384;
+        tc::sts128(ac + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
+        tc::sts128(ac + 16384 + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
       }
-      tc::mma_commit(&mma_bar);
     }
-    live = tc::mbar_wait(&mma_bar, phase, &abort_flag, nullptr, 0);
+    // the K chunks' MMAs: with X^T resident one batch; else per chunk, each
+    // chunk of X^T converted once the previous chunk's MMAs have read the buffer
+    const int nb = nbc == kc ? 1 : kc;
+    for (int bi = 0; bi < nb && live; ++bi) {
+      if (nbc != kc) {
+        if (bi > 0) {
+          live = tc::mbar_wait(&mma_bar, phase, &abort_flag, nullptr, 0);
+          phase ^= 1u;
+          live = __syncthreads_and(live);
+          if (!live) break;
+        }
+        convert_b(bi, b_s);
+      }
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc::tc_fence_after();
+        const int c0 = nbc == kc ? 0 : bi, c1 = nbc == kc ? kc : bi + 1;
+        for (int c = c0; c < c1; ++c) {
+          const uint32_t ac = a_s + (uint32_t)c * 2 * 16384, bc = b_s + (uint32_t)(nbc == kc ? c : 0) * 2 * b_part;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ah = tc::sdesc_sw128(ac + kk * 32, 16, 1024), al = tc::sdesc_sw128(ac + 16384 + kk * 32, 16, 1024);
+            const uint64_t bh = tc::sdesc_sw128(bc + kk * 32, 16, 1024), bl = tc::sdesc_sw128(bc + b_part + kk * 32, 16, 1024);
+            tc::mma_bf16(tmem, ah, bh, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_bf16(tmem, ah, bl, idesc, 1u);
+            tc::mma_bf16(tmem, al, bh, idesc, 1u);
+          }
+        }
+        tc::mma_commit(&mma_bar);
+      }
+    }
+    if (live) live = tc::mbar_wait(&mma_bar, phase, &abort_flag, nullptr, 0);
     phase ^= 1u;
     live = __syncthreads_and(live);
     tc::tc_fence_after();
@@ -824,59 +521,23 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
     gb.e[i].out = batch.p[i].gram;
   }
   const size_t chol_smem = sizeof(float) * chol_smem_floats(r);
-  const int apply_rows = tri_rows(r);
-  const size_t apply_smem = sizeof(float) * tri_smem_floats(r);
   cudaError_t err = cudaFuncSetAttribute(chol_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)chol_smem);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(tri_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)apply_smem);
+  // the triangular products on the tensor cores, kTtcRows rows of one problem per block
+  const size_t tc_smem = ttc_smem_bytes(r);
+  err = cudaFuncSetAttribute(tri_apply_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem);
   if (err != cudaSuccess) return err;
-  // the triangular products: on the tensor cores up to rank 128, else SIMT
-  const bool tcore = ttc_ok(r);
-  const size_t tc_smem = tcore ? ttc_smem_bytes(r) : 0;
-  if (tcore) {
-    err = cudaFuncSetAttribute(tri_apply_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem);
-    if (err != cudaSuccess) return err;
-  }
-  const bool pipe = !tcore && tri_pipe_ok(r);
-  const size_t pipe_smem = pipe ? tri_pipe_smem_bytes(r) : 0;
-  if (pipe) {
-    err = cudaFuncSetAttribute(tri_apply_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)pipe_smem);
-    if (err != cudaSuccess) return err;
-  }
   static thread_local TriGrid tg;
-  if (tcore || pipe) {
-    const int64_t rows = tcore ? kTtcRows : (int64_t)256 * kTriBlocks;
-    tg.blk_begin[0] = 0;
-    for (int i = 0; i < batch.n; ++i) tg.blk_begin[i + 1] = tg.blk_begin[i] + (int)ceil_div(batch.p[i].k, rows);
-  }
-  const bool small = !tcore && !pipe && r <= 64;
-  const int small_rows = small ? tri_rows_small(r) : 0;
-  const size_t small_smem = small ? sizeof(float) * tri_small_smem_floats(r) : 0;
-  if (small) {
-    err = cudaFuncSetAttribute(tri_apply_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)small_smem);
-    if (err != cudaSuccess) return err;
-  }
+  tg.blk_begin[0] = 0;
+  for (int i = 0; i < batch.n; ++i) tg.blk_begin[i + 1] = tg.blk_begin[i] + (int)ceil_div(batch.p[i].k, (int64_t)kTtcRows);
   for (int pass = 0; pass < 2; ++pass) {
     err = launch_gram(gb, stream, true);
     if (err != cudaSuccess) return err;
     count_launch();
     chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch);
     count_launch();
-    if (tcore)
-      tri_apply_tc_kernel<<<(unsigned)tg.blk_begin[batch.n], kTtcThreads, tc_smem, stream>>>(batch, tg, pass == 1);
-    else if (pipe)
-      tri_apply_pipe_kernel<<<(unsigned)tg.blk_begin[batch.n], kTriThreads, pipe_smem, stream>>>(batch, tg,
-                                                                                                  pass == 1);
-    else if (small)
-      tri_apply_small_kernel<<<dim3((unsigned)ceil_div(max_k, small_rows), batch.n), 256, small_smem, stream>>>(
-          batch, pass == 1);
-    else
-      tri_apply_kernel<<<dim3((unsigned)ceil_div(max_k, apply_rows), batch.n), 256, apply_smem, stream>>>(
-          batch, pass == 1);
+    tri_apply_tc_kernel<<<(unsigned)tg.blk_begin[batch.n], kTtcThreads, tc_smem, stream>>>(batch, tg, pass == 1);
   }
   return cudaGetLastError();
 }

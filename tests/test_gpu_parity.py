@@ -68,7 +68,7 @@ def test_rademacher_bit_exact(k, r, layer, step):
 @pytest.mark.parametrize("k,r,layer,step", [(512, 16, 0, 0), (4096, 64, 2, 1), (12288, 64, 5, 3),
                                             (2048, 256, 1, 0), (1000, 50, 4, 7), (64, 16, 0, 2),
                                             (8192, 4, 3, 3), (1600, 200, 2, 1), (640, 33, 0, 0),
-                                            (2048, 128, 1, 2)])
+                                            (2048, 128, 1, 2), (1000, 136, 3, 0), (4096, 192, 2, 2)])
 def test_qr_projection_matches_oracle(k, r, layer, step):
     P = torch.empty(k, r, dtype=torch.float32, device=DEV)
     status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
