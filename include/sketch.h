@@ -106,10 +106,14 @@ SKETCH_API size_t sketch_workspace_bytes(sketch_op op, int64_t T, int64_t d, int
  * Compression", "How it works": a new random projection after every update;
  * "LoGRA: Low-Rank Gradient Sketches", "Why Refreshing the Projection
  * Enables New Update Directions").
- * SKETCH_PROJ_GAUSSIAN_QR needs 4*r <= k (CholeskyQR2 in fp32 keeps the frame
- * orthonormal to ~1e-6 only for well-conditioned Gaussian matrices) and a
- * workspace; it reports a QR breakdown in *dev_status (nullable) as
- * SKETCH_DEV_QR_BREAKDOWN.  SKETCH_PROJ_RADEMACHER needs no workspace. */
+ * SKETCH_PROJ_GAUSSIAN_QR needs r <= k (SKETCH_ERR_INVALID_ARG otherwise) and
+ * a workspace.  For 4*r <= k the frame comes from CholeskyQR2 in fp32 (the
+ * Gaussian matrix is then well conditioned; P^T P = (k/r) I to ~1e-6), and a
+ * QR breakdown is reported in *dev_status (nullable) as
+ * SKETCH_DEV_QR_BREAKDOWN.  For r <= k < 4*r, up to the square case r = k
+ * where P P^T = I, it comes from Householder QR in fp64, one thread block per
+ * problem (a few ms at the largest size), which cannot break down.
+ * SKETCH_PROJ_RADEMACHER needs no workspace. */
 SKETCH_API sketch_status sketch_sample_projection(sketch_proj_kind kind, uint64_t seed, uint32_t layer,
                                        uint32_t step, int64_t k, int64_t r, float* P,
                                        int32_t* dev_status, void* ws, size_t ws_bytes,

@@ -179,50 +179,62 @@ sketch_status do_sample(sketch_proj_kind kind, uint64_t seed, uint32_t step, int
     TRY(check_projection(probs[i]));
     if (probs[i].k * r > (int64_t(1) << 34)) return fail(SKETCH_ERR_INVALID_ARG, "k*r too large");
     if (kind == SKETCH_PROJ_GAUSSIAN_QR) {
-      if (4 * r > probs[i].k)
-        return fail(SKETCH_ERR_UNSUPPORTED, "Gaussian-QR projection needs 4*r <= k (k=%lld, r=%lld)",
+      if (r > probs[i].k)
+        return fail(SKETCH_ERR_INVALID_ARG, "Gaussian-QR projection needs r <= k (k=%lld, r=%lld)",
                     (long long)probs[i].k, (long long)r);
       need += qr_ws_bytes(probs[i].k, r);
     }
   }
   if (kind == SKETCH_PROJ_GAUSSIAN_QR) TRY(check_ws(ws, ws_bytes, need));
-  static thread_local rgs::ProjBatch batch;
+  // Up to two batches are filled at once: CholeskyQR2 frames (and Rademacher
+  // draws) in `batch`, fp64 Householder frames (r <= k < 4r) in `wide`; each is
+  // launched when full and at the end.
+  static thread_local rgs::ProjBatch batch, wide;
+  for (rgs::ProjBatch* b : {&batch, &wide}) {
+    b->n = 0;
+    b->r = (int)r;
+    b->seed = seed;
+    b->step = step;
+  }
   rgs::WsCursor cur;
   cur.base = static_cast<char*>(ws);
-  int32_t* first_status = nullptr;
+  int32_t* status = dev_status;
   cudaError_t err = cudaSuccess;
-  for (int base = 0; base < n && err == cudaSuccess; base += rgs::kMaxBatch) {
-    const int m = (n - base) < rgs::kMaxBatch ? (n - base) : rgs::kMaxBatch;
-    batch.n = m;
-    batch.r = (int)r;
-    batch.seed = seed;
-    batch.step = step;
-    int64_t max_k = 0;
-    for (int i = 0; i < m; ++i) {
-      const sketch_projection_problem& pr = probs[base + i];
-      rgs::ProjProblem& pb = batch.p[i];
-      pb.P = pr.P;
-      pb.k = pr.k;
-      pb.layer = pr.layer;
-      max_k = pr.k > max_k ? pr.k : max_k;
-      if (kind == SKETCH_PROJ_RADEMACHER) {
-        pb.scale = (float)(1.0 / std::sqrt((double)r));
-      } else {
-        rgs::carve_qr_workspace(cur, pr.k, (int)r, &pb);
-        int32_t* scratch = cur.take<int32_t>(1);
-        cur.take<char>(0);
-        if (first_status == nullptr) first_status = scratch;
-        pb.scale = (float)std::sqrt((double)pr.k / (double)r);
-      }
-    }
+  int64_t max_k = 0;
+  auto flush = [&](rgs::ProjBatch& b) {
+    if (b.n == 0 || err != cudaSuccess) return;
     if (kind == SKETCH_PROJ_RADEMACHER) {
-      err = rgs::launch_rademacher(batch, max_k, s);
+      err = rgs::launch_rademacher(b, max_k, s);
     } else {
-      batch.status = dev_status ? dev_status : first_status;
-      if (base == 0) err = cudaMemsetAsync(batch.status, 0, sizeof(int32_t), s);
-      if (err == cudaSuccess) err = rgs::launch_gaussian_qr(batch, max_k, s);
+      b.status = status;
+      err = (&b == &wide) ? rgs::launch_wide_qr(b, s) : rgs::launch_gaussian_qr(b, max_k, s);
     }
+    if (&b == &batch) max_k = 0;
+    b.n = 0;
+  };
+  for (int i = 0; i < n && err == cudaSuccess; ++i) {
+    const sketch_projection_problem& pr = probs[i];
+    const bool is_wide = kind == SKETCH_PROJ_GAUSSIAN_QR && rgs::qr_is_wide(pr.k, r);
+    rgs::ProjBatch& b = is_wide ? wide : batch;
+    rgs::ProjProblem& pb = b.p[b.n++];
+    pb.P = pr.P;
+    pb.k = pr.k;
+    pb.layer = pr.layer;
+    if (kind == SKETCH_PROJ_RADEMACHER) {
+      pb.scale = (float)(1.0 / std::sqrt((double)r));
+    } else {
+      rgs::carve_qr_workspace(cur, pr.k, (int)r, &pb);
+      int32_t* scratch = cur.take<int32_t>(1);
+      cur.take<char>(0);
+      if (status == nullptr) status = scratch;
+      pb.scale = (float)std::sqrt((double)pr.k / (double)r);
+      if (i == 0) err = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
+    }
+    if (!is_wide) max_k = pr.k > max_k ? pr.k : max_k;
+    if (b.n == rgs::kMaxBatch) flush(b);
   }
+  flush(batch);
+  flush(wide);
   if (err == cudaSuccess && kind == SKETCH_PROJ_RADEMACHER && dev_status)
     err = cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s);
   return launch_result(err, "sample_projection");

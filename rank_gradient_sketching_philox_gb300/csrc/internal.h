@@ -108,6 +108,7 @@ struct ProjProblem {
   float2* partials; // QR: nchunks(k) x r x r (hi, lo) pairs
   double* gram;     // QR: r x r
   float* rinv;      // QR: r x r
+  double* wide;     // QR with r <= k < 4r: two k x r fp64 arrays (the others unused)
 };
 struct ProjBatch {
   int n;
@@ -119,6 +120,9 @@ struct ProjBatch {
 };
 // Workspace of one QR problem.
 void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p);
+// Frames with r <= k < 4r go to the fp64 Householder kernel, the rest to CholeskyQR2.
+inline bool qr_is_wide(int64_t k, int64_t r) { return 4 * r > k; }
+cudaError_t launch_wide_qr(const ProjBatch& batch, cudaStream_t stream);
 
 cudaError_t launch_rademacher(const ProjBatch& batch, int64_t max_k, cudaStream_t stream);
 cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream_t stream);

@@ -6,11 +6,15 @@
 //
 // Gaussian QR: P = sqrt(k/r) Q with Q the orthonormal factor of a Gaussian
 // k x r matrix and diag(R) > 0 ("Randomized Gradient Compression",
-// footnote 1).  The frame is computed by CholeskyQR2 in fp32: twice
-// (Gram A = G^T G, Cholesky A = R^T R, G <- G R^-1).  Cholesky factors have a
-// positive diagonal, so the result is the sign-corrected QR factor without an
-// explicit sign fix.  For 4r <= k the Gaussian matrix is well conditioned and
-// the second pass leaves P^T P = (k/r) I to about 1e-6.
+// footnote 1).  For 4r <= k the frame is computed by CholeskyQR2 in fp32:
+// twice (Gram A = G^T G, Cholesky A = R^T R, G <- G R^-1).  Cholesky factors
+// have a positive diagonal, so the result is the sign-corrected QR factor
+// without an explicit sign fix.  There the Gaussian matrix is well conditioned
+// and the second pass leaves P^T P = (k/r) I to about 1e-6.
+// For r <= k < 4r (at most 1023 x 256, up to square) the Gaussian matrix can be
+// as ill conditioned as a square one, whose condition number grows like k, so
+// the frame is drawn and factored in fp64 by Householder QR, one block per
+// problem (wide_qr_kernel), and the signs of R's diagonal applied explicitly.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -485,9 +489,151 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
   if (warp == 0) tc::tmem_dealloc(tmem, cols);
 }
 
+
+// ---- fp64 Householder QR for r <= k < 4r ------------------------------------
+// One block per problem.  The block draws the Gaussian matrix G (k x r) in fp64
+// from the same Philox stream as gaussian_kernel (Box-Muller in double, as the
+// exact definition reads), factors it by Householder reflections
+// H_j = I - tau_j v_j v_j^T, forms Q = H_0 ... H_{r-1} [I; 0], flips the columns
+// whose R_jj is negative and writes P = sqrt(k/r) Q rounded to fp32.
+// Workspace: two column-major k x r fp64 arrays (column l of G, then of Q, is
+// k contiguous doubles): `a` holds G, then R above the diagonal and v_j from
+// the diagonal down; `q` holds Q.  A k x r problem touches about 4 k r^2
+// doubles in L1/L2, a few ms at the largest size (1016 x 256).
+constexpr int kWqThreads = 512, kWqWarps = kWqThreads / 32, kWqMaxK = 1024;
+
+__device__ __forceinline__ double wq_warp_sum(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__global__ void __launch_bounds__(kWqThreads) wide_qr_kernel(const ProjBatch batch) {
+  __shared__ double vsh[kWqMaxK];           // the current reflector, rows j .. k-1
+  __shared__ double tau[kMaxRank], diag[kMaxRank];
+  __shared__ double red[kWqWarps];
+  __shared__ double norm2;                  // ||a[j:, j]||^2 of the next column
+  const ProjProblem& pb = batch.p[blockIdx.x];
+  const int k = (int)pb.k, r = batch.r;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  double* a = pb.wide;
+  double* q = pb.wide + (size_t)k * r;
+
+  // G: element e = i*r + l from Philox block e/4, lane e%4 (as gaussian4)
+  for (int b = tid; b < k * r / 4; b += kWqThreads) {
+    const Philox4 blk = stream_block(batch.seed, pb.layer, batch.step, kTagGaussian, (uint32_t)b);
+    const uint32_t w[4] = {blk.w0, blk.w1, blk.w2, blk.w3};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const double ua = ((double)w[2 * t] + 0.5) * 0x1p-32;
+      const double ub = ((double)w[2 * t + 1] + 0.5) * 0x1p-32;
+      const double radius = sqrt(-2.0 * log(ua));
+      double sn, cs;
+      sincospi(2.0 * ub, &sn, &cs);
+      const int e0 = 4 * b + 2 * t;
+      a[(size_t)(e0 % r) * k + e0 / r] = radius * cs;
+      a[(size_t)((e0 + 1) % r) * k + (e0 + 1) / r] = radius * sn;
+    }
+  }
+  __syncthreads();
+  {  // ||a[:, 0]||^2
+    double s = 0.0;
+    for (int i = tid; i < k; i += kWqThreads) s += a[i] * a[i];
+    s = wq_warp_sum(s);
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+      double t = 0.0;
+      for (int w = 0; w < kWqWarps; ++w) t += red[w];
+      norm2 = t;
+    }
+    __syncthreads();
+  }
+
+  // factorization, one column at a time
+  for (int j = 0; j < r; ++j) {
+    double* aj = a + (size_t)j * k;
+    const double x0 = aj[j], nrm2 = norm2;
+    const double alpha = x0 >= 0.0 ? -sqrt(nrm2) : sqrt(nrm2);
+    const double v0 = x0 - alpha;
+    const double vnorm2 = (nrm2 - x0 * x0) + v0 * v0;
+    const bool skip = !(vnorm2 > 0.0);  // a zero column: H_j = I, R_jj = x0
+    const double tj = skip ? 0.0 : 2.0 / vnorm2;
+    for (int i = j + tid; i < k; i += kWqThreads) vsh[i] = (i == j) ? v0 : aj[i];
+    __syncthreads();  // every thread has read x0 and norm2; vsh is complete
+    if (tid == 0) {
+      tau[j] = tj;
+      diag[j] = skip ? x0 : alpha;
+      aj[j] = v0;
+    }
+    if (!skip) {
+      for (int c = j + 1 + warp; c < r; c += kWqWarps) {
+        double* ac = a + (size_t)c * k;
+        double dot = 0.0;
+        for (int i = j + lane; i < k; i += 32) dot += vsh[i] * ac[i];
+        const double f = tj * wq_warp_sum(dot);
+        double s = 0.0;
+        for (int i = j + lane; i < k; i += 32) {
+          const double x = fma(-f, vsh[i], ac[i]);
+          ac[i] = x;
+          if (i > j) s += x * x;
+        }
+        if (c == j + 1) {
+          s = wq_warp_sum(s);
+          if (lane == 0) norm2 = s;
+        }
+      }
+    } else if (j + 1 < r && warp == 0) {
+      const double* ac = a + (size_t)(j + 1) * k;
+      double s = 0.0;
+      for (int i = j + 1 + lane; i < k; i += 32) s += ac[i] * ac[i];
+      s = wq_warp_sum(s);
+      if (lane == 0) norm2 = s;
+    }
+    __syncthreads();
+  }
+
+  // Q = H_0 ... H_{r-1} [I; 0], right to left; H_j touches rows j.. of columns j..
+  for (int e = tid; e < k * r; e += kWqThreads) q[e] = (e % k == e / k) ? 1.0 : 0.0;
+  __syncthreads();
+  for (int j = r - 1; j >= 0; --j) {
+    const double tj = tau[j];
+    if (tj == 0.0) continue;  // uniform over the block
+    const double* aj = a + (size_t)j * k;
+    for (int i = j + tid; i < k; i += kWqThreads) vsh[i] = aj[i];
+    __syncthreads();
+    for (int c = j + warp; c < r; c += kWqWarps) {
+      double* qc = q + (size_t)c * k;
+      double dot = 0.0;
+      for (int i = j + lane; i < k; i += 32) dot += vsh[i] * qc[i];
+      const double f = tj * wq_warp_sum(dot);
+      for (int i = j + lane; i < k; i += 32) qc[i] = fma(-f, vsh[i], qc[i]);
+    }
+    __syncthreads();
+  }
+
+  // P = sqrt(k/r) sign(R_ll) Q, row-major fp32
+  const double scale = sqrt((double)k / (double)r);
+  for (int e = tid; e < k * r; e += kWqThreads) {
+    const int i = e / r, l = e % r;
+    const double sg = diag[l] < 0.0 ? -scale : scale;
+    pb.P[e] = (float)(sg * q[(size_t)l * k + i]);
+  }
+}
+
 }  // namespace
 
 void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
+  if (qr_is_wide(k, r)) {
+    double* a = cur.take<double>((size_t)2 * k * r);
+    if (p) {
+      p->partials = nullptr;
+      p->gram = nullptr;
+      p->rinv = nullptr;
+      p->wide = a;
+    }
+    return;
+  }
   const GramChunks g = gram_chunks(k);
   float2* partials = cur.take<float2>((size_t)g.nchunks * r * r);
   double* gram = cur.take<double>((size_t)r * r);
@@ -496,6 +642,7 @@ void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
     p->partials = partials;
     p->gram = gram;
     p->rinv = rinv;
+    p->wide = nullptr;
   }
 }
 
@@ -503,6 +650,12 @@ cudaError_t launch_rademacher(const ProjBatch& batch, int64_t max_k, cudaStream_
   const int64_t words = ceil_div(max_k * batch.r, 32);
   count_launch();
   rademacher_kernel<<<dim3((unsigned)ceil_div(words, 256), batch.n), 256, 0, stream>>>(batch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wide_qr(const ProjBatch& batch, cudaStream_t stream) {
+  count_launch();
+  wide_qr_kernel<<<batch.n, kWqThreads, 0, stream>>>(batch);
   return cudaGetLastError();
 }
 

@@ -61,7 +61,7 @@ def sweep(Ds, Xs, ranks=(4, 16, 64, 256), steps=8):
     rows = []
     for kind in (binding.PROJ_RADEMACHER, binding.PROJ_GAUSSIAN_QR):
         for r in ranks:
-            if kind == binding.PROJ_GAUSSIAN_QR and 4 * r > k:
+            if kind == binding.PROJ_GAUSSIAN_QR and r > k:
                 continue
             for refreshed in (False, True):
                 cos, rel = reconstruction(Ds, Xs, r, kind, steps=steps, refreshed=refreshed)

@@ -81,11 +81,46 @@ def test_qr_projection_matches_oracle(k, r, layer, step):
     assert np.abs(M - (k / r) * np.eye(r)).max() / (k / r) < 1e-5
 
 
-def test_qr_rejects_wide_frames():
-    P = torch.empty(32, 16, dtype=torch.float32, device=DEV)
+@pytest.mark.parametrize("k,r,layer,step", [(32, 16, 0, 0), (64, 64, 1, 0), (8, 8, 2, 1), (8, 3, 0, 4),
+                                            (200, 56, 3, 2), (1000, 251, 1, 1), (1016, 256, 4, 0),
+                                            (256, 256, 0, 3), (520, 136, 2, 5)])
+def test_wide_qr_projection_matches_oracle(k, r, layer, step):
+    """Frames with r <= k < 4r (fp64 Householder on the device), up to square
+    ones, whose Gaussian matrix has a condition number of order k: the frame
+    matches the exact one to fp32 rounding, and P^T P = (k/r) I; for r = k the
+    frame is orthogonal, so P P^T = I as well."""
+    P = torch.empty(k, r, dtype=torch.float32, device=DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 77, layer, step, P, dev_status=status)
+    assert int(status.item()) == 0
+    got = P.cpu().numpy().astype(np.float64)
+    ref = orc.sample_qr(77, layer, step, k, r)
+    assert rel_fro(got, ref) < 1e-6
+    M = got.T @ got
+    assert np.abs(M - (k / r) * np.eye(r)).max() / (k / r) < 1e-6
+    if r == k:
+        assert np.abs(got @ got.T - np.eye(k)).max() < 1e-6
+
+
+def test_qr_mixed_batch_matches_oracle():
+    """One batched call over frames of both kinds (CholeskyQR2 for 4r <= k,
+    Householder below), in an interleaved order."""
+    r, seed, step = 64, 23, 4
+    ks = [64, 1024, 200, 256, 512, 136, 4096]
+    Ps = [torch.empty(k, r, dtype=torch.float32, device=DEV) for k in ks]
+    layers = [5 + i for i in range(len(ks))]
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    rgs.sample_projection_batched(rgs.PROJ_GAUSSIAN_QR, seed, step, Ps, layers, dev_status=status)
+    assert int(status.item()) == 0
+    for P, k, layer in zip(Ps, ks, layers):
+        assert rel_fro(P.cpu().numpy(), orc.sample_qr(seed, layer, step, k, r)) < 1e-5, k
+
+
+def test_qr_rejects_rank_above_width():
+    P = torch.empty(16, 32, dtype=torch.float32, device=DEV)
     with pytest.raises(binding.SketchError) as ei:
         rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 0, 0, 0, P)
-    assert ei.value.status == binding.ERR_UNSUPPORTED
+    assert ei.value.status == binding.ERR_INVALID_ARG
 
 
 def test_projection_deterministic():
@@ -397,10 +432,11 @@ def _rand_c(d, r, seed, scale=1.0):
 @pytest.mark.parametrize("d,k,r,kind", [(256, 512, 16, 1), (256, 512, 16, 0), (40, 24, 4, 0),
                                         (130, 136, 20, 1), (1024, 2048, 128, 1), (200, 520, 96, 1),
                                         (100, 600, 136, 1), (96, 256, 48, 0),
-                                        (300, 4096, 256, 1), (7, 8, 1, 0)])
+                                        (300, 4096, 256, 1), (7, 8, 1, 0), (192, 256, 256, 1),
+                                        (64, 200, 72, 1)])
 def test_normsgd_matches_oracle(d, k, r, kind):
     W0 = synth.layer_weight(d, k, 3)
-    P = (orc.sample_qr(2, 3, 1, k, r) if kind == 1 and 4 * r <= k
+    P = (orc.sample_qr(2, 3, 1, k, r) if kind == 1 and r <= k
          else orc.sample_rademacher(2, 3, 1, k, r))
     C = _rand_c(d, r, d + k)
     W = W0.to(DEV)
@@ -413,6 +449,32 @@ def test_normsgd_matches_oracle(d, k, r, kind):
     assert st == 0
     _w_check(bits(W), W_or)
     assert abs(out.item() - orc.norm_w(W_or) ** 2) <= 1e-6 * orc.norm_w(W_or) ** 2
+
+
+def test_square_frame_update_is_dense_normalized_sgd():
+    """r = k: the device's own orthogonal frame makes H = C P^T the gradient
+    G itself, so the device update is the textbook dense normalized SGD step
+    W - tau ||W|| G / ||G||, rounded stochastically: every new weight lies
+    within one BF16 step of that value, and W matches the oracle's update."""
+    d, k = 160, 256
+    r, tau = k, 1e-2
+    P = torch.empty(k, r, dtype=torch.float32, device=DEV)
+    rgs.sample_projection(rgs.PROJ_GAUSSIAN_QR, 31, 2, 5, P)
+    Pn = P.cpu().numpy()
+    G = np.random.default_rng(12).standard_normal((d, k))
+    C = (G @ Pn.astype(np.float64)).astype(np.float32)
+    W0 = synth.layer_weight(d, k, 4)
+    W = W0.to(DEV)
+    rgs.apply_update_normsgd(W, torch.from_numpy(C).to(DEV), P, tau, 9, 2, 5)
+    W_or, st, _ = orc.update_normsgd(bits(W0), C, Pn, tau, 9, 2, 5, dense_h_norm=True)
+    assert st == 0
+    _w_check(bits(W), W_or)
+    w0 = orc.bf16_to_f32(bits(W0)).astype(np.float64)
+    text = w0 - tau * np.linalg.norm(w0) * G / np.linalg.norm(G)
+    got = orc.bf16_to_f32(bits(W)).astype(np.float64)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(text), 2.0 ** -126))) - 7)
+    step = tau * np.linalg.norm(w0) * np.abs(G).max() / np.linalg.norm(G)
+    assert np.all(np.abs(got - text) <= ulp + 1e-5 * step)
 
 
 def test_normsgd_strided_w_keeps_padding():
