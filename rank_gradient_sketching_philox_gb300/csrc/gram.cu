@@ -225,6 +225,37 @@ __device__ __forceinline__ uint32_t gtc_pack(float y0, float y1, uint32_t& lo) {
   lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
   return (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
 }
+// Largest magnitude of n floats from p (NaN if any is NaN): float4 loads, four
+// in flight per thread, once p is 16-byte aligned.
+__device__ __forceinline__ float gtc_chunk_max(const float* __restrict__ p, int64_t n) {
+  float m = 0.f;
+  auto take = [&](float x) { m = (m != m || x != x) ? __int_as_float(0x7FC00000) : fmaxf(m, fabsf(x)); };
+  const int64_t head = (int64_t)(((16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15) / 4) < n
+                           ? (int64_t)(((16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15) / 4) : n;
+  if (threadIdx.x < head) take(p[threadIdx.x]);
+  const float4* q = reinterpret_cast<const float4*>(p + head);
+  const int64_t n4 = (n - head) / 4;
+  int64_t i = threadIdx.x;
+  for (; i + 3 * kGtcThreads < n4; i += 4 * kGtcThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = q[i + u * kGtcThreads];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) { take(v[u].x); take(v[u].y); take(v[u].z); take(v[u].w); }
+  }
+  for (; i < n4; i += kGtcThreads) {
+    const float4 v = q[i];
+    take(v.x); take(v.y); take(v.z); take(v.w);
+  }
+  for (int64_t e = head + 4 * n4 + threadIdx.x; e < n; e += kGtcThreads) take(p[e]);
+  return m;
+}
+
+// IPT: conversion items per thread per 64-row step (r * 8 items: 1 up to
+// rank 32, 2 up to 64, 4 up to 128, 8 up to 256); each item is 8 rows of one
+// column.  The next step's items are loaded into registers while this step's
+// are converted.
+template <int IPT>
 __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch batch) {
   extern __shared__ uint8_t gtc_raw[];
   __shared__ __align__(8) uint64_t mma_bar[2];
@@ -253,24 +284,29 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
   if (warp == 0) tc::tmem_alloc(&tmem_slot, cols);
   // every tile zero: rows m >= r (padding to the MMA's M and N) stay so
   for (uint32_t e = tid; e < 4 * tile_bytes / 16; e += kGtcThreads) tc::sts128(base + 16u * e, make_uint4(0, 0, 0, 0));
-  // the chunk's largest magnitude (NaN if any element is NaN)
+  // the largest magnitude: given by the producer of A (a bound, or the maximum
+  // it recorded), else the chunk's own (NaN if any element is NaN)
+  const bool given = en.amax != nullptr || en.bound > 0.f;
   float m = 0.f;
-  for (int64_t e = row_begin * r + tid; e < row_end * r; e += kGtcThreads) {
-    const float x = A[e];
-    m = (m != m || x != x) ? __int_as_float(0x7FC00000) : fmaxf(m, fabsf(x));
+  if (!given) {
+    m = gtc_chunk_max(A + row_begin * r, (row_end - row_begin) * r);
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+      m = (m != m || om != om) ? __int_as_float(0x7FC00000) : fmaxf(m, om);
+    }
+    if (lane == 0) wmax[warp] = m;
   }
-  for (int o = 16; o > 0; o >>= 1) {
-    const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-    m = (m != m || om != om) ? __int_as_float(0x7FC00000) : fmaxf(m, om);
-  }
-  if (lane == 0) wmax[warp] = m;
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_slot;
   float bm = 0.f;
-  for (int w = 0; w < kGtcThreads / 32; ++w)
-    bm = (bm != bm || wmax[w] != wmax[w]) ? __int_as_float(0x7FC00000) : fmaxf(bm, wmax[w]);
+  if (given) {
+    bm = en.amax != nullptr ? __uint_as_float(*en.amax) : en.bound;
+  } else {
+    for (int w = 0; w < kGtcThreads / 32; ++w)
+      bm = (bm != bm || wmax[w] != wmax[w]) ? __int_as_float(0x7FC00000) : fmaxf(bm, wmax[w]);
+  }
   // 2^e brings the largest magnitude into [2^14, 2^15); a non-finite one keeps
   // e = 0, so that the products carry it into the Gram
   int e = 0;
@@ -283,10 +319,38 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
   const float scale = ldexpf(1.f, e), unscale = ldexpf(1.f, -e);
   const uint32_t idesc = tc::idesc_f16(128, npad, false, false);
   const int nsteps = (int)((row_end - row_begin + kGtcStep - 1) / kGtcStep);
+  // item q of this thread: it = tid + q kGtcThreads, column it % r, rows 8 (it / r) ..
+  const int nitems = r * 8;
+  int mcq[IPT], k8q[IPT];
+#pragma unroll
+  for (int q = 0; q < IPT; ++q) {
+    mcq[q] = (tid + q * kGtcThreads) % r;
+    k8q[q] = (tid + q * kGtcThreads) / r;
+  }
+  float xn[IPT][8];
+  auto load_step = [&](int st) {
+    const int64_t row0 = row_begin + (int64_t)st * kGtcStep;
+#pragma unroll
+    for (int q = 0; q < IPT; ++q) {
+      const bool on = tid + q * kGtcThreads < nitems;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int64_t ra = row0 + 8 * k8q[q] + t;
+        xn[q][t] = (on && ra < row_end) ? A[ra * r + mcq[q]] : 0.f;
+      }
+    }
+  };
+  if (nsteps > 0) load_step(0);
   bool live = true;
   for (int st = 0; st < nsteps; ++st) {
     const int b = st & 1;
     const uint32_t hi_s = base + 2u * b * tile_bytes, lo_s = hi_s + tile_bytes;
+    float xc[IPT][8];
+#pragma unroll
+    for (int q = 0; q < IPT; ++q)
+#pragma unroll
+      for (int t = 0; t < 8; ++t) xc[q][t] = xn[q][t];
+    if (st + 1 < nsteps) load_step(st + 1);
     if (st >= 2) {  // the MMAs of step st - 2 have read this buffer
       live = tc::mbar_wait(&mma_bar[b], (uint32_t)((st >> 1) - 1) & 1u, &abort_flag, nullptr, 0);
       live = __syncthreads_and(live);
@@ -295,22 +359,20 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
     // rows [row0, row0 + 64) into buffer b: item (column m of A, 8-row group
     // k8) is one 16-byte chunk of tile row m; consecutive threads take
     // consecutive columns, so that each row's loads are coalesced
-    const int64_t row0 = row_begin + (int64_t)st * kGtcStep;
-    for (int it = tid; it < r * 8; it += kGtcThreads) {
-      const int mc = it % r, k8 = it / r;
-      uint32_t hv[4], lv[4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int64_t ra = row0 + 8 * k8 + 2 * t, rb = ra + 1;
-        const float x0 = ra < row_end ? A[ra * r + mc] : 0.f;
-        const float x1 = rb < row_end ? A[rb * r + mc] : 0.f;
-        hv[t] = gtc_pack(x0 * scale, x1 * scale, lv[t]);
+    for (int q = 0; q < IPT; ++q) {
+      const int it = tid + q * kGtcThreads;
+      if (it < nitems) {
+        const int mc = mcq[q], k8 = k8q[q];
+        uint32_t hv[4], lv[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) hv[t] = gtc_pack(xc[q][2 * t] * scale, xc[q][2 * t + 1] * scale, lv[t]);
+        const uint32_t off = (uint32_t)((mc >> 3) * 1024 + (mc & 7) * 128 + ((k8 ^ (mc & 7)) << 4));
+        tc::sts128(hi_s + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
+        tc::sts128(lo_s + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
       }
-      const uint32_t off = (uint32_t)((mc >> 3) * 1024 + (mc & 7) * 128 + ((k8 ^ (mc & 7)) << 4));
-      tc::sts128(hi_s + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
-      tc::sts128(lo_s + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
     }
-    tc::fence_proxy_async_smem();
+  tc::fence_proxy_async_smem();
     live = __syncthreads_and(live);
     if (!live) break;
     if (tid == 0) {
@@ -415,10 +477,12 @@ cudaError_t launch_gram(const GramBatch& batch_in, cudaStream_t stream, bool ten
     const int max_blocks = 512 / (int)gtc_tmem_cols(r);
     const size_t tmem_bound = (size_t)233472 / (size_t)(max_blocks + 1) - 1024 + 16;
     const size_t smem = tiles > tmem_bound ? tiles : tmem_bound;
-    err = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int ipt = r <= 32 ? 1 : r <= 64 ? 2 : r <= 128 ? 4 : 8;
+    auto kern = ipt == 1 ? gram_tc_kernel<1> : ipt == 2 ? gram_tc_kernel<2> : ipt == 4 ? gram_tc_kernel<4> : gram_tc_kernel<8>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     count_launch();
-    gram_tc_kernel<<<dim3(64, batch.n), kGtcThreads, smem, stream>>>(batch);
+    kern<<<dim3(64, batch.n), kGtcThreads, smem, stream>>>(batch);
   } else {
     const int tiles = (int)ceil_div(batch.r, kTile);
     const size_t smem = gram_smem_bytes(tiles > 1);

@@ -65,6 +65,11 @@ struct GramEntry {
   int64_t rows;
   float2* partials; // gram_chunks(rows).nchunks x r x r (hi, lo) pairs
   double* out;      // r x r
+  // tensor-core kernel only: a bound on max |A| known to the caller (> 0), or
+  // the bits of max |A| recorded by A's producer (NaN if A holds one); with
+  // neither, each chunk finds its own maximum first
+  const uint32_t* amax = nullptr;
+  float bound = 0.f;
 };
 // The tensor-core kernel: each chunk's products go, 64 rows at a time, to
 // gram_tc_accs(r) TMEM accumulators in turn (as many as 512 columns hold, up
@@ -109,6 +114,7 @@ struct ProjProblem {
   double* gram;     // QR: r x r
   float* rinv;      // QR: r x r
   double* wide;     // QR with r <= k < 4r: two k x r fp64 arrays (the others unused)
+  uint32_t* amax;   // QR: bits of max |P| after the first triangular product
 };
 struct ProjBatch {
   int n;

@@ -70,6 +70,10 @@ __device__ __forceinline__ float4 gaussian4(const Philox4& blk) {
   return make_float4(-ra * ca, -ra * sa, -rb * cb, -rb * sb);
 }
 
+// |draw| <= sqrt(-2 ln 2^-33) ~ 6.77 (u >= 2^-33, |cos|, |sin| <= 1), so 8
+// bounds every value gaussian4 returns.
+constexpr float kGaussianBound = 8.0f;
+
 __global__ void __launch_bounds__(256) gaussian_kernel(const ProjBatch batch) {
   const ProjProblem& pb = batch.p[blockIdx.y];
   const int64_t n = pb.k * batch.r;
@@ -102,12 +106,15 @@ __host__ __device__ inline size_t chol_smem_floats(int r) {
 __device__ __forceinline__ float* chol_tile(float* S, int nb, int bi, int bj) {
   return S + (size_t)(bi * nb - bi * (bi - 1) / 2 + (bj - bi)) * (kCT * kCTs);
 }
-__global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch) {
+// reset_amax: clear the problem's max |P| word, which the triangular product
+// that follows records for the next Gram.
+__global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch, int reset_amax) {
   extern __shared__ float S[];
   __shared__ int broken;
   const ProjProblem& pb = batch.p[blockIdx.x];
   const int r = batch.r, nb = chol_tiles(r);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (reset_amax && tid == 0) *pb.amax = 0u;
   constexpr int kWarps = 8;
   float* T = S + (size_t)nb * (nb + 1) / 2 * (kCT * kCTs);  // scratch: nb tiles
   if (tid == 0) broken = 0;
@@ -456,10 +463,13 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
     live = __syncthreads_and(live);
     tc::tc_fence_after();
     if (!live) break;
-    // warps 0..3: row m = TMEM lane 32 w + lane, scaled back and written over P
+    // warps 0..3: row m = TMEM lane 32 w + lane, scaled back and written over
+    // P; the first pass also records max |P| (as bits, so that a NaN, whose
+    // bits exceed those of +inf, wins) for the next Gram
     if (warp < 4) {
       const int mr = warp * 32 + lane;
       const float us = ldexpf(1.f, -(row_e[mr] + g)) * out_scale;
+      uint32_t mbits = 0u;
       for (int cg = 0; cg * 32 < npad; ++cg) {
         uint32_t v[32];
         tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cg * 32), v);
@@ -468,16 +478,28 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
           float* dst = P + (row0 + mr) * r + cg * 32;
           if (vec && cg * 32 + 32 <= r) {
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
-              reinterpret_cast<float4*>(dst)[t] =
-                  make_float4(__uint_as_float(v[4 * t]) * us, __uint_as_float(v[4 * t + 1]) * us,
-                              __uint_as_float(v[4 * t + 2]) * us, __uint_as_float(v[4 * t + 3]) * us);
+            for (int t = 0; t < 8; ++t) {
+              const float4 o = make_float4(__uint_as_float(v[4 * t]) * us, __uint_as_float(v[4 * t + 1]) * us,
+                                           __uint_as_float(v[4 * t + 2]) * us, __uint_as_float(v[4 * t + 3]) * us);
+              reinterpret_cast<float4*>(dst)[t] = o;
+              if (!final_pass)
+                mbits = max(max(max(mbits, __float_as_uint(fabsf(o.x))), __float_as_uint(fabsf(o.y))),
+                            max(__float_as_uint(fabsf(o.z)), __float_as_uint(fabsf(o.w))));
+            }
           } else {
 #pragma unroll
             for (int t = 0; t < 32; ++t)
-              if (cg * 32 + t < r) dst[t] = __uint_as_float(v[t]) * us;
+              if (cg * 32 + t < r) {
+                const float o = __uint_as_float(v[t]) * us;
+                dst[t] = o;
+                mbits = max(mbits, __float_as_uint(fabsf(o)));
+              }
           }
         }
+      }
+      if (!final_pass) {
+        mbits = __reduce_max_sync(0xFFFFFFFFu, mbits);
+        if (lane == 0) atomicMax(pb.amax, mbits);
       }
     }
     tc::tc_fence_before();
@@ -631,6 +653,7 @@ void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
       p->gram = nullptr;
       p->rinv = nullptr;
       p->wide = a;
+      p->amax = nullptr;
     }
     return;
   }
@@ -638,11 +661,13 @@ void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
   float2* partials = cur.take<float2>((size_t)g.nchunks * r * r);
   double* gram = cur.take<double>((size_t)r * r);
   float* rinv = cur.take<float>((size_t)r * r);
+  uint32_t* amax = cur.take<uint32_t>(1);
   if (p) {
     p->partials = partials;
     p->gram = gram;
     p->rinv = rinv;
     p->wide = nullptr;
+    p->amax = amax;
   }
 }
 
@@ -685,10 +710,16 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
   tg.blk_begin[0] = 0;
   for (int i = 0; i < batch.n; ++i) tg.blk_begin[i + 1] = tg.blk_begin[i] + (int)ceil_div(batch.p[i].k, (int64_t)kTtcRows);
   for (int pass = 0; pass < 2; ++pass) {
+    // the Gram's scale: the first pass's from a bound on the draws, the
+    // second's from the maximum the first triangular product recorded
+    for (int i = 0; i < batch.n; ++i) {
+      gb.e[i].bound = pass == 0 ? kGaussianBound : 0.f;
+      gb.e[i].amax = pass == 0 ? nullptr : batch.p[i].amax;
+    }
     err = launch_gram(gb, stream, true);
     if (err != cudaSuccess) return err;
     count_launch();
-    chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch);
+    chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch, pass == 0);
     count_launch();
     tri_apply_tc_kernel<<<(unsigned)tg.blk_begin[batch.n], kTtcThreads, tc_smem, stream>>>(batch, tg, pass == 1);
   }

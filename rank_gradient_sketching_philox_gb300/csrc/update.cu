@@ -1423,7 +1423,7 @@ cudaError_t launch_update_normsgd(int n, const UpdateProblem* probs, const Updat
       fb.ticket[i] = w.ticket;
       fb.wnorm2_out[i] = pr.wnorm2_out;
     }
-    err = launch_gram(gb, stream, false);
+    err = launch_gram(gb, stream, true);
     if (err != cudaSuccess) return err;
     fb.rr = r * r;
     fb.tau = tau;
