@@ -2,14 +2,10 @@
 // Used by the CholeskyQR2 projection and by the normalized-SGD step, where
 // ||C P^T||_F^2 = <P^T P, C^T C>.
 //
-// Two deterministic passes over a batch of matrices: partial Grams over at
-// most 64 fixed row chunks, then a fixed-order sum over the chunks.  Within a
-// chunk, products are summed in fp32 over 32-row steps and the step sums are
-// added with TwoSum into a (hi, lo) pair; the chunk sum carries the pairs the
-// same way.  Only the 32-term tile sums round, so an entry is good to about 1e-7 of
-// the sum of its |terms| however many rows there are, without FP64 arithmetic
-// (far slower than fp32 on this GPU).  Neither pass uses atomics, so the
-// result does not depend on scheduling.
+// Two deterministic passes over a batch of matrices: partial Grams of fixed
+// row chunks on the tensor cores (gram_tc_kernel), then a fixed-order sum over
+// the chunks (gram_reduce_kernel).  Neither pass uses atomics, so the result
+// does not depend on scheduling.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -19,9 +15,6 @@
 namespace rgs {
 namespace {
 
-constexpr int kTile = 64;   // output tile edge
-constexpr int kRows = 32;   // rows staged per step
-
 // (hi, lo) += x with TwoSum (Knuth): exact error of the addition kept in lo.
 __device__ __forceinline__ void acc2(float& hi, float& lo, float x) {
   const float s = __fadd_rn(hi, x);
@@ -29,164 +22,6 @@ __device__ __forceinline__ void acc2(float& hi, float& lo, float x) {
   const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(x, bb));
   hi = s;
   lo = __fadd_rn(lo, e);
-}
-
-constexpr int kStages = 3;  // row steps in flight
-
-// Asynchronous copy of rows [row, row + 32) x columns [c0, c0 + 64) of A into
-// a 32 x 64 shared tile (elements e = threadIdx.x + 256h, h < 2: row e / 16,
-// columns 4 (e % 16) .. + 3), zero outside the matrix.  16-byte copies when r is
-// a multiple of 4, else 4-byte ones.
-__device__ __forceinline__ void stage_rows(float* tile, const float* __restrict__ A, int r, int64_t row,
-                                           int64_t row_end, int c0) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int e = threadIdx.x + 256 * h;
-    const int64_t rw = row + (e >> 4);
-    const int c = c0 + 4 * (e & 15);
-    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(tile + (e >> 4) * kTile + 4 * (e & 15));
-    const bool row_in = rw < row_end;
-    if ((r & 3) == 0) {
-      const bool in = row_in && c < r;
-      const float* src = in ? A + rw * r + c : A;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(in ? 16 : 0)
-                   : "memory");
-    } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const bool in = row_in && c + q < r;
-        const float* src = in ? A + rw * r + c + q : A;
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst + 4 * q), "l"(src), "r"(in ? 4 : 0)
-                     : "memory");
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Dynamic shared memory of the partial kernel: the staged rows (one 32 x 64
-// tile per stage for a diagonal pair, two otherwise) and every thread's 16
-// (hi, lo) pairs.
-__host__ __device__ inline size_t gram_smem_bytes(bool two_tiles) {
-  return sizeof(float) * ((size_t)kStages * (two_tiles ? 2 : 1) * kRows * kTile + 256 * 32);
-}
-
-// grid (64 chunks, tile pairs ta <= tb, batch); block 256.  A tile pair is
-// 16 x 16 blocks of 4 x 4 outputs a = a0 + 4bi + i, b = b0 + 4bj + j.  An
-// off-diagonal pair gives thread t the block (t / 16, t % 16); a diagonal one
-// needs only its 136 blocks bi <= bj (the rest is the mirror image), so
-// threads 0..135 take those in row order and the other warps only stage rows.
-// Rows arrive by asynchronous copies kStages - 1 steps ahead; each thread's
-// (hi, lo) pairs live in shared memory (touched once per 32 rows), which keeps
-// its registers for the products.
-__global__ void __launch_bounds__(256, 4) gram_partial_kernel(const GramBatch batch) {
-  extern __shared__ __align__(16) float gsm[];
-  const GramEntry& en = batch.e[blockIdx.z];
-  const int r = batch.r;
-  const GramChunks g = gram_chunks(en.rows);
-  if ((int)blockIdx.x >= g.nchunks) return;
-  const int tiles = (int)ceil_div(r, kTile);
-  // blockIdx.y enumerates the pairs ta <= tb row by row
-  int ta = 0, rem = (int)blockIdx.y;
-  while (rem >= tiles - ta) {
-    rem -= tiles - ta;
-    ++ta;
-  }
-  const int tb = ta + rem;
-  const bool diag = ta == tb;
-  const int a0 = ta * kTile, b0 = tb * kTile;
-  int bi, bj;
-  bool active = true;
-  if (diag) {
-    int t = threadIdx.x;
-    bi = 0;
-    while (bi < 16 && t >= 16 - bi) {
-      t -= 16 - bi;
-      ++bi;
-    }
-    bj = bi + t;
-    active = threadIdx.x < 136;
-  } else {
-    bi = threadIdx.x >> 4;
-    bj = threadIdx.x & 15;
-  }
-  const int64_t row_begin = (int64_t)blockIdx.x * g.chunk_rows;
-  int64_t row_end = row_begin + g.chunk_rows;
-  if (row_end > en.rows) row_end = en.rows;
-  const int nsteps = (int)ceil_div(row_end - row_begin, kRows);
-  const float* __restrict__ A = en.A;
-  const int tile_floats = kRows * kTile;
-  float* sa = gsm;                                       // kStages x (32 x 64)
-  float* sb = diag ? sa : gsm + kStages * tile_floats;   // kStages x (32 x 64)
-  float4* hl = reinterpret_cast<float4*>(gsm + kStages * tile_floats * (diag ? 1 : 2));  // [8][256]
-#pragma unroll
-  for (int q = 0; q < 8; ++q) hl[q * 256 + threadIdx.x] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) {
-    if (st < nsteps) {
-      stage_rows(sa + st * tile_floats, A, r, row_begin + (int64_t)st * kRows, row_end, a0);
-      if (!diag) stage_rows(sb + st * tile_floats, A, r, row_begin + (int64_t)st * kRows, row_end, b0);
-    }
-    cp_async_commit();
-  }
-  for (int step = 0; step < nsteps; ++step) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();  // this step's rows are in; the slot refilled below is free
-    {
-      const int nx = step + kStages - 1;
-      if (nx < nsteps) {
-        const int slot = nx % kStages;
-        stage_rows(sa + slot * tile_floats, A, r, row_begin + (int64_t)nx * kRows, row_end, a0);
-        if (!diag) stage_rows(sb + slot * tile_floats, A, r, row_begin + (int64_t)nx * kRows, row_end, b0);
-      }
-      cp_async_commit();
-    }
-    if (active) {
-      const float* ta_s = sa + (step % kStages) * tile_floats;
-      const float* tb_s = sb + (step % kStages) * tile_floats;
-      float t[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) t[e] = 0.f;
-#pragma unroll 4
-      for (int i = 0; i < kRows; ++i) {
-        const float4 av = *reinterpret_cast<const float4*>(ta_s + i * kTile + 4 * bi);
-        const float4 bv = *reinterpret_cast<const float4*>(tb_s + i * kTile + 4 * bj);
-        const float aa[4] = {av.x, av.y, av.z, av.w}, bb[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) t[4 * p + q] = fmaf(aa[p], bb[q], t[4 * p + q]);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float4 h = hl[q * 256 + threadIdx.x], l = hl[(4 + q) * 256 + threadIdx.x];
-        acc2(h.x, l.x, t[4 * q + 0]);
-        acc2(h.y, l.y, t[4 * q + 1]);
-        acc2(h.z, l.z, t[4 * q + 2]);
-        acc2(h.w, l.w, t[4 * q + 3]);
-        hl[q * 256 + threadIdx.x] = h;
-        hl[(4 + q) * 256 + threadIdx.x] = l;
-      }
-    }
-  }
-  cp_async_wait<0>();
-  if (!active) return;
-  float2* out = en.partials + (size_t)blockIdx.x * r * r;
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const float4 h = hl[p * 256 + threadIdx.x], l = hl[(4 + p) * 256 + threadIdx.x];
-    const float hv[4] = {h.x, h.y, h.z, h.w}, lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int a = a0 + 4 * bi + p, b = b0 + 4 * bj + q;
-      if (a < r && b < r) out[(size_t)a * r + b] = make_float2(hv[q], lv[q]);
-    }
-  }
 }
 
 // ---- tensor-core partial Gram ------------------------------------------------
@@ -253,32 +88,51 @@ __device__ __forceinline__ float gtc_chunk_max(const float* __restrict__ p, int6
 
 // IPT: conversion items per thread per 64-row step (r * 8 items: 1 up to
 // rank 32, 2 up to 64, 4 up to 128, 8 up to 256); each item is 8 rows of one
-// column.  The next step's items are loaded into registers while this step's
-// are converted.
-template <int IPT>
+// column.  A step's rows are contiguous in A.  BULK (shared memory leaves room
+// for a ring of at least two copies, batch.raw_stages, and every A starts on
+// 16 bytes with rows * r a multiple of 4): thread 0 copies each step's rows
+// into the ring with a bulk copy, raw_stages steps ahead, and the threads
+// convert from there.  Otherwise each thread loads the next step's items into
+// registers while this step's are converted.
+constexpr int kGtcMaxRaw = 4;
+template <int IPT, bool BULK>
 __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch batch) {
   extern __shared__ uint8_t gtc_raw[];
   __shared__ __align__(8) uint64_t mma_bar[2];
+  __shared__ __align__(8) uint64_t raw_bar[kGtcMaxRaw];
   __shared__ uint32_t tmem_slot;
   __shared__ float wmax[kGtcThreads / 32];
   __shared__ volatile int abort_flag;
-  const GramEntry& en = batch.e[blockIdx.y];
+  // this block's matrix y and chunk c (the grid lists the chunks that exist)
+  int y = 0;
+  {
+    int hi = batch.n - 1;
+    while (y < hi) {
+      const int mid = (y + hi + 1) >> 1;
+      if (batch.chunk_begin[mid] <= (int)blockIdx.x) y = mid; else hi = mid - 1;
+    }
+  }
+  const int chunk = (int)blockIdx.x - batch.chunk_begin[y];
+  const GramEntry& en = batch.e[y];
   const int r = batch.r;
   const GramChunks g = gram_chunks_tc(en.rows, r);
-  if ((int)blockIdx.x >= g.nchunks) return;  // the same for the whole block
   const int mpad = gtc_mpad(r), npad = gtc_npad(r), nmh = mpad / 128, nacc = gram_tc_accs(r);
   const uint32_t cols = gtc_tmem_cols(r);
   const uint32_t tile_bytes = (uint32_t)mpad * 128;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // buffer b: hi tile at base + 2 b tile_bytes, lo tile right after it
   const uint32_t base = tc::smem_u32(gtc_align1024(gtc_raw));
-  const int64_t row_begin = (int64_t)blockIdx.x * g.chunk_rows;
+  const int64_t row_begin = (int64_t)chunk * g.chunk_rows;
   const int64_t row_end = row_begin + g.chunk_rows < en.rows ? row_begin + g.chunk_rows : en.rows;
   const float* __restrict__ A = en.A;
+  const int nstages = batch.raw_stages;
+  constexpr bool bulk = BULK;
+  const uint32_t raw_base = base + 4 * tile_bytes, raw_bytes = (uint32_t)kGtcStep * r * 4;
   if (tid == 0) {
     abort_flag = 0;
     tc::mbar_init(&mma_bar[0], 1);
     tc::mbar_init(&mma_bar[1], 1);
+    for (int q = 0; q < kGtcMaxRaw; ++q) tc::mbar_init(&raw_bar[q], 1);
     tc::fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, cols);
@@ -340,19 +194,53 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
       }
     }
   };
-  if (nsteps > 0) load_step(0);
+  // bulk path: step s goes to ring stage s % nstages (stage and phase kept
+  // incrementally); thread 0 issues the first nstages steps here
+  auto issue = [&](int sidx, uint32_t stage) {
+    const int64_t r0 = row_begin + (int64_t)sidx * kGtcStep;
+    const int64_t nr = row_end - r0 < kGtcStep ? row_end - r0 : kGtcStep;
+    const uint32_t bytes = (uint32_t)(nr * r * 4);  // a multiple of 16: 64 r, or the chunk's remainder
+    tc::mbar_arrive_expect_tx(&raw_bar[stage], bytes);
+    tc::bulk_load_1d(raw_base + stage * raw_bytes, A + r0 * r, bytes, &raw_bar[stage]);
+  };
+  int issued = 0, consumed = 0;  // steps copied / converted (the same in every thread)
+  uint32_t rstage = 0, rphase = 0;
+  if (bulk) {
+    issued = nsteps < nstages ? nsteps : nstages;
+    if (tid == 0)
+      for (int q = 0; q < issued; ++q) issue(q, (uint32_t)q);
+  } else if (nsteps > 0) {
+    load_step(0);
+  }
   bool live = true;
   for (int st = 0; st < nsteps; ++st) {
     const int b = st & 1;
     const uint32_t hi_s = base + 2u * b * tile_bytes, lo_s = hi_s + tile_bytes;
     float xc[IPT][8];
+    if constexpr (BULK) {
+      // this step's rows (row m of the step at rs + 4 m r), zeros past the chunk
+      live = tc::mbar_wait(&raw_bar[rstage], rphase, &abort_flag, nullptr, 0) && live;
+      const uint32_t rs = raw_base + rstage * raw_bytes;
+      const int64_t row0 = row_begin + (int64_t)st * kGtcStep;
+      const int nr = (int)(row_end - row0 < kGtcStep ? row_end - row0 : kGtcStep);
 #pragma unroll
-    for (int q = 0; q < IPT; ++q)
+      for (int q = 0; q < IPT; ++q) {
+        const bool on = tid + q * kGtcThreads < nitems;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) xc[q][t] = xn[q][t];
-    if (st + 1 < nsteps) load_step(st + 1);
+        for (int t = 0; t < 8; ++t) {
+          const int m = 8 * k8q[q] + t;
+          xc[q][t] = (on && m < nr) ? tc::lds_f32(rs + (uint32_t)(m * r + mcq[q]) * 4u) : 0.f;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < IPT; ++q)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) xc[q][t] = xn[q][t];
+      if (st + 1 < nsteps) load_step(st + 1);
+    }
     if (st >= 2) {  // the MMAs of step st - 2 have read this buffer
-      live = tc::mbar_wait(&mma_bar[b], (uint32_t)((st >> 1) - 1) & 1u, &abort_flag, nullptr, 0);
+      live = tc::mbar_wait(&mma_bar[b], (uint32_t)((st >> 1) - 1) & 1u, &abort_flag, nullptr, 0) && live;
       live = __syncthreads_and(live);
       if (!live) break;
     }
@@ -372,10 +260,14 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
         tc::sts128(lo_s + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
       }
     }
-  tc::fence_proxy_async_smem();
+    tc::fence_proxy_async_smem();  // also orders this step's reads of the ring before its refill
     live = __syncthreads_and(live);
     if (!live) break;
+    consumed = st + 1;
+    // the stage this step read takes step st + nstages
+    const bool refill = bulk && st + nstages < nsteps;
     if (tid == 0) {
+      if (refill) issue(st + nstages, rstage);
       tc::tc_fence_after();
       const int acc = st % nacc;  // this step's accumulator
       for (int mh = 0; mh < nmh; ++mh) {
@@ -394,6 +286,18 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
       }
       tc::mma_commit(&mma_bar[b]);  // also covers every earlier MMA of this thread
     }
+    if (refill) ++issued;
+    if (bulk && ++rstage == (uint32_t)nstages) {
+      rstage = 0;
+      rphase ^= 1u;
+    }
+  }
+  // a loop that gave up leaves copies in flight: thread 0 waits (bounded, the
+  // abort flag aside) until each has landed before the block's memory is released
+  if (tid == 0 && bulk) {
+    volatile int no_abort = 0;
+    for (int q = consumed; q < issued; ++q)
+      tc::mbar_wait(&raw_bar[q % nstages], (uint32_t)(q / nstages) & 1u, &no_abort, nullptr, 0);
   }
   if (live)
     live = tc::mbar_wait(&mma_bar[(nsteps - 1) & 1], (uint32_t)((nsteps - 1) >> 1) & 1u, &abort_flag, nullptr, 0);
@@ -402,7 +306,7 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
   // warps 0..3: the sums of TMEM lane m (row m of A^T A) scaled back by
   // 2^-2e; a wait that gave up leaves the partial NaN
   if (warp < 4) {
-    float2* out = en.partials + (size_t)blockIdx.x * r * r;
+    float2* out = en.partials + (size_t)chunk * r * r;
     for (int mh = 0; mh < nmh; ++mh) {
       const int mrow = mh * 128 + warp * 32 + lane;
       for (int cg = 0; cg * 32 < npad; ++cg) {
@@ -450,7 +354,7 @@ __global__ void gram_reduce_kernel(const GramBatch batch) {
     b = t;
   }
   const int src = a * r + b;
-  const int nchunks = batch.tc ? gram_chunks_tc(en.rows, r).nchunks : gram_chunks(en.rows).nchunks;
+  const int nchunks = gram_chunks_tc(en.rows, r).nchunks;
   float hi = 0.f, lo = 0.f;
 #pragma unroll 8
   for (int c = 0; c < nchunks; ++c) {
@@ -463,35 +367,47 @@ __global__ void gram_reduce_kernel(const GramBatch batch) {
 
 }  // namespace
 
-cudaError_t launch_gram(const GramBatch& batch_in, cudaStream_t stream, bool tensor_cores) {
+cudaError_t launch_gram(const GramBatch& batch_in, cudaStream_t stream) {
   if (batch_in.n <= 0) return cudaSuccess;
   static thread_local GramBatch batch;
   batch = batch_in;
-  batch.tc = tensor_cores ? 1 : 0;
-  cudaError_t err = cudaSuccess;
-  if (tensor_cores) {
-    // shared memory: two buffers of two tiles, or more, so that the blocks
-    // resident on an SM never ask for more than its 512 TMEM columns
-    const int r = batch.r;
-    const size_t tiles = (size_t)4 * gtc_mpad(r) * 128 + 1024;
-    const int max_blocks = 512 / (int)gtc_tmem_cols(r);
-    const size_t tmem_bound = (size_t)233472 / (size_t)(max_blocks + 1) - 1024 + 16;
-    const size_t smem = tiles > tmem_bound ? tiles : tmem_bound;
-    const int ipt = r <= 32 ? 1 : r <= 64 ? 2 : r <= 128 ? 4 : 8;
-    auto kern = ipt == 1 ? gram_tc_kernel<1> : ipt == 2 ? gram_tc_kernel<2> : ipt == 4 ? gram_tc_kernel<4> : gram_tc_kernel<8>;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    count_launch();
-    kern<<<dim3(64, batch.n), kGtcThreads, smem, stream>>>(batch);
-  } else {
-    const int tiles = (int)ceil_div(batch.r, kTile);
-    const size_t smem = gram_smem_bytes(tiles > 1);
-    err = cudaFuncSetAttribute(gram_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    count_launch();
-    gram_partial_kernel<<<dim3(64, tiles * (tiles + 1) / 2, batch.n), 256, smem, stream>>>(batch);
-  }
-  const int rr = batch.r * batch.r;
+  const int r = batch.r;
+  batch.chunk_begin[0] = 0;
+  for (int i = 0; i < batch.n; ++i)
+    batch.chunk_begin[i + 1] = batch.chunk_begin[i] + gram_chunks_tc(batch.e[i].rows, r).nchunks;
+  // shared memory: two buffers of two tiles, or more, so that the blocks
+  // resident on an SM never ask for more than its 512 TMEM columns
+  const size_t tiles = (size_t)4 * gtc_mpad(r) * 128 + 1024;
+  const int max_blocks = 512 / (int)gtc_tmem_cols(r);
+  const size_t tmem_bound = (size_t)233472 / (size_t)(max_blocks + 1) - 1024 + 16;
+  size_t smem = tiles > tmem_bound ? tiles : tmem_bound;
+  // the ring of fp32 row copies in what the blocks an SM's TMEM admits leave
+  // (each block also holds 1 KB reserved by the system and the kernel's
+  // static shared memory)
+  cudaFuncAttributes fa;
+  cudaError_t err = cudaFuncGetAttributes(&fa, gram_tc_kernel<2, true>);
+  if (err != cudaSuccess) return err;
+  const size_t per_block = (size_t)233472 / (size_t)max_blocks - 1024 - fa.sharedSizeBytes;
+  const size_t raw_bytes = (size_t)kGtcStep * r * 4;
+  int stages = per_block > tiles ? (int)((per_block - tiles) / raw_bytes) : 0;
+  if (stages > kGtcMaxRaw) stages = kGtcMaxRaw;
+  if (stages < 2 || r > 128) stages = 0;
+  // the bulk copies need every A on 16 bytes and a whole number of 16-byte
+  // pieces per chunk (chunks start on multiples of 64 rows)
+  for (int i = 0; i < batch.n && stages > 0; ++i)
+    if ((reinterpret_cast<uintptr_t>(batch.e[i].A) & 15) != 0 || (batch.e[i].rows * r) % 4 != 0) stages = 0;
+  batch.raw_stages = stages;
+  const int ipt = r <= 32 ? 1 : r <= 64 ? 2 : r <= 128 ? 4 : 8;
+  auto kern = ipt == 1   ? gram_tc_kernel<1, false>
+              : ipt == 2 ? (stages ? gram_tc_kernel<2, true> : gram_tc_kernel<2, false>)
+              : ipt == 4 ? (stages ? gram_tc_kernel<4, true> : gram_tc_kernel<4, false>)
+                         : gram_tc_kernel<8, false>;
+  if (stages > 0 && tiles + stages * raw_bytes > smem) smem = tiles + stages * raw_bytes;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  count_launch();
+  kern<<<(unsigned)batch.chunk_begin[batch.n], kGtcThreads, smem, stream>>>(batch);
+  const int rr = r * r;
   count_launch();
   gram_reduce_kernel<<<dim3((unsigned)ceil_div(rr, 256), batch.n), 256, 0, stream>>>(batch);
   return cudaGetLastError();

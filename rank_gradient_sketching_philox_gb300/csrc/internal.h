@@ -41,29 +41,16 @@ uint64_t launches_issued();
 // Message returned by sketch_last_error() on this thread.
 void set_last_error(const char* message);
 
+// ---- Gram matrices of tall-skinny fp32 matrices ----------------------------
 // Row chunking of a partial Gram matrix over `rows` rows: at most 64 chunks.
 struct GramChunks {
   int nchunks;
   int chunk_rows;
 };
-// Row chunks of a Gram: about 128 rows each (four steps of 32 rows; a layer's
-// few thousand rows then occupy several blocks per SM, which the partial
-// kernel, latency-bound at one block per SM, needs), at most 64.
-__host__ __device__ inline GramChunks gram_chunks(int64_t rows) {
-  int64_t n = (rows + 127) / 128;
-  if (n > 64) n = 64;
-  if (n < 1) n = 1;
-  GramChunks g;
-  g.nchunks = (int)n;
-  g.chunk_rows = (int)((rows + n - 1) / n);
-  return g;
-}
-
-// ---- Gram matrices of tall-skinny fp32 matrices ----------------------------
 struct GramEntry {
   const float* A;   // rows x r, row-major
   int64_t rows;
-  float2* partials; // gram_chunks(rows).nchunks x r x r (hi, lo) pairs
+  float2* partials; // gram_chunks_tc(rows, r).nchunks x r x r (hi, lo) pairs
   double* out;      // r x r
   // tensor-core kernel only: a bound on max |A| known to the caller (> 0), or
   // the bits of max |A| recorded by A's producer (NaN if A holds one); with
@@ -71,38 +58,43 @@ struct GramEntry {
   const uint32_t* amax = nullptr;
   float bound = 0.f;
 };
-// The tensor-core kernel: each chunk's products go, 64 rows at a time, to
-// gram_tc_accs(r) TMEM accumulators in turn (as many as 512 columns hold, up
-// to 4), and each accumulator takes about 256 rows per chunk: the tensor
-// cores' fp32 accumulation drifts in proportion to the length of a chain, so
-// longer chains lose measurably (QR orthogonality 7.5e-6 with 1024 rows per
-// accumulator against 1.9e-6 with 256).  At most 64 chunks, so the partials fit
-// the same workspace as the SIMT kernel's.
+// Each chunk's products go, 64 rows at a time, to gram_tc_accs(r) TMEM
+// accumulators in turn (as many as 512 columns hold, up to 4), and each
+// accumulator takes about 256 rows per chunk: the tensor cores' fp32
+// accumulation drifts in proportion to the length of a chain, so longer chains
+// lose measurably (QR orthogonality 7.5e-6 with 1024 rows per accumulator
+// against 1.9e-6 with 256).  At most 64 chunks.
 __host__ __device__ inline int gram_tc_accs(int r) {
   const int npad = (r + 15) / 16 * 16, nmh = r <= 128 ? 1 : 2;
   int a = 512 / (npad * nmh);
   if (a > 4) a = 4;
   return a >= 4 ? 4 : (a >= 2 ? 2 : 1);
 }
+// Chunks start on a multiple of 64 rows (one conversion step), so that a
+// chunk's rows can be copied in 64-row pieces that start on 16 bytes.
 __host__ __device__ inline GramChunks gram_chunks_tc(int64_t rows, int r) {
   const int64_t target = 256 * (int64_t)gram_tc_accs(r);
   int64_t n = (rows + target - 1) / target;
   if (n > 64) n = 64;
   if (n < 1) n = 1;
+  int64_t per = (rows + n - 1) / n;
+  per = (per + 63) / 64 * 64;
   GramChunks g;
-  g.nchunks = (int)n;
-  g.chunk_rows = (int)((rows + n - 1) / n);
+  g.chunk_rows = (int)per;
+  g.nchunks = (int)((rows + per - 1) / per);
+  if (g.nchunks < 1) g.nchunks = 1;
   return g;
 }
 struct GramBatch {
   int n;
   int r;
-  int tc;  // set by launch_gram: 1 when the tensor-core kernel wrote the partials
+  int raw_stages;  // set by launch_gram: the kernel's ring of fp32 row copies (0: none)
   GramEntry e[kMaxBatch];
+  int chunk_begin[kMaxBatch + 1];  // set by launch_gram: prefix of the entries' chunk counts
 };
-// tensor_cores: partial Grams on the tensor cores (FP16 split of each chunk,
-// good to ~1e-6 of an entry's scale), else the compensated fp32 kernel (~1e-7).
-cudaError_t launch_gram(const GramBatch& batch, cudaStream_t stream, bool tensor_cores);
+// Partial Grams on the tensor cores (FP16 split of each chunk, an entry good to
+// ~1e-6 of the entry's scale), then the fixed-order sum over the chunks.
+cudaError_t launch_gram(const GramBatch& batch, cudaStream_t stream);
 
 // ---- (a) projection -------------------------------------------------------
 struct ProjProblem {

@@ -657,7 +657,7 @@ void carve_qr_workspace(WsCursor& cur, int64_t k, int r, ProjProblem* p) {
     }
     return;
   }
-  const GramChunks g = gram_chunks(k);
+  const GramChunks g = gram_chunks_tc(k, r);
   float2* partials = cur.take<float2>((size_t)g.nchunks * r * r);
   double* gram = cur.take<double>((size_t)r * r);
   float* rinv = cur.take<float>((size_t)r * r);
@@ -716,7 +716,7 @@ cudaError_t launch_gaussian_qr(const ProjBatch& batch, int64_t max_k, cudaStream
       gb.e[i].bound = pass == 0 ? kGaussianBound : 0.f;
       gb.e[i].amax = pass == 0 ? nullptr : batch.p[i].amax;
     }
-    err = launch_gram(gb, stream, true);
+    err = launch_gram(gb, stream);
     if (err != cudaSuccess) return err;
     count_launch();
     chol_inv_kernel<<<batch.n, 256, chol_smem, stream>>>(batch, pass == 0);

@@ -955,9 +955,15 @@ cudaError_t launch_update_tc(int n, const UpdateProblem* probs, const UpdateWork
   const size_t max_smem = 227 * 1024 - fa.sharedSizeBytes;
   const size_t fixed = (size_t)parts * a.a_bytes + 1024;
   const size_t p_stage = (size_t)parts * a.b_bytes;
-  // two P stages (each one 64-wide chunk of r) when they still leave three W
-  // stages (W comes from HBM and needs the deeper ring), else one
+  // P stages (each one 64-wide chunk of r): up to rank 128 two, when they
+  // still leave three W stages (W comes from HBM and needs the deeper ring),
+  // else one; above, as many as leave two W stages (rank 256: a tile's four
+  // chunks, 4% faster than two).  The rest of shared memory goes to the W ring.
   int p_stages = (fixed + 2 * p_stage + 3 * (size_t)a.w_bytes <= max_smem) ? 2 : 1;
+  if (a.kchunks > 2) {
+    p_stages = 2 * a.kchunks;
+    while (p_stages > 1 && fixed + p_stages * p_stage + 2 * (size_t)a.w_bytes > max_smem) --p_stages;
+  }
   int w_stages = (int)((max_smem - fixed - p_stages * p_stage) / a.w_bytes);
   if (w_stages > kMaxStagesUpd) w_stages = kMaxStagesUpd;
   if (w_stages < 1) return cudaErrorInvalidConfiguration;
@@ -1357,8 +1363,8 @@ size_t carve_update_workspace(WsCursor& cur, int64_t d, int64_t k, int r, bool n
   UpdateWorkspace w{};
   const int r_pad = round16(r);
   if (normsgd) {
-    w.gram_partials_p = cur.take<float2>((size_t)gram_chunks(k).nchunks * r * r);
-    w.gram_partials_c = cur.take<float2>((size_t)gram_chunks(d).nchunks * r * r);
+    w.gram_partials_p = cur.take<float2>((size_t)gram_chunks_tc(k, r).nchunks * r * r);
+    w.gram_partials_c = cur.take<float2>((size_t)gram_chunks_tc(d, r).nchunks * r * r);
     w.gram_p = cur.take<double>((size_t)r * r);
     w.gram_c = cur.take<double>((size_t)r * r);
     w.wnorm_partials = cur.take<double>(kWnormBlocks);
@@ -1423,7 +1429,7 @@ cudaError_t launch_update_normsgd(int n, const UpdateProblem* probs, const Updat
       fb.ticket[i] = w.ticket;
       fb.wnorm2_out[i] = pr.wnorm2_out;
     }
-    err = launch_gram(gb, stream, true);
+    err = launch_gram(gb, stream);
     if (err != cudaSuccess) return err;
     fb.rr = r * r;
     fb.tau = tau;
