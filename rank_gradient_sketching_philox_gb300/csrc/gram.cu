@@ -54,12 +54,6 @@ __host__ __device__ inline uint32_t gtc_tmem_cols(int r) {
 __device__ __forceinline__ uint8_t* gtc_align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
-__device__ __forceinline__ uint32_t gtc_pack(float y0, float y1, uint32_t& lo) {
-  const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
-  const __half l0 = __float2half_rn(y0 - __half2float(h0)), l1 = __float2half_rn(y1 - __half2float(h1));
-  lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
-  return (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-}
 // Largest magnitude of n floats from p (NaN if any is NaN): float4 loads, four
 // in flight per thread, once p is 16-byte aligned.
 __device__ __forceinline__ float gtc_chunk_max(const float* __restrict__ p, int64_t n) {
@@ -226,10 +220,14 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
 #pragma unroll
       for (int q = 0; q < IPT; ++q) {
         const bool on = tid + q * kGtcThreads < nitems;
+        const uint32_t a0 = rs + (uint32_t)(8 * k8q[q] * r + mcq[q]) * 4u;
+        if (nr == kGtcStep) {  // a full step: every row is there
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int m = 8 * k8q[q] + t;
-          xc[q][t] = (on && m < nr) ? tc::lds_f32(rs + (uint32_t)(m * r + mcq[q]) * 4u) : 0.f;
+          for (int t = 0; t < 8; ++t) xc[q][t] = on ? tc::lds_f32(a0 + (uint32_t)(t * r) * 4u) : 0.f;
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            xc[q][t] = (on && 8 * k8q[q] + t < nr) ? tc::lds_f32(a0 + (uint32_t)(t * r) * 4u) : 0.f;
         }
       }
     } else {
@@ -254,7 +252,7 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
         const int mc = mcq[q], k8 = k8q[q];
         uint32_t hv[4], lv[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) hv[t] = gtc_pack(xc[q][2 * t] * scale, xc[q][2 * t + 1] * scale, lv[t]);
+        for (int t = 0; t < 4; ++t) hv[t] = tc::split_f16x2(xc[q][2 * t], xc[q][2 * t + 1], scale, lv[t]);
         const uint32_t off = (uint32_t)((mc >> 3) * 1024 + (mc & 7) * 128 + ((k8 ^ (mc & 7)) << 4));
         tc::sts128(hi_s + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
         tc::sts128(lo_s + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));

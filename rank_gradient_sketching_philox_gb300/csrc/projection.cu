@@ -282,12 +282,6 @@ __host__ __device__ inline uint32_t ttc_tmem_cols(int r) {
   while ((int)c < ttc_npad(r)) c <<= 1;
   return c;
 }
-__device__ __forceinline__ uint32_t ttc_split2(float y0, float y1, uint32_t& lo) {
-  const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
-  const __half l0 = __float2half_rn(y0 - __half2float(h0)), l1 = __float2half_rn(y1 - __half2float(h1));
-  lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
-  return (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-}
 // 2^e that brings a largest magnitude m into [2^14, 2^15) (0 for m = 0 or not finite)
 __device__ __forceinline__ int ttc_exponent(float m) {
   if (!(m > 0.f) || !(m <= 3.4028234e38f)) return 0;
@@ -370,7 +364,7 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
       for (int t = 0; t < 4; ++t) {
         const int k0 = c * 64 + k8 * 8 + 2 * t;
         const float x0 = k0 < r ? X[k0 * r + n] : 0.f, x1 = k0 + 1 < r ? X[(k0 + 1) * r + n] : 0.f;
-        hv[t] = ttc_split2(x0 * sx, x1 * sx, lv[t]);
+        hv[t] = tc::split_f16x2(x0, x1, sx, lv[t]);
       }
       const uint32_t off = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((k8 ^ (n & 7)) << 4));
       tc::sts128(bc + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
@@ -418,7 +412,7 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
       const float sp = ldexpf(1.f, em);
       uint32_t hv[4], lv[4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) hv[t] = ttc_split2(x[2 * t] * sp, x[2 * t + 1] * sp, lv[t]);
+      for (int t = 0; t < 4; ++t) hv[t] = tc::split_f16x2(x[2 * t], x[2 * t + 1], sp, lv[t]);
       if (c < kc) {
         const uint32_t off = (uint32_t)((mr >> 3) * 1024 + (mr & 7) * 128 + ((k8 ^ (mr & 7)) << 4));
         const uint32_t ac = a_s + (uint32_t)c * 2 * 16384;

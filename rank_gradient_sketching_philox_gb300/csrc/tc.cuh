@@ -100,6 +100,23 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+// FP16 high and low parts of (x0 s, x1 s), s a power of two, packed with x0 in
+// the low half: hi = fp16(y), lo = fp16(y - hi), each rounded to nearest, as
+// the scalar conversions give them, in packed instructions (a pair per
+// instruction for the scaling, the FP16 roundings and the subtraction).
+__device__ __forceinline__ uint32_t split_f16x2(float x0, float x1, float s, uint32_t& lo) {
+  uint32_t hi, l;
+  asm("{\n\t.reg .b64 x, y, h, d;\n\t.reg .b16 h0, h1;\n\t.reg .f32 f0, f1, y0, y1;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\tmul.rn.f32x2 y, x, y;\n\t"
+      "mov.b64 {y0, y1}, y;\n\tcvt.rn.f16x2.f32 %0, y1, y0;\n\t"
+      "mov.b32 {h0, h1}, %0;\n\tcvt.f32.f16 f0, h0;\n\tcvt.f32.f16 f1, h1;\n\t"
+      "mov.b64 h, {f0, f1};\n\tsub.rn.f32x2 d, y, h;\n\tmov.b64 {f0, f1}, d;\n\t"
+      "cvt.rn.f16x2.f32 %1, f1, f0;\n\t}"
+      : "=r"(hi), "=r"(l)
+      : "f"(x0), "f"(x1), "f"(s));
+  lo = l;
+  return hi;
+}
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));

@@ -284,13 +284,7 @@ __global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__
       if (c0 >= r_pad) continue;  // lanes past the padded row (r_pad not a multiple of 4 lpr)
       uint32_t hi2[2], lo2[2];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const float y0 = v[q][2 * t] * sc, y1 = v[q][2 * t + 1] * sc;
-        const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
-        const __half l0 = __float2half_rn(y0 - __half2float(h0)), l1 = __float2half_rn(y1 - __half2float(h1));
-        hi2[t] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-        lo2[t] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
-      }
+      for (int t = 0; t < 2; ++t) hi2[t] = tc::split_f16x2(v[q][2 * t], v[q][2 * t + 1], sc, lo2[t]);
       // r_pad is a multiple of 16: the 4 columns are inside the row, 8-byte aligned
       *reinterpret_cast<uint2*>(dst + c0) = make_uint2(hi2[0], hi2[1]);
       *reinterpret_cast<uint2*>(dst + r_pad + c0) = make_uint2(lo2[0], lo2[1]);
