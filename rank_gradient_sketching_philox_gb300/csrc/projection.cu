@@ -387,37 +387,50 @@ __global__ void __launch_bounds__(kTtcThreads) tri_apply_tc_kernel(const __grid_
     // A = this tile of P, each row scaled by its own power of two 2^e_m: item
     // (row m, chunk c, 8-column group k8), the items of a row on consecutive
     // threads, which find the row's largest magnitude together
-    for (int it = tid; it < 128 * per_row; it += kTtcThreads) {
-      const int k8 = it & 7, c = (it >> 3) & (kcp - 1), mr = it / per_row;
-      const int k0 = c * 64 + k8 * 8;  // c >= kc: padding items (zeros, not stored)
-      const float* src = P + (row0 + mr) * r + k0;
-      float x[8];
-      if (vec && mr < rows && c < kc && k0 + 8 <= r) {  // two 16-byte loads (rows start on 16 bytes when 4 | r)
-        const float4 u0 = reinterpret_cast<const float4*>(src)[0], u1 = reinterpret_cast<const float4*>(src)[1];
-        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
-        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
-      } else {
+    // 128 per_row items are a multiple of 4 kTtcThreads: each thread loads four
+    // items before it converts any, so that their loads are in flight together
+    for (int it0 = tid; it0 < 128 * per_row; it0 += 4 * kTtcThreads) {
+      float xb[4][8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) x[t] = (mr < rows && c < kc && k0 + t < r) ? src[t] : 0.f;
+      for (int b = 0; b < 4; ++b) {
+        const int it = it0 + b * kTtcThreads;
+        const int k8 = it & 7, c = (it >> 3) & (kcp - 1), mr = it / per_row;
+        const int k0 = c * 64 + k8 * 8;  // c >= kc: padding items (zeros, not stored)
+        const float* src = P + (row0 + mr) * r + k0;
+        float* x = xb[b];
+        if (vec && mr < rows && c < kc && k0 + 8 <= r) {  // two 16-byte loads (rows start on 16 bytes when 4 | r)
+          const float4 u0 = reinterpret_cast<const float4*>(src)[0], u1 = reinterpret_cast<const float4*>(src)[1];
+          x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+          x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) x[t] = (mr < rows && c < kc && k0 + t < r) ? src[t] : 0.f;
+        }
       }
-      float mx = 0.f;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) mx = (mx != mx || x[t] != x[t]) ? __int_as_float(0x7FC00000) : fmaxf(mx, fabsf(x[t]));
-      for (int o = 1; o < per_row; o <<= 1) {
-        const float om = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
-        mx = (mx != mx || om != om) ? __int_as_float(0x7FC00000) : fmaxf(mx, om);
-      }
-      const int em = ttc_exponent(mx);
-      if ((it & (per_row - 1)) == 0) row_e[mr] = em;
-      const float sp = ldexpf(1.f, em);
-      uint32_t hv[4], lv[4];
+      for (int b = 0; b < 4; ++b) {
+        const int it = it0 + b * kTtcThreads;
+        const int k8 = it & 7, c = (it >> 3) & (kcp - 1), mr = it / per_row;
+        const float* x = xb[b];
+        float mx = 0.f;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) hv[t] = tc::split_f16x2(x[2 * t], x[2 * t + 1], sp, lv[t]);
-      if (c < kc) {
-        const uint32_t off = (uint32_t)((mr >> 3) * 1024 + (mr & 7) * 128 + ((k8 ^ (mr & 7)) << 4));
-        const uint32_t ac = a_s + (uint32_t)c * 2 * 16384;
-        tc::sts128(ac + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
-        tc::sts128(ac + 16384 + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
+        for (int t = 0; t < 8; ++t) mx = (mx != mx || x[t] != x[t]) ? __int_as_float(0x7FC00000) : fmaxf(mx, fabsf(x[t]));
+        for (int o = 1; o < per_row; o <<= 1) {
+          const float om = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
+          mx = (mx != mx || om != om) ? __int_as_float(0x7FC00000) : fmaxf(mx, om);
+        }
+        const int em = ttc_exponent(mx);
+        if ((it & (per_row - 1)) == 0) row_e[mr] = em;
+        const float sp = ldexpf(1.f, em);
+        uint32_t hv[4], lv[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) hv[t] = tc::split_f16x2(x[2 * t], x[2 * t + 1], sp, lv[t]);
+        if (c < kc) {
+          const uint32_t off = (uint32_t)((mr >> 3) * 1024 + (mr & 7) * 128 + ((k8 ^ (mr & 7)) << 4));
+          const uint32_t ac = a_s + (uint32_t)c * 2 * 16384;
+          tc::sts128(ac + off, make_uint4(hv[0], hv[1], hv[2], hv[3]));
+          tc::sts128(ac + 16384 + off, make_uint4(lv[0], lv[1], lv[2], lv[3]));
+        }
       }
     }
     // the K chunks' MMAs: with X^T resident one batch; else per chunk, each
