@@ -151,14 +151,21 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch, in
     }
     __syncthreads();
     if (broken) break;
-    // tile row k: R_kj = R_kk^-T A_kj, one column per thread (forward substitution)
+    // tile row k: R_kj = R_kk^-T A_kj, one column per thread (forward
+    // substitution; the column in registers, R_kk read by every lane at once)
     for (int cidx = tid; cidx < (nb - 1 - k) * kCT; cidx += 256) {
       float* B = chol_tile(S, nb, k, k + 1 + (cidx >> 5));
       const int c = cidx & 31;
+      float bc[kCT];
+#pragma unroll
+      for (int p = 0; p < kCT; ++p) bc[p] = B[p * kCTs + c];
+#pragma unroll
       for (int p = 0; p < kCT; ++p) {
-        float v = B[p * kCTs + c];
-        for (int m = 0; m < p; ++m) v = fmaf(-D[m * kCTs + p], B[m * kCTs + c], v);
-        B[p * kCTs + c] = v / D[p * kCTs + p];
+        float v = bc[p];
+#pragma unroll
+        for (int m = 0; m < p; ++m) v = fmaf(-D[m * kCTs + p], bc[m], v);
+        bc[p] = v / D[p * kCTs + p];
+        B[p * kCTs + c] = bc[p];
       }
     }
     __syncthreads();
