@@ -382,10 +382,13 @@ cudaError_t launch_gram(const GramBatch& batch_in, cudaStream_t stream) {
   // the ring of fp32 row copies in what the blocks an SM's TMEM admits leave
   // (each block also holds 1 KB reserved by the system and the kernel's
   // static shared memory)
-  cudaFuncAttributes fa;
-  cudaError_t err = cudaFuncGetAttributes(&fa, gram_tc_kernel<2, true>);
-  if (err != cudaSuccess) return err;
-  const size_t per_block = (size_t)233472 / (size_t)max_blocks - 1024 - fa.sharedSizeBytes;
+  // (the static size is a property of the compiled kernel: asked once)
+  static const size_t static_smem = [] {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, gram_tc_kernel<2, true>) == cudaSuccess ? fa.sharedSizeBytes : (size_t)1024;
+  }();
+  cudaError_t err = cudaSuccess;
+  const size_t per_block = (size_t)233472 / (size_t)max_blocks - 1024 - static_smem;
   const size_t raw_bytes = (size_t)kGtcStep * r * 4;
   int stages = per_block > tiles ? (int)((per_block - tiles) / raw_bytes) : 0;
   if (stages > kGtcMaxRaw) stages = kGtcMaxRaw;
