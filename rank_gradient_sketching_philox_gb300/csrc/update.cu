@@ -164,10 +164,14 @@ __device__ __forceinline__ bool split_exponent(float m, int& e) {
 }
 
 // One block of 256 threads per 128 rows of an entry (grid over all entries'
-// blocks).  A row takes lpr lanes (r_pad / 4 rounded up to a power of two, at
-// most 32), lane c its columns 4c..4c+3 of each 4 lpr-column step; warp w takes
-// rows 16w..16w+15.  For P the block's largest |p| is found first (the rows are
-// read twice; the second read comes from L2).
+// blocks).  A row takes lpr lanes (r_pad / 16 rounded up to a power of two, at
+// least 2 and at most 32), lane c its columns 4c..4c+3 of each of up to four 4 lpr-column
+// steps, so that a lane converts up to 16 values per row and the row's lanes
+// combine their sums and maxima in few shuffles; warp w takes rows
+// 16w..16w+15.  Largest magnitudes are taken as integer maxima of the
+// magnitude bits (a NaN's exceed +inf's, so a NaN wins).  For P the block's
+// largest |p| is found first (the rows are read twice; the second read comes
+// from L2).
 __global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__ SplitBatch b) {
   __shared__ float wmax[8];
   __shared__ int blk_e;
@@ -195,10 +199,10 @@ __global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__
   const int r = b.r, r_pad = b.r_pad;
   const bool vec = (r & 3) == 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int lpr = 1;
-  while (lpr < 32 && 4 * lpr < r_pad) lpr <<= 1;
+  int lpr = 2;  // at least two, so that a warp step covers at most its 16 rows
+  while (lpr < 32 && 16 * lpr < r_pad) lpr <<= 1;
   const int rps = 32 / lpr, sub = lane / lpr, cl = lane % lpr;
-  const int nq = (r_pad + 4 * lpr - 1) / (4 * lpr);  // column steps: 1, or 2 when r_pad > 128
+  const int nq = (r_pad + 4 * lpr - 1) / (4 * lpr);  // column steps: up to 4 (r_pad <= 512)
   auto load4 = [&](int64_t row, int c0, float (&v)[4]) {
     const float* s4 = src + row * r + c0;
     if (vec && c0 < r) {
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__
     }
   };
   if (is_p) {
-    float m = 0.f;
+    uint32_t mb = 0u;
     for (int st = 0; st < 16 / rps; ++st) {
       const int64_t row = row0 + warp * 16 + st * rps + sub;
       if (row >= rows) continue;
@@ -221,18 +225,16 @@ __global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__
         float v[4];
         load4(row, 4 * cl + 4 * lpr * q, v);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) m = fmaxf(m, fabsf(v[t]) + 0.f * v[t]);  // NaN stays NaN
+        for (int t = 0; t < 4; ++t) mb = max(mb, __float_as_uint(v[t]) & 0x7FFFFFFFu);
       }
     }
-    for (int o = 16; o > 0; o >>= 1) {
-      const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-      m = (m != m || om != om) ? __int_as_float(0x7FC00000) : fmaxf(m, om);
-    }
-    if (lane == 0) wmax[warp] = m;
+    mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+    if (lane == 0) wmax[warp] = __uint_as_float(mb);
     __syncthreads();
     if (threadIdx.x == 0) {
-      float bm = 0.f;
-      for (int w = 0; w < 8; ++w) bm = (bm != bm || wmax[w] != wmax[w]) ? __int_as_float(0x7FC00000) : fmaxf(bm, wmax[w]);
+      uint32_t bb = 0u;
+      for (int w = 0; w < 8; ++w) bb = max(bb, __float_as_uint(wmax[w]));
+      const float bm = __uint_as_float(bb);
       int e;
       blk_ok = split_exponent(bm, e);
       blk_e = e;
@@ -243,25 +245,28 @@ __global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__
   for (int st = 0; st < 16 / rps; ++st) {
     const int64_t row = row0 + warp * 16 + st * rps + sub;
     const bool in = row < rows;
-    float v[2][4];
-    float sq = 0.f, m = 0.f;
+    float v[4][4];
+    float sq = 0.f;
+    uint32_t mb = 0u;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < 4; ++q) {
 #pragma unroll
       for (int t = 0; t < 4; ++t) v[q][t] = 0.f;
       if (in && q < nq) load4(row, 4 * cl + 4 * lpr * q, v[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         sq = fmaf(v[q][t], v[q][t], sq);
-        m = fmaxf(m, fabsf(v[q][t]) + 0.f * v[q][t]);
+        mb = max(mb, __float_as_uint(v[q][t]) & 0x7FFFFFFFu);
       }
-    }
     // the row's lanes combine their squares and maxima (groups of lpr lanes)
     for (int o = lpr >> 1; o > 0; o >>= 1) {
       sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-      const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-      m = (m != m || om != om) ? __int_as_float(0x7FC00000) : fmaxf(m, om);
+      mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
     }
+    const float m = __uint_as_float(mb);
     int e;
     bool ok;
     if (is_p) {
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(256) split_fp16_kernel(const __grid_constant__
     const float sc = ldexpf(1.f, e);
     uint16_t* dst = b.dst[en] + row * 2 * r_pad;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < 4; ++q) {
       if (q >= nq) break;
       const int c0 = 4 * cl + 4 * lpr * q;
       if (c0 >= r_pad) continue;  // lanes past the padded row (r_pad not a multiple of 4 lpr)
