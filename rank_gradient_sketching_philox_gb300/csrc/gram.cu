@@ -136,8 +136,16 @@ __global__ void __launch_bounds__(kGtcThreads) gram_tc_kernel(const GramBatch ba
   // it recorded), else the chunk's own (NaN if any element is NaN)
   const bool given = en.amax != nullptr || en.bound > 0.f;
   float m = 0.f;
-  if (!given) {
+  if (!given && en.row_norms != nullptr) {
+    // the largest row norm of the chunk (integer maximum of the bits: a NaN
+    // norm wins), a bound within a factor sqrt(r) of the largest magnitude
+    uint32_t nb = 0u;
+    for (int64_t i = row_begin + tid; i < row_end; i += kGtcThreads) nb = max(nb, __float_as_uint(en.row_norms[i]));
+    m = __uint_as_float(nb);
+  } else if (!given) {
     m = gtc_chunk_max(A + row_begin * r, (row_end - row_begin) * r);
+  }
+  if (!given) {
     for (int o = 16; o > 0; o >>= 1) {
       const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
       m = (m != m || om != om) ? __int_as_float(0x7FC00000) : fmaxf(m, om);

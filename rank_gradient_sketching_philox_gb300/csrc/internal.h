@@ -52,11 +52,14 @@ struct GramEntry {
   int64_t rows;
   float2* partials; // gram_chunks_tc(rows, r).nchunks x r x r (hi, lo) pairs
   double* out;      // r x r
-  // tensor-core kernel only: a bound on max |A| known to the caller (> 0), or
-  // the bits of max |A| recorded by A's producer (NaN if A holds one); with
-  // neither, each chunk finds its own maximum first
+  // a bound on max |A| known to the caller (> 0), or the bits of max |A|
+  // recorded by A's producer (NaN if A holds one); with neither (nor
+  // row_norms), each chunk finds its own maximum first
   const uint32_t* amax = nullptr;
   float bound = 0.f;
+  // else, when set, the rows' Euclidean norms (rows floats, >= each row's
+  // largest magnitude): their maximum over a chunk is the chunk's bound
+  const float* row_norms = nullptr;
 };
 // Each chunk's products go, 64 rows at a time, to gram_tc_accs(r) TMEM
 // accumulators in turn (as many as 512 columns hold, up to 4), and each

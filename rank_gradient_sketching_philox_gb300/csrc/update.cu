@@ -1344,9 +1344,12 @@ cudaError_t launch_split(int n, const UpdateProblem* probs, const UpdateWorkspac
   return cudaGetLastError();
 }
 
+// split_done: the normalized-SGD step has already split C and P (its Grams take
+// their scales from the split's row norms).
 cudaError_t launch_update(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, bool normsgd,
-                          float scale_val, uint64_t seed, uint32_t step, cudaStream_t stream) {
-  cudaError_t err = launch_split(n, probs, ws, r, stream);
+                          float scale_val, uint64_t seed, uint32_t step, cudaStream_t stream,
+                          bool split_done = false) {
+  cudaError_t err = split_done ? cudaSuccess : launch_split(n, probs, ws, r, stream);
   if (err != cudaSuccess) return err;
   const int ncols = update_ncols(r);
   err = (ncols == 128) ? launch_update_tc<128>(n, probs, ws, r, normsgd, scale_val, seed, step, stream)
@@ -1394,7 +1397,9 @@ cudaError_t launch_update_normsgd(int n, const UpdateProblem* probs, const Updat
   static thread_local WnormBatch wb;
   static thread_local GramBatch gb;
   static thread_local FinalizeBatch fb;
-  cudaError_t err = cudaSuccess;
+  // the split first: its row norms bound each Gram chunk's largest magnitude
+  cudaError_t err = launch_split(n, probs, ws, r, stream);
+  if (err != cudaSuccess) return err;
   for (int base = 0; base < n; base += kMaxAux) {
     const int m = (n - base) < kMaxAux ? (n - base) : kMaxAux;
     int nw = 0;
@@ -1418,7 +1423,9 @@ cudaError_t launch_update_normsgd(int n, const UpdateProblem* probs, const Updat
       const UpdateProblem& pr = probs[base + i];
       const UpdateWorkspace& w = ws[base + i];
       gb.e[2 * i] = GramEntry{pr.P, pr.k, w.gram_partials_p, w.gram_p};
+      gb.e[2 * i].row_norms = w.p_norm;
       gb.e[2 * i + 1] = GramEntry{pr.C, pr.d, w.gram_partials_c, w.gram_c};
+      gb.e[2 * i + 1].row_norms = w.c_norm;
       fb.wnorm_partials[i] = w.wnorm_partials;
       fb.wnorm2_in[i] = pr.wnorm2_in;
       fb.gram_p[i] = w.gram_p;
@@ -1435,7 +1442,7 @@ cudaError_t launch_update_normsgd(int n, const UpdateProblem* probs, const Updat
     count_launch();
     normsgd_finalize_kernel<<<m, 256, 0, stream>>>(fb);
   }
-  return launch_update(n, probs, ws, r, true, 0.f, seed, step, stream);
+  return launch_update(n, probs, ws, r, true, 0.f, seed, step, stream, true);
 }
 
 cudaError_t launch_update_sgd(int n, const UpdateProblem* probs, const UpdateWorkspace* ws, int r, float alpha_eta,
