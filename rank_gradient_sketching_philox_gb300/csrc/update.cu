@@ -1171,6 +1171,7 @@ __device__ __forceinline__ void fix_element(const FixBatch& b, int p, uint16_t* 
 __global__ void __launch_bounds__(kFixThreads) exact_fix_kernel(const __grid_constant__ FixBatch b) {
   constexpr int kSets = 32 * kFixSetsPerLane;
   __shared__ uint32_t pre[kFixThreads / 32][kSets];  // tags of the warp's sets before each set
+  __shared__ uint32_t wtot[kFixThreads / 32];         // tags of each warp's sets
   __shared__ unsigned block_done;
   const int p = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1199,21 +1200,41 @@ __global__ void __launch_bounds__(kFixThreads) exact_fix_kernel(const __grid_con
     pre[warp][32 * q + lane] = total + incl - cnt[q];
     total += __shfl_sync(0xFFFFFFFFu, incl, 31);
   }
-  __syncwarp();
+  if (lane == 0) wtot[warp] = total;
+  __syncthreads();
+  // the block's tags are dealt over all its threads: warp w's tags follow
+  // those of warps 0 .. w-1
+  uint32_t woff[kFixThreads / 32], btotal = 0;
+#pragma unroll
+  for (int w = 0; w < kFixThreads / 32; ++w) {
+    woff[w] = btotal;
+    btotal += wtot[w];
+  }
+  const int64_t bbase = (int64_t)blockIdx.x * (kFixThreads / 32) * kSets;
   unsigned done = 0;
-  if (total != 0) {
+  if (btotal != 0) {
     const int kcols = b.ncols / 4;
     const float s = b.scale_dev[p] ? *b.scale_dev[p] : b.scale_val;
     const uint32_t k8 = (uint32_t)b.k[p] >> 3;
     double* wn = b.wnorm2_out[p];
-    for (uint32_t idx = lane; idx < total; idx += 32) {
-      // the last set whose tags start at or before idx (it holds tag idx)
+    for (uint32_t idx = threadIdx.x; idx < btotal; idx += kFixThreads) {
+      // the warp whose sets hold tag idx, then the last of its sets whose tags
+      // start at or before it
+      int w = 0;
+      uint32_t wo = 0;
+#pragma unroll
+      for (int v = 1; v < kFixThreads / 32; ++v)
+        if (woff[v] <= idx) {
+          w = v;
+          wo = woff[v];
+        }
+      const uint32_t li = idx - wo;
       int lo = 0;
 #pragma unroll
       for (int step = kSets / 2; step > 0; step >>= 1)
-        if (pre[warp][lo + step] <= idx) lo += step;
-      const int64_t sset = base + lo;
-      const uint32_t tag = b.tags[p][sset * kFixCap + (idx - pre[warp][lo])];
+        if (pre[w][lo + step] <= li) lo += step;
+      const int64_t sset = bbase + (int64_t)w * kSets + lo;
+      const uint32_t tag = b.tags[p][sset * kFixCap + (li - pre[w][lo])];
       const int t = (int)(sset / kEpiWarps), ew = (int)(sset % kEpiWarps);
       const int rb = t / b.n_ct[p], ct = t % b.n_ct[p];
       const int i = rb * 128 + (ew & 3) * 32 + (int)((tag >> 8) & 31u);
