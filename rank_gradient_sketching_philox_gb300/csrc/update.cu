@@ -1115,16 +1115,16 @@ __device__ __forceinline__ float thread_dot2(const float* c, const float* p, int
     he = __fadd_rn(he, __fadd_rn(err, __fmaf_rn(cv, pv, -m)));
   };
   if ((r & 3) == 0) {
-    for (int l0 = 0; l0 < r; l0 += 32) {
-      float4 cv[8], pv[8];
+    for (int l0 = 0; l0 < r; l0 += 16) {
+      float4 cv[4], pv[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 4; ++q) {
         const bool in = l0 + 4 * q < r;
         cv[q] = in ? __ldg(reinterpret_cast<const float4*>(c + l0) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
         pv[q] = in ? __ldg(reinterpret_cast<const float4*>(p + l0) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 4; ++q) {
         if (l0 + 4 * q >= r) break;
         term(cv[q].x, pv[q].x);
         term(cv[q].y, pv[q].y);
@@ -1168,7 +1168,7 @@ __device__ __forceinline__ void fix_element(const FixBatch& b, int p, uint16_t* 
 // set while the others wait.  For a tag: the group's Philox block and weights
 // (original ones where flagged) from W, then fix_element for each flagged
 // element.
-__global__ void __launch_bounds__(kFixThreads) exact_fix_kernel(const __grid_constant__ FixBatch b) {
+__global__ void __launch_bounds__(kFixThreads, 4) exact_fix_kernel(const __grid_constant__ FixBatch b) {
   constexpr int kSets = 32 * kFixSetsPerLane;
   __shared__ uint32_t pre[kFixThreads / 32][kSets];  // tags of the warp's sets before each set
   __shared__ uint32_t wtot[kFixThreads / 32];         // tags of each warp's sets
