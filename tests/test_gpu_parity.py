@@ -451,6 +451,27 @@ def test_normsgd_matches_oracle(d, k, r, kind):
     assert abs(out.item() - orc.norm_w(W_or) ** 2) <= 1e-6 * orc.norm_w(W_or) ** 2
 
 
+@pytest.mark.parametrize("d,k,r", [(1100, 1024, 64), (300, 2048, 128)])
+def test_normsgd_rows_of_very_different_scales(d, k, r):
+    """Rows of C spread over eight orders of magnitude, some of them zero: the
+    Gram chunks take their scale from the largest row norm, so the small rows
+    ride far below it; ||H|| and W still match the oracle."""
+    W0 = synth.layer_weight(d, k, 5)
+    P = orc.sample_qr(3, 1, 2, k, r)
+    rng = np.random.default_rng(d + r)
+    C = rng.standard_normal((d, r)) * 10.0 ** rng.uniform(-6, 2, size=(d, 1))
+    C[rng.choice(d, d // 10, replace=False)] = 0.0
+    C = C.astype(np.float32)
+    W = W0.to(DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    rgs.apply_update_normsgd(W, torch.from_numpy(C).to(DEV), torch.from_numpy(P).to(DEV), 1e-3, 4, 1, 2,
+                             dev_status=status)
+    assert int(status.item()) == 0
+    W_or, st, _ = orc.update_normsgd(bits(W0), C, P, 1e-3, 4, 1, 2, dense_h_norm=True)
+    assert st == 0
+    _w_check(bits(W), W_or)
+
+
 def test_square_frame_update_is_dense_normalized_sgd():
     """r = k: the device's own orthogonal frame makes H = C P^T the gradient
     G itself, so the device update is the textbook dense normalized SGD step
