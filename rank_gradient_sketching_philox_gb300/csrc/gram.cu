@@ -25,9 +25,12 @@ __device__ __forceinline__ void acc2(float& hi, float& lo, float x) {
 }
 
 // ---- tensor-core partial Gram ------------------------------------------------
-// Chunks of gram_chunks_tc rows, one block per (chunk, matrix), the products
-// on the tensor cores: the chunk's largest magnitude gives a power
-// of two 2^e that brings it into [2^14, 2^15); each element x 2^e is split into
+// Chunks of gram_chunks_tc rows, one block per chunk that exists (the grid
+// lists them matrix by matrix), the products on the tensor cores: a bound on
+// the chunk's largest magnitude (given by the caller, recorded by A's
+// producer, the largest of the rows' norms, or found by a pass over the chunk)
+// gives a power of two 2^e that brings it into [2^14, 2^15) or a little
+// below; each element x 2^e is split into
 // FP16 high and low parts (hi + lo within ~2^-22 of it) written, 64 rows at a
 // time, into shared-memory tiles laid out as the MMA's K-major operand (column m
 // of A is row m of the tile, 128-byte swizzle), two sets of tiles so that one
@@ -36,7 +39,7 @@ __device__ __forceinline__ void acc2(float& hi, float& lo, float x) {
 // A^T A into TMEM (two M halves when r > 128), the steps going to the
 // gram_tc_accs accumulators in turn; warps 0..3, one per TMEM lane quarter, add
 // the accumulators and scale the sums by 2^-2e into the chunk's partial (written with a
-// zero low word), which gram_reduce_kernel adds up as for the SIMT kernel.
+// zero low word), which gram_reduce_kernel adds up in chunk order.
 constexpr int kGtcThreads = 256;
 constexpr int kGtcStep = 64;  // rows per step: one 128-byte swizzled row of FP16 per column of A
 __host__ __device__ inline int gtc_mpad(int r) { return r <= 128 ? 128 : 256; }

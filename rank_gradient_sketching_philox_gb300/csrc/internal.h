@@ -183,8 +183,8 @@ struct UpdateProblem {
   int32_t* dev_status;
 };
 struct UpdateWorkspace {
-  float2* gram_partials_p; // nchunks(k) x r x r
-  float2* gram_partials_c; // nchunks(d) x r x r
+  float2* gram_partials_p; // gram_chunks_tc(k, r).nchunks x r x r
+  float2* gram_partials_c; // gram_chunks_tc(d, r).nchunks x r x r
   double* gram_p;          // r x r
   double* gram_c;          // r x r
   float* c_norm;           // d: Euclidean norm of each row of C
