@@ -90,8 +90,10 @@ __global__ void __launch_bounds__(256) gaussian_kernel(const ProjBatch batch) {
 // row rather than a few times per matrix row: the upper tiles live in shared
 // memory (row stride 33, so that columns of a tile fall in distinct banks), the
 // matrix padded to a multiple of 32 with the identity.
-//   Cholesky, right-looking, per tile column k: one warp factors the diagonal
-//   tile; each thread solves one column of the tile row (R_kj = R_kk^-T A_kj);
+//   Cholesky, right-looking, per tile column k: the block factors the diagonal
+//   tile pivot by pivot (one warp scales the pivot row, every thread updates
+//   one trailing element); each thread solves one column of the tile row
+//   (R_kj = R_kk^-T A_kj, the column in registers);
 //   every warp updates four rows of the trailing tiles (A_ij -= R_ki^T R_kj).
 //   Inverse: each warp inverts one diagonal tile (X_kk = R_kk^-1, one column per
 //   lane); then tile rows from the bottom: X_ij = -X_ii (sum over i < m <= j of
@@ -131,23 +133,28 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const ProjBatch batch, in
   // ---- Cholesky ----
   for (int k = 0; k < nb; ++k) {
     float* D = chol_tile(S, nb, k, k);
-    if (warp == 0) {  // the diagonal tile, in place
-      for (int p = 0; p < kCT; ++p) {
+    // the diagonal tile, in place, pivot by pivot with the whole block: the
+    // pivot row scaled by 1/sqrt(pivot) (warp 0), then the trailing triangle
+    // A_ic -= R_pi R_pc (p < i <= c) one element per thread
+    for (int p = 0; p < kCT; ++p) {
+      if (warp == 0) {
         const float d = D[p * kCTs + p];
         if (!(d > 0.0f) || !isfinite(d)) {  // the same in every lane
           if (lane == 0) broken = 1;
-          break;
+        } else {
+          const float rp = sqrtf(d), inv = 1.0f / rp;
+          if (lane > p) D[p * kCTs + lane] = D[p * kCTs + lane] * inv;
+          if (lane == p) D[p * kCTs + p] = rp;
         }
-        const float rp = sqrtf(d), inv = 1.0f / rp;
-        __syncwarp();
-        const float rpl = lane > p ? D[p * kCTs + lane] * inv : 0.0f;
-        if (lane > p) D[p * kCTs + lane] = rpl;
-        if (lane == p) D[p * kCTs + p] = rp;
-        __syncwarp();
-        if (lane > p)
-          for (int i = p + 1; i <= lane; ++i) D[i * kCTs + lane] = fmaf(-D[p * kCTs + i], rpl, D[i * kCTs + lane]);
-        __syncwarp();
       }
+      __syncthreads();
+      if (broken) break;
+      const int n = kCT - 1 - p;
+      for (int e = tid; e < n * n; e += 256) {
+        const int i = p + 1 + e / n, c = p + 1 + e % n;
+        if (i <= c) D[i * kCTs + c] = fmaf(-D[p * kCTs + i], D[p * kCTs + c], D[i * kCTs + c]);
+      }
+      __syncthreads();
     }
     __syncthreads();
     if (broken) break;
