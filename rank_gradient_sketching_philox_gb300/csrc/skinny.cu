@@ -702,7 +702,7 @@ __global__ void __launch_bounds__(kAccThreads, 1) proj_persistent_kernel(const _
 
 // P (k x r fp32) -> P^T split into BF16 high and low parts: rows [0, n_pad)
 // hold the high part, rows [n_pad, 2 n_pad) the low part, each k wide; rank
-// rows r..n_pad-1 are zero.  32 x 32 tiles transposed through shared memory;
+// rows r..n_pad-1 are zero.  64 x 32 tiles transposed through shared memory;
 // grid.z indexes the problem.  Problem i writes rows [row_off, row_off + rows)
 // of the high half and the same rows of the low half (which starts n_pad_out
 // rows down); rows past r are zero.  A plain split has row_off 0 and rows =
@@ -719,33 +719,41 @@ struct SplitT {
 };
 
 __global__ void __launch_bounds__(256) split_transpose_kernel(const __grid_constant__ SplitT a) {
-  __shared__ float t[32][33];
+  __shared__ float t[64][33];
   const int pr = blockIdx.z;
   const int64_t k = a.k[pr];
-  const int64_t j0 = (int64_t)blockIdx.x * 32;
+  const int64_t j0 = (int64_t)blockIdx.x * 64;
   if (j0 >= k) return;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int l0 = blockIdx.y * 32;
   const int r = a.r, rows = a.rows[pr];
   if (l0 >= rows) return;
   const float* P = a.P[pr];
-  for (int dy = ty; dy < 32; dy += 8) {
+  for (int dy = ty; dy < 64; dy += 8) {
     const int64_t j = j0 + dy;
     const int l = l0 + tx;
     t[dy][tx] = (j < k && l < r) ? P[j * r + l] : 0.f;
   }
   __syncthreads();
+  // a pair of columns j, j + 1 per thread (k is a multiple of 8 and the
+  // output 16-byte aligned, so the pair is one aligned 4-byte store per part)
   uint16_t* hi = a.out[pr] + (int64_t)a.row_off[pr] * k;
   uint16_t* lo = hi + (int64_t)a.n_pad_out[pr] * k;
   for (int dy = ty; dy < 32; dy += 8) {
     const int l = l0 + dy;
-    const int64_t j = j0 + tx;
+    const int64_t j = j0 + 2 * tx;
     if (l < rows && j < k) {
-      const float v = t[tx][dy];
-      const __nv_bfloat16 h = __float2bfloat16_rn(v);
-      const __nv_bfloat16 w = __float2bfloat16_rn(v - __bfloat162float(h));
-      hi[(int64_t)l * k + j] = __bfloat16_as_ushort(h);
-      lo[(int64_t)l * k + j] = __bfloat16_as_ushort(w);
+      uint32_t hp = 0, lp = 0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float v = t[2 * tx + e][dy];
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        const __nv_bfloat16 w = __float2bfloat16_rn(v - __bfloat162float(h));
+        hp |= (uint32_t)__bfloat16_as_ushort(h) << (16 * e);
+        lp |= (uint32_t)__bfloat16_as_ushort(w) << (16 * e);
+      }
+      *reinterpret_cast<uint32_t*>(hi + (int64_t)l * k + j) = hp;
+      *reinterpret_cast<uint32_t*>(lo + (int64_t)l * k + j) = lp;
     }
   }
 }
@@ -902,7 +910,7 @@ cudaError_t launch_split_projection(int n, const float* const* P, const int64_t*
     }
     sp.r = r;
     count_launch();
-    split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 32), (unsigned)ceil_div(n_pad, 32), (unsigned)m), 256, 0,
+    split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 64), (unsigned)ceil_div(n_pad, 32), (unsigned)m), 256, 0,
                              stream>>>(sp);
   }
   return cudaGetLastError();
@@ -916,7 +924,7 @@ cudaError_t launch_split_projection_grouped(int n, const SplitGroup* groups, int
     if (i == 0) return cudaSuccess;
     sp.r = r;
     count_launch();
-    split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 32), (unsigned)ceil_div(max_rows, 32), (unsigned)i), 256,
+    split_transpose_kernel<<<dim3((unsigned)ceil_div(max_k, 64), (unsigned)ceil_div(max_rows, 32), (unsigned)i), 256,
                              0, stream>>>(sp);
     i = 0;
     max_rows = 0;
