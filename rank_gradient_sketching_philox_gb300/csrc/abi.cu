@@ -194,6 +194,7 @@ sketch_status do_sample(sketch_proj_kind kind, uint64_t seed, uint32_t step, int
     b->n = 0;
     b->r = (int)r;
     b->seed = seed;
+    rgs::philox_round_keys(seed, b->rk0, b->rk1);
     b->step = step;
   }
   rgs::WsCursor cur;

@@ -115,6 +115,7 @@ struct ProjBatch {
   int n;
   int r;
   uint64_t seed;
+  uint32_t rk0[10], rk1[10];  // Philox round keys of the seed (philox_round_keys)
   uint32_t step;
   int32_t* status;  // one status word for the whole batch (QR breakdown flag)
   ProjProblem p[kMaxBatch];

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(256) rademacher_kernel(const ProjBatch batch) 
   const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t e0 = w * 32;
   if (e0 >= n) return;
-  const Philox4 blk = stream_block(batch.seed, pb.layer, batch.step, kTagRademacher, (uint32_t)(w >> 2));
+  const Philox4 blk = philox4x32_10_rk((uint32_t)(w >> 2), batch.step, pb.layer, kTagRademacher, batch.rk0, batch.rk1);
   const uint32_t word = (w & 3) == 0 ? blk.w0 : (w & 3) == 1 ? blk.w1 : (w & 3) == 2 ? blk.w2 : blk.w3;
   const float pos = pb.scale, neg = -pb.scale;
   float4* out = reinterpret_cast<float4*>(pb.P + e0);
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(256) gaussian_kernel(const ProjBatch batch) {
   const int64_t n = pb.k * batch.r;
   const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (4 * b >= n) return;
-  const Philox4 blk = stream_block(batch.seed, pb.layer, batch.step, kTagGaussian, (uint32_t)b);
+  const Philox4 blk = philox4x32_10_rk((uint32_t)b, batch.step, pb.layer, kTagGaussian, batch.rk0, batch.rk1);
   reinterpret_cast<float4*>(pb.P)[b] = gaussian4(blk);
 }
 
